@@ -1,0 +1,316 @@
+"""GB300 softmax-attention training kernels: thin Python binding of libattn.so.
+
+Every function here only marshals torch tensors (device memory and the current
+stream) into the C ABI declared in include/attn.h; all arithmetic runs in the
+library's CUDA kernels.  There is no CPU or eager fallback: if the library is
+missing or a call fails, an exception is raised.
+
+Entry points (same names as the C ABI):
+  attn_fwd, attn_bwd_workspace_size, attn_bwd_preprocess, attn_bwd,
+  sparse_attn_fwd, sparse_attn_bwd_workspace_size, sparse_attn_bwd,
+  attn_status_string, attn_version
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import warnings
+
+import torch
+
+__all__ = [
+    "ATTN_DQ_ATOMIC", "ATTN_DQ_SPLIT", "AttnError", "lib", "attn_fwd", "attn_bwd_workspace_size",
+    "attn_bwd_preprocess", "attn_bwd", "sparse_attn_fwd", "sparse_attn_bwd_workspace_size",
+    "sparse_attn_bwd", "attn_status_string", "attn_version", "dense_backward",
+    "SPARSE_DIM_QK", "SPARSE_DIM_V", "EXPORTED_SYMBOLS",
+]
+
+ATTN_DQ_ATOMIC = 0
+ATTN_DQ_SPLIT = 1
+SPARSE_DIM_QK = 576
+SPARSE_DIM_V = 512
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libattn.so")
+
+EXPORTED_SYMBOLS = (
+    "attn_fwd", "attn_bwd_workspace_size", "attn_bwd_preprocess", "attn_bwd",
+    "sparse_attn_fwd", "sparse_attn_bwd_workspace_size", "sparse_attn_bwd",
+    "attn_status_string", "attn_version",
+)
+
+
+class AttnError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        super().__init__(f"{fn}: {attn_status_string(code)} (status {code})")
+        self.code = code
+
+
+class _Problem(ctypes.Structure):
+    _fields_ = [
+        ("batch", ctypes.c_int), ("seqlen", ctypes.c_int), ("heads_q", ctypes.c_int),
+        ("heads_kv", ctypes.c_int), ("head_dim", ctypes.c_int), ("causal", ctypes.c_int),
+        ("scale", ctypes.c_float), ("cu_seqlens", ctypes.c_void_p), ("num_seqs", ctypes.c_int),
+        ("capacity", ctypes.c_int), ("max_seqlen", ctypes.c_int), ("error_word", ctypes.c_void_p),
+    ]
+
+
+class _SparseProblem(ctypes.Structure):
+    _fields_ = [
+        ("tokens", ctypes.c_int), ("heads", ctypes.c_int), ("dim_qk", ctypes.c_int),
+        ("dim_v", ctypes.c_int), ("topk", ctypes.c_int), ("scale", ctypes.c_float),
+        ("error_word", ctypes.c_void_p),
+    ]
+
+
+_LIB = None
+
+
+def lib() -> ctypes.CDLL:
+    """Loads libattn.so (built by __graft_entry__.build() or build.py)."""
+    global _LIB
+    if _LIB is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                               "`python -m softmax_attention_backward_gb300.build`")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, sz, i32 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int
+        P = ctypes.POINTER(_Problem)
+        SP = ctypes.POINTER(_SparseProblem)
+        L.attn_fwd.argtypes = [P, vp, vp, vp, vp, vp, vp]
+        L.attn_bwd_workspace_size.argtypes = [P, i32]
+        L.attn_bwd_workspace_size.restype = sz
+        L.attn_bwd_preprocess.argtypes = [P, i32, vp, vp, vp, vp, sz, vp]
+        L.attn_bwd.argtypes = [P, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+        L.sparse_attn_fwd.argtypes = [SP, vp, vp, vp, vp, vp, vp]
+        L.sparse_attn_bwd_workspace_size.argtypes = [SP]
+        L.sparse_attn_bwd_workspace_size.restype = sz
+        L.sparse_attn_bwd.argtypes = [SP, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+        L.attn_status_string.argtypes = [i32]
+        L.attn_status_string.restype = ctypes.c_char_p
+        L.attn_version.argtypes = []
+        for name in ("attn_fwd", "attn_bwd_preprocess", "attn_bwd", "sparse_attn_fwd",
+                     "sparse_attn_bwd"):
+            getattr(L, name).restype = i32
+        _LIB = L
+    return _LIB
+
+
+def attn_status_string(code: int) -> str:
+    return lib().attn_status_string(int(code)).decode()
+
+
+def attn_version() -> int:
+    return int(lib().attn_version())
+
+
+# ----------------------------------------------------------------------------
+# marshalling helpers
+# ----------------------------------------------------------------------------
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(fn, code):
+    if code != 0:
+        raise AttnError(fn, code)
+
+
+def _need(t, name, dtype, device=None):
+    if t is None:
+        raise ValueError(f"{name} is required")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    return t
+
+
+def _nondeterministic(what: str):
+    if torch.are_deterministic_algorithms_enabled():
+        msg = f"{what} accumulates with fp32 atomics and is not bitwise reproducible"
+        if torch.is_deterministic_algorithms_warn_only_enabled():
+            warnings.warn(msg, RuntimeWarning, stacklevel=3)
+        else:
+            raise RuntimeError(msg + "; use dq_mode=ATTN_DQ_SPLIT for the dense path")
+
+
+def _problem(q, k, causal, scale, cu_seqlens, max_seqlen, error_word):
+    p = _Problem()
+    if cu_seqlens is None:
+        if q.dim() != 4:
+            raise ValueError("dense q must be [batch, seqlen, heads, head_dim]")
+        p.batch, p.seqlen, p.heads_q, p.head_dim = q.shape
+        p.heads_kv = k.shape[2]
+        p.cu_seqlens = None
+        p.num_seqs = 0
+        p.capacity = 0
+        p.max_seqlen = q.shape[1]
+    else:
+        if q.dim() != 3:
+            raise ValueError("THD q must be [capacity, heads, head_dim]")
+        _need(cu_seqlens, "cu_seqlens", torch.int32, q.device)
+        p.batch, p.seqlen = 1, 0
+        p.capacity, p.heads_q, p.head_dim = q.shape
+        p.heads_kv = k.shape[1]
+        p.cu_seqlens = cu_seqlens.data_ptr()
+        p.num_seqs = cu_seqlens.numel() - 1
+        if max_seqlen is None:
+            max_seqlen = int((cu_seqlens[1:] - cu_seqlens[:-1]).max().item()) if p.num_seqs > 0 else 0
+        p.max_seqlen = int(max_seqlen)
+    p.causal = 1 if causal else 0
+    p.scale = float(scale if scale is not None else 1.0 / math.sqrt(p.head_dim))
+    p.error_word = None if error_word is None else error_word.data_ptr()
+    return p
+
+
+def _lse_shape(q, cu_seqlens):
+    if cu_seqlens is None:
+        return (q.shape[0], q.shape[2], q.shape[1])
+    return (q.shape[1], q.shape[0])
+
+
+# ----------------------------------------------------------------------------
+# dense / THD
+# ----------------------------------------------------------------------------
+def attn_fwd(q, k, v, *, causal=False, scale=None, cu_seqlens=None, max_seqlen=None, out=None,
+             lse=None, error_word=None, stream=None):
+    """Returns (o, lse).  Dense: q [B,S,Hq,D], k/v [B,S,Hkv,D], lse [B,Hq,S].
+    THD: q [cap,Hq,D], k/v [cap,Hkv,D], cu_seqlens int32 [n+1], lse [Hq,cap]."""
+    dev = q.device
+    for n, t in (("q", q), ("k", k), ("v", v)):
+        _need(t, n, torch.bfloat16, dev)
+    o = out if out is not None else torch.empty_like(q)
+    lse = lse if lse is not None else torch.empty(_lse_shape(q, cu_seqlens), dtype=torch.float32,
+                                                  device=dev)
+    _need(o, "out", torch.bfloat16, dev)
+    _need(lse, "lse", torch.float32, dev)
+    p = _problem(q, k, causal, scale, cu_seqlens, max_seqlen, error_word)
+    _check("attn_fwd", lib().attn_fwd(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(o),
+                                      _ptr(lse), _stream(stream)))
+    return o, lse
+
+
+def attn_bwd_workspace_size(q, k, *, mode=ATTN_DQ_ATOMIC, causal=False, cu_seqlens=None,
+                            max_seqlen=None, scale=None) -> int:
+    p = _problem(q, k, causal, scale, cu_seqlens, max_seqlen, None)
+    return int(lib().attn_bwd_workspace_size(ctypes.byref(p), int(mode)))
+
+
+def attn_bwd_preprocess(q, k, o, dout, *, mode=ATTN_DQ_ATOMIC, workspace=None, causal=False,
+                        scale=None, cu_seqlens=None, max_seqlen=None, delta=None,
+                        error_word=None, stream=None):
+    """Returns delta = rowsum(dO * O) (fp32, layout of lse); clears the atomic
+    dQ accumulator inside `workspace` (a uint8 CUDA tensor)."""
+    dev = q.device
+    _need(o, "o", torch.bfloat16, dev)
+    _need(dout, "dout", torch.bfloat16, dev)
+    delta = delta if delta is not None else torch.empty(_lse_shape(q, cu_seqlens),
+                                                        dtype=torch.float32, device=dev)
+    p = _problem(q, k, causal, scale, cu_seqlens, max_seqlen, error_word)
+    ws_ptr, ws_bytes = (None, 0) if workspace is None else (_ptr(workspace), workspace.numel())
+    _check("attn_bwd_preprocess",
+           lib().attn_bwd_preprocess(ctypes.byref(p), int(mode), _ptr(o), _ptr(dout), _ptr(delta),
+                                     ws_ptr, ws_bytes, _stream(stream)))
+    return delta
+
+
+def attn_bwd(q, k, v, dout, lse, delta, *, mode=ATTN_DQ_ATOMIC, workspace, causal=False,
+             scale=None, cu_seqlens=None, max_seqlen=None, dq=None, dk=None, dv=None,
+             error_word=None, stream=None):
+    """Returns (dq, dk, dv) bf16.  Call attn_bwd_preprocess first with the same
+    workspace and mode."""
+    if int(mode) == ATTN_DQ_ATOMIC:
+        _nondeterministic("attn_bwd(dq_mode=ATTN_DQ_ATOMIC)")
+    dev = q.device
+    for n, t in (("q", q), ("k", k), ("v", v), ("dout", dout)):
+        _need(t, n, torch.bfloat16, dev)
+    _need(lse, "lse", torch.float32, dev)
+    _need(delta, "delta", torch.float32, dev)
+    dq = dq if dq is not None else torch.empty_like(q)
+    dk = dk if dk is not None else torch.empty_like(k)
+    dv = dv if dv is not None else torch.empty_like(v)
+    p = _problem(q, k, causal, scale, cu_seqlens, max_seqlen, error_word)
+    _check("attn_bwd",
+           lib().attn_bwd(ctypes.byref(p), int(mode), _ptr(q), _ptr(k), _ptr(v), _ptr(dout),
+                          _ptr(lse), _ptr(delta), _ptr(dq), _ptr(dk), _ptr(dv),
+                          _ptr(workspace), workspace.numel(), _stream(stream)))
+    return dq, dk, dv
+
+
+def dense_backward(q, k, v, o, lse, dout, *, mode=ATTN_DQ_ATOMIC, causal=False, scale=None,
+                   cu_seqlens=None, max_seqlen=None, workspace=None, error_word=None,
+                   stream=None):
+    """Preprocess + backward with a workspace allocated here when not given."""
+    if workspace is None:
+        n = attn_bwd_workspace_size(q, k, mode=mode, causal=causal, cu_seqlens=cu_seqlens,
+                                    max_seqlen=max_seqlen)
+        workspace = torch.empty(max(n, 16), dtype=torch.uint8, device=q.device)
+    kw = dict(mode=mode, causal=causal, scale=scale, cu_seqlens=cu_seqlens, max_seqlen=max_seqlen,
+              error_word=error_word, stream=stream)
+    delta = attn_bwd_preprocess(q, k, o, dout, workspace=workspace, **kw)
+    return attn_bwd(q, k, v, dout, lse, delta, workspace=workspace, **kw)
+
+
+# ----------------------------------------------------------------------------
+# top-k sparse
+# ----------------------------------------------------------------------------
+def _sparse_problem(q, idx, scale, error_word):
+    p = _SparseProblem()
+    p.tokens, p.heads, p.dim_qk = q.shape
+    p.dim_v = SPARSE_DIM_V
+    p.topk = idx.shape[1]
+    p.scale = float(scale if scale is not None else 1.0 / math.sqrt(p.dim_qk))
+    p.error_word = None if error_word is None else error_word.data_ptr()
+    return p
+
+
+def sparse_attn_fwd(q, kv, idx, *, scale=None, out=None, lse=None, error_word=None, stream=None):
+    """q [T,H,576], kv [T,576], idx int32 [T,K] -> (o [T,H,512], lse [T,H])."""
+    dev = q.device
+    _need(q, "q", torch.bfloat16, dev)
+    _need(kv, "kv", torch.bfloat16, dev)
+    _need(idx, "idx", torch.int32, dev)
+    T, H, _ = q.shape
+    o = out if out is not None else torch.empty(T, H, SPARSE_DIM_V, dtype=torch.bfloat16, device=dev)
+    lse = lse if lse is not None else torch.empty(T, H, dtype=torch.float32, device=dev)
+    p = _sparse_problem(q, idx, scale, error_word)
+    _check("sparse_attn_fwd",
+           lib().sparse_attn_fwd(ctypes.byref(p), _ptr(q), _ptr(kv), _ptr(idx), _ptr(o), _ptr(lse),
+                                 _stream(stream)))
+    return o, lse
+
+
+def sparse_attn_bwd_workspace_size(q, idx, *, scale=None) -> int:
+    p = _sparse_problem(q, idx, scale, None)
+    return int(lib().sparse_attn_bwd_workspace_size(ctypes.byref(p)))
+
+
+def sparse_attn_bwd(q, kv, idx, o, dout, lse, *, scale=None, workspace=None, dq=None, dkv=None,
+                    error_word=None, stream=None):
+    """Returns (dq [T,H,576], dkv [T,576]) bf16."""
+    _nondeterministic("sparse_attn_bwd (dKV)")
+    dev = q.device
+    for n, t in (("q", q), ("kv", kv), ("o", o), ("dout", dout)):
+        _need(t, n, torch.bfloat16, dev)
+    _need(idx, "idx", torch.int32, dev)
+    _need(lse, "lse", torch.float32, dev)
+    if workspace is None:
+        n = sparse_attn_bwd_workspace_size(q, idx, scale=scale)
+        workspace = torch.empty(max(n, 16), dtype=torch.uint8, device=dev)
+    dq = dq if dq is not None else torch.empty_like(q)
+    dkv = dkv if dkv is not None else torch.empty_like(kv)
+    p = _sparse_problem(q, idx, scale, error_word)
+    _check("sparse_attn_bwd",
+           lib().sparse_attn_bwd(ctypes.byref(p), _ptr(q), _ptr(kv), _ptr(idx), _ptr(o),
+                                 _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dkv), _ptr(workspace),
+                                 workspace.numel(), _stream(stream)))
+    return dq, dkv

@@ -1,0 +1,328 @@
+// C ABI of the library: argument validation, TMA descriptor encoding and the
+// launch sequence of each entry point (declared and documented in attn.h).
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "attn.h"
+#include "launch.h"
+
+namespace attn {
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+// 4-D map over a bf16 tensor [batch, rows, heads, dim] (dim contiguous), box of
+// 64 dims x 1 head x box_rows rows x 1 batch, 128-byte swizzle, zero fill.
+bool make_map(CUtensorMap* m, const void* ptr, int batch, int rows, int heads, int dim,
+              int box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(dim), static_cast<cuuint64_t>(heads),
+                        static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(batch)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(dim) * 2,
+                           static_cast<cuuint64_t>(heads) * dim * 2,
+                           static_cast<cuuint64_t>(rows) * heads * dim * 2};
+  cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(box_rows), 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Validates a dense/THD problem.  Sets *empty when there is nothing to compute.
+attn_status_t check_problem(const attn_problem_t* p, bool* empty) {
+  *empty = false;
+  if (!p) return ATTN_ERR_INVALID_ARG;
+  if (p->heads_q <= 0 || p->heads_kv <= 0 || p->head_dim <= 0) return ATTN_ERR_INVALID_ARG;
+  if (p->heads_q % p->heads_kv) return ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(p->scale)) return ATTN_ERR_INVALID_ARG;
+  if (p->head_dim != 64 && p->head_dim != 128) return ATTN_ERR_UNSUPPORTED;
+  if (p->cu_seqlens) {
+    if (p->num_seqs <= 0 || p->capacity < 0 || p->max_seqlen < 0) return ATTN_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(p->cu_seqlens) & 3u) != 0) return ATTN_ERR_ALIGNMENT;
+    if (p->capacity == 0 || p->max_seqlen == 0) *empty = true;
+    if (static_cast<int64_t>(p->capacity) * p->heads_q * p->head_dim >= (int64_t(1) << 31))
+      return ATTN_ERR_UNSUPPORTED;
+  } else {
+    if (p->batch < 0 || p->seqlen < 0) return ATTN_ERR_INVALID_ARG;
+    if (p->batch == 0 || p->seqlen == 0) *empty = true;
+    if (static_cast<int64_t>(p->seqlen) * p->heads_q * p->head_dim >= (int64_t(1) << 31))
+      return ATTN_ERR_UNSUPPORTED;
+    if (p->batch > 65535) return ATTN_ERR_UNSUPPORTED;
+  }
+  if (p->heads_q > 65535) return ATTN_ERR_UNSUPPORTED;
+  return ATTN_OK;
+}
+
+Problem to_kernel(const attn_problem_t* p) {
+  Problem k;
+  const bool thd = p->cu_seqlens != nullptr;
+  k.batch = thd ? 1 : p->batch;
+  k.rows_total = thd ? p->capacity : p->seqlen;
+  k.heads_q = p->heads_q;
+  k.heads_kv = p->heads_kv;
+  k.causal = p->causal ? 1 : 0;
+  k.scale = p->scale;
+  k.cu_seqlens = p->cu_seqlens;
+  k.num_seqs = thd ? p->num_seqs : 0;
+  k.max_seqlen = thd ? p->max_seqlen : p->seqlen;
+  k.err = p->error_word;
+  return k;
+}
+
+size_t dq_elems(const Problem& k, int D) {
+  return static_cast<size_t>(k.batch) * k.rows_total * k.heads_q * D;
+}
+
+int n_kv_tiles(const Problem& k) { return (k.max_seqlen + 127) / 128; }
+
+attn_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA; }
+
+}  // namespace
+}  // namespace attn
+
+using namespace attn;
+
+extern "C" {
+
+const char* attn_status_string(attn_status_t s) {
+  switch (s) {
+    case ATTN_OK: return "ok";
+    case ATTN_ERR_INVALID_ARG: return "invalid argument";
+    case ATTN_ERR_UNSUPPORTED: return "unsupported problem";
+    case ATTN_ERR_ALIGNMENT: return "pointer not 16-byte aligned";
+    case ATTN_ERR_CUDA: return "CUDA error";
+    case ATTN_ERR_WORKSPACE: return "workspace missing or too small";
+    case ATTN_ERR_INDEX_RANGE: return "sparse index out of range";
+    case ATTN_ERR_TIMEOUT: return "device wait timed out";
+  }
+  return "unknown status";
+}
+
+int attn_version(void) { return 100; }
+
+attn_status_t attn_fwd(const attn_problem_t* p, const void* q, const void* k, const void* v,
+                       void* o, float* lse, attn_stream_t stream) {
+  bool empty;
+  attn_status_t s = check_problem(p, &empty);
+  if (s != ATTN_OK) return s;
+  if (!q || !k || !v || !o || !lse) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return ATTN_ERR_ALIGNMENT;
+  if (empty) return ATTN_OK;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const Problem kp = to_kernel(p);
+  const int D = p->head_dim;
+  CUtensorMap mq, mk, mv;
+  if (!make_map(&mq, q, kp.batch, kp.rows_total, kp.heads_q, D, 128) ||
+      !make_map(&mk, k, kp.batch, kp.rows_total, kp.heads_kv, D, 128) ||
+      !make_map(&mv, v, kp.batch, kp.rows_total, kp.heads_kv, D, 128))
+    return ATTN_ERR_CUDA;
+  FwdArgs a;
+  a.p = kp;
+  a.o = static_cast<__nv_bfloat16*>(o);
+  a.lse = lse;
+  a.scale_log2 = p->scale * kLog2e;
+  const int gx = tile_bound(kp.rows_total, kp.num_seqs, 256, kp.cu_seqlens != nullptr);
+  cudaError_t e = (D == 64) ? launch_attn_fwd<64>(mq, mk, mv, a, gx, st)
+                            : launch_attn_fwd<128>(mq, mk, mv, a, gx, st);
+  if (e == cudaSuccess && kp.cu_seqlens) e = launch_thd_fwd_pad(kp, a.o, lse, D, st);
+  return cuda_status(e);
+}
+
+size_t attn_bwd_workspace_size(const attn_problem_t* p, attn_dq_mode_t mode) {
+  bool empty;
+  if (check_problem(p, &empty) != ATTN_OK) return 0;
+  if (empty) return 0;
+  const Problem kp = to_kernel(p);
+  const size_t elems = dq_elems(kp, p->head_dim);
+  if (mode == ATTN_DQ_SPLIT) return elems * sizeof(float) * static_cast<size_t>(n_kv_tiles(kp));
+  return elems * sizeof(float);
+}
+
+attn_status_t attn_bwd_preprocess(const attn_problem_t* p, attn_dq_mode_t mode, const void* o,
+                                  const void* dout, float* delta, void* workspace,
+                                  size_t workspace_bytes, attn_stream_t stream) {
+  bool empty;
+  attn_status_t s = check_problem(p, &empty);
+  if (s != ATTN_OK) return s;
+  if (mode != ATTN_DQ_ATOMIC && mode != ATTN_DQ_SPLIT) return ATTN_ERR_INVALID_ARG;
+  if (!o || !dout || !delta) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(o) || !aligned16(dout) || !aligned16(delta)) return ATTN_ERR_ALIGNMENT;
+  if (empty) return ATTN_OK;
+  const size_t need = attn_bwd_workspace_size(p, mode);
+  if (mode == ATTN_DQ_ATOMIC && (!workspace || workspace_bytes < need)) return ATTN_ERR_WORKSPACE;
+  if (workspace && !aligned16(workspace)) return ATTN_ERR_ALIGNMENT;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const Problem kp = to_kernel(p);
+  float* acc = (mode == ATTN_DQ_ATOMIC) ? static_cast<float*>(workspace) : nullptr;
+  const size_t n = (mode == ATTN_DQ_ATOMIC) ? dq_elems(kp, p->head_dim) : 0;
+  const auto* ob = static_cast<const __nv_bfloat16*>(o);
+  const auto* db = static_cast<const __nv_bfloat16*>(dout);
+  cudaError_t e = (p->head_dim == 64) ? launch_bwd_preprocess<64>(kp, ob, db, delta, acc, n, st)
+                                      : launch_bwd_preprocess<128>(kp, ob, db, delta, acc, n, st);
+  return cuda_status(e);
+}
+
+attn_status_t attn_bwd(const attn_problem_t* p, attn_dq_mode_t mode, const void* q,
+                       const void* k, const void* v, const void* dout, const float* lse,
+                       const float* delta, void* dq, void* dk, void* dv, void* workspace,
+                       size_t workspace_bytes, attn_stream_t stream) {
+  bool empty;
+  attn_status_t s = check_problem(p, &empty);
+  if (s != ATTN_OK) return s;
+  if (mode != ATTN_DQ_ATOMIC && mode != ATTN_DQ_SPLIT) return ATTN_ERR_INVALID_ARG;
+  if (!q || !k || !v || !dout || !lse || !delta || !dq || !dk || !dv)
+    return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dout) || !aligned16(lse) ||
+      !aligned16(delta) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+    return ATTN_ERR_ALIGNMENT;
+  if (empty) return ATTN_OK;
+  const size_t need = attn_bwd_workspace_size(p, mode);
+  if (!workspace || workspace_bytes < need) return ATTN_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return ATTN_ERR_ALIGNMENT;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const Problem kp = to_kernel(p);
+  const int D = p->head_dim;
+  CUtensorMap mq, mk, mv, mdo;
+  const int bm = (D == 64) ? 128 : 64;
+  if (!make_map(&mq, q, kp.batch, kp.rows_total, kp.heads_q, D, bm) ||
+      !make_map(&mdo, dout, kp.batch, kp.rows_total, kp.heads_q, D, bm) ||
+      !make_map(&mk, k, kp.batch, kp.rows_total, kp.heads_kv, D, 128) ||
+      !make_map(&mv, v, kp.batch, kp.rows_total, kp.heads_kv, D, 128))
+    return ATTN_ERR_CUDA;
+  BwdArgs a;
+  a.p = kp;
+  a.lse = lse;
+  a.delta = delta;
+  a.dk = static_cast<__nv_bfloat16*>(dk);
+  a.dv = static_cast<__nv_bfloat16*>(dv);
+  a.dq_acc = static_cast<float*>(workspace);
+  a.split = (mode == ATTN_DQ_SPLIT) ? 1 : 0;
+  a.slab_elems = a.split ? dq_elems(kp, D) : 0;
+  a.n_split = a.split ? n_kv_tiles(kp) : 0;
+  a.scale_log2 = p->scale * kLog2e;
+  const int gx = tile_bound(kp.rows_total, kp.num_seqs, 128, kp.cu_seqlens != nullptr);
+  cudaError_t e = (D == 64) ? launch_attn_bwd<64>(mq, mk, mv, mdo, a, gx, st)
+                            : launch_attn_bwd<128>(mq, mk, mv, mdo, a, gx, st);
+  if (e != cudaSuccess) return ATTN_ERR_CUDA;
+  auto* dqb = static_cast<__nv_bfloat16*>(dq);
+  e = (D == 64) ? launch_dq_finalize<64>(kp, a.dq_acc, a.slab_elems, a.split, a.n_split, dqb,
+                                         a.dk, a.dv, st)
+                : launch_dq_finalize<128>(kp, a.dq_acc, a.slab_elems, a.split, a.n_split, dqb,
+                                          a.dk, a.dv, st);
+  return cuda_status(e);
+}
+
+
+// ---------------------------------------------------------------------------
+// Sparse
+// ---------------------------------------------------------------------------
+static attn_status_t check_sparse(const sparse_attn_problem_t* p, bool* empty) {
+  *empty = false;
+  if (!p) return ATTN_ERR_INVALID_ARG;
+  if (p->tokens < 0 || p->heads <= 0 || p->topk < 0 || p->dim_qk <= 0 || p->dim_v <= 0)
+    return ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(p->scale)) return ATTN_ERR_INVALID_ARG;
+  if (p->dim_qk != 576 || p->dim_v != 512) return ATTN_ERR_UNSUPPORTED;
+  if (p->heads != 16 && p->heads != 32 && p->heads != 64 && p->heads != 128)
+    return ATTN_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(p->tokens) * p->heads * p->dim_qk >= (int64_t(1) << 31))
+    return ATTN_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(p->tokens) * p->topk >= (int64_t(1) << 31)) return ATTN_ERR_UNSUPPORTED;
+  if (p->tokens > 2147483647 / 2) return ATTN_ERR_UNSUPPORTED;
+  if (p->tokens == 0) *empty = true;
+  return ATTN_OK;
+}
+
+static SparseArgs sparse_args(const sparse_attn_problem_t* p) {
+  SparseArgs a{};
+  a.T = p->tokens;
+  a.H = p->heads;
+  a.K = p->topk;
+  a.scale = p->scale;
+  a.scale_log2 = p->scale * kLog2e;
+  a.err = p->error_word;
+  return a;
+}
+
+static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+attn_status_t sparse_attn_fwd(const sparse_attn_problem_t* p, const void* q, const void* kv,
+                              const int32_t* idx, void* o, float* lse, attn_stream_t stream) {
+  bool empty;
+  attn_status_t s = check_sparse(p, &empty);
+  if (s != ATTN_OK) return s;
+  if (!q || !kv || !o || !lse || (!idx && p->topk > 0)) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(kv) || !aligned16(o) || !aligned16(lse) ||
+      (reinterpret_cast<uintptr_t>(idx) & 3u))
+    return ATTN_ERR_ALIGNMENT;
+  if (empty) return ATTN_OK;
+  SparseArgs a = sparse_args(p);
+  a.q = static_cast<const __nv_bfloat16*>(q);
+  a.kv = static_cast<const __nv_bfloat16*>(kv);
+  a.idx = idx;
+  a.o = static_cast<__nv_bfloat16*>(o);
+  a.lse = lse;
+  return cuda_status(launch_sparse_fwd(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t sparse_attn_bwd_workspace_size(const sparse_attn_problem_t* p) {
+  bool empty;
+  if (check_sparse(p, &empty) != ATTN_OK || empty) return 0;
+  return align256(static_cast<size_t>(p->tokens) * p->dim_qk * sizeof(float)) +
+         align256(static_cast<size_t>(p->tokens) * p->heads * sizeof(float));
+}
+
+attn_status_t sparse_attn_bwd(const sparse_attn_problem_t* p, const void* q, const void* kv,
+                              const int32_t* idx, const void* o, const void* dout,
+                              const float* lse, void* dq, void* dkv, void* workspace,
+                              size_t workspace_bytes, attn_stream_t stream) {
+  bool empty;
+  attn_status_t s = check_sparse(p, &empty);
+  if (s != ATTN_OK) return s;
+  if (!q || !kv || !o || !dout || !lse || !dq || !dkv || (!idx && p->topk > 0))
+    return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(kv) || !aligned16(o) || !aligned16(dout) || !aligned16(lse) ||
+      !aligned16(dq) || !aligned16(dkv) || (reinterpret_cast<uintptr_t>(idx) & 3u))
+    return ATTN_ERR_ALIGNMENT;
+  if (empty) return ATTN_OK;
+  const size_t need = sparse_attn_bwd_workspace_size(p);
+  if (!workspace || workspace_bytes < need) return ATTN_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return ATTN_ERR_ALIGNMENT;
+  SparseArgs a = sparse_args(p);
+  a.q = static_cast<const __nv_bfloat16*>(q);
+  a.kv = static_cast<const __nv_bfloat16*>(kv);
+  a.idx = idx;
+  a.o = static_cast<__nv_bfloat16*>(const_cast<void*>(o));
+  a.dout = static_cast<const __nv_bfloat16*>(dout);
+  a.lse_in = lse;
+  a.dq = static_cast<__nv_bfloat16*>(dq);
+  a.dkv_acc = static_cast<float*>(workspace);
+  float* delta = reinterpret_cast<float*>(
+      static_cast<uint8_t*>(workspace) +
+      align256(static_cast<size_t>(p->tokens) * p->dim_qk * sizeof(float)));
+  return cuda_status(launch_sparse_bwd(a, delta, static_cast<__nv_bfloat16*>(dkv),
+                                       reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

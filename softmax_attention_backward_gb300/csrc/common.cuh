@@ -1,0 +1,89 @@
+// Shared host/device definitions of the attention kernels: problem
+// descriptors passed to kernels, work decoding for dense and THD-packed
+// layouts, and small math helpers.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include "sm100.cuh"
+
+namespace attn {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Kernel-side view of a dense (BSHD) or THD-packed problem.  For THD the
+// tensors are treated as batch 1 with `rows_total` = capacity rows.
+struct Problem {
+  int batch;        // dense batch (1 for THD)
+  int rows_total;   // rows of the S dimension of every tensor (seqlen or capacity)
+  int heads_q;
+  int heads_kv;
+  int causal;
+  float scale;
+  const int32_t* cu_seqlens;  // null for dense
+  int num_seqs;
+  int max_seqlen;   // THD: bound on any sequence length
+  int32_t* err;
+};
+
+// One sequence of a problem: rows [row0, row0 + len) of batch entry `b`.
+struct SeqRef {
+  int b;
+  int row0;
+  int len;
+};
+
+// Decodes the linear tile index `x` (tiles of `tile_rows` rows) into a
+// sequence and the local tile index inside it.  Returns false when `x` maps to
+// no work (grids are sized by an upper bound for THD).
+__device__ __forceinline__ bool decode_tile(const Problem& p, int x, int bz, int tile_rows,
+                                            SeqRef& s, int& tile) {
+  if (p.cu_seqlens == nullptr) {
+    s.b = bz;
+    s.row0 = 0;
+    s.len = p.rows_total;
+    const int n = (p.rows_total + tile_rows - 1) / tile_rows;
+    if (x >= n) return false;
+    tile = x;
+    return true;
+  }
+  int rem = x;
+  int prev = __ldg(p.cu_seqlens);
+  for (int n = 0; n < p.num_seqs; ++n) {
+    const int next = __ldg(p.cu_seqlens + n + 1);
+    const int len = next > prev ? next - prev : 0;
+    const int nt = (len + tile_rows - 1) / tile_rows;
+    if (rem < nt) {
+      s.b = 0;
+      s.row0 = prev;
+      s.len = len;
+      tile = rem;
+      return true;
+    }
+    rem -= nt;
+    prev = next;
+  }
+  return false;
+}
+
+// Upper bound on the number of tiles of `tile_rows` rows over all sequences.
+inline int tile_bound(int rows_total, int num_seqs, int tile_rows, bool packed) {
+  const int base = (rows_total + tile_rows - 1) / tile_rows;
+  return packed ? base + num_seqs : base;
+}
+
+// End of the valid rows of a THD problem (cu_seqlens[num_seqs]); rows_total for dense.
+__device__ __forceinline__ int valid_end(const Problem& p) {
+  return p.cu_seqlens ? __ldg(p.cu_seqlens + p.num_seqs) : p.rows_total;
+}
+
+}  // namespace attn

@@ -1,0 +1,72 @@
+// Argument blocks and launch wrappers shared by the kernel translation units
+// and the C ABI layer.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+
+namespace attn {
+
+struct FwdArgs {
+  Problem p;
+  __nv_bfloat16* o;
+  float* lse;
+  float scale_log2;
+};
+
+struct BwdArgs {
+  Problem p;
+  const float* lse;
+  const float* delta;
+  __nv_bfloat16* dk;
+  __nv_bfloat16* dv;
+  float* dq_acc;        // ATOMIC: accumulator [rows, Hq, D]; SPLIT: slab base
+  size_t slab_elems;    // SPLIT: elements per slab (0 for ATOMIC)
+  int n_split;          // SPLIT: number of slabs
+  int split;            // 1 = SPLIT
+  float scale_log2;
+};
+
+template <int D>
+cudaError_t launch_attn_fwd(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                            const FwdArgs& a, int grid_x, cudaStream_t st);
+cudaError_t launch_thd_fwd_pad(const Problem& p, __nv_bfloat16* o, float* lse, int head_dim,
+                               cudaStream_t st);
+template <int D>
+cudaError_t launch_attn_bwd(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                            const CUtensorMap& dO, const BwdArgs& a, int grid_x, cudaStream_t st);
+template <int D>
+cudaError_t launch_bwd_preprocess(const Problem& p, const __nv_bfloat16* o,
+                                  const __nv_bfloat16* dout, float* delta, float* dq_acc,
+                                  size_t acc_elems, cudaStream_t st);
+template <int D>
+cudaError_t launch_dq_finalize(const Problem& p, const float* acc, size_t slab_elems, int split,
+                               int n_split, __nv_bfloat16* dq, __nv_bfloat16* dk,
+                               __nv_bfloat16* dv, cudaStream_t st);
+
+}  // namespace attn
+
+namespace attn {
+
+struct SparseArgs {
+  const __nv_bfloat16* q;
+  const __nv_bfloat16* kv;
+  const int32_t* idx;
+  __nv_bfloat16* o;
+  float* lse;
+  const __nv_bfloat16* dout;
+  const float* lse_in;
+  const float* delta;
+  __nv_bfloat16* dq;
+  float* dkv_acc;
+  int T, H, K;
+  float scale, scale_log2;
+  int32_t* err;
+};
+
+cudaError_t launch_sparse_fwd(const SparseArgs& a, cudaStream_t st);
+cudaError_t launch_sparse_bwd(const SparseArgs& a, float* delta, __nv_bfloat16* dkv,
+                              cudaStream_t st);
+
+}  // namespace attn

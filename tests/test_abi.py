@@ -1,0 +1,128 @@
+"""Host-only checks of the C ABI: the library builds and loads, exports every
+function declared in include/attn.h, and rejects invalid calls before touching
+the GPU (no kernel is launched here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import softmax_attention_backward_gb300 as A
+from softmax_attention_backward_gb300 import build as B
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include",
+                      "attn.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    B.build()
+    return A.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\*?\s*([a-z_0-9]+)\(", text,
+                                 flags=re.M)))
+
+
+def test_every_declared_function_is_exported(L):
+    names = declared_functions()
+    assert set(names) == set(A.EXPORTED_SYMBOLS), names
+    for n in names:
+        assert getattr(L, n) is not None
+
+
+def test_status_strings_and_version(L):
+    assert A.attn_status_string(0) == "ok"
+    assert "aligned" in A.attn_status_string(3)
+    assert A.attn_status_string(99) == "unknown status"
+    assert A.attn_version() >= 100
+
+
+def _problem(**kw):
+    p = A._Problem()
+    p.batch, p.seqlen, p.heads_q, p.heads_kv, p.head_dim = 1, 128, 2, 2, 64
+    p.causal, p.scale = 0, 0.125
+    p.cu_seqlens, p.num_seqs, p.capacity, p.max_seqlen, p.error_word = None, 0, 0, 0, None
+    for k, v in kw.items():
+        setattr(p, k, v)
+    return p
+
+
+FAKE = 0x10000   # 16-byte aligned; never dereferenced (validation fails first or nothing runs)
+
+
+def _fwd(L, p, ptrs=(FAKE,) * 5):
+    return L.attn_fwd(ctypes.byref(p), *[ctypes.c_void_p(x) for x in ptrs], None)
+
+
+def test_dense_validation(L):
+    assert _fwd(L, _problem(head_dim=96)) == 2                     # unsupported dim
+    assert _fwd(L, _problem(heads_q=3, heads_kv=2)) == 1           # group mismatch
+    assert _fwd(L, _problem(heads_kv=0)) == 1
+    assert _fwd(L, _problem(scale=float("nan"))) == 1
+    assert _fwd(L, _problem(), (FAKE, 0, FAKE, FAKE, FAKE)) == 1   # null k
+    assert _fwd(L, _problem(), (FAKE, FAKE + 8, FAKE, FAKE, FAKE)) == 3
+    assert _fwd(L, _problem(seqlen=0)) == 0                         # empty: nothing enqueued
+    assert _fwd(L, _problem(batch=0)) == 0
+    assert L.attn_fwd(None, *[ctypes.c_void_p(FAKE)] * 5, None) == 1
+
+
+def test_thd_validation_and_workspace(L):
+    thd = dict(cu_seqlens=FAKE, num_seqs=4, capacity=32768, max_seqlen=3670, head_dim=128,
+               heads_q=16, heads_kv=16)
+    assert _fwd(L, _problem(**dict(thd, num_seqs=0))) == 1
+    assert _fwd(L, _problem(**dict(thd, cu_seqlens=FAKE + 2))) == 3
+    assert _fwd(L, _problem(**dict(thd, capacity=0))) == 0
+    p = _problem(**thd)
+    per = 32768 * 16 * 128 * 4
+    assert L.attn_bwd_workspace_size(ctypes.byref(p), 0) == per
+    assert L.attn_bwd_workspace_size(ctypes.byref(p), 1) == per * ((3670 + 127) // 128)
+    # workspace missing / too small is rejected before any launch
+    args = [ctypes.c_void_p(FAKE)] * 10
+    assert L.attn_bwd(ctypes.byref(p), 0, *args[:9], None, 0, None) == 5
+    assert L.attn_bwd(ctypes.byref(p), 0, *args[:9], ctypes.c_void_p(FAKE), 16, None) == 5
+    assert L.attn_bwd(ctypes.byref(p), 7, *args[:9], ctypes.c_void_p(FAKE), per, None) == 1
+    assert L.attn_bwd_preprocess(ctypes.byref(p), 0, *args[:3], None, 0, None) == 5
+
+
+def test_dense_workspace_sizes(L):
+    p = _problem(batch=4, seqlen=4096, heads_q=32, heads_kv=8, head_dim=128, causal=1)
+    per = 4 * 4096 * 32 * 128 * 4
+    assert L.attn_bwd_workspace_size(ctypes.byref(p), 0) == per
+    assert L.attn_bwd_workspace_size(ctypes.byref(p), 1) == per * 32
+    assert L.attn_bwd_workspace_size(ctypes.byref(_problem(head_dim=80)), 0) == 0
+
+
+def _sparse(**kw):
+    p = A._SparseProblem()
+    p.tokens, p.heads, p.dim_qk, p.dim_v, p.topk, p.scale, p.error_word = 8192, 64, 576, 512, \
+        2048, 1 / 24, None
+    for k, v in kw.items():
+        setattr(p, k, v)
+    return p
+
+
+def test_sparse_validation(L):
+    f = lambda p, ptrs=(FAKE,) * 5: L.sparse_attn_fwd(ctypes.byref(p),
+                                                      *[ctypes.c_void_p(x) for x in ptrs], None)
+    assert f(_sparse(dim_qk=512)) == 2
+    assert f(_sparse(dim_v=256)) == 2
+    assert f(_sparse(heads=48)) == 2
+    assert f(_sparse(tokens=-1)) == 1
+    assert f(_sparse(), (FAKE, FAKE, FAKE + 2, FAKE, FAKE)) == 3     # idx not 4-byte aligned
+    assert f(_sparse(tokens=0)) == 0
+    p = _sparse()
+    ws = L.sparse_attn_bwd_workspace_size(ctypes.byref(p))
+    assert ws == 8192 * 576 * 4 + 8192 * 64 * 4
+    args = [ctypes.c_void_p(FAKE)] * 8          # q kv idx o dout lse dq dkv
+    assert L.sparse_attn_bwd(ctypes.byref(p), *args, ctypes.c_void_p(FAKE), ws - 1, None) == 5
+
+
+def test_python_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(A, "_LIB", None)
+    monkeypatch.setattr(A, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="missing"):
+        A.lib()

@@ -1,0 +1,178 @@
+"""GPU parity of the CUDA path (through the C ABI) against the fp64 oracle.
+
+Small cases are compared in full; the full-size workloads are compared on
+sampled independent units (a (batch, kv-head) group, a sequence, a token, a
+key row) that the oracle computes on their own, with the kernels launched at
+full size exactly as the benchmark launches them."""
+import pytest
+import torch
+
+import oracle
+import softmax_attention_backward_gb300 as A
+from softmax_attention_backward_gb300 import workloads as W
+from _util import assert_close, assert_lse, workload_inputs
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda:0") if torch.cuda.is_available() else None
+MODES = [A.ATTN_DQ_ATOMIC, A.ATTN_DQ_SPLIT]
+
+
+def _gpu(*ts):
+    return [t.to(DEV) for t in ts]
+
+
+def _err_word():
+    return torch.zeros(1, dtype=torch.int32, device=DEV)
+
+
+def _check_err(err, expect=0):
+    torch.cuda.synchronize()
+    assert int(err.item()) == expect, f"device error word {int(err.item()):#x}"
+
+
+def run_dense(q, k, v, do, causal, scale, mode, cu=None, max_seqlen=None):
+    err = _err_word()
+    gq, gk, gv, gdo = _gpu(q, k, v, do)
+    gcu = cu.to(DEV) if cu is not None else None
+    o, lse = A.attn_fwd(gq, gk, gv, causal=causal, scale=scale, cu_seqlens=gcu,
+                        max_seqlen=max_seqlen, error_word=err)
+    dq, dk, dv = A.dense_backward(gq, gk, gv, o, lse, gdo, mode=mode, causal=causal, scale=scale,
+                                  cu_seqlens=gcu, max_seqlen=max_seqlen, error_word=err)
+    _check_err(err)
+    return dict(o=o, lse=lse, dq=dq, dk=dk, dv=dv)
+
+
+def compare_dense(got, ref, units, hq, hkv):
+    grp = hq // hkv
+    for b, g in units:
+        hs = slice(g * grp, (g + 1) * grp)
+        assert_close(f"o[{b},{g}]", got["o"][b, :, hs], ref["o"][b, :, hs])
+        assert_lse(f"lse[{b},{g}]", got["lse"][b, hs], ref["lse"][b, hs])
+        assert_close(f"dq[{b},{g}]", got["dq"][b, :, hs], ref["dq"][b, :, hs])
+        assert_close(f"dk[{b},{g}]", got["dk"][b, :, g], ref["dk"][b, :, g])
+        assert_close(f"dv[{b},{g}]", got["dv"][b, :, g], ref["dv"][b, :, g])
+
+
+# ----------------------------------------------------------------------------
+# Dense BSHD
+# ----------------------------------------------------------------------------
+@pytest.mark.parametrize("mode", MODES)
+def test_mha_s128_d64_full(mode):
+    w, x = workload_inputs("mha_s128_d64")
+    got = run_dense(x["q"], x["k"], x["v"], x["do"], w.causal, w.scale, mode)
+    ref = oracle.dense_backward(x["q"], x["k"], x["v"], x["do"], w.scale, w.causal)
+    compare_dense(got, ref, [(0, 0), (0, 1)], 2, 2)
+
+
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("B,S,hq,hkv,D,causal", [
+    (2, 200, 4, 2, 64, True),      # ragged tail, GQA 2:1
+    (1, 129, 2, 2, 128, False),    # one row past a tile
+    (2, 333, 8, 2, 128, True),     # several tiles + tail, GQA 4:1
+    (1, 1, 2, 1, 64, True),        # a single row
+    (1, 384, 3, 1, 64, False),     # three query heads per kv head
+])
+def test_dense_small_full(mode, B, S, hq, hkv, D, causal):
+    q, k, v, do = W.dense_inputs(B, S, hq, hkv, D, seed=100 + S)
+    scale = D ** -0.5
+    got = run_dense(q, k, v, do, causal, scale, mode)
+    ref = oracle.dense_backward(q, k, v, do, scale, causal)
+    compare_dense(got, ref, [(b, g) for b in range(B) for g in range(hkv)], hq, hkv)
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_mha_causal_b8_h32_s1024_d64_sampled(mode):
+    w, x = workload_inputs("mha_causal_b8_h32_s1024_d64")
+    got = run_dense(x["q"], x["k"], x["v"], x["do"], w.causal, w.scale, mode)
+    units = [(0, 0), (3, 17), (7, 31)]
+    ref = oracle.dense_backward(x["q"], x["k"], x["v"], x["do"], w.scale, w.causal, kv_heads=units)
+    compare_dense(got, ref, units, w.heads_q, w.heads_kv)
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_gqa_causal_b4_h32x8_s4096_d128_sampled(mode):
+    w, x = workload_inputs("gqa_causal_b4_h32x8_s4096_d128")
+    got = run_dense(x["q"], x["k"], x["v"], x["do"], w.causal, w.scale, mode)
+    units = [(0, 0), (3, 7)]
+    ref = oracle.dense_backward(x["q"], x["k"], x["v"], x["do"], w.scale, w.causal, kv_heads=units)
+    compare_dense(got, ref, units, w.heads_q, w.heads_kv)
+
+
+# ----------------------------------------------------------------------------
+# THD packed variable length
+# ----------------------------------------------------------------------------
+def compare_thd(got, ref, cu, seqs, hq, hkv):
+    cu = cu.tolist()
+    for n in seqs:
+        s = slice(cu[n], cu[n + 1])
+        assert_close(f"o[seq {n}]", got["o"][s], ref["o"][s])
+        assert_lse(f"lse[seq {n}]", got["lse"][:, s], ref["lse"][:, s])
+        for key in ("dq", "dk", "dv"):
+            assert_close(f"{key}[seq {n}]", got[key][s], ref[key][s])
+    end = cu[-1]
+    for key in ("o", "dq", "dk", "dv"):
+        pad = got[key][end:]
+        assert (pad == 0).all(), f"{key}: padding rows are not exact zeros"
+    assert torch.isneginf(got["lse"][:, end:]).all()
+
+
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("D", [64, 128])
+def test_thd_small_full(mode, D):
+    lens = [1, 130, 77, 256, 3]
+    cap = 600
+    cu = W.cu_seqlens_from(lens)
+    q, k, v, do = W.thd_inputs(cap, 4, 2, D, seed=7)
+    scale = D ** -0.5
+    got = run_dense(q, k, v, do, True, scale, mode, cu=cu, max_seqlen=max(lens))
+    ref = oracle.thd_backward(q, k, v, do, cu, scale, True)
+    compare_thd(got, ref, cu, range(len(lens)), 4, 2)
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_thd_varlen_causal_h16_d128_sampled(mode):
+    w, x = workload_inputs("thd_varlen_causal_h16_d128")
+    got = run_dense(x["q"], x["k"], x["v"], x["do"], w.causal, w.scale, mode, cu=x["cu_seqlens"],
+                    max_seqlen=max(w.lengths))
+    ref = oracle.thd_backward(x["q"], x["k"], x["v"], x["do"], x["cu_seqlens"], w.scale, w.causal,
+                              seqs=[1])
+    compare_thd(got, ref, x["cu_seqlens"], [1], w.heads_q, w.heads_kv)
+
+
+# ----------------------------------------------------------------------------
+# Top-k sparse
+# ----------------------------------------------------------------------------
+def run_sparse(q, kv, idx, do, scale):
+    err = _err_word()
+    gq, gkv, gidx, gdo = _gpu(q, kv, idx, do)
+    o, lse = A.sparse_attn_fwd(gq, gkv, gidx, scale=scale, error_word=err)
+    dq, dkv = A.sparse_attn_bwd(gq, gkv, gidx, o, gdo, lse, scale=scale, error_word=err)
+    _check_err(err)
+    return dict(o=o, lse=lse, dq=dq, dkv=dkv)
+
+
+@pytest.mark.parametrize("T,H,K", [(600, 64, 256), (300, 16, 100), (200, 128, 64), (150, 32, 33)])
+def test_sparse_small_full(T, H, K):
+    q, kv, do, idx = W.sparse_inputs(T, H, K, seed=20 + H)
+    scale = 576 ** -0.5
+    got = run_sparse(q, kv, idx, do, scale)
+    ref = oracle.sparse_backward(q, kv, idx, do, scale)
+    assert_close("o", got["o"], ref["o"])
+    assert_lse("lse", got["lse"], ref["lse"])
+    assert_close("dq", got["dq"], ref["dq"])
+    assert_close("dkv", got["dkv"], ref["dkv"])
+
+
+def test_sparse_topk2048_t8192_h64_sampled():
+    w, x = workload_inputs("sparse_topk2048_t8192_h64")
+    got = run_sparse(x["q"], x["kv"], x["idx"], x["do"], w.scale)
+    q, kv, idx, do = (x[n].double() if n != "idx" else x[n] for n in ("q", "kv", "idx", "do"))
+    for t in (0, 1, 2047, 2048, 5000, 8191):
+        r = oracle.sparse_token(q[t], kv, idx[t], do[t], w.scale)
+        assert_close(f"o[{t}]", got["o"][t], r["o"])
+        assert_lse(f"lse[{t}]", got["lse"][t], r["lse"])
+        assert_close(f"dq[{t}]", got["dq"][t], r["dq"])
+    rows = [8191, 8150, 8100]
+    ref = oracle.sparse_dkv_rows(x["q"], x["kv"], x["idx"], x["do"], w.scale, rows)
+    for c, j in enumerate(rows):
+        assert_close(f"dkv[{j}]", got["dkv"][j], ref[c])

@@ -1,0 +1,452 @@
+#!/usr/bin/env python
+"""Benchmark of the attention training step (forward + backward) on GB300.
+
+One step = attn_fwd + attn_bwd_preprocess + attn_bwd + attn_bwd_postprocess over
+the dense causal MHA workload B=8, H=32, S=1024, D=64 (bf16, synthetic N(0,1)
+inputs).  Prints one JSON line.  `--impl reference` times the fp64 CPU oracle on
+the same workload instead (bounded samples on the host cores).
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+For N > 1 launch with torchrun; every rank runs the full workload (weak scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from softmax_attention_backward_gb300 import workloads as W  # noqa: E402
+
+METRIC = "attention fwd+bwd TFLOP/s (bf16, 1 GB300) and % of dense BF16 tensor peak"
+DEFAULT_WORKLOAD = "mha_causal_b8_h32_s1024_d64"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_FLUSH_BYTES = 256 << 20
+
+
+# ----------------------------------------------------------------------------
+# helpers
+# ----------------------------------------------------------------------------
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def dense_flops(w):
+    """Algorithmic FLOPs: forward 4*B*H*S^2*D (x0.5 causal), backward 2.5x forward."""
+    if w.kind == "thd":
+        f = 4.0 * w.heads_q * w.head_dim * sum(n * n for n in w.lengths) * (0.5 if w.causal else 1)
+    else:
+        f = 4.0 * w.batch * w.heads_q * w.seqlen ** 2 * w.head_dim * (0.5 if w.causal else 1.0)
+    return f, 2.5 * f
+
+
+def source_sha(rel):
+    with open(os.path.join(ROOT, rel), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()
+
+
+def profiled_traffic(kernel, workload, src_rel):
+    """dram bytes per launch from a committed ncu summary, if the kernel source
+    has not changed since it was captured (else None)."""
+    pdir = os.path.join(ROOT, "profiles")
+    if not os.path.isdir(pdir):
+        return None
+    sha = source_sha(src_rel)
+    for fn in sorted(os.listdir(pdir)):
+        if not fn.endswith((".md", ".txt")):
+            continue
+        text = open(os.path.join(pdir, fn)).read()
+        fields = dict(re.findall(r"^\s*[-*]?\s*([a-z_0-9]+):\s*`?([^`\n]+)`?\s*$", text, re.M))
+        if (fields.get("kernel") == kernel and fields.get("workload") == workload
+                and fields.get("source_sha256") == sha and "dram_bytes_per_launch" in fields):
+            return float(fields["dram_bytes_per_launch"])
+    return None
+
+
+class ClockSampler:
+    """Samples nvidia-smi every 50 ms while active; keeps samples inside marks."""
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+    NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+    def __init__(self, index):
+        self.samples, self.t0, self.t1 = [], None, None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={index}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.th = threading.Thread(target=self._read, daemon=True)
+            self.th.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), [x.strip() for x in line.split(",")]))
+
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.12)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        inside = [s for t, s in self.samples if self.t0 - 0.06 <= t <= self.t1 + 0.06]
+        if not inside and self.samples:   # timed region shorter than the period
+            mid = 0.5 * (self.t0 + self.t1)
+            inside = [min(self.samples, key=lambda ts: abs(ts[0] - mid))[1]]
+        sm, smax, reasons = [], [], set()
+        for s in inside:
+            try:
+                sm.append(float(s[0]))
+                smax.append(float(s[1]))
+            except (ValueError, IndexError):
+                continue
+            for name, val in zip(self.NAMES, s[3:7]):
+                if val.strip().lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    return world, rank, local
+
+
+def reduce_max(x, world):
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    dev = torch.device("cuda", torch.cuda.current_device()) if torch.cuda.is_available() else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ----------------------------------------------------------------------------
+# oracle (CPU) leg
+# ----------------------------------------------------------------------------
+def oracle_unit_rate(w, x, budget_s, units=None):
+    """Times the fp64 oracle over (batch, kv-head) units until `budget_s` is spent.
+    Returns (TFLOP/s, units done, seconds)."""
+    import oracle
+    f_fwd, f_bwd = dense_flops(w)
+    per_unit = (f_fwd + f_bwd) / (w.batch * w.heads_kv)
+    all_units = units or [(b, g) for b in range(w.batch) for g in range(w.heads_kv)]
+    done, t0 = 0, time.perf_counter()
+    while True:
+        b, g = all_units[done % len(all_units)]
+        oracle.dense_backward(x["q"], x["k"], x["v"], x["do"], w.scale, w.causal, kv_heads=[(b, g)])
+        done += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    return per_unit * done / el / 1e12, done, el
+
+
+def run_reference(args, w, world, rank):
+    if rank != 0:
+        return
+    torch.set_num_threads(len(os.sched_getaffinity(0)))
+    x = W.make_inputs(w)
+    cores = torch.get_num_threads()
+    for _ in range(args.warmup):
+        oracle_unit_rate(w, x, 0.0)
+    times, units = [], 0
+    f_fwd, f_bwd = dense_flops(w)
+    per_unit = (f_fwd + f_bwd) / (w.batch * w.heads_kv)
+    for _ in range(args.steps):
+        _, n, el = oracle_unit_rate(w, x, 0.0)
+        times.append(el)
+        units += n
+    total = sum(times)
+    value = per_unit * units / total / 1e12
+    sample = f"{units} (batch, kv-head) units of {w.name}, one per step, fp64 oracle"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_of(w, "oracle", world),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_of(w, mode, world):
+    c = {"workload": w.name, "batch": w.batch, "seqlen": w.seqlen, "heads_q": w.heads_q,
+         "heads_kv": w.heads_kv, "head_dim": w.head_dim, "causal": w.causal, "dq_mode": mode,
+         "l2": "flushed between timed steps (256 MiB write)",
+         "parallelism": "replicas" if world == 1 else f"replicas x{world}"}
+    return c
+
+
+# ----------------------------------------------------------------------------
+# our leg
+# ----------------------------------------------------------------------------
+def run_ours(args, w, world, rank, local):
+    import softmax_attention_backward_gb300 as A
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    A.lib()
+    x = W.make_inputs(w)
+    q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "do"))
+    o = torch.empty_like(q)
+    lse = torch.empty(w.batch, w.heads_q, w.seqlen, dtype=torch.float32, device=dev)
+    delta = torch.empty_like(lse)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    kw = dict(causal=w.causal, scale=w.scale)
+    ws = {}
+    for mode in (A.ATTN_DQ_ATOMIC, A.ATTN_DQ_SPLIT):
+        n = A.attn_bwd_workspace_size(q, k, mode=mode, **kw)
+        ws[mode] = torch.empty(n, dtype=torch.uint8, device=dev)
+    f_fwd, f_bwd = dense_flops(w)
+    stream = torch.cuda.current_stream()
+
+    def step(mode, ev=None):
+        if ev:
+            ev[0].record(stream)
+        A.attn_fwd(q, k, v, out=o, lse=lse, **kw)
+        if ev:
+            ev[1].record(stream)
+        A.attn_bwd_preprocess(q, k, o, do, mode=mode, workspace=ws[mode], delta=delta, **kw)
+        if ev:
+            ev[2].record(stream)
+        A.attn_bwd(q, k, v, do, lse, delta, mode=mode, workspace=ws[mode], dk=dk, dv=dv, **kw)
+        if ev:
+            ev[3].record(stream)
+        A.attn_bwd_postprocess(q, k, dk, dv, mode=mode, workspace=ws[mode], dq=dq, **kw)
+        if ev:
+            ev[4].record(stream)
+
+    def timed(mode, steps, sampler=None):
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(steps)]
+        barrier(world)
+        torch.cuda.synchronize()
+        if sampler:
+            sampler.mark_start()
+        for i in range(steps):
+            flush.zero_()
+            step(mode, evs[i])
+        torch.cuda.synchronize()
+        if sampler:
+            sampler.mark_end()
+        barrier(world)
+        tot = [e[0].elapsed_time(e[4]) for e in evs]
+        fwd = [e[0].elapsed_time(e[1]) for e in evs]
+        bwd = [e[1].elapsed_time(e[4]) for e in evs]
+        main = [e[2].elapsed_time(e[3]) for e in evs]
+        return {k_: sum(v_) / steps for k_, v_ in
+                (("total", tot), ("fwd", fwd), ("bwd", bwd), ("bwd_main", main))}
+
+    # warm-up (both modes), then the timed atomic-mode steps with clocks sampled
+    for _ in range(args.warmup):
+        step(A.ATTN_DQ_ATOMIC)
+        step(A.ATTN_DQ_SPLIT)
+    torch.cuda.synchronize()
+    sampler = ClockSampler(f"GPU-{torch.cuda.get_device_properties(dev).uuid}") if rank == 0 else None
+    t_atomic = timed(A.ATTN_DQ_ATOMIC, args.steps, sampler)
+    clocks = sampler.stop() if sampler else None
+    t_split = timed(A.ATTN_DQ_SPLIT, args.steps)
+
+    ms = reduce_max(t_atomic["total"], world)
+    ms_main = reduce_max(t_atomic["bwd_main"], world)
+    ms_fwd = reduce_max(t_atomic["fwd"], world)
+    ms_bwd = reduce_max(t_atomic["bwd"], world)
+    ms_split = reduce_max(t_split["total"], world)
+    ms_split_bwd = reduce_max(t_split["bwd"], world)
+
+    # end to end through the public API: pinned host inputs -> device -> results -> host
+    hq, hk, hv, hdo = (x[n].pin_memory() for n in ("q", "k", "v", "do"))
+    out_h = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (dq, dk, dv)]
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo))
+    d2h = sum(t.numel() * t.element_size() for t in out_h)
+
+    def e2e_step():
+        q.copy_(hq, non_blocking=True)
+        k.copy_(hk, non_blocking=True)
+        v.copy_(hv, non_blocking=True)
+        do.copy_(hdo, non_blocking=True)
+        step(A.ATTN_DQ_ATOMIC)
+        for h, d in zip(out_h, (dq, dk, dv)):
+            h.copy_(d, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e_start.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e_end.record(stream)
+    torch.cuda.synchronize()
+    ms_e2e = reduce_max(e_start.elapsed_time(e_end) / args.steps, world)
+
+    extra = {}
+    if rank == 0 and not args.no_sparse:
+        extra["sparse"] = bench_sparse(args, dev, flush)
+
+    if rank != 0:
+        return
+    pk, pk_kind = peaks()
+    tflops = lambda flops, ms_: flops / (ms_ * 1e-3) / 1e12
+    value = world * tflops(f_fwd + f_bwd, ms)
+    peak = pk["bf16_tflops"]
+    achieved = tflops(f_bwd, ms_main)
+    traffic = profiled_traffic("attn_bwd_kernel", w.name,
+                               "softmax_attention_backward_gb300/csrc/attn_bwd.cu")
+    cpu = cpu_baseline(w, args.cpu_seconds)
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": config_of(w, "atomic", world),
+        "pct_of_peak": 100.0 * tflops(f_fwd + f_bwd, ms) / peak,
+        "fwd_tflops": tflops(f_fwd, ms_fwd), "bwd_tflops": tflops(f_bwd, ms_bwd),
+        "split": {"fwd_bwd_tflops": tflops(f_fwd + f_bwd, ms_split),
+                  "bwd_tflops": tflops(f_bwd, ms_split_bwd), "ms_per_step": ms_split},
+        "roofline": {"kernel": "attn_bwd_kernel", "bound": "tensor", "achieved": achieved,
+                     "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                     "peak_kind": f"{pk_kind} bf16 burst",
+                     "traffic": traffic, "flops_per_launch": f_bwd},
+        "cpu_baseline": cpu,
+        "clocks": clocks,
+        "e2e": {"value": world * tflops(f_fwd + f_bwd, ms_e2e), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e},
+        "gpu_launches": 4 * args.steps,
+        **extra,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def sparse_logical_bytes(T, H, idx):
+    """Logical bytes of the sparse path: gathered KV rows (576 bf16 once per
+    token and selected key), Q, O, idx; backward adds dO, dQ and 576 fp32
+    atomic adds per selected key."""
+    pairs = int((idx >= 0).sum().item())
+    q_b, o_b = T * H * 576 * 2, T * H * 512 * 2
+    idx_b = idx.numel() * 4
+    gather = pairs * 576 * 2
+    fwd = q_b + gather + idx_b + o_b + T * H * 4
+    bwd = q_b + gather + idx_b + 2 * o_b + T * H * 4 + T * H * 576 * 2 + pairs * 576 * 4 * 2
+    return fwd, bwd, pairs
+
+
+def bench_sparse(args, dev, flush):
+    import softmax_attention_backward_gb300 as A
+    w = W.get_workload("sparse_topk2048_t8192_h64")
+    x = W.make_inputs(w)
+    q, kv, do, idx = (x[n].to(dev) for n in ("q", "kv", "do", "idx"))
+    o = torch.empty(w.seqlen, w.heads_q, 512, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(w.seqlen, w.heads_q, dtype=torch.float32, device=dev)
+    dq, dkv = torch.empty_like(q), torch.empty_like(kv)
+    ws = torch.empty(A.sparse_attn_bwd_workspace_size(q, idx), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    steps = max(3, min(args.steps, 10))
+    for _ in range(3):
+        A.sparse_attn_fwd(q, kv, idx, scale=w.scale, out=o, lse=lse)
+        A.sparse_attn_bwd(q, kv, idx, o, do, lse, scale=w.scale, workspace=ws, dq=dq, dkv=dkv)
+    f_ms, b_ms = [], []
+    for _ in range(steps):
+        flush.zero_()
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        e[0].record(stream)
+        A.sparse_attn_fwd(q, kv, idx, scale=w.scale, out=o, lse=lse)
+        e[1].record(stream)
+        A.sparse_attn_bwd(q, kv, idx, o, do, lse, scale=w.scale, workspace=ws, dq=dq, dkv=dkv)
+        e[2].record(stream)
+        torch.cuda.synchronize()
+        f_ms.append(e[0].elapsed_time(e[1]))
+        b_ms.append(e[1].elapsed_time(e[2]))
+    fb, bb, pairs = sparse_logical_bytes(w.seqlen, w.heads_q, x["idx"])
+    fm, bm = sum(f_ms) / steps, sum(b_ms) / steps
+    hbm = peaks()[0]["hbm_gbs"]
+    flops_f = pairs * w.heads_q * 2 * (576 + 512)
+    flops_b = pairs * w.heads_q * 2 * (3 * 576 + 2 * 512)
+    return {"workload": w.name, "steps": steps, "fwd_ms": fm, "bwd_ms": bm,
+            "fwd_logical_gbs": fb / fm / 1e6, "bwd_logical_gbs": bb / bm / 1e6,
+            "fwd_frac_hbm": fb / fm / 1e6 / hbm, "bwd_frac_hbm": bb / bm / 1e6 / hbm,
+            "fwd_tflops": flops_f / fm / 1e9, "bwd_tflops": flops_b / bm / 1e9,
+            "valid_pairs": pairs}
+
+
+def cpu_baseline(w, seconds):
+    torch.set_num_threads(len(os.sched_getaffinity(0)))
+    x = W.make_inputs(w)
+    rate, units, el = oracle_unit_rate(w, x, seconds)
+    return {"value": rate, "unit": "TFLOP/s", "cores": torch.get_num_threads(), "kind": "oracle",
+            "sample": f"{units} (batch, kv-head) units of {w.name} (fwd+bwd, fp64) in {el:.1f} s"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-sparse", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    world, rank, local = dist_setup()
+    w = W.get_workload(args.workload)
+    if w.kind != "dense":
+        raise SystemExit("bench.py times the dense workloads; use the tests for the others")
+    if args.impl == "reference":
+        run_reference(args, w, world, rank)
+    else:
+        run_ours(args, w, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

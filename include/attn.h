@@ -12,11 +12,12 @@
  *   attn_bwd              recomputes P = exp(scale * Q K^T - LSE) tile by tile
  *                         and forms dV = P^T dO, dP = dO V^T,
  *                         dS = P o (dP - Delta), dK = scale dS^T Q,
- *                         dQ = scale dS K.  dQ is accumulated with fp32 atomics
- *                         (ATTN_DQ_ATOMIC; #940 description: fp32, never bf16,
- *                         atomics) or as per-KV-tile partials summed in a fixed
- *                         order (ATTN_DQ_SPLIT; #940 "split+sum template"),
- *                         then cast to bf16 (the "postprocess" stage).
+ *                         dQ = scale dS K.  dQ is accumulated in the workspace
+ *                         with fp32 atomics (ATTN_DQ_ATOMIC; #940 description:
+ *                         fp32, never bf16, atomics) or as per-KV-tile partials
+ *                         (ATTN_DQ_SPLIT; #940 "split+sum template").
+ *   attn_bwd_postprocess  dQ = bf16(scale * accumulator) or bf16(scale * sum of
+ *                         the partials in ascending KV-tile order).
  *   sparse_attn_fwd/bwd   the same with a per-token top-k key list over one
  *                         shared KV head of 576 = 512 + 64 dims, values the
  *                         first 512 dims ("[2/2] Add TileLang fused DSA kernels
@@ -121,13 +122,22 @@ attn_status_t attn_bwd_preprocess(const attn_problem_t* p, attn_dq_mode_t mode, 
                                   const void* dout, float* delta, void* workspace,
                                   size_t workspace_bytes, attn_stream_t stream);
 
-/* Backward: q, k, v, dout bf16; lse, delta fp32 (from attn_fwd and
- * attn_bwd_preprocess) -> dq, dk, dv bf16.  GQA dK/dV are summed over each KV
- * head's query heads inside the kernel (no atomics on dK/dV). */
+/* Backward main pass: q, k, v, dout bf16; lse, delta fp32 (from attn_fwd and
+ * attn_bwd_preprocess) -> dk, dv bf16 (every non-padding row) and the fp32 dQ
+ * accumulator or partials inside `workspace`.  GQA dK/dV are summed over each
+ * KV head's query heads inside the kernel (no atomics on dK/dV).  Must be
+ * followed by attn_bwd_postprocess with the same workspace and mode. */
 attn_status_t attn_bwd(const attn_problem_t* p, attn_dq_mode_t mode, const void* q,
                        const void* k, const void* v, const void* dout, const float* lse,
-                       const float* delta, void* dq, void* dk, void* dv, void* workspace,
+                       const float* delta, void* dk, void* dv, void* workspace,
                        size_t workspace_bytes, attn_stream_t stream);
+
+/* Backward postprocess: dq bf16 from the workspace of attn_bwd; for THD it also
+ * writes the padding rows (at or past cu_seqlens[num_seqs]) of dq, dk and dv as
+ * exact zeros.  After it, every element of dq, dk and dv has been written. */
+attn_status_t attn_bwd_postprocess(const attn_problem_t* p, attn_dq_mode_t mode,
+                                   const void* workspace, size_t workspace_bytes, void* dq,
+                                   void* dk, void* dv, attn_stream_t stream);
 
 /*
  * Top-k sparse attention over one shared KV head (SparseMLA style).

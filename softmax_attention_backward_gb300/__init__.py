@@ -6,7 +6,7 @@ library's CUDA kernels.  There is no CPU or eager fallback: if the library is
 missing or a call fails, an exception is raised.
 
 Entry points (same names as the C ABI):
-  attn_fwd, attn_bwd_workspace_size, attn_bwd_preprocess, attn_bwd,
+  attn_fwd, attn_bwd_workspace_size, attn_bwd_preprocess, attn_bwd, attn_bwd_postprocess,
   sparse_attn_fwd, sparse_attn_bwd_workspace_size, sparse_attn_bwd,
   attn_status_string, attn_version
 """
@@ -21,7 +21,7 @@ import torch
 
 __all__ = [
     "ATTN_DQ_ATOMIC", "ATTN_DQ_SPLIT", "AttnError", "lib", "attn_fwd", "attn_bwd_workspace_size",
-    "attn_bwd_preprocess", "attn_bwd", "sparse_attn_fwd", "sparse_attn_bwd_workspace_size",
+    "attn_bwd_preprocess", "attn_bwd", "attn_bwd_postprocess", "sparse_attn_fwd", "sparse_attn_bwd_workspace_size",
     "sparse_attn_bwd", "attn_status_string", "attn_version", "dense_backward",
     "SPARSE_DIM_QK", "SPARSE_DIM_V", "EXPORTED_SYMBOLS",
 ]
@@ -33,7 +33,7 @@ SPARSE_DIM_V = 512
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libattn.so")
 
 EXPORTED_SYMBOLS = (
-    "attn_fwd", "attn_bwd_workspace_size", "attn_bwd_preprocess", "attn_bwd",
+    "attn_fwd", "attn_bwd_workspace_size", "attn_bwd_preprocess", "attn_bwd", "attn_bwd_postprocess",
     "sparse_attn_fwd", "sparse_attn_bwd_workspace_size", "sparse_attn_bwd",
     "attn_status_string", "attn_version",
 )
@@ -80,7 +80,8 @@ def lib() -> ctypes.CDLL:
         L.attn_bwd_workspace_size.argtypes = [P, i32]
         L.attn_bwd_workspace_size.restype = sz
         L.attn_bwd_preprocess.argtypes = [P, i32, vp, vp, vp, vp, sz, vp]
-        L.attn_bwd.argtypes = [P, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+        L.attn_bwd.argtypes = [P, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+        L.attn_bwd_postprocess.argtypes = [P, i32, vp, sz, vp, vp, vp, vp]
         L.sparse_attn_fwd.argtypes = [SP, vp, vp, vp, vp, vp, vp]
         L.sparse_attn_bwd_workspace_size.argtypes = [SP]
         L.sparse_attn_bwd_workspace_size.restype = sz
@@ -88,8 +89,8 @@ def lib() -> ctypes.CDLL:
         L.attn_status_string.argtypes = [i32]
         L.attn_status_string.restype = ctypes.c_char_p
         L.attn_version.argtypes = []
-        for name in ("attn_fwd", "attn_bwd_preprocess", "attn_bwd", "sparse_attn_fwd",
-                     "sparse_attn_bwd"):
+        for name in ("attn_fwd", "attn_bwd_preprocess", "attn_bwd", "attn_bwd_postprocess",
+                     "sparse_attn_fwd", "sparse_attn_bwd"):
             getattr(L, name).restype = i32
         _LIB = L
     return _LIB
@@ -224,10 +225,11 @@ def attn_bwd_preprocess(q, k, o, dout, *, mode=ATTN_DQ_ATOMIC, workspace=None, c
 
 
 def attn_bwd(q, k, v, dout, lse, delta, *, mode=ATTN_DQ_ATOMIC, workspace, causal=False,
-             scale=None, cu_seqlens=None, max_seqlen=None, dq=None, dk=None, dv=None,
-             error_word=None, stream=None):
-    """Returns (dq, dk, dv) bf16.  Call attn_bwd_preprocess first with the same
-    workspace and mode."""
+             scale=None, cu_seqlens=None, max_seqlen=None, dk=None, dv=None, error_word=None,
+             stream=None):
+    """Main backward pass: returns (dk, dv) bf16 and leaves dQ (fp32) in the
+    workspace.  Call attn_bwd_preprocess before and attn_bwd_postprocess after,
+    with the same workspace and mode."""
     if int(mode) == ATTN_DQ_ATOMIC:
         _nondeterministic("attn_bwd(dq_mode=ATTN_DQ_ATOMIC)")
     dev = q.device
@@ -235,15 +237,27 @@ def attn_bwd(q, k, v, dout, lse, delta, *, mode=ATTN_DQ_ATOMIC, workspace, causa
         _need(t, n, torch.bfloat16, dev)
     _need(lse, "lse", torch.float32, dev)
     _need(delta, "delta", torch.float32, dev)
-    dq = dq if dq is not None else torch.empty_like(q)
     dk = dk if dk is not None else torch.empty_like(k)
     dv = dv if dv is not None else torch.empty_like(v)
     p = _problem(q, k, causal, scale, cu_seqlens, max_seqlen, error_word)
     _check("attn_bwd",
            lib().attn_bwd(ctypes.byref(p), int(mode), _ptr(q), _ptr(k), _ptr(v), _ptr(dout),
-                          _ptr(lse), _ptr(delta), _ptr(dq), _ptr(dk), _ptr(dv),
-                          _ptr(workspace), workspace.numel(), _stream(stream)))
-    return dq, dk, dv
+                          _ptr(lse), _ptr(delta), _ptr(dk), _ptr(dv), _ptr(workspace),
+                          workspace.numel(), _stream(stream)))
+    return dk, dv
+
+
+def attn_bwd_postprocess(q, k, dk, dv, *, mode=ATTN_DQ_ATOMIC, workspace, causal=False, scale=None,
+                         cu_seqlens=None, max_seqlen=None, dq=None, error_word=None, stream=None):
+    """Writes dq (bf16) from the workspace of attn_bwd; returns dq."""
+    dq = dq if dq is not None else torch.empty_like(q)
+    _need(dq, "dq", torch.bfloat16, q.device)
+    p = _problem(q, k, causal, scale, cu_seqlens, max_seqlen, error_word)
+    _check("attn_bwd_postprocess",
+           lib().attn_bwd_postprocess(ctypes.byref(p), int(mode), _ptr(workspace),
+                                      workspace.numel(), _ptr(dq), _ptr(dk), _ptr(dv),
+                                      _stream(stream)))
+    return dq
 
 
 def dense_backward(q, k, v, o, lse, dout, *, mode=ATTN_DQ_ATOMIC, causal=False, scale=None,
@@ -257,7 +271,9 @@ def dense_backward(q, k, v, o, lse, dout, *, mode=ATTN_DQ_ATOMIC, causal=False, 
     kw = dict(mode=mode, causal=causal, scale=scale, cu_seqlens=cu_seqlens, max_seqlen=max_seqlen,
               error_word=error_word, stream=stream)
     delta = attn_bwd_preprocess(q, k, o, dout, workspace=workspace, **kw)
-    return attn_bwd(q, k, v, dout, lse, delta, workspace=workspace, **kw)
+    dk, dv = attn_bwd(q, k, v, dout, lse, delta, workspace=workspace, **kw)
+    dq = attn_bwd_postprocess(q, k, dk, dv, workspace=workspace, **kw)
+    return dq, dk, dv
 
 
 # ----------------------------------------------------------------------------

@@ -185,16 +185,15 @@ attn_status_t attn_bwd_preprocess(const attn_problem_t* p, attn_dq_mode_t mode, 
 
 attn_status_t attn_bwd(const attn_problem_t* p, attn_dq_mode_t mode, const void* q,
                        const void* k, const void* v, const void* dout, const float* lse,
-                       const float* delta, void* dq, void* dk, void* dv, void* workspace,
+                       const float* delta, void* dk, void* dv, void* workspace,
                        size_t workspace_bytes, attn_stream_t stream) {
   bool empty;
   attn_status_t s = check_problem(p, &empty);
   if (s != ATTN_OK) return s;
   if (mode != ATTN_DQ_ATOMIC && mode != ATTN_DQ_SPLIT) return ATTN_ERR_INVALID_ARG;
-  if (!q || !k || !v || !dout || !lse || !delta || !dq || !dk || !dv)
-    return ATTN_ERR_INVALID_ARG;
+  if (!q || !k || !v || !dout || !lse || !delta || !dk || !dv) return ATTN_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dout) || !aligned16(lse) ||
-      !aligned16(delta) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+      !aligned16(delta) || !aligned16(dk) || !aligned16(dv))
     return ATTN_ERR_ALIGNMENT;
   if (empty) return ATTN_OK;
   const size_t need = attn_bwd_workspace_size(p, mode);
@@ -224,15 +223,37 @@ attn_status_t attn_bwd(const attn_problem_t* p, attn_dq_mode_t mode, const void*
   const int gx = tile_bound(kp.rows_total, kp.num_seqs, 128, kp.cu_seqlens != nullptr);
   cudaError_t e = (D == 64) ? launch_attn_bwd<64>(mq, mk, mv, mdo, a, gx, st)
                             : launch_attn_bwd<128>(mq, mk, mv, mdo, a, gx, st);
-  if (e != cudaSuccess) return ATTN_ERR_CUDA;
-  auto* dqb = static_cast<__nv_bfloat16*>(dq);
-  e = (D == 64) ? launch_dq_finalize<64>(kp, a.dq_acc, a.slab_elems, a.split, a.n_split, dqb,
-                                         a.dk, a.dv, st)
-                : launch_dq_finalize<128>(kp, a.dq_acc, a.slab_elems, a.split, a.n_split, dqb,
-                                          a.dk, a.dv, st);
   return cuda_status(e);
 }
 
+attn_status_t attn_bwd_postprocess(const attn_problem_t* p, attn_dq_mode_t mode,
+                                   const void* workspace, size_t workspace_bytes, void* dq,
+                                   void* dk, void* dv, attn_stream_t stream) {
+  bool empty;
+  attn_status_t s = check_problem(p, &empty);
+  if (s != ATTN_OK) return s;
+  if (mode != ATTN_DQ_ATOMIC && mode != ATTN_DQ_SPLIT) return ATTN_ERR_INVALID_ARG;
+  if (!dq || !dk || !dv) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(dq) || !aligned16(dk) || !aligned16(dv)) return ATTN_ERR_ALIGNMENT;
+  if (empty) return ATTN_OK;
+  const size_t need = attn_bwd_workspace_size(p, mode);
+  if (!workspace || workspace_bytes < need) return ATTN_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return ATTN_ERR_ALIGNMENT;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const Problem kp = to_kernel(p);
+  const int D = p->head_dim;
+  const int split = (mode == ATTN_DQ_SPLIT) ? 1 : 0;
+  const size_t slab = split ? dq_elems(kp, D) : 0;
+  const int n_split = split ? n_kv_tiles(kp) : 0;
+  const float* acc = static_cast<const float*>(workspace);
+  auto* dqb = static_cast<__nv_bfloat16*>(dq);
+  auto* dkb = static_cast<__nv_bfloat16*>(dk);
+  auto* dvb = static_cast<__nv_bfloat16*>(dv);
+  cudaError_t e = (D == 64) ? launch_dq_finalize<64>(kp, acc, slab, split, n_split, dqb, dkb, dvb, st)
+                            : launch_dq_finalize<128>(kp, acc, slab, split, n_split, dqb, dkb, dvb,
+                                                      st);
+  return cuda_status(e);
+}
 
 // ---------------------------------------------------------------------------
 // Sparse

@@ -81,11 +81,14 @@ def test_thd_validation_and_workspace(L):
     assert L.attn_bwd_workspace_size(ctypes.byref(p), 0) == per
     assert L.attn_bwd_workspace_size(ctypes.byref(p), 1) == per * ((3670 + 127) // 128)
     # workspace missing / too small is rejected before any launch
-    args = [ctypes.c_void_p(FAKE)] * 10
-    assert L.attn_bwd(ctypes.byref(p), 0, *args[:9], None, 0, None) == 5
-    assert L.attn_bwd(ctypes.byref(p), 0, *args[:9], ctypes.c_void_p(FAKE), 16, None) == 5
-    assert L.attn_bwd(ctypes.byref(p), 7, *args[:9], ctypes.c_void_p(FAKE), per, None) == 1
+    args = [ctypes.c_void_p(FAKE)] * 8           # q k v dout lse delta dk dv
+    assert L.attn_bwd(ctypes.byref(p), 0, *args, None, 0, None) == 5
+    assert L.attn_bwd(ctypes.byref(p), 0, *args, ctypes.c_void_p(FAKE), 16, None) == 5
+    assert L.attn_bwd(ctypes.byref(p), 7, *args, ctypes.c_void_p(FAKE), per, None) == 1
     assert L.attn_bwd_preprocess(ctypes.byref(p), 0, *args[:3], None, 0, None) == 5
+    assert L.attn_bwd_postprocess(ctypes.byref(p), 0, None, 0, *args[:3], None) == 5
+    assert L.attn_bwd_postprocess(ctypes.byref(p), 1, ctypes.c_void_p(FAKE), per, *args[:3],
+                                  None) == 5
 
 
 def test_dense_workspace_sizes(L):

@@ -140,6 +140,41 @@ attn_status_t attn_bwd_postprocess(const attn_problem_t* p, attn_dq_mode_t mode,
                                    void* dk, void* dv, attn_stream_t stream);
 
 /*
+ * Backward without any caller-provided device memory.  The source pages have no
+ * counterpart: this entry point exists for callers that cannot allocate device
+ * memory at all -- for example a plugin running inside a host framework that
+ * owns every device allocation through its own pool, or a latency-critical loop
+ * where cudaMalloc (which may synchronize the device) is not allowed -- and so
+ * cannot provide the workspace that attn_bwd_preprocess / attn_bwd /
+ * attn_bwd_postprocess need.
+ *
+ * It runs those three stages in ATTN_DQ_ATOMIC mode, with Delta and the fp32 dQ
+ * accumulator kept in one static device array of ATTN_FIXED_SCRATCH_BYTES that
+ * the library owns; every GPU that loads the library holds that array until the
+ * process exits.  It calls no cudaMalloc, cudaFree or other allocating routine.
+ *   - Inputs: q, k, v, o, dout bf16 and lse fp32 (from attn_fwd); outputs dq, dk,
+ *     dv bf16 -- all caller-owned device pointers, layouts as in attn_problem_t.
+ *   - Capacity: rows * heads_q * (head_dim + 1) * 4 bytes (plus 256 bytes of
+ *     alignment) must fit in ATTN_FIXED_SCRATCH_BYTES, with rows = batch * seqlen
+ *     (dense) or capacity (THD); larger problems return ATTN_ERR_UNSUPPORTED and
+ *     enqueue nothing.
+ *   - Set-up: the first call on each device looks up the array's device address
+ *     (with that device current) and caches it, so make that first call before
+ *     any stream capture; later calls only read the cache.  Calls must be made
+ *     with the device that owns `stream` current.
+ *   - Sharing: every call uses the same array and leaves its contents behind; the
+ *     call clears what must start at zero itself.  Calls whose work overlaps on
+ *     the GPU (for example on two streams) race on the array and give wrong
+ *     results; serialize them.
+ */
+#define ATTN_FIXED_SCRATCH_BYTES (16u << 20)
+
+attn_status_t attn_bwd_fixed_scratch(const attn_problem_t* p, const void* q, const void* k,
+                                     const void* v, const void* o, const void* dout,
+                                     const float* lse, void* dq, void* dk, void* dv,
+                                     attn_stream_t stream);
+
+/*
  * Top-k sparse attention over one shared KV head (SparseMLA style).
  * q [tokens, heads, dim_qk] bf16, kv [tokens, dim_qk] bf16 (the key is the whole
  * row; the value is its first dim_v entries), idx int32 [tokens, topk]: token t

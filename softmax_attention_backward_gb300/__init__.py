@@ -23,7 +23,8 @@ __all__ = [
     "ATTN_DQ_ATOMIC", "ATTN_DQ_SPLIT", "AttnError", "lib", "attn_fwd", "attn_bwd_workspace_size",
     "attn_bwd_preprocess", "attn_bwd", "attn_bwd_postprocess", "sparse_attn_fwd", "sparse_attn_bwd_workspace_size",
     "sparse_attn_bwd", "attn_status_string", "attn_version", "dense_backward",
-    "SPARSE_DIM_QK", "SPARSE_DIM_V", "EXPORTED_SYMBOLS",
+    "SPARSE_DIM_QK", "SPARSE_DIM_V", "EXPORTED_SYMBOLS", "attn_bwd_fixed_scratch",
+    "FIXED_SCRATCH_BYTES",
 ]
 
 ATTN_DQ_ATOMIC = 0
@@ -35,8 +36,9 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libattn.so"
 EXPORTED_SYMBOLS = (
     "attn_fwd", "attn_bwd_workspace_size", "attn_bwd_preprocess", "attn_bwd", "attn_bwd_postprocess",
     "sparse_attn_fwd", "sparse_attn_bwd_workspace_size", "sparse_attn_bwd",
-    "attn_status_string", "attn_version",
+    "attn_status_string", "attn_version", "attn_bwd_fixed_scratch",
 )
+FIXED_SCRATCH_BYTES = 16 << 20
 
 
 class AttnError(RuntimeError):
@@ -86,11 +88,12 @@ def lib() -> ctypes.CDLL:
         L.sparse_attn_bwd_workspace_size.argtypes = [SP]
         L.sparse_attn_bwd_workspace_size.restype = sz
         L.sparse_attn_bwd.argtypes = [SP, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+        L.attn_bwd_fixed_scratch.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
         L.attn_status_string.argtypes = [i32]
         L.attn_status_string.restype = ctypes.c_char_p
         L.attn_version.argtypes = []
         for name in ("attn_fwd", "attn_bwd_preprocess", "attn_bwd", "attn_bwd_postprocess",
-                     "sparse_attn_fwd", "sparse_attn_bwd"):
+                     "sparse_attn_fwd", "sparse_attn_bwd", "attn_bwd_fixed_scratch"):
             getattr(L, name).restype = i32
         _LIB = L
     return _LIB
@@ -273,6 +276,36 @@ def dense_backward(q, k, v, o, lse, dout, *, mode=ATTN_DQ_ATOMIC, causal=False, 
     delta = attn_bwd_preprocess(q, k, o, dout, workspace=workspace, **kw)
     dk, dv = attn_bwd(q, k, v, dout, lse, delta, workspace=workspace, **kw)
     dq = attn_bwd_postprocess(q, k, dk, dv, workspace=workspace, **kw)
+    return dq, dk, dv
+
+
+def attn_bwd_fixed_scratch(q, k, v, o, dout, lse, *, causal=False, scale=None, cu_seqlens=None,
+                           max_seqlen=None, dq=None, dk=None, dv=None, error_word=None,
+                           stream=None):
+    """Backward for callers that cannot allocate device memory: no workspace
+    argument; Delta and the fp32 dQ accumulator live in a 16 MiB array the
+    library owns on each GPU.  Returns (dq, dk, dv).  Problems whose scratch
+    need exceeds the array raise ValueError; calls that overlap on the GPU race
+    on the shared array."""
+    _nondeterministic("attn_bwd_fixed_scratch")
+    dev = q.device
+    for n, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dout", dout)):
+        _need(t, n, torch.bfloat16, dev)
+    _need(lse, "lse", torch.float32, dev)
+    rows = q.shape[0] if cu_seqlens is not None else q.shape[0] * q.shape[1]
+    hq, d = q.shape[-2], q.shape[-1]
+    need = (rows * hq * d * 4 + 255) // 256 * 256 + rows * hq * 4
+    if need > FIXED_SCRATCH_BYTES:
+        raise ValueError(f"attn_bwd_fixed_scratch: problem needs {need} bytes of scratch, "
+                         f"more than the fixed {FIXED_SCRATCH_BYTES}")
+    dq = dq if dq is not None else torch.empty_like(q)
+    dk = dk if dk is not None else torch.empty_like(k)
+    dv = dv if dv is not None else torch.empty_like(v)
+    p = _problem(q, k, causal, scale, cu_seqlens, max_seqlen, error_word)
+    _check("attn_bwd_fixed_scratch",
+           lib().attn_bwd_fixed_scratch(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(o),
+                                        _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv),
+                                        _stream(stream)))
     return dq, dk, dv
 
 

@@ -167,22 +167,37 @@ def barrier(world):
 # ----------------------------------------------------------------------------
 # oracle (CPU) leg
 # ----------------------------------------------------------------------------
-def oracle_unit_rate(w, x, budget_s, units=None):
-    """Times the fp64 oracle over (batch, kv-head) units until `budget_s` is spent.
+def oracle_units(w):
+    """Independent units of a workload for the oracle: (batch, kv-head) groups of
+    a dense problem, sequences of a THD problem; with their FLOPs (fwd+bwd)."""
+    if w.kind == "thd":
+        per = [3.5 * 4.0 * w.heads_q * w.head_dim * L * L * (0.5 if w.causal else 1.0)
+               for L in w.lengths]
+        return [(n, per[n]) for n in range(len(w.lengths))]
+    f_fwd, f_bwd = dense_flops(w)
+    per = (f_fwd + f_bwd) / (w.batch * w.heads_kv)
+    return [((b, g), per) for b in range(w.batch) for g in range(w.heads_kv)]
+
+
+def oracle_unit_rate(w, x, budget_s):
+    """Times the fp64 oracle over independent units until `budget_s` is spent.
     Returns (TFLOP/s, units done, seconds)."""
     import oracle
-    f_fwd, f_bwd = dense_flops(w)
-    per_unit = (f_fwd + f_bwd) / (w.batch * w.heads_kv)
-    all_units = units or [(b, g) for b in range(w.batch) for g in range(w.heads_kv)]
-    done, t0 = 0, time.perf_counter()
+    units = oracle_units(w)
+    done, flops, t0 = 0, 0.0, time.perf_counter()
     while True:
-        b, g = all_units[done % len(all_units)]
-        oracle.dense_backward(x["q"], x["k"], x["v"], x["do"], w.scale, w.causal, kv_heads=[(b, g)])
+        u, f = units[done % len(units)]
+        if w.kind == "thd":
+            oracle.thd_backward(x["q"], x["k"], x["v"], x["do"], x["cu_seqlens"], w.scale, w.causal,
+                                seqs=[u])
+        else:
+            oracle.dense_backward(x["q"], x["k"], x["v"], x["do"], w.scale, w.causal, kv_heads=[u])
         done += 1
+        flops += f
         el = time.perf_counter() - t0
         if el >= budget_s:
             break
-    return per_unit * done / el / 1e12, done, el
+    return flops / el / 1e12, done, el
 
 
 def run_reference(args, w, world, rank):
@@ -193,16 +208,15 @@ def run_reference(args, w, world, rank):
     cores = torch.get_num_threads()
     for _ in range(args.warmup):
         oracle_unit_rate(w, x, 0.0)
-    times, units = [], 0
-    f_fwd, f_bwd = dense_flops(w)
-    per_unit = (f_fwd + f_bwd) / (w.batch * w.heads_kv)
+    times, units, flops = [], 0, 0.0
     for _ in range(args.steps):
-        _, n, el = oracle_unit_rate(w, x, 0.0)
+        rate, n, el = oracle_unit_rate(w, x, 0.0)
         times.append(el)
         units += n
+        flops += rate * el * 1e12
     total = sum(times)
-    value = per_unit * units / total / 1e12
-    sample = f"{units} (batch, kv-head) units of {w.name}, one per step, fp64 oracle"
+    value = flops / total / 1e12
+    sample = f"{units} independent units of {w.name}, one per step, fp64 oracle"
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
@@ -218,6 +232,7 @@ def run_reference(args, w, world, rank):
 
 def config_of(w, mode, world):
     c = {"workload": w.name, "batch": w.batch, "seqlen": w.seqlen, "heads_q": w.heads_q,
+         **({"lengths": w.lengths, "capacity": w.capacity} if w.kind == "thd" else {}),
          "heads_kv": w.heads_kv, "head_dim": w.head_dim, "causal": w.causal, "dq_mode": mode,
          "l2": "flushed between timed steps (256 MiB write)",
          "parallelism": "replicas" if world == 1 else f"replicas x{world}"}
@@ -235,13 +250,19 @@ def run_ours(args, w, world, rank, local):
     x = W.make_inputs(w)
     q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "do"))
     o = torch.empty_like(q)
-    lse = torch.empty(w.batch, w.heads_q, w.seqlen, dtype=torch.float32, device=dev)
+    if w.kind == "thd":
+        lse = torch.empty(w.heads_q, w.capacity, dtype=torch.float32, device=dev)
+    else:
+        lse = torch.empty(w.batch, w.heads_q, w.seqlen, dtype=torch.float32, device=dev)
     delta = torch.empty_like(lse)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     kw = dict(causal=w.causal, scale=w.scale)
+    if w.kind == "thd":
+        kw.update(cu_seqlens=x["cu_seqlens"].to(dev), max_seqlen=max(w.lengths))
     ws = {}
-    for mode in (A.ATTN_DQ_ATOMIC, A.ATTN_DQ_SPLIT):
+    modes = (A.ATTN_DQ_ATOMIC,) if args.no_split else (A.ATTN_DQ_ATOMIC, A.ATTN_DQ_SPLIT)
+    for mode in modes:
         n = A.attn_bwd_workspace_size(q, k, mode=mode, **kw)
         ws[mode] = torch.empty(n, dtype=torch.uint8, device=dev)
     f_fwd, f_bwd = dense_flops(w)
@@ -285,20 +306,20 @@ def run_ours(args, w, world, rank, local):
 
     # warm-up (both modes), then the timed atomic-mode steps with clocks sampled
     for _ in range(args.warmup):
-        step(A.ATTN_DQ_ATOMIC)
-        step(A.ATTN_DQ_SPLIT)
+        for mode in modes:
+            step(mode)
     torch.cuda.synchronize()
     sampler = ClockSampler(f"GPU-{torch.cuda.get_device_properties(dev).uuid}") if rank == 0 else None
     t_atomic = timed(A.ATTN_DQ_ATOMIC, args.steps, sampler)
     clocks = sampler.stop() if sampler else None
-    t_split = timed(A.ATTN_DQ_SPLIT, args.steps)
+    t_split = None if args.no_split else timed(A.ATTN_DQ_SPLIT, args.steps)
 
     ms = reduce_max(t_atomic["total"], world)
     ms_main = reduce_max(t_atomic["bwd_main"], world)
     ms_fwd = reduce_max(t_atomic["fwd"], world)
     ms_bwd = reduce_max(t_atomic["bwd"], world)
-    ms_split = reduce_max(t_split["total"], world)
-    ms_split_bwd = reduce_max(t_split["bwd"], world)
+    ms_split = reduce_max(t_split["total"], world) if t_split else None
+    ms_split_bwd = reduce_max(t_split["bwd"], world) if t_split else None
 
     # end to end through the public API: pinned host inputs -> device -> results -> host
     hq, hk, hv, hdo = (x[n].pin_memory() for n in ("q", "k", "v", "do"))
@@ -348,8 +369,9 @@ def run_ours(args, w, world, rank, local):
         "config": config_of(w, "atomic", world),
         "pct_of_peak": 100.0 * tflops(f_fwd + f_bwd, ms) / peak,
         "fwd_tflops": tflops(f_fwd, ms_fwd), "bwd_tflops": tflops(f_bwd, ms_bwd),
-        "split": {"fwd_bwd_tflops": tflops(f_fwd + f_bwd, ms_split),
-                  "bwd_tflops": tflops(f_bwd, ms_split_bwd), "ms_per_step": ms_split},
+        "split": None if ms_split is None else {
+            "fwd_bwd_tflops": tflops(f_fwd + f_bwd, ms_split),
+            "bwd_tflops": tflops(f_bwd, ms_split_bwd), "ms_per_step": ms_split},
         "roofline": {"kernel": "attn_bwd_kernel", "bound": "tensor", "achieved": achieved,
                      "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
                      "peak_kind": f"{pk_kind} bf16 burst",
@@ -358,7 +380,7 @@ def run_ours(args, w, world, rank, local):
         "clocks": clocks,
         "e2e": {"value": world * tflops(f_fwd + f_bwd, ms_e2e), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e},
-        "gpu_launches": 4 * args.steps,
+        "gpu_launches": (5 if w.kind == "thd" else 4) * args.steps,
         **extra,
     }
     print(json.dumps(line), flush=True)
@@ -420,7 +442,7 @@ def cpu_baseline(w, seconds):
     x = W.make_inputs(w)
     rate, units, el = oracle_unit_rate(w, x, seconds)
     return {"value": rate, "unit": "TFLOP/s", "cores": torch.get_num_threads(), "kind": "oracle",
-            "sample": f"{units} (batch, kv-head) units of {w.name} (fwd+bwd, fp64) in {el:.1f} s"}
+            "sample": f"{units} independent units of {w.name} (fwd+bwd, fp64) in {el:.1f} s"}
 
 
 def main():
@@ -432,13 +454,14 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-sparse", action="store_true")
+    ap.add_argument("--no-split", action="store_true", help="time only the atomic dQ mode")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     world, rank, local = dist_setup()
     w = W.get_workload(args.workload)
-    if w.kind != "dense":
-        raise SystemExit("bench.py times the dense workloads; use the tests for the others")
+    if w.kind == "sparse":
+        raise SystemExit("the sparse workload is timed inside every default run (key 'sparse')")
     if args.impl == "reference":
         run_reference(args, w, world, rank)
     else:

@@ -7,16 +7,20 @@
 // for the whole CTA and are stored once (the group reduction of the #940 GQA
 // backward, where dK is indexed by head // groups, happens on chip, without
 // atomics).  Per query tile i of head h (KV rows j, query rows q):
-//   S^T  = K Q_i^T            (TMEM)   P^T  = exp2(S^T * c - LSE_q * log2 e)
-//   dP^T = V dO_i^T           (TMEM)   dS^T = P^T o (dP^T - Delta_q)
-//   dV  += P^T dO_i           (TMEM)   dK  += dS^T Q_i           (TMEM)
+//   S^T  = K Q_i^T   (TMEM)     P^T  = exp2(S^T * c - LSE_q * log2 e)
+//   dP^T = V dO_i^T  (TMEM)     dS^T = P^T o (dP^T - Delta_q)
+//   dV  += P^T dO_i             dK  += dS^T Q_i
+// with P^T and dS^T written back into TMEM as packed bf16 over the S^T / dP^T
+// columns they came from and used as the TMEM A operand of the dV / dK MMAs, and
 //   dQ_i  = dS K  (D = 64, 128-row query tiles)  or
-//   dQ_i^T = K^T dS^T (D = 128, 64-row query tiles), streamed out of TMEM and
-//   either added with fp32 atomics into one accumulator (ATOMIC) or stored into
-//   the partial slab of this KV tile (SPLIT, summed in order later).
-// Roles: warp 8 TMA, warp 9 MMA issue, warps 0..3 P/dS (one KV row per
-// thread), warps 4..7 dQ drain.  The scale factor of dK is applied in the
-// epilogue and that of dQ in the finalize pass.
+//   dQ_i^T = K^T dS^T (D = 128, 64-row query tiles) from a bf16 dS tile in
+// shared memory, streamed out of TMEM through a shared-memory tile and either
+// added into one fp32 accumulator with a bulk reduce-add (ATOMIC) or
+// bulk-stored into the partial slab of this KV tile (SPLIT, summed in order
+// later).  The accumulator and slabs are head-major, [batch, head, row, dim],
+// so a query tile of one head is one contiguous block.
+// The scale factor of dK is applied in the epilogue and that of dQ in the
+// postprocess pass.
 #include <cuda_runtime.h>
 
 #include "launch.h"
@@ -27,36 +31,38 @@ template <int D>
 struct BwdCfg {
   static constexpr int BN = 128;                      // KV rows per CTA
   static constexpr int BM = (D == 64) ? 128 : 64;     // query rows per step
+  static constexpr int HALF = BM / 2;                 // query columns per P/dS thread
   static constexpr int KV_BYTES = BN * D * 2;
   static constexpr int QT_BYTES = BM * D * 2;
-  static constexpr int PT_BYTES = BN * BM * 2;
-  static constexpr int NST = 2;                       // Q/dO stages
-  static constexpr int SMEM = 2 * KV_BYTES + 2 * NST * QT_BYTES + 2 * PT_BYTES + 1024;
-  static constexpr int THREADS = 320;
+  static constexpr int DS_BYTES = BN * BM * 2;        // bf16 dS tile (for dQ)
+  static constexpr int DQ_BYTES = BM * D * 4;         // fp32 dQ staging tile
+  static constexpr int NST = 3;                       // Q/dO stages
+  static constexpr int SMEM = 2 * KV_BYTES + 2 * NST * QT_BYTES + DS_BYTES + DQ_BYTES + 1024;
+  static constexpr int THREADS = 512;
   static constexpr uint32_t TMEM_COLS = 512;
-  static constexpr uint32_t COL_S = 0;
-  static constexpr uint32_t COL_DP = BM;
+  static constexpr uint32_t COL_S = 0;                // S^T, then P^T (packed) in place
+  static constexpr uint32_t COL_DP = BM;              // dP^T, then dS^T (packed) in place
   static constexpr uint32_t COL_DV = 2 * BM;
   static constexpr uint32_t COL_DK = 2 * BM + D;
   static constexpr uint32_t COL_DQ = 2 * BM + 2 * D;  // two 64-column buffers
+  // TMEM column (relative to COL_S / COL_DP) of the packed bf16 operand for the
+  // 16 query columns of K-step kk: warpgroup w = 16 kk / HALF stores its HALF
+  // columns as HALF/2 packed columns at the start of its own HALF-column range.
+  __host__ __device__ static constexpr uint32_t packed_col(int kk) { return 8 * kk + (16 * kk / HALF) * (HALF / 2); }
 };
 
-__device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
-  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b),
-               "f"(c), "f"(d)
-               : "memory");
-}
-__device__ __forceinline__ void red_add(float* addr, float a) {
-  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(addr), "f"(a) : "memory");
-}
-
+// Warp roles (512 threads): 0..7 P/dS (two warpgroups, each owns half of the
+// query columns of every KV row), 8..11 dQ drain, 12 TMA, 13..15 MMA issuers
+// (S^T and dP^T; dV and dK; dQ).  One issuing thread needs ~100 cycles per
+// tcgen05.mma, so the five GEMMs of a step are spread over three issuers that
+// run independently, synchronized only through the data they exchange.
 template <int D>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(512, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                     const BwdArgs a) {
   using C = BwdCfg<D>;
-  constexpr int BM = C::BM, BN = C::BN;
+  constexpr int BM = C::BM, BN = C::BN, HALF = C::HALF;
   constexpr int PANELS = D / 64;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -65,12 +71,12 @@ __global__ void __launch_bounds__(320, 1)
   uint8_t* sV = sK + C::KV_BYTES;
   uint8_t* sQ = sV + C::KV_BYTES;                 // NST stages
   uint8_t* sdO = sQ + C::NST * C::QT_BYTES;       // NST stages
-  uint8_t* sPt = sdO + C::NST * C::QT_BYTES;
-  uint8_t* sdS = sPt + C::PT_BYTES;
+  uint8_t* sdS = sdO + C::NST * C::QT_BYTES;
+  float* sDQ = reinterpret_cast<float*>(sdS + C::DS_BYTES);
 
   __shared__ uint64_t bar_kv, bar_qfull[C::NST], bar_qempty[C::NST];
-  __shared__ uint64_t bar_s, bar_dp, bar_p, bar_ds, bar_pt_empty, bar_ds_empty, bar_done;
-  __shared__ uint64_t bar_dq_full[2], bar_dq_empty[2];
+  __shared__ uint64_t bar_s, bar_dp, bar_p, bar_ds, bar_pt_done, bar_dst_done, bar_dss_free;
+  __shared__ uint64_t bar_done, bar_dq_full[2], bar_dq_empty[2];
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_flag;
   __shared__ float s_lse[2][BM], s_delta[2][BM];
@@ -96,14 +102,15 @@ __global__ void __launch_bounds__(320, 1)
     mbar_init(&bar_kv, 1);
     for (int s = 0; s < C::NST; ++s) {
       mbar_init(&bar_qfull[s], 1);
-      mbar_init(&bar_qempty[s], 1);
+      mbar_init(&bar_qempty[s], 2);     // S/dP issuer and dV/dK issuer
     }
     mbar_init(&bar_s, 1);
     mbar_init(&bar_dp, 1);
-    mbar_init(&bar_p, 128);
-    mbar_init(&bar_ds, 128);
-    mbar_init(&bar_pt_empty, 1);
-    mbar_init(&bar_ds_empty, 1);
+    mbar_init(&bar_p, 256);
+    mbar_init(&bar_ds, 256);
+    mbar_init(&bar_pt_done, 1);
+    mbar_init(&bar_dst_done, 1);
+    mbar_init(&bar_dss_free, 1);
     mbar_init(&bar_done, 1);
     for (int b = 0; b < 2; ++b) {
       mbar_init(&bar_dq_full[b], 1);
@@ -111,13 +118,13 @@ __global__ void __launch_bounds__(320, 1)
     }
     fence_mbar_init();
   }
-  if (warp == 9) tmem_alloc(&tmem_base_sh, C::TMEM_COLS);
+  if (warp == 13) tmem_alloc(&tmem_base_sh, C::TMEM_COLS);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
 
-  if (warp == 8) {
+  if (warp == 12) {
     // ---------------- TMA producer ----------------
     if (lane_id() == 0) {
       tma_prefetch_desc(&tmQ);
@@ -143,204 +150,230 @@ __global__ void __launch_bounds__(320, 1)
         }
       }
     }
-  } else if (warp == 9) {
-    // ---------------- MMA issuer ----------------
+  } else if (warp == 13) {
+    // ---------------- issuer 1: S^T = K Q_i^T, dP^T = V dO_i^T ----------------
     if (lane_id() == 0) {
-      const uint32_t idSD = idesc_bf16(128, BM, false, false);   // S^T, dP^T
-      const uint32_t idKV = idesc_bf16(128, D, false, true);     // dV, dK
-      const uint32_t idQ = idesc_bf16(128, 64, true, true);      // dQ or dQ^T
-      const uint32_t aK = smem_u32(sK), aV = smem_u32(sV), aQ = smem_u32(sQ),
-                     adO = smem_u32(sdO), aPt = smem_u32(sPt), adS = smem_u32(sdS);
-      auto issue_s = [&](int it) {
-        const uint32_t q = aQ + (it % C::NST) * C::QT_BYTES;
-#pragma unroll
-        for (int k = 0; k < D / 16; ++k)
-          umma_ss(tmem + C::COL_S, desc_kmajor(aK, BN, k), desc_kmajor(q, BM, k), idSD, k > 0);
-        umma_commit(&bar_s);
-      };
-      auto issue_dp = [&](int it) {
-        const uint32_t o = adO + (it % C::NST) * C::QT_BYTES;
-#pragma unroll
-        for (int k = 0; k < D / 16; ++k)
-          umma_ss(tmem + C::COL_DP, desc_kmajor(aV, BN, k), desc_kmajor(o, BM, k), idSD, k > 0);
-        umma_commit(&bar_dp);
-      };
-      bool ok = mbar_wait(&bar_kv, 0, ac) && mbar_wait(&bar_qfull[0], 0, ac);
-      if (ok) {
-        tc_fence_after();
-        issue_s(0);
-        issue_dp(0);
-      }
+      const uint32_t idSD = idesc_bf16(128, BM, false, false);
+      const uint64_t dK_k = desc_kmajor_base(smem_u32(sK));
+      const uint64_t dV_k = desc_kmajor_base(smem_u32(sV));
+      const uint64_t dQ_k0 = desc_kmajor_base(smem_u32(sQ));
+      const uint64_t ddO_k0 = desc_kmajor_base(smem_u32(sdO));
+      bool ok = mbar_wait(&bar_kv, 0, ac);
       for (int it = 0; ok && it < n_it; ++it) {
         const int st = it % C::NST;
-        const uint32_t q = aQ + st * C::QT_BYTES, o = adO + st * C::QT_BYTES;
-        // dV += P^T dO_i
+        if (!mbar_wait(&bar_qfull[st], (it / C::NST) & 1, ac)) break;
+        // S^T region is free once dV(it-1) has consumed P^T(it-1) stored there
+        if (it > 0 && !mbar_wait(&bar_pt_done, (it - 1) & 1, ac)) break;
+        tc_fence_after();
+        const uint64_t qd = desc_advance(dQ_k0, st * C::QT_BYTES);
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k)
+          umma_ss(tmem + C::COL_S, desc_advance(dK_k, kmajor_step_bytes(BN, k)),
+                  desc_advance(qd, kmajor_step_bytes(BM, k)), idSD, k > 0);
+        umma_commit(&bar_s);
+        // dP^T region is free once dK(it-1) has consumed dS^T(it-1)
+        if (it > 0 && !mbar_wait(&bar_dst_done, (it - 1) & 1, ac)) break;
+        tc_fence_after();
+        const uint64_t od = desc_advance(ddO_k0, st * C::QT_BYTES);
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k)
+          umma_ss(tmem + C::COL_DP, desc_advance(dV_k, kmajor_step_bytes(BN, k)),
+                  desc_advance(od, kmajor_step_bytes(BM, k)), idSD, k > 0);
+        umma_commit(&bar_dp);
+        umma_commit(&bar_qempty[st]);
+      }
+    }
+  } else if (warp == 14) {
+    // ---------------- issuer 2: dV += P^T dO_i, dK += dS^T Q_i (A from TMEM) ----
+    if (lane_id() == 0) {
+      const uint32_t idKV = idesc_bf16(128, D, false, true);
+      const uint64_t dQ_mn0 = desc_mnmajor_base(smem_u32(sQ), BM);
+      const uint64_t ddO_mn0 = desc_mnmajor_base(smem_u32(sdO), BM);
+      bool ok = true;
+      for (int it = 0; ok && it < n_it; ++it) {
+        const int st = it % C::NST;
+        if (!mbar_wait(&bar_qfull[st], (it / C::NST) & 1, ac)) break;
         if (!mbar_wait(&bar_p, it & 1, ac)) break;
         tc_fence_after();
+        const uint64_t omn = desc_advance(ddO_mn0, st * C::QT_BYTES);
 #pragma unroll
         for (int k = 0; k < BM / 16; ++k)
-          umma_ss(tmem + C::COL_DV, desc_kmajor(aPt, BN, k), desc_mnmajor(o, BM, k), idKV,
-                  (it > 0 || k > 0) ? 1u : 0u);
-        umma_commit(&bar_pt_empty);
-        // next S^T as soon as its inputs are in
-        if (it + 1 < n_it) {
-          if (!mbar_wait(&bar_qfull[(it + 1) % C::NST], ((it + 1) / C::NST) & 1, ac)) break;
-          tc_fence_after();
-          issue_s(it + 1);
-        }
-        // dK += dS^T Q_i ; dQ
+          umma_ts(tmem + C::COL_DV, tmem + C::COL_S + C::packed_col(k),
+                  desc_advance(omn, mnmajor_step_bytes(k)), idKV, (it > 0 || k > 0) ? 1u : 0u);
+        umma_commit(&bar_pt_done);
         if (!mbar_wait(&bar_ds, it & 1, ac)) break;
         tc_fence_after();
+        const uint64_t qmn = desc_advance(dQ_mn0, st * C::QT_BYTES);
 #pragma unroll
         for (int k = 0; k < BM / 16; ++k)
-          umma_ss(tmem + C::COL_DK, desc_kmajor(adS, BN, k), desc_mnmajor(q, BM, k), idKV,
-                  (it > 0 || k > 0) ? 1u : 0u);
-        const int qb = it & 1, qu = it >> 1;
-        if (!mbar_wait(&bar_dq_empty[qb], (qu & 1) ^ 1, ac)) break;
-        tc_fence_after();
-#pragma unroll
-        for (int k = 0; k < BN / 16; ++k) {
-          if (D == 64)   // dQ[q, d] = dS[q, kv] K[kv, d]
-            umma_ss(tmem + C::COL_DQ + 64 * qb, desc_mnmajor(adS, BN, k),
-                    desc_mnmajor(aK, BN, k), idQ, k > 0);
-          else           // dQ^T[d, q] = K^T[d, kv] dS^T[kv, q]
-            umma_ss(tmem + C::COL_DQ + 64 * qb, desc_mnmajor(aK, BN, k),
-                    desc_mnmajor(adS, BN, k), idQ, k > 0);
-        }
-        umma_commit(&bar_dq_full[qb]);
-        umma_commit(&bar_ds_empty);
+          umma_ts(tmem + C::COL_DK, tmem + C::COL_DP + C::packed_col(k),
+                  desc_advance(qmn, mnmajor_step_bytes(k)), idKV, (it > 0 || k > 0) ? 1u : 0u);
+        umma_commit(&bar_dst_done);
         umma_commit(&bar_qempty[st]);
-        if (it + 1 < n_it) issue_dp(it + 1);
       }
       umma_commit(&bar_done);
     }
-  } else if (warp < 4) {
-    // ---------------- P / dS warpgroup (one KV row per thread) ----------------
-    const int r = threadIdx.x;                         // KV row in tile == TMEM lane
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+  } else if (warp == 15) {
+    // ---------------- issuer 3: dQ (both operands in shared memory) ----------
+    if (lane_id() == 0) {
+      const uint32_t idQ = idesc_bf16(128, 64, true, true);
+      const uint64_t dK_mn = desc_mnmajor_base(smem_u32(sK), BN);
+      const uint64_t ddS_mn = desc_mnmajor_base(smem_u32(sdS), BN);
+      bool ok = mbar_wait(&bar_kv, 0, ac);
+      for (int it = 0; ok && it < n_it; ++it) {
+        if (!mbar_wait(&bar_ds, it & 1, ac)) break;
+        const int qb = it & 1, qu = it >> 1;
+        if (!mbar_wait(&bar_dq_empty[qb], (qu & 1) ^ 1, ac)) break;
+        tc_fence_after();
+        const uint32_t tDQ = tmem + C::COL_DQ + 64 * qb;
+#pragma unroll
+        for (int k = 0; k < BN / 16; ++k) {
+          if (D == 64)   // dQ[q, d] = dS[q, kv] K[kv, d]
+            umma_ss(tDQ, desc_advance(ddS_mn, mnmajor_step_bytes(k)),
+                    desc_advance(dK_mn, mnmajor_step_bytes(k)), idQ, k > 0);
+          else           // dQ^T[d, q] = K^T[d, kv] dS^T[kv, q]
+            umma_ss(tDQ, desc_advance(dK_mn, mnmajor_step_bytes(k)),
+                    desc_advance(ddS_mn, mnmajor_step_bytes(k)), idQ, k > 0);
+        }
+        umma_commit(&bar_dq_full[qb]);
+        umma_commit(&bar_dss_free);
+      }
+    }
+  } else if (warp < 8) {
+    // ---------------- P / dS warpgroups ----------------
+    const int tid = threadIdx.x;                       // 0..255
+    const int wg = warp >> 2;                          // column half
+    const int r = (warp & 3) * 32 + lane_id();         // KV row in tile == TMEM lane
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const int c0 = wg * HALF;
     const int kv = kv0 + r;                            // KV row inside the sequence
     const bool kv_ok = kv < seq.len;
     const float sl2 = a.scale_log2;
-    bool ok = true;
-    for (int it = 0; it < n_it; ++it) {
+    // LSE (log2 domain) or Delta of one query column, fetched one step ahead
+    auto fetch = [&](int it) -> float {
+      if (tid >= 2 * BM) return 0.f;
+      const bool is_lse = tid < BM;
+      const int c = is_lse ? tid : tid - BM;
       const int h = hk * G + it / n_i;
+      const int q = (i_start + it % n_i) * BM + c;
+      if (q >= seq.len) return is_lse ? INFINITY : 0.f;
+      size_t li;
+      if (p.cu_seqlens)
+        li = static_cast<size_t>(h) * p.rows_total + seq.row0 + q;
+      else
+        li = (static_cast<size_t>(seq.b) * p.heads_q + h) * p.rows_total + q;
+      return is_lse ? __ldg(a.lse + li) * kLog2e : __ldg(a.delta + li);
+    };
+    float pf = (n_it > 0) ? fetch(0) : 0.f;
+    bool ok = true;
+    const uint32_t tSme = tmem + lane_base + C::COL_S + c0;    // this thread's S / P columns
+    const uint32_t tDPme = tmem + lane_base + C::COL_DP + c0;  // this thread's dP / dS columns
+    for (int it = 0; it < n_it; ++it) {
       const int q0 = (i_start + it % n_i) * BM;
       const int buf = it & 1;
-      if (r < BM) {
-        const int q = q0 + r;
-        float l = INFINITY, dl = 0.f;
-        if (q < seq.len) {
-          size_t li;
-          if (p.cu_seqlens)
-            li = static_cast<size_t>(h) * p.rows_total + seq.row0 + q;
-          else
-            li = (static_cast<size_t>(seq.b) * p.heads_q + h) * p.rows_total + q;
-          l = __ldg(a.lse + li) * kLog2e;
-          dl = __ldg(a.delta + li);
-        }
-        s_lse[buf][r] = l;
-        s_delta[buf][r] = dl;
-      }
-      named_bar_sync(1, 128);
-      // ---- P^T row ----
+      if (tid < BM) s_lse[buf][tid] = pf;
+      else if (tid < 2 * BM) s_delta[buf][tid - BM] = pf;
+      if (it + 1 < n_it) pf = fetch(it + 1);
+      named_bar_sync(1, 256);
+      // ---- P^T (KV row r, query columns c0 .. c0 + HALF) ----
       if (!mbar_wait(&bar_s, it & 1, ac)) { ok = false; break; }
       tc_fence_after();
-      float pv[BM];
+      float pv[HALF];
+      {
+        uint32_t u[HALF];
 #pragma unroll
-      for (int c = 0; c < BM; c += 32) {
-        uint32_t u[32];
-        tmem_ld32(tmem + lane_base + C::COL_S + c, u);
+        for (int c = 0; c < HALF; c += 32) tmem_ld32_nowait(tSme + c, u + c);
         tmem_wait_ld();
 #pragma unroll
-        for (int i = 0; i < 32; ++i) pv[c + i] = __uint_as_float(u[i]);
+        for (int c = 0; c < HALF; ++c) pv[c] = __uint_as_float(u[c]);
       }
       const bool diag = p.causal && (q0 < kv0 + BN);
 #pragma unroll
-      for (int c = 0; c < BM; ++c) {
-        float e = ex2(fmaf(pv[c], sl2, -s_lse[buf][c]));
-        if (!kv_ok || (diag && q0 + c < kv)) e = 0.f;
+      for (int c = 0; c < HALF; ++c) {
+        float e = ex2(fmaf(pv[c], sl2, -s_lse[buf][c0 + c]));
+        if (!kv_ok || (diag && q0 + c0 + c < kv)) e = 0.f;
         pv[c] = e;
       }
-      if (it > 0 && !mbar_wait(&bar_pt_empty, (it - 1) & 1, ac)) { ok = false; break; }
+      {
+        uint32_t pk[HALF / 2];
 #pragma unroll
-      for (int ch = 0; ch < BM / 8; ++ch) {
-        const uint32_t off = (ch >> 3) * BN * 128 + r * 128 + (((ch & 7) ^ (r & 7)) << 4);
-        uint4 v = make_uint4(pack_bf16(pv[ch * 8 + 0], pv[ch * 8 + 1]),
-                             pack_bf16(pv[ch * 8 + 2], pv[ch * 8 + 3]),
-                             pack_bf16(pv[ch * 8 + 4], pv[ch * 8 + 5]),
-                             pack_bf16(pv[ch * 8 + 6], pv[ch * 8 + 7]));
-        *reinterpret_cast<uint4*>(sPt + off) = v;
+        for (int c = 0; c < HALF / 2; ++c) pk[c] = pack_bf16(pv[2 * c], pv[2 * c + 1]);
+        if constexpr (HALF / 2 == 32) tmem_st32(tSme, pk);
+        else tmem_st16(tSme, *reinterpret_cast<uint32_t(*)[16]>(pk));
       }
-      fence_proxy_async_smem();
+      tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&bar_p);
-      // ---- dS^T row ----
+      // ---- dS^T = P^T o (dP^T - Delta) ----
       if (!mbar_wait(&bar_dp, it & 1, ac)) { ok = false; break; }
       tc_fence_after();
+      {
+        uint32_t u[HALF];
 #pragma unroll
-      for (int c = 0; c < BM; c += 32) {
-        uint32_t u[32];
-        tmem_ld32(tmem + lane_base + C::COL_DP + c, u);
+        for (int c = 0; c < HALF; c += 32) tmem_ld32_nowait(tDPme + c, u + c);
         tmem_wait_ld();
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-          pv[c + i] = pv[c + i] * (__uint_as_float(u[i]) - s_delta[buf][c + i]);
+        for (int c = 0; c < HALF; ++c)
+          pv[c] = pv[c] * (__uint_as_float(u[c]) - s_delta[buf][c0 + c]);
       }
-      if (it > 0 && !mbar_wait(&bar_ds_empty, (it - 1) & 1, ac)) { ok = false; break; }
+      uint32_t pk[HALF / 2];
 #pragma unroll
-      for (int ch = 0; ch < BM / 8; ++ch) {
+      for (int c = 0; c < HALF / 2; ++c) pk[c] = pack_bf16(pv[2 * c], pv[2 * c + 1]);
+      if constexpr (HALF / 2 == 32) tmem_st32(tDPme, pk);
+      else tmem_st16(tDPme, *reinterpret_cast<uint32_t(*)[16]>(pk));
+      // dS (bf16) also to shared memory for the dQ GEMM
+      if (it > 0 && !mbar_wait(&bar_dss_free, (it - 1) & 1, ac)) { ok = false; break; }
+#pragma unroll
+      for (int i = 0; i < HALF / 8; ++i) {
+        const int ch = c0 / 8 + i;
         const uint32_t off = (ch >> 3) * BN * 128 + r * 128 + (((ch & 7) ^ (r & 7)) << 4);
-        uint4 v = make_uint4(pack_bf16(pv[ch * 8 + 0], pv[ch * 8 + 1]),
-                             pack_bf16(pv[ch * 8 + 2], pv[ch * 8 + 3]),
-                             pack_bf16(pv[ch * 8 + 4], pv[ch * 8 + 5]),
-                             pack_bf16(pv[ch * 8 + 6], pv[ch * 8 + 7]));
-        *reinterpret_cast<uint4*>(sdS + off) = v;
+        *reinterpret_cast<uint4*>(sdS + off) =
+            make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
       }
+      tmem_wait_st();
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(&bar_ds);
     }
-    // ---- epilogue: dK (x scale) and dV rows ----
+    // ---- epilogue: dK (x scale) and dV, this thread's half of the head dims ----
     if (ok && mbar_wait(&bar_done, 0, ac)) {
       tc_fence_after();
+      constexpr int DH = D / 2;
+      const int d0 = wg * DH;
       const size_t grow = static_cast<size_t>(seq.b) * p.rows_total + seq.row0 + kv;
-      __nv_bfloat16* dkrow = a.dk + (grow * p.heads_kv + hk) * D;
-      __nv_bfloat16* dvrow = a.dv + (grow * p.heads_kv + hk) * D;
+      __nv_bfloat16* dkrow = a.dk + (grow * p.heads_kv + hk) * D + d0;
+      __nv_bfloat16* dvrow = a.dv + (grow * p.heads_kv + hk) * D + d0;
       const float sc = p.scale;
 #pragma unroll
-      for (int c = 0; c < D; c += 16) {
-        uint32_t u[16], w[16];
-        tmem_ld16(tmem + lane_base + C::COL_DK + c, u);
-        tmem_ld16(tmem + lane_base + C::COL_DV + c, w);
+      for (int c0d = 0; c0d < DH; c0d += 32) {
+        uint32_t u[32], w[32];
+        tmem_ld32_nowait(tmem + lane_base + C::COL_DK + d0 + c0d, u);
+        tmem_ld32_nowait(tmem + lane_base + C::COL_DV + d0 + c0d, w);
         tmem_wait_ld();
         if (kv_ok) {
-          uint4 k0, k1, v0, v1;
-          k0.x = pack_bf16(__uint_as_float(u[0]) * sc, __uint_as_float(u[1]) * sc);
-          k0.y = pack_bf16(__uint_as_float(u[2]) * sc, __uint_as_float(u[3]) * sc);
-          k0.z = pack_bf16(__uint_as_float(u[4]) * sc, __uint_as_float(u[5]) * sc);
-          k0.w = pack_bf16(__uint_as_float(u[6]) * sc, __uint_as_float(u[7]) * sc);
-          k1.x = pack_bf16(__uint_as_float(u[8]) * sc, __uint_as_float(u[9]) * sc);
-          k1.y = pack_bf16(__uint_as_float(u[10]) * sc, __uint_as_float(u[11]) * sc);
-          k1.z = pack_bf16(__uint_as_float(u[12]) * sc, __uint_as_float(u[13]) * sc);
-          k1.w = pack_bf16(__uint_as_float(u[14]) * sc, __uint_as_float(u[15]) * sc);
-          v0.x = pack_bf16(__uint_as_float(w[0]), __uint_as_float(w[1]));
-          v0.y = pack_bf16(__uint_as_float(w[2]), __uint_as_float(w[3]));
-          v0.z = pack_bf16(__uint_as_float(w[4]), __uint_as_float(w[5]));
-          v0.w = pack_bf16(__uint_as_float(w[6]), __uint_as_float(w[7]));
-          v1.x = pack_bf16(__uint_as_float(w[8]), __uint_as_float(w[9]));
-          v1.y = pack_bf16(__uint_as_float(w[10]), __uint_as_float(w[11]));
-          v1.z = pack_bf16(__uint_as_float(w[12]), __uint_as_float(w[13]));
-          v1.w = pack_bf16(__uint_as_float(w[14]), __uint_as_float(w[15]));
-          *reinterpret_cast<uint4*>(dkrow + c) = k0;
-          *reinterpret_cast<uint4*>(dkrow + c + 8) = k1;
-          *reinterpret_cast<uint4*>(dvrow + c) = v0;
-          *reinterpret_cast<uint4*>(dvrow + c + 8) = v1;
+#pragma unroll
+          for (int c = 0; c < 32; c += 8) {
+            uint4 kk, vv;
+            kk.x = pack_bf16(__uint_as_float(u[c + 0]) * sc, __uint_as_float(u[c + 1]) * sc);
+            kk.y = pack_bf16(__uint_as_float(u[c + 2]) * sc, __uint_as_float(u[c + 3]) * sc);
+            kk.z = pack_bf16(__uint_as_float(u[c + 4]) * sc, __uint_as_float(u[c + 5]) * sc);
+            kk.w = pack_bf16(__uint_as_float(u[c + 6]) * sc, __uint_as_float(u[c + 7]) * sc);
+            vv.x = pack_bf16(__uint_as_float(w[c + 0]), __uint_as_float(w[c + 1]));
+            vv.y = pack_bf16(__uint_as_float(w[c + 2]), __uint_as_float(w[c + 3]));
+            vv.z = pack_bf16(__uint_as_float(w[c + 4]), __uint_as_float(w[c + 5]));
+            vv.w = pack_bf16(__uint_as_float(w[c + 6]), __uint_as_float(w[c + 7]));
+            *reinterpret_cast<uint4*>(dkrow + c0d + c) = kk;
+            *reinterpret_cast<uint4*>(dvrow + c0d + c) = vv;
+          }
         }
       }
     }
   } else {
-    // ---------------- dQ drain (warps 4..7) ----------------
-    const int t = threadIdx.x - 128;
+    // ---------------- dQ drain (warps 8..11) ----------------
+    // TMEM -> fp32 staging tile in shared memory (row-major [query][dim], the
+    // layout of one head's rows in the head-major accumulator) -> one bulk
+    // reduce-add (ATOMIC) or bulk store into this KV tile's slab (SPLIT).
+    const int t = threadIdx.x - 256;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     float* base = a.dq_acc;
     bool slab_ok = true;
@@ -358,59 +391,49 @@ __global__ void __launch_bounds__(320, 1)
       const int qb = it & 1, qu = it >> 1;
       if (!mbar_wait(&bar_dq_full[qb], qu & 1, ac)) break;
       tc_fence_after();
-      uint32_t u[64];
-      {
-        uint32_t (&u0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&u[0]);
-        uint32_t (&u1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&u[32]);
-        tmem_ld32(tmem + lane_base + C::COL_DQ + 64 * qb, u0);
-        tmem_ld32(tmem + lane_base + C::COL_DQ + 64 * qb + 32, u1);
+      if (t == 0) bulk_wait_read<0>();   // previous bulk copy finished reading the tile
+      named_bar_sync(2, 128);
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t u[32];
+        tmem_ld32_nowait(tmem + lane_base + C::COL_DQ + 64 * qb + 32 * half, u);
         tmem_wait_ld();
-      }
-      tc_fence_before();
-      mbar_arrive(&bar_dq_empty[qb]);
-      if (!slab_ok) continue;
-      if (D == 64) {
-        // lane = query row, 64 columns = head dims
-        const int q = q0 + t;
-        if (q < seq.len) {
-          float* dst = base + ((static_cast<size_t>(seq.b) * p.rows_total + seq.row0 + q) *
-                                   p.heads_q + h) * D;
-          if (a.split) {
-#pragma unroll
-            for (int c = 0; c < 64; c += 4)
-              *reinterpret_cast<float4*>(dst + c) =
-                  make_float4(__uint_as_float(u[c]), __uint_as_float(u[c + 1]),
-                              __uint_as_float(u[c + 2]), __uint_as_float(u[c + 3]));
-          } else {
-#pragma unroll
-            for (int c = 0; c < 64; c += 4)
-              red_add_v4(dst + c, __uint_as_float(u[c]), __uint_as_float(u[c + 1]),
-                         __uint_as_float(u[c + 2]), __uint_as_float(u[c + 3]));
-          }
+        if (half == 1) {
+          tc_fence_before();
+          mbar_arrive(&bar_dq_empty[qb]);
         }
-      } else {
-        // lane = head dim, 64 columns = query rows
-        const int d = t;
-        const int nq = min(BM, seq.len - q0);
-        float* dst = base + ((static_cast<size_t>(seq.b) * p.rows_total + seq.row0 + q0) *
-                                 p.heads_q + h) * D + d;
-        const size_t rs = static_cast<size_t>(p.heads_q) * D;
-        if (a.split) {
+        if (D == 64) {
+          // lane = query row, 64 columns = head dims
+          float4* row = reinterpret_cast<float4*>(sDQ + t * D + 32 * half);
 #pragma unroll
-          for (int c = 0; c < 64; ++c)
-            if (c < nq) dst[c * rs] = __uint_as_float(u[c]);
+          for (int c = 0; c < 8; ++c)
+            row[c] = make_float4(__uint_as_float(u[4 * c]), __uint_as_float(u[4 * c + 1]),
+                                 __uint_as_float(u[4 * c + 2]), __uint_as_float(u[4 * c + 3]));
         } else {
+          // lane = head dim, 64 columns = query rows
 #pragma unroll
-          for (int c = 0; c < 64; ++c)
-            if (c < nq) red_add(dst + c * rs, __uint_as_float(u[c]));
+          for (int c = 0; c < 32; ++c) sDQ[(c + 32 * half) * D + t] = __uint_as_float(u[c]);
         }
+      }
+      fence_proxy_async_smem();
+      named_bar_sync(2, 128);
+      if (t == 0 && slab_ok) {
+        const int nq = min(BM, seq.len - q0);
+        float* dst = base + ((static_cast<size_t>(seq.b) * p.heads_q + h) * p.rows_total +
+                             seq.row0 + q0) * D;
+        if (a.split)
+          bulk_store(dst, sDQ, static_cast<uint32_t>(nq) * D * 4);
+        else
+          bulk_reduce_add_f32(dst, sDQ, static_cast<uint32_t>(nq) * D * 4);
+        bulk_commit();
       }
     }
+    if (t == 0) bulk_wait<0>();
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == 13) {
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);
     tmem_relinquish();

@@ -88,10 +88,13 @@ __global__ void __launch_bounds__(256) attn_dq_finalize_kernel(Problem p, const 
     const size_t rh = c / CPR;
     const int sub = static_cast<int>(c % CPR);
     const size_t bs = rh / p.heads_q;
+    const int hh = static_cast<int>(rh % p.heads_q);
     const int srow = static_cast<int>(bs % p.rows_total);
+    const size_t bb = bs / p.rows_total;
     float v[8] = {0, 0, 0, 0, 0, 0, 0, 0};
     if (srow < end) {
-      const size_t e0 = rh * D + sub * 8;
+      // accumulator / slabs are head-major: [batch, head, row, dim]
+      const size_t e0 = ((bb * p.heads_q + hh) * p.rows_total + srow) * D + sub * 8;
       if (!split) {
         const float4 a0 = *reinterpret_cast<const float4*>(acc + e0);
         const float4 a1 = *reinterpret_cast<const float4*>(acc + e0 + 4);

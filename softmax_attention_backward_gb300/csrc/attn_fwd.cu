@@ -5,16 +5,22 @@
 //
 // One CTA owns two 128-row query tiles of one (batch, query head) and streams
 // 128-row K/V tiles through a TMA ring:
-//   warp 8      TMA producer (Q once, then K_j, V_j into the ring)
-//   warp 9      MMA issuer: S_w = Q_w K_j^T and O_w += P_w V_j on tcgen05,
-//               accumulators in TMEM (S0, S1, O0, O1 = 512 columns for D=128)
-//   warps 0..3  softmax for query tile 0, warps 4..7 for query tile 1: each
-//               thread owns one row (TMEM lane), computes the online softmax
-//               in the log2 domain, writes P (bf16) to shared memory for the
-//               next MMA and rescales its O row in TMEM when the running max
-//               grew by more than 2^8.
-// The two tiles alternate on the tensor core so one tile's softmax overlaps
-// the other tile's MMAs.
+//   warp 8        TMA producer (Q once, then K_j, V_j into the ring)
+//   warps 9, 10   MMA issuers, one per query tile w: S_w = Q_w K_j^T (both
+//                 operands in shared memory) and O_w += P_w V_j with P_w read
+//                 from TMEM (it overwrites the first 64 columns of S_w as
+//                 packed bf16 pairs); accumulators S0, S1, O0, O1 in TMEM
+//                 (512 columns for D = 128)
+//   warps 0..3    softmax for query tile 0, warps 4..7 for query tile 1: each
+//                 thread owns one row (TMEM lane), runs the online softmax in
+//                 the log2 domain, rescales its O row in TMEM when the running
+//                 max grew by more than 2^8, and stores P back into TMEM.
+// A single issuing thread needs ~100 cycles per tcgen05.mma, so each query
+// tile has its own issuer; the two tiles alternate on the tensor core, one
+// tile's softmax overlapping the other tile's MMAs.  Each issuer runs
+// S_w(j), [P_w(j) ready] PV_w(j), S_w(j+1), ...: MMAs from one thread execute
+// in order, so S_w(j+1) never overwrites P_w(j) before PV_w(j) has read it,
+// and a completed S_w(j+1) also means O_w holds every PV_w up to j.
 #include <cuda_runtime.h>
 
 #include "launch.h"
@@ -27,16 +33,15 @@ struct FwdCfg {
   static constexpr int BN = 128;                   // rows per key/value tile
   static constexpr int Q_BYTES = BM * D * 2;
   static constexpr int KV_BYTES = BN * D * 2;
-  static constexpr int P_BYTES = BM * BN * 2;
-  static constexpr int NSLOT = (D == 128) ? 3 : 4; // K/V ring slots
-  static constexpr int SMEM = 2 * Q_BYTES + 2 * P_BYTES + NSLOT * KV_BYTES + 1024;
-  static constexpr int THREADS = 320;
+  static constexpr int NSLOT = (D == 128) ? 4 : 6; // K/V ring slots
+  static constexpr int SMEM = 2 * Q_BYTES + NSLOT * KV_BYTES + 1024;
+  static constexpr int THREADS = 352;
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t COL_S0 = 0, COL_S1 = 128, COL_O0 = 256, COL_O1 = 256 + D;
 };
 
 template <int D>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(352, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const FwdArgs a) {
   using C = FwdCfg<D>;
@@ -45,8 +50,7 @@ __global__ void __launch_bounds__(320, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   uint8_t* sQ = smem;                                   // 2 tiles
-  uint8_t* sP = smem + 2 * C::Q_BYTES;                  // 2 tiles
-  uint8_t* sRing = sP + 2 * C::P_BYTES;                 // NSLOT tiles
+  uint8_t* sRing = sQ + 2 * C::Q_BYTES;                 // NSLOT tiles
 
   __shared__ uint64_t bar_q, bar_full[C::NSLOT], bar_empty[C::NSLOT];
   __shared__ uint64_t bar_s[2], bar_p[2], bar_o[2];
@@ -88,7 +92,7 @@ __global__ void __launch_bounds__(320, 1)
     mbar_init(&bar_q, 1);
     for (int i = 0; i < C::NSLOT; ++i) {
       mbar_init(&bar_full[i], 1);
-      mbar_init(&bar_empty[i], 1);
+      mbar_init(&bar_empty[i], 2);       // released by both issuers
     }
     for (int w = 0; w < 2; ++w) {
       mbar_init(&bar_s[w], 1);
@@ -127,55 +131,50 @@ __global__ void __launch_bounds__(320, 1)
                       row_base + (i >> 1) * C::BN, seq.b);
       }
     }
-  } else if (warp == 9) {
-    // ---------------- MMA issuer ----------------
+  } else if (warp == 9 || warp == 10) {
+    // ---------------- MMA issuer of query tile w ----------------
+    const int w = warp - 9;
     if (lane_id() == 0) {
       const uint32_t idS = idesc_bf16(C::BM, C::BN, false, false);
       const uint32_t idO = idesc_bf16(C::BM, D, false, true);
-      const uint32_t qaddr = smem_u32(sQ), paddr = smem_u32(sP), raddr = smem_u32(sRing);
-      const uint32_t colS[2] = {C::COL_S0, C::COL_S1};
-      const uint32_t colO[2] = {C::COL_O0, C::COL_O1};
+      const uint64_t dQw = desc_kmajor_base(smem_u32(sQ + w * C::Q_BYTES));
+      const uint64_t dR_k0 = desc_kmajor_base(smem_u32(sRing));
+      const uint64_t dR_mn0 = desc_mnmajor_base(smem_u32(sRing), C::BN);
+      const uint32_t tS = tmem + (w ? C::COL_S1 : C::COL_S0);
+      const uint32_t tO = tmem + (w ? C::COL_O1 : C::COL_O0);
+      const int nt = n_w[w];
       bool ok = mbar_wait(&bar_q, 0, ac);
-      auto ring_wait = [&](int i) -> bool {
-        return mbar_wait(&bar_full[i % C::NSLOT], (i / C::NSLOT) & 1, ac);
-      };
-      auto issue_s = [&](int w, int i_k) {
-        const uint32_t kaddr = raddr + (i_k % C::NSLOT) * C::KV_BYTES;
+      // this tile stops after nt key tiles, but every ring slot up to n_kv must
+      // still be released twice
+      for (int j = 0; ok && j < n_kv; ++j) {
+        const int ik = 2 * j, iv = 2 * j + 1;
+        const int sk = ik % C::NSLOT, sv = iv % C::NSLOT;
+        if (j >= nt) {                      // release without using
+          if (!mbar_wait(&bar_full[sk], (ik / C::NSLOT) & 1, ac)) break;
+          mbar_arrive(&bar_empty[sk]);
+          if (!mbar_wait(&bar_full[sv], (iv / C::NSLOT) & 1, ac)) break;
+          mbar_arrive(&bar_empty[sv]);
+          continue;
+        }
+        if (!mbar_wait(&bar_full[sk], (ik / C::NSLOT) & 1, ac)) break;
+        tc_fence_after();
+        const uint64_t kd = desc_advance(dR_k0, sk * C::KV_BYTES);
 #pragma unroll
         for (int k = 0; k < D / 16; ++k)
-          umma_ss(tmem + colS[w], desc_kmajor(qaddr + w * C::Q_BYTES, C::BM, k),
-                  desc_kmajor(kaddr, C::BN, k), idS, k > 0);
+          umma_ss(tS, desc_advance(dQw, kmajor_step_bytes(C::BM, k)),
+                  desc_advance(kd, kmajor_step_bytes(C::BN, k)), idS, k > 0);
         umma_commit(&bar_s[w]);
-      };
-      if (ok && n_kv > 0) {
-        ok = ring_wait(0);
-        if (ok) {
-          tc_fence_after();
-          for (int w = 0; w < 2; ++w)
-            if (n_w[w] > 0) issue_s(w, 0);
-          umma_commit(&bar_empty[0]);
-        }
-      }
-      for (int j = 0; ok && j < n_kv; ++j) {
-        const int iv = 2 * j + 1, ik = 2 * j + 2;
-        if (!ring_wait(iv)) break;
-        if (j + 1 < n_kv && !ring_wait(ik)) break;
+        umma_commit(&bar_empty[sk]);
+        if (!mbar_wait(&bar_full[sv], (iv / C::NSLOT) & 1, ac)) break;
+        if (!mbar_wait(&bar_p[w], j & 1, ac)) break;
         tc_fence_after();
-        const uint32_t vaddr = raddr + (iv % C::NSLOT) * C::KV_BYTES;
-        for (int w = 0; w < 2; ++w) {
-          if (j >= n_w[w]) continue;
-          if (!mbar_wait(&bar_p[w], j & 1, ac)) { ok = false; break; }
-          tc_fence_after();
-          if (j + 1 < n_w[w]) issue_s(w, ik);
+        const uint64_t vd = desc_advance(dR_mn0, sv * C::KV_BYTES);
 #pragma unroll
-          for (int k = 0; k < C::BN / 16; ++k)
-            umma_ss(tmem + colO[w], desc_kmajor(paddr + w * C::P_BYTES, C::BM, k),
-                    desc_mnmajor(vaddr, C::BN, k), idO, (j > 0 || k > 0) ? 1u : 0u);
-          umma_commit(&bar_o[w]);
-        }
-        if (!ok) break;
-        umma_commit(&bar_empty[iv % C::NSLOT]);
-        if (j + 1 < n_kv) umma_commit(&bar_empty[ik % C::NSLOT]);
+        for (int k = 0; k < C::BN / 16; ++k)   // P: 8 packed columns per 16 keys
+          umma_ts(tO, tS + 8 * k, desc_advance(vd, mnmajor_step_bytes(k)), idO,
+                  (j > 0 || k > 0) ? 1u : 0u);
+        umma_commit(&bar_o[w]);
+        umma_commit(&bar_empty[sv]);
       }
     }
   } else {
@@ -189,19 +188,19 @@ __global__ void __launch_bounds__(320, 1)
     const int nt = n_w[w];
     const float sl2 = a.scale_log2;
     float m_run = -INFINITY, l_run = 0.f;
-    uint8_t* myP = sP + w * C::P_BYTES;
     bool ok = true;
     for (int j = 0; j < nt; ++j) {
+      // S_w(j) complete also means PV_w(j-1) is complete (same issuer, in order)
       if (!mbar_wait(&bar_s[w], j & 1, ac)) { ok = false; break; }
       tc_fence_after();
       float s[C::BN];
+      {
+        uint32_t u[C::BN];
 #pragma unroll
-      for (int c = 0; c < C::BN; c += 32) {
-        uint32_t r[32];
-        tmem_ld32(tS + c, r);
+        for (int c = 0; c < C::BN; c += 32) tmem_ld32_nowait(tS + c, u + c);
         tmem_wait_ld();
 #pragma unroll
-        for (int i = 0; i < 32; ++i) s[c + i] = __uint_as_float(r[i]);
+        for (int c = 0; c < C::BN; ++c) s[c] = __uint_as_float(u[c]);
       }
       const int kv0 = j * C::BN;
       const bool need_mask =
@@ -212,52 +211,46 @@ __global__ void __launch_bounds__(320, 1)
         for (int c = 0; c < C::BN; ++c)
           if (kv0 + c > lim) s[c] = -INFINITY;
       }
-      float mt = -INFINITY;
+      // row max with independent partial maxima (short dependency chains)
+      float mx[8];
 #pragma unroll
-      for (int c = 0; c < C::BN; ++c) mt = fmaxf(mt, s[c]);
-      mt *= sl2;
+      for (int i = 0; i < 8; ++i) mx[i] = s[i];
+#pragma unroll
+      for (int c = 8; c < C::BN; ++c) mx[c & 7] = fmaxf(mx[c & 7], s[c]);
+      const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                             fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * sl2;
       const float m_new = fmaxf(m_run, mt);
       const bool grow = m_new > m_run + 8.0f;          // also true on the first finite max
       const float m_use = grow ? m_new : m_run;
       const float alpha = grow ? ex2(m_run - m_use) : 1.0f;
       const float msub = (m_use == -INFINITY) ? 0.f : m_use;
-      const bool warp_rescale = __any_sync(0xffffffffu, grow) && j > 0;
-      float rs = 0.f;
+      const bool warp_rescale = j > 0 && __any_sync(0xffffffffu, grow);
+      float rsum[4] = {0.f, 0.f, 0.f, 0.f};
       uint32_t pk[C::BN / 2];
 #pragma unroll
       for (int c = 0; c < C::BN; c += 2) {
         const float p0 = ex2(fmaf(s[c], sl2, -msub));
         const float p1 = ex2(fmaf(s[c + 1], sl2, -msub));
-        rs += p0 + p1;
+        rsum[(c >> 1) & 3] += p0 + p1;
         pk[c / 2] = pack_bf16(p0, p1);
       }
-      l_run = l_run * alpha + rs;
+      l_run = l_run * alpha + ((rsum[0] + rsum[1]) + (rsum[2] + rsum[3]));
       m_run = m_use;
-      if (j > 0) {
-        if (!mbar_wait(&bar_o[w], (j - 1) & 1, ac)) { ok = false; break; }
-        tc_fence_after();
-        if (warp_rescale) {
+      if (warp_rescale) {
 #pragma unroll
-          for (int c = 0; c < D; c += 16) {
-            uint32_t r[16];
-            tmem_ld16(tO + c, r);
-            tmem_wait_ld();
+        for (int c = 0; c < D; c += 32) {
+          uint32_t r[32];
+          tmem_ld32_nowait(tO + c, r);
+          tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 16; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-            tmem_st16(tO + c, r);
-          }
-          tmem_wait_st();
+          for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+          tmem_st32(tO + c, r);
         }
       }
-      // P row -> shared memory, K-major 128B-swizzled (two 64-column panels)
-#pragma unroll
-      for (int ch = 0; ch < C::BN / 8; ++ch) {
-        const int panel = ch >> 3;
-        const uint32_t off = panel * C::BM * 128 + t * 128 + (((ch & 7) ^ (t & 7)) << 4);
-        uint4 v = make_uint4(pk[ch * 4 + 0], pk[ch * 4 + 1], pk[ch * 4 + 2], pk[ch * 4 + 3]);
-        *reinterpret_cast<uint4*>(myP + off) = v;
-      }
-      fence_proxy_async_smem();
+      // P (bf16 pairs) into the first 64 columns of this row's S
+      tmem_st32(tS, pk);
+      tmem_st32(tS + 32, pk + 32);
+      tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&bar_p[w]);
     }
@@ -269,22 +262,20 @@ __global__ void __launch_bounds__(320, 1)
       const size_t grow_idx = (static_cast<size_t>(seq.b) * p.rows_total + seq.row0 + row);
       __nv_bfloat16* orow = a.o + (grow_idx * p.heads_q + h) * D;
 #pragma unroll
-      for (int c = 0; c < D; c += 16) {
-        uint32_t r[16];
-        tmem_ld16(tO + c, r);
+      for (int c = 0; c < D; c += 32) {
+        uint32_t r[32];
+        tmem_ld32_nowait(tO + c, r);
         tmem_wait_ld();
         if (valid) {
-          uint4 v0, v1;
-          v0.x = pack_bf16(__uint_as_float(r[0]) * inv_l, __uint_as_float(r[1]) * inv_l);
-          v0.y = pack_bf16(__uint_as_float(r[2]) * inv_l, __uint_as_float(r[3]) * inv_l);
-          v0.z = pack_bf16(__uint_as_float(r[4]) * inv_l, __uint_as_float(r[5]) * inv_l);
-          v0.w = pack_bf16(__uint_as_float(r[6]) * inv_l, __uint_as_float(r[7]) * inv_l);
-          v1.x = pack_bf16(__uint_as_float(r[8]) * inv_l, __uint_as_float(r[9]) * inv_l);
-          v1.y = pack_bf16(__uint_as_float(r[10]) * inv_l, __uint_as_float(r[11]) * inv_l);
-          v1.z = pack_bf16(__uint_as_float(r[12]) * inv_l, __uint_as_float(r[13]) * inv_l);
-          v1.w = pack_bf16(__uint_as_float(r[14]) * inv_l, __uint_as_float(r[15]) * inv_l);
-          *reinterpret_cast<uint4*>(orow + c) = v0;
-          *reinterpret_cast<uint4*>(orow + c + 8) = v1;
+#pragma unroll
+          for (int i = 0; i < 32; i += 8) {
+            uint4 v;
+            v.x = pack_bf16(__uint_as_float(r[i + 0]) * inv_l, __uint_as_float(r[i + 1]) * inv_l);
+            v.y = pack_bf16(__uint_as_float(r[i + 2]) * inv_l, __uint_as_float(r[i + 3]) * inv_l);
+            v.z = pack_bf16(__uint_as_float(r[i + 4]) * inv_l, __uint_as_float(r[i + 5]) * inv_l);
+            v.w = pack_bf16(__uint_as_float(r[i + 6]) * inv_l, __uint_as_float(r[i + 7]) * inv_l);
+            *reinterpret_cast<uint4*>(orow + c + i) = v;
+          }
         }
       }
       if (valid) {

@@ -21,7 +21,7 @@ struct BwdArgs {
   const float* delta;
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
-  float* dq_acc;        // ATOMIC: accumulator [rows, Hq, D]; SPLIT: slab base
+  float* dq_acc;        // ATOMIC: accumulator [B, Hq, rows, D]; SPLIT: slab base
   size_t slab_elems;    // SPLIT: elements per slab (0 for ATOMIC)
   int n_split;          // SPLIT: number of slabs
   int split;            // 1 = SPLIT

@@ -40,15 +40,22 @@ struct BwdCfg {
   static constexpr int SMEM = 2 * KV_BYTES + 2 * NST * QT_BYTES + DS_BYTES + DQ_BYTES + 1024;
   static constexpr int THREADS = 512;
   static constexpr uint32_t TMEM_COLS = 512;
-  static constexpr uint32_t COL_S = 0;                // S^T, then P^T (packed) in place
-  static constexpr uint32_t COL_DP = BM;              // dP^T, then dS^T (packed) in place
+  static constexpr uint32_t COL_S = 0;                // S^T (fp32)
+  static constexpr uint32_t COL_DP = BM;              // dP^T (fp32)
   static constexpr uint32_t COL_DV = 2 * BM;
   static constexpr uint32_t COL_DK = 2 * BM + D;
-  static constexpr uint32_t COL_DQ = 2 * BM + 2 * D;  // two 64-column buffers
-  // TMEM column (relative to COL_S / COL_DP) of the packed bf16 operand for the
-  // 16 query columns of K-step kk: warpgroup w = 16 kk / HALF stores its HALF
-  // columns as HALF/2 packed columns at the start of its own HALF-column range.
-  __host__ __device__ static constexpr uint32_t packed_col(int kk) { return 8 * kk + (16 * kk / HALF) * (HALF / 2); }
+  static constexpr uint32_t COL_DQ = 2 * BM + 2 * D;  // one 64-column dQ tile
+  static constexpr uint32_t COL_PT = COL_DQ + 64;     // P^T, packed bf16 (BM/2 columns)
+  // D = 128 also has room for dS^T (packed) of its own; D = 64 writes dS^T
+  // over the dP^T columns it came from (each thread over its own columns).
+  static constexpr bool DS_ALIAS = (COL_PT + BM / 2 + BM / 2 > TMEM_COLS);
+  static constexpr uint32_t COL_DST = DS_ALIAS ? COL_DP : COL_PT + BM / 2;
+  // TMEM column (relative to COL_DST) of the packed dS^T columns of K-step kk.
+  // Dedicated region: 8 per step.  Aliased: warpgroup w = 16 kk / HALF keeps
+  // its HALF/2 packed columns at the start of its own HALF-column range.
+  __host__ __device__ static constexpr uint32_t dst_col(int kk) {
+    return DS_ALIAS ? 8 * kk + (16 * kk / HALF) * (HALF / 2) : 8 * kk;
+  }
 };
 
 // Warp roles (512 threads): 0..7 P/dS (two warpgroups, each owns half of the
@@ -76,10 +83,11 @@ __global__ void __launch_bounds__(512, 1)
 
   __shared__ uint64_t bar_kv, bar_qfull[C::NST], bar_qempty[C::NST];
   __shared__ uint64_t bar_s, bar_dp, bar_p, bar_ds, bar_pt_done, bar_dst_done, bar_dss_free;
-  __shared__ uint64_t bar_done, bar_dq_full[2], bar_dq_empty[2];
+  __shared__ uint64_t bar_s_free, bar_dp_free, bar_done, bar_dq_full, bar_dq_empty;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_flag;
-  __shared__ float s_lse[2][BM], s_delta[2][BM];
+  __shared__ __align__(16) float s_nlse[2][BM];   // -LSE * log2(e) per query column
+  __shared__ __align__(16) float s_delta[2][BM];
 
   const Problem& p = a.p;
   const int warp = warp_id();
@@ -111,11 +119,11 @@ __global__ void __launch_bounds__(512, 1)
     mbar_init(&bar_pt_done, 1);
     mbar_init(&bar_dst_done, 1);
     mbar_init(&bar_dss_free, 1);
+    mbar_init(&bar_s_free, 256);
+    mbar_init(&bar_dp_free, 256);
     mbar_init(&bar_done, 1);
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&bar_dq_full[b], 1);
-      mbar_init(&bar_dq_empty[b], 128);
-    }
+    mbar_init(&bar_dq_full, 1);
+    mbar_init(&bar_dq_empty, 128);
     fence_mbar_init();
   }
   if (warp == 13) tmem_alloc(&tmem_base_sh, C::TMEM_COLS);
@@ -162,8 +170,8 @@ __global__ void __launch_bounds__(512, 1)
       for (int it = 0; ok && it < n_it; ++it) {
         const int st = it % C::NST;
         if (!mbar_wait(&bar_qfull[st], (it / C::NST) & 1, ac)) break;
-        // S^T region is free once dV(it-1) has consumed P^T(it-1) stored there
-        if (it > 0 && !mbar_wait(&bar_pt_done, (it - 1) & 1, ac)) break;
+        // S^T region is free once the P/dS warps have read S^T(it-1)
+        if (it > 0 && !mbar_wait(&bar_s_free, (it - 1) & 1, ac)) break;
         tc_fence_after();
         const uint64_t qd = desc_advance(dQ_k0, st * C::QT_BYTES);
 #pragma unroll
@@ -171,8 +179,10 @@ __global__ void __launch_bounds__(512, 1)
           umma_ss(tmem + C::COL_S, desc_advance(dK_k, kmajor_step_bytes(BN, k)),
                   desc_advance(qd, kmajor_step_bytes(BM, k)), idSD, k > 0);
         umma_commit(&bar_s);
-        // dP^T region is free once dK(it-1) has consumed dS^T(it-1)
-        if (it > 0 && !mbar_wait(&bar_dst_done, (it - 1) & 1, ac)) break;
+        // dP^T region is free once dP^T(it-1) has been read and, when dS^T is
+        // stored over it, once dK(it-1) has consumed dS^T(it-1)
+        if (it > 0 && !mbar_wait(C::DS_ALIAS ? &bar_dst_done : &bar_dp_free, (it - 1) & 1, ac))
+          break;
         tc_fence_after();
         const uint64_t od = desc_advance(ddO_k0, st * C::QT_BYTES);
 #pragma unroll
@@ -198,7 +208,7 @@ __global__ void __launch_bounds__(512, 1)
         const uint64_t omn = desc_advance(ddO_mn0, st * C::QT_BYTES);
 #pragma unroll
         for (int k = 0; k < BM / 16; ++k)
-          umma_ts(tmem + C::COL_DV, tmem + C::COL_S + C::packed_col(k),
+          umma_ts(tmem + C::COL_DV, tmem + C::COL_PT + 8 * k,
                   desc_advance(omn, mnmajor_step_bytes(k)), idKV, (it > 0 || k > 0) ? 1u : 0u);
         umma_commit(&bar_pt_done);
         if (!mbar_wait(&bar_ds, it & 1, ac)) break;
@@ -206,7 +216,7 @@ __global__ void __launch_bounds__(512, 1)
         const uint64_t qmn = desc_advance(dQ_mn0, st * C::QT_BYTES);
 #pragma unroll
         for (int k = 0; k < BM / 16; ++k)
-          umma_ts(tmem + C::COL_DK, tmem + C::COL_DP + C::packed_col(k),
+          umma_ts(tmem + C::COL_DK, tmem + C::COL_DST + C::dst_col(k),
                   desc_advance(qmn, mnmajor_step_bytes(k)), idKV, (it > 0 || k > 0) ? 1u : 0u);
         umma_commit(&bar_dst_done);
         umma_commit(&bar_qempty[st]);
@@ -222,10 +232,9 @@ __global__ void __launch_bounds__(512, 1)
       bool ok = mbar_wait(&bar_kv, 0, ac);
       for (int it = 0; ok && it < n_it; ++it) {
         if (!mbar_wait(&bar_ds, it & 1, ac)) break;
-        const int qb = it & 1, qu = it >> 1;
-        if (!mbar_wait(&bar_dq_empty[qb], (qu & 1) ^ 1, ac)) break;
+        if (!mbar_wait(&bar_dq_empty, (it & 1) ^ 1, ac)) break;
         tc_fence_after();
-        const uint32_t tDQ = tmem + C::COL_DQ + 64 * qb;
+        const uint32_t tDQ = tmem + C::COL_DQ;
 #pragma unroll
         for (int k = 0; k < BN / 16; ++k) {
           if (D == 64)   // dQ[q, d] = dS[q, kv] K[kv, d]
@@ -235,7 +244,7 @@ __global__ void __launch_bounds__(512, 1)
             umma_ss(tDQ, desc_advance(dK_mn, mnmajor_step_bytes(k)),
                     desc_advance(ddS_mn, mnmajor_step_bytes(k)), idQ, k > 0);
         }
-        umma_commit(&bar_dq_full[qb]);
+        umma_commit(&bar_dq_full);
         umma_commit(&bar_dss_free);
       }
     }
@@ -249,7 +258,8 @@ __global__ void __launch_bounds__(512, 1)
     const int kv = kv0 + r;                            // KV row inside the sequence
     const bool kv_ok = kv < seq.len;
     const float sl2 = a.scale_log2;
-    // LSE (log2 domain) or Delta of one query column, fetched one step ahead
+    // LSE or Delta of one query column, loaded one step ahead; the loaded value
+    // is not touched until the next step, so the load latency stays hidden
     auto fetch = [&](int it) -> float {
       if (tid >= 2 * BM) return 0.f;
       const bool is_lse = tid < BM;
@@ -262,44 +272,65 @@ __global__ void __launch_bounds__(512, 1)
         li = static_cast<size_t>(h) * p.rows_total + seq.row0 + q;
       else
         li = (static_cast<size_t>(seq.b) * p.heads_q + h) * p.rows_total + q;
-      return is_lse ? __ldg(a.lse + li) * kLog2e : __ldg(a.delta + li);
+      return __ldg((is_lse ? a.lse : a.delta) + li);
     };
     float pf = (n_it > 0) ? fetch(0) : 0.f;
     bool ok = true;
-    const uint32_t tSme = tmem + lane_base + C::COL_S + c0;    // this thread's S / P columns
-    const uint32_t tDPme = tmem + lane_base + C::COL_DP + c0;  // this thread's dP / dS columns
+    const uint32_t tSme = tmem + lane_base + C::COL_S + c0;      // this thread's S columns
+    const uint32_t tDPme = tmem + lane_base + C::COL_DP + c0;    // this thread's dP columns
+    const uint32_t tPTme = tmem + lane_base + C::COL_PT + c0 / 2;
+    const uint32_t tDSTme = tmem + lane_base + C::COL_DST + (C::DS_ALIAS ? c0 : c0 / 2);
     for (int it = 0; it < n_it; ++it) {
       const int q0 = (i_start + it % n_i) * BM;
       const int buf = it & 1;
-      if (tid < BM) s_lse[buf][tid] = pf;
+      if (tid < BM) s_nlse[buf][tid] = -pf * kLog2e;   // LSE in the log2 domain, negated
       else if (tid < 2 * BM) s_delta[buf][tid - BM] = pf;
       if (it + 1 < n_it) pf = fetch(it + 1);
       named_bar_sync(1, 256);
       // ---- P^T (KV row r, query columns c0 .. c0 + HALF) ----
       if (!mbar_wait(&bar_s, it & 1, ac)) { ok = false; break; }
       tc_fence_after();
-      float pv[HALF];
+      // P^T in fp32 pairs: p2[i] = (P[2i], P[2i+1]) of this thread's columns
+      uint64_t p2[HALF / 2];
       {
         uint32_t u[HALF];
 #pragma unroll
         for (int c = 0; c < HALF; c += 32) tmem_ld32_nowait(tSme + c, u + c);
         tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(&bar_s_free);
+        // masking on S: the whole row past the sequence end, the causal
+        // triangle on diagonal tiles (columns c < lim hold earlier queries)
+        int lim = 0;
+        if (!kv_ok) lim = HALF;
+        else if (p.causal && q0 < kv0 + BN) lim = kv - q0 - c0;
+        if (lim > 0) {
 #pragma unroll
-        for (int c = 0; c < HALF; ++c) pv[c] = __uint_as_float(u[c]);
-      }
-      const bool diag = p.causal && (q0 < kv0 + BN);
+          for (int c = 0; c < HALF; ++c)
+            if (c < lim) u[c] = 0xff800000u;   // -inf
+        }
+        const uint64_t sl2x2 = f2_pack(sl2, sl2);
 #pragma unroll
-      for (int c = 0; c < HALF; ++c) {
-        float e = ex2(fmaf(pv[c], sl2, -s_lse[buf][c0 + c]));
-        if (!kv_ok || (diag && q0 + c0 + c < kv)) e = 0.f;
-        pv[c] = e;
+        for (int c = 0; c < HALF; c += 4) {
+          const float4 l4 = *reinterpret_cast<const float4*>(&s_nlse[buf][c0 + c]);
+          float a0, a1, a2, a3;
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(u[c]), __uint_as_float(u[c + 1])), sl2x2,
+                           f2_pack(l4.x, l4.y)), a0, a1);
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(u[c + 2]), __uint_as_float(u[c + 3])), sl2x2,
+                           f2_pack(l4.z, l4.w)), a2, a3);
+          p2[c / 2] = f2_pack(ex2(a0), ex2(a1));
+          p2[c / 2 + 1] = f2_pack(ex2(a2), ex2(a3));
+        }
       }
       {
         uint32_t pk[HALF / 2];
 #pragma unroll
-        for (int c = 0; c < HALF / 2; ++c) pk[c] = pack_bf16(pv[2 * c], pv[2 * c + 1]);
-        if constexpr (HALF / 2 == 32) tmem_st32(tSme, pk);
-        else tmem_st16(tSme, *reinterpret_cast<uint32_t(*)[16]>(pk));
+        for (int i = 0; i < HALF / 2; ++i) pk[i] = f2_to_bf16x2(p2[i]);
+        // P^T(it-1) must have been consumed by dV(it-1)
+        if (it > 0 && !mbar_wait(&bar_pt_done, (it - 1) & 1, ac)) { ok = false; break; }
+        tc_fence_after();
+        if constexpr (HALF / 2 == 32) tmem_st32(tPTme, pk);
+        else tmem_st16p(tPTme, pk);
       }
       tmem_wait_st();
       tc_fence_before();
@@ -307,20 +338,37 @@ __global__ void __launch_bounds__(512, 1)
       // ---- dS^T = P^T o (dP^T - Delta) ----
       if (!mbar_wait(&bar_dp, it & 1, ac)) { ok = false; break; }
       tc_fence_after();
+      uint32_t pk[HALF / 2];
       {
         uint32_t u[HALF];
 #pragma unroll
         for (int c = 0; c < HALF; c += 32) tmem_ld32_nowait(tDPme + c, u + c);
         tmem_wait_ld();
+        if constexpr (!C::DS_ALIAS) {
+          tc_fence_before();
+          mbar_arrive(&bar_dp_free);
+        }
 #pragma unroll
-        for (int c = 0; c < HALF; ++c)
-          pv[c] = pv[c] * (__uint_as_float(u[c]) - s_delta[buf][c0 + c]);
+        for (int c = 0; c < HALF; c += 4) {
+          const float4 d4 = *reinterpret_cast<const float4*>(&s_delta[buf][c0 + c]);
+          const uint64_t ds01 = f2_mul(
+              f2_sub(f2_pack(__uint_as_float(u[c]), __uint_as_float(u[c + 1])), f2_pack(d4.x, d4.y)),
+              p2[c / 2]);
+          const uint64_t ds23 = f2_mul(
+              f2_sub(f2_pack(__uint_as_float(u[c + 2]), __uint_as_float(u[c + 3])),
+                     f2_pack(d4.z, d4.w)),
+              p2[c / 2 + 1]);
+          pk[c / 2] = f2_to_bf16x2(ds01);
+          pk[c / 2 + 1] = f2_to_bf16x2(ds23);
+        }
       }
-      uint32_t pk[HALF / 2];
-#pragma unroll
-      for (int c = 0; c < HALF / 2; ++c) pk[c] = pack_bf16(pv[2 * c], pv[2 * c + 1]);
-      if constexpr (HALF / 2 == 32) tmem_st32(tDPme, pk);
-      else tmem_st16(tDPme, *reinterpret_cast<uint32_t(*)[16]>(pk));
+      if constexpr (!C::DS_ALIAS) {
+        // dS^T(it-1) must have been consumed by dK(it-1)
+        if (it > 0 && !mbar_wait(&bar_dst_done, (it - 1) & 1, ac)) { ok = false; break; }
+        tc_fence_after();
+      }
+      if constexpr (HALF / 2 == 32) tmem_st32(tDSTme, pk);
+      else tmem_st16p(tDSTme, pk);
       // dS (bf16) also to shared memory for the dQ GEMM
       if (it > 0 && !mbar_wait(&bar_dss_free, (it - 1) & 1, ac)) { ok = false; break; }
 #pragma unroll
@@ -388,32 +436,28 @@ __global__ void __launch_bounds__(512, 1)
     for (int it = 0; it < n_it; ++it) {
       const int h = hk * G + it / n_i;
       const int q0 = (i_start + it % n_i) * BM;
-      const int qb = it & 1, qu = it >> 1;
-      if (!mbar_wait(&bar_dq_full[qb], qu & 1, ac)) break;
+      if (!mbar_wait(&bar_dq_full, it & 1, ac)) break;
       tc_fence_after();
+      // free the TMEM tile first, then wait for the staging tile
+      uint32_t u[64];
+      tmem_ld32_nowait(tmem + lane_base + C::COL_DQ, u);
+      tmem_ld32_nowait(tmem + lane_base + C::COL_DQ + 32, u + 32);
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(&bar_dq_empty);
       if (t == 0) bulk_wait_read<0>();   // previous bulk copy finished reading the tile
       named_bar_sync(2, 128);
+      if (D == 64) {
+        // lane = query row, 64 columns = head dims
+        float4* row = reinterpret_cast<float4*>(sDQ + t * D);
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t u[32];
-        tmem_ld32_nowait(tmem + lane_base + C::COL_DQ + 64 * qb + 32 * half, u);
-        tmem_wait_ld();
-        if (half == 1) {
-          tc_fence_before();
-          mbar_arrive(&bar_dq_empty[qb]);
-        }
-        if (D == 64) {
-          // lane = query row, 64 columns = head dims
-          float4* row = reinterpret_cast<float4*>(sDQ + t * D + 32 * half);
+        for (int c = 0; c < 16; ++c)
+          row[c] = make_float4(__uint_as_float(u[4 * c]), __uint_as_float(u[4 * c + 1]),
+                               __uint_as_float(u[4 * c + 2]), __uint_as_float(u[4 * c + 3]));
+      } else {
+        // lane = head dim, 64 columns = query rows
 #pragma unroll
-          for (int c = 0; c < 8; ++c)
-            row[c] = make_float4(__uint_as_float(u[4 * c]), __uint_as_float(u[4 * c + 1]),
-                                 __uint_as_float(u[4 * c + 2]), __uint_as_float(u[4 * c + 3]));
-        } else {
-          // lane = head dim, 64 columns = query rows
-#pragma unroll
-          for (int c = 0; c < 32; ++c) sDQ[(c + 32 * half) * D + t] = __uint_as_float(u[c]);
-        }
+        for (int c = 0; c < 64; ++c) sDQ[c * D + t] = __uint_as_float(u[c]);
       }
       fence_proxy_async_smem();
       named_bar_sync(2, 128);

@@ -8,9 +8,9 @@
 //   warp 8        TMA producer (Q once, then K_j, V_j into the ring)
 //   warps 9, 10   MMA issuers, one per query tile w: S_w = Q_w K_j^T (both
 //                 operands in shared memory) and O_w += P_w V_j with P_w read
-//                 from TMEM (it overwrites the first 64 columns of S_w as
-//                 packed bf16 pairs); accumulators S0, S1, O0, O1 in TMEM
-//                 (512 columns for D = 128)
+//                 from TMEM as packed bf16 pairs (64 columns of its own for
+//                 D = 64, the first 64 columns of S_w for D = 128, where S0,
+//                 S1, O0, O1 already fill the 512 columns)
 //   warps 0..3    softmax for query tile 0, warps 4..7 for query tile 1: each
 //                 thread owns one row (TMEM lane), runs the online softmax in
 //                 the log2 domain, rescales its O row in TMEM when the running
@@ -33,11 +33,17 @@ struct FwdCfg {
   static constexpr int BN = 128;                   // rows per key/value tile
   static constexpr int Q_BYTES = BM * D * 2;
   static constexpr int KV_BYTES = BN * D * 2;
-  static constexpr int NSLOT = (D == 128) ? 4 : 6; // K/V ring slots
+  static constexpr int NSLOT = (D == 128) ? 5 : 6; // K/V ring slots
   static constexpr int SMEM = 2 * Q_BYTES + NSLOT * KV_BYTES + 1024;
   static constexpr int THREADS = 352;
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t COL_S0 = 0, COL_S1 = 128, COL_O0 = 256, COL_O1 = 256 + D;
+  // With D = 64 each tile also gets its own P region (64 packed columns), so
+  // S_w(j+1) can be computed while the softmax of tile j runs; with D = 128 P
+  // overwrites the first 64 columns of S_w.
+  static constexpr bool SEP_P = (256 + 2 * D + 2 * 64 <= 512);
+  static constexpr uint32_t COL_P0 = SEP_P ? 256 + 2 * D : COL_S0;
+  static constexpr uint32_t COL_P1 = SEP_P ? 256 + 2 * D + 64 : COL_S1;
 };
 
 template <int D>
@@ -53,7 +59,7 @@ __global__ void __launch_bounds__(352, 1)
   uint8_t* sRing = sQ + 2 * C::Q_BYTES;                 // NSLOT tiles
 
   __shared__ uint64_t bar_q, bar_full[C::NSLOT], bar_empty[C::NSLOT];
-  __shared__ uint64_t bar_s[2], bar_p[2], bar_o[2];
+  __shared__ uint64_t bar_s[2], bar_p[2], bar_o[2], bar_sfree[2], bar_stagger;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_flag;
 
@@ -98,7 +104,9 @@ __global__ void __launch_bounds__(352, 1)
       mbar_init(&bar_s[w], 1);
       mbar_init(&bar_p[w], 128);
       mbar_init(&bar_o[w], 1);
+      mbar_init(&bar_sfree[w], 128);
     }
+    mbar_init(&bar_stagger, 1);
     fence_mbar_init();
   }
   if (warp == 9) tmem_alloc(&tmem_base_sh, C::TMEM_COLS);
@@ -142,21 +150,16 @@ __global__ void __launch_bounds__(352, 1)
       const uint64_t dR_mn0 = desc_mnmajor_base(smem_u32(sRing), C::BN);
       const uint32_t tS = tmem + (w ? C::COL_S1 : C::COL_S0);
       const uint32_t tO = tmem + (w ? C::COL_O1 : C::COL_O0);
+      const uint32_t tP = tmem + (w ? C::COL_P1 : C::COL_P0);
       const int nt = n_w[w];
       bool ok = mbar_wait(&bar_q, 0, ac);
-      // this tile stops after nt key tiles, but every ring slot up to n_kv must
-      // still be released twice
-      for (int j = 0; ok && j < n_kv; ++j) {
-        const int ik = 2 * j, iv = 2 * j + 1;
-        const int sk = ik % C::NSLOT, sv = iv % C::NSLOT;
-        if (j >= nt) {                      // release without using
-          if (!mbar_wait(&bar_full[sk], (ik / C::NSLOT) & 1, ac)) break;
-          mbar_arrive(&bar_empty[sk]);
-          if (!mbar_wait(&bar_full[sv], (iv / C::NSLOT) & 1, ac)) break;
-          mbar_arrive(&bar_empty[sv]);
-          continue;
-        }
-        if (!mbar_wait(&bar_full[sk], (ik / C::NSLOT) & 1, ac)) break;
+      // Tile 1 starts one softmax phase after tile 0 (when P_0(0) is ready), so
+      // that one tile's softmax overlaps the other tile's MMAs instead of both
+      // running in lockstep.  bar_stagger completes exactly once.
+      if (w == 1 && ok) ok = mbar_wait(&bar_stagger, 0, ac);
+      auto issue_s = [&](int j) -> bool {
+        const int ik = 2 * j, sk = ik % C::NSLOT;
+        if (!mbar_wait(&bar_full[sk], (ik / C::NSLOT) & 1, ac)) return false;
         tc_fence_after();
         const uint64_t kd = desc_advance(dR_k0, sk * C::KV_BYTES);
 #pragma unroll
@@ -165,17 +168,46 @@ __global__ void __launch_bounds__(352, 1)
                   desc_advance(kd, kmajor_step_bytes(C::BN, k)), idS, k > 0);
         umma_commit(&bar_s[w]);
         umma_commit(&bar_empty[sk]);
-        if (!mbar_wait(&bar_full[sv], (iv / C::NSLOT) & 1, ac)) break;
-        if (!mbar_wait(&bar_p[w], j & 1, ac)) break;
+        return true;
+      };
+      auto issue_pv = [&](int j) -> bool {
+        const int iv = 2 * j + 1, sv = iv % C::NSLOT;
+        if (!mbar_wait(&bar_full[sv], (iv / C::NSLOT) & 1, ac)) return false;
+        if (!mbar_wait(&bar_p[w], j & 1, ac)) return false;
+        if (w == 0 && j == 0) mbar_arrive(&bar_stagger);
         tc_fence_after();
         const uint64_t vd = desc_advance(dR_mn0, sv * C::KV_BYTES);
 #pragma unroll
         for (int k = 0; k < C::BN / 16; ++k)   // P: 8 packed columns per 16 keys
-          umma_ts(tO, tS + 8 * k, desc_advance(vd, mnmajor_step_bytes(k)), idO,
+          umma_ts(tO, tP + 8 * k, desc_advance(vd, mnmajor_step_bytes(k)), idO,
                   (j > 0 || k > 0) ? 1u : 0u);
         umma_commit(&bar_o[w]);
         umma_commit(&bar_empty[sv]);
+        return true;
+      };
+      // release a ring slot this tile does not use (both issuers release each)
+      auto skip = [&](int i) -> bool {
+        if (!mbar_wait(&bar_full[i % C::NSLOT], (i / C::NSLOT) & 1, ac)) return false;
+        mbar_arrive(&bar_empty[i % C::NSLOT]);
+        return true;
+      };
+      if (C::SEP_P) {
+        // S(j+1) as soon as the softmax has read S(j); PV(j) once P(j) is ready
+        if (ok && nt > 0) ok = issue_s(0);
+        for (int j = 0; ok && j < nt; ++j) {
+          if (j + 1 < nt) {
+            if (!mbar_wait(&bar_sfree[w], j & 1, ac) || !issue_s(j + 1)) break;
+          }
+          if (!issue_pv(j)) break;
+        }
+      } else {
+        // S(j), PV(j), S(j+1), ...: MMAs of one thread execute in order, so
+        // S(j+1) cannot overwrite P(j) (stored over S) before PV(j) read it
+        for (int j = 0; ok && j < nt; ++j)
+          if (!issue_s(j) || !issue_pv(j)) ok = false;
       }
+      for (int j = nt; ok && j < n_kv; ++j)
+        if (!skip(2 * j) || !skip(2 * j + 1)) ok = false;
     }
   } else {
     // ---------------- softmax warpgroups ----------------
@@ -184,13 +216,15 @@ __global__ void __launch_bounds__(352, 1)
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + lane_base + (w ? C::COL_S1 : C::COL_S0);
     const uint32_t tO = tmem + lane_base + (w ? C::COL_O1 : C::COL_O0);
+    const uint32_t tP = tmem + lane_base + (w ? C::COL_P1 : C::COL_P0);
     const int row = m0 + w * C::BM + t;      // row inside the sequence
     const int nt = n_w[w];
     const float sl2 = a.scale_log2;
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
     for (int j = 0; j < nt; ++j) {
-      // S_w(j) complete also means PV_w(j-1) is complete (same issuer, in order)
+      // without a separate P region, S_w(j) complete also means PV_w(j-1) is
+      // complete (same issuer, in order)
       if (!mbar_wait(&bar_s[w], j & 1, ac)) { ok = false; break; }
       tc_fence_after();
       float s[C::BN];
@@ -199,6 +233,10 @@ __global__ void __launch_bounds__(352, 1)
 #pragma unroll
         for (int c = 0; c < C::BN; c += 32) tmem_ld32_nowait(tS + c, u + c);
         tmem_wait_ld();
+        if (C::SEP_P) {
+          tc_fence_before();
+          mbar_arrive(&bar_sfree[w]);
+        }
 #pragma unroll
         for (int c = 0; c < C::BN; ++c) s[c] = __uint_as_float(u[c]);
       }
@@ -211,31 +249,48 @@ __global__ void __launch_bounds__(352, 1)
         for (int c = 0; c < C::BN; ++c)
           if (kv0 + c > lim) s[c] = -INFINITY;
       }
-      // row max with independent partial maxima (short dependency chains)
+      // row max: eight independent partial maxima over 3-input max steps
       float mx[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) mx[i] = s[i];
+      for (int i = 0; i < 8; ++i) {
+        mx[i] = s[i];
 #pragma unroll
-      for (int c = 8; c < C::BN; ++c) mx[c & 7] = fmaxf(mx[c & 7], s[c]);
-      const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                             fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * sl2;
+        for (int b = 1; b + 1 < C::BN / 8; b += 2) mx[i] = fmax3(mx[i], s[8 * b + i], s[8 * b + 8 + i]);
+        if constexpr ((C::BN / 8) % 2 == 0) mx[i] = fmaxf(mx[i], s[C::BN - 8 + i]);
+      }
+      const float mt = fmaxf(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], fmax3(mx[5], mx[6], mx[7]))) * sl2;
       const float m_new = fmaxf(m_run, mt);
       const bool grow = m_new > m_run + 8.0f;          // also true on the first finite max
       const float m_use = grow ? m_new : m_run;
       const float alpha = grow ? ex2(m_run - m_use) : 1.0f;
       const float msub = (m_use == -INFINITY) ? 0.f : m_use;
       const bool warp_rescale = j > 0 && __any_sync(0xffffffffu, grow);
-      float rsum[4] = {0.f, 0.f, 0.f, 0.f};
+      // P = 2^(S * scale * log2 e - m): packed fp32x2 argument, row sum in four
+      // packed partial sums, bf16 pairs for the PV MMA
+      const uint64_t sl2x2 = f2_pack(sl2, sl2);
+      const uint64_t nm2 = f2_pack(-msub, -msub);
+      uint64_t rs2[4] = {0ull, 0ull, 0ull, 0ull};
       uint32_t pk[C::BN / 2];
 #pragma unroll
       for (int c = 0; c < C::BN; c += 2) {
-        const float p0 = ex2(fmaf(s[c], sl2, -msub));
-        const float p1 = ex2(fmaf(s[c + 1], sl2, -msub));
-        rsum[(c >> 1) & 3] += p0 + p1;
+        float x0, x1;
+        f2_unpack(f2_fma(f2_pack(s[c], s[c + 1]), sl2x2, nm2), x0, x1);
+        const float p0 = ex2(x0), p1 = ex2(x1);
+        rs2[(c >> 1) & 3] = f2_add(rs2[(c >> 1) & 3], f2_pack(p0, p1));
         pk[c / 2] = pack_bf16(p0, p1);
       }
-      l_run = l_run * alpha + ((rsum[0] + rsum[1]) + (rsum[2] + rsum[3]));
+      float r0, r1, r2, r3, r4, r5, r6, r7;
+      f2_unpack(rs2[0], r0, r1);
+      f2_unpack(rs2[1], r2, r3);
+      f2_unpack(rs2[2], r4, r5);
+      f2_unpack(rs2[3], r6, r7);
+      l_run = l_run * alpha + (((r0 + r1) + (r2 + r3)) + ((r4 + r5) + (r6 + r7)));
       m_run = m_use;
+      if (C::SEP_P && j > 0) {
+        // PV(j-1) must be done before O is rescaled and P(j) overwrites P(j-1)
+        if (!mbar_wait(&bar_o[w], (j - 1) & 1, ac)) { ok = false; break; }
+        tc_fence_after();
+      }
       if (warp_rescale) {
 #pragma unroll
         for (int c = 0; c < D; c += 32) {
@@ -247,9 +302,9 @@ __global__ void __launch_bounds__(352, 1)
           tmem_st32(tO + c, r);
         }
       }
-      // P (bf16 pairs) into the first 64 columns of this row's S
-      tmem_st32(tS, pk);
-      tmem_st32(tS + 32, pk + 32);
+      // P (bf16 pairs): 64 packed columns
+      tmem_st32(tP, pk);
+      tmem_st32(tP + 32, pk + 32);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&bar_p[w]);

@@ -389,13 +389,13 @@ def run_ours(args, w, world, rank, local):
 def sparse_logical_bytes(T, H, idx):
     """Logical bytes of the sparse path: gathered KV rows (576 bf16 once per
     token and selected key), Q, O, idx; backward adds dO, dQ and 576 fp32
-    atomic adds per selected key."""
+    atomic adds (4 bytes each) per selected key."""
     pairs = int((idx >= 0).sum().item())
     q_b, o_b = T * H * 576 * 2, T * H * 512 * 2
     idx_b = idx.numel() * 4
     gather = pairs * 576 * 2
     fwd = q_b + gather + idx_b + o_b + T * H * 4
-    bwd = q_b + gather + idx_b + 2 * o_b + T * H * 4 + T * H * 576 * 2 + pairs * 576 * 4 * 2
+    bwd = q_b + gather + idx_b + 2 * o_b + T * H * 4 + T * H * 576 * 2 + pairs * 576 * 4
     return fwd, bwd, pairs
 
 

@@ -1,0 +1,174 @@
+"""GPU tests of the buffer, determinism, graph and error contracts of the C ABI.
+
+- ATTN_DQ_SPLIT gradients are bitwise identical run to run (disjoint partial
+  stores + fixed-order sum), and independent of the workspace contents.
+- Every output element is written: buffers pre-filled with NaN come out
+  finite, and THD padding rows come out as exact zeros (the exact-zero
+  contract of cudnn-frontend #427 for tokens past cu_seqlens[-1]).
+- The launch sequence can be captured in a CUDA graph and replayed with new
+  device-side cu_seqlens contents.
+- Problems only the device sees are reported through the error word.
+"""
+import pytest
+import torch
+
+import oracle
+import softmax_attention_backward_gb300 as A
+from softmax_attention_backward_gb300 import workloads as W
+from _util import assert_close, assert_lse
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda:0") if torch.cuda.is_available() else None
+
+
+def _dense(B=2, S=333, hq=8, hkv=2, D=64, seed=3):
+    return [t.to(DEV) for t in W.dense_inputs(B, S, hq, hkv, D, seed=seed)]
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_split_mode_is_bitwise_deterministic(D):
+    q, k, v, do = _dense(D=D)
+    o, lse = A.attn_fwd(q, k, v, causal=True)
+    runs = []
+    for i in range(5):
+        n = A.attn_bwd_workspace_size(q, k, mode=A.ATTN_DQ_SPLIT, causal=True)
+        ws = torch.full((n,), 0xFF if i % 2 else 0x7F, dtype=torch.uint8, device=DEV)  # NaN-ish junk
+        runs.append(A.dense_backward(q, k, v, o, lse, do, mode=A.ATTN_DQ_SPLIT, causal=True,
+                                     workspace=ws))
+    for r in runs[1:]:
+        for a, b in zip(runs[0], r):
+            assert torch.equal(a, b)
+
+
+def test_outputs_fully_written_dense():
+    q, k, v, do = _dense(B=1, S=200, hq=4, hkv=4, D=128)
+    o = torch.full_like(q, float("nan"))
+    lse = torch.full((1, 4, 200), float("nan"), dtype=torch.float32, device=DEV)
+    A.attn_fwd(q, k, v, causal=True, out=o, lse=lse)
+    assert torch.isfinite(o).all() and torch.isfinite(lse).all()
+    for mode in (A.ATTN_DQ_ATOMIC, A.ATTN_DQ_SPLIT):
+        dq, dk, dv = (torch.full_like(t, float("nan")) for t in (q, k, v))
+        n = A.attn_bwd_workspace_size(q, k, mode=mode, causal=True)
+        ws = torch.full((n,), 0xFF, dtype=torch.uint8, device=DEV)
+        delta = A.attn_bwd_preprocess(q, k, o, do, mode=mode, workspace=ws, causal=True)
+        A.attn_bwd(q, k, v, do, lse, delta, mode=mode, workspace=ws, causal=True, dk=dk, dv=dv)
+        A.attn_bwd_postprocess(q, k, dk, dv, mode=mode, workspace=ws, causal=True, dq=dq)
+        for t in (dq, dk, dv):
+            assert torch.isfinite(t).all()
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_thd_padding_rows_exact_zero_in_nan_buffers(mode):
+    lens = [5, 130, 64]
+    cap = 256
+    cu = W.cu_seqlens_from(lens).to(DEV)
+    q, k, v, do = (t.to(DEV) for t in W.thd_inputs(cap, 4, 2, 64, seed=12))
+    o = torch.full_like(q, float("nan"))
+    lse = torch.full((4, cap), float("nan"), dtype=torch.float32, device=DEV)
+    A.attn_fwd(q, k, v, causal=True, cu_seqlens=cu, max_seqlen=130, out=o, lse=lse)
+    dq, dk, dv = (torch.full_like(t, float("nan")) for t in (q, k, v))
+    n = A.attn_bwd_workspace_size(q, k, mode=mode, causal=True, cu_seqlens=cu, max_seqlen=130)
+    ws = torch.full((n,), 0xFF, dtype=torch.uint8, device=DEV)
+    kw = dict(mode=mode, causal=True, cu_seqlens=cu, max_seqlen=130, workspace=ws)
+    delta = A.attn_bwd_preprocess(q, k, o, do, **kw)
+    A.attn_bwd(q, k, v, do, lse, delta, dk=dk, dv=dv, **kw)
+    A.attn_bwd_postprocess(q, k, dk, dv, dq=dq, **kw)
+    end = sum(lens)
+    for t in (o, dq, dk, dv):
+        assert torch.isfinite(t).all()
+        assert (t[end:] == 0).all()
+    assert torch.isneginf(lse[:, end:]).all() and torch.isfinite(lse[:, :end]).all()
+    ref = oracle.thd_backward(*(t.cpu() for t in (q, k, v, do)), cu.cpu(), 0.125, True)
+    assert_close("dq", dq, ref["dq"])
+    assert_close("dk", dk, ref["dk"])
+
+
+def test_graph_capture_and_replay_with_new_cu_seqlens():
+    cap, H, D = 512, 4, 64
+    q, k, v, do = (t.to(DEV) for t in W.thd_inputs(cap, H, H, D, seed=21))
+    cu = W.cu_seqlens_from([100, 200, 50]).to(DEV)
+    max_seqlen = 300
+    o = torch.empty_like(q)
+    lse = torch.empty(H, cap, dtype=torch.float32, device=DEV)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    n = A.attn_bwd_workspace_size(q, k, mode=A.ATTN_DQ_SPLIT, causal=True, cu_seqlens=cu,
+                                  max_seqlen=max_seqlen)
+    ws = torch.empty(n, dtype=torch.uint8, device=DEV)
+    kw = dict(causal=True, cu_seqlens=cu, max_seqlen=max_seqlen)
+
+    def step():
+        A.attn_fwd(q, k, v, out=o, lse=lse, **kw)
+        delta = A.attn_bwd_preprocess(q, k, o, do, mode=A.ATTN_DQ_SPLIT, workspace=ws, **kw)
+        A.attn_bwd(q, k, v, do, lse, delta, mode=A.ATTN_DQ_SPLIT, workspace=ws, dk=dk, dv=dv, **kw)
+        A.attn_bwd_postprocess(q, k, dk, dv, mode=A.ATTN_DQ_SPLIT, workspace=ws, dq=dq, **kw)
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        step()                                   # warm-up outside the capture
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    for lens in ([100, 200, 50], [300, 1, 120], [17, 0, 260]):
+        cu.copy_(W.cu_seqlens_from(lens).to(DEV))
+        g.replay()
+        torch.cuda.synchronize()
+        ref = oracle.thd_backward(*(t.cpu() for t in (q, k, v, do)), cu.cpu(), 0.125, True)
+        end = sum(lens)
+        assert_close(f"o {lens}", o[:end], ref["o"][:end])
+        assert_lse(f"lse {lens}", lse[:, :end], ref["lse"][:, :end])
+        for key, t in (("dq", dq), ("dk", dk), ("dv", dv)):
+            assert_close(f"{key} {lens}", t, ref[key])
+
+
+def test_sparse_out_of_range_index_is_flagged_and_skipped():
+    T, H, K = 80, 16, 24
+    q, kv, do, idx = W.sparse_inputs(T, H, K, seed=31)
+    bad = idx.clone()
+    bad[50, 3] = T + 7           # out of range
+    bad[60, 0] = -5              # below the -1 sentinel
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    o, lse = A.sparse_attn_fwd(q.to(DEV), kv.to(DEV), bad.to(DEV), error_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & 0x1
+    cleaned = bad.clone()
+    cleaned[(cleaned < -1) | (cleaned >= T)] = -1
+    ref_o, ref_lse = oracle.sparse_forward(q, kv, cleaned, 576 ** -0.5)
+    assert_close("o", o, ref_o)
+    assert_lse("lse", lse, ref_lse)
+
+
+def test_split_mode_flags_sequence_longer_than_max_seqlen():
+    cap, H, D = 384, 2, 64
+    q, k, v, do = (t.to(DEV) for t in W.thd_inputs(cap, H, H, D, seed=41))
+    cu = W.cu_seqlens_from([300, 20]).to(DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    o, lse = A.attn_fwd(q, k, v, causal=True, cu_seqlens=cu, max_seqlen=128)
+    A.dense_backward(q, k, v, o, lse, do, mode=A.ATTN_DQ_SPLIT, causal=True, cu_seqlens=cu,
+                     max_seqlen=128, error_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & 0x4
+
+
+def test_binding_rejects_bad_tensors():
+    q, k, v, _ = _dense(B=1, S=64, hq=2, hkv=2, D=64)
+    with pytest.raises(A.AttnError, match="unsupported"):
+        A.attn_fwd(q[..., :32].contiguous(), k[..., :32].contiguous(), v[..., :32].contiguous())
+    with pytest.raises(ValueError, match="contiguous"):
+        A.attn_fwd(q.transpose(1, 2), k, v)
+    with pytest.raises(TypeError):
+        A.attn_fwd(q.float(), k, v)
+
+
+def test_sparse_outputs_fully_written():
+    T, H, K = 96, 32, 40
+    q, kv, do, idx = (t.to(DEV) for t in W.sparse_inputs(T, H, K, seed=51))
+    o = torch.full((T, H, 512), float("nan"), dtype=torch.bfloat16, device=DEV)
+    lse = torch.full((T, H), float("nan"), dtype=torch.float32, device=DEV)
+    A.sparse_attn_fwd(q, kv, idx, out=o, lse=lse)
+    dq, dkv = torch.full_like(q, float("nan")), torch.full_like(kv, float("nan"))
+    ws = torch.full((A.sparse_attn_bwd_workspace_size(q, idx),), 0xFF, dtype=torch.uint8, device=DEV)
+    A.sparse_attn_bwd(q, kv, idx, o, do, lse, workspace=ws, dq=dq, dkv=dkv)
+    for t in (o, lse, dq, dkv):
+        assert torch.isfinite(t).all()

@@ -5,6 +5,7 @@
 
 #include <cmath>
 #include <cstdint>
+#include <cstring>
 #include <mutex>
 
 #include "attn.h"
@@ -43,6 +44,29 @@ bool make_map(CUtensorMap* m, const void* ptr, int batch, int rows, int heads, i
   cuuint32_t es[4] = {1, 1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box,
             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Map over the fp32 dQ accumulator [batch, heads, rows, dim] (head-major), or
+// over `n_split` such slabs when n_split > 0 (5-D, slab outermost): box of 32
+// dims x 128 rows, 128-byte swizzle, matching the staging layout of the
+// backward kernel.  Rows past `rows` are clipped by the copy.
+bool make_dq_map(CUtensorMap* m, float* acc, int batch, int rows, int heads, int dim, int n_split,
+                 size_t slab_elems) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint32_t rank = n_split > 0 ? 5 : 4;
+  cuuint64_t dims[5] = {static_cast<cuuint64_t>(dim), static_cast<cuuint64_t>(rows),
+                        static_cast<cuuint64_t>(heads), static_cast<cuuint64_t>(batch),
+                        static_cast<cuuint64_t>(n_split > 0 ? n_split : 1)};
+  cuuint64_t strides[4] = {static_cast<cuuint64_t>(dim) * 4,
+                           static_cast<cuuint64_t>(rows) * dim * 4,
+                           static_cast<cuuint64_t>(heads) * rows * dim * 4,
+                           static_cast<cuuint64_t>(slab_elems) * 4};
+  cuuint32_t box[5] = {32, 128, 1, 1, 1};
+  cuuint32_t es[5] = {1, 1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, rank, acc, dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -97,6 +121,20 @@ int n_kv_tiles(const Problem& k) { return (k.max_seqlen + 127) / 128; }
 
 attn_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA; }
 
+// Streaming multiprocessors of the current device (persistent grid size).
+int sm_count() {
+  constexpr int kMaxDevices = 64;
+  static int cached[kMaxDevices] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
 }  // namespace
 }  // namespace attn
 
@@ -143,8 +181,20 @@ attn_status_t attn_fwd(const attn_problem_t* p, const void* q, const void* k, co
   a.lse = lse;
   a.scale_log2 = p->scale * kLog2e;
   const int gx = tile_bound(kp.rows_total, kp.num_seqs, 256, kp.cu_seqlens != nullptr);
-  cudaError_t e = (D == 64) ? launch_attn_fwd<64>(mq, mk, mv, a, gx, st)
-                            : launch_attn_fwd<128>(mq, mk, mv, a, gx, st);
+  const int64_t total = static_cast<int64_t>(gx) * kp.heads_q * kp.batch;
+  if (total >= (int64_t(1) << 31)) return ATTN_ERR_UNSUPPORTED;
+  a.total_items = static_cast<int>(total);
+  a.n_x = gx;
+  // D = 64: one persistent CTA per SM (the next item's query tiles and first
+  // MMAs overlap the current epilogue); D = 128: one CTA per item (its shared
+  // memory holds a single query-pair buffer).
+  const int sms = sm_count();
+  if (sms <= 0) return ATTN_ERR_CUDA;
+  const bool persistent = D == 64 && total > sms;
+  a.x_major = persistent ? 1 : 0;
+  const int grid = persistent ? sms : static_cast<int>(total);
+  cudaError_t e = (D == 64) ? launch_attn_fwd<64>(mq, mk, mv, a, grid, st)
+                            : launch_attn_fwd<128>(mq, mk, mv, a, grid, st);
   if (e == cudaSuccess && kp.cu_seqlens) e = launch_thd_fwd_pad(kp, a.o, lse, D, st);
   return cuda_status(e);
 }
@@ -220,9 +270,34 @@ attn_status_t attn_bwd(const attn_problem_t* p, attn_dq_mode_t mode, const void*
   a.slab_elems = a.split ? dq_elems(kp, D) : 0;
   a.n_split = a.split ? n_kv_tiles(kp) : 0;
   a.scale_log2 = p->scale * kLog2e;
+  // D = 64 stages dQ tiles one query row per thread, which only the swizzled
+  // TMA layout keeps free of bank conflicts.  A THD slab store of a tile that
+  // crosses a sequence end would overwrite the next sequence's rows of the
+  // same slab, so THD + SPLIT keeps the row-exact bulk copy.
+  a.dq_tma = (D == 64 && !(kp.cu_seqlens && a.split)) ? 1 : 0;
+  CUtensorMap mdq, mdk, mdv;
+  memset(&mdq, 0, sizeof(mdq));
+  if (a.dq_tma && !make_dq_map(&mdq, a.dq_acc, kp.batch, kp.rows_total, kp.heads_q, D,
+                               a.split ? a.n_split : 0, a.slab_elems))
+    return ATTN_ERR_CUDA;
+  if (!make_map(&mdk, dk, kp.batch, kp.rows_total, kp.heads_kv, D, 128) ||
+      !make_map(&mdv, dv, kp.batch, kp.rows_total, kp.heads_kv, D, 128))
+    return ATTN_ERR_CUDA;
+  // persistent grid: one CTA per SM over (K/V tile slot x kv head x batch) items
   const int gx = tile_bound(kp.rows_total, kp.num_seqs, 128, kp.cu_seqlens != nullptr);
-  cudaError_t e = (D == 64) ? launch_attn_bwd<64>(mq, mk, mv, mdo, a, gx, st)
-                            : launch_attn_bwd<128>(mq, mk, mv, mdo, a, gx, st);
+  const int64_t total = static_cast<int64_t>(gx) * kp.heads_kv * kp.batch;
+  if (total >= (int64_t(1) << 31)) return ATTN_ERR_UNSUPPORTED;
+  a.total_items = static_cast<int>(total);
+  a.n_x = gx;
+  // One persistent CTA per SM walks the items, so K/V loads and the dK/dV
+  // epilogue of one item overlap the next.
+  const int sms = sm_count();
+  if (sms <= 0) return ATTN_ERR_CUDA;
+  const bool persistent = total > sms;
+  const int grid = persistent ? sms : static_cast<int>(total);
+  a.x_major = persistent ? 1 : 0;
+  cudaError_t e = (D == 64) ? launch_attn_bwd<64>(mq, mk, mv, mdo, mdq, mdk, mdv, a, grid, st)
+                            : launch_attn_bwd<128>(mq, mk, mv, mdo, mdq, mdk, mdv, a, grid, st);
   return cuda_status(e);
 }
 

@@ -3,8 +3,8 @@
 // template, and optimize atomic_add performance for bwd examples",
 // tile-ai/tilelang #940, code-graph section).
 //
-// One CTA owns two 128-row query tiles of one (batch, query head) and streams
-// 128-row K/V tiles through a TMA ring:
+// Work item = two 128-row query tiles of one (batch, query head); the CTA that
+// runs it streams 128-row K/V tiles through a TMA ring:
 //   warp 8        TMA producer (Q once, then K_j, V_j into the ring)
 //   warps 9, 10   MMA issuers, one per query tile w: S_w = Q_w K_j^T (both
 //                 operands in shared memory) and O_w += P_w V_j with P_w read
@@ -21,6 +21,9 @@
 // S_w(j), [P_w(j) ready] PV_w(j), S_w(j+1), ...: MMAs from one thread execute
 // in order, so S_w(j+1) never overwrites P_w(j) before PV_w(j) has read it,
 // and a completed S_w(j+1) also means O_w holds every PV_w up to j.
+// With D = 64 the grid is persistent (one CTA per SM walking a static item
+// list, longest first): the next item's query tiles load into a second buffer
+// and its first S MMAs run while the softmax warps write out the previous O.
 #include <cuda_runtime.h>
 
 #include "launch.h"
@@ -34,7 +37,8 @@ struct FwdCfg {
   static constexpr int Q_BYTES = BM * D * 2;
   static constexpr int KV_BYTES = BN * D * 2;
   static constexpr int NSLOT = (D == 128) ? 5 : 6; // K/V ring slots
-  static constexpr int SMEM = 2 * Q_BYTES + NSLOT * KV_BYTES + 1024;
+  static constexpr int QBUFS = (D == 128) ? 1 : 2; // query-pair buffers (next item prefetch)
+  static constexpr int SMEM = QBUFS * 2 * Q_BYTES + NSLOT * KV_BYTES + 1024;
   static constexpr int THREADS = 352;
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t COL_S0 = 0, COL_S1 = 128, COL_O0 = 256, COL_O1 = 256 + D;
@@ -46,6 +50,58 @@ struct FwdCfg {
   static constexpr uint32_t COL_P1 = SEP_P ? 256 + 2 * D + 64 : COL_S1;
 };
 
+// One work item: the two 128-row query tiles m0 .. m0 + 255 of query head h;
+// tile w meets n_w[w] key/value tiles, the pair n_kv = max of both.
+struct FwdItem {
+  SeqRef seq;
+  int h, m0, n_w[2], n_kv;
+};
+
+// Advances the CTA's round counter `k` to its next valid item (same dealing
+// as the backward: round k takes items k*G .. k*G + G - 1 in snake order).
+// Numbering (`x_major`): 1 = pair slot slowest, so the list runs from the
+// longest items to the shortest; 0 = pair slot fastest within each (batch,
+// head), i.e. blockIdx order of the one-CTA-per-item grid.  Under causal
+// masking the last pair of a sequence is the longest, so slots are reversed.
+template <int BM, int BN>
+__device__ __forceinline__ bool next_fwd_item(const Problem& p, int total, int n_x, int x_major,
+                                              int& k, FwdItem& w) {
+  const int G = gridDim.x, c = blockIdx.x;
+  const int n_bh = p.heads_q * p.batch;
+  for (; k * G < total; ++k) {
+    const int idx = k * G + ((k & 1) ? (G - 1 - c) : c);
+    if (idx >= total) continue;
+    int bh, x;
+    if (x_major) {
+      x = idx / n_bh;
+      bh = idx - x * n_bh;
+    } else {
+      bh = idx / n_x;
+      x = idx - bh * n_x;
+    }
+    w.h = bh % p.heads_q;
+    int pair;
+    if (!decode_tile(p, x, bh / p.heads_q, 2 * BM, w.seq, pair)) continue;
+    if (p.causal) pair = (w.seq.len + 2 * BM - 1) / (2 * BM) - 1 - pair;
+    w.m0 = pair * 2 * BM;
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+      const int r0 = w.m0 + t * BM;
+      if (r0 >= w.seq.len) {
+        w.n_w[t] = 0;
+      } else {
+        const int kv_end = p.causal ? min(w.seq.len, r0 + BM) : w.seq.len;
+        w.n_w[t] = (kv_end + BN - 1) / BN;
+      }
+    }
+    w.n_kv = max(w.n_w[0], w.n_w[1]);
+    if (w.n_kv <= 0) continue;
+    ++k;
+    return true;
+  }
+  return false;
+}
+
 template <int D>
 __global__ void __launch_bounds__(352, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -55,47 +111,27 @@ __global__ void __launch_bounds__(352, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  uint8_t* sQ = smem;                                   // 2 tiles
-  uint8_t* sRing = sQ + 2 * C::Q_BYTES;                 // NSLOT tiles
+  uint8_t* sQ = smem;                                   // QBUFS x 2 tiles
+  uint8_t* sRing = sQ + C::QBUFS * 2 * C::Q_BYTES;      // NSLOT tiles
 
-  __shared__ uint64_t bar_q, bar_full[C::NSLOT], bar_empty[C::NSLOT];
+  __shared__ uint64_t bar_q[C::QBUFS], bar_qempty[C::QBUFS];
+  __shared__ uint64_t bar_full[C::NSLOT], bar_empty[C::NSLOT];
   __shared__ uint64_t bar_s[2], bar_p[2], bar_o[2], bar_sfree[2], bar_stagger;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_flag;
 
   const Problem& p = a.p;
   const int warp = warp_id();
+  const int total = a.total_items;
   AbortCtx ac{&abort_flag, p.err};
-
-  // ---- work decode ---------------------------------------------------------
-  SeqRef seq;
-  int pair;
-  const int h = blockIdx.y;
-  if (!decode_tile(p, blockIdx.x, blockIdx.z, 2 * C::BM, seq, pair)) return;
-  {
-    // heaviest (last) pairs first under causal masking
-    const int npairs = (seq.len + 2 * C::BM - 1) / (2 * C::BM);
-    if (p.causal) pair = npairs - 1 - pair;
-  }
-  const int hk = h / (p.heads_q / p.heads_kv);
-  const int m0 = pair * 2 * C::BM;
-  int n_w[2];
-#pragma unroll
-  for (int w = 0; w < 2; ++w) {
-    const int r0 = m0 + w * C::BM;
-    if (r0 >= seq.len) {
-      n_w[w] = 0;
-    } else {
-      const int kv_end = p.causal ? min(seq.len, r0 + C::BM) : seq.len;
-      n_w[w] = (kv_end + C::BN - 1) / C::BN;
-    }
-  }
-  const int n_kv = max(n_w[0], n_w[1]);
 
   // ---- setup ---------------------------------------------------------------
   if (threadIdx.x == 0) {
     abort_flag = 0;
-    mbar_init(&bar_q, 1);
+    for (int b = 0; b < C::QBUFS; ++b) {
+      mbar_init(&bar_q[b], 1);
+      mbar_init(&bar_qempty[b], 2);      // released by both issuers
+    }
     for (int i = 0; i < C::NSLOT; ++i) {
       mbar_init(&bar_full[i], 1);
       mbar_init(&bar_empty[i], 2);       // released by both issuers
@@ -121,227 +157,267 @@ __global__ void __launch_bounds__(352, 1)
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
-      const int row_base = seq.row0;
-      mbar_arrive_expect_tx(&bar_q, 2 * C::Q_BYTES);
-      for (int w = 0; w < 2; ++w)
-        for (int pn = 0; pn < PANELS; ++pn)
-          tma_load_4d(&tmQ, &bar_q, sQ + w * C::Q_BYTES + pn * C::BM * 128, pn * 64, h,
-                      row_base + m0 + w * C::BM, seq.b);
-      for (int i = 0; i < 2 * n_kv; ++i) {
-        const int slot = i % C::NSLOT;
-        const int use = i / C::NSLOT;
-        if (!mbar_wait(&bar_empty[slot], (use & 1) ^ 1, ac)) break;
-        const CUtensorMap* m = (i & 1) ? &tmV : &tmK;
-        uint8_t* dst = sRing + slot * C::KV_BYTES;
-        mbar_arrive_expect_tx(&bar_full[slot], C::KV_BYTES);
-        for (int pn = 0; pn < PANELS; ++pn)
-          tma_load_4d(m, &bar_full[slot], dst + pn * C::BN * 128, pn * 64, hk,
-                      row_base + (i >> 1) * C::BN, seq.b);
+      FwdItem w;
+      int k = 0, ic = 0, gring = 0;
+      bool ok = true;
+      while (ok && next_fwd_item<C::BM, C::BN>(p, total, a.n_x, a.x_major, k, w)) {
+        const int hk = w.h / (p.heads_q / p.heads_kv);
+        const int qb = ic % C::QBUFS, qu = ic / C::QBUFS;
+        if (!mbar_wait(&bar_qempty[qb], (qu & 1) ^ 1, ac)) break;
+        mbar_arrive_expect_tx(&bar_q[qb], 2 * C::Q_BYTES);
+        for (int t = 0; t < 2; ++t)
+          for (int pn = 0; pn < PANELS; ++pn)
+            tma_load_4d(&tmQ, &bar_q[qb], sQ + (qb * 2 + t) * C::Q_BYTES + pn * C::BM * 128,
+                        pn * 64, w.h, w.seq.row0 + w.m0 + t * C::BM, w.seq.b);
+        for (int i = 0; i < 2 * w.n_kv; ++i) {
+          const int gi = gring + i;
+          const int slot = gi % C::NSLOT, use = gi / C::NSLOT;
+          if (!mbar_wait(&bar_empty[slot], (use & 1) ^ 1, ac)) { ok = false; break; }
+          const CUtensorMap* m = (i & 1) ? &tmV : &tmK;
+          uint8_t* dst = sRing + slot * C::KV_BYTES;
+          mbar_arrive_expect_tx(&bar_full[slot], C::KV_BYTES);
+          for (int pn = 0; pn < PANELS; ++pn)
+            tma_load_4d(m, &bar_full[slot], dst + pn * C::BN * 128, pn * 64, hk,
+                        w.seq.row0 + (i >> 1) * C::BN, w.seq.b);
+        }
+        gring += 2 * w.n_kv;
+        ++ic;
       }
     }
   } else if (warp == 9 || warp == 10) {
-    // ---------------- MMA issuer of query tile w ----------------
-    const int w = warp - 9;
+    // ---------------- MMA issuer of query tile t ----------------
+    const int t = warp - 9;
     if (lane_id() == 0) {
       const uint32_t idS = idesc_bf16(C::BM, C::BN, false, false);
       const uint32_t idO = idesc_bf16(C::BM, D, false, true);
-      const uint64_t dQw = desc_kmajor_base(smem_u32(sQ + w * C::Q_BYTES));
       const uint64_t dR_k0 = desc_kmajor_base(smem_u32(sRing));
       const uint64_t dR_mn0 = desc_mnmajor_base(smem_u32(sRing), C::BN);
-      const uint32_t tS = tmem + (w ? C::COL_S1 : C::COL_S0);
-      const uint32_t tO = tmem + (w ? C::COL_O1 : C::COL_O0);
-      const uint32_t tP = tmem + (w ? C::COL_P1 : C::COL_P0);
-      const int nt = n_w[w];
-      bool ok = mbar_wait(&bar_q, 0, ac);
-      // Tile 1 starts one softmax phase after tile 0 (when P_0(0) is ready), so
-      // that one tile's softmax overlaps the other tile's MMAs instead of both
-      // running in lockstep.  bar_stagger completes exactly once.
-      if (w == 1 && ok) ok = mbar_wait(&bar_stagger, 0, ac);
-      auto issue_s = [&](int j) -> bool {
-        const int ik = 2 * j, sk = ik % C::NSLOT;
-        if (!mbar_wait(&bar_full[sk], (ik / C::NSLOT) & 1, ac)) return false;
-        tc_fence_after();
-        const uint64_t kd = desc_advance(dR_k0, sk * C::KV_BYTES);
+      const uint32_t tS = tmem + (t ? C::COL_S1 : C::COL_S0);
+      const uint32_t tO = tmem + (t ? C::COL_O1 : C::COL_O0);
+      const uint32_t tP = tmem + (t ? C::COL_P1 : C::COL_P0);
+      FwdItem w;
+      int k = 0, ic = 0, gring = 0, cs = 0;   // cs: S tiles of this query tile so far
+      bool ok = true;
+      while (ok && next_fwd_item<C::BM, C::BN>(p, total, a.n_x, a.x_major, k, w)) {
+        const int qb = ic % C::QBUFS, qu = ic / C::QBUFS;
+        const int nt = w.n_w[t];
+        if (!mbar_wait(&bar_q[qb], qu & 1, ac)) break;
+        // Tile 1 starts one softmax phase after tile 0 (when P_0(0) of the
+        // first item is ready), so that one tile's softmax overlaps the other
+        // tile's MMAs instead of both running in lockstep.  bar_stagger
+        // completes exactly once.
+        if (t == 1 && ic == 0 && !mbar_wait(&bar_stagger, 0, ac)) break;
+        const uint64_t dQt = desc_kmajor_base(smem_u32(sQ + (qb * 2 + t) * C::Q_BYTES));
+        auto issue_s = [&](int j) -> bool {
+          const int gi = gring + 2 * j, sk = gi % C::NSLOT;
+          if (!mbar_wait(&bar_full[sk], (gi / C::NSLOT) & 1, ac)) return false;
+          tc_fence_after();
+          const uint64_t kd = desc_advance(dR_k0, sk * C::KV_BYTES);
 #pragma unroll
-        for (int k = 0; k < D / 16; ++k)
-          umma_ss(tS, desc_advance(dQw, kmajor_step_bytes(C::BM, k)),
-                  desc_advance(kd, kmajor_step_bytes(C::BN, k)), idS, k > 0);
-        umma_commit(&bar_s[w]);
-        umma_commit(&bar_empty[sk]);
-        return true;
-      };
-      auto issue_pv = [&](int j) -> bool {
-        const int iv = 2 * j + 1, sv = iv % C::NSLOT;
-        if (!mbar_wait(&bar_full[sv], (iv / C::NSLOT) & 1, ac)) return false;
-        if (!mbar_wait(&bar_p[w], j & 1, ac)) return false;
-        if (w == 0 && j == 0) mbar_arrive(&bar_stagger);
-        tc_fence_after();
-        const uint64_t vd = desc_advance(dR_mn0, sv * C::KV_BYTES);
+          for (int kk = 0; kk < D / 16; ++kk)
+            umma_ss(tS, desc_advance(dQt, kmajor_step_bytes(C::BM, kk)),
+                    desc_advance(kd, kmajor_step_bytes(C::BN, kk)), idS, kk > 0);
+          umma_commit(&bar_s[t]);
+          umma_commit(&bar_empty[sk]);
+          return true;
+        };
+        auto issue_pv = [&](int j) -> bool {
+          const int gi = gring + 2 * j + 1, sv = gi % C::NSLOT;
+          if (!mbar_wait(&bar_full[sv], (gi / C::NSLOT) & 1, ac)) return false;
+          if (!mbar_wait(&bar_p[t], (cs + j) & 1, ac)) return false;
+          if (t == 0 && ic == 0 && j == 0) mbar_arrive(&bar_stagger);
+          tc_fence_after();
+          const uint64_t vd = desc_advance(dR_mn0, sv * C::KV_BYTES);
 #pragma unroll
-        for (int k = 0; k < C::BN / 16; ++k)   // P: 8 packed columns per 16 keys
-          umma_ts(tO, tP + 8 * k, desc_advance(vd, mnmajor_step_bytes(k)), idO,
-                  (j > 0 || k > 0) ? 1u : 0u);
-        umma_commit(&bar_o[w]);
-        umma_commit(&bar_empty[sv]);
-        return true;
-      };
-      // release a ring slot this tile does not use (both issuers release each)
-      auto skip = [&](int i) -> bool {
-        if (!mbar_wait(&bar_full[i % C::NSLOT], (i / C::NSLOT) & 1, ac)) return false;
-        mbar_arrive(&bar_empty[i % C::NSLOT]);
-        return true;
-      };
-      if (C::SEP_P) {
-        // S(j+1) as soon as the softmax has read S(j); PV(j) once P(j) is ready
-        if (ok && nt > 0) ok = issue_s(0);
-        for (int j = 0; ok && j < nt; ++j) {
-          if (j + 1 < nt) {
-            if (!mbar_wait(&bar_sfree[w], j & 1, ac) || !issue_s(j + 1)) break;
+          for (int kk = 0; kk < C::BN / 16; ++kk)   // P: 8 packed columns per 16 keys
+            umma_ts(tO, tP + 8 * kk, desc_advance(vd, mnmajor_step_bytes(kk)), idO,
+                    (j > 0 || kk > 0) ? 1u : 0u);
+          umma_commit(&bar_o[t]);
+          umma_commit(&bar_empty[sv]);
+          return true;
+        };
+        // release a ring slot this tile does not use (both issuers release each)
+        auto skip = [&](int i) -> bool {
+          const int gi = gring + i;
+          if (!mbar_wait(&bar_full[gi % C::NSLOT], (gi / C::NSLOT) & 1, ac)) return false;
+          mbar_arrive(&bar_empty[gi % C::NSLOT]);
+          return true;
+        };
+        if (C::SEP_P) {
+          // S(j+1) as soon as the softmax has read S(j); PV(j) once P(j) is
+          // ready.  S(0) of an item waits for the read of the previous S.
+          for (int j = 0; ok && j < nt; ++j) {
+            if (j == 0) {
+              if (cs > 0 && !mbar_wait(&bar_sfree[t], (cs - 1) & 1, ac)) { ok = false; break; }
+              if (!issue_s(0)) { ok = false; break; }
+            }
+            if (j + 1 < nt) {
+              if (!mbar_wait(&bar_sfree[t], (cs + j) & 1, ac) || !issue_s(j + 1)) {
+                ok = false;
+                break;
+              }
+            }
+            if (!issue_pv(j)) ok = false;
           }
-          if (!issue_pv(j)) break;
+        } else {
+          // S(j), PV(j), S(j+1), ...: MMAs of one thread execute in order, so
+          // S(j+1) cannot overwrite P(j) (stored over S) before PV(j) read it
+          for (int j = 0; ok && j < nt; ++j)
+            if (!issue_s(j) || !issue_pv(j)) ok = false;
         }
-      } else {
-        // S(j), PV(j), S(j+1), ...: MMAs of one thread execute in order, so
-        // S(j+1) cannot overwrite P(j) (stored over S) before PV(j) read it
-        for (int j = 0; ok && j < nt; ++j)
-          if (!issue_s(j) || !issue_pv(j)) ok = false;
+        // the query tile is free once this tile's S MMAs have completed
+        if (ok) {
+          if (nt > 0) umma_commit(&bar_qempty[qb]);
+          else mbar_arrive(&bar_qempty[qb]);
+        }
+        for (int j = nt; ok && j < w.n_kv; ++j)
+          if (!skip(2 * j) || !skip(2 * j + 1)) ok = false;
+        gring += 2 * w.n_kv;
+        cs += nt;
+        ++ic;
       }
-      for (int j = nt; ok && j < n_kv; ++j)
-        if (!skip(2 * j) || !skip(2 * j + 1)) ok = false;
     }
   } else {
     // ---------------- softmax warpgroups ----------------
-    const int w = warp >> 2;                 // query tile of this warpgroup
-    const int t = threadIdx.x & 127;         // row within the tile == TMEM lane
+    const int t = warp >> 2;                 // query tile of this warpgroup
+    const int tr = threadIdx.x & 127;        // row within the tile == TMEM lane
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const uint32_t tS = tmem + lane_base + (w ? C::COL_S1 : C::COL_S0);
-    const uint32_t tO = tmem + lane_base + (w ? C::COL_O1 : C::COL_O0);
-    const uint32_t tP = tmem + lane_base + (w ? C::COL_P1 : C::COL_P0);
-    const int row = m0 + w * C::BM + t;      // row inside the sequence
-    const int nt = n_w[w];
+    const uint32_t tS = tmem + lane_base + (t ? C::COL_S1 : C::COL_S0);
+    const uint32_t tO = tmem + lane_base + (t ? C::COL_O1 : C::COL_O0);
+    const uint32_t tP = tmem + lane_base + (t ? C::COL_P1 : C::COL_P0);
     const float sl2 = a.scale_log2;
-    float m_run = -INFINITY, l_run = 0.f;
+    FwdItem w;
+    int k = 0, cs = 0;
     bool ok = true;
-    for (int j = 0; j < nt; ++j) {
-      // without a separate P region, S_w(j) complete also means PV_w(j-1) is
-      // complete (same issuer, in order)
-      if (!mbar_wait(&bar_s[w], j & 1, ac)) { ok = false; break; }
-      tc_fence_after();
-      float s[C::BN];
-      {
-        uint32_t u[C::BN];
-#pragma unroll
-        for (int c = 0; c < C::BN; c += 32) tmem_ld32_nowait(tS + c, u + c);
-        tmem_wait_ld();
-        if (C::SEP_P) {
-          tc_fence_before();
-          mbar_arrive(&bar_sfree[w]);
-        }
-#pragma unroll
-        for (int c = 0; c < C::BN; ++c) s[c] = __uint_as_float(u[c]);
-      }
-      const int kv0 = j * C::BN;
-      const bool need_mask =
-          (kv0 + C::BN > seq.len) || (p.causal && kv0 + C::BN - 1 > m0 + w * C::BM);
-      if (need_mask) {
-        const int lim = p.causal ? min(seq.len - 1, row) : seq.len - 1;
-#pragma unroll
-        for (int c = 0; c < C::BN; ++c)
-          if (kv0 + c > lim) s[c] = -INFINITY;
-      }
-      // row max: eight independent partial maxima over 3-input max steps
-      float mx[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        mx[i] = s[i];
-#pragma unroll
-        for (int b = 1; b + 1 < C::BN / 8; b += 2) mx[i] = fmax3(mx[i], s[8 * b + i], s[8 * b + 8 + i]);
-        if constexpr ((C::BN / 8) % 2 == 0) mx[i] = fmaxf(mx[i], s[C::BN - 8 + i]);
-      }
-      const float mt = fmaxf(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], fmax3(mx[5], mx[6], mx[7]))) * sl2;
-      const float m_new = fmaxf(m_run, mt);
-      const bool grow = m_new > m_run + 8.0f;          // also true on the first finite max
-      const float m_use = grow ? m_new : m_run;
-      const float alpha = grow ? ex2(m_run - m_use) : 1.0f;
-      const float msub = (m_use == -INFINITY) ? 0.f : m_use;
-      const bool warp_rescale = j > 0 && __any_sync(0xffffffffu, grow);
-      // P = 2^(S * scale * log2 e - m): packed fp32x2 argument, row sum in four
-      // packed partial sums, bf16 pairs for the PV MMA
-      const uint64_t sl2x2 = f2_pack(sl2, sl2);
-      const uint64_t nm2 = f2_pack(-msub, -msub);
-      uint64_t rs2[4] = {0ull, 0ull, 0ull, 0ull};
-      uint32_t pk[C::BN / 2];
-#pragma unroll
-      for (int c = 0; c < C::BN; c += 2) {
-        float x0, x1;
-        f2_unpack(f2_fma(f2_pack(s[c], s[c + 1]), sl2x2, nm2), x0, x1);
-        const float p0 = ex2(x0), p1 = ex2(x1);
-        rs2[(c >> 1) & 3] = f2_add(rs2[(c >> 1) & 3], f2_pack(p0, p1));
-        pk[c / 2] = pack_bf16(p0, p1);
-      }
-      float r0, r1, r2, r3, r4, r5, r6, r7;
-      f2_unpack(rs2[0], r0, r1);
-      f2_unpack(rs2[1], r2, r3);
-      f2_unpack(rs2[2], r4, r5);
-      f2_unpack(rs2[3], r6, r7);
-      l_run = l_run * alpha + (((r0 + r1) + (r2 + r3)) + ((r4 + r5) + (r6 + r7)));
-      m_run = m_use;
-      if (C::SEP_P && j > 0) {
-        // PV(j-1) must be done before O is rescaled and P(j) overwrites P(j-1)
-        if (!mbar_wait(&bar_o[w], (j - 1) & 1, ac)) { ok = false; break; }
+    while (ok && next_fwd_item<C::BM, C::BN>(p, total, a.n_x, a.x_major, k, w)) {
+      const int row = w.m0 + t * C::BM + tr;   // row inside the sequence
+      const int nt = w.n_w[t];
+      float m_run = -INFINITY, l_run = 0.f;
+      for (int j = 0; j < nt; ++j) {
+        const int c = cs + j;
+        // without a separate P region, S_t(j) complete also means PV_t(j-1) is
+        // complete (same issuer, in order)
+        if (!mbar_wait(&bar_s[t], c & 1, ac)) { ok = false; break; }
         tc_fence_after();
-      }
-      if (warp_rescale) {
+        float s[C::BN];
+        {
+          uint32_t u[C::BN];
 #pragma unroll
-        for (int c = 0; c < D; c += 32) {
-          uint32_t r[32];
-          tmem_ld32_nowait(tO + c, r);
+          for (int cc = 0; cc < C::BN; cc += 32) tmem_ld32_nowait(tS + cc, u + cc);
           tmem_wait_ld();
+          if (C::SEP_P) {
+            tc_fence_before();
+            mbar_arrive(&bar_sfree[t]);
+          }
 #pragma unroll
-          for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-          tmem_st32(tO + c, r);
+          for (int cc = 0; cc < C::BN; ++cc) s[cc] = __uint_as_float(u[cc]);
         }
-      }
-      // P (bf16 pairs): 64 packed columns
-      tmem_st32(tP, pk);
-      tmem_st32(tP + 32, pk + 32);
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(&bar_p[w]);
-    }
-    // ---- epilogue: O / l, LSE ----
-    if (ok && nt > 0 && mbar_wait(&bar_o[w], (nt - 1) & 1, ac)) {
-      tc_fence_after();
-      const bool valid = row < seq.len;
-      const float inv_l = (l_run > 0.f) ? 1.0f / l_run : 0.f;
-      const size_t grow_idx = (static_cast<size_t>(seq.b) * p.rows_total + seq.row0 + row);
-      __nv_bfloat16* orow = a.o + (grow_idx * p.heads_q + h) * D;
+        const int kv0 = j * C::BN;
+        const bool need_mask =
+            (kv0 + C::BN > w.seq.len) || (p.causal && kv0 + C::BN - 1 > w.m0 + t * C::BM);
+        if (need_mask) {
+          const int lim = p.causal ? min(w.seq.len - 1, row) : w.seq.len - 1;
 #pragma unroll
-      for (int c = 0; c < D; c += 32) {
-        uint32_t r[32];
-        tmem_ld32_nowait(tO + c, r);
-        tmem_wait_ld();
-        if (valid) {
+          for (int cc = 0; cc < C::BN; ++cc)
+            if (kv0 + cc > lim) s[cc] = -INFINITY;
+        }
+        // row max: eight independent partial maxima over 3-input max steps
+        float mx[8];
 #pragma unroll
-          for (int i = 0; i < 32; i += 8) {
-            uint4 v;
-            v.x = pack_bf16(__uint_as_float(r[i + 0]) * inv_l, __uint_as_float(r[i + 1]) * inv_l);
-            v.y = pack_bf16(__uint_as_float(r[i + 2]) * inv_l, __uint_as_float(r[i + 3]) * inv_l);
-            v.z = pack_bf16(__uint_as_float(r[i + 4]) * inv_l, __uint_as_float(r[i + 5]) * inv_l);
-            v.w = pack_bf16(__uint_as_float(r[i + 6]) * inv_l, __uint_as_float(r[i + 7]) * inv_l);
-            *reinterpret_cast<uint4*>(orow + c + i) = v;
+        for (int i = 0; i < 8; ++i) {
+          mx[i] = s[i];
+#pragma unroll
+          for (int b = 1; b + 1 < C::BN / 8; b += 2) mx[i] = fmax3(mx[i], s[8 * b + i], s[8 * b + 8 + i]);
+          if constexpr ((C::BN / 8) % 2 == 0) mx[i] = fmaxf(mx[i], s[C::BN - 8 + i]);
+        }
+        const float mt =
+            fmaxf(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], fmax3(mx[5], mx[6], mx[7]))) * sl2;
+        const float m_new = fmaxf(m_run, mt);
+        const bool grow = m_new > m_run + 8.0f;          // also true on the first finite max
+        const float m_use = grow ? m_new : m_run;
+        const float alpha = grow ? ex2(m_run - m_use) : 1.0f;
+        const float msub = (m_use == -INFINITY) ? 0.f : m_use;
+        const bool warp_rescale = j > 0 && __any_sync(0xffffffffu, grow);
+        // P = 2^(S * scale * log2 e - m): packed fp32x2 argument, row sum in
+        // four packed partial sums, bf16 pairs for the PV MMA
+        const uint64_t sl2x2 = f2_pack(sl2, sl2);
+        const uint64_t nm2 = f2_pack(-msub, -msub);
+        uint64_t rs2[4] = {0ull, 0ull, 0ull, 0ull};
+        uint32_t pk[C::BN / 2];
+#pragma unroll
+        for (int cc = 0; cc < C::BN; cc += 2) {
+          float x0, x1;
+          f2_unpack(f2_fma(f2_pack(s[cc], s[cc + 1]), sl2x2, nm2), x0, x1);
+          const float p0 = ex2(x0), p1 = ex2(x1);
+          rs2[(cc >> 1) & 3] = f2_add(rs2[(cc >> 1) & 3], f2_pack(p0, p1));
+          pk[cc / 2] = pack_bf16(p0, p1);
+        }
+        float r0, r1, r2, r3, r4, r5, r6, r7;
+        f2_unpack(rs2[0], r0, r1);
+        f2_unpack(rs2[1], r2, r3);
+        f2_unpack(rs2[2], r4, r5);
+        f2_unpack(rs2[3], r6, r7);
+        l_run = l_run * alpha + (((r0 + r1) + (r2 + r3)) + ((r4 + r5) + (r6 + r7)));
+        m_run = m_use;
+        if (C::SEP_P && j > 0) {
+          // PV(j-1) must be done before O is rescaled and P(j) overwrites P(j-1)
+          if (!mbar_wait(&bar_o[t], (c - 1) & 1, ac)) { ok = false; break; }
+          tc_fence_after();
+        }
+        if (warp_rescale) {
+#pragma unroll
+          for (int cc = 0; cc < D; cc += 32) {
+            uint32_t r[32];
+            tmem_ld32_nowait(tO + cc, r);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+            tmem_st32(tO + cc, r);
           }
         }
+        // P (bf16 pairs): 64 packed columns
+        tmem_st32(tP, pk);
+        tmem_st32(tP + 32, pk + 32);
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&bar_p[t]);
       }
-      if (valid) {
-        const float lse = (l_run > 0.f) ? (m_run + __log2f(l_run)) * kLn2 : -INFINITY;
-        size_t li;
-        if (p.cu_seqlens)
-          li = static_cast<size_t>(h) * p.rows_total + seq.row0 + row;
-        else
-          li = (static_cast<size_t>(seq.b) * p.heads_q + h) * p.rows_total + row;
-        a.lse[li] = lse;
+      // ---- epilogue: O / l, LSE (the next item's first PV waits for the P
+      // this warpgroup writes after reading O here) ----
+      if (ok && nt > 0 && mbar_wait(&bar_o[t], (cs + nt - 1) & 1, ac)) {
+        tc_fence_after();
+        const bool valid = row < w.seq.len;
+        const float inv_l = (l_run > 0.f) ? 1.0f / l_run : 0.f;
+        const size_t grow_idx = (static_cast<size_t>(w.seq.b) * p.rows_total + w.seq.row0 + row);
+        __nv_bfloat16* orow = a.o + (grow_idx * p.heads_q + w.h) * D;
+#pragma unroll
+        for (int cc = 0; cc < D; cc += 32) {
+          uint32_t r[32];
+          tmem_ld32_nowait(tO + cc, r);
+          tmem_wait_ld();
+          if (valid) {
+#pragma unroll
+            for (int i = 0; i < 32; i += 8) {
+              uint4 v;
+              v.x = pack_bf16(__uint_as_float(r[i + 0]) * inv_l, __uint_as_float(r[i + 1]) * inv_l);
+              v.y = pack_bf16(__uint_as_float(r[i + 2]) * inv_l, __uint_as_float(r[i + 3]) * inv_l);
+              v.z = pack_bf16(__uint_as_float(r[i + 4]) * inv_l, __uint_as_float(r[i + 5]) * inv_l);
+              v.w = pack_bf16(__uint_as_float(r[i + 6]) * inv_l, __uint_as_float(r[i + 7]) * inv_l);
+              *reinterpret_cast<uint4*>(orow + cc + i) = v;
+            }
+          }
+        }
+        if (valid) {
+          const float lse = (l_run > 0.f) ? (m_run + __log2f(l_run)) * kLn2 : -INFINITY;
+          size_t li;
+          if (p.cu_seqlens)
+            li = static_cast<size_t>(w.h) * p.rows_total + w.seq.row0 + row;
+          else
+            li = (static_cast<size_t>(w.seq.b) * p.heads_q + w.h) * p.rows_total + row;
+          a.lse[li] = lse;
+        }
       }
+      cs += nt;
     }
   }
 
@@ -377,8 +453,7 @@ cudaError_t launch_attn_fwd(const CUtensorMap& q, const CUtensorMap& k, const CU
   auto kern = attn_fwd_kernel<D>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
-  dim3 grid(grid_x, a.p.heads_q, a.p.batch);
-  kern<<<grid, C::THREADS, C::SMEM, st>>>(q, k, v, a);
+  kern<<<grid_x, C::THREADS, C::SMEM, st>>>(q, k, v, a);
   return cudaGetLastError();
 }
 

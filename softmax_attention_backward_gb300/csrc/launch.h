@@ -13,6 +13,9 @@ struct FwdArgs {
   __nv_bfloat16* o;
   float* lse;
   float scale_log2;
+  int total_items;      // work items: query-tile-pair slots x heads x batch
+  int n_x;              // query-tile-pair slots per (batch, head)
+  int x_major;          // item numbering, see next_fwd_item
 };
 
 struct BwdArgs {
@@ -25,6 +28,10 @@ struct BwdArgs {
   size_t slab_elems;    // SPLIT: elements per slab (0 for ATOMIC)
   int n_split;          // SPLIT: number of slabs
   int split;            // 1 = SPLIT
+  int dq_tma;           // 1 = dQ tiles leave through the swizzled TMA map of the accumulator
+  int total_items;      // work items: K/V tile slots x kv heads x batch
+  int n_x;              // K/V tile slots per (batch, kv head)
+  int x_major;          // item numbering, see next_bwd_item
   float scale_log2;
 };
 
@@ -35,7 +42,8 @@ cudaError_t launch_thd_fwd_pad(const Problem& p, __nv_bfloat16* o, float* lse, i
                                cudaStream_t st);
 template <int D>
 cudaError_t launch_attn_bwd(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
-                            const CUtensorMap& dO, const BwdArgs& a, int grid_x, cudaStream_t st);
+                            const CUtensorMap& dO, const CUtensorMap& dq, const CUtensorMap& dk,
+                            const CUtensorMap& dv, const BwdArgs& a, int grid, cudaStream_t st);
 template <int D>
 cudaError_t launch_bwd_preprocess(const Problem& p, const __nv_bfloat16* o,
                                   const __nv_bfloat16* dout, float* delta, float* dq_acc,

@@ -301,8 +301,11 @@ def run_ours(args, w, world, rank, local):
         fwd = [e[0].elapsed_time(e[1]) for e in evs]
         bwd = [e[1].elapsed_time(e[4]) for e in evs]
         main = [e[2].elapsed_time(e[3]) for e in evs]
+        pre = [e[1].elapsed_time(e[2]) for e in evs]
+        post = [e[3].elapsed_time(e[4]) for e in evs]
         return {k_: sum(v_) / steps for k_, v_ in
-                (("total", tot), ("fwd", fwd), ("bwd", bwd), ("bwd_main", main))}
+                (("total", tot), ("fwd", fwd), ("bwd", bwd), ("bwd_main", main), ("pre", pre),
+                 ("post", post))}
 
     # warm-up (both modes), then the timed atomic-mode steps with clocks sampled
     for _ in range(args.warmup):
@@ -321,32 +324,71 @@ def run_ours(args, w, world, rank, local):
     ms_split = reduce_max(t_split["total"], world) if t_split else None
     ms_split_bwd = reduce_max(t_split["bwd"], world) if t_split else None
 
-    # end to end through the public API: pinned host inputs -> device -> results -> host
-    hq, hk, hv, hdo = (x[n].pin_memory() for n in ("q", "k", "v", "do"))
-    out_h = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (dq, dk, dv)]
-    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo))
-    d2h = sum(t.numel() * t.element_size() for t in out_h)
+    # end to end through the public API: pinned host inputs -> device -> results
+    # -> host, every step.  Three streams overlap step i's compute with the
+    # host->device copy of step i+1's inputs and the device->host copy of step
+    # i-1's gradients (inputs and gradients double-buffered on the device and
+    # on the host).
+    hin = [[x[n].pin_memory() for n in ("q", "k", "v", "do")]]
+    hin.append([t.clone().pin_memory() for t in hin[0]])
+    dins = [[q, k, v, do], [torch.empty_like(t) for t in (q, k, v, do)]]
+    douts = [[dq, dk, dv], [torch.empty_like(t) for t in (dq, dk, dv)]]
+    hout = [[torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (dq, dk, dv)]
+            for _ in range(2)]
+    h2d = sum(t.numel() * t.element_size() for t in hin[0])
+    d2h = sum(t.numel() * t.element_size() for t in hout[0])
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev = lambda: torch.cuda.Event()
+    in_ready = [ev(), ev()]
+    in_free = [ev(), ev()]
+    out_ready = [ev(), ev()]
+    out_free = [ev(), ev()]
+    for e_ in in_free + out_free:
+        e_.record(stream)
 
-    def e2e_step():
-        q.copy_(hq, non_blocking=True)
-        k.copy_(hk, non_blocking=True)
-        v.copy_(hv, non_blocking=True)
-        do.copy_(hdo, non_blocking=True)
-        step(A.ATTN_DQ_ATOMIC)
-        for h, d in zip(out_h, (dq, dk, dv)):
-            h.copy_(d, non_blocking=True)
+    def e2e_step(i):
+        b = i & 1
+        qi, ki, vi, doi = dins[b]
+        dqi, dki, dvi = douts[b]
+        with torch.cuda.stream(s_in):
+            s_in.wait_event(in_free[b])
+            for d_, h_ in zip(dins[b], hin[b]):
+                d_.copy_(h_, non_blocking=True)
+            in_ready[b].record(s_in)
+        stream.wait_event(in_ready[b])
+        stream.wait_event(out_free[b])
+        A.attn_fwd(qi, ki, vi, out=o, lse=lse, stream=stream, **kw)
+        A.attn_bwd_preprocess(qi, ki, o, doi, mode=A.ATTN_DQ_ATOMIC, workspace=ws[A.ATTN_DQ_ATOMIC],
+                              delta=delta, stream=stream, **kw)
+        A.attn_bwd(qi, ki, vi, doi, lse, delta, mode=A.ATTN_DQ_ATOMIC,
+                   workspace=ws[A.ATTN_DQ_ATOMIC], dk=dki, dv=dvi, stream=stream, **kw)
+        A.attn_bwd_postprocess(qi, ki, dki, dvi, mode=A.ATTN_DQ_ATOMIC,
+                               workspace=ws[A.ATTN_DQ_ATOMIC], dq=dqi, stream=stream, **kw)
+        in_free[b].record(stream)
+        out_ready[b].record(stream)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(out_ready[b])
+            for h_, d_ in zip(hout[b], douts[b]):
+                h_.copy_(d_, non_blocking=True)
+            out_free[b].record(s_out)
 
-    for _ in range(max(1, args.warmup)):
-        e2e_step()
+    for i in range(max(1, args.warmup)):
+        e2e_step(i)
     torch.cuda.synchronize()
     barrier(world)
     e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e_start.record(stream)
-    for _ in range(args.steps):
-        e2e_step()
+    s_in.wait_stream(stream)
+    s_out.wait_stream(stream)
+    for i in range(args.steps):
+        e2e_step(i)
+    stream.wait_stream(s_out)
     e_end.record(stream)
     torch.cuda.synchronize()
     ms_e2e = reduce_max(e_start.elapsed_time(e_end) / args.steps, world)
+    # the last step's gradients must have reached the host intact
+    for h_, d_ in zip(hout[(args.steps - 1) & 1], douts[(args.steps - 1) & 1]):
+        assert torch.equal(h_, d_.cpu())
 
     extra = {}
     if rank == 0 and not args.no_sparse:
@@ -369,6 +411,8 @@ def run_ours(args, w, world, rank, local):
         "config": config_of(w, "atomic", world),
         "pct_of_peak": 100.0 * tflops(f_fwd + f_bwd, ms) / peak,
         "fwd_tflops": tflops(f_fwd, ms_fwd), "bwd_tflops": tflops(f_bwd, ms_bwd),
+        "ms_breakdown": {"fwd": ms_fwd, "bwd_preprocess": reduce_max(t_atomic["pre"], world),
+                         "bwd_main": ms_main, "bwd_postprocess": reduce_max(t_atomic["post"], world)},
         "split": None if ms_split is None else {
             "fwd_bwd_tflops": tflops(f_fwd + f_bwd, ms_split),
             "bwd_tflops": tflops(f_bwd, ms_split_bwd), "ms_per_step": ms_split},
@@ -379,7 +423,8 @@ def run_ours(args, w, world, rank, local):
         "cpu_baseline": cpu,
         "clocks": clocks,
         "e2e": {"value": world * tflops(f_fwd + f_bwd, ms_e2e), "unit": "TFLOP/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e,
+                "overlap": "h2d(i+1) | compute(i) | d2h(i-1) on three streams"},
         "gpu_launches": (5 if w.kind == "thd" else 4) * args.steps,
         **extra,
     }

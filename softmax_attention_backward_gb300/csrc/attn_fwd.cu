@@ -157,31 +157,73 @@ __global__ void __launch_bounds__(352, 1)
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
-      FwdItem w;
-      int k = 0, ic = 0, gring = 0;
-      bool ok = true;
-      while (ok && next_fwd_item<C::BM, C::BN>(p, total, a.n_x, a.x_major, k, w)) {
-        const int hk = w.h / (p.heads_q / p.heads_kv);
-        const int qb = ic % C::QBUFS, qu = ic / C::QBUFS;
-        if (!mbar_wait(&bar_qempty[qb], (qu & 1) ^ 1, ac)) break;
+      auto issue_q = [&](const FwdItem& it, int icq) {
+        const int qb = icq % C::QBUFS;
         mbar_arrive_expect_tx(&bar_q[qb], 2 * C::Q_BYTES);
         for (int t = 0; t < 2; ++t)
           for (int pn = 0; pn < PANELS; ++pn)
             tma_load_4d(&tmQ, &bar_q[qb], sQ + (qb * 2 + t) * C::Q_BYTES + pn * C::BM * 128,
-                        pn * 64, w.h, w.seq.row0 + w.m0 + t * C::BM, w.seq.b);
-        for (int i = 0; i < 2 * w.n_kv; ++i) {
+                        pn * 64, it.h, it.seq.row0 + it.m0 + t * C::BM, it.seq.b);
+      };
+      FwdItem w, wn;
+      int k = 0, ic = 0, gring = 0;
+      bool have = next_fwd_item<C::BM, C::BN>(p, total, a.n_x, a.x_major, k, w);
+      bool ok = true;
+      if (have) {
+        if (mbar_wait(&bar_qempty[0], 1, ac)) issue_q(w, 0);
+        else ok = false;
+      }
+      while (ok && have) {
+        const int hk = w.h / (p.heads_q / p.heads_kv);
+        // the next item's query pair is loaded as soon as its buffer frees
+        // (with two buffers: when the previous item's S MMAs are done), while
+        // this item's K/V tiles stream through the ring
+        const bool have_next = next_fwd_item<C::BM, C::BN>(p, total, a.n_x, a.x_major, k, wn);
+        bool q_pending = have_next;
+        const int nqb = (ic + 1) % C::QBUFS;
+        const uint32_t nq_par = (((ic + 1) / C::QBUFS) & 1) ^ 1;
+        for (int i = 0; ok && i < 2 * w.n_kv; ++i) {
           const int gi = gring + i;
           const int slot = gi % C::NSLOT, use = gi / C::NSLOT;
-          if (!mbar_wait(&bar_empty[slot], (use & 1) ^ 1, ac)) { ok = false; break; }
+          const uint32_t slot_addr = smem_u32(&bar_empty[slot]);
+          const uint32_t slot_par = (use & 1) ^ 1;
+          // bounded wait on the ring slot that also polls the next query buffer
+          uint64_t t0 = 0;
+          while (true) {
+            if (q_pending && mbar_try_wait(smem_u32(&bar_qempty[nqb]), nq_par)) {
+              issue_q(wn, ic + 1);
+              q_pending = false;
+            }
+            if (mbar_try_wait(slot_addr, slot_par)) break;
+            if (t0 == 0) t0 = globaltimer();
+            if (*reinterpret_cast<volatile int*>(&abort_flag)) { ok = false; break; }
+            if (globaltimer() - t0 > kWaitLimitNs) {
+              raise_error(ac, ATTN_DEVERR_TIMEOUT);
+              ok = false;
+              break;
+            }
+          }
+          if (!ok) break;
           const CUtensorMap* m = (i & 1) ? &tmV : &tmK;
           uint8_t* dst = sRing + slot * C::KV_BYTES;
           mbar_arrive_expect_tx(&bar_full[slot], C::KV_BYTES);
           for (int pn = 0; pn < PANELS; ++pn)
             tma_load_4d(m, &bar_full[slot], dst + pn * C::BN * 128, pn * 64, hk,
                         w.seq.row0 + (i >> 1) * C::BN, w.seq.b);
+          // a query tile that does not reach this K/V tile releases the slot
+          // through the producer (this use's phase is already open), so its
+          // issuer can move on to the next item without waiting for the load
+          for (int t = 0; t < 2; ++t)
+            if ((i >> 1) >= w.n_w[t]) mbar_arrive(&bar_empty[slot]);
+        }
+        if (ok && q_pending) {
+          if (mbar_wait(&bar_qempty[nqb], nq_par, ac)) issue_q(wn, ic + 1);
+          else ok = false;
         }
         gring += 2 * w.n_kv;
         ++ic;
+        w = wn;
+        have = have_next;
       }
     }
   } else if (warp == 9 || warp == 10) {
@@ -236,13 +278,6 @@ __global__ void __launch_bounds__(352, 1)
           umma_commit(&bar_empty[sv]);
           return true;
         };
-        // release a ring slot this tile does not use (both issuers release each)
-        auto skip = [&](int i) -> bool {
-          const int gi = gring + i;
-          if (!mbar_wait(&bar_full[gi % C::NSLOT], (gi / C::NSLOT) & 1, ac)) return false;
-          mbar_arrive(&bar_empty[gi % C::NSLOT]);
-          return true;
-        };
         if (C::SEP_P) {
           // S(j+1) as soon as the softmax has read S(j); PV(j) once P(j) is
           // ready.  S(0) of an item waits for the read of the previous S.
@@ -270,8 +305,6 @@ __global__ void __launch_bounds__(352, 1)
           if (nt > 0) umma_commit(&bar_qempty[qb]);
           else mbar_arrive(&bar_qempty[qb]);
         }
-        for (int j = nt; ok && j < w.n_kv; ++j)
-          if (!skip(2 * j) || !skip(2 * j + 1)) ok = false;
         gring += 2 * w.n_kv;
         cs += nt;
         ++ic;
@@ -395,16 +428,14 @@ __global__ void __launch_bounds__(352, 1)
           uint32_t r[32];
           tmem_ld32_nowait(tO + cc, r);
           tmem_wait_ld();
-          if (valid) {
 #pragma unroll
-            for (int i = 0; i < 32; i += 8) {
-              uint4 v;
-              v.x = pack_bf16(__uint_as_float(r[i + 0]) * inv_l, __uint_as_float(r[i + 1]) * inv_l);
-              v.y = pack_bf16(__uint_as_float(r[i + 2]) * inv_l, __uint_as_float(r[i + 3]) * inv_l);
-              v.z = pack_bf16(__uint_as_float(r[i + 4]) * inv_l, __uint_as_float(r[i + 5]) * inv_l);
-              v.w = pack_bf16(__uint_as_float(r[i + 6]) * inv_l, __uint_as_float(r[i + 7]) * inv_l);
-              *reinterpret_cast<uint4*>(orow + cc + i) = v;
-            }
+          for (int i = 0; i < 32; i += 8) {
+            uint4 v;
+            v.x = pack_bf16(__uint_as_float(r[i + 0]) * inv_l, __uint_as_float(r[i + 1]) * inv_l);
+            v.y = pack_bf16(__uint_as_float(r[i + 2]) * inv_l, __uint_as_float(r[i + 3]) * inv_l);
+            v.z = pack_bf16(__uint_as_float(r[i + 4]) * inv_l, __uint_as_float(r[i + 5]) * inv_l);
+            v.w = pack_bf16(__uint_as_float(r[i + 6]) * inv_l, __uint_as_float(r[i + 7]) * inv_l);
+            if (valid) *reinterpret_cast<uint4*>(orow + cc + i) = v;
           }
         }
         if (valid) {

@@ -428,6 +428,81 @@ __global__ void __launch_bounds__(512, 1)
         // ---- P^T (KV row r, query columns c0 .. c0 + HALF) ----
         if (!mbar_wait(&bar_s, g & 1, ac)) { ok = false; break; }
         tc_fence_after();
+        if constexpr (C::PT_ALIAS) {
+          // D = 64: both passes run as rolled loops over 32-column chunks.  The
+          // smaller loop body keeps the hot code of the eight P/dS warps, the
+          // drain warps and the issuers small enough to stay in the
+          // instruction cache (measured ~15% faster per step than the fully
+          // unrolled 64-column body), and frees registers.
+          const int lim_all = !kv_ok ? HALF : ((p.causal && q0 < w.kv0 + BN) ? kv - q0 - c0 : 0);
+          const uint64_t sl2x2 = f2_pack(sl2, sl2);
+#pragma unroll 1
+          for (int c1 = 0; c1 < HALF; c1 += 32) {
+            uint32_t u[32];
+            tmem_ld32_nowait(tSme + c1, u);
+            tmem_wait_ld();
+            const int lim = lim_all - c1;
+            if (lim > 0) {
+#pragma unroll
+              for (int c = 0; c < 32; ++c)
+                if (c < lim) u[c] = 0xff800000u;
+            }
+            uint32_t pk[16];
+#pragma unroll
+            for (int c = 0; c < 32; c += 4) {
+              const float4 l4 = *reinterpret_cast<const float4*>(&s_nlse[buf][c0 + c1 + c]);
+              float a0, a1, a2, a3;
+              f2_unpack(f2_fma(f2_pack(__uint_as_float(u[c]), __uint_as_float(u[c + 1])), sl2x2,
+                               f2_pack(l4.x, l4.y)), a0, a1);
+              f2_unpack(f2_fma(f2_pack(__uint_as_float(u[c + 2]), __uint_as_float(u[c + 3])),
+                               sl2x2, f2_pack(l4.z, l4.w)), a2, a3);
+              pk[c / 2] = f2_to_bf16x2(f2_pack(ex2(a0), ex2(a1)));
+              pk[c / 2 + 1] = f2_to_bf16x2(f2_pack(ex2(a2), ex2(a3)));
+            }
+            tmem_st16p(tPTme + c1 / 2, pk);
+          }
+          tmem_wait_st();
+          tc_fence_before();
+          mbar_arrive(&bar_p);
+          if (!mbar_wait(&bar_dp, g & 1, ac)) { ok = false; break; }
+          if (g > 0 && !mbar_wait(&bar_dst_done, (g - 1) & 1, ac)) { ok = false; break; }
+          if (g > 0 && !mbar_wait(&bar_dss_free, (g - 1) & 1, ac)) { ok = false; break; }
+          tc_fence_after();
+#pragma unroll 1
+          for (int c1 = 0; c1 < HALF; c1 += 32) {
+            uint32_t u[32], pp[16];
+            tmem_ld32_nowait(tDPme + c1, u);
+            tmem_ld16_nowait(tPTme + c1 / 2, pp);
+            tmem_wait_ld();
+            if (c1 + 32 == HALF) {
+              tc_fence_before();
+              mbar_arrive(&bar_s_free);
+            }
+            uint32_t pk[16];
+#pragma unroll
+            for (int c = 0; c < 32; c += 4) {
+              const uint64_t pa = f2_pack(__uint_as_float(pp[c / 2] << 16),
+                                          __uint_as_float(pp[c / 2] & 0xffff0000u));
+              const uint64_t pb = f2_pack(__uint_as_float(pp[c / 2 + 1] << 16),
+                                          __uint_as_float(pp[c / 2 + 1] & 0xffff0000u));
+              const float4 d4 = *reinterpret_cast<const float4*>(&s_delta[buf][c0 + c1 + c]);
+              pk[c / 2] = f2_to_bf16x2(f2_mul(f2_sub(f2_pack(__uint_as_float(u[c]),
+                                                             __uint_as_float(u[c + 1])),
+                                                     f2_pack(d4.x, d4.y)), pa));
+              pk[c / 2 + 1] = f2_to_bf16x2(f2_mul(f2_sub(f2_pack(__uint_as_float(u[c + 2]),
+                                                                 __uint_as_float(u[c + 3])),
+                                                         f2_pack(d4.z, d4.w)), pb));
+            }
+            tmem_st16p(tDSTme + c1 / 2, pk);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int ch = (c0 + c1) / 8 + i;
+              const uint32_t off = (ch >> 3) * BN * 128 + r * 128 + (((ch & 7) ^ (r & 7)) << 4);
+              *reinterpret_cast<uint4*>(sdS + off) =
+                  make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+            }
+          }
+        } else {
         // P^T in fp32 pairs: p2[i] = (P[2i], P[2i+1]) of this thread's
         // columns; kept for the dS pass unless P^T is read back from TMEM there
         uint64_t p2[C::PT_ALIAS ? 1 : HALF / 2];
@@ -544,6 +619,7 @@ __global__ void __launch_bounds__(512, 1)
           const uint32_t off = (ch >> 3) * BN * 128 + r * 128 + (((ch & 7) ^ (r & 7)) << 4);
           *reinterpret_cast<uint4*>(sdS + off) =
               make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+        }
         }
         tmem_wait_st();
         fence_proxy_async_smem();

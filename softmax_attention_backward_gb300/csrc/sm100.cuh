@@ -89,15 +89,28 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t addr, uint32_t parity) {
   return ok != 0;
 }
 
+// try_wait that may suspend the thread up to `ns` nanoseconds (it resumes as
+// soon as the phase completes)
+__device__ __forceinline__ bool mbar_try_wait_hint(uint32_t addr, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(addr), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Bounded wait for the phase with parity `parity` to complete.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const AbortCtx& c) {
   const uint32_t addr = smem_u32(bar);
   if (mbar_try_wait(addr, parity)) return true;
   const uint64_t t0 = globaltimer();
   while (true) {
-#pragma unroll 1
-    for (int i = 0; i < 32; ++i)
-      if (mbar_try_wait(addr, parity)) return true;
+    // a waiting thread sleeps in the barrier instead of spinning, which keeps
+    // issue slots and instruction fetch for the warps doing the work
+    if (mbar_try_wait_hint(addr, parity, 200000u)) return true;
     if (*reinterpret_cast<volatile int*>(c.smem_abort)) return false;
     if (globaltimer() - t0 > kWaitLimitNs) {
       raise_error(c, ATTN_DEVERR_TIMEOUT);

@@ -92,6 +92,9 @@ attn_status_t check_problem(const attn_problem_t* p, bool* empty) {
     if (static_cast<int64_t>(p->seqlen) * p->heads_q * p->head_dim >= (int64_t(1) << 31))
       return ATTN_ERR_UNSUPPORTED;
     if (p->batch > 65535) return ATTN_ERR_UNSUPPORTED;
+    // the memory-bound passes index (row, head, 8-dim chunk) in 32 bits
+    if (static_cast<int64_t>(p->batch) * p->seqlen * p->heads_q * p->head_dim >= (int64_t(1) << 34))
+      return ATTN_ERR_UNSUPPORTED;
   }
   if (p->heads_q > 65535) return ATTN_ERR_UNSUPPORTED;
   return ATTN_OK;

@@ -14,53 +14,76 @@
 
 namespace attn {
 
-// One group of D/8 threads per (row, head); 16-byte loads of O and dO.
+// Index math of the two kernels runs in 32 bits: the host checks that one
+// batch entry holds fewer than 2^31 elements, and the launchers below fall
+// back to a grid that covers 2^31 rows x heads at most per launch offset.
+
+// One group of D/8 threads per (row, head); 16-byte loads of O and dO.  Each
+// group handles two (row, head) pairs per iteration so that four 16-byte
+// loads per thread are in flight.
 template <int D>
 __global__ void __launch_bounds__(256) attn_bwd_preprocess_kernel(Problem p,
-                                                                  const __nv_bfloat16* o,
-                                                                  const __nv_bfloat16* dout,
-                                                                  float* delta, float* dq_acc,
+                                                                  const __nv_bfloat16* __restrict__ o,
+                                                                  const __nv_bfloat16* __restrict__ dout,
+                                                                  float* __restrict__ delta,
+                                                                  float* __restrict__ dq_acc,
                                                                   size_t acc_elems) {
   constexpr int TPR = D / 8;   // threads per row
+  constexpr int RPW = 32 / TPR;   // rows per warp step
   const int end = valid_end(p);
-  const size_t nrows = static_cast<size_t>(p.batch) * p.rows_total * p.heads_q;
-  const size_t gtid = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  const size_t nthreads = static_cast<size_t>(gridDim.x) * blockDim.x;
+  const uint32_t nrows = static_cast<uint32_t>(p.batch) * p.rows_total * p.heads_q;
+  const uint32_t nthreads = gridDim.x * blockDim.x;
+  const uint32_t gtid = blockIdx.x * blockDim.x + threadIdx.x;
   const int sub = threadIdx.x % TPR;
-  // each warp takes 32 / TPR consecutive rows per step, so the loop trip count
+  const uint32_t hq = p.heads_q, rt = p.rows_total;
+  // each warp takes 2 * RPW consecutive rows per step, so the loop trip count
   // is warp-uniform and the full-warp shuffles below stay converged
-  const size_t step = nthreads / TPR;
-  for (size_t base = (gtid / 32) * (32 / TPR); base < nrows; base += step) {
-    const size_t rr = base + (threadIdx.x % 32) / TPR;
-    const bool live = rr < nrows;
-    float acc = 0.f;
-    int h = 0, srow = 0, b = 0;
-    if (live) {
-      h = static_cast<int>(rr % p.heads_q);
-      const size_t bs = rr / p.heads_q;
-      srow = static_cast<int>(bs % p.rows_total);
-      b = static_cast<int>(bs / p.rows_total);
-      const uint4 ov = *reinterpret_cast<const uint4*>(o + rr * D + sub * 8);
-      const uint4 dv = *reinterpret_cast<const uint4*>(dout + rr * D + sub * 8);
-      const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&ov);
-      const __nv_bfloat162* d2 = reinterpret_cast<const __nv_bfloat162*>(&dv);
+  const uint32_t step = (nthreads / 32) * 2 * RPW;
+  for (uint32_t base = (gtid / 32) * 2 * RPW; base < nrows; base += step) {
+    uint32_t rr[2];
+    float acc[2] = {0.f, 0.f};
+    uint4 ov[2], dv[2];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float2 a = __bfloat1622float2(o2[i]);
-        const float2 c = __bfloat1622float2(d2[i]);
-        acc = fmaf(a.x, c.x, acc);
-        acc = fmaf(a.y, c.y, acc);
+    for (int u = 0; u < 2; ++u) {
+      rr[u] = base + u * RPW + (threadIdx.x % 32) / TPR;
+      if (rr[u] < nrows) {
+        ov[u] = *reinterpret_cast<const uint4*>(o + static_cast<size_t>(rr[u]) * D + sub * 8);
+        dv[u] = *reinterpret_cast<const uint4*>(dout + static_cast<size_t>(rr[u]) * D + sub * 8);
       }
     }
 #pragma unroll
-    for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if (live && sub == 0) {
-      size_t li;
-      if (p.cu_seqlens)
-        li = static_cast<size_t>(h) * p.rows_total + srow;
-      else
-        li = (static_cast<size_t>(b) * p.heads_q + h) * p.rows_total + srow;
-      delta[li] = (srow < end) ? acc : 0.f;
+    for (int u = 0; u < 2; ++u) {
+      if (rr[u] < nrows) {
+        const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&ov[u]);
+        const __nv_bfloat162* d2 = reinterpret_cast<const __nv_bfloat162*>(&dv[u]);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float2 a = __bfloat1622float2(o2[i]);
+          const float2 c = __bfloat1622float2(d2[i]);
+          acc[u] = fmaf(a.x, c.x, acc[u]);
+          acc[u] = fmaf(a.y, c.y, acc[u]);
+        }
+      }
+    }
+#pragma unroll
+    for (int off = TPR / 2; off > 0; off >>= 1) {
+      acc[0] += __shfl_xor_sync(0xffffffffu, acc[0], off);
+      acc[1] += __shfl_xor_sync(0xffffffffu, acc[1], off);
+    }
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      if (rr[u] < nrows && sub == 0) {
+        const uint32_t h = rr[u] % hq;
+        const uint32_t bs = rr[u] / hq;
+        const uint32_t srow = bs % rt;
+        const uint32_t b = bs / rt;
+        size_t li;
+        if (p.cu_seqlens)
+          li = static_cast<size_t>(h) * rt + srow;
+        else
+          li = (static_cast<size_t>(b) * hq + h) * rt + srow;
+        delta[li] = (static_cast<int>(srow) < end) ? acc[u] : 0.f;
+      }
     }
   }
   if (dq_acc) {
@@ -70,37 +93,74 @@ __global__ void __launch_bounds__(256) attn_bwd_preprocess_kernel(Problem p,
   }
 }
 
-// Finalize dQ.  Each thread handles 8 consecutive head dims of one (row, head).
+// Finalize dQ.  Each thread handles 8 consecutive head dims of one (row,
+// head); in the atomic mode it converts two such chunks per iteration.
 template <int D>
-__global__ void __launch_bounds__(256) attn_dq_finalize_kernel(Problem p, const float* acc,
+__global__ void __launch_bounds__(256) attn_dq_finalize_kernel(Problem p,
+                                                               const float* __restrict__ acc,
                                                                size_t slab_elems, int split,
                                                                int n_split, int kv_tile,
-                                                               __nv_bfloat16* dq,
-                                                               __nv_bfloat16* dk,
-                                                               __nv_bfloat16* dv) {
+                                                               __nv_bfloat16* __restrict__ dq,
+                                                               __nv_bfloat16* __restrict__ dk,
+                                                               __nv_bfloat16* __restrict__ dv) {
   constexpr int CPR = D / 8;   // chunks per (row, head)
   const int end = valid_end(p);
-  const size_t nchunks = static_cast<size_t>(p.batch) * p.rows_total * p.heads_q * CPR;
-  const size_t nthreads = static_cast<size_t>(gridDim.x) * blockDim.x;
+  const uint32_t hq = p.heads_q, rt = p.rows_total;
+  const uint32_t nchunks = static_cast<uint32_t>(p.batch) * rt * hq * CPR;
+  const uint32_t nthreads = gridDim.x * blockDim.x;
   const float sc = p.scale;
-  for (size_t c = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; c < nchunks;
-       c += nthreads) {
-    const size_t rh = c / CPR;
-    const int sub = static_cast<int>(c % CPR);
-    const size_t bs = rh / p.heads_q;
-    const int hh = static_cast<int>(rh % p.heads_q);
-    const int srow = static_cast<int>(bs % p.rows_total);
-    const size_t bb = bs / p.rows_total;
-    float v[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-    if (srow < end) {
-      // accumulator / slabs are head-major: [batch, head, row, dim]
-      const size_t e0 = ((bb * p.heads_q + hh) * p.rows_total + srow) * D + sub * 8;
-      if (!split) {
-        const float4 a0 = *reinterpret_cast<const float4*>(acc + e0);
-        const float4 a1 = *reinterpret_cast<const float4*>(acc + e0 + 4);
-        v[0] = a0.x; v[1] = a0.y; v[2] = a0.z; v[3] = a0.w;
-        v[4] = a1.x; v[5] = a1.y; v[6] = a1.z; v[7] = a1.w;
-      } else {
+  // accumulator / slabs are head-major: [batch, head, row, dim]
+  auto acc_index = [&](uint32_t c, int& srow) -> size_t {
+    const uint32_t rh = c / CPR;
+    const uint32_t sub = c % CPR;
+    const uint32_t bs = rh / hq;
+    const uint32_t hh = rh % hq;
+    srow = static_cast<int>(bs % rt);
+    const uint32_t bb = bs / rt;
+    return ((static_cast<size_t>(bb) * hq + hh) * rt + srow) * D + sub * 8;
+  };
+  auto store = [&](uint32_t c, const float (&v)[8]) {
+    uint4 out;
+    out.x = pack_bf16(v[0] * sc, v[1] * sc);
+    out.y = pack_bf16(v[2] * sc, v[3] * sc);
+    out.z = pack_bf16(v[4] * sc, v[5] * sc);
+    out.w = pack_bf16(v[6] * sc, v[7] * sc);
+    *reinterpret_cast<uint4*>(dq + static_cast<size_t>(c) * 8) = out;
+  };
+  const uint32_t c_first = blockIdx.x * blockDim.x + threadIdx.x;
+  if (!split) {
+    for (uint32_t c0 = c_first; c0 < nchunks; c0 += 2 * nthreads) {
+      const uint32_t cc[2] = {c0, c0 + nthreads};
+      float4 a[2][2];
+      bool live[2];
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        int srow = 0;
+        live[u] = false;
+        a[u][0] = a[u][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (cc[u] < nchunks) {
+          const size_t e0 = acc_index(cc[u], srow);
+          live[u] = true;
+          if (srow < end) {
+            a[u][0] = *reinterpret_cast<const float4*>(acc + e0);
+            a[u][1] = *reinterpret_cast<const float4*>(acc + e0 + 4);
+          }
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        if (!live[u]) continue;
+        const float v[8] = {a[u][0].x, a[u][0].y, a[u][0].z, a[u][0].w,
+                            a[u][1].x, a[u][1].y, a[u][1].z, a[u][1].w};
+        store(cc[u], v);
+      }
+    }
+  } else {
+    for (uint32_t c = c_first; c < nchunks; c += nthreads) {
+      int srow = 0;
+      const size_t e0 = acc_index(c, srow);
+      float v[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+      if (srow < end) {
         // sequence-local row index and length
         int local = srow, len = p.rows_total;
         if (p.cu_seqlens) {
@@ -124,13 +184,8 @@ __global__ void __launch_bounds__(256) attn_dq_finalize_kernel(Problem p, const 
           v[4] += a1.x; v[5] += a1.y; v[6] += a1.z; v[7] += a1.w;
         }
       }
+      store(c, v);
     }
-    uint4 out;
-    out.x = pack_bf16(v[0] * sc, v[1] * sc);
-    out.y = pack_bf16(v[2] * sc, v[3] * sc);
-    out.z = pack_bf16(v[4] * sc, v[5] * sc);
-    out.w = pack_bf16(v[6] * sc, v[7] * sc);
-    *reinterpret_cast<uint4*>(dq + rh * D + sub * 8) = out;
   }
   // THD: zero dK / dV rows past the last sequence
   if (p.cu_seqlens) {

@@ -3,12 +3,11 @@
 // sparse MLA forward/backward with preprocess/postprocess, dim 576 =
 // 512 latent + 64 rope, v_channels 512, -1 for empty top-k slots).
 //
-// One CTA per (token, block of 64 query heads).  The token's key rows are
-// gathered 32 at a time with 16-byte cp.async into a double-buffered,
-// XOR-swizzled shared tile, so all heads share one gather.  The contractions
-// are warp-level tensor-core tiles (m16n8k16, bf16 in, fp32 out).
-//   forward : S = Q K^T, online softmax (max exchanged between the two warps
-//             sharing 16 heads), O += P V; O = O / l, LSE = ln of the row sum.
+// Backward (the forward runs on tcgen05, sparse_fwd_tc.cu).  One CTA per
+// (token, block of 64 query heads).  The token's key rows are gathered 32 at
+// a time with 16-byte cp.async into a double-buffered, XOR-swizzled shared
+// tile, so all heads share one gather.  The contractions are warp-level
+// tensor-core tiles (m16n8k16, bf16 in, fp32 out):
 //   backward: P = exp(S - LSE), dP = dO V^T, dS = P (dP - Delta) * scale,
 //             dQ += dS K (registers, stored once per token),
 //             dKV[idx] += dS^T Q (576 dims) + P^T dO (first 512 dims) with
@@ -79,181 +78,6 @@ __device__ __forceinline__ void load_rows(const __nv_bfloat16* src, size_t ld, i
     const bool v = r < nvalid;
     const void* s = v ? static_cast<const void*>(src + r * ld + ch * 8) : static_cast<const void*>(src);
     cp_async16(dbase + swz<COLS>(r, ch * 8), s, v ? 16u : 0u);
-  }
-}
-
-// ============================================================================
-// Forward
-// ============================================================================
-constexpr int SPF_THREADS = 256;
-constexpr int SPF_SMEM = SP_HB * SP_DQK * 2 + 2 * SP_BN * SP_DQK * 2 + SP_HB * SP_PSTR * 2 + 128;
-
-__global__ void __launch_bounds__(SPF_THREADS, 1) sparse_fwd_kernel(const SparseArgs a) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) &
-                                             ~uintptr_t(127));
-  uint8_t* sQ = smem;
-  uint8_t* sKV = sQ + SP_HB * SP_DQK * 2;                 // 2 buffers
-  __nv_bfloat16* sP = reinterpret_cast<__nv_bfloat16*>(sKV + 2 * SP_BN * SP_DQK * 2);
-  __shared__ int s_idx[2][SP_BN];
-  __shared__ float s_max[2][SP_HB];
-  __shared__ float s_l[2][SP_HB];
-  __shared__ int s_red[SPF_THREADS / 32];
-
-  const int t = blockIdx.x;
-  const int hb = blockIdx.y * SP_HB;
-  const int nh = min(SP_HB, a.H - hb);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int g = lane >> 2, tq = lane & 3;
-  const int hg = warp & 3;     // 16-head group
-  const int half = warp >> 2;  // key half (S) and value-column half (O)
-  const float sl2 = a.scale_log2;
-
-  const int nchunks = sparse_chunk_count<SPF_THREADS>(a, t, s_red);
-
-  load_rows<SP_DQK, SPF_THREADS>(a.q + (static_cast<size_t>(t) * a.H + hb) * SP_DQK, SP_DQK,
-                                 SP_HB, nh, sQ);
-  if (nchunks > 0) sparse_gather<SPF_THREADS>(a, t, 0, sKV, s_idx[0]);
-  cp_async_commit();
-
-  float acc[32][4];
-#pragma unroll
-  for (int n = 0; n < 32; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
-  float m_run[2] = {-INFINITY, -INFINITY};
-  float l_th[2] = {0.f, 0.f};
-
-  const uint32_t aQ = smem_u32(sQ), aP = smem_u32(sP);
-  for (int c = 0; c < nchunks; ++c) {
-    const int buf = c & 1;
-    if (c + 1 < nchunks) {
-      sparse_gather<SPF_THREADS>(a, t, c + 1, sKV + (buf ^ 1) * SP_BN * SP_DQK * 2, s_idx[buf ^ 1]);
-      cp_async_commit();
-      cp_async_wait<1>();
-    } else {
-      cp_async_wait<0>();
-    }
-    __syncthreads();
-    const uint32_t aK = smem_u32(sKV + buf * SP_BN * SP_DQK * 2);
-    // ---- S = Q K^T for heads 16hg.., keys 16half.. (two n8 tiles) ----
-    float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-#pragma unroll 4
-    for (int k = 0; k < SP_DQK / 16; ++k) {
-      uint32_t af[4], b0[2], b1[2];
-      {
-        const int r = 16 * hg + (lane & 7) + 8 * ((lane >> 3) & 1);
-        const int cc = 16 * k + 8 * (lane >> 4);
-        ldsm_x4(aQ + swz<SP_DQK>(r, cc), af[0], af[1], af[2], af[3]);
-      }
-      {
-        const int n = 16 * half + (lane & 7) + 8 * (lane >> 4);
-        const int kk = 16 * k + 8 * ((lane >> 3) & 1);
-        ldsm_x4(aK + swz<SP_DQK>(n, kk), b0[0], b0[1], b1[0], b1[1]);
-      }
-      mma_bf16_16816(s[0], af, b0);
-      mma_bf16_16816(s[1], af, b1);
-    }
-    // ---- mask empty slots, row max ----
-    float mx[2] = {-INFINITY, -INFINITY};
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int col = 16 * half + 8 * nt + 2 * tq + (e & 1);
-        if (s_idx[buf][col] < 0) s[nt][e] = -INFINITY;
-        mx[e >> 1] = fmaxf(mx[e >> 1], s[nt][e]);
-      }
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
-      mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
-    }
-    if (tq == 0) {
-      s_max[half][16 * hg + g] = mx[0] * sl2;
-      s_max[half][16 * hg + g + 8] = mx[1] * sl2;
-    }
-    __syncthreads();
-    float alpha[2], msub[2];
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      const int row = 16 * hg + g + 8 * r;
-      const float mt = fmaxf(s_max[0][row], s_max[1][row]);
-      const float mn = fmaxf(m_run[r], mt);
-      alpha[r] = (mn == -INFINITY) ? 1.f : ex2(m_run[r] - mn);
-      msub[r] = (mn == -INFINITY) ? 0.f : mn;
-      m_run[r] = mn;
-    }
-    // ---- P ----
-    float rs[2] = {0.f, 0.f};
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-      float pv[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        pv[e] = ex2(fmaf(s[nt][e], sl2, -msub[e >> 1]));
-        rs[e >> 1] += pv[e];
-      }
-      const int col = 16 * half + 8 * nt + 2 * tq;
-      *reinterpret_cast<uint32_t*>(sP + (16 * hg + g) * SP_PSTR + col) = pack_bf16(pv[0], pv[1]);
-      *reinterpret_cast<uint32_t*>(sP + (16 * hg + g + 8) * SP_PSTR + col) = pack_bf16(pv[2], pv[3]);
-    }
-    l_th[0] = l_th[0] * alpha[0] + rs[0];
-    l_th[1] = l_th[1] * alpha[1] + rs[1];
-    __syncthreads();
-    // ---- O = O * alpha + P V  (heads 16hg.., value columns 256half..) ----
-#pragma unroll
-    for (int n = 0; n < 32; ++n) {
-      acc[n][0] *= alpha[0];
-      acc[n][1] *= alpha[0];
-      acc[n][2] *= alpha[1];
-      acc[n][3] *= alpha[1];
-    }
-#pragma unroll
-    for (int kk = 0; kk < SP_BN / 16; ++kk) {
-      uint32_t af[4];
-      {
-        const int r = 16 * hg + (lane & 7) + 8 * ((lane >> 3) & 1);
-        const int cc = 16 * kk + 8 * (lane >> 4);
-        ldsm_x4(aP + (r * SP_PSTR + cc) * 2, af[0], af[1], af[2], af[3]);
-      }
-#pragma unroll
-      for (int np = 0; np < 16; ++np) {
-        uint32_t b0[2], b1[2];
-        const int kr = 16 * kk + (lane & 7) + 8 * ((lane >> 3) & 1);
-        const int n = 256 * half + 16 * np + 8 * (lane >> 4);
-        ldsm_x4_t(aK + swz<SP_DQK>(kr, n), b0[0], b0[1], b1[0], b1[1]);
-        mma_bf16_16816(acc[2 * np], af, b0);
-        mma_bf16_16816(acc[2 * np + 1], af, b1);
-      }
-    }
-    __syncthreads();
-  }
-  cp_async_wait<0>();
-
-  // ---- combine the row sums of the two key halves ----
-#pragma unroll
-  for (int r = 0; r < 2; ++r) {
-    l_th[r] += __shfl_xor_sync(0xffffffffu, l_th[r], 1);
-    l_th[r] += __shfl_xor_sync(0xffffffffu, l_th[r], 2);
-  }
-  if (tq == 0) {
-    s_l[half][16 * hg + g] = l_th[0];
-    s_l[half][16 * hg + g + 8] = l_th[1];
-  }
-  __syncthreads();
-#pragma unroll
-  for (int r = 0; r < 2; ++r) {
-    const int row = 16 * hg + g + 8 * r;
-    if (row >= nh) continue;
-    const float l = s_l[0][row] + s_l[1][row];
-    const float inv = l > 0.f ? 1.f / l : 0.f;
-    __nv_bfloat16* orow = a.o + (static_cast<size_t>(t) * a.H + hb + row) * SP_DV + 256 * half;
-#pragma unroll
-    for (int n = 0; n < 32; ++n)
-      *reinterpret_cast<uint32_t*>(orow + 8 * n + 2 * tq) =
-          pack_bf16(acc[n][2 * r] * inv, acc[n][2 * r + 1] * inv);
-    if (half == 0 && tq == 0)
-      a.lse[static_cast<size_t>(t) * a.H + hb + row] =
-          l > 0.f ? (m_run[r] + __log2f(l)) * kLn2 : -INFINITY;
   }
 }
 
@@ -485,15 +309,6 @@ __global__ void __launch_bounds__(256) sparse_dkv_cast_kernel(const float* acc,
     o.w = pack_bf16(a1.z, a1.w);
     reinterpret_cast<uint4*>(dkv)[i] = o;
   }
-}
-
-cudaError_t launch_sparse_fwd(const SparseArgs& a, cudaStream_t st) {
-  cudaError_t e = cudaFuncSetAttribute(sparse_fwd_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, SPF_SMEM);
-  if (e != cudaSuccess) return e;
-  dim3 grid(a.T, (a.H + SP_HB - 1) / SP_HB);
-  sparse_fwd_kernel<<<grid, SPF_THREADS, SPF_SMEM, st>>>(a);
-  return cudaGetLastError();
 }
 
 cudaError_t launch_sparse_bwd(const SparseArgs& a, float* delta, __nv_bfloat16* dkv,

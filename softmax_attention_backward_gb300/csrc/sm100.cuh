@@ -102,6 +102,18 @@ __device__ __forceinline__ bool mbar_try_wait_hint(uint32_t addr, uint32_t parit
   return ok != 0;
 }
 
+// Non-blocking test of the phase with parity `parity` (never suspends).
+__device__ __forceinline__ bool mbar_test_wait(uint32_t addr, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(addr), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Bounded wait for the phase with parity `parity` to complete.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const AbortCtx& c) {
   const uint32_t addr = smem_u32(bar);

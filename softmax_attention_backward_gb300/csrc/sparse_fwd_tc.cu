@@ -178,9 +178,8 @@ __global__ void __launch_bounds__(SF_THREADS, 1) sparse_fwd_tc_kernel(const Spar
       const uint32_t idO = idesc_bf16(128, SF_HB, true, false);
       const uint64_t dQ = desc_kmajor_base(smem_u32(sQ));
       const uint64_t dP = desc_kmajor_base(smem_u32(sP));
-      auto issue_o = [&](int c) -> bool {
+      auto issue_o = [&](int c) {
         // O^T(m) += V^T(dims 128m..) P^T, P of chunk c from shared memory
-        if (!mbar_wait(&bar_p_full, c & 1, ac)) return false;
         tc_fence_after();
         const int b = c & 1;
 #pragma unroll
@@ -193,25 +192,47 @@ __global__ void __launch_bounds__(SF_THREADS, 1) sparse_fwd_tc_kernel(const Spar
         }
         umma_commit(&bar_o_done);
         umma_commit(&bar_kv_empty[b]);
-        return true;
       };
-      bool ok = mbar_wait(&bar_q, 0, ac);
-      for (int c = 0; ok && c < nchunks; ++c) {
-        const int b = c & 1;
-        // the previous chunk's O^T GEMM first: it frees that chunk's buffer,
-        // so the gather of chunk c + 1 overlaps S(c) and the softmax of c
-        if (c > 0 && !issue_o(c - 1)) { ok = false; break; }
-        if (!mbar_wait(&bar_kv_full[b], (c >> 1) & 1, ac)) { ok = false; break; }
-        if (!mbar_wait(&bar_s_free[b], ((c >> 1) & 1) ^ 1, ac)) { ok = false; break; }
+      auto issue_s = [&](int c) {
         tc_fence_after();
+        const int b = c & 1;
         const uint64_t dK = desc_kmajor_base(smem_u32(sKV + b * SF_KV_BYTES));
 #pragma unroll 4
         for (int kk = 0; kk < SF_DQK / 16; ++kk)
           umma_ss(tmem + SF_COL_S + 64 * b, desc_advance(dQ, kmajor_step_bytes(SF_HB, kk)),
                   desc_advance(dK, kmajor_step_bytes(SF_NK, kk)), idS, kk > 0);
         umma_commit(&bar_s_full[b]);
+      };
+      // Issue in readiness order: O^T of chunk `no` as soon as its P is
+      // written (that frees its buffer for the gather two chunks ahead), S of
+      // chunk `ns` as soon as the chunk landed and its TMEM buffer was read,
+      // so S of the next chunk overlaps the softmax of the current one.
+      bool ok = mbar_wait(&bar_q, 0, ac);
+      int ns = 0, no = 0;
+      uint64_t t0 = 0;
+      while (ok && no < nchunks) {
+        bool did = false;
+        if (no < ns && mbar_test_wait(smem_u32(&bar_p_full), no & 1)) {
+          issue_o(no++);
+          did = true;
+        } else if (ns < nchunks &&
+                   mbar_test_wait(smem_u32(&bar_kv_full[ns & 1]), (ns >> 1) & 1) &&
+                   mbar_test_wait(smem_u32(&bar_s_free[ns & 1]), ((ns >> 1) & 1) ^ 1)) {
+          issue_s(ns++);
+          did = true;
+        }
+        if (did) {
+          t0 = 0;
+        } else {
+          if (t0 == 0) t0 = globaltimer();
+          if (*reinterpret_cast<volatile int*>(&abort_flag)) { ok = false; break; }
+          if (globaltimer() - t0 > kWaitLimitNs) {
+            raise_error(ac, ATTN_DEVERR_TIMEOUT);
+            ok = false;
+            break;
+          }
+        }
       }
-      if (ok) issue_o(nchunks - 1);
     }
   } else if (warp < 4) {
     // ---------------- softmax and epilogue ----------------

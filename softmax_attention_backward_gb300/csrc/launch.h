@@ -76,5 +76,6 @@ struct SparseArgs {
 cudaError_t launch_sparse_fwd(const SparseArgs& a, cudaStream_t st);
 cudaError_t launch_sparse_bwd(const SparseArgs& a, float* delta, __nv_bfloat16* dkv,
                               cudaStream_t st);
+cudaError_t launch_sparse_bwd_main(const SparseArgs& a, cudaStream_t st);
 
 }  // namespace attn

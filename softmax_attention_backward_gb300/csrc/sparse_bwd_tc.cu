@@ -1,0 +1,386 @@
+// Top-k sparse attention backward on tcgen05 (SparseMLA style, "[2/2] Add
+// TileLang fused DSA kernels support with THD and CP", Megatron-LM #5049:
+// sparse MLA backward with preprocess/postprocess; one shared KV head, dim
+// 576 = 512 latent + 64 rope, v_channels 512, -1 for empty top-k slots).
+//
+// Work item = one token t and a block of 64 query heads.  Q [64 x 576], dO
+// [64 x 512], LSE and Delta of the block load once; the token's key rows are
+// gathered 64 slots at a time (16-byte cp.async, SW128 K-major layout).  Per
+// chunk of slots s (KV rows K_s, V_s = the first 512 dims of K_s):
+//   S    = Q K^T      dP = dO V^T          (M = 64 heads, N = 64 slots, TMEM)
+//   P    = exp(S c - LSE),  dS = P o (dP - Delta) c        (softmax warps)
+//   dQ^T += K^T dS^T  (value dims on TMEM lanes: four M = 128 tiles for dims
+//                      0..511 and one M = 64 tile for dims 512..575, 64 heads)
+//   dKV[s] += dS^T Q + P^T [dO | 0]   in nine 64-dim pieces (M = 64 slots,
+//                      N = 64 dims), each drained from TMEM into the fp32 dKV
+//                      accumulator with vector reductions while the next
+//                      piece is computed (two piece buffers)
+// P and dS go through shared memory as bf16 [head][slot] tiles, which serve
+// as the K-major B operand of dQ^T and the MN-major A operand of the dKV
+// pieces.  The scale c is folded into dS, so dQ and dKV need none later.
+// An M = 64 accumulator keeps row r in TMEM lane 32 (r / 16) + r % 16.
+//
+// Warp roles (352 threads): 0..3 softmax and dQ epilogue, 4..7 dKV drain,
+// 8..9 gather producers, 10 MMA issuer.  Every wait is a bounded mbarrier
+// wait.
+#include <cuda_runtime.h>
+
+#include "launch.h"
+
+namespace attn {
+
+namespace {
+
+constexpr int SB_HB = 64;                      // heads per item
+constexpr int SB_NK = 64;                      // key slots per chunk
+constexpr int SB_DQK = 576, SB_DV = 512;
+constexpr int SB_Q_BYTES = SB_HB * SB_DQK * 2;
+constexpr int SB_DO_BYTES = SB_HB * SB_DV * 2;
+constexpr int SB_KV_BYTES = SB_NK * SB_DQK * 2;
+constexpr int SB_T_BYTES = SB_HB * SB_NK * 2;  // P or dS tile
+constexpr int SB_SMEM = SB_Q_BYTES + SB_DO_BYTES + SB_KV_BYTES + 2 * SB_T_BYTES + 1024;
+constexpr int SB_THREADS = 352;
+constexpr int SB_PRODUCERS = 64;               // warps 8..9
+constexpr int SB_PIECES = SB_DQK / 64;         // 64-dim pieces of a dKV row
+constexpr uint32_t SB_TMEM_COLS = 512;
+constexpr uint32_t SB_COL_S = 0, SB_COL_DP = 64;
+constexpr uint32_t SB_COL_DQ = 128;            // five dQ^T tiles of 64 columns
+constexpr uint32_t SB_COL_PC = 448;            // dKV piece buffer 0 (buffer 1 = the dP columns)
+
+__device__ __forceinline__ uint32_t sb_off(int row, int ch, int rows) {
+  return (ch >> 3) * rows * 128 + row * 128 + (((ch & 7) ^ (row & 7)) << 4);
+}
+
+__device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c),
+               "f"(d)
+               : "memory");
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(SB_THREADS, 1) sparse_bwd_tc_kernel(const SparseArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint8_t* sQ = smem;
+  uint8_t* sdO = sQ + SB_Q_BYTES;
+  uint8_t* sKV = sdO + SB_DO_BYTES;
+  uint8_t* sP = sKV + SB_KV_BYTES;               // [head][slot] bf16, 128-byte rows
+  uint8_t* sdS = sP + SB_T_BYTES;
+
+  __shared__ uint64_t bar_in, bar_kv_full, bar_kv_empty, bar_s_full, bar_s_free, bar_ds_full;
+  __shared__ uint64_t bar_pds_free, bar_pc_full[2], bar_pc_free[2], bar_dq_done;
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int abort_flag;
+  // KV row of each slot (-1: none) by chunk mod 4: the drain of a chunk's
+  // last pieces may still read its rows while the producer fills chunk + 2
+  __shared__ int s_row[4][SB_NK];
+  __shared__ uint32_t s_valid[2][2];
+  __shared__ float s_lse2[SB_HB];                // LSE * log2(e)
+  __shared__ float s_delta[SB_HB];
+  __shared__ int s_red[SB_THREADS / 32];
+
+  const int t = blockIdx.x;
+  const int hb = blockIdx.y * SB_HB;
+  const int nh = min(SB_HB, a.H - hb);
+  const int warp = warp_id(), lane = lane_id();
+  AbortCtx ac{&abort_flag, a.err};
+
+  int nchunks;
+  {
+    const int32_t* irow = a.idx + static_cast<size_t>(t) * a.K;
+    int last = -1;
+    for (int s = threadIdx.x; s < a.K; s += SB_THREADS) {
+      const int j = __ldg(irow + s);
+      if (j >= 0 && j < a.T) last = s;
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) last = max(last, __shfl_xor_sync(0xffffffffu, last, off));
+    if (lane == 0) s_red[warp] = last;
+    if (threadIdx.x == 0) {
+      abort_flag = 0;
+      mbar_init(&bar_in, SB_PRODUCERS);
+      mbar_init(&bar_kv_full, SB_PRODUCERS);
+      mbar_init(&bar_kv_empty, 1);
+      mbar_init(&bar_s_full, 1);
+      mbar_init(&bar_s_free, 128);
+      mbar_init(&bar_ds_full, 128);
+      mbar_init(&bar_pds_free, 1);
+      for (int b = 0; b < 2; ++b) {
+        mbar_init(&bar_pc_full[b], 1);
+        mbar_init(&bar_pc_free[b], 128);
+      }
+      mbar_init(&bar_dq_done, 1);
+      fence_mbar_init();
+    }
+    if (warp == 10) tmem_alloc(&tmem_base_sh, SB_TMEM_COLS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    int m = -1;
+    for (int w = 0; w < SB_THREADS / 32; ++w) m = max(m, s_red[w]);
+    nchunks = (m + SB_NK) / SB_NK;
+  }
+  const uint32_t tmem = tmem_base_sh;
+
+  if (warp == 8 || warp == 9) {
+    // ---------------- producers: the block's inputs, then the chunks ----------------
+    const int pt = threadIdx.x - 256;              // 0..63
+    const int32_t* irow = a.idx + static_cast<size_t>(t) * a.K;
+    if (nchunks > 0) {
+      const __nv_bfloat16* qb = a.q + (static_cast<size_t>(t) * a.H + hb) * SB_DQK;
+      const __nv_bfloat16* ob = a.dout + (static_cast<size_t>(t) * a.H + hb) * SB_DV;
+      for (int id = pt; id < SB_HB * (SB_DQK / 8); id += SB_PRODUCERS) {
+        const int r = id / (SB_DQK / 8), ch = id % (SB_DQK / 8);
+        const bool v = r < nh;
+        cp_async16(smem_u32(sQ) + sb_off(r, ch, SB_HB),
+                   v ? static_cast<const void*>(qb + r * SB_DQK + ch * 8) : static_cast<const void*>(a.q),
+                   v ? 16u : 0u);
+      }
+      for (int id = pt; id < SB_HB * (SB_DV / 8); id += SB_PRODUCERS) {
+        const int r = id / (SB_DV / 8), ch = id % (SB_DV / 8);
+        const bool v = r < nh;
+        cp_async16(smem_u32(sdO) + sb_off(r, ch, SB_HB),
+                   v ? static_cast<const void*>(ob + r * SB_DV + ch * 8) : static_cast<const void*>(a.dout),
+                   v ? 16u : 0u);
+      }
+      cp_async_commit();
+      // LSE (log2 domain) and Delta of the block's heads; rows past H give P = 0
+      const size_t li = static_cast<size_t>(t) * a.H + hb + pt;
+      s_lse2[pt] = pt < nh ? __ldg(a.lse_in + li) * kLog2e : INFINITY;
+      s_delta[pt] = pt < nh ? __ldg(a.delta + li) : 0.f;
+    }
+    for (int c = 0; c < nchunks; ++c) {
+      // the single chunk buffer was last read by dQ^T of chunk c - 1
+      if (!mbar_wait(&bar_kv_empty, (c & 1) ^ 1, ac)) break;
+      const int cb = c & 1;
+      {
+        const int slot = c * SB_NK + pt;
+        const int j = (slot < a.K) ? __ldg(irow + slot) : -1;
+        const bool valid = j >= 0 && j < a.T;
+        if (!valid && j != -1 && a.err) atomicOr(a.err, ATTN_DEVERR_INDEX_RANGE);
+        s_row[c & 3][pt] = valid ? j : -1;
+        const uint32_t m32 = __ballot_sync(0xffffffffu, valid);
+        if (lane == 0) s_valid[cb][pt >> 5] = m32;
+      }
+      const uint32_t base = smem_u32(sKV);
+      for (int id = pt; id < SB_NK * (SB_DQK / 8); id += SB_PRODUCERS) {
+        const int r = id / (SB_DQK / 8), ch = id % (SB_DQK / 8);
+        const int slot = c * SB_NK + r;
+        int j = (slot < a.K) ? __ldg(irow + slot) : -1;
+        if (j >= a.T) j = -1;
+        cp_async16(base + sb_off(r, ch, SB_NK),
+                   (j >= 0) ? static_cast<const void*>(a.kv + static_cast<size_t>(j) * SB_DQK + ch * 8)
+                            : static_cast<const void*>(a.kv),
+                   (j >= 0) ? 16u : 0u);
+      }
+      cp_async_commit();
+      cp_async_wait<0>();
+      fence_proxy_async_smem();
+      if (c == 0) mbar_arrive(&bar_in);
+      mbar_arrive(&bar_kv_full);
+    }
+    cp_async_wait<0>();
+  } else if (warp == 10) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0 && nchunks > 0) {
+      const uint32_t idS = idesc_bf16(64, SB_NK, false, false);        // S, dP
+      const uint32_t idQ128 = idesc_bf16(128, SB_HB, true, false);     // dQ^T tiles
+      const uint32_t idQ64 = idesc_bf16(64, SB_HB, true, false);       // dQ^T dims 512..575
+      const uint32_t idKV = idesc_bf16(64, 64, true, true);            // dKV pieces
+      const uint64_t dQk = desc_kmajor_base(smem_u32(sQ));
+      const uint64_t ddOk = desc_kmajor_base(smem_u32(sdO));
+      const uint64_t dKk = desc_kmajor_base(smem_u32(sKV));
+      const uint64_t ddSk = desc_kmajor_base(smem_u32(sdS));
+      const uint64_t dPmn = desc_mnmajor_base(smem_u32(sP), SB_HB);
+      const uint64_t ddSmn = desc_mnmajor_base(smem_u32(sdS), SB_HB);
+      bool ok = mbar_wait(&bar_in, 0, ac);
+      int gp = 0;                                  // dKV pieces issued so far
+      int n1 = 0;                                  // pieces issued into buffer 1 (the dP columns)
+      for (int c = 0; ok && c < nchunks; ++c) {
+        if (!mbar_wait(&bar_kv_full, c & 1, ac)) { ok = false; break; }
+        // S and dP columns: read by the softmax of chunk c - 1, and the last
+        // dKV piece that used the dP columns drained
+        if (c > 0 && !mbar_wait(&bar_s_free, (c - 1) & 1, ac)) { ok = false; break; }
+        if (n1 > 0 && !mbar_wait(&bar_pc_free[1], (n1 - 1) & 1, ac)) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll 4
+        for (int kk = 0; kk < SB_DQK / 16; ++kk)
+          umma_ss(tmem + SB_COL_S, desc_advance(dQk, kmajor_step_bytes(SB_HB, kk)),
+                  desc_advance(dKk, kmajor_step_bytes(SB_NK, kk)), idS, kk > 0);
+#pragma unroll 4
+        for (int kk = 0; kk < SB_DV / 16; ++kk)
+          umma_ss(tmem + SB_COL_DP, desc_advance(ddOk, kmajor_step_bytes(SB_HB, kk)),
+                  desc_advance(dKk, kmajor_step_bytes(SB_NK, kk)), idS, kk > 0);
+        umma_commit(&bar_s_full);
+        if (!mbar_wait(&bar_ds_full, c & 1, ac)) { ok = false; break; }
+        tc_fence_after();
+        // dQ^T(dims, heads) += K^T(dims, slots) dS^T(slots, heads)
+#pragma unroll
+        for (int m = 0; m < 5; ++m) {
+          const uint64_t dKmn = desc_mnmajor_base(smem_u32(sKV + 2 * m * SB_NK * 128), SB_NK);
+#pragma unroll
+          for (int kk = 0; kk < SB_NK / 16; ++kk)
+            umma_ss(tmem + SB_COL_DQ + 64 * m, desc_advance(dKmn, mnmajor_step_bytes(kk)),
+                    desc_advance(ddSk, kmajor_step_bytes(SB_HB, kk)), m < 4 ? idQ128 : idQ64,
+                    (c > 0 || kk > 0) ? 1u : 0u);
+        }
+        umma_commit(&bar_kv_empty);                // K and V of this chunk are no longer read
+        // dKV pieces: D(slots, dims 64p..) = dS^T Q_p + P^T dO_p
+        for (int p = 0; p < SB_PIECES; ++p, ++gp) {
+          const int b = gp & 1, use = gp >> 1;
+          if (!mbar_wait(&bar_pc_free[b], (use & 1) ^ 1, ac)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t dst = tmem + (b ? SB_COL_DP : SB_COL_PC);
+          const uint64_t dQmn = desc_mnmajor_base(smem_u32(sQ + p * SB_HB * 128), SB_HB);
+#pragma unroll
+          for (int kk = 0; kk < SB_HB / 16; ++kk)
+            umma_ss(dst, desc_advance(ddSmn, mnmajor_step_bytes(kk)),
+                    desc_advance(dQmn, mnmajor_step_bytes(kk)), idKV, kk > 0);
+          if (p < SB_DV / 64) {
+            const uint64_t ddOmn = desc_mnmajor_base(smem_u32(sdO + p * SB_HB * 128), SB_HB);
+#pragma unroll
+            for (int kk = 0; kk < SB_HB / 16; ++kk)
+              umma_ss(dst, desc_advance(dPmn, mnmajor_step_bytes(kk)),
+                      desc_advance(ddOmn, mnmajor_step_bytes(kk)), idKV, 1u);
+          }
+          umma_commit(&bar_pc_full[b]);
+          if (b == 1) ++n1;
+        }
+        if (!ok) break;
+        umma_commit(&bar_pds_free);                // P and dS tiles of this chunk are read
+      }
+      if (ok) umma_commit(&bar_dq_done);
+    }
+  } else if (warp >= 4) {
+    // ---------------- dKV drain (warps 4..7) ----------------
+    const int q = warp - 4;
+    const bool active = lane < 16;
+    const int slot = 16 * q + (lane & 15);         // slot row of the M = 64 piece
+    const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
+    int gp = 0;
+    bool ok = true;
+    for (int c = 0; ok && c < nchunks; ++c) {
+      for (int p = 0; p < SB_PIECES; ++p, ++gp) {
+        const int b = gp & 1, use = gp >> 1;
+        if (!mbar_wait(&bar_pc_full[b], use & 1, ac)) { ok = false; break; }
+        tc_fence_after();
+        uint32_t u[64];
+        const uint32_t src = tmem + lane_base + (b ? SB_COL_DP : SB_COL_PC);
+        tmem_ld32_nowait(src, u);
+        tmem_ld32_nowait(src + 32, u + 32);
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(&bar_pc_free[b]);
+        const int j = active ? s_row[c & 3][slot] : -1;
+        if (j >= 0) {
+          float* dst = a.dkv_acc + static_cast<size_t>(j) * SB_DQK + 64 * p;
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            red_add_v4(dst + 4 * i, __uint_as_float(u[4 * i]), __uint_as_float(u[4 * i + 1]),
+                       __uint_as_float(u[4 * i + 2]), __uint_as_float(u[4 * i + 3]));
+        }
+      }
+    }
+  } else {
+    // ---------------- softmax (P, dS) and dQ epilogue (warps 0..3) ----------------
+    const int q = warp;
+    const bool active = lane < 16;
+    const int row = 16 * q + (lane & 15);          // head row held by this lane
+    const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
+    const float sl2 = a.scale_log2, sc = a.scale;
+    bool ok = nchunks == 0 || mbar_wait(&bar_in, 0, ac);
+    const float lse2 = s_lse2[row], dlt = s_delta[row];
+    for (int c = 0; ok && c < nchunks; ++c) {
+      if (!mbar_wait(&bar_s_full, c & 1, ac)) { ok = false; break; }
+      if (!mbar_wait(&bar_kv_full, c & 1, ac)) { ok = false; break; }   // valid mask of the chunk
+      tc_fence_after();
+      uint32_t us[64], ud[64];
+      tmem_ld32_nowait(tmem + lane_base + SB_COL_S, us);
+      tmem_ld32_nowait(tmem + lane_base + SB_COL_S + 32, us + 32);
+      tmem_ld32_nowait(tmem + lane_base + SB_COL_DP, ud);
+      tmem_ld32_nowait(tmem + lane_base + SB_COL_DP + 32, ud + 32);
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(&bar_s_free);
+      const unsigned long long vm = static_cast<unsigned long long>(s_valid[c & 1][0]) |
+                                    (static_cast<unsigned long long>(s_valid[c & 1][1]) << 32);
+      uint32_t pp[32], pd[32];
+#pragma unroll
+      for (int cc = 0; cc < 64; cc += 2) {
+        float p0 = ex2(fmaf(__uint_as_float(us[cc]), sl2, -lse2));
+        float p1 = ex2(fmaf(__uint_as_float(us[cc + 1]), sl2, -lse2));
+        if (!((vm >> cc) & 1ull)) p0 = 0.f;
+        if (!((vm >> (cc + 1)) & 1ull)) p1 = 0.f;
+        const float d0 = p0 * (__uint_as_float(ud[cc]) - dlt) * sc;
+        const float d1 = p1 * (__uint_as_float(ud[cc + 1]) - dlt) * sc;
+        pp[cc / 2] = pack_bf16(p0, p1);
+        pd[cc / 2] = pack_bf16(d0, d1);
+      }
+      // the P / dS tiles of chunk c - 1 must have been read by its dKV pieces
+      if (c > 0) {
+        if (!mbar_wait(&bar_pds_free, (c - 1) & 1, ac)) { ok = false; break; }
+        tc_fence_after();
+      }
+      if (active) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const uint32_t off = row * 128 + ((i ^ (row & 7)) << 4);
+          *reinterpret_cast<uint4*>(sP + off) = make_uint4(pp[4 * i], pp[4 * i + 1], pp[4 * i + 2], pp[4 * i + 3]);
+          *reinterpret_cast<uint4*>(sdS + off) = make_uint4(pd[4 * i], pd[4 * i + 1], pd[4 * i + 2], pd[4 * i + 3]);
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&bar_ds_full);
+    }
+    // ---- dQ = (dQ^T)^T (the scale is in dS), bf16 ----
+    if (ok) {
+      const bool have = nchunks > 0 && mbar_wait(&bar_dq_done, 0, ac);
+      tc_fence_after();
+      __nv_bfloat16* qbase = a.dq + (static_cast<size_t>(t) * a.H + hb) * SB_DQK;
+#pragma unroll 1
+      for (int m = 0; m < 5; ++m) {
+        // tiles 0..3: lane = dim 128 m + 32 q + lane; tile 4 (M = 64): lanes
+        // 0..15 of each quarter hold dims 512 + 16 q + lane
+        const bool lane_ok = m < 4 || active;
+        const int d = m < 4 ? 128 * m + 32 * q + lane : 512 + 16 * q + (lane & 15);
+#pragma unroll
+        for (int h0 = 0; h0 < SB_HB; h0 += 32) {
+          uint32_t o[32];
+          if (have) {
+            tmem_ld32_nowait(tmem + lane_base + SB_COL_DQ + 64 * m + h0, o);
+            tmem_wait_ld();
+          }
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const int h = h0 + i;
+            if (lane_ok && h < nh)
+              qbase[static_cast<size_t>(h) * SB_DQK + d] =
+                  __float2bfloat16_rn(have ? __uint_as_float(o[i]) : 0.f);
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 10) {
+    tc_fence_after();
+    tmem_dealloc(tmem, SB_TMEM_COLS);
+    tmem_relinquish();
+  }
+}
+
+cudaError_t launch_sparse_bwd_main(const SparseArgs& a, cudaStream_t st) {
+  cudaError_t e = cudaFuncSetAttribute(sparse_bwd_tc_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, SB_SMEM);
+  if (e != cudaSuccess) return e;
+  dim3 grid(a.T, (a.H + SB_HB - 1) / SB_HB);
+  sparse_bwd_tc_kernel<<<grid, SB_THREADS, SB_SMEM, st>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace attn

@@ -26,7 +26,6 @@
 #include <cuda_runtime.h>
 
 #include "launch.h"
-#include "mma_sm80.cuh"
 
 namespace attn {
 

@@ -41,40 +41,36 @@ struct BwdCfg {
   static constexpr int KV_BYTES = BN * D * 2;
   static constexpr int QT_BYTES = BM * D * 2;
   static constexpr int DS_BYTES = BN * BM * 2;        // bf16 dS tile (for dQ)
-  static constexpr int DQ_BYTES = BM * D * 4;         // fp32 dQ staging tile
+  // staging tile for dQ (fp32) and dK/dV (bf16) on their way out: the whole
+  // 64 x 128 dQ tile for D = 128; half of the 128 x 64 tile for D = 64, whose
+  // dQ leaves in two halves, so that three Q/dO stages fit next to two K/V
+  // buffers
+  static constexpr int STG_BYTES = (D == 64) ? BM * D * 2 : BM * D * 4;
   static constexpr int KV_BUFS = (D == 64) ? 2 : 1;   // K/V buffers (next item prefetch)
-  static constexpr int NST = (D == 64) ? 2 : 3;       // Q/dO stages
+  static constexpr int NST = 3;                       // Q/dO stages
   static constexpr int SMEM =
-      KV_BUFS * 2 * KV_BYTES + 2 * NST * QT_BYTES + DS_BYTES + DQ_BYTES + 1024;
-  static constexpr int THREADS = 512;
+      KV_BUFS * 2 * KV_BYTES + 2 * NST * QT_BYTES + DS_BYTES + STG_BYTES + 1024;
+  static constexpr int THREADS = (D == 64) ? 448 : 512;   // one or three issuer warps
   static constexpr uint32_t TMEM_COLS = 512;
   // TMEM columns.  S^T and dP^T are BM fp32 columns each; P^T and dS^T are
-  // packed bf16 pairs (BM / 2 columns each).  D = 128 (BM = 64) gives every
-  // operand its own columns.  D = 64 (BM = 128) has no room for that: P^T is
-  // written over the S^T columns it came from (each thread over its own
-  // columns), so S^T of the next step waits until dV has consumed P^T, and the
-  // dS pass reads P back (bf16) from there instead of keeping it in registers.
-  static constexpr bool PT_ALIAS = (D == 64);
+  // packed bf16 pairs (BM / 2 columns each), P^T in columns of its own so that
+  // S^T of the next step can be issued as soon as S^T of this one has been read.
+  // D = 64 (BM = 128) has no room left for dS^T: dK reads dS^T from the bf16
+  // dS tile in shared memory (the tile the dQ GEMM reads), as a K-major A.
+  //   D = 64:  S^T 0..127, dP^T 128..255, dV 256, dK 320, dQ 384, P^T 448
+  //   D = 128: S^T 0..63, dP^T 64..127, dV 128, dK 256, dQ 384, P^T 448, dS^T 480
+  static constexpr bool DK_SS = (D == 64);
   static constexpr uint32_t COL_S = 0;                // S^T (fp32)
   static constexpr uint32_t COL_DP = BM;              // dP^T (fp32)
-  // D = 64:  S^T|P^T 0..127, dP^T 128..255, dS^T 256..319, dV 320, dK 384, dQ 448
-  // D = 128: S^T 0..63, dP^T 64..127, dV 128, dK 256, dQ 384, P^T 448, dS^T 480
-  static constexpr uint32_t COL_DV = PT_ALIAS ? 2 * BM + BM / 2 : 2 * BM;
+  static constexpr uint32_t COL_DV = 2 * BM;
   static constexpr uint32_t COL_DK = COL_DV + D;
   static constexpr uint32_t COL_DQ = COL_DK + D;      // one 64-column dQ tile
-  static constexpr uint32_t COL_PT = PT_ALIAS ? COL_S : COL_DQ + 64;
-  static constexpr uint32_t COL_DST = PT_ALIAS ? 2 * BM : COL_PT + BM / 2;
-  static_assert(COL_DQ + 64 + (PT_ALIAS ? 0 : BM) <= TMEM_COLS, "TMEM budget");
-  // dK/dV leave through the dQ staging tile: both at once for D = 64, one
-  // after the other for D = 128
-  static_assert((D == 64 ? 2 : 1) * BN * D * 2 <= DQ_BYTES, "dK/dV staging");
-  // TMEM column (relative to COL_PT) of the packed P^T columns of K-step kk
-  // (16 queries).  Dedicated region: 8 per step.  Aliased: the warpgroup w =
-  // 16 kk / HALF keeps its HALF/2 packed columns at the start of its own
-  // HALF-column range of S^T.
-  __host__ __device__ static constexpr uint32_t pt_col(int kk) {
-    return PT_ALIAS ? (16 * kk / HALF) * HALF + (16 * kk % HALF) / 2 : 8 * kk;
-  }
+  static constexpr uint32_t COL_PT = COL_DQ + 64;
+  static constexpr uint32_t COL_DST = COL_PT + BM / 2;
+  static_assert(COL_DST + (DK_SS ? 0 : BM / 2) <= TMEM_COLS, "TMEM budget");
+  // dK and dV leave one after the other through the staging tile
+  static_assert(BN * D * 2 <= STG_BYTES, "dK/dV staging");
+  static_assert(SMEM <= 227 * 1024 - 4096, "shared memory budget");
 };
 
 // One work item: K/V tile `jt` (rows kv0 .. kv0 + 127 of the sequence) of kv
@@ -127,13 +123,15 @@ __device__ __forceinline__ bool next_bwd_item(const Problem& p, int total, int n
   return false;
 }
 
-// Warp roles (512 threads): 0..7 P/dS (two warpgroups, each owns half of the
-// query columns of every KV row), 8..11 dQ drain and dK/dV epilogue, 12 TMA,
-// 13..15 MMA issuers (S^T and dP^T; dV and dK; dQ).  The issuers run
+// Warp roles: 0..7 P/dS (two warpgroups, each owns half of the query columns
+// of every KV row), 8..11 dQ drain and dK/dV epilogue, 12 TMA, then the MMA
+// issuers: D = 64 one warp (13) that interleaves independent GEMMs; D = 128
+// three warps (13: S^T and dP^T; 14: dV and dK; 15: dQ) that run
 // independently, synchronized only through the data they exchange, so a
-// step's five GEMMs start as soon as their own operands are ready.
+// step's GEMMs start as soon as their own operands are ready (measured faster
+// for the shorter P/dS passes of 64-row query tiles).
 template <int D>
-__global__ void __launch_bounds__(512, 1)
+__global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                     const __grid_constant__ CUtensorMap tmDQ, const __grid_constant__ CUtensorMap tmdK,
@@ -154,8 +152,10 @@ __global__ void __launch_bounds__(512, 1)
 
   __shared__ uint64_t bar_kv_full[C::KV_BUFS], bar_kv_empty[C::KV_BUFS];
   __shared__ uint64_t bar_qfull[C::NST], bar_qempty[C::NST];
-  __shared__ uint64_t bar_s, bar_dp, bar_p, bar_ds, bar_pt_done, bar_dst_done, bar_dss_free;
-  __shared__ uint64_t bar_s_free, bar_dp_free, bar_done, bar_dq_full, bar_dq_empty;
+  __shared__ uint64_t bar_s, bar_dp, bar_p, bar_ds, bar_pt_done, bar_ds_free;
+  __shared__ uint64_t bar_done, bar_dq_full, bar_dq_empty;
+  // D = 128 (three issuers): S^T / dP^T read, dS^T consumed by dK, dS tile by dQ
+  __shared__ uint64_t bar_s_free, bar_dp_free, bar_dst_done, bar_dss_free;
   __shared__ uint64_t bar_dv_empty, bar_dk_empty;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_flag;
@@ -172,21 +172,22 @@ __global__ void __launch_bounds__(512, 1)
     abort_flag = 0;
     for (int b = 0; b < C::KV_BUFS; ++b) {
       mbar_init(&bar_kv_full[b], 1);
-      mbar_init(&bar_kv_empty[b], 2);   // S/dP issuer and dQ issuer
+      mbar_init(&bar_kv_empty[b], D == 64 ? 1 : 2);   // D = 128: S/dP and dQ issuers
     }
     for (int s = 0; s < C::NST; ++s) {
       mbar_init(&bar_qfull[s], 1);
-      mbar_init(&bar_qempty[s], 2);     // S/dP issuer and dV/dK issuer
+      mbar_init(&bar_qempty[s], D == 64 ? 1 : 2);     // D = 128: S/dP and dV/dK issuers
     }
     mbar_init(&bar_s, 1);
     mbar_init(&bar_dp, 1);
     mbar_init(&bar_p, 256);
     mbar_init(&bar_ds, 256);
     mbar_init(&bar_pt_done, 1);
-    mbar_init(&bar_dst_done, 1);
-    mbar_init(&bar_dss_free, 1);
+    mbar_init(&bar_ds_free, 1);
     mbar_init(&bar_s_free, 256);
     mbar_init(&bar_dp_free, 256);
+    mbar_init(&bar_dst_done, 1);
+    mbar_init(&bar_dss_free, 1);
     mbar_init(&bar_done, 1);
     mbar_init(&bar_dq_full, 1);
     mbar_init(&bar_dq_empty, 128);
@@ -238,8 +239,135 @@ __global__ void __launch_bounds__(512, 1)
         ++ic;
       }
     }
-  } else if (warp == 13) {
-    // ---------------- issuer 1: S^T = K Q_i^T, dP^T = V dO_i^T ----------------
+  } else if (D == 64 && warp == 13) {
+    // ---------------- D = 64: one MMA issuer ----------------
+    // MMAs into one accumulator run one after the other (each K-step waits
+    // for the previous one), while MMAs into different accumulators overlap
+    // in the tensor pipe.  So the GEMMs that become ready together are issued
+    // with their K-steps interleaved, in two phases per step g:
+    //   after P(g):  dV(g) with S^T(g+1)
+    //   after dS(g): dK(g) and dQ(g) with dP^T(g+1)
+    // Step g+1's S^T/dP^T are issued here when its K/V tile is resident
+    // (same item, or a second K/V buffer); otherwise at the start of its item.
+    if (lane_id() == 0) {
+      constexpr int KS = D / 16;     // K-steps of S^T and dP^T
+      constexpr int KV = BM / 16;    // K-steps of dV and dK
+      constexpr int KQ = BN / 16;    // K-steps of dQ
+      const uint32_t idSD = idesc_bf16(128, BM, false, false);
+      const uint32_t idKV = idesc_bf16(128, D, false, true);
+      const uint32_t idQ = idesc_bf16(128, 64, true, true);
+      const uint64_t dQ_k0 = desc_kmajor_base(smem_u32(sQ));
+      const uint64_t ddO_k0 = desc_kmajor_base(smem_u32(sdO));
+      const uint64_t dQ_mn0 = desc_mnmajor_base(smem_u32(sQ), BM);
+      const uint64_t ddO_mn0 = desc_mnmajor_base(smem_u32(sdO), BM);
+      const uint64_t ddS_mn = desc_mnmajor_base(smem_u32(sdS), BN);
+      const uint64_t ddS_k = desc_kmajor_base(smem_u32(sdS));
+      auto issue_s = [&](int kb, int st, int kk) {
+        umma_ss(tmem + C::COL_S, desc_advance(desc_kmajor_base(smem_u32(sK(kb))), kmajor_step_bytes(BN, kk)),
+                desc_advance(dQ_k0, st * C::QT_BYTES + kmajor_step_bytes(BM, kk)), idSD, kk > 0);
+      };
+      auto issue_dp = [&](int kb, int st, int kk) {
+        umma_ss(tmem + C::COL_DP, desc_advance(desc_kmajor_base(smem_u32(sV(kb))), kmajor_step_bytes(BN, kk)),
+                desc_advance(ddO_k0, st * C::QT_BYTES + kmajor_step_bytes(BM, kk)), idSD, kk > 0);
+      };
+      // S^T and dP^T of one step, interleaved (both operands resident)
+      auto issue_sdp = [&](int kb, int st) {
+#pragma unroll
+        for (int kk = 0; kk < KS; ++kk) {
+          issue_s(kb, st, kk);
+          issue_dp(kb, st, kk);
+        }
+        umma_commit(&bar_s);
+        umma_commit(&bar_dp);
+      };
+      BwdItem w, wn;
+      int k = 0, ic = 0, gs = 0;
+      bool ok = true;
+      bool have = next_bwd_item<BN, BM>(p, total, a.n_x, a.x_major, k, w);
+      bool sdp_done = false;   // S^T/dP^T of the next step already issued
+      while (ok && have) {
+        const int kb = ic % C::KV_BUFS, ku = ic / C::KV_BUFS;
+        const bool have_next = next_bwd_item<BN, BM>(p, total, a.n_x, a.x_major, k, wn);
+        const int kbn = (ic + 1) % C::KV_BUFS, kun = (ic + 1) / C::KV_BUFS;
+        if (!mbar_wait(&bar_kv_full[kb], ku & 1, ac)) break;
+        const uint64_t dK_mn = desc_mnmajor_base(smem_u32(sK(kb)), BN);
+        for (int it = 0; it < w.n_it; ++it) {
+          const int g = gs + it;
+          const int st = g % C::NST;
+          if (!sdp_done) {
+            if (!mbar_wait(&bar_qfull[st], (g / C::NST) & 1, ac)) { ok = false; break; }
+            tc_fence_after();
+            issue_sdp(kb, st);
+          }
+          // step g+1: its K/V buffer and whether its S^T/dP^T go out now
+          const bool last = it + 1 == w.n_it;
+          const bool nx = !last || (have_next && C::KV_BUFS > 1);
+          const int kb1 = last ? kbn : kb;
+          const int st1 = (g + 1) % C::NST;
+          // ---- phase A: dV(g) [+ S^T(g+1)] ----
+          if (!mbar_wait(&bar_p, g & 1, ac)) { ok = false; break; }
+          if (it == 0 && ic > 0 && !mbar_wait(&bar_dv_empty, (ic - 1) & 1, ac)) { ok = false; break; }
+          if (nx && last && !mbar_wait(&bar_kv_full[kbn], kun & 1, ac)) { ok = false; break; }
+          if (nx && !mbar_wait(&bar_qfull[st1], ((g + 1) / C::NST) & 1, ac)) { ok = false; break; }
+          tc_fence_after();
+          const uint64_t omn = desc_advance(ddO_mn0, st * C::QT_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < (KV > KS ? KV : KS); ++kk) {
+            if (kk < KV)
+              umma_ts(tmem + C::COL_DV, tmem + C::COL_PT + 8 * kk,
+                      desc_advance(omn, mnmajor_step_bytes(kk)), idKV, (it > 0 || kk > 0) ? 1u : 0u);
+            if (nx && kk < KS) {
+              issue_s(kb1, st1, kk);
+              if (kk == KS - 1) umma_commit(&bar_s);
+            }
+          }
+          umma_commit(&bar_pt_done);
+          // ---- phase B: dK(g), dQ(g) [+ dP^T(g+1)] ----
+          if (!mbar_wait(&bar_ds, g & 1, ac)) { ok = false; break; }
+          if (!mbar_wait(&bar_dq_empty, (g & 1) ^ 1, ac)) { ok = false; break; }
+          if (it == 0 && ic > 0 && !mbar_wait(&bar_dk_empty, (ic - 1) & 1, ac)) { ok = false; break; }
+          tc_fence_after();
+          const uint64_t qmn = desc_advance(dQ_mn0, st * C::QT_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < (KQ > KV ? KQ : KV); ++kk) {
+            if (kk < KV) {
+              const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
+              if constexpr (C::DK_SS)   // A = dS^T [kv][query] from the dS tile (K-major)
+                umma_ss(tmem + C::COL_DK, desc_advance(ddS_k, kmajor_step_bytes(BN, kk)),
+                        desc_advance(qmn, mnmajor_step_bytes(kk)), idKV, acc);
+              else
+                umma_ts(tmem + C::COL_DK, tmem + C::COL_DST + 8 * kk,
+                        desc_advance(qmn, mnmajor_step_bytes(kk)), idKV, acc);
+            }
+            if (kk < KQ) {
+              if (D == 64)   // dQ[q, d] = dS[q, kv] K[kv, d]
+                umma_ss(tmem + C::COL_DQ, desc_advance(ddS_mn, mnmajor_step_bytes(kk)),
+                        desc_advance(dK_mn, mnmajor_step_bytes(kk)), idQ, kk > 0);
+              else           // dQ^T[d, q] = K^T[d, kv] dS^T[kv, q]
+                umma_ss(tmem + C::COL_DQ, desc_advance(dK_mn, mnmajor_step_bytes(kk)),
+                        desc_advance(ddS_mn, mnmajor_step_bytes(kk)), idQ, kk > 0);
+            }
+            if (nx && kk < KS) {
+              issue_dp(kb1, st1, kk);
+              if (kk == KS - 1) umma_commit(&bar_dp);
+            }
+          }
+          umma_commit(&bar_dq_full);
+          umma_commit(&bar_ds_free);
+          umma_commit(&bar_qempty[st]);
+          sdp_done = nx;
+        }
+        if (!ok) break;
+        umma_commit(&bar_done);   // dV and dK of this item are final
+        umma_commit(&bar_kv_empty[kb]);
+        gs += w.n_it;
+        ++ic;
+        w = wn;
+        have = have_next;
+      }
+    }
+  } else if (D != 64 && warp == 13) {
+    // ---------------- D = 128 issuer 1: S^T = K Q_i^T, dP^T = V dO_i^T ----------------
     if (lane_id() == 0) {
       const uint32_t idSD = idesc_bf16(128, BM, false, false);
       const uint64_t dQ_k0 = desc_kmajor_base(smem_u32(sQ));
@@ -256,13 +384,8 @@ __global__ void __launch_bounds__(512, 1)
           const int g = gs + it;
           const int st = g % C::NST;
           if (!mbar_wait(&bar_qfull[st], (g / C::NST) & 1, ac)) { ok = false; break; }
-          // S^T region is free once the P/dS warps have read S^T(g-1) (and,
-          // when P^T lives there, read P^T(g-1) back and dV(g-1) consumed it)
+          // S^T region is free once the P pass has read S^T(g-1)
           if (g > 0 && !mbar_wait(&bar_s_free, (g - 1) & 1, ac)) { ok = false; break; }
-          if (C::PT_ALIAS && g > 0 && !mbar_wait(&bar_pt_done, (g - 1) & 1, ac)) {
-            ok = false;
-            break;
-          }
           tc_fence_after();
           const uint64_t qd = desc_advance(dQ_k0, st * C::QT_BYTES);
 #pragma unroll
@@ -270,9 +393,8 @@ __global__ void __launch_bounds__(512, 1)
             umma_ss(tmem + C::COL_S, desc_advance(dK_k, kmajor_step_bytes(BN, kk)),
                     desc_advance(qd, kmajor_step_bytes(BM, kk)), idSD, kk > 0);
           umma_commit(&bar_s);
-          // dP^T region is free once dP^T(g-1) has been read (with P^T
-          // aliased, s_free already covers that read)
-          if (!C::PT_ALIAS && g > 0 && !mbar_wait(&bar_dp_free, (g - 1) & 1, ac)) {
+          // dP^T region is free once the dS pass has read dP^T(g-1)
+          if (g > 0 && !mbar_wait(&bar_dp_free, (g - 1) & 1, ac)) {
             ok = false;
             break;
           }
@@ -291,12 +413,13 @@ __global__ void __launch_bounds__(512, 1)
         ++ic;
       }
     }
-  } else if (warp == 14) {
+  } else if (D != 64 && warp == 14) {
     // ---------------- issuer 2: dV += P^T dO_i, dK += dS^T Q_i (A from TMEM) ----
     if (lane_id() == 0) {
       const uint32_t idKV = idesc_bf16(128, D, false, true);
       const uint64_t dQ_mn0 = desc_mnmajor_base(smem_u32(sQ), BM);
       const uint64_t ddO_mn0 = desc_mnmajor_base(smem_u32(sdO), BM);
+      const uint64_t ddS_k = desc_kmajor_base(smem_u32(sdS));
       BwdItem w;
       int k = 0, ic = 0, gs = 0;
       bool ok = true;
@@ -315,7 +438,7 @@ __global__ void __launch_bounds__(512, 1)
           const uint64_t omn = desc_advance(ddO_mn0, st * C::QT_BYTES);
 #pragma unroll
           for (int kk = 0; kk < BM / 16; ++kk)
-            umma_ts(tmem + C::COL_DV, tmem + C::COL_PT + C::pt_col(kk),
+            umma_ts(tmem + C::COL_DV, tmem + C::COL_PT + 8 * kk,
                     desc_advance(omn, mnmajor_step_bytes(kk)), idKV, (it > 0 || kk > 0) ? 1u : 0u);
           umma_commit(&bar_pt_done);
           if (!mbar_wait(&bar_ds, g & 1, ac)) { ok = false; break; }
@@ -326,9 +449,15 @@ __global__ void __launch_bounds__(512, 1)
           tc_fence_after();
           const uint64_t qmn = desc_advance(dQ_mn0, st * C::QT_BYTES);
 #pragma unroll
-          for (int kk = 0; kk < BM / 16; ++kk)
-            umma_ts(tmem + C::COL_DK, tmem + C::COL_DST + 8 * kk,
-                    desc_advance(qmn, mnmajor_step_bytes(kk)), idKV, (it > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < BM / 16; ++kk) {
+            const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
+            if constexpr (C::DK_SS)   // A = dS^T [kv][query] from the dS tile (K-major)
+              umma_ss(tmem + C::COL_DK, desc_advance(ddS_k, kmajor_step_bytes(BN, kk)),
+                      desc_advance(qmn, mnmajor_step_bytes(kk)), idKV, acc);
+            else
+              umma_ts(tmem + C::COL_DK, tmem + C::COL_DST + 8 * kk,
+                      desc_advance(qmn, mnmajor_step_bytes(kk)), idKV, acc);
+          }
           umma_commit(&bar_dst_done);
           umma_commit(&bar_qempty[st]);
         }
@@ -338,7 +467,7 @@ __global__ void __launch_bounds__(512, 1)
         ++ic;
       }
     }
-  } else if (warp == 15) {
+  } else if (D != 64 && warp == 15) {
     // ---------------- issuer 3: dQ (both operands in shared memory) ----------
     if (lane_id() == 0) {
       const uint32_t idQ = idesc_bf16(128, 64, true, true);
@@ -400,7 +529,7 @@ __global__ void __launch_bounds__(512, 1)
     };
     const uint32_t tSme = tmem + lane_base + C::COL_S + c0;      // this thread's S columns
     const uint32_t tDPme = tmem + lane_base + C::COL_DP + c0;    // this thread's dP columns
-    const uint32_t tPTme = tmem + lane_base + C::COL_PT + (C::PT_ALIAS ? c0 : c0 / 2);
+    const uint32_t tPTme = tmem + lane_base + C::COL_PT + c0 / 2;
     const uint32_t tDSTme = tmem + lane_base + C::COL_DST + c0 / 2;
     BwdItem w;
     int k = 0, gs = 0;
@@ -428,14 +557,18 @@ __global__ void __launch_bounds__(512, 1)
         // ---- P^T (KV row r, query columns c0 .. c0 + HALF) ----
         if (!mbar_wait(&bar_s, g & 1, ac)) { ok = false; break; }
         tc_fence_after();
-        if constexpr (C::PT_ALIAS) {
+        if constexpr (D == 64) {
           // D = 64: both passes run as rolled loops over 32-column chunks.  The
           // smaller loop body keeps the hot code of the eight P/dS warps, the
-          // drain warps and the issuers small enough to stay in the
+          // drain warps and the issuer small enough to stay in the
           // instruction cache (measured ~15% faster per step than the fully
-          // unrolled 64-column body), and frees registers.
+          // unrolled 64-column body), and frees registers.  P comes back from
+          // the P^T columns in the dS pass.
           const int lim_all = !kv_ok ? HALF : ((p.causal && q0 < w.kv0 + BN) ? kv - q0 - c0 : 0);
           const uint64_t sl2x2 = f2_pack(sl2, sl2);
+          // P^T(g-1) must have been consumed by dV(g-1)
+          if (g > 0 && !mbar_wait(&bar_pt_done, (g - 1) & 1, ac)) { ok = false; break; }
+          tc_fence_after();
 #pragma unroll 1
           for (int c1 = 0; c1 < HALF; c1 += 32) {
             uint32_t u[32];
@@ -465,8 +598,8 @@ __global__ void __launch_bounds__(512, 1)
           tc_fence_before();
           mbar_arrive(&bar_p);
           if (!mbar_wait(&bar_dp, g & 1, ac)) { ok = false; break; }
-          if (g > 0 && !mbar_wait(&bar_dst_done, (g - 1) & 1, ac)) { ok = false; break; }
-          if (g > 0 && !mbar_wait(&bar_dss_free, (g - 1) & 1, ac)) { ok = false; break; }
+          // dK(g-1) and dQ(g-1) have consumed the dS tile
+          if (g > 0 && !mbar_wait(&bar_ds_free, (g - 1) & 1, ac)) { ok = false; break; }
           tc_fence_after();
 #pragma unroll 1
           for (int c1 = 0; c1 < HALF; c1 += 32) {
@@ -474,10 +607,6 @@ __global__ void __launch_bounds__(512, 1)
             tmem_ld32_nowait(tDPme + c1, u);
             tmem_ld16_nowait(tPTme + c1 / 2, pp);
             tmem_wait_ld();
-            if (c1 + 32 == HALF) {
-              tc_fence_before();
-              mbar_arrive(&bar_s_free);
-            }
             uint32_t pk[16];
 #pragma unroll
             for (int c = 0; c < 32; c += 4) {
@@ -493,7 +622,6 @@ __global__ void __launch_bounds__(512, 1)
                                                                  __uint_as_float(u[c + 3])),
                                                          f2_pack(d4.z, d4.w)), pb));
             }
-            tmem_st16p(tDSTme + c1 / 2, pk);
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
               const int ch = (c0 + c1) / 8 + i;
@@ -505,17 +633,15 @@ __global__ void __launch_bounds__(512, 1)
         } else {
         // P^T in fp32 pairs: p2[i] = (P[2i], P[2i+1]) of this thread's
         // columns; kept for the dS pass unless P^T is read back from TMEM there
-        uint64_t p2[C::PT_ALIAS ? 1 : HALF / 2];
+        uint64_t p2[HALF / 2];
         uint32_t pk[HALF / 2];
         {
           uint32_t u[HALF];
 #pragma unroll
           for (int c = 0; c < HALF; c += 32) tmem_ld32_nowait(tSme + c, u + c);
           tmem_wait_ld();
-          if constexpr (!C::PT_ALIAS) {
-            tc_fence_before();
-            mbar_arrive(&bar_s_free);
-          }
+          tc_fence_before();
+          mbar_arrive(&bar_s_free);
           // masking on S: the whole row past the sequence end, the causal
           // triangle on diagonal tiles (columns c < lim hold earlier queries)
           int lim = 0;
@@ -539,19 +665,13 @@ __global__ void __launch_bounds__(512, 1)
             const uint64_t q23 = f2_pack(ex2(a2), ex2(a3));
             pk[c / 2] = f2_to_bf16x2(q01);
             pk[c / 2 + 1] = f2_to_bf16x2(q23);
-            if constexpr (!C::PT_ALIAS) {
-              p2[c / 2] = q01;
-              p2[c / 2 + 1] = q23;
-            }
+            p2[c / 2] = q01;
+            p2[c / 2 + 1] = q23;
           }
         }
-        if constexpr (!C::PT_ALIAS) {
-          // P^T(g-1) must have been consumed by dV(g-1)
-          if (g > 0 && !mbar_wait(&bar_pt_done, (g - 1) & 1, ac)) { ok = false; break; }
-          tc_fence_after();
-        }
-        // (aliased: S^T(g) was issued after dV(g-1) completed, so the
-        // columns hold nothing that is still to be read)
+        // P^T(g-1) must have been consumed by dV(g-1)
+        if (g > 0 && !mbar_wait(&bar_pt_done, (g - 1) & 1, ac)) { ok = false; break; }
+        tc_fence_after();
         if constexpr (HALF / 2 == 32) tmem_st32(tPTme, pk);
         else tmem_st16p(tPTme, pk);
         tmem_wait_st();
@@ -561,13 +681,8 @@ __global__ void __launch_bounds__(512, 1)
         if (!mbar_wait(&bar_dp, g & 1, ac)) { ok = false; break; }
         tc_fence_after();
         {
-          // dP^T in column chunks of 32 (fewer live registers); with P^T
-          // aliased, P (bf16 pairs) comes back from the S^T columns
+          // dP^T in column chunks of 32 (fewer live registers)
           constexpr int CH = HALF < 32 ? HALF : 32;
-          if constexpr (C::PT_ALIAS) {
-            if constexpr (HALF / 2 == 32) tmem_ld32_nowait(tPTme, pk);
-            else tmem_ld16_nowait(tPTme, pk);
-          }
 #pragma unroll
           for (int c1 = 0; c1 < HALF; c1 += CH) {
             uint32_t u[CH];
@@ -575,23 +690,14 @@ __global__ void __launch_bounds__(512, 1)
             else tmem_ld16_nowait(tDPme + c1, u);
             tmem_wait_ld();
             if (c1 + CH == HALF) {
-              // every read of the S^T / dP^T columns of this step is done
+              // every read of the dP^T columns of this step is done
               tc_fence_before();
-              mbar_arrive(C::PT_ALIAS ? &bar_s_free : &bar_dp_free);
+              mbar_arrive(&bar_dp_free);
             }
 #pragma unroll
             for (int cc = 0; cc < CH; cc += 4) {
               const int c = c1 + cc;
-              uint64_t pa, pb;
-              if constexpr (C::PT_ALIAS) {
-                pa = f2_pack(__uint_as_float(pk[c / 2] << 16),
-                             __uint_as_float(pk[c / 2] & 0xffff0000u));
-                pb = f2_pack(__uint_as_float(pk[c / 2 + 1] << 16),
-                             __uint_as_float(pk[c / 2 + 1] & 0xffff0000u));
-              } else {
-                pa = p2[c / 2];
-                pb = p2[c / 2 + 1];
-              }
+              const uint64_t pa = p2[c / 2], pb = p2[c / 2 + 1];
               const float4 d4 = *reinterpret_cast<const float4*>(&s_delta[buf][c0 + c]);
               const uint64_t ds01 = f2_mul(f2_sub(f2_pack(__uint_as_float(u[cc]),
                                                           __uint_as_float(u[cc + 1])),
@@ -632,13 +738,15 @@ __global__ void __launch_bounds__(512, 1)
   } else {
     // ---------------- dQ drain and dK/dV epilogue (warps 8..11) ----------------
     // dQ: TMEM -> fp32 staging tile in shared memory -> reduce-add into the
-    // accumulator (ATOMIC) or store into this KV tile's slab (SPLIT).  With
-    // dq_tma (D = 64) the tile is staged as two 32-column boxes in the 128-byte
-    // swizzled layout of the accumulator's tensor map (one query row per
-    // thread, conflict-free) and leaves through two TMA tensor copies, clipped
-    // at the end of the rows by the map; otherwise it is staged row-major
-    // [query][dim] (the layout of one head's rows in the head-major
-    // accumulator) and leaves through one bulk copy of the valid rows.
+    // accumulator (ATOMIC) or store into this KV tile's slab (SPLIT).  D = 64
+    // leaves in two halves: with dq_tma each 32-column box is staged in the
+    // 128-byte swizzled layout of the accumulator's tensor map (one query row
+    // per thread, conflict-free) and leaves through one TMA tensor copy,
+    // clipped at the end of the rows by the map; otherwise 64 query rows at a
+    // time are staged row-major [query][dim] (the layout of one head's rows in
+    // the head-major accumulator) and leave through one bulk copy of the valid
+    // rows.  D = 128 stages the whole tile ([query][dim], lane = dim) and
+    // leaves through one bulk copy.
     // dK / dV: at the end of every item, TMEM -> bf16 (dK x scale) -> the same
     // staging tile in the 128-byte swizzled layout of the dK/dV tensor maps ->
     // TMA stores; a THD tile that ends past its sequence is written row by row
@@ -678,50 +786,70 @@ __global__ void __launch_bounds__(512, 1)
         tmem_wait_ld();
         tc_fence_before();
         mbar_arrive(&bar_dq_empty);
-        if (t == 0) bulk_wait_read<0>();   // previous copy finished reading the tile
-        named_bar_sync(2, 128);
-        if (D == 64 && a.dq_tma) {
+        if constexpr (D == 64) {
+          // two halves through the staging tile: the two 32-dim boxes of the
+          // accumulator's map (dq_tma), else query rows 0..63 and 64..127
 #pragma unroll
-          for (int c = 0; c < 16; ++c) {
-            const uint32_t off = (c >> 3) * (BM * 128) + t * 128 + ((((c & 7) ^ (t & 7))) << 4);
-            *reinterpret_cast<float4*>(stg + off) =
-                make_float4(__uint_as_float(u[4 * c]), __uint_as_float(u[4 * c + 1]),
-                            __uint_as_float(u[4 * c + 2]), __uint_as_float(u[4 * c + 3]));
+          for (int hx = 0; hx < 2; ++hx) {
+            if (t == 0) bulk_wait_read<0>();   // previous copy finished reading the tile
+            named_bar_sync(2, 128);
+            if (a.dq_tma) {
+#pragma unroll
+              for (int c = 0; c < 8; ++c) {
+                const int cc = 8 * hx + c;
+                const uint32_t off = t * 128 + ((c ^ (t & 7)) << 4);
+                *reinterpret_cast<float4*>(stg + off) =
+                    make_float4(__uint_as_float(u[4 * cc]), __uint_as_float(u[4 * cc + 1]),
+                                __uint_as_float(u[4 * cc + 2]), __uint_as_float(u[4 * cc + 3]));
+              }
+            } else if ((t >> 6) == hx) {
+              // lane = query row, 64 columns = head dims
+              float4* row = reinterpret_cast<float4*>(sDQ + (t & 63) * D);
+#pragma unroll
+              for (int c = 0; c < 16; ++c)
+                row[c] = make_float4(__uint_as_float(u[4 * c]), __uint_as_float(u[4 * c + 1]),
+                                     __uint_as_float(u[4 * c + 2]), __uint_as_float(u[4 * c + 3]));
+            }
+            fence_proxy_async_smem();
+            named_bar_sync(2, 128);
+            if (t == 0 && slab_ok) {
+              if (a.dq_tma) {
+                if (a.split)
+                  tma_store_5d(&tmDQ, stg, hx * 32, w.seq.row0 + q0, h, w.seq.b, w.jt);
+                else
+                  tma_reduce_add_4d(&tmDQ, stg, hx * 32, w.seq.row0 + q0, h, w.seq.b);
+              } else {
+                const int nq = min(64, w.seq.len - q0 - 64 * hx);
+                if (nq > 0) {
+                  float* dst = base + ((static_cast<size_t>(w.seq.b) * p.heads_q + h) *
+                                           p.rows_total + w.seq.row0 + q0 + 64 * hx) * D;
+                  if (a.split)
+                    bulk_store(dst, sDQ, static_cast<uint32_t>(nq) * D * 4);
+                  else
+                    bulk_reduce_add_f32(dst, sDQ, static_cast<uint32_t>(nq) * D * 4);
+                }
+              }
+              bulk_commit();
+            }
           }
-        } else if (D == 64) {
-          // lane = query row, 64 columns = head dims
-          float4* row = reinterpret_cast<float4*>(sDQ + t * D);
-#pragma unroll
-          for (int c = 0; c < 16; ++c)
-            row[c] = make_float4(__uint_as_float(u[4 * c]), __uint_as_float(u[4 * c + 1]),
-                                 __uint_as_float(u[4 * c + 2]), __uint_as_float(u[4 * c + 3]));
         } else {
+          if (t == 0) bulk_wait_read<0>();   // previous copy finished reading the tile
+          named_bar_sync(2, 128);
           // lane = head dim, 64 columns = query rows
 #pragma unroll
           for (int c = 0; c < 64; ++c) sDQ[c * D + t] = __uint_as_float(u[c]);
-        }
-        fence_proxy_async_smem();
-        named_bar_sync(2, 128);
-        if (t == 0 && slab_ok && a.dq_tma) {
-#pragma unroll
-          for (int pn = 0; pn < D / 32; ++pn) {
+          fence_proxy_async_smem();
+          named_bar_sync(2, 128);
+          if (t == 0 && slab_ok) {
+            const int nq = min(BM, w.seq.len - q0);
+            float* dst = base + ((static_cast<size_t>(w.seq.b) * p.heads_q + h) * p.rows_total +
+                                 w.seq.row0 + q0) * D;
             if (a.split)
-              tma_store_5d(&tmDQ, stg + pn * (BM * 128), pn * 32, w.seq.row0 + q0, h, w.seq.b,
-                           w.jt);
+              bulk_store(dst, sDQ, static_cast<uint32_t>(nq) * D * 4);
             else
-              tma_reduce_add_4d(&tmDQ, stg + pn * (BM * 128), pn * 32, w.seq.row0 + q0, h,
-                                w.seq.b);
+              bulk_reduce_add_f32(dst, sDQ, static_cast<uint32_t>(nq) * D * 4);
+            bulk_commit();
           }
-          bulk_commit();
-        } else if (t == 0 && slab_ok) {
-          const int nq = min(BM, w.seq.len - q0);
-          float* dst = base + ((static_cast<size_t>(w.seq.b) * p.heads_q + h) * p.rows_total +
-                               w.seq.row0 + q0) * D;
-          if (a.split)
-            bulk_store(dst, sDQ, static_cast<uint32_t>(nq) * D * 4);
-          else
-            bulk_reduce_add_f32(dst, sDQ, static_cast<uint32_t>(nq) * D * 4);
-          bulk_commit();
         }
       }
       if (!ok) break;
@@ -731,19 +859,16 @@ __global__ void __launch_bounds__(512, 1)
       const int kv = w.kv0 + t;
       const bool rows_exact = p.cu_seqlens != nullptr && w.kv0 + BN > w.seq.len;
       const size_t grow = static_cast<size_t>(w.seq.b) * p.rows_total + w.seq.row0 + kv;
-      // dV first (the next item's first MMA overwrites it first), then dK;
-      // each in panels of 64 dims staged at panel * BN * 128 (D = 64 keeps dK
-      // in the second half of the tile, D = 128 reuses the tile for dK)
+      // dV first (the next item's first MMA overwrites it first), then dK,
+      // each in panels of 64 dims staged at panel * BN * 128 of the tile
 #pragma unroll
       for (int which = 0; which < 2; ++which) {
         const uint32_t col = which == 0 ? C::COL_DV : C::COL_DK;
         const float mul = which == 0 ? 1.0f : p.scale;
-        uint8_t* tile = stg + ((D == 64 && which == 1) ? BN * 128 : 0);
+        uint8_t* tile = stg;
         __nv_bfloat16* gdst = (which == 0 ? a.dv : a.dk) + (grow * p.heads_kv + w.hk) * D;
-        if (which == 0 || D == 128) {
-          if (t == 0) bulk_wait_read<0>();   // the staging tile is free again
-          named_bar_sync(2, 128);
-        }
+        if (t == 0) bulk_wait_read<0>();   // the staging tile is free again
+        named_bar_sync(2, 128);
 #pragma unroll
         for (int pn = 0; pn < PANELS; ++pn) {
           uint32_t x[64];

@@ -249,7 +249,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     //   after dS(g): dK(g) and dQ(g) with dP^T(g+1)
     // Step g+1's S^T/dP^T are issued here when its K/V tile is resident
     // (same item, or a second K/V buffer); otherwise at the start of its item.
-    if (lane_id() == 0) {
+    {   // warp-uniform: one elected lane issues
       constexpr int KS = D / 16;     // K-steps of S^T and dP^T
       constexpr int KV = BM / 16;    // K-steps of dV and dK
       constexpr int KQ = BN / 16;    // K-steps of dQ
@@ -263,11 +263,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       const uint64_t ddS_mn = desc_mnmajor_base(smem_u32(sdS), BN);
       const uint64_t ddS_k = desc_kmajor_base(smem_u32(sdS));
       auto issue_s = [&](int kb, int st, int kk) {
-        umma_ss(tmem + C::COL_S, desc_advance(desc_kmajor_base(smem_u32(sK(kb))), kmajor_step_bytes(BN, kk)),
+        umma_ss_w(tmem + C::COL_S, desc_advance(desc_kmajor_base(smem_u32(sK(kb))), kmajor_step_bytes(BN, kk)),
                 desc_advance(dQ_k0, st * C::QT_BYTES + kmajor_step_bytes(BM, kk)), idSD, kk > 0);
       };
       auto issue_dp = [&](int kb, int st, int kk) {
-        umma_ss(tmem + C::COL_DP, desc_advance(desc_kmajor_base(smem_u32(sV(kb))), kmajor_step_bytes(BN, kk)),
+        umma_ss_w(tmem + C::COL_DP, desc_advance(desc_kmajor_base(smem_u32(sV(kb))), kmajor_step_bytes(BN, kk)),
                 desc_advance(ddO_k0, st * C::QT_BYTES + kmajor_step_bytes(BM, kk)), idSD, kk > 0);
       };
       // S^T and dP^T of one step, interleaved (both operands resident)
@@ -277,8 +277,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
           issue_s(kb, st, kk);
           issue_dp(kb, st, kk);
         }
-        umma_commit(&bar_s);
-        umma_commit(&bar_dp);
+        umma_commit_w(&bar_s);
+        umma_commit_w(&bar_dp);
       };
       BwdItem w, wn;
       int k = 0, ic = 0, gs = 0;
@@ -289,13 +289,13 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         const int kb = ic % C::KV_BUFS, ku = ic / C::KV_BUFS;
         const bool have_next = next_bwd_item<BN, BM>(p, total, a.n_x, a.x_major, k, wn);
         const int kbn = (ic + 1) % C::KV_BUFS, kun = (ic + 1) / C::KV_BUFS;
-        if (!mbar_wait(&bar_kv_full[kb], ku & 1, ac)) break;
+        if (!mbar_wait_w(&bar_kv_full[kb], ku & 1, ac)) break;
         const uint64_t dK_mn = desc_mnmajor_base(smem_u32(sK(kb)), BN);
         for (int it = 0; it < w.n_it; ++it) {
           const int g = gs + it;
           const int st = g % C::NST;
           if (!sdp_done) {
-            if (!mbar_wait(&bar_qfull[st], (g / C::NST) & 1, ac)) { ok = false; break; }
+            if (!mbar_wait_w(&bar_qfull[st], (g / C::NST) & 1, ac)) { ok = false; break; }
             tc_fence_after();
             issue_sdp(kb, st);
           }
@@ -305,27 +305,27 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
           const int kb1 = last ? kbn : kb;
           const int st1 = (g + 1) % C::NST;
           // ---- phase A: dV(g) [+ S^T(g+1)] ----
-          if (!mbar_wait(&bar_p, g & 1, ac)) { ok = false; break; }
-          if (it == 0 && ic > 0 && !mbar_wait(&bar_dv_empty, (ic - 1) & 1, ac)) { ok = false; break; }
-          if (nx && last && !mbar_wait(&bar_kv_full[kbn], kun & 1, ac)) { ok = false; break; }
-          if (nx && !mbar_wait(&bar_qfull[st1], ((g + 1) / C::NST) & 1, ac)) { ok = false; break; }
+          if (!mbar_wait_w(&bar_p, g & 1, ac)) { ok = false; break; }
+          if (it == 0 && ic > 0 && !mbar_wait_w(&bar_dv_empty, (ic - 1) & 1, ac)) { ok = false; break; }
+          if (nx && last && !mbar_wait_w(&bar_kv_full[kbn], kun & 1, ac)) { ok = false; break; }
+          if (nx && !mbar_wait_w(&bar_qfull[st1], ((g + 1) / C::NST) & 1, ac)) { ok = false; break; }
           tc_fence_after();
           const uint64_t omn = desc_advance(ddO_mn0, st * C::QT_BYTES);
 #pragma unroll
           for (int kk = 0; kk < (KV > KS ? KV : KS); ++kk) {
             if (kk < KV)
-              umma_ts(tmem + C::COL_DV, tmem + C::COL_PT + 8 * kk,
+              umma_ts_w(tmem + C::COL_DV, tmem + C::COL_PT + 8 * kk,
                       desc_advance(omn, mnmajor_step_bytes(kk)), idKV, (it > 0 || kk > 0) ? 1u : 0u);
             if (nx && kk < KS) {
               issue_s(kb1, st1, kk);
-              if (kk == KS - 1) umma_commit(&bar_s);
+              if (kk == KS - 1) umma_commit_w(&bar_s);
             }
           }
-          umma_commit(&bar_pt_done);
+          umma_commit_w(&bar_pt_done);
           // ---- phase B: dK(g), dQ(g) [+ dP^T(g+1)] ----
-          if (!mbar_wait(&bar_ds, g & 1, ac)) { ok = false; break; }
-          if (!mbar_wait(&bar_dq_empty, (g & 1) ^ 1, ac)) { ok = false; break; }
-          if (it == 0 && ic > 0 && !mbar_wait(&bar_dk_empty, (ic - 1) & 1, ac)) { ok = false; break; }
+          if (!mbar_wait_w(&bar_ds, g & 1, ac)) { ok = false; break; }
+          if (!mbar_wait_w(&bar_dq_empty, (g & 1) ^ 1, ac)) { ok = false; break; }
+          if (it == 0 && ic > 0 && !mbar_wait_w(&bar_dk_empty, (ic - 1) & 1, ac)) { ok = false; break; }
           tc_fence_after();
           const uint64_t qmn = desc_advance(dQ_mn0, st * C::QT_BYTES);
 #pragma unroll
@@ -333,33 +333,33 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
             if (kk < KV) {
               const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
               if constexpr (C::DK_SS)   // A = dS^T [kv][query] from the dS tile (K-major)
-                umma_ss(tmem + C::COL_DK, desc_advance(ddS_k, kmajor_step_bytes(BN, kk)),
+                umma_ss_w(tmem + C::COL_DK, desc_advance(ddS_k, kmajor_step_bytes(BN, kk)),
                         desc_advance(qmn, mnmajor_step_bytes(kk)), idKV, acc);
               else
-                umma_ts(tmem + C::COL_DK, tmem + C::COL_DST + 8 * kk,
+                umma_ts_w(tmem + C::COL_DK, tmem + C::COL_DST + 8 * kk,
                         desc_advance(qmn, mnmajor_step_bytes(kk)), idKV, acc);
             }
             if (kk < KQ) {
               if (D == 64)   // dQ[q, d] = dS[q, kv] K[kv, d]
-                umma_ss(tmem + C::COL_DQ, desc_advance(ddS_mn, mnmajor_step_bytes(kk)),
+                umma_ss_w(tmem + C::COL_DQ, desc_advance(ddS_mn, mnmajor_step_bytes(kk)),
                         desc_advance(dK_mn, mnmajor_step_bytes(kk)), idQ, kk > 0);
               else           // dQ^T[d, q] = K^T[d, kv] dS^T[kv, q]
-                umma_ss(tmem + C::COL_DQ, desc_advance(dK_mn, mnmajor_step_bytes(kk)),
+                umma_ss_w(tmem + C::COL_DQ, desc_advance(dK_mn, mnmajor_step_bytes(kk)),
                         desc_advance(ddS_mn, mnmajor_step_bytes(kk)), idQ, kk > 0);
             }
             if (nx && kk < KS) {
               issue_dp(kb1, st1, kk);
-              if (kk == KS - 1) umma_commit(&bar_dp);
+              if (kk == KS - 1) umma_commit_w(&bar_dp);
             }
           }
-          umma_commit(&bar_dq_full);
-          umma_commit(&bar_ds_free);
-          umma_commit(&bar_qempty[st]);
+          umma_commit_w(&bar_dq_full);
+          umma_commit_w(&bar_ds_free);
+          umma_commit_w(&bar_qempty[st]);
           sdp_done = nx;
         }
         if (!ok) break;
-        umma_commit(&bar_done);   // dV and dK of this item are final
-        umma_commit(&bar_kv_empty[kb]);
+        umma_commit_w(&bar_done);   // dV and dK of this item are final
+        umma_commit_w(&bar_kv_empty[kb]);
         gs += w.n_it;
         ++ic;
         w = wn;
@@ -368,7 +368,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     }
   } else if (D != 64 && warp == 13) {
     // ---------------- D = 128 issuer 1: S^T = K Q_i^T, dP^T = V dO_i^T ----------------
-    if (lane_id() == 0) {
+    {   // warp-uniform: one elected lane issues
       const uint32_t idSD = idesc_bf16(128, BM, false, false);
       const uint64_t dQ_k0 = desc_kmajor_base(smem_u32(sQ));
       const uint64_t ddO_k0 = desc_kmajor_base(smem_u32(sdO));
@@ -377,24 +377,24 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       bool ok = true;
       while (ok && next_bwd_item<BN, BM>(p, total, a.n_x, a.x_major, k, w)) {
         const int kb = ic % C::KV_BUFS, ku = ic / C::KV_BUFS;
-        if (!mbar_wait(&bar_kv_full[kb], ku & 1, ac)) break;
+        if (!mbar_wait_w(&bar_kv_full[kb], ku & 1, ac)) break;
         const uint64_t dK_k = desc_kmajor_base(smem_u32(sK(kb)));
         const uint64_t dV_k = desc_kmajor_base(smem_u32(sV(kb)));
         for (int it = 0; it < w.n_it; ++it) {
           const int g = gs + it;
           const int st = g % C::NST;
-          if (!mbar_wait(&bar_qfull[st], (g / C::NST) & 1, ac)) { ok = false; break; }
+          if (!mbar_wait_w(&bar_qfull[st], (g / C::NST) & 1, ac)) { ok = false; break; }
           // S^T region is free once the P pass has read S^T(g-1)
-          if (g > 0 && !mbar_wait(&bar_s_free, (g - 1) & 1, ac)) { ok = false; break; }
+          if (g > 0 && !mbar_wait_w(&bar_s_free, (g - 1) & 1, ac)) { ok = false; break; }
           tc_fence_after();
           const uint64_t qd = desc_advance(dQ_k0, st * C::QT_BYTES);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk)
-            umma_ss(tmem + C::COL_S, desc_advance(dK_k, kmajor_step_bytes(BN, kk)),
+            umma_ss_w(tmem + C::COL_S, desc_advance(dK_k, kmajor_step_bytes(BN, kk)),
                     desc_advance(qd, kmajor_step_bytes(BM, kk)), idSD, kk > 0);
-          umma_commit(&bar_s);
+          umma_commit_w(&bar_s);
           // dP^T region is free once the dS pass has read dP^T(g-1)
-          if (g > 0 && !mbar_wait(&bar_dp_free, (g - 1) & 1, ac)) {
+          if (g > 0 && !mbar_wait_w(&bar_dp_free, (g - 1) & 1, ac)) {
             ok = false;
             break;
           }
@@ -402,20 +402,20 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
           const uint64_t od = desc_advance(ddO_k0, st * C::QT_BYTES);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk)
-            umma_ss(tmem + C::COL_DP, desc_advance(dV_k, kmajor_step_bytes(BN, kk)),
+            umma_ss_w(tmem + C::COL_DP, desc_advance(dV_k, kmajor_step_bytes(BN, kk)),
                     desc_advance(od, kmajor_step_bytes(BM, kk)), idSD, kk > 0);
-          umma_commit(&bar_dp);
-          umma_commit(&bar_qempty[st]);
+          umma_commit_w(&bar_dp);
+          umma_commit_w(&bar_qempty[st]);
         }
         if (!ok) break;
-        umma_commit(&bar_kv_empty[kb]);
+        umma_commit_w(&bar_kv_empty[kb]);
         gs += w.n_it;
         ++ic;
       }
     }
   } else if (D != 64 && warp == 14) {
     // ---------------- issuer 2: dV += P^T dO_i, dK += dS^T Q_i (A from TMEM) ----
-    if (lane_id() == 0) {
+    {   // warp-uniform: one elected lane issues
       const uint32_t idKV = idesc_bf16(128, D, false, true);
       const uint64_t dQ_mn0 = desc_mnmajor_base(smem_u32(sQ), BM);
       const uint64_t ddO_mn0 = desc_mnmajor_base(smem_u32(sdO), BM);
@@ -427,10 +427,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         for (int it = 0; it < w.n_it; ++it) {
           const int g = gs + it;
           const int st = g % C::NST;
-          if (!mbar_wait(&bar_qfull[st], (g / C::NST) & 1, ac)) { ok = false; break; }
-          if (!mbar_wait(&bar_p, g & 1, ac)) { ok = false; break; }
+          if (!mbar_wait_w(&bar_qfull[st], (g / C::NST) & 1, ac)) { ok = false; break; }
+          if (!mbar_wait_w(&bar_p, g & 1, ac)) { ok = false; break; }
           // the epilogue of the previous item must have read dV out of TMEM
-          if (it == 0 && ic > 0 && !mbar_wait(&bar_dv_empty, (ic - 1) & 1, ac)) {
+          if (it == 0 && ic > 0 && !mbar_wait_w(&bar_dv_empty, (ic - 1) & 1, ac)) {
             ok = false;
             break;
           }
@@ -438,11 +438,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
           const uint64_t omn = desc_advance(ddO_mn0, st * C::QT_BYTES);
 #pragma unroll
           for (int kk = 0; kk < BM / 16; ++kk)
-            umma_ts(tmem + C::COL_DV, tmem + C::COL_PT + 8 * kk,
+            umma_ts_w(tmem + C::COL_DV, tmem + C::COL_PT + 8 * kk,
                     desc_advance(omn, mnmajor_step_bytes(kk)), idKV, (it > 0 || kk > 0) ? 1u : 0u);
-          umma_commit(&bar_pt_done);
-          if (!mbar_wait(&bar_ds, g & 1, ac)) { ok = false; break; }
-          if (it == 0 && ic > 0 && !mbar_wait(&bar_dk_empty, (ic - 1) & 1, ac)) {
+          umma_commit_w(&bar_pt_done);
+          if (!mbar_wait_w(&bar_ds, g & 1, ac)) { ok = false; break; }
+          if (it == 0 && ic > 0 && !mbar_wait_w(&bar_dk_empty, (ic - 1) & 1, ac)) {
             ok = false;
             break;
           }
@@ -452,24 +452,24 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
           for (int kk = 0; kk < BM / 16; ++kk) {
             const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
             if constexpr (C::DK_SS)   // A = dS^T [kv][query] from the dS tile (K-major)
-              umma_ss(tmem + C::COL_DK, desc_advance(ddS_k, kmajor_step_bytes(BN, kk)),
+              umma_ss_w(tmem + C::COL_DK, desc_advance(ddS_k, kmajor_step_bytes(BN, kk)),
                       desc_advance(qmn, mnmajor_step_bytes(kk)), idKV, acc);
             else
-              umma_ts(tmem + C::COL_DK, tmem + C::COL_DST + 8 * kk,
+              umma_ts_w(tmem + C::COL_DK, tmem + C::COL_DST + 8 * kk,
                       desc_advance(qmn, mnmajor_step_bytes(kk)), idKV, acc);
           }
-          umma_commit(&bar_dst_done);
-          umma_commit(&bar_qempty[st]);
+          umma_commit_w(&bar_dst_done);
+          umma_commit_w(&bar_qempty[st]);
         }
         if (!ok) break;
-        umma_commit(&bar_done);   // dV and dK of this item are final
+        umma_commit_w(&bar_done);   // dV and dK of this item are final
         gs += w.n_it;
         ++ic;
       }
     }
   } else if (D != 64 && warp == 15) {
     // ---------------- issuer 3: dQ (both operands in shared memory) ----------
-    if (lane_id() == 0) {
+    {   // warp-uniform: one elected lane issues
       const uint32_t idQ = idesc_bf16(128, 64, true, true);
       const uint64_t ddS_mn = desc_mnmajor_base(smem_u32(sdS), BN);
       BwdItem w;
@@ -477,28 +477,28 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       bool ok = true;
       while (ok && next_bwd_item<BN, BM>(p, total, a.n_x, a.x_major, k, w)) {
         const int kb = ic % C::KV_BUFS, ku = ic / C::KV_BUFS;
-        if (!mbar_wait(&bar_kv_full[kb], ku & 1, ac)) break;
+        if (!mbar_wait_w(&bar_kv_full[kb], ku & 1, ac)) break;
         const uint64_t dK_mn = desc_mnmajor_base(smem_u32(sK(kb)), BN);
         for (int it = 0; it < w.n_it; ++it) {
           const int g = gs + it;
-          if (!mbar_wait(&bar_ds, g & 1, ac)) { ok = false; break; }
-          if (!mbar_wait(&bar_dq_empty, (g & 1) ^ 1, ac)) { ok = false; break; }
+          if (!mbar_wait_w(&bar_ds, g & 1, ac)) { ok = false; break; }
+          if (!mbar_wait_w(&bar_dq_empty, (g & 1) ^ 1, ac)) { ok = false; break; }
           tc_fence_after();
           const uint32_t tDQ = tmem + C::COL_DQ;
 #pragma unroll
           for (int kk = 0; kk < BN / 16; ++kk) {
             if (D == 64)   // dQ[q, d] = dS[q, kv] K[kv, d]
-              umma_ss(tDQ, desc_advance(ddS_mn, mnmajor_step_bytes(kk)),
+              umma_ss_w(tDQ, desc_advance(ddS_mn, mnmajor_step_bytes(kk)),
                       desc_advance(dK_mn, mnmajor_step_bytes(kk)), idQ, kk > 0);
             else           // dQ^T[d, q] = K^T[d, kv] dS^T[kv, q]
-              umma_ss(tDQ, desc_advance(dK_mn, mnmajor_step_bytes(kk)),
+              umma_ss_w(tDQ, desc_advance(dK_mn, mnmajor_step_bytes(kk)),
                       desc_advance(ddS_mn, mnmajor_step_bytes(kk)), idQ, kk > 0);
           }
-          umma_commit(&bar_dq_full);
-          umma_commit(&bar_dss_free);
+          umma_commit_w(&bar_dq_full);
+          umma_commit_w(&bar_dss_free);
         }
         if (!ok) break;
-        umma_commit(&bar_kv_empty[kb]);
+        umma_commit_w(&bar_kv_empty[kb]);
         gs += w.n_it;
         ++ic;
       }

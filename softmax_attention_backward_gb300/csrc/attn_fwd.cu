@@ -229,7 +229,7 @@ __global__ void __launch_bounds__(352, 1)
   } else if (warp == 9 || warp == 10) {
     // ---------------- MMA issuer of query tile t ----------------
     const int t = warp - 9;
-    if (lane_id() == 0) {
+    {   // warp-uniform: one elected lane issues
       const uint32_t idS = idesc_bf16(C::BM, C::BN, false, false);
       const uint32_t idO = idesc_bf16(C::BM, D, false, true);
       const uint64_t dR_k0 = desc_kmajor_base(smem_u32(sRing));
@@ -243,39 +243,39 @@ __global__ void __launch_bounds__(352, 1)
       while (ok && next_fwd_item<C::BM, C::BN>(p, total, a.n_x, a.x_major, k, w)) {
         const int qb = ic % C::QBUFS, qu = ic / C::QBUFS;
         const int nt = w.n_w[t];
-        if (!mbar_wait(&bar_q[qb], qu & 1, ac)) break;
+        if (!mbar_wait_w(&bar_q[qb], qu & 1, ac)) break;
         // Tile 1 starts one softmax phase after tile 0 (when P_0(0) of the
         // first item is ready), so that one tile's softmax overlaps the other
         // tile's MMAs instead of both running in lockstep.  bar_stagger
         // completes exactly once.
-        if (t == 1 && ic == 0 && !mbar_wait(&bar_stagger, 0, ac)) break;
+        if (t == 1 && ic == 0 && !mbar_wait_w(&bar_stagger, 0, ac)) break;
         const uint64_t dQt = desc_kmajor_base(smem_u32(sQ + (qb * 2 + t) * C::Q_BYTES));
         auto issue_s = [&](int j) -> bool {
           const int gi = gring + 2 * j, sk = gi % C::NSLOT;
-          if (!mbar_wait(&bar_full[sk], (gi / C::NSLOT) & 1, ac)) return false;
+          if (!mbar_wait_w(&bar_full[sk], (gi / C::NSLOT) & 1, ac)) return false;
           tc_fence_after();
           const uint64_t kd = desc_advance(dR_k0, sk * C::KV_BYTES);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk)
-            umma_ss(tS, desc_advance(dQt, kmajor_step_bytes(C::BM, kk)),
+            umma_ss_w(tS, desc_advance(dQt, kmajor_step_bytes(C::BM, kk)),
                     desc_advance(kd, kmajor_step_bytes(C::BN, kk)), idS, kk > 0);
-          umma_commit(&bar_s[t]);
-          umma_commit(&bar_empty[sk]);
+          umma_commit_w(&bar_s[t]);
+          umma_commit_w(&bar_empty[sk]);
           return true;
         };
         auto issue_pv = [&](int j) -> bool {
           const int gi = gring + 2 * j + 1, sv = gi % C::NSLOT;
-          if (!mbar_wait(&bar_full[sv], (gi / C::NSLOT) & 1, ac)) return false;
-          if (!mbar_wait(&bar_p[t], (cs + j) & 1, ac)) return false;
-          if (t == 0 && ic == 0 && j == 0) mbar_arrive(&bar_stagger);
+          if (!mbar_wait_w(&bar_full[sv], (gi / C::NSLOT) & 1, ac)) return false;
+          if (!mbar_wait_w(&bar_p[t], (cs + j) & 1, ac)) return false;
+          if (t == 0 && ic == 0 && j == 0 && lane_id() == 0) mbar_arrive(&bar_stagger);
           tc_fence_after();
           const uint64_t vd = desc_advance(dR_mn0, sv * C::KV_BYTES);
 #pragma unroll
           for (int kk = 0; kk < C::BN / 16; ++kk)   // P: 8 packed columns per 16 keys
-            umma_ts(tO, tP + 8 * kk, desc_advance(vd, mnmajor_step_bytes(kk)), idO,
+            umma_ts_w(tO, tP + 8 * kk, desc_advance(vd, mnmajor_step_bytes(kk)), idO,
                     (j > 0 || kk > 0) ? 1u : 0u);
-          umma_commit(&bar_o[t]);
-          umma_commit(&bar_empty[sv]);
+          umma_commit_w(&bar_o[t]);
+          umma_commit_w(&bar_empty[sv]);
           return true;
         };
         if (C::SEP_P) {
@@ -283,11 +283,11 @@ __global__ void __launch_bounds__(352, 1)
           // ready.  S(0) of an item waits for the read of the previous S.
           for (int j = 0; ok && j < nt; ++j) {
             if (j == 0) {
-              if (cs > 0 && !mbar_wait(&bar_sfree[t], (cs - 1) & 1, ac)) { ok = false; break; }
+              if (cs > 0 && !mbar_wait_w(&bar_sfree[t], (cs - 1) & 1, ac)) { ok = false; break; }
               if (!issue_s(0)) { ok = false; break; }
             }
             if (j + 1 < nt) {
-              if (!mbar_wait(&bar_sfree[t], (cs + j) & 1, ac) || !issue_s(j + 1)) {
+              if (!mbar_wait_w(&bar_sfree[t], (cs + j) & 1, ac) || !issue_s(j + 1)) {
                 ok = false;
                 break;
               }
@@ -302,8 +302,8 @@ __global__ void __launch_bounds__(352, 1)
         }
         // the query tile is free once this tile's S MMAs have completed
         if (ok) {
-          if (nt > 0) umma_commit(&bar_qempty[qb]);
-          else mbar_arrive(&bar_qempty[qb]);
+          if (nt > 0) umma_commit_w(&bar_qempty[qb]);
+          else if (lane_id() == 0) mbar_arrive(&bar_qempty[qb]);
         }
         gring += 2 * w.n_kv;
         cs += nt;

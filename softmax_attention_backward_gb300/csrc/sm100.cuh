@@ -479,3 +479,46 @@ __device__ __forceinline__ void cp_async_wait() {
 }
 
 }  // namespace attn
+
+namespace attn {
+
+// The same tcgen05 issue operations for warp-uniform code: every lane of the
+// warp makes the call with the same operands and one lane, chosen by
+// elect.sync, issues the instruction.  Issuing from warp-uniform code instead
+// of a one-lane branch measured about three times the MMA rate (the issue
+// cost per instruction, not the tensor pipe, limited the one-lane form).
+__device__ __forceinline__ void umma_ss_w(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p, e;\n setp.ne.b32 p, %4, 0;\n elect.sync _|e, 0xffffffff;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void umma_ts_w(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p, e;\n setp.ne.b32 p, %4, 0;\n elect.sync _|e, 0xffffffff;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void umma_commit_w(uint64_t* bar) {
+  asm volatile(
+      "{\n .reg .pred e;\n elect.sync _|e, 0xffffffff;\n"
+      " @e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}\n" ::"r"(
+          smem_u32(bar))
+      : "memory");
+}
+// Bounded wait with a warp-uniform result (every lane returns the same value,
+// so the warp stays converged for elect.sync).
+__device__ __forceinline__ bool mbar_wait_w(uint64_t* bar, uint32_t parity, const AbortCtx& c) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, c));
+}
+// Non-blocking phase test with lane 0's answer broadcast (a completed phase
+// stays completed, so any lane's answer is a valid one).
+__device__ __forceinline__ bool mbar_test_wait_w(uint32_t addr, uint32_t parity) {
+  return __shfl_sync(0xffffffffu, mbar_test_wait(addr, parity) ? 1 : 0, 0) != 0;
+}
+
+}  // namespace attn

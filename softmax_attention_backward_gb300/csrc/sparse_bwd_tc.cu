@@ -184,7 +184,7 @@ __global__ void __launch_bounds__(SB_THREADS, 1) sparse_bwd_tc_kernel(const Spar
     cp_async_wait<0>();
   } else if (warp == 10) {
     // ---------------- MMA issuer ----------------
-    if (lane == 0 && nchunks > 0) {
+    if (nchunks > 0) {   // warp-uniform: one elected lane issues
       const uint32_t idS = idesc_bf16(64, SB_NK, false, false);        // S, dP
       const uint32_t idQ128 = idesc_bf16(128, SB_HB, true, false);     // dQ^T tiles
       const uint32_t idQ64 = idesc_bf16(64, SB_HB, true, false);       // dQ^T dims 512..575
@@ -195,26 +195,26 @@ __global__ void __launch_bounds__(SB_THREADS, 1) sparse_bwd_tc_kernel(const Spar
       const uint64_t ddSk = desc_kmajor_base(smem_u32(sdS));
       const uint64_t dPmn = desc_mnmajor_base(smem_u32(sP), SB_HB);
       const uint64_t ddSmn = desc_mnmajor_base(smem_u32(sdS), SB_HB);
-      bool ok = mbar_wait(&bar_in, 0, ac);
+      bool ok = mbar_wait_w(&bar_in, 0, ac);
       int gp = 0;                                  // dKV pieces issued so far
       int n1 = 0;                                  // pieces issued into buffer 1 (the dP columns)
       for (int c = 0; ok && c < nchunks; ++c) {
-        if (!mbar_wait(&bar_kv_full, c & 1, ac)) { ok = false; break; }
+        if (!mbar_wait_w(&bar_kv_full, c & 1, ac)) { ok = false; break; }
         // S and dP columns: read by the softmax of chunk c - 1, and the last
         // dKV piece that used the dP columns drained
-        if (c > 0 && !mbar_wait(&bar_s_free, (c - 1) & 1, ac)) { ok = false; break; }
-        if (n1 > 0 && !mbar_wait(&bar_pc_free[1], (n1 - 1) & 1, ac)) { ok = false; break; }
+        if (c > 0 && !mbar_wait_w(&bar_s_free, (c - 1) & 1, ac)) { ok = false; break; }
+        if (n1 > 0 && !mbar_wait_w(&bar_pc_free[1], (n1 - 1) & 1, ac)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll 4
         for (int kk = 0; kk < SB_DQK / 16; ++kk)
-          umma_ss(tmem + SB_COL_S, desc_advance(dQk, kmajor_step_bytes(SB_HB, kk)),
+          umma_ss_w(tmem + SB_COL_S, desc_advance(dQk, kmajor_step_bytes(SB_HB, kk)),
                   desc_advance(dKk, kmajor_step_bytes(SB_NK, kk)), idS, kk > 0);
 #pragma unroll 4
         for (int kk = 0; kk < SB_DV / 16; ++kk)
-          umma_ss(tmem + SB_COL_DP, desc_advance(ddOk, kmajor_step_bytes(SB_HB, kk)),
+          umma_ss_w(tmem + SB_COL_DP, desc_advance(ddOk, kmajor_step_bytes(SB_HB, kk)),
                   desc_advance(dKk, kmajor_step_bytes(SB_NK, kk)), idS, kk > 0);
-        umma_commit(&bar_s_full);
-        if (!mbar_wait(&bar_ds_full, c & 1, ac)) { ok = false; break; }
+        umma_commit_w(&bar_s_full);
+        if (!mbar_wait_w(&bar_ds_full, c & 1, ac)) { ok = false; break; }
         tc_fence_after();
         // dQ^T(dims, heads) += K^T(dims, slots) dS^T(slots, heads)
 #pragma unroll
@@ -222,36 +222,36 @@ __global__ void __launch_bounds__(SB_THREADS, 1) sparse_bwd_tc_kernel(const Spar
           const uint64_t dKmn = desc_mnmajor_base(smem_u32(sKV + 2 * m * SB_NK * 128), SB_NK);
 #pragma unroll
           for (int kk = 0; kk < SB_NK / 16; ++kk)
-            umma_ss(tmem + SB_COL_DQ + 64 * m, desc_advance(dKmn, mnmajor_step_bytes(kk)),
+            umma_ss_w(tmem + SB_COL_DQ + 64 * m, desc_advance(dKmn, mnmajor_step_bytes(kk)),
                     desc_advance(ddSk, kmajor_step_bytes(SB_HB, kk)), m < 4 ? idQ128 : idQ64,
                     (c > 0 || kk > 0) ? 1u : 0u);
         }
-        umma_commit(&bar_kv_empty);                // K and V of this chunk are no longer read
+        umma_commit_w(&bar_kv_empty);                // K and V of this chunk are no longer read
         // dKV pieces: D(slots, dims 64p..) = dS^T Q_p + P^T dO_p
         for (int p = 0; p < SB_PIECES; ++p, ++gp) {
           const int b = gp & 1, use = gp >> 1;
-          if (!mbar_wait(&bar_pc_free[b], (use & 1) ^ 1, ac)) { ok = false; break; }
+          if (!mbar_wait_w(&bar_pc_free[b], (use & 1) ^ 1, ac)) { ok = false; break; }
           tc_fence_after();
           const uint32_t dst = tmem + (b ? SB_COL_DP : SB_COL_PC);
           const uint64_t dQmn = desc_mnmajor_base(smem_u32(sQ + p * SB_HB * 128), SB_HB);
 #pragma unroll
           for (int kk = 0; kk < SB_HB / 16; ++kk)
-            umma_ss(dst, desc_advance(ddSmn, mnmajor_step_bytes(kk)),
+            umma_ss_w(dst, desc_advance(ddSmn, mnmajor_step_bytes(kk)),
                     desc_advance(dQmn, mnmajor_step_bytes(kk)), idKV, kk > 0);
           if (p < SB_DV / 64) {
             const uint64_t ddOmn = desc_mnmajor_base(smem_u32(sdO + p * SB_HB * 128), SB_HB);
 #pragma unroll
             for (int kk = 0; kk < SB_HB / 16; ++kk)
-              umma_ss(dst, desc_advance(dPmn, mnmajor_step_bytes(kk)),
+              umma_ss_w(dst, desc_advance(dPmn, mnmajor_step_bytes(kk)),
                       desc_advance(ddOmn, mnmajor_step_bytes(kk)), idKV, 1u);
           }
-          umma_commit(&bar_pc_full[b]);
+          umma_commit_w(&bar_pc_full[b]);
           if (b == 1) ++n1;
         }
         if (!ok) break;
-        umma_commit(&bar_pds_free);                // P and dS tiles of this chunk are read
+        umma_commit_w(&bar_pds_free);                // P and dS tiles of this chunk are read
       }
-      if (ok) umma_commit(&bar_dq_done);
+      if (ok) umma_commit_w(&bar_dq_done);
     }
   } else if (warp >= 4) {
     // ---------------- dKV drain (warps 4..7) ----------------

@@ -172,7 +172,7 @@ __global__ void __launch_bounds__(SF_THREADS, 1) sparse_fwd_tc_kernel(const Spar
     cp_async_wait<0>();
   } else if (warp == 6) {
     // ---------------- MMA issuer ----------------
-    if (lane == 0 && nchunks > 0) {
+    if (nchunks > 0) {   // warp-uniform: one elected lane issues
       const uint32_t idS = idesc_bf16(64, SF_NK, false, false);
       const uint32_t idO = idesc_bf16(128, SF_HB, true, false);
       const uint64_t dQ = desc_kmajor_base(smem_u32(sQ));
@@ -186,11 +186,11 @@ __global__ void __launch_bounds__(SF_THREADS, 1) sparse_fwd_tc_kernel(const Spar
           const uint64_t dV = desc_mnmajor_base(smem_u32(sKV + b * SF_KV_BYTES + 2 * m * SF_NK * 128), SF_NK);
 #pragma unroll
           for (int kk = 0; kk < SF_NK / 16; ++kk)
-            umma_ss(tmem + SF_COL_O + 64 * m, desc_advance(dV, mnmajor_step_bytes(kk)),
+            umma_ss_w(tmem + SF_COL_O + 64 * m, desc_advance(dV, mnmajor_step_bytes(kk)),
                     desc_advance(dP, kmajor_step_bytes(SF_HB, kk)), idO, (c > 0 || kk > 0) ? 1u : 0u);
         }
-        umma_commit(&bar_o_done);
-        umma_commit(&bar_kv_empty[b]);
+        umma_commit_w(&bar_o_done);
+        umma_commit_w(&bar_kv_empty[b]);
       };
       auto issue_s = [&](int c) {
         tc_fence_after();
@@ -198,34 +198,38 @@ __global__ void __launch_bounds__(SF_THREADS, 1) sparse_fwd_tc_kernel(const Spar
         const uint64_t dK = desc_kmajor_base(smem_u32(sKV + b * SF_KV_BYTES));
 #pragma unroll 4
         for (int kk = 0; kk < SF_DQK / 16; ++kk)
-          umma_ss(tmem + SF_COL_S + 64 * b, desc_advance(dQ, kmajor_step_bytes(SF_HB, kk)),
+          umma_ss_w(tmem + SF_COL_S + 64 * b, desc_advance(dQ, kmajor_step_bytes(SF_HB, kk)),
                   desc_advance(dK, kmajor_step_bytes(SF_NK, kk)), idS, kk > 0);
-        umma_commit(&bar_s_full[b]);
+        umma_commit_w(&bar_s_full[b]);
       };
       // Issue in readiness order: O^T of chunk `no` as soon as its P is
       // written (that frees its buffer for the gather two chunks ahead), S of
       // chunk `ns` as soon as the chunk landed and its TMEM buffer was read,
       // so S of the next chunk overlaps the softmax of the current one.
-      bool ok = mbar_wait(&bar_q, 0, ac);
+      bool ok = mbar_wait_w(&bar_q, 0, ac);
       int ns = 0, no = 0;
       uint64_t t0 = 0;
       while (ok && no < nchunks) {
         bool did = false;
-        if (no < ns && mbar_test_wait(smem_u32(&bar_p_full), no & 1)) {
+        if (no < ns && mbar_test_wait_w(smem_u32(&bar_p_full), no & 1)) {
           issue_o(no++);
           did = true;
         } else if (ns < nchunks &&
-                   mbar_test_wait(smem_u32(&bar_kv_full[ns & 1]), (ns >> 1) & 1) &&
-                   mbar_test_wait(smem_u32(&bar_s_free[ns & 1]), ((ns >> 1) & 1) ^ 1)) {
+                   mbar_test_wait_w(smem_u32(&bar_kv_full[ns & 1]), (ns >> 1) & 1) &&
+                   mbar_test_wait_w(smem_u32(&bar_s_free[ns & 1]), ((ns >> 1) & 1) ^ 1)) {
           issue_s(ns++);
           did = true;
         }
         if (did) {
           t0 = 0;
         } else {
+          // lane 0 decides for the warp, which stays converged
           if (t0 == 0) t0 = globaltimer();
-          if (*reinterpret_cast<volatile int*>(&abort_flag)) { ok = false; break; }
-          if (globaltimer() - t0 > kWaitLimitNs) {
+          if (__shfl_sync(0xffffffffu, *reinterpret_cast<volatile int*>(&abort_flag), 0)) {
+            ok = false;
+            break;
+          }
+          if (__shfl_sync(0xffffffffu, (globaltimer() - t0 > kWaitLimitNs) ? 1 : 0, 0)) {
             raise_error(ac, ATTN_DEVERR_TIMEOUT);
             ok = false;
             break;

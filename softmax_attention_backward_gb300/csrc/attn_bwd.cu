@@ -55,11 +55,12 @@ struct BwdCfg {
   // TMEM columns.  S^T and dP^T are BM fp32 columns each; P^T and dS^T are
   // packed bf16 pairs (BM / 2 columns each), P^T in columns of its own so that
   // S^T of the next step can be issued as soon as S^T of this one has been read.
-  // D = 64 (BM = 128) has no room left for dS^T: dK reads dS^T from the bf16
-  // dS tile in shared memory (the tile the dQ GEMM reads), as a K-major A.
-  //   D = 64:  S^T 0..127, dP^T 128..255, dV 256, dK 320, dQ 384, P^T 448
+  // D = 64 (BM = 128) has no room left for dS^T: each thread writes its packed
+  // dS^T over the dP^T columns it has just read (the first half of its own
+  // HALF-column range), and the next dP^T is issued after dK has read them.
+  //   D = 64:  S^T 0..127, dP^T|dS^T 128..255, dV 256, dK 320, dQ 384, P^T 448
   //   D = 128: S^T 0..63, dP^T 64..127, dV 128, dK 256, dQ 384, P^T 448, dS^T 480
-  static constexpr bool DK_SS = (D == 64);
+  static constexpr bool DS_IN_DP = (D == 64);
   static constexpr uint32_t COL_S = 0;                // S^T (fp32)
   static constexpr uint32_t COL_DP = BM;              // dP^T (fp32)
   static constexpr uint32_t COL_DV = 2 * BM;
@@ -67,7 +68,11 @@ struct BwdCfg {
   static constexpr uint32_t COL_DQ = COL_DK + D;      // one 64-column dQ tile
   static constexpr uint32_t COL_PT = COL_DQ + 64;
   static constexpr uint32_t COL_DST = COL_PT + BM / 2;
-  static_assert(COL_DST + (DK_SS ? 0 : BM / 2) <= TMEM_COLS, "TMEM budget");
+  static_assert(COL_DST + (DS_IN_DP ? 0 : BM / 2) <= TMEM_COLS, "TMEM budget");
+  // TMEM column of the packed dS^T columns of K-step kk (16 queries)
+  __host__ __device__ static constexpr uint32_t ds_col(int kk) {
+    return DS_IN_DP ? COL_DP + (16 * kk / HALF) * HALF + (16 * kk % HALF) / 2 : COL_DST + 8 * kk;
+  }
   // dK and dV leave one after the other through the staging tile
   static_assert(BN * D * 2 <= STG_BYTES, "dK/dV staging");
   static_assert(SMEM <= 227 * 1024 - 4096, "shared memory budget");
@@ -261,7 +266,6 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       const uint64_t dQ_mn0 = desc_mnmajor_base(smem_u32(sQ), BM);
       const uint64_t ddO_mn0 = desc_mnmajor_base(smem_u32(sdO), BM);
       const uint64_t ddS_mn = desc_mnmajor_base(smem_u32(sdS), BN);
-      const uint64_t ddS_k = desc_kmajor_base(smem_u32(sdS));
       auto issue_s = [&](int kb, int st, int kk) {
         umma_ss_w(tmem + C::COL_S, desc_advance(desc_kmajor_base(smem_u32(sK(kb))), kmajor_step_bytes(BN, kk)),
                 desc_advance(dQ_k0, st * C::QT_BYTES + kmajor_step_bytes(BM, kk)), idSD, kk > 0);
@@ -328,29 +332,25 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
           if (it == 0 && ic > 0 && !mbar_wait_w(&bar_dk_empty, (ic - 1) & 1, ac)) { ok = false; break; }
           tc_fence_after();
           const uint64_t qmn = desc_advance(dQ_mn0, st * C::QT_BYTES);
+          // dK reads dS^T from the dP^T columns, so the next dP^T goes out
+          // after it (MMAs of one thread execute in order)
 #pragma unroll
-          for (int kk = 0; kk < (KQ > KV ? KQ : KV); ++kk) {
-            if (kk < KV) {
-              const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
-              if constexpr (C::DK_SS)   // A = dS^T [kv][query] from the dS tile (K-major)
-                umma_ss_w(tmem + C::COL_DK, desc_advance(ddS_k, kmajor_step_bytes(BN, kk)),
-                        desc_advance(qmn, mnmajor_step_bytes(kk)), idKV, acc);
-              else
-                umma_ts_w(tmem + C::COL_DK, tmem + C::COL_DST + 8 * kk,
-                        desc_advance(qmn, mnmajor_step_bytes(kk)), idKV, acc);
-            }
-            if (kk < KQ) {
-              if (D == 64)   // dQ[q, d] = dS[q, kv] K[kv, d]
-                umma_ss_w(tmem + C::COL_DQ, desc_advance(ddS_mn, mnmajor_step_bytes(kk)),
+          for (int kk = 0; kk < KV; ++kk)
+            umma_ts_w(tmem + C::COL_DK, tmem + C::ds_col(kk), desc_advance(qmn, mnmajor_step_bytes(kk)),
+                      idKV, (it > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+          for (int kk = 0; kk < KQ; ++kk) {
+            if (D == 64)   // dQ[q, d] = dS[q, kv] K[kv, d]
+              umma_ss_w(tmem + C::COL_DQ, desc_advance(ddS_mn, mnmajor_step_bytes(kk)),
                         desc_advance(dK_mn, mnmajor_step_bytes(kk)), idQ, kk > 0);
-              else           // dQ^T[d, q] = K^T[d, kv] dS^T[kv, q]
-                umma_ss_w(tmem + C::COL_DQ, desc_advance(dK_mn, mnmajor_step_bytes(kk)),
+            else           // dQ^T[d, q] = K^T[d, kv] dS^T[kv, q]
+              umma_ss_w(tmem + C::COL_DQ, desc_advance(dK_mn, mnmajor_step_bytes(kk)),
                         desc_advance(ddS_mn, mnmajor_step_bytes(kk)), idQ, kk > 0);
-            }
-            if (nx && kk < KS) {
-              issue_dp(kb1, st1, kk);
-              if (kk == KS - 1) umma_commit_w(&bar_dp);
-            }
+          }
+          if (nx) {
+#pragma unroll
+            for (int kk = 0; kk < KS; ++kk) issue_dp(kb1, st1, kk);
+            umma_commit_w(&bar_dp);
           }
           umma_commit_w(&bar_dq_full);
           umma_commit_w(&bar_ds_free);
@@ -419,7 +419,6 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       const uint32_t idKV = idesc_bf16(128, D, false, true);
       const uint64_t dQ_mn0 = desc_mnmajor_base(smem_u32(sQ), BM);
       const uint64_t ddO_mn0 = desc_mnmajor_base(smem_u32(sdO), BM);
-      const uint64_t ddS_k = desc_kmajor_base(smem_u32(sdS));
       BwdItem w;
       int k = 0, ic = 0, gs = 0;
       bool ok = true;
@@ -451,12 +450,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
 #pragma unroll
           for (int kk = 0; kk < BM / 16; ++kk) {
             const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
-            if constexpr (C::DK_SS)   // A = dS^T [kv][query] from the dS tile (K-major)
-              umma_ss_w(tmem + C::COL_DK, desc_advance(ddS_k, kmajor_step_bytes(BN, kk)),
-                      desc_advance(qmn, mnmajor_step_bytes(kk)), idKV, acc);
-            else
-              umma_ts_w(tmem + C::COL_DK, tmem + C::COL_DST + 8 * kk,
-                      desc_advance(qmn, mnmajor_step_bytes(kk)), idKV, acc);
+            umma_ts_w(tmem + C::COL_DK, tmem + C::ds_col(kk), desc_advance(qmn, mnmajor_step_bytes(kk)),
+                      idKV, acc);
           }
           umma_commit_w(&bar_dst_done);
           umma_commit_w(&bar_qempty[st]);
@@ -531,6 +526,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     const uint32_t tDPme = tmem + lane_base + C::COL_DP + c0;    // this thread's dP columns
     const uint32_t tPTme = tmem + lane_base + C::COL_PT + c0 / 2;
     const uint32_t tDSTme = tmem + lane_base + C::COL_DST + c0 / 2;
+    const uint32_t tDSme = tmem + lane_base + C::COL_DP + c0;    // D = 64: dS^T over dP^T
     BwdItem w;
     int k = 0, gs = 0;
     bool have = next_bwd_item<BN, BM>(p, total, a.n_x, a.x_major, k, w);
@@ -622,6 +618,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
                                                                  __uint_as_float(u[c + 3])),
                                                          f2_pack(d4.z, d4.w)), pb));
             }
+            tmem_st16p(tDSme + c1 / 2, pk);   // dS^T over the dP^T columns just read
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
               const int ch = (c0 + c1) / 8 + i;

@@ -109,23 +109,26 @@ __global__ void __launch_bounds__(256) attn_dq_finalize_kernel(Problem p,
   const uint32_t nchunks = static_cast<uint32_t>(p.batch) * rt * hq * CPR;
   const uint32_t nthreads = gridDim.x * blockDim.x;
   const float sc = p.scale;
-  // accumulator / slabs are head-major: [batch, head, row, dim]
-  auto acc_index = [&](uint32_t c, int& srow) -> size_t {
-    const uint32_t rh = c / CPR;
+  // Chunk c (8 dims) walks the head-major accumulator / slabs [batch, head,
+  // row, dim] in memory order, so a warp reads one contiguous kilobyte; its dQ
+  // destination [batch, row, head, dim] is a whole 128-byte line per (row,
+  // head) for D = 64.  Returns the dQ element offset and the row.
+  auto dq_index = [&](uint32_t c, int& srow) -> size_t {
     const uint32_t sub = c % CPR;
-    const uint32_t bs = rh / hq;
-    const uint32_t hh = rh % hq;
-    srow = static_cast<int>(bs % rt);
-    const uint32_t bb = bs / rt;
-    return ((static_cast<size_t>(bb) * hq + hh) * rt + srow) * D + sub * 8;
+    const uint32_t rh = c / CPR;             // (batch, head, row)
+    srow = static_cast<int>(rh % rt);
+    const uint32_t bh = rh / rt;
+    const uint32_t hh = bh % hq;
+    const uint32_t bb = bh / hq;
+    return ((static_cast<size_t>(bb) * rt + srow) * hq + hh) * D + sub * 8;
   };
-  auto store = [&](uint32_t c, const float (&v)[8]) {
+  auto store = [&](size_t di, const float (&v)[8]) {
     uint4 out;
     out.x = pack_bf16(v[0] * sc, v[1] * sc);
     out.y = pack_bf16(v[2] * sc, v[3] * sc);
     out.z = pack_bf16(v[4] * sc, v[5] * sc);
     out.w = pack_bf16(v[6] * sc, v[7] * sc);
-    *reinterpret_cast<uint4*>(dq + static_cast<size_t>(c) * 8) = out;
+    *reinterpret_cast<uint4*>(dq + di) = out;
   };
   const uint32_t c_first = blockIdx.x * blockDim.x + threadIdx.x;
   if (!split) {
@@ -133,15 +136,18 @@ __global__ void __launch_bounds__(256) attn_dq_finalize_kernel(Problem p,
       const uint32_t cc[2] = {c0, c0 + nthreads};
       float4 a[2][2];
       bool live[2];
+      size_t di[2];
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
         int srow = 0;
         live[u] = false;
+        di[u] = 0;
         a[u][0] = a[u][1] = make_float4(0.f, 0.f, 0.f, 0.f);
         if (cc[u] < nchunks) {
-          const size_t e0 = acc_index(cc[u], srow);
+          di[u] = dq_index(cc[u], srow);
           live[u] = true;
           if (srow < end) {
+            const size_t e0 = static_cast<size_t>(cc[u]) * 8;
             a[u][0] = *reinterpret_cast<const float4*>(acc + e0);
             a[u][1] = *reinterpret_cast<const float4*>(acc + e0 + 4);
           }
@@ -152,13 +158,14 @@ __global__ void __launch_bounds__(256) attn_dq_finalize_kernel(Problem p,
         if (!live[u]) continue;
         const float v[8] = {a[u][0].x, a[u][0].y, a[u][0].z, a[u][0].w,
                             a[u][1].x, a[u][1].y, a[u][1].z, a[u][1].w};
-        store(cc[u], v);
+        store(di[u], v);
       }
     }
   } else {
     for (uint32_t c = c_first; c < nchunks; c += nthreads) {
       int srow = 0;
-      const size_t e0 = acc_index(c, srow);
+      const size_t di = dq_index(c, srow);
+      const size_t e0 = static_cast<size_t>(c) * 8;
       float v[8] = {0, 0, 0, 0, 0, 0, 0, 0};
       if (srow < end) {
         // sequence-local row index and length
@@ -184,7 +191,7 @@ __global__ void __launch_bounds__(256) attn_dq_finalize_kernel(Problem p,
           v[4] += a1.x; v[5] += a1.y; v[6] += a1.z; v[7] += a1.w;
         }
       }
-      store(c, v);
+      store(di, v);
     }
   }
   // THD: zero dK / dV rows past the last sequence

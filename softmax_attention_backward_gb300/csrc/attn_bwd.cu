@@ -246,12 +246,12 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     }
   } else if (D == 64 && warp == 13) {
     // ---------------- D = 64: one MMA issuer ----------------
-    // MMAs into one accumulator run one after the other (each K-step waits
-    // for the previous one), while MMAs into different accumulators overlap
-    // in the tensor pipe.  So the GEMMs that become ready together are issued
-    // with their K-steps interleaved, in two phases per step g:
-    //   after P(g):  dV(g) with S^T(g+1)
-    //   after dS(g): dK(g) and dQ(g) with dP^T(g+1)
+    // The GEMMs go out in two phases per step g, each as soon as the P/dS
+    // warps have produced its operand:
+    //   after P(g):  S^T(g+1), then dV(g)
+    //   after dS(g): dK(g), dQ(g), then dP^T(g+1)
+    // each GEMM as one run of K-steps (measured faster than interleaving the
+    // K-steps of independent GEMMs).
     // Step g+1's S^T/dP^T are issued here when its K/V tile is resident
     // (same item, or a second K/V buffer); otherwise at the start of its item.
     {   // warp-uniform: one elected lane issues
@@ -308,25 +308,24 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
           const bool nx = !last || (have_next && C::KV_BUFS > 1);
           const int kb1 = last ? kbn : kb;
           const int st1 = (g + 1) % C::NST;
-          // ---- phase A: dV(g) [+ S^T(g+1)] ----
+          // ---- phase A: [S^T(g+1)], dV(g) ----
           if (!mbar_wait_w(&bar_p, g & 1, ac)) { ok = false; break; }
           if (it == 0 && ic > 0 && !mbar_wait_w(&bar_dv_empty, (ic - 1) & 1, ac)) { ok = false; break; }
           if (nx && last && !mbar_wait_w(&bar_kv_full[kbn], kun & 1, ac)) { ok = false; break; }
           if (nx && !mbar_wait_w(&bar_qfull[st1], ((g + 1) / C::NST) & 1, ac)) { ok = false; break; }
           tc_fence_after();
           const uint64_t omn = desc_advance(ddO_mn0, st * C::QT_BYTES);
+          if (nx) {
 #pragma unroll
-          for (int kk = 0; kk < (KV > KS ? KV : KS); ++kk) {
-            if (kk < KV)
-              umma_ts_w(tmem + C::COL_DV, tmem + C::COL_PT + 8 * kk,
-                      desc_advance(omn, mnmajor_step_bytes(kk)), idKV, (it > 0 || kk > 0) ? 1u : 0u);
-            if (nx && kk < KS) {
-              issue_s(kb1, st1, kk);
-              if (kk == KS - 1) umma_commit_w(&bar_s);
-            }
+            for (int kk = 0; kk < KS; ++kk) issue_s(kb1, st1, kk);
+            umma_commit_w(&bar_s);
           }
+#pragma unroll
+          for (int kk = 0; kk < KV; ++kk)
+            umma_ts_w(tmem + C::COL_DV, tmem + C::COL_PT + 8 * kk,
+                      desc_advance(omn, mnmajor_step_bytes(kk)), idKV, (it > 0 || kk > 0) ? 1u : 0u);
           umma_commit_w(&bar_pt_done);
-          // ---- phase B: dK(g), dQ(g) [+ dP^T(g+1)] ----
+          // ---- phase B: dK(g), dQ(g) [, dP^T(g+1)] ----
           if (!mbar_wait_w(&bar_ds, g & 1, ac)) { ok = false; break; }
           if (!mbar_wait_w(&bar_dq_empty, (g & 1) ^ 1, ac)) { ok = false; break; }
           if (it == 0 && ic > 0 && !mbar_wait_w(&bar_dk_empty, (ic - 1) & 1, ac)) { ok = false; break; }

@@ -470,8 +470,30 @@ def bench_sparse(args, dev, flush):
         torch.cuda.synchronize()
         f_ms.append(e[0].elapsed_time(e[1]))
         b_ms.append(e[1].elapsed_time(e[2]))
+    # ordered (deterministic) dKV: same inputs, its own workspace (fp32 rows per
+    # (token, slot)); bitwise repeat checked on the last two runs
+    del ws
+    wsd = torch.empty(A.sparse_attn_bwd_deterministic_workspace_size(q, idx), dtype=torch.uint8,
+                      device=dev)
+    dkv_prev = torch.empty_like(kv)
+    d_ms = []
+    for i in range(2 + steps):
+        flush.zero_()
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        e[0].record(stream)
+        A.sparse_attn_bwd_deterministic(q, kv, idx, o, do, lse, scale=w.scale, workspace=wsd,
+                                        dq=dq, dkv=dkv)
+        e[1].record(stream)
+        torch.cuda.synchronize()
+        if i >= 2:
+            d_ms.append(e[0].elapsed_time(e[1]))
+        if i == 1 + steps - 1:
+            dkv_prev.copy_(dkv)
+    repeat_equal = bool(torch.equal(dkv_prev, dkv))
+    del wsd
     fb, bb, pairs = sparse_logical_bytes(w.seqlen, w.heads_q, x["idx"])
     fm, bm = sum(f_ms) / steps, sum(b_ms) / steps
+    dm = sum(d_ms) / len(d_ms)
     hbm = peaks()[0]["hbm_gbs"]
     flops_f = pairs * w.heads_q * 2 * (576 + 512)
     flops_b = pairs * w.heads_q * 2 * (3 * 576 + 2 * 512)
@@ -479,6 +501,7 @@ def bench_sparse(args, dev, flush):
             "fwd_logical_gbs": fb / fm / 1e6, "bwd_logical_gbs": bb / bm / 1e6,
             "fwd_frac_hbm": fb / fm / 1e6 / hbm, "bwd_frac_hbm": bb / bm / 1e6 / hbm,
             "fwd_tflops": flops_f / fm / 1e9, "bwd_tflops": flops_b / bm / 1e9,
+            "bwd_deterministic_ms": dm, "bwd_deterministic_bitwise_repeat": repeat_equal,
             "valid_pairs": pairs}
 
 

@@ -209,6 +209,22 @@ attn_status_t sparse_attn_bwd(const sparse_attn_problem_t* p, const void* q, con
                               const float* lse, void* dq, void* dkv, void* workspace,
                               size_t workspace_bytes, attn_stream_t stream);
 
+/* Deterministic variant of sparse_attn_bwd: the same dq (bitwise) and dkv
+ * within rounding, with dkv bitwise reproducible.  Instead of adding into a
+ * shared accumulator, the main kernel stores each (token, slot, 64-head block)
+ * contribution to dkv once in the workspace; the index lists are inverted
+ * into a per-key-row list of (token, slot) in ascending token order, and each
+ * key row sums its contributions in that order (fp32) before the bf16 cast.
+ * Workspace: tokens * topk * ceil(heads / 64) * dim_qk fp32 contribution rows
+ * plus Delta and the inverted lists (tokens * topk int32 and small tables);
+ * at tokens 8192, topk 2048, 64 heads about 38.7 GB. */
+size_t sparse_attn_bwd_deterministic_workspace_size(const sparse_attn_problem_t* p);
+attn_status_t sparse_attn_bwd_deterministic(const sparse_attn_problem_t* p, const void* q,
+                                            const void* kv, const int32_t* idx, const void* o,
+                                            const void* dout, const float* lse, void* dq,
+                                            void* dkv, void* workspace, size_t workspace_bytes,
+                                            attn_stream_t stream);
+
 /* Static description of a status code. */
 const char* attn_status_string(attn_status_t s);
 

@@ -8,6 +8,7 @@ missing or a call fails, an exception is raised.
 Entry points (same names as the C ABI):
   attn_fwd, attn_bwd_workspace_size, attn_bwd_preprocess, attn_bwd, attn_bwd_postprocess,
   sparse_attn_fwd, sparse_attn_bwd_workspace_size, sparse_attn_bwd,
+  sparse_attn_bwd_deterministic_workspace_size, sparse_attn_bwd_deterministic,
   attn_status_string, attn_version
 """
 from __future__ import annotations
@@ -22,7 +23,8 @@ import torch
 __all__ = [
     "ATTN_DQ_ATOMIC", "ATTN_DQ_SPLIT", "AttnError", "lib", "attn_fwd", "attn_bwd_workspace_size",
     "attn_bwd_preprocess", "attn_bwd", "attn_bwd_postprocess", "sparse_attn_fwd", "sparse_attn_bwd_workspace_size",
-    "sparse_attn_bwd", "attn_status_string", "attn_version", "dense_backward",
+    "sparse_attn_bwd", "sparse_attn_bwd_deterministic_workspace_size", "sparse_attn_bwd_deterministic",
+    "attn_status_string", "attn_version", "dense_backward",
     "SPARSE_DIM_QK", "SPARSE_DIM_V", "EXPORTED_SYMBOLS", "attn_bwd_fixed_scratch",
     "FIXED_SCRATCH_BYTES",
 ]
@@ -36,6 +38,7 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libattn.so"
 EXPORTED_SYMBOLS = (
     "attn_fwd", "attn_bwd_workspace_size", "attn_bwd_preprocess", "attn_bwd", "attn_bwd_postprocess",
     "sparse_attn_fwd", "sparse_attn_bwd_workspace_size", "sparse_attn_bwd",
+    "sparse_attn_bwd_deterministic_workspace_size", "sparse_attn_bwd_deterministic",
     "attn_status_string", "attn_version", "attn_bwd_fixed_scratch",
 )
 FIXED_SCRATCH_BYTES = 16 << 20
@@ -88,6 +91,9 @@ def lib() -> ctypes.CDLL:
         L.sparse_attn_bwd_workspace_size.argtypes = [SP]
         L.sparse_attn_bwd_workspace_size.restype = sz
         L.sparse_attn_bwd.argtypes = [SP, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+        L.sparse_attn_bwd_deterministic_workspace_size.argtypes = [SP]
+        L.sparse_attn_bwd_deterministic_workspace_size.restype = sz
+        L.sparse_attn_bwd_deterministic.argtypes = [SP, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
         L.attn_bwd_fixed_scratch.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
         L.attn_status_string.argtypes = [i32]
         L.attn_status_string.restype = ctypes.c_char_p
@@ -362,4 +368,31 @@ def sparse_attn_bwd(q, kv, idx, o, dout, lse, *, scale=None, workspace=None, dq=
            lib().sparse_attn_bwd(ctypes.byref(p), _ptr(q), _ptr(kv), _ptr(idx), _ptr(o),
                                  _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dkv), _ptr(workspace),
                                  workspace.numel(), _stream(stream)))
+    return dq, dkv
+
+
+def sparse_attn_bwd_deterministic_workspace_size(q, idx, *, scale=None) -> int:
+    p = _sparse_problem(q, idx, scale, None)
+    return int(lib().sparse_attn_bwd_deterministic_workspace_size(ctypes.byref(p)))
+
+
+def sparse_attn_bwd_deterministic(q, kv, idx, o, dout, lse, *, scale=None, workspace=None, dq=None,
+                                  dkv=None, error_word=None, stream=None):
+    """Returns (dq [T,H,576], dkv [T,576]) bf16 with dkv bitwise reproducible
+    (fixed per-key-row summation order; see include/attn.h for the workspace)."""
+    dev = q.device
+    for n, t in (("q", q), ("kv", kv), ("o", o), ("dout", dout)):
+        _need(t, n, torch.bfloat16, dev)
+    _need(idx, "idx", torch.int32, dev)
+    _need(lse, "lse", torch.float32, dev)
+    if workspace is None:
+        n = sparse_attn_bwd_deterministic_workspace_size(q, idx, scale=scale)
+        workspace = torch.empty(max(n, 16), dtype=torch.uint8, device=dev)
+    dq = dq if dq is not None else torch.empty_like(q)
+    dkv = dkv if dkv is not None else torch.empty_like(kv)
+    p = _sparse_problem(q, idx, scale, error_word)
+    _check("sparse_attn_bwd_deterministic",
+           lib().sparse_attn_bwd_deterministic(ctypes.byref(p), _ptr(q), _ptr(kv), _ptr(idx),
+                                               _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dkv),
+                                               _ptr(workspace), workspace.numel(), _stream(stream)))
     return dq, dkv

@@ -67,7 +67,8 @@ struct SparseArgs {
   const float* lse_in;
   const float* delta;
   __nv_bfloat16* dq;
-  float* dkv_acc;
+  float* dkv_acc;        // atomic path: fp32 dKV accumulator [T, 576]
+  float* contrib;        // ordered path: per (token, slot, head block) dKV rows, else null
   int T, H, K;
   float scale, scale_log2;
   int32_t* err;
@@ -77,5 +78,26 @@ cudaError_t launch_sparse_fwd(const SparseArgs& a, cudaStream_t st);
 cudaError_t launch_sparse_bwd(const SparseArgs& a, float* delta, __nv_bfloat16* dkv,
                               cudaStream_t st);
 cudaError_t launch_sparse_bwd_main(const SparseArgs& a, cudaStream_t st);
+
+// Deterministic dKV (sparse_dkv_ordered.cu): CSR of the index lists by key
+// row, entries in ascending token order, and the ordered row reduction.
+struct SparseCsrLayout {
+  int nblk, tb;                // token blocks of tb tokens
+  size_t table_elems;          // int32 [nblk, T]
+  size_t total_elems;          // int32 [T]
+  size_t off_elems;            // int32 [T + 1]
+  size_t entry_elems;          // int32 [T * K]
+};
+SparseCsrLayout sparse_csr_layout(int T, int K);
+cudaError_t launch_sparse_csr(const int32_t* idx, int T, int K, const SparseCsrLayout& l,
+                              int32_t* table, int32_t* total, int32_t* off, int32_t* entries,
+                              cudaStream_t st);
+cudaError_t launch_sparse_dkv_reduce(const float* contrib, const int32_t* entries,
+                                     const int32_t* off, int T, int nhb, __nv_bfloat16* dkv,
+                                     cudaStream_t st);
+// Ordered backward: Delta, CSR, main kernel storing contribution rows, reduce.
+cudaError_t launch_sparse_bwd_ordered(const SparseArgs& a, float* delta, int32_t* table,
+                                      int32_t* total, int32_t* off, int32_t* entries,
+                                      __nv_bfloat16* dkv, cudaStream_t st);
 
 }  // namespace attn

@@ -46,7 +46,7 @@ __global__ void __launch_bounds__(256) sparse_bwd_preprocess_kernel(const Sparse
     if (lane == 0) delta[r] = acc;
   }
   float4* z = reinterpret_cast<float4*>(a.dkv_acc);
-  const size_t n4 = static_cast<size_t>(a.T) * SP_DQK / 4;
+  const size_t n4 = a.dkv_acc ? static_cast<size_t>(a.T) * SP_DQK / 4 : 0;
   for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4;
        i += static_cast<size_t>(gridDim.x) * blockDim.x)
     z[i] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -83,6 +83,26 @@ cudaError_t launch_sparse_bwd(const SparseArgs& a, float* delta, __nv_bfloat16* 
   if (gc > 152 * 8) gc = 152 * 8;
   sparse_dkv_cast_kernel<<<gc, 256, 0, st>>>(a.dkv_acc, dkv, n8);
   return cudaGetLastError();
+}
+
+cudaError_t launch_sparse_bwd_ordered(const SparseArgs& a, float* delta, int32_t* table,
+                                      int32_t* total, int32_t* off, int32_t* entries,
+                                      __nv_bfloat16* dkv, cudaStream_t st) {
+  cudaError_t e;
+  const size_t rows = static_cast<size_t>(a.T) * a.H;
+  int g = static_cast<int>((rows * 32 + 255) / 256);
+  if (g > 152 * 8) g = 152 * 8;
+  SparseArgs pa = a;
+  pa.dkv_acc = nullptr;   // Delta only: there is no accumulator to clear
+  sparse_bwd_preprocess_kernel<<<g, 256, 0, st>>>(pa, delta);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  const SparseCsrLayout l = sparse_csr_layout(a.T, a.K);
+  if ((e = launch_sparse_csr(a.idx, a.T, a.K, l, table, total, off, entries, st)) != cudaSuccess)
+    return e;
+  pa.delta = delta;
+  if ((e = launch_sparse_bwd_main(pa, st)) != cudaSuccess) return e;
+  const int nhb = (a.H + 63) / 64;
+  return launch_sparse_dkv_reduce(a.contrib, entries, off, a.T, nhb, dkv, st);
 }
 
 }  // namespace attn

@@ -274,7 +274,18 @@ __global__ void __launch_bounds__(SB_THREADS, 1) sparse_bwd_tc_kernel(const Spar
         tc_fence_before();
         mbar_arrive(&bar_pc_free[b]);
         const int j = active ? s_row[c & 3][slot] : -1;
-        if (j >= 0) {
+        if (j >= 0 && a.contrib) {
+          // ordered path: this (token, slot, head block) row, stored once
+          float* dst = a.contrib +
+                       ((static_cast<size_t>(t) * a.K + c * SB_NK + slot) * gridDim.y + blockIdx.y) *
+                           SB_DQK +
+                       64 * p;
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            *reinterpret_cast<float4*>(dst + 4 * i) =
+                make_float4(__uint_as_float(u[4 * i]), __uint_as_float(u[4 * i + 1]),
+                            __uint_as_float(u[4 * i + 2]), __uint_as_float(u[4 * i + 3]));
+        } else if (j >= 0) {
           float* dst = a.dkv_acc + static_cast<size_t>(j) * SB_DQK + 64 * p;
 #pragma unroll
           for (int i = 0; i < 16; ++i)

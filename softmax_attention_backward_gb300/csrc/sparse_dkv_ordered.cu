@@ -1,0 +1,179 @@
+// Deterministic dKV for the top-k sparse backward: disjoint ownership instead
+// of atomics (the ordering discipline of "[2/2] Add TileLang fused DSA kernels
+// support with THD and CP", Megatron-LM #5049, whose sparse MLA backward adds
+// dKV with fp32 atomics; its review thread and the CSA kernels' notes on
+// bitwise reproducibility ask for a fixed reduction order).
+//
+// The backward main kernel stores every (token, slot, head block)
+// contribution row dS^T Q + P^T [dO | 0] (fp32, dim_qk wide) once, into a
+// workspace indexed by (token * topk + slot) * head_blocks + head_block,
+// instead of adding it into dKV.  Here the index lists are inverted into a
+// CSR by key row, each row's entries in ascending token order:
+//   count  per (token block, key row) the slots that name the row
+//   scan   down the token blocks per key row (block bases and totals), then
+//          across key rows (row offsets)
+//   fill   each token block walks its tokens in order and appends (t, slot)
+//          at its row's running position
+// and one warp per key row sums its contribution rows in that order and
+// writes the bf16 dKV row.  The result is bitwise reproducible; it differs
+// from the atomic path only in the order of the fp32 additions.
+#include <cuda_runtime.h>
+
+#include "launch.h"
+
+namespace attn {
+
+namespace {
+
+constexpr int kDqk = 576;
+constexpr int kCsrThreads = 512;
+
+__global__ void __launch_bounds__(kCsrThreads) csr_count_kernel(const int32_t* __restrict__ idx,
+                                                                int T, int K, int tb,
+                                                                int32_t* __restrict__ table) {
+  const int b = blockIdx.x;
+  const int t_end = min(T, (b + 1) * tb);
+  int32_t* row = table + static_cast<size_t>(b) * T;
+  for (int t = b * tb; t < t_end; ++t) {
+    const int32_t* it = idx + static_cast<size_t>(t) * K;
+    for (int s = threadIdx.x; s < K; s += blockDim.x) {
+      const int j = __ldg(it + s);
+      if (j >= 0 && j < T) atomicAdd(row + j, 1);
+    }
+  }
+}
+
+// Per key row j: exclusive prefix over the token blocks (in place), total.
+__global__ void __launch_bounds__(256) csr_colscan_kernel(int32_t* __restrict__ table, int T,
+                                                          int nblk, int32_t* __restrict__ total) {
+  const int j = blockIdx.x * blockDim.x + threadIdx.x;
+  if (j >= T) return;
+  int run = 0;
+  for (int b = 0; b < nblk; ++b) {
+    int32_t* c = table + static_cast<size_t>(b) * T + j;
+    const int v = *c;
+    *c = run;
+    run += v;
+  }
+  total[j] = run;
+}
+
+// Exclusive prefix of total[0..T) into off[0..T], one block.
+__global__ void __launch_bounds__(1024) csr_rowscan_kernel(const int32_t* __restrict__ total,
+                                                           int T, int32_t* __restrict__ off) {
+  __shared__ int part[1024];
+  const int n = blockDim.x, tid = threadIdx.x;
+  const int per = (T + n - 1) / n;
+  const int lo = min(T, tid * per), hi = min(T, lo + per);
+  int sum = 0;
+  for (int j = lo; j < hi; ++j) sum += total[j];
+  part[tid] = sum;
+  __syncthreads();
+  // Hillis-Steele inclusive scan of the per-thread sums
+  for (int d = 1; d < n; d <<= 1) {
+    const int v = tid >= d ? part[tid - d] : 0;
+    __syncthreads();
+    part[tid] += v;
+    __syncthreads();
+  }
+  int run = part[tid] - sum;
+  for (int j = lo; j < hi; ++j) {
+    off[j] = run;
+    run += total[j];
+  }
+  if (tid == n - 1) off[T] = part[n - 1];
+}
+
+__global__ void __launch_bounds__(kCsrThreads) csr_fill_kernel(const int32_t* __restrict__ idx,
+                                                               int T, int K, int tb,
+                                                               int32_t* __restrict__ table,
+                                                               const int32_t* __restrict__ off,
+                                                               int32_t* __restrict__ entries) {
+  const int b = blockIdx.x;
+  const int t_end = min(T, (b + 1) * tb);
+  int32_t* row = table + static_cast<size_t>(b) * T;
+  for (int t = b * tb; t < t_end; ++t) {
+    const int32_t* it = idx + static_cast<size_t>(t) * K;
+    for (int s = threadIdx.x; s < K; s += blockDim.x) {
+      const int j = __ldg(it + s);
+      // a token names a row at most once, so within a token the running
+      // positions do not collide; the atomic only keeps the positions
+      // distinct for lists that break that contract
+      if (j >= 0 && j < T) entries[off[j] + atomicAdd(row + j, 1)] = t * K + s;
+    }
+    __syncthreads();   // tokens append in ascending order
+  }
+}
+
+// One warp per key row: lane l owns dims 2l + 64k, k = 0..8 (float2 each).
+__global__ void __launch_bounds__(256) dkv_reduce_kernel(const float* __restrict__ contrib,
+                                                         const int32_t* __restrict__ entries,
+                                                         const int32_t* __restrict__ off, int T,
+                                                         int nhb, __nv_bfloat16* __restrict__ dkv) {
+  const int j = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (j >= T) return;
+  float acc[18];
+#pragma unroll
+  for (int i = 0; i < 18; ++i) acc[i] = 0.f;
+  const int e0 = off[j], e1 = off[j + 1];
+  for (int e = e0; e < e1; ++e) {
+    const size_t base = static_cast<size_t>(__ldg(entries + e)) * nhb * kDqk;
+    for (int h = 0; h < nhb; ++h) {
+      const float2* r = reinterpret_cast<const float2*>(contrib + base + static_cast<size_t>(h) * kDqk);
+      float2 v[9];
+#pragma unroll
+      for (int k = 0; k < 9; ++k) v[k] = __ldcs(r + lane + 32 * k);
+#pragma unroll
+      for (int k = 0; k < 9; ++k) {
+        acc[2 * k] += v[k].x;
+        acc[2 * k + 1] += v[k].y;
+      }
+    }
+  }
+  uint32_t* out = reinterpret_cast<uint32_t*>(dkv + static_cast<size_t>(j) * kDqk);
+#pragma unroll
+  for (int k = 0; k < 9; ++k) out[lane + 32 * k] = pack_bf16(acc[2 * k], acc[2 * k + 1]);
+}
+
+}  // namespace
+
+SparseCsrLayout sparse_csr_layout(int T, int K) {
+  SparseCsrLayout l{};
+  const int nblk_max = 128;
+  l.nblk = T < nblk_max ? T : nblk_max;
+  if (l.nblk < 1) l.nblk = 1;
+  l.tb = (T + l.nblk - 1) / l.nblk;
+  l.nblk = (T + l.tb - 1) / l.tb;
+  l.table_elems = static_cast<size_t>(l.nblk) * T;
+  l.total_elems = static_cast<size_t>(T);
+  l.off_elems = static_cast<size_t>(T) + 1;
+  l.entry_elems = static_cast<size_t>(T) * K;
+  return l;
+}
+
+cudaError_t launch_sparse_csr(const int32_t* idx, int T, int K, const SparseCsrLayout& l,
+                              int32_t* table, int32_t* total, int32_t* off, int32_t* entries,
+                              cudaStream_t st) {
+  cudaError_t e;
+  if ((e = cudaMemsetAsync(table, 0, l.table_elems * sizeof(int32_t), st)) != cudaSuccess) return e;
+  csr_count_kernel<<<l.nblk, kCsrThreads, 0, st>>>(idx, T, K, l.tb, table);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  csr_colscan_kernel<<<(T + 255) / 256, 256, 0, st>>>(table, T, l.nblk, total);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  csr_rowscan_kernel<<<1, 1024, 0, st>>>(total, T, off);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  csr_fill_kernel<<<l.nblk, kCsrThreads, 0, st>>>(idx, T, K, l.tb, table, off, entries);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_sparse_dkv_reduce(const float* contrib, const int32_t* entries,
+                                     const int32_t* off, int T, int nhb, __nv_bfloat16* dkv,
+                                     cudaStream_t st) {
+  const int warps_per_block = 8;
+  dkv_reduce_kernel<<<(T + warps_per_block - 1) / warps_per_block, 32 * warps_per_block, 0, st>>>(
+      contrib, entries, off, T, nhb, dkv);
+  return cudaGetLastError();
+}
+
+}  // namespace attn

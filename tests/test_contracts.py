@@ -137,6 +137,16 @@ def test_sparse_out_of_range_index_is_flagged_and_skipped():
     ref_o, ref_lse = oracle.sparse_forward(q, kv, cleaned, 576 ** -0.5)
     assert_close("o", o, ref_o)
     assert_lse("lse", lse, ref_lse)
+    # both backward paths skip the bad slots (the ordered one also when it
+    # inverts the index lists) and flag them
+    ref = oracle.sparse_backward(q, kv, cleaned, do, 576 ** -0.5)
+    for bwd in (A.sparse_attn_bwd, A.sparse_attn_bwd_deterministic):
+        err.zero_()
+        dq, dkv = bwd(q.to(DEV), kv.to(DEV), bad.to(DEV), o, do.to(DEV), lse, error_word=err)
+        torch.cuda.synchronize()
+        assert int(err.item()) & 0x1
+        assert_close("dq", dq, ref["dq"])
+        assert_close("dkv", dkv, ref["dkv"])
 
 
 def test_split_mode_flags_sequence_longer_than_max_seqlen():
@@ -172,3 +182,14 @@ def test_sparse_outputs_fully_written():
     A.sparse_attn_bwd(q, kv, idx, o, do, lse, workspace=ws, dq=dq, dkv=dkv)
     for t in (o, lse, dq, dkv):
         assert torch.isfinite(t).all()
+    # ordered path: 0xFF-filled workspace and NaN outputs, every slot still written,
+    # key rows that no token names get exact zeros
+    dq2, dkv2 = torch.full_like(q, float("nan")), torch.full_like(kv, float("nan"))
+    ws2 = torch.full((A.sparse_attn_bwd_deterministic_workspace_size(q, idx),), 0xFF,
+                     dtype=torch.uint8, device=DEV)
+    A.sparse_attn_bwd_deterministic(q, kv, idx, o, do, lse, workspace=ws2, dq=dq2, dkv=dkv2)
+    assert torch.isfinite(dq2).all() and torch.isfinite(dkv2).all()
+    named = torch.zeros(T, dtype=torch.bool, device=DEV)
+    named[idx[idx >= 0].long()] = True
+    assert (dkv2[~named] == 0).all()
+    assert torch.equal(dq2, dq)

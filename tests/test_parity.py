@@ -142,13 +142,14 @@ def test_thd_varlen_causal_h16_d128_sampled(mode):
 # ----------------------------------------------------------------------------
 # Top-k sparse
 # ----------------------------------------------------------------------------
-def run_sparse(q, kv, idx, do, scale):
+def run_sparse(q, kv, idx, do, scale, deterministic=False):
     err = _err_word()
     gq, gkv, gidx, gdo = _gpu(q, kv, idx, do)
     o, lse = A.sparse_attn_fwd(gq, gkv, gidx, scale=scale, error_word=err)
-    dq, dkv = A.sparse_attn_bwd(gq, gkv, gidx, o, gdo, lse, scale=scale, error_word=err)
+    bwd = A.sparse_attn_bwd_deterministic if deterministic else A.sparse_attn_bwd
+    dq, dkv = bwd(gq, gkv, gidx, o, gdo, lse, scale=scale, error_word=err)
     _check_err(err)
-    return dict(o=o, lse=lse, dq=dq, dkv=dkv)
+    return dict(o=o, lse=lse, dq=dq, dkv=dkv, gpu=(gq, gkv, gidx, gdo))
 
 
 @pytest.mark.parametrize("T,H,K", [(600, 64, 256), (300, 16, 100), (200, 128, 64), (150, 32, 33)])
@@ -161,6 +162,42 @@ def test_sparse_small_full(T, H, K):
     assert_lse("lse", got["lse"], ref["lse"])
     assert_close("dq", got["dq"], ref["dq"])
     assert_close("dkv", got["dkv"], ref["dkv"])
+
+
+@pytest.mark.parametrize("T,H,K", [(600, 64, 256), (300, 16, 100), (200, 128, 64), (150, 32, 33)])
+def test_sparse_deterministic_small_full(T, H, K):
+    """Ordered dKV: parity with the oracle, dKV bitwise equal over repeated
+    runs, dQ bitwise equal to the atomic path (the same kernel computes it)."""
+    q, kv, do, idx = W.sparse_inputs(T, H, K, seed=20 + H)
+    scale = 576 ** -0.5
+    got = run_sparse(q, kv, idx, do, scale, deterministic=True)
+    ref = oracle.sparse_backward(q, kv, idx, do, scale)
+    assert_close("dq", got["dq"], ref["dq"])
+    assert_close("dkv", got["dkv"], ref["dkv"])
+    gq, gkv, gidx, gdo = got["gpu"]
+    for _ in range(3):
+        dq2, dkv2 = A.sparse_attn_bwd_deterministic(gq, gkv, gidx, got["o"], gdo, got["lse"],
+                                                    scale=scale)
+        assert torch.equal(dkv2, got["dkv"]) and torch.equal(dq2, got["dq"])
+    dq_at, _ = A.sparse_attn_bwd(gq, gkv, gidx, got["o"], gdo, got["lse"], scale=scale)
+    assert torch.equal(dq_at, got["dq"])
+
+
+def test_sparse_deterministic_topk2048_t8192_h64_sampled():
+    w, x = workload_inputs("sparse_topk2048_t8192_h64")
+    got = run_sparse(x["q"], x["kv"], x["idx"], x["do"], w.scale, deterministic=True)
+    q, kv, idx, do = (x[n].double() if n != "idx" else x[n] for n in ("q", "kv", "idx", "do"))
+    for t in (0, 2048, 8191):
+        r = oracle.sparse_token(q[t], kv, idx[t], do[t], w.scale)
+        assert_close(f"dq[{t}]", got["dq"][t], r["dq"])
+    rows = [8191, 8150, 4000, 0]
+    ref = oracle.sparse_dkv_rows(x["q"], x["kv"], x["idx"], x["do"], w.scale, rows)
+    for c, j in enumerate(rows):
+        assert_close(f"dkv[{j}]", got["dkv"][j], ref[c])
+    gq, gkv, gidx, gdo = got["gpu"]
+    _, dkv2 = A.sparse_attn_bwd_deterministic(gq, gkv, gidx, got["o"], gdo, got["lse"],
+                                              scale=w.scale)
+    assert torch.equal(dkv2, got["dkv"])
 
 
 def test_sparse_topk2048_t8192_h64_sampled():

@@ -113,6 +113,9 @@ Problem to_kernel(const attn_problem_t* p) {
   k.num_seqs = thd ? p->num_seqs : 0;
   k.max_seqlen = thd ? p->max_seqlen : p->seqlen;
   k.err = p->error_word;
+  k.fd_hq = make_fastdiv(static_cast<uint32_t>(k.heads_q));
+  k.fd_hkv = make_fastdiv(static_cast<uint32_t>(k.heads_kv));
+  k.fd_grp = make_fastdiv(static_cast<uint32_t>(k.heads_kv > 0 ? k.heads_q / k.heads_kv : 1));
   return k;
 }
 
@@ -188,6 +191,8 @@ attn_status_t attn_fwd(const attn_problem_t* p, const void* q, const void* k, co
   if (total >= (int64_t(1) << 31)) return ATTN_ERR_UNSUPPORTED;
   a.total_items = static_cast<int>(total);
   a.n_x = gx;
+  a.fd_nx = make_fastdiv(static_cast<uint32_t>(gx));
+  a.fd_nbh = make_fastdiv(static_cast<uint32_t>(kp.heads_q * kp.batch));
   // D = 64: one persistent CTA per SM (the next item's query tiles and first
   // MMAs overlap the current epilogue); D = 128: one CTA per item (its shared
   // memory holds a single query-pair buffer).
@@ -292,6 +297,8 @@ attn_status_t attn_bwd(const attn_problem_t* p, attn_dq_mode_t mode, const void*
   if (total >= (int64_t(1) << 31)) return ATTN_ERR_UNSUPPORTED;
   a.total_items = static_cast<int>(total);
   a.n_x = gx;
+  a.fd_nx = make_fastdiv(static_cast<uint32_t>(gx));
+  a.fd_nbh = make_fastdiv(static_cast<uint32_t>(kp.heads_kv * kp.batch));
   // One persistent CTA per SM walks the items, so K/V loads and the dK/dV
   // epilogue of one item overlap the next.
   const int sms = sm_count();

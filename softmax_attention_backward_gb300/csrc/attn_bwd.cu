@@ -97,24 +97,26 @@ struct BwdItem {
 //    in reverse, so CTAs resident together work on the same heads.
 template <int BN, int BM>
 __device__ __forceinline__ bool next_bwd_item(const Problem& p, int total, int n_x, int x_major,
+                                              const FastDiv& fd_nbh, const FastDiv& fd_nx,
                                               int& k, BwdItem& w) {
   const int G = gridDim.x, c = blockIdx.x;
-  const int groups = p.heads_q / p.heads_kv;
+  const int groups = static_cast<int>(p.fd_grp.d);
   const int n_bh = p.heads_kv * p.batch;
   for (; k * G < total; ++k) {
     const int idx = k * G + ((k & 1) ? (G - 1 - c) : c);
     if (idx >= total) continue;
     int bh, x;
     if (x_major) {
-      x = idx / n_bh;
+      x = static_cast<int>(fdiv(idx, fd_nbh));
       bh = idx - x * n_bh;
     } else {
-      bh = idx / n_x;
+      bh = static_cast<int>(fdiv(idx, fd_nx));
       x = idx - bh * n_x;
     }
-    w.hk = bh % p.heads_kv;
+    const int b = static_cast<int>(fdiv(bh, p.fd_hkv));
+    w.hk = bh - b * p.heads_kv;
     int jt;
-    if (!decode_tile(p, x, bh / p.heads_kv, BN, w.seq, jt)) continue;
+    if (!decode_tile(p, x, b, BN, w.seq, jt)) continue;
     if (!x_major && p.causal) jt = (w.seq.len + BN - 1) / BN - 1 - jt;
     w.jt = jt;
     w.kv0 = jt * BN;
@@ -170,7 +172,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
   const Problem& p = a.p;
   const int warp = warp_id();
   const int total = a.total_items;
-  const int G = p.heads_q / p.heads_kv;
+  const int G = static_cast<int>(p.fd_grp.d);   // query heads per kv head
   AbortCtx ac{&abort_flag, p.err};
 
   if (threadIdx.x == 0) {
@@ -216,7 +218,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       BwdItem w;
       int k = 0, ic = 0, gs = 0;
       bool ok = true;
-      while (ok && next_bwd_item<BN, BM>(p, total, a.n_x, a.x_major, k, w)) {
+      while (ok && next_bwd_item<BN, BM>(p, total, a.n_x, a.x_major, a.fd_nbh, a.fd_nx, k, w)) {
         const int kb = ic % C::KV_BUFS, ku = ic / C::KV_BUFS;
         if (!mbar_wait(&bar_kv_empty[kb], (ku & 1) ^ 1, ac)) break;
         mbar_arrive_expect_tx(&bar_kv_full[kb], 2 * C::KV_BYTES);
@@ -226,12 +228,15 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
           tma_load_4d(&tmV, &bar_kv_full[kb], sV(kb) + pn * BN * 128, pn * 64, w.hk,
                       w.seq.row0 + w.kv0, w.seq.b);
         }
+        // step it = ih * n_i + ii: query head hk * G + ih, query tile i_start + ii
+        int ih = 0, ii = -1;
         for (int it = 0; it < w.n_it; ++it) {
+          if (++ii == w.n_i) { ii = 0; ++ih; }
           const int g = gs + it;
           const int st = g % C::NST, use = g / C::NST;
           if (!mbar_wait(&bar_qempty[st], (use & 1) ^ 1, ac)) { ok = false; break; }
-          const int h = w.hk * G + it / w.n_i;
-          const int q0 = (w.i_start + it % w.n_i) * BM;
+          const int h = w.hk * G + ih;
+          const int q0 = (w.i_start + ii) * BM;
           mbar_arrive_expect_tx(&bar_qfull[st], 2 * C::QT_BYTES);
           for (int pn = 0; pn < PANELS; ++pn) {
             tma_load_4d(&tmQ, &bar_qfull[st], sQ + st * C::QT_BYTES + pn * BM * 128, pn * 64, h,
@@ -287,11 +292,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       BwdItem w, wn;
       int k = 0, ic = 0, gs = 0;
       bool ok = true;
-      bool have = next_bwd_item<BN, BM>(p, total, a.n_x, a.x_major, k, w);
+      bool have = next_bwd_item<BN, BM>(p, total, a.n_x, a.x_major, a.fd_nbh, a.fd_nx, k, w);
       bool sdp_done = false;   // S^T/dP^T of the next step already issued
       while (ok && have) {
         const int kb = ic % C::KV_BUFS, ku = ic / C::KV_BUFS;
-        const bool have_next = next_bwd_item<BN, BM>(p, total, a.n_x, a.x_major, k, wn);
+        const bool have_next = next_bwd_item<BN, BM>(p, total, a.n_x, a.x_major, a.fd_nbh, a.fd_nx, k, wn);
         const int kbn = (ic + 1) % C::KV_BUFS, kun = (ic + 1) / C::KV_BUFS;
         if (!mbar_wait_w(&bar_kv_full[kb], ku & 1, ac)) break;
         const uint64_t dK_mn = desc_mnmajor_base(smem_u32(sK(kb)), BN);
@@ -374,7 +379,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       BwdItem w;
       int k = 0, ic = 0, gs = 0;
       bool ok = true;
-      while (ok && next_bwd_item<BN, BM>(p, total, a.n_x, a.x_major, k, w)) {
+      while (ok && next_bwd_item<BN, BM>(p, total, a.n_x, a.x_major, a.fd_nbh, a.fd_nx, k, w)) {
         const int kb = ic % C::KV_BUFS, ku = ic / C::KV_BUFS;
         if (!mbar_wait_w(&bar_kv_full[kb], ku & 1, ac)) break;
         const uint64_t dK_k = desc_kmajor_base(smem_u32(sK(kb)));
@@ -421,7 +426,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       BwdItem w;
       int k = 0, ic = 0, gs = 0;
       bool ok = true;
-      while (ok && next_bwd_item<BN, BM>(p, total, a.n_x, a.x_major, k, w)) {
+      while (ok && next_bwd_item<BN, BM>(p, total, a.n_x, a.x_major, a.fd_nbh, a.fd_nx, k, w)) {
         for (int it = 0; it < w.n_it; ++it) {
           const int g = gs + it;
           const int st = g % C::NST;
@@ -469,7 +474,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       BwdItem w;
       int k = 0, ic = 0, gs = 0;
       bool ok = true;
-      while (ok && next_bwd_item<BN, BM>(p, total, a.n_x, a.x_major, k, w)) {
+      while (ok && next_bwd_item<BN, BM>(p, total, a.n_x, a.x_major, a.fd_nbh, a.fd_nx, k, w)) {
         const int kb = ic % C::KV_BUFS, ku = ic / C::KV_BUFS;
         if (!mbar_wait_w(&bar_kv_full[kb], ku & 1, ac)) break;
         const uint64_t dK_mn = desc_mnmajor_base(smem_u32(sK(kb)), BN);
@@ -507,12 +512,12 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     const float sl2 = a.scale_log2;
     // LSE or Delta of one query column, loaded one step ahead; the loaded value
     // is not touched until the next step, so the load latency stays hidden
-    auto fetch = [&](const BwdItem& w, int it) -> float {
+    auto fetch = [&](const BwdItem& w, int ih, int ii) -> float {
       if (tid >= 2 * BM) return 0.f;
       const bool is_lse = tid < BM;
       const int c = is_lse ? tid : tid - BM;
-      const int h = w.hk * G + it / w.n_i;
-      const int q = (w.i_start + it % w.n_i) * BM + c;
+      const int h = w.hk * G + ih;
+      const int q = (w.i_start + ii) * BM + c;
       if (q >= w.seq.len) return is_lse ? INFINITY : 0.f;
       size_t li;
       if (p.cu_seqlens)
@@ -528,25 +533,28 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     const uint32_t tDSme = tmem + lane_base + C::COL_DP + c0;    // D = 64: dS^T over dP^T
     BwdItem w;
     int k = 0, gs = 0;
-    bool have = next_bwd_item<BN, BM>(p, total, a.n_x, a.x_major, k, w);
-    float pf = have ? fetch(w, 0) : 0.f;
+    bool have = next_bwd_item<BN, BM>(p, total, a.n_x, a.x_major, a.fd_nbh, a.fd_nx, k, w);
+    float pf = have ? fetch(w, 0, 0) : 0.f;
     bool ok = true;
     while (ok && have) {
       const int kv = w.kv0 + r;                        // KV row inside the sequence
       const bool kv_ok = kv < w.seq.len;
+      int ih = 0, ii = -1;   // step it = ih * n_i + ii
       for (int it = 0; it < w.n_it; ++it) {
+        if (++ii == w.n_i) { ii = 0; ++ih; }
         const int g = gs + it;
-        const int q0 = (w.i_start + it % w.n_i) * BM;
+        const int q0 = (w.i_start + ii) * BM;
         const int buf = g & 1;
         if (tid < BM) s_nlse[buf][tid] = -pf * kLog2e;   // LSE in the log2 domain, negated
         else if (tid < 2 * BM) s_delta[buf][tid - BM] = pf;
         if (it + 1 < w.n_it) {
-          pf = fetch(w, it + 1);
+          const bool wrap = ii + 1 == w.n_i;
+          pf = fetch(w, wrap ? ih + 1 : ih, wrap ? 0 : ii + 1);
         } else {
           // last step of the item: look up the next one for the prefetch
           BwdItem wn;
           int kn = k;
-          if (next_bwd_item<BN, BM>(p, total, a.n_x, a.x_major, kn, wn)) pf = fetch(wn, 0);
+          if (next_bwd_item<BN, BM>(p, total, a.n_x, a.x_major, a.fd_nbh, a.fd_nx, kn, wn)) pf = fetch(wn, 0, 0);
         }
         named_bar_sync(1, 256);
         // ---- P^T (KV row r, query columns c0 .. c0 + HALF) ----
@@ -729,7 +737,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         mbar_arrive(&bar_ds);
       }
       gs += w.n_it;
-      have = next_bwd_item<BN, BM>(p, total, a.n_x, a.x_major, k, w);
+      have = next_bwd_item<BN, BM>(p, total, a.n_x, a.x_major, a.fd_nbh, a.fd_nx, k, w);
     }
   } else {
     // ---------------- dQ drain and dK/dV epilogue (warps 8..11) ----------------
@@ -758,7 +766,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     BwdItem w;
     int k = 0, ic = 0, gs = 0;
     bool ok = true;
-    while (ok && next_bwd_item<BN, BM>(p, total, a.n_x, a.x_major, k, w)) {
+    while (ok && next_bwd_item<BN, BM>(p, total, a.n_x, a.x_major, a.fd_nbh, a.fd_nx, k, w)) {
       float* base = a.dq_acc;
       bool slab_ok = true;
       if (a.split) {
@@ -769,10 +777,12 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
           base += static_cast<size_t>(w.jt) * a.slab_elems;
         }
       }
+      int ih = 0, ii = -1;   // step it = ih * n_i + ii
       for (int it = 0; it < w.n_it; ++it) {
+        if (++ii == w.n_i) { ii = 0; ++ih; }
         const int g = gs + it;
-        const int h = w.hk * G + it / w.n_i;
-        const int q0 = (w.i_start + it % w.n_i) * BM;
+        const int h = w.hk * G + ih;
+        const int q0 = (w.i_start + ii) * BM;
         if (!mbar_wait(&bar_dq_full, g & 1, ac)) { ok = false; break; }
         tc_fence_after();
         // free the TMEM tile first, then wait for the staging tile

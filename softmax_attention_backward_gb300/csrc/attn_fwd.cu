@@ -65,6 +65,7 @@ struct FwdItem {
 // masking the last pair of a sequence is the longest, so slots are reversed.
 template <int BM, int BN>
 __device__ __forceinline__ bool next_fwd_item(const Problem& p, int total, int n_x, int x_major,
+                                              const FastDiv& fd_nbh, const FastDiv& fd_nx,
                                               int& k, FwdItem& w) {
   const int G = gridDim.x, c = blockIdx.x;
   const int n_bh = p.heads_q * p.batch;
@@ -73,15 +74,16 @@ __device__ __forceinline__ bool next_fwd_item(const Problem& p, int total, int n
     if (idx >= total) continue;
     int bh, x;
     if (x_major) {
-      x = idx / n_bh;
+      x = static_cast<int>(fdiv(idx, fd_nbh));
       bh = idx - x * n_bh;
     } else {
-      bh = idx / n_x;
+      bh = static_cast<int>(fdiv(idx, fd_nx));
       x = idx - bh * n_x;
     }
-    w.h = bh % p.heads_q;
+    const int b = static_cast<int>(fdiv(bh, p.fd_hq));
+    w.h = bh - b * p.heads_q;
     int pair;
-    if (!decode_tile(p, x, bh / p.heads_q, 2 * BM, w.seq, pair)) continue;
+    if (!decode_tile(p, x, b, 2 * BM, w.seq, pair)) continue;
     if (p.causal) pair = (w.seq.len + 2 * BM - 1) / (2 * BM) - 1 - pair;
     w.m0 = pair * 2 * BM;
 #pragma unroll
@@ -167,18 +169,18 @@ __global__ void __launch_bounds__(352, 1)
       };
       FwdItem w, wn;
       int k = 0, ic = 0, gring = 0;
-      bool have = next_fwd_item<C::BM, C::BN>(p, total, a.n_x, a.x_major, k, w);
+      bool have = next_fwd_item<C::BM, C::BN>(p, total, a.n_x, a.x_major, a.fd_nbh, a.fd_nx, k, w);
       bool ok = true;
       if (have) {
         if (mbar_wait(&bar_qempty[0], 1, ac)) issue_q(w, 0);
         else ok = false;
       }
       while (ok && have) {
-        const int hk = w.h / (p.heads_q / p.heads_kv);
+        const int hk = static_cast<int>(fdiv(w.h, p.fd_grp));
         // the next item's query pair is loaded as soon as its buffer frees
         // (with two buffers: when the previous item's S MMAs are done), while
         // this item's K/V tiles stream through the ring
-        const bool have_next = next_fwd_item<C::BM, C::BN>(p, total, a.n_x, a.x_major, k, wn);
+        const bool have_next = next_fwd_item<C::BM, C::BN>(p, total, a.n_x, a.x_major, a.fd_nbh, a.fd_nx, k, wn);
         bool q_pending = have_next;
         const int nqb = (ic + 1) % C::QBUFS;
         const uint32_t nq_par = (((ic + 1) / C::QBUFS) & 1) ^ 1;
@@ -240,7 +242,7 @@ __global__ void __launch_bounds__(352, 1)
       FwdItem w;
       int k = 0, ic = 0, gring = 0, cs = 0;   // cs: S tiles of this query tile so far
       bool ok = true;
-      while (ok && next_fwd_item<C::BM, C::BN>(p, total, a.n_x, a.x_major, k, w)) {
+      while (ok && next_fwd_item<C::BM, C::BN>(p, total, a.n_x, a.x_major, a.fd_nbh, a.fd_nx, k, w)) {
         const int qb = ic % C::QBUFS, qu = ic / C::QBUFS;
         const int nt = w.n_w[t];
         if (!mbar_wait_w(&bar_q[qb], qu & 1, ac)) break;
@@ -322,7 +324,7 @@ __global__ void __launch_bounds__(352, 1)
     FwdItem w;
     int k = 0, cs = 0;
     bool ok = true;
-    while (ok && next_fwd_item<C::BM, C::BN>(p, total, a.n_x, a.x_major, k, w)) {
+    while (ok && next_fwd_item<C::BM, C::BN>(p, total, a.n_x, a.x_major, a.fd_nbh, a.fd_nx, k, w)) {
       const int row = w.m0 + t * C::BM + tr;   // row inside the sequence
       const int nt = w.n_w[t];
       float m_run = -INFINITY, l_run = 0.f;

@@ -7,6 +7,7 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 
+#include "fastdiv.h"
 #include "sm100.cuh"
 
 namespace attn {
@@ -33,6 +34,7 @@ struct Problem {
   int num_seqs;
   int max_seqlen;   // THD: bound on any sequence length
   int32_t* err;
+  FastDiv fd_hq, fd_hkv, fd_grp;   // heads_q, heads_kv, heads_q / heads_kv
 };
 
 // One sequence of a problem: rows [row0, row0 + len) of batch entry `b`.

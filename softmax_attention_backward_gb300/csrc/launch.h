@@ -16,6 +16,7 @@ struct FwdArgs {
   int total_items;      // work items: query-tile-pair slots x heads x batch
   int n_x;              // query-tile-pair slots per (batch, head)
   int x_major;          // item numbering, see next_fwd_item
+  FastDiv fd_nx, fd_nbh; // n_x and heads_q * batch
 };
 
 struct BwdArgs {
@@ -33,6 +34,7 @@ struct BwdArgs {
   int n_x;              // K/V tile slots per (batch, kv head)
   int x_major;          // item numbering, see next_bwd_item
   float scale_log2;
+  FastDiv fd_nx, fd_nbh; // n_x and heads_kv * batch
 };
 
 template <int D>

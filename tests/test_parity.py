@@ -81,6 +81,23 @@ def test_dense_small_full(mode, B, S, hq, hkv, D, causal):
 
 
 @pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("B,S,hq,hkv,D", [
+    (5, 1000, 10, 5, 64),    # persistent grids over 5*5 kv heads, ragged last tile
+    (4, 3000, 6, 2, 128),    # persistent backward, 3:1 groups, ragged last tile
+])
+def test_dense_persistent_odd_shapes_sampled(mode, B, S, hq, hkv, D):
+    """More items than SMs with batch * heads and tile counts that are not
+    powers of two: the item decoding of the persistent grids (division by
+    invariant integers) on the paths the small cases do not take."""
+    q, k, v, do = W.dense_inputs(B, S, hq, hkv, D, seed=200 + S)
+    scale = D ** -0.5
+    got = run_dense(q, k, v, do, True, scale, mode)
+    units = [(0, 0), (B - 1, hkv - 1), (B // 2, hkv // 2)]
+    ref = oracle.dense_backward(q, k, v, do, scale, True, kv_heads=units)
+    compare_dense(got, ref, units, hq, hkv)
+
+
+@pytest.mark.parametrize("mode", MODES)
 def test_mha_causal_b8_h32_s1024_d64_sampled(mode):
     w, x = workload_inputs("mha_causal_b8_h32_s1024_d64")
     got = run_dense(x["q"], x["k"], x["v"], x["do"], w.causal, w.scale, mode)

@@ -14,7 +14,11 @@
 //   dKV[s] += dS^T Q + P^T [dO | 0]   in nine 64-dim pieces (M = 64 slots,
 //                      N = 64 dims), each drained from TMEM into the fp32 dKV
 //                      accumulator with vector reductions while the next
-//                      piece is computed (two piece buffers)
+//                      piece is computed (two piece buffers); in the ordered
+//                      (deterministic) path the drain instead stores the
+//                      piece into this (token, slot, head block)'s own
+//                      contribution row, summed later in token order
+//                      (sparse_dkv_ordered.cu)
 // P and dS go through shared memory as bf16 [head][slot] tiles, which serve
 // as the K-major B operand of dQ^T and the MN-major A operand of the dKV
 // pieces.  The scale c is folded into dS, so dQ and dKV need none later.

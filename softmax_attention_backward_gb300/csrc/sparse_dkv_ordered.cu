@@ -117,18 +117,40 @@ __global__ void __launch_bounds__(256) dkv_reduce_kernel(const float* __restrict
 #pragma unroll
   for (int i = 0; i < 18; ++i) acc[i] = 0.f;
   const int e0 = off[j], e1 = off[j + 1];
-  for (int e = e0; e < e1; ++e) {
-    const size_t base = static_cast<size_t>(__ldg(entries + e)) * nhb * kDqk;
-    for (int h = 0; h < nhb; ++h) {
-      const float2* r = reinterpret_cast<const float2*>(contrib + base + static_cast<size_t>(h) * kDqk);
-      float2 v[9];
+  const int nrow = (e1 - e0) * nhb;   // contribution rows of key row j, in order
+  auto row_of = [&](int i) -> const float2* {
+    const int e = e0 + i / nhb, h = i - (i / nhb) * nhb;
+    const size_t base = (static_cast<size_t>(__ldg(entries + e)) * nhb + h) * kDqk;
+    return reinterpret_cast<const float2*>(contrib + base) + lane;
+  };
+  int i = 0;
+  // four rows in flight per warp (the loads of a row are independent of the
+  // sums, so they overlap; the additions stay in row order)
+  for (; i + 4 <= nrow; i += 4) {
+    float2 v[4][9];
 #pragma unroll
-      for (int k = 0; k < 9; ++k) v[k] = __ldcs(r + lane + 32 * k);
+    for (int u = 0; u < 4; ++u) {
+      const float2* r = row_of(i + u);
+#pragma unroll
+      for (int k = 0; k < 9; ++k) v[u][k] = __ldcs(r + 32 * k);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
 #pragma unroll
       for (int k = 0; k < 9; ++k) {
-        acc[2 * k] += v[k].x;
-        acc[2 * k + 1] += v[k].y;
+        acc[2 * k] += v[u][k].x;
+        acc[2 * k + 1] += v[u][k].y;
       }
+  }
+  for (; i < nrow; ++i) {
+    const float2* r = row_of(i);
+    float2 v[9];
+#pragma unroll
+    for (int k = 0; k < 9; ++k) v[k] = __ldcs(r + 32 * k);
+#pragma unroll
+    for (int k = 0; k < 9; ++k) {
+      acc[2 * k] += v[k].x;
+      acc[2 * k + 1] += v[k].y;
     }
   }
   uint32_t* out = reinterpret_cast<uint32_t*>(dkv + static_cast<size_t>(j) * kDqk);

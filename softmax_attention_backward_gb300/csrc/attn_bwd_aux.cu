@@ -132,29 +132,31 @@ __global__ void __launch_bounds__(256) attn_dq_finalize_kernel(Problem p,
   };
   const uint32_t c_first = blockIdx.x * blockDim.x + threadIdx.x;
   if (!split) {
-    for (uint32_t c0 = c_first; c0 < nchunks; c0 += 2 * nthreads) {
-      const uint32_t cc[2] = {c0, c0 + nthreads};
-      float4 a[2][2];
-      bool live[2];
-      size_t di[2];
+    // four chunks (128 bytes of the accumulator) in flight per thread
+    constexpr int U = 4;
+    for (uint32_t c0 = c_first; c0 < nchunks; c0 += U * nthreads) {
+      float4 a[U][2];
+      bool live[U];
+      size_t di[U];
 #pragma unroll
-      for (int u = 0; u < 2; ++u) {
+      for (int u = 0; u < U; ++u) {
+        const uint32_t cu = c0 + u * nthreads;
         int srow = 0;
         live[u] = false;
         di[u] = 0;
         a[u][0] = a[u][1] = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (cc[u] < nchunks) {
-          di[u] = dq_index(cc[u], srow);
+        if (cu < nchunks) {
+          di[u] = dq_index(cu, srow);
           live[u] = true;
           if (srow < end) {
-            const size_t e0 = static_cast<size_t>(cc[u]) * 8;
-            a[u][0] = *reinterpret_cast<const float4*>(acc + e0);
-            a[u][1] = *reinterpret_cast<const float4*>(acc + e0 + 4);
+            const float4* src = reinterpret_cast<const float4*>(acc + static_cast<size_t>(cu) * 8);
+            a[u][0] = __ldcs(src);
+            a[u][1] = __ldcs(src + 1);
           }
         }
       }
 #pragma unroll
-      for (int u = 0; u < 2; ++u) {
+      for (int u = 0; u < U; ++u) {
         if (!live[u]) continue;
         const float v[8] = {a[u][0].x, a[u][0].y, a[u][0].z, a[u][0].w,
                             a[u][1].x, a[u][1].y, a[u][1].z, a[u][1].w};

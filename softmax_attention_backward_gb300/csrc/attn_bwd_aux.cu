@@ -46,7 +46,12 @@ __global__ void __launch_bounds__(256) attn_bwd_preprocess_kernel(Problem p,
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
       rr[u] = base + u * RPW + (threadIdx.x % 32) / TPR;
-      if (rr[u] < nrows) {
+      // THD rows past the last sequence (srow >= end) get Delta = 0 without
+      // reading O and dO
+      ov[u] = dv[u] = make_uint4(0u, 0u, 0u, 0u);
+      // (THD has batch 1, so the row of pair rr is rr / heads_q)
+      if (rr[u] < nrows &&
+          (p.cu_seqlens == nullptr || static_cast<int>(fdiv(rr[u], p.fd_hq)) < end)) {
         ov[u] = *reinterpret_cast<const uint4*>(o + static_cast<size_t>(rr[u]) * D + sub * 8);
         dv[u] = *reinterpret_cast<const uint4*>(dout + static_cast<size_t>(rr[u]) * D + sub * 8);
       }
@@ -87,9 +92,23 @@ __global__ void __launch_bounds__(256) attn_bwd_preprocess_kernel(Problem p,
     }
   }
   if (dq_acc) {
+    // the accumulator is [batch, head, row, dim]: clear the first `end` rows of
+    // every (batch, head) segment (all rows for dense; the finalize writes
+    // zeros for THD rows past the last sequence without reading them)
     float4* z = reinterpret_cast<float4*>(dq_acc);
-    const size_t n4 = acc_elems / 4;
-    for (size_t i = gtid; i < n4; i += nthreads) z[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (p.cu_seqlens == nullptr) {
+      const size_t n4 = acc_elems / 4;
+      for (size_t i = gtid; i < n4; i += nthreads) z[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    } else {
+      // THD (batch 1): rows [0, end) of each head's segment
+      const uint32_t seg4 = static_cast<uint32_t>(end) * (D / 4);
+      const size_t stride4 = static_cast<size_t>(rt) * (D / 4);
+      const uint32_t n4 = seg4 * hq;
+      for (uint32_t i = gtid; i < n4; i += nthreads) {
+        const uint32_t sgm = i / seg4;
+        z[sgm * stride4 + (i - sgm * seg4)] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
   }
 }
 

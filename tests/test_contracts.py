@@ -70,10 +70,15 @@ def test_thd_padding_rows_exact_zero_in_nan_buffers(mode):
     n = A.attn_bwd_workspace_size(q, k, mode=mode, causal=True, cu_seqlens=cu, max_seqlen=130)
     ws = torch.full((n,), 0xFF, dtype=torch.uint8, device=DEV)
     kw = dict(mode=mode, causal=True, cu_seqlens=cu, max_seqlen=130, workspace=ws)
-    delta = A.attn_bwd_preprocess(q, k, o, do, **kw)
+    delta = torch.full((4, cap), float("nan"), dtype=torch.float32, device=DEV)
+    A.attn_bwd_preprocess(q, k, o, do, delta=delta, **kw)
+    # Delta = rowsum(dO * O) on the valid rows, exact zeros on the padding rows
+    end = sum(lens)
+    want = (do.double() * o.double()).sum(-1).t()[:, :end]
+    assert torch.allclose(delta[:, :end].double(), want, rtol=1e-4, atol=1e-4)
+    assert (delta[:, end:] == 0).all()
     A.attn_bwd(q, k, v, do, lse, delta, dk=dk, dv=dv, **kw)
     A.attn_bwd_postprocess(q, k, dk, dv, dq=dq, **kw)
-    end = sum(lens)
     for t in (o, dq, dk, dv):
         assert torch.isfinite(t).all()
         assert (t[end:] == 0).all()

@@ -97,6 +97,29 @@ def test_dense_persistent_odd_shapes_sampled(mode, B, S, hq, hkv, D):
     compare_dense(got, ref, units, hq, hkv)
 
 
+def _random_dense_cases(n=8, seed=2026):
+    """Seeded shapes: batch 1-3, ragged lengths 1-700, 1-8 kv heads with 1-4 query
+    heads each, D in {64, 128}, causal or not."""
+    g = torch.Generator().manual_seed(seed)
+    r = lambda lo, hi: int(torch.randint(lo, hi + 1, (1,), generator=g))
+    cases = []
+    for _ in range(n):
+        hkv = r(1, 8)
+        cases.append((r(1, 3), r(1, 700), hkv * r(1, 4), hkv, (64, 128)[r(0, 1)], bool(r(0, 1))))
+    return cases
+
+
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("B,S,hq,hkv,D,causal", _random_dense_cases())
+def test_dense_random_shapes(mode, B, S, hq, hkv, D, causal):
+    q, k, v, do = W.dense_inputs(B, S, hq, hkv, D, seed=300 + S)
+    scale = D ** -0.5
+    got = run_dense(q, k, v, do, causal, scale, mode)
+    units = sorted({(0, 0), (B - 1, hkv - 1)})
+    ref = oracle.dense_backward(q, k, v, do, scale, causal, kv_heads=units)
+    compare_dense(got, ref, units, hq, hkv)
+
+
 @pytest.mark.parametrize("mode", MODES)
 def test_mha_causal_b8_h32_s1024_d64_sampled(mode):
     w, x = workload_inputs("mha_causal_b8_h32_s1024_d64")

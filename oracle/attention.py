@@ -59,7 +59,10 @@ def head_forward(q, k, v, scale, allowed):
     """q [Sq,D], k [Sk,D], v [Sk,Dv], allowed [Sq,Sk] bool -> o [Sq,Dv], lse [Sq]."""
     s = scale * (q @ k.T)
     s = torch.where(allowed, s, torch.full_like(s, NEG_INF))
-    m = s.max(dim=1, keepdim=True).values
+    if s.shape[1] == 0:                             # no key at all: the empty sum
+        m = torch.full((s.shape[0], 1), NEG_INF, dtype=s.dtype)
+    else:
+        m = s.max(dim=1, keepdim=True).values
     has = torch.isfinite(m)
     m_safe = torch.where(has, m, torch.zeros_like(m))
     e = torch.exp(s - m_safe)                       # exp(-inf) = 0 for masked pairs

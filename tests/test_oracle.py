@@ -273,6 +273,32 @@ def test_sparse_single_index_closed_form_and_unselected_rows():
     torch.testing.assert_close(r2["dq"], r["dq"], rtol=0, atol=0)
 
 
+def test_sparse_empty_index_list_and_slot_order():
+    """A token whose list holds no valid slot: the empty sum gives lse = -inf,
+    o = 0 and dq = 0, and the token adds nothing to dKV.  The -1 sentinel may
+    sit anywhere in a list: permuting each list's slots changes nothing."""
+    T, H, Dk, Dv, K = 12, 3, 8, 5, 6
+    q, kv, do = rnd(T, H, Dk, seed=57), rnd(T, Dk, seed=58), rnd(T, H, Dv, seed=59)
+    idx = workloads.topk_indices(T, K, seed=9)
+    idx[[4, 11]] = -1
+    r = oracle.sparse_backward(q, kv, idx, do, 0.5, dv_dims=Dv)
+    for t in (4, 11):
+        assert torch.isneginf(r["lse"][t]).all()
+        assert (r["o"][t] == 0).all() and (r["dq"][t] == 0).all() and (r["delta"][t] == 0).all()
+    assert torch.isfinite(r["dkv"]).all()
+    q2, do2 = q.clone(), do.clone()
+    q2[[4, 11]], do2[[4, 11]] = 7.0, -3.0
+    r2 = oracle.sparse_backward(q2, kv, idx, do2, 0.5, dv_dims=Dv)
+    torch.testing.assert_close(r2["dkv"], r["dkv"], rtol=0, atol=0)
+    g = torch.Generator().manual_seed(60)
+    perm = torch.stack([row[torch.randperm(K, generator=g)] for row in idx])
+    assert not torch.equal(perm, idx)
+    r3 = oracle.sparse_backward(q, kv, perm, do, 0.5, dv_dims=Dv)
+    for key in ("o", "dq", "dkv"):
+        torch.testing.assert_close(r3[key], r[key], rtol=0, atol=1e-12)
+    torch.testing.assert_close(r3["lse"], r["lse"], rtol=0, atol=1e-12)
+
+
 def test_sparse_dkv_rows_matches_full():
     T, H, Dk, Dv, K = 30, 2, 8, 5, 7
     q, kv, do = rnd(T, H, Dk, seed=42), rnd(T, Dk, seed=43), rnd(T, H, Dv, seed=44)

@@ -223,6 +223,28 @@ def test_sparse_deterministic_small_full(T, H, K):
     assert torch.equal(dq_at, got["dq"])
 
 
+@pytest.mark.parametrize("deterministic", [False, True])
+def test_sparse_empty_lists_and_scattered_sentinels(deterministic):
+    """Tokens whose whole list is -1 (o = 0, lse = -inf, dq = 0), the -1
+    sentinel scattered through every list instead of trailing, and more slots
+    than tokens (topk 130 over 70 tokens: three chunks, the last ragged)."""
+    T, H, K = 70, 32, 130
+    q, kv, do, idx = W.sparse_inputs(T, H, K, seed=61)
+    idx[[5, 33, 69]] = -1
+    g = torch.Generator().manual_seed(62)
+    idx = torch.stack([row[torch.randperm(K, generator=g)] for row in idx])
+    scale = 576 ** -0.5
+    got = run_sparse(q, kv, idx, do, scale, deterministic)
+    ref = oracle.sparse_backward(q, kv, idx, do, scale)
+    assert_close("o", got["o"], ref["o"])
+    assert_lse("lse", got["lse"], ref["lse"])
+    assert_close("dq", got["dq"], ref["dq"])
+    assert_close("dkv", got["dkv"], ref["dkv"])
+    for t in (5, 33, 69):
+        assert torch.isneginf(got["lse"][t]).all()
+        assert (got["o"][t] == 0).all() and (got["dq"][t] == 0).all()
+
+
 def test_sparse_deterministic_topk2048_t8192_h64_sampled():
     w, x = workload_inputs("sparse_topk2048_t8192_h64")
     got = run_sparse(x["q"], x["kv"], x["idx"], x["do"], w.scale, deterministic=True)

@@ -45,6 +45,7 @@ constexpr int SB_T_BYTES = SB_HB * SB_NK * 2;  // P or dS tile
 constexpr int SB_SMEM = SB_Q_BYTES + SB_DO_BYTES + SB_KV_BYTES + 2 * SB_T_BYTES + 1024;
 constexpr int SB_THREADS = 352;
 constexpr int SB_PRODUCERS = 64;               // warps 8..9
+static_assert(SB_PRODUCERS == SB_NK, "one producer lane holds each slot's index");
 constexpr int SB_PIECES = SB_DQK / 64;         // 64-dim pieces of a dKV row
 constexpr uint32_t SB_TMEM_COLS = 512;
 constexpr uint32_t SB_COL_S = 0, SB_COL_DP = 64;
@@ -156,28 +157,33 @@ __global__ void __launch_bounds__(SB_THREADS, 1) sparse_bwd_tc_kernel(const Spar
       s_delta[pt] = pt < nh ? __ldg(a.delta + li) : 0.f;
     }
     for (int c = 0; c < nchunks; ++c) {
-      // the single chunk buffer was last read by dQ^T of chunk c - 1
-      if (!mbar_wait(&bar_kv_empty, (c & 1) ^ 1, ac)) break;
+      // the single chunk buffer was last read by dQ^T of chunk c - 1 (warp-uniform
+      // answer: the lanes exchange indices below)
+      if (!mbar_wait_w(&bar_kv_empty, (c & 1) ^ 1, ac)) break;
       const int cb = c & 1;
-      {
-        const int slot = c * SB_NK + pt;
-        const int j = (slot < a.K) ? __ldg(irow + slot) : -1;
-        const bool valid = j >= 0 && j < a.T;
-        if (!valid && j != -1 && a.err) atomicOr(a.err, ATTN_DEVERR_INDEX_RANGE);
-        s_row[c & 3][pt] = valid ? j : -1;
-        const uint32_t m32 = __ballot_sync(0xffffffffu, valid);
-        if (lane == 0) s_valid[cb][pt >> 5] = m32;
-      }
+      const int slot = c * SB_NK + pt;
+      const int j = (slot < a.K) ? __ldg(irow + slot) : -1;
+      const bool valid = j >= 0 && j < a.T;
+      if (!valid && j != -1 && a.err) atomicOr(a.err, ATTN_DEVERR_INDEX_RANGE);
+      const int jr = valid ? j : -1;
+      s_row[c & 3][pt] = jr;
+      const uint32_t m32 = __ballot_sync(0xffffffffu, valid);
+      if (lane == 0) s_valid[cb][pt >> 5] = m32;
+      // each producer warp gathers the 32 rows whose indices its lanes hold, in
+      // (row, 16-byte column) order, taking a row's index by a shuffle rather
+      // than a load per copy; the chunk's gather is on the critical path (one
+      // buffer), and it runs faster the more copies are unrolled in flight
       const uint32_t base = smem_u32(sKV);
-      for (int id = pt; id < SB_NK * (SB_DQK / 8); id += SB_PRODUCERS) {
-        const int r = id / (SB_DQK / 8), ch = id % (SB_DQK / 8);
-        const int slot = c * SB_NK + r;
-        int j = (slot < a.K) ? __ldg(irow + slot) : -1;
-        if (j >= a.T) j = -1;
-        cp_async16(base + sb_off(r, ch, SB_NK),
-                   (j >= 0) ? static_cast<const void*>(a.kv + static_cast<size_t>(j) * SB_DQK + ch * 8)
-                            : static_cast<const void*>(a.kv),
-                   (j >= 0) ? 16u : 0u);
+      const int rw = pt & ~31;
+#pragma unroll 16
+      for (int k = 0; k < SB_DQK / 8; ++k) {   // 32 rows x 72 columns / 32 lanes
+        const int e = 32 * k + lane;
+        const int rl = e / (SB_DQK / 8), ch = e - rl * (SB_DQK / 8);
+        const int jj = __shfl_sync(0xffffffffu, jr, rl);
+        cp_async16(base + sb_off(rw + rl, ch, SB_NK),
+                   (jj >= 0) ? static_cast<const void*>(a.kv + static_cast<size_t>(jj) * SB_DQK + ch * 8)
+                             : static_cast<const void*>(a.kv),
+                   (jj >= 0) ? 16u : 0u);
       }
       cp_async_commit();
       cp_async_wait<0>();

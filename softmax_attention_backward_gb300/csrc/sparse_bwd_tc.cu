@@ -172,10 +172,11 @@ __global__ void __launch_bounds__(SB_THREADS, 1) sparse_bwd_tc_kernel(const Spar
       // each producer warp gathers the 32 rows whose indices its lanes hold, in
       // (row, 16-byte column) order, taking a row's index by a shuffle rather
       // than a load per copy; the chunk's gather is on the critical path (one
-      // buffer), and it runs faster the more copies are unrolled in flight
+      // buffer), and it runs faster the more copies are issued back to back,
+      // so the 72 copies of a lane are fully unrolled
       const uint32_t base = smem_u32(sKV);
       const int rw = pt & ~31;
-#pragma unroll 16
+#pragma unroll
       for (int k = 0; k < SB_DQK / 8; ++k) {   // 32 rows x 72 columns / 32 lanes
         const int e = 32 * k + lane;
         const int rl = e / (SB_DQK / 8), ch = e - rl * (SB_DQK / 8);

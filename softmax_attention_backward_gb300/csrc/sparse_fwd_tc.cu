@@ -40,6 +40,17 @@ constexpr int SF_P_BYTES = SF_HB * SF_NK * 2;
 constexpr int SF_SMEM = SF_Q_BYTES + 2 * SF_KV_BYTES + SF_P_BYTES + 1024;
 constexpr int SF_THREADS = 256;
 constexpr int SF_PRODUCERS = 96;               // threads of warps 4, 5 and 7
+constexpr int SF_GATHER_PER_WARP = SF_NK * (SF_DQK / 8) / 3;   // 16-byte copies per chunk and warp
+constexpr int SF_GATHER_ROWS = 22;             // key rows one warp's copies touch
+static_assert(SF_GATHER_PER_WARP % 32 == 0, "whole warp iterations");
+// first row and number of rows of producer warp w's copies
+constexpr int sf_gather_row0(int w) { return SF_GATHER_PER_WARP * w / (SF_DQK / 8); }
+constexpr int sf_gather_rows(int w) {
+  return (SF_GATHER_PER_WARP * (w + 1) - 1) / (SF_DQK / 8) - sf_gather_row0(w) + 1;
+}
+static_assert(sf_gather_rows(0) <= SF_GATHER_ROWS && sf_gather_rows(1) <= SF_GATHER_ROWS &&
+                  sf_gather_rows(2) <= SF_GATHER_ROWS && sf_gather_row0(2) + SF_GATHER_ROWS <= SF_NK,
+              "each warp's copies stay within the rows its lanes hold");
 constexpr uint32_t SF_TMEM_COLS = 512;
 constexpr uint32_t SF_COL_S = 0;               // two S buffers of 64 columns
 constexpr uint32_t SF_COL_O = 128;             // four O^T tiles of 64 columns
@@ -133,8 +144,9 @@ __global__ void __launch_bounds__(SF_THREADS, 1) sparse_fwd_tc_kernel(const Spar
     bool ok = true;
     auto issue_chunk = [&](int c) -> bool {
       const int b = c & 1;
-      // buffer b was last read by the O^T GEMM of chunk c - 2
-      if (!mbar_wait(&bar_kv_empty[b], ((c >> 1) & 1) ^ 1, ac)) return false;
+      // buffer b was last read by the O^T GEMM of chunk c - 2 (warp-uniform
+      // answer: the lanes exchange indices below)
+      if (!mbar_wait_w(&bar_kv_empty[b], ((c >> 1) & 1) ^ 1, ac)) return false;
       if (pt < SF_NK) {
         // slot pt of the chunk: range check, and one word of the valid mask per warp
         const int slot = c * SF_NK + pt;
@@ -144,12 +156,26 @@ __global__ void __launch_bounds__(SF_THREADS, 1) sparse_fwd_tc_kernel(const Spar
         const uint32_t m32 = __ballot_sync(0xffffffffu, valid);
         if ((pt & 31) == 0) s_valid[b][pt >> 5] = m32;
       }
+      // Producer warp pw takes copies [SF_GATHER_PER_WARP * pw, + SF_GATHER_PER_WARP) of
+      // the chunk in (row, 16-byte column) order.  Its lanes first load the key
+      // row indices of the (at most SF_GATHER_ROWS) rows those copies touch, once;
+      // each copy then takes its row's index by a shuffle.  The 48 copies of a
+      // lane are fully unrolled: the gather is issue-bound, and it runs faster
+      // the more copies go out back to back.
       const uint32_t base = smem_u32(sKV + b * SF_KV_BYTES);
-      for (int id = pt; id < SF_NK * (SF_DQK / 8); id += SF_PRODUCERS) {
-        const int r = id / (SF_DQK / 8), ch = id % (SF_DQK / 8);
-        const int slot = c * SF_NK + r;
-        int j = (slot < a.K) ? __ldg(irow + slot) : -1;
-        if (j >= a.T) j = -1;
+      const int pw = pt >> 5;
+      const int e0 = pw * SF_GATHER_PER_WARP, r0 = e0 / (SF_DQK / 8);
+      int jl = -1;
+      if (lane < SF_GATHER_ROWS) {
+        const int slot = c * SF_NK + r0 + lane;
+        jl = (slot < a.K) ? __ldg(irow + slot) : -1;
+        if (jl >= a.T) jl = -1;
+      }
+#pragma unroll
+      for (int k = 0; k < SF_GATHER_PER_WARP / 32; ++k) {
+        const int id = e0 + 32 * k + lane;
+        const int r = id / (SF_DQK / 8), ch = id - r * (SF_DQK / 8);
+        const int j = __shfl_sync(0xffffffffu, jl, r - r0);
         const void* src = (j >= 0) ? static_cast<const void*>(a.kv + static_cast<size_t>(j) * SF_DQK + ch * 8)
                                    : static_cast<const void*>(a.kv);
         cp_async16(base + sf_off(r, ch, SF_NK), src, (j >= 0) ? 16u : 0u);

@@ -127,6 +127,9 @@ int n_kv_tiles(const Problem& k) { return (k.max_seqlen + 127) / 128; }
 
 attn_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA; }
 
+
+}  // namespace
+
 // Streaming multiprocessors of the current device (persistent grid size).
 int sm_count() {
   constexpr int kMaxDevices = 64;
@@ -141,7 +144,6 @@ int sm_count() {
   return cached[dev];
 }
 
-}  // namespace
 }  // namespace attn
 
 using namespace attn;

@@ -229,20 +229,12 @@ __global__ void __launch_bounds__(256) attn_dq_finalize_kernel(Problem p,
   }
 }
 
-static int grid_for(size_t work, int per_block) {
-  size_t g = (work + per_block - 1) / per_block;
-  const size_t cap = 152 * 8;
-  if (g > cap) g = cap;
-  if (g < 1) g = 1;
-  return static_cast<int>(g);
-}
-
 template <int D>
 cudaError_t launch_bwd_preprocess(const Problem& p, const __nv_bfloat16* o,
                                   const __nv_bfloat16* dout, float* delta, float* dq_acc,
                                   size_t acc_elems, cudaStream_t st) {
   const size_t rows = static_cast<size_t>(p.batch) * p.rows_total * p.heads_q;
-  const int g = grid_for(rows * (D / 8), 256);
+  const int g = resident_grid(attn_bwd_preprocess_kernel<D>, rows * (D / 8), 256);
   attn_bwd_preprocess_kernel<D><<<g, 256, 0, st>>>(p, o, dout, delta, dq_acc, acc_elems);
   return cudaGetLastError();
 }
@@ -252,7 +244,9 @@ cudaError_t launch_dq_finalize(const Problem& p, const float* acc, size_t slab_e
                                int n_split, __nv_bfloat16* dq, __nv_bfloat16* dk,
                                __nv_bfloat16* dv, cudaStream_t st) {
   const size_t chunks = static_cast<size_t>(p.batch) * p.rows_total * p.heads_q * (D / 8);
-  const int g = grid_for(chunks, 256);
+  // two waves measured faster than one for the dense finalize (causal B 8, H 32, S 1024,
+  // D 64: 20.0 vs 21.1 us)
+  const int g = resident_grid(attn_dq_finalize_kernel<D>, chunks, 256, 2);
   attn_dq_finalize_kernel<D><<<g, 256, 0, st>>>(p, acc, slab_elems, split, n_split, 128, dq,
                                                         dk, dv);
   return cudaGetLastError();

@@ -8,6 +8,28 @@
 
 namespace attn {
 
+// Streaming multiprocessors of the current device (0 if it cannot be read).
+int sm_count();
+
+// Grid of a grid-stride kernel: at most `waves` whole waves of co-resident
+// blocks (SMs x the blocks of `threads` threads that fit on one SM at the
+// kernel's register and shared-memory use), fewer when the work is smaller.
+// A grid that is not a whole number of waves ends in a partial wave that
+// leaves most of every SM idle.
+template <typename Kernel>
+inline int resident_grid(Kernel kernel, size_t work, int threads, int waves = 1) {
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, 0) != cudaSuccess ||
+      per_sm < 1)
+    per_sm = 1;
+  const int sms = sm_count();
+  const size_t cap = static_cast<size_t>(sms > 0 ? sms : 1) * per_sm * (waves > 0 ? waves : 1);
+  size_t g = (work + threads - 1) / threads;
+  if (g > cap) g = cap;
+  if (g < 1) g = 1;
+  return static_cast<int>(g);
+}
+
 struct FwdArgs {
   Problem p;
   __nv_bfloat16* o;

@@ -71,16 +71,14 @@ cudaError_t launch_sparse_bwd(const SparseArgs& a, float* delta, __nv_bfloat16* 
                               cudaStream_t st) {
   cudaError_t e;
   const size_t rows = static_cast<size_t>(a.T) * a.H;
-  int g = static_cast<int>((rows * 32 + 255) / 256);
-  if (g > 152 * 8) g = 152 * 8;
+  const int g = resident_grid(sparse_bwd_preprocess_kernel, rows * 32, 256);
   SparseArgs pa = a;
   sparse_bwd_preprocess_kernel<<<g, 256, 0, st>>>(pa, delta);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   pa.delta = delta;
   if ((e = launch_sparse_bwd_main(pa, st)) != cudaSuccess) return e;
   const size_t n8 = static_cast<size_t>(a.T) * SP_DQK / 8;
-  int gc = static_cast<int>((n8 + 255) / 256);
-  if (gc > 152 * 8) gc = 152 * 8;
+  const int gc = resident_grid(sparse_dkv_cast_kernel, n8, 256);
   sparse_dkv_cast_kernel<<<gc, 256, 0, st>>>(a.dkv_acc, dkv, n8);
   return cudaGetLastError();
 }
@@ -90,8 +88,7 @@ cudaError_t launch_sparse_bwd_ordered(const SparseArgs& a, float* delta, int32_t
                                       __nv_bfloat16* dkv, cudaStream_t st) {
   cudaError_t e;
   const size_t rows = static_cast<size_t>(a.T) * a.H;
-  int g = static_cast<int>((rows * 32 + 255) / 256);
-  if (g > 152 * 8) g = 152 * 8;
+  const int g = resident_grid(sparse_bwd_preprocess_kernel, rows * 32, 256);
   SparseArgs pa = a;
   pa.dkv_acc = nullptr;   // Delta only: there is no accumulator to clear
   sparse_bwd_preprocess_kernel<<<g, 256, 0, st>>>(pa, delta);

@@ -144,13 +144,13 @@ def _need(t, name, dtype, device=None):
     return t
 
 
-def _nondeterministic(what: str):
+def _nondeterministic(what: str, instead: str):
     if torch.are_deterministic_algorithms_enabled():
         msg = f"{what} accumulates with fp32 atomics and is not bitwise reproducible"
         if torch.is_deterministic_algorithms_warn_only_enabled():
             warnings.warn(msg, RuntimeWarning, stacklevel=3)
         else:
-            raise RuntimeError(msg + "; use dq_mode=ATTN_DQ_SPLIT for the dense path")
+            raise RuntimeError(f"{msg}; use {instead}")
 
 
 def _problem(q, k, causal, scale, cu_seqlens, max_seqlen, error_word):
@@ -240,7 +240,7 @@ def attn_bwd(q, k, v, dout, lse, delta, *, mode=ATTN_DQ_ATOMIC, workspace, causa
     workspace.  Call attn_bwd_preprocess before and attn_bwd_postprocess after,
     with the same workspace and mode."""
     if int(mode) == ATTN_DQ_ATOMIC:
-        _nondeterministic("attn_bwd(dq_mode=ATTN_DQ_ATOMIC)")
+        _nondeterministic("attn_bwd(dq_mode=ATTN_DQ_ATOMIC)", "dq_mode=ATTN_DQ_SPLIT")
     dev = q.device
     for n, t in (("q", q), ("k", k), ("v", v), ("dout", dout)):
         _need(t, n, torch.bfloat16, dev)
@@ -293,7 +293,7 @@ def attn_bwd_fixed_scratch(q, k, v, o, dout, lse, *, causal=False, scale=None, c
     library owns on each GPU.  Returns (dq, dk, dv).  Problems whose scratch
     need exceeds the array raise ValueError; calls that overlap on the GPU race
     on the shared array."""
-    _nondeterministic("attn_bwd_fixed_scratch")
+    _nondeterministic("attn_bwd_fixed_scratch", "attn_bwd with dq_mode=ATTN_DQ_SPLIT")
     dev = q.device
     for n, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dout", dout)):
         _need(t, n, torch.bfloat16, dev)
@@ -352,7 +352,7 @@ def sparse_attn_bwd_workspace_size(q, idx, *, scale=None) -> int:
 def sparse_attn_bwd(q, kv, idx, o, dout, lse, *, scale=None, workspace=None, dq=None, dkv=None,
                     error_word=None, stream=None):
     """Returns (dq [T,H,576], dkv [T,576]) bf16."""
-    _nondeterministic("sparse_attn_bwd (dKV)")
+    _nondeterministic("sparse_attn_bwd (dKV)", "sparse_attn_bwd_deterministic")
     dev = q.device
     for n, t in (("q", q), ("kv", kv), ("o", o), ("dout", dout)):
         _need(t, n, torch.bfloat16, dev)

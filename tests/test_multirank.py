@@ -44,9 +44,15 @@ def test_deterministic_mode_guard_on_host():
     torch.use_deterministic_algorithms(True)
     try:
         x = torch.zeros(1)
-        with pytest.raises(RuntimeError, match="not bitwise reproducible"):
+        with pytest.raises(RuntimeError, match="not bitwise reproducible; use dq_mode=ATTN_DQ_SPLIT"):
             A.attn_bwd(x, x, x, x, x, x, mode=A.ATTN_DQ_ATOMIC, workspace=x)
-        with pytest.raises(RuntimeError, match="not bitwise reproducible"):
+        with pytest.raises(RuntimeError, match="not bitwise reproducible; use sparse_attn_bwd_deterministic"):
             A.sparse_attn_bwd(x, x, x, x, x, x)
+        # the reproducible paths pass the guard (and fail later on the dummy tensors)
+        for call in (lambda: A.attn_bwd(x, x, x, x, x, x, mode=A.ATTN_DQ_SPLIT, workspace=x),
+                     lambda: A.sparse_attn_bwd_deterministic(x, x, x, x, x, x)):
+            with pytest.raises(Exception) as e:
+                call()
+            assert "bitwise" not in str(e.value)
     finally:
         torch.use_deterministic_algorithms(False)

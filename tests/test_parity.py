@@ -169,6 +169,36 @@ def test_thd_small_full(mode, D):
     compare_thd(got, ref, cu, range(len(lens)), 4, 2)
 
 
+def _random_thd_cases(n=4, seed=2030):
+    """Seeded THD problems: 1-6 sequences of 0-400 rows (an empty one in about
+    half the cases), 0-100 padding rows, 1-4 kv heads with 1-3 query heads each,
+    D in {64, 128}, causal or not."""
+    g = torch.Generator().manual_seed(seed)
+    r = lambda lo, hi: int(torch.randint(lo, hi + 1, (1,), generator=g))
+    cases = []
+    for _ in range(n):
+        lens = [r(0, 400) for _ in range(r(1, 6))]
+        if r(0, 1):
+            lens[r(0, len(lens) - 1)] = 0
+        if sum(lens) == 0:
+            lens[0] = 1
+        hkv = r(1, 4)
+        cases.append((tuple(lens), r(0, 100), hkv * r(1, 3), hkv, (64, 128)[r(0, 1)], bool(r(0, 1))))
+    return cases
+
+
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("lens,pad,hq,hkv,D,causal", _random_thd_cases())
+def test_thd_random_lengths(mode, lens, pad, hq, hkv, D, causal):
+    cap = sum(lens) + pad
+    cu = W.cu_seqlens_from(lens)
+    q, k, v, do = W.thd_inputs(cap, hq, hkv, D, seed=400 + cap)
+    scale = D ** -0.5
+    got = run_dense(q, k, v, do, causal, scale, mode, cu=cu, max_seqlen=max(lens))
+    ref = oracle.thd_backward(q, k, v, do, cu, scale, causal)
+    compare_thd(got, ref, cu, [n for n in range(len(lens)) if lens[n] > 0], hq, hkv)
+
+
 @pytest.mark.parametrize("mode", MODES)
 def test_thd_varlen_causal_h16_d128_sampled(mode):
     w, x = workload_inputs("thd_varlen_causal_h16_d128")
@@ -243,6 +273,43 @@ def test_sparse_empty_lists_and_scattered_sentinels(deterministic):
     for t in (5, 33, 69):
         assert torch.isneginf(got["lse"][t]).all()
         assert (got["o"][t] == 0).all() and (got["dq"][t] == 0).all()
+
+
+def _random_sparse_cases(n=4, seed=2030):
+    """Seeded top-k problems: 1-300 tokens, heads in {16, 32, 64, 128}, top-k 1-300."""
+    g = torch.Generator().manual_seed(seed)
+    r = lambda lo, hi: int(torch.randint(lo, hi + 1, (1,), generator=g))
+    return [(r(1, 300), (16, 32, 64, 128)[r(0, 3)], r(1, 300), r(0, 10 ** 6)) for _ in range(n)]
+
+
+def _random_index_lists(T, K, seed):
+    """int32 [T, K]: each token names min(K, T) distinct rows drawn from all T
+    (not only a causal window), drops about a fifth of them to -1, and lists
+    its slots in random order."""
+    g = torch.Generator().manual_seed(seed)
+    idx = torch.full((T, K), -1, dtype=torch.int32)
+    n = min(K, T)
+    for t in range(T):
+        sel = torch.randperm(T, generator=g)[:n].to(torch.int32)
+        sel[torch.rand(n, generator=g) < 0.2] = -1
+        row = torch.full((K,), -1, dtype=torch.int32)
+        row[:n] = sel
+        idx[t] = row[torch.randperm(K, generator=g)]
+    return idx
+
+
+@pytest.mark.parametrize("deterministic", [False, True])
+@pytest.mark.parametrize("T,H,K,seed", _random_sparse_cases())
+def test_sparse_random_shapes(deterministic, T, H, K, seed):
+    q, kv, do, _ = W.sparse_inputs(T, H, 1, seed=seed)
+    idx = _random_index_lists(T, K, seed)
+    scale = 576 ** -0.5
+    got = run_sparse(q, kv, idx, do, scale, deterministic)
+    ref = oracle.sparse_backward(q, kv, idx, do, scale)
+    assert_close("o", got["o"], ref["o"])
+    assert_lse("lse", got["lse"], ref["lse"])
+    assert_close("dq", got["dq"], ref["dq"])
+    assert_close("dkv", got["dkv"], ref["dkv"])
 
 
 def test_sparse_deterministic_topk2048_t8192_h64_sampled():

@@ -159,9 +159,13 @@ attn_status_t attn_bwd_postprocess(const attn_problem_t* p, attn_dq_mode_t mode,
  *     (dense) or capacity (THD); larger problems return ATTN_ERR_UNSUPPORTED and
  *     enqueue nothing.
  *   - Set-up: the first call on each device looks up the array's device address
- *     (with that device current) and caches it, so make that first call before
- *     any stream capture; later calls only read the cache.  Calls must be made
- *     with the device that owns `stream` current.
+ *     (with that device current) and caches it with the id of the current
+ *     context, so make that first call before any stream capture; later calls
+ *     only read the cache.  After a device reset (a new primary context) the
+ *     next call looks the address up again, which also must not happen under
+ *     capture.  Calls must be made with the device that owns `stream` current.
+ *   - Validation: the problem is checked exactly as attn_bwd checks it before any
+ *     scratch size is computed; invalid problems return that status.
  *   - Sharing: every call uses the same array and leaves its contents behind; the
  *     call clears what must start at zero itself.  Calls whose work overlaps on
  *     the GPU (for example on two streams) race on the array and give wrong

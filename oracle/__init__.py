@@ -9,5 +9,5 @@ logsumexp), closed forms, identities and brute-force masks.
 from .attention import (  # noqa: F401
     causal_mask, full_mask, head_forward, head_backward, dense_forward, dense_backward,
     thd_backward, sparse_token, sparse_forward, sparse_backward, sparse_dkv_rows,
-    sparse_valid, flops_dense,
+    sparse_valid,
 )

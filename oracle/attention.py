@@ -40,8 +40,6 @@ dKV[:, :576] collects scale * ds^T q and dKV[:, :512] additionally p^T do.
 """
 from __future__ import annotations
 
-import math
-
 import torch
 
 F64 = torch.float64
@@ -258,9 +256,10 @@ def sparse_backward(q, kv, idx, do, scale, dv_dims=512):
     return dict(o=o, lse=lse, delta=delta, dq=dq, dkv=dkv)
 
 
-def sparse_dkv_rows(q, kv, idx, do, scale, rows):
+def sparse_dkv_rows(q, kv, idx, do, scale, rows, dv_dims=512):
     """dKV for a few key rows only: sums the contributions of every token whose
-    index list holds the row (exact, independent of the other rows)."""
+    index list holds the row (exact, independent of the other rows).  Equal to
+    ``sparse_backward(...)["dkv"][rows]``; a row that no token names is zero."""
     q, kv, do = _f64(q), _f64(kv), _f64(do)
     rows = [int(r) for r in rows]
     want = torch.tensor(rows, dtype=idx.dtype)
@@ -268,22 +267,10 @@ def sparse_dkv_rows(q, kv, idx, do, scale, rows):
     out = torch.zeros(len(rows), kv.shape[1], dtype=F64)
     tok = torch.nonzero(hit.any(dim=1)).flatten().tolist()
     for t in tok:
-        r = sparse_token(q[t], kv, idx[t], do[t], scale)
+        r = sparse_token(q[t], kv, idx[t], do[t], scale, dv_dims)
         sel = r["rows"].tolist()
         pos = {key: n for n, key in enumerate(sel)}
         for c, key in enumerate(rows):
             if key in pos:
                 out[c] += r["dkv_rows"][pos[key]]
     return out
-
-
-def flops_dense(batch, seqlen, heads_q, head_dim, causal):
-    """Algorithmic FLOPs: forward 4*B*H*S^2*D (x0.5 causal), backward 2.5x."""
-    f = 4.0 * batch * heads_q * seqlen * seqlen * head_dim * (0.5 if causal else 1.0)
-    return f, 2.5 * f
-
-
-def log_sum_exp_row(values):
-    """Reference row log-sum-exp of a plain Python list (used by pins)."""
-    m = max(values)
-    return m + math.log(sum(math.exp(x - m) for x in values))

@@ -174,7 +174,10 @@ def _problem(q, k, causal, scale, cu_seqlens, max_seqlen, error_word):
         p.cu_seqlens = cu_seqlens.data_ptr()
         p.num_seqs = cu_seqlens.numel() - 1
         if max_seqlen is None:
-            max_seqlen = int((cu_seqlens[1:] - cu_seqlens[:-1]).max().item()) if p.num_seqs > 0 else 0
+            # Deriving it from cu_seqlens would read device memory on the host: a
+            # hidden synchronisation, and a stale value under graph capture.
+            raise ValueError("THD calls need max_seqlen, an upper bound on every "
+                             "sequence length (the host never reads cu_seqlens)")
         p.max_seqlen = int(max_seqlen)
     p.causal = 1 if causal else 0
     p.scale = float(scale if scale is not None else 1.0 / math.sqrt(p.head_dim))

@@ -130,6 +130,10 @@ attn_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : A
 
 }  // namespace
 
+attn_status_t validate_dense_problem(const attn_problem_t* p, bool* empty) {
+  return check_problem(p, empty);
+}
+
 // Streaming multiprocessors of the current device (persistent grid size).
 int sm_count() {
   constexpr int kMaxDevices = 64;

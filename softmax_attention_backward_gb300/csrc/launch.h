@@ -4,9 +4,14 @@
 
 #include <cuda_runtime.h>
 
+#include "attn.h"
 #include "common.cuh"
 
 namespace attn {
+
+// The argument checks of every dense/THD entry point (status codes of attn.h);
+// sets *empty when there is nothing to compute.
+attn_status_t validate_dense_problem(const attn_problem_t* p, bool* empty);
 
 // Streaming multiprocessors of the current device (0 if it cannot be read).
 int sm_count();

@@ -299,21 +299,47 @@ def test_sparse_empty_index_list_and_slot_order():
     torch.testing.assert_close(r3["lse"], r["lse"], rtol=0, atol=1e-12)
 
 
-def test_sparse_dkv_rows_matches_full():
-    T, H, Dk, Dv, K = 30, 2, 8, 5, 7
-    q, kv, do = rnd(T, H, Dk, seed=42), rnd(T, Dk, seed=43), rnd(T, H, Dv, seed=44)
-    idx = workloads.topk_indices(T, K, seed=6)
-    full = oracle.sparse_backward(q, kv, idx, do, 0.5, dv_dims=Dv)["dkv"]
-    # sparse_dkv_rows uses the default 512 value dims; rebuild with the same dims
-    rows = [0, 7, 29]
-    part = torch.zeros(len(rows), Dk, dtype=F64)
+def test_sparse_token_and_valid_against_full():
+    """sparse_valid keeps exactly the slots >= 0 in list order; sparse_token's per-token
+    outputs equal the rows of the finite-difference-pinned sparse_backward, and its dkv
+    rows, scattered to their key rows, add up to the full dKV."""
+    T, H, Dk, Dv, K = 16, 2, 8, 5, 6
+    q, kv, do = rnd(T, H, Dk, seed=71), rnd(T, Dk, seed=72), rnd(T, H, Dv, seed=73)
+    idx = workloads.topk_indices(T, K, seed=11)
+    idx[9, 2] = -1
+    full = oracle.sparse_backward(q, kv, idx, do, 0.5, dv_dims=Dv)
+    acc = torch.zeros_like(full["dkv"])
     for t in range(T):
+        sel = oracle.sparse_valid(idx[t])
+        assert sel.tolist() == [int(x) for x in idx[t].tolist() if x >= 0]
         r = oracle.sparse_token(q[t], kv, idx[t], do[t], 0.5, Dv)
-        for c, key in enumerate(rows):
-            hit = (r["rows"] == key).nonzero()
-            if hit.numel():
-                part[c] += r["dkv_rows"][int(hit[0, 0])]
-    torch.testing.assert_close(part, full[rows], rtol=0, atol=1e-12)
+        assert torch.equal(r["rows"], sel)
+        for key in ("o", "lse", "dq", "delta"):
+            torch.testing.assert_close(r[key], full[key][t], rtol=0, atol=1e-13)
+        for n, row in enumerate(sel.tolist()):
+            acc[row] += r["dkv_rows"][n]
+    torch.testing.assert_close(acc, full["dkv"], rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("T,H,Dk,Dv,K,seed", [(30, 2, 8, 5, 7, 6), (24, 2, 576, 512, 32, 8)])
+def test_sparse_dkv_rows_matches_full(T, H, Dk, Dv, K, seed):
+    """sparse_dkv_rows against the finite-difference-pinned sparse_backward, on row
+    sets holding a row every token names (row 0 with K >= T), a row no token names
+    (every occurrence of row 3 replaced by a -1 sentinel mid-list), heavily and
+    lightly named rows, a repeated row and the last row."""
+    q, kv, do = rnd(T, H, Dk, seed=42 + seed), rnd(T, Dk, seed=43 + seed), rnd(T, H, Dv, seed=44 + seed)
+    idx = workloads.topk_indices(T, K, seed=seed)
+    idx[idx == 3] = -1
+    mid = (idx[:, :-1] == -1) & (idx[:, 1:] >= 0)
+    assert mid.any()                                # a -1 slot sits before a valid one
+    full = oracle.sparse_backward(q, kv, idx, do, 0.5, dv_dims=Dv)["dkv"]
+    if K >= T:
+        assert (idx[:, 0] == 0).all()               # row 0 is named by every token
+    for rows in ([0], [3], [0, 3, 7, T - 1], [T - 1, 1, 1, 2]):
+        part = oracle.sparse_dkv_rows(q, kv, idx, do, 0.5, rows, dv_dims=Dv)
+        torch.testing.assert_close(part, full[rows], rtol=0, atol=1e-12)
+    assert (oracle.sparse_dkv_rows(q, kv, idx, do, 0.5, [3], dv_dims=Dv) == 0).all()
+    assert full[0].abs().max() > 0
 
 
 # ----------------------------------------------------------------------------

@@ -4,6 +4,8 @@ Small cases are compared in full; the full-size workloads are compared on
 sampled independent units (a (batch, kv-head) group, a sequence, a token, a
 key row) that the oracle computes on their own, with the kernels launched at
 full size exactly as the benchmark launches them."""
+import functools
+
 import pytest
 import torch
 
@@ -133,7 +135,7 @@ def test_mha_causal_b8_h32_s1024_d64_sampled(mode):
 def test_gqa_causal_b4_h32x8_s4096_d128_sampled(mode):
     w, x = workload_inputs("gqa_causal_b4_h32x8_s4096_d128")
     got = run_dense(x["q"], x["k"], x["v"], x["do"], w.causal, w.scale, mode)
-    units = [(0, 0), (3, 7)]
+    units = [(0, 0), (1, 3), (2, 5), (3, 7)]
     ref = oracle.dense_backward(x["q"], x["k"], x["v"], x["do"], w.scale, w.causal, kv_heads=units)
     compare_dense(got, ref, units, w.heads_q, w.heads_kv)
 
@@ -204,9 +206,10 @@ def test_thd_varlen_causal_h16_d128_sampled(mode):
     w, x = workload_inputs("thd_varlen_causal_h16_d128")
     got = run_dense(x["q"], x["k"], x["v"], x["do"], w.causal, w.scale, mode, cu=x["cu_seqlens"],
                     max_seqlen=max(w.lengths))
+    seqs = [0, 1]                     # the longest (3670 rows) and the shortest (1053)
     ref = oracle.thd_backward(x["q"], x["k"], x["v"], x["do"], x["cu_seqlens"], w.scale, w.causal,
-                              seqs=[1])
-    compare_thd(got, ref, x["cu_seqlens"], [1], w.heads_q, w.heads_kv)
+                              seqs=seqs)
+    compare_thd(got, ref, x["cu_seqlens"], seqs, w.heads_q, w.heads_kv)
 
 
 # ----------------------------------------------------------------------------
@@ -312,6 +315,17 @@ def test_sparse_random_shapes(deterministic, T, H, K, seed):
     assert_close("dkv", got["dkv"], ref["dkv"])
 
 
+# Key rows compared at full size: rows below 2048 are named by every token after
+# them (row 0 by about 4900 tokens), the last rows by a few dozen or one.
+C5_ROWS = (0, 1, 1000, 2047, 4000, 4096, 8100, 8150, 8191)
+
+
+@functools.lru_cache(maxsize=1)
+def _c5_dkv_reference():
+    w, x = workload_inputs("sparse_topk2048_t8192_h64")
+    return oracle.sparse_dkv_rows(x["q"], x["kv"], x["idx"], x["do"], w.scale, C5_ROWS)
+
+
 def test_sparse_deterministic_topk2048_t8192_h64_sampled():
     w, x = workload_inputs("sparse_topk2048_t8192_h64")
     got = run_sparse(x["q"], x["kv"], x["idx"], x["do"], w.scale, deterministic=True)
@@ -319,9 +333,8 @@ def test_sparse_deterministic_topk2048_t8192_h64_sampled():
     for t in (0, 2048, 8191):
         r = oracle.sparse_token(q[t], kv, idx[t], do[t], w.scale)
         assert_close(f"dq[{t}]", got["dq"][t], r["dq"])
-    rows = [8191, 8150, 4000, 0]
-    ref = oracle.sparse_dkv_rows(x["q"], x["kv"], x["idx"], x["do"], w.scale, rows)
-    for c, j in enumerate(rows):
+    ref = _c5_dkv_reference()
+    for c, j in enumerate(C5_ROWS):
         assert_close(f"dkv[{j}]", got["dkv"][j], ref[c])
     gq, gkv, gidx, gdo = got["gpu"]
     _, dkv2 = A.sparse_attn_bwd_deterministic(gq, gkv, gidx, got["o"], gdo, got["lse"],
@@ -338,7 +351,6 @@ def test_sparse_topk2048_t8192_h64_sampled():
         assert_close(f"o[{t}]", got["o"][t], r["o"])
         assert_lse(f"lse[{t}]", got["lse"][t], r["lse"])
         assert_close(f"dq[{t}]", got["dq"][t], r["dq"])
-    rows = [8191, 8150, 8100]
-    ref = oracle.sparse_dkv_rows(x["q"], x["kv"], x["idx"], x["do"], w.scale, rows)
-    for c, j in enumerate(rows):
+    ref = _c5_dkv_reference()
+    for c, j in enumerate(C5_ROWS):
         assert_close(f"dkv[{j}]", got["dkv"][j], ref[c])

@@ -2,11 +2,16 @@
 """Benchmark of the attention training step (forward + backward) on GB300.
 
 One step = attn_fwd + attn_bwd_preprocess + attn_bwd + attn_bwd_postprocess over
-the dense causal MHA workload B=8, H=32, S=1024, D=64 (bf16, synthetic N(0,1)
-inputs).  Prints one JSON line.  `--impl reference` times the fp64 CPU oracle on
-the same workload instead (bounded samples on the host cores).
+the largest dense workload, causal GQA B=4, Hq=32, Hkv=8, S=4096, D=128 (bf16,
+synthetic N(0,1) inputs); the headline value is its fwd+bwd TFLOP/s.  The same
+line carries, under extra keys, the causal MHA B=8 H=32 S=1024 D=64 and the THD
+varlen H=16 D=128 workloads (each timed the same way, with its own roofline), the
+top-k sparse workload, and the CPU oracle's rate.  Prints one JSON line.
+`--impl reference` times the fp64 CPU oracle on the headline workload instead
+(one query head per step, on the host cores).
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+           [--workload NAME] [--no-extras] [--no-sparse] [--no-split]
 For N > 1 launch with torchrun; every rank runs the full workload (weak scaling).
 """
 from __future__ import annotations
@@ -14,7 +19,6 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
-import math
 import os
 import re
 import statistics
@@ -31,7 +35,8 @@ sys.path.insert(0, ROOT)
 from softmax_attention_backward_gb300 import workloads as W  # noqa: E402
 
 METRIC = "attention fwd+bwd TFLOP/s (bf16, 1 GB300) and % of dense BF16 tensor peak"
-DEFAULT_WORKLOAD = "mha_causal_b8_h32_s1024_d64"
+DEFAULT_WORKLOAD = "gqa_causal_b4_h32x8_s4096_d128"
+EXTRA_DENSE = ("mha_causal_b8_h32_s1024_d64", "thd_varlen_causal_h16_d128")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_FLUSH_BYTES = 256 << 20
 
@@ -168,30 +173,37 @@ def barrier(world):
 # oracle (CPU) leg
 # ----------------------------------------------------------------------------
 def oracle_units(w):
-    """Independent units of a workload for the oracle: (batch, kv-head) groups of
-    a dense problem, sequences of a THD problem; with their FLOPs (fwd+bwd)."""
+    """Independent samples of a workload for the oracle, with their FLOPs
+    (fwd+bwd): one query head of one batch entry (its O, LSE, dQ and its share of
+    dK/dV) for a dense problem, one sequence of a THD problem."""
+    causal = 0.5 if w.causal else 1.0
     if w.kind == "thd":
-        per = [3.5 * 4.0 * w.heads_q * w.head_dim * L * L * (0.5 if w.causal else 1.0)
-               for L in w.lengths]
+        per = [3.5 * 4.0 * w.heads_q * w.head_dim * L * L * causal for L in w.lengths]
         return [(n, per[n]) for n in range(len(w.lengths))]
-    f_fwd, f_bwd = dense_flops(w)
-    per = (f_fwd + f_bwd) / (w.batch * w.heads_kv)
-    return [((b, g), per) for b in range(w.batch) for g in range(w.heads_kv)]
+    per = 3.5 * 4.0 * w.seqlen * w.seqlen * w.head_dim * causal
+    return [((b, h), per) for b in range(w.batch) for h in range(w.heads_q)]
 
 
-def oracle_unit_rate(w, x, budget_s):
-    """Times the fp64 oracle over independent units until `budget_s` is spent.
-    Returns (TFLOP/s, units done, seconds)."""
+def oracle_unit_rate(w, x, budget_s, start=0):
+    """Times the fp64 oracle over independent samples until `budget_s` is spent
+    (at least one).  Returns (TFLOP/s, samples done, seconds)."""
     import oracle
     units = oracle_units(w)
+    if w.kind != "thd":
+        q, k, v, do = (x[n].double() for n in ("q", "k", "v", "do"))
+        mask = oracle.causal_mask(w.seqlen, w.seqlen) if w.causal else \
+            oracle.full_mask(w.seqlen, w.seqlen)
+        grp = w.heads_q // w.heads_kv
     done, flops, t0 = 0, 0.0, time.perf_counter()
     while True:
-        u, f = units[done % len(units)]
+        u, f = units[(start + done) % len(units)]
         if w.kind == "thd":
             oracle.thd_backward(x["q"], x["k"], x["v"], x["do"], x["cu_seqlens"], w.scale, w.causal,
                                 seqs=[u])
         else:
-            oracle.dense_backward(x["q"], x["k"], x["v"], x["do"], w.scale, w.causal, kv_heads=[u])
+            b, h = u
+            oracle.head_backward(q[b, :, h], k[b, :, h // grp], v[b, :, h // grp], do[b, :, h],
+                                 w.scale, mask)
         done += 1
         flops += f
         el = time.perf_counter() - t0
@@ -206,23 +218,24 @@ def run_reference(args, w, world, rank):
     torch.set_num_threads(len(os.sched_getaffinity(0)))
     x = W.make_inputs(w)
     cores = torch.get_num_threads()
-    for _ in range(args.warmup):
-        oracle_unit_rate(w, x, 0.0)
+    for i in range(args.warmup):
+        oracle_unit_rate(w, x, 0.0, start=i)
     times, units, flops = [], 0, 0.0
-    for _ in range(args.steps):
-        rate, n, el = oracle_unit_rate(w, x, 0.0)
+    for i in range(args.steps):
+        rate, n, el = oracle_unit_rate(w, x, 0.0, start=args.warmup + i)
         times.append(el)
         units += n
         flops += rate * el * 1e12
     total = sum(times)
     value = flops / total / 1e12
-    sample = f"{units} independent units of {w.name}, one per step, fp64 oracle"
+    what = "sequence" if w.kind == "thd" else "query head (one batch entry)"
+    sample = f"{units} samples of {w.name}, one {what} per step, fp64 oracle fwd+bwd"
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": config_of(w, "oracle", world),
+        "config": config_of(w, world),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -230,23 +243,53 @@ def run_reference(args, w, world, rank):
     print(json.dumps(line), flush=True)
 
 
-def config_of(w, mode, world):
+def config_of(w, world):
     c = {"workload": w.name, "batch": w.batch, "seqlen": w.seqlen, "heads_q": w.heads_q,
          **({"lengths": w.lengths, "capacity": w.capacity} if w.kind == "thd" else {}),
-         "heads_kv": w.heads_kv, "head_dim": w.head_dim, "causal": w.causal, "dq_mode": mode,
+         "heads_kv": w.heads_kv, "head_dim": w.head_dim, "causal": w.causal, "dq_mode": "atomic",
          "l2": "flushed between timed steps (256 MiB write)",
          "parallelism": "replicas" if world == 1 else f"replicas x{world}"}
     return c
 
 
+def cpu_baseline(w, seconds):
+    torch.set_num_threads(len(os.sched_getaffinity(0)))
+    x = W.make_inputs(w)
+    rate, units, el = oracle_unit_rate(w, x, seconds)
+    what = "sequences" if w.kind == "thd" else "query heads"
+    return {"value": rate, "unit": "TFLOP/s", "cores": torch.get_num_threads(), "kind": "oracle",
+            "sample": f"{units} {what} of {w.name} (fwd+bwd, fp64) in {el:.1f} s"}
+
+
 # ----------------------------------------------------------------------------
-# our leg
+# our leg: one dense workload
 # ----------------------------------------------------------------------------
-def run_ours(args, w, world, rank, local):
+def tflops(flops, ms):
+    return flops / (ms * 1e-3) / 1e12
+
+
+def dense_pass_bytes(w):
+    """Algorithmic bytes of the two memory-bound passes (atomic dQ mode).
+    Preprocess: reads O and dO, writes Delta and clears the fp32 accumulator row,
+    for every valid row-head.  Postprocess: reads the accumulator and writes bf16
+    dQ for every valid row-head, and writes the exact zeros of THD padding rows of
+    dQ, dK and dV."""
+    D = w.head_dim
+    if w.kind == "thd":
+        valid = sum(w.lengths)
+        pad = w.capacity - valid
+    else:
+        valid, pad = w.batch * w.seqlen, 0
+    rh = valid * w.heads_q
+    pre = rh * (2 * D * 2 + 4 + 4 * D)
+    post = rh * (4 * D + 2 * D) + pad * (w.heads_q + 2 * w.heads_kv) * D * 2
+    return pre, post
+
+
+def bench_dense(args, w, dev, flush, world, rank, sampler=None, e2e=False):
+    """Times K steps of fwd + preprocess + bwd + postprocess (atomic dQ; then split
+    dQ unless --no-split) and returns the per-workload block of the JSON line."""
     import softmax_attention_backward_gb300 as A
-    dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
-    A.lib()
     x = W.make_inputs(w)
     q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "do"))
     o = torch.empty_like(q)
@@ -256,7 +299,6 @@ def run_ours(args, w, world, rank, local):
         lse = torch.empty(w.batch, w.heads_q, w.seqlen, dtype=torch.float32, device=dev)
     delta = torch.empty_like(lse)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     kw = dict(causal=w.causal, scale=w.scale)
     if w.kind == "thd":
         kw.update(cu_seqlens=x["cu_seqlens"].to(dev), max_seqlen=max(w.lengths))
@@ -284,51 +326,96 @@ def run_ours(args, w, world, rank, local):
         if ev:
             ev[4].record(stream)
 
-    def timed(mode, steps, sampler=None):
+    def timed(mode, steps, smp=None):
         evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(steps)]
         barrier(world)
         torch.cuda.synchronize()
-        if sampler:
-            sampler.mark_start()
+        if smp:
+            smp.mark_start()
         for i in range(steps):
             flush.zero_()
             step(mode, evs[i])
         torch.cuda.synchronize()
-        if sampler:
-            sampler.mark_end()
+        if smp:
+            smp.mark_end()
         barrier(world)
-        tot = [e[0].elapsed_time(e[4]) for e in evs]
-        fwd = [e[0].elapsed_time(e[1]) for e in evs]
-        bwd = [e[1].elapsed_time(e[4]) for e in evs]
-        main = [e[2].elapsed_time(e[3]) for e in evs]
-        pre = [e[1].elapsed_time(e[2]) for e in evs]
-        post = [e[3].elapsed_time(e[4]) for e in evs]
-        return {k_: sum(v_) / steps for k_, v_ in
-                (("total", tot), ("fwd", fwd), ("bwd", bwd), ("bwd_main", main), ("pre", pre),
-                 ("post", post))}
+        r = {}
+        for key, a, b in (("total", 0, 4), ("fwd", 0, 1), ("bwd", 1, 4), ("pre", 1, 2),
+                          ("main", 2, 3), ("post", 3, 4)):
+            r[key] = reduce_max(sum(e[a].elapsed_time(e[b]) for e in evs) / steps, world)
+        return r
 
-    # warm-up (both modes), then the timed atomic-mode steps with clocks sampled
     for _ in range(args.warmup):
         for mode in modes:
             step(mode)
     torch.cuda.synchronize()
-    sampler = ClockSampler(f"GPU-{torch.cuda.get_device_properties(dev).uuid}") if rank == 0 else None
-    t_atomic = timed(A.ATTN_DQ_ATOMIC, args.steps, sampler)
-    clocks = sampler.stop() if sampler else None
-    t_split = None if args.no_split else timed(A.ATTN_DQ_SPLIT, args.steps)
+    t_at = timed(A.ATTN_DQ_ATOMIC, args.steps, sampler)
+    t_sp = None if args.no_split else timed(A.ATTN_DQ_SPLIT, args.steps)
+    del ws
+    ws_split_bytes = 0 if args.no_split else A.attn_bwd_workspace_size(
+        q, k, mode=A.ATTN_DQ_SPLIT, **kw)
 
-    ms = reduce_max(t_atomic["total"], world)
-    ms_main = reduce_max(t_atomic["bwd_main"], world)
-    ms_fwd = reduce_max(t_atomic["fwd"], world)
-    ms_bwd = reduce_max(t_atomic["bwd"], world)
-    ms_split = reduce_max(t_split["total"], world) if t_split else None
-    ms_split_bwd = reduce_max(t_split["bwd"], world) if t_split else None
+    pk, pk_kind = peaks()
+    peak, hbm = pk["bf16_tflops"], pk["hbm_gbs"]
+    pre_b, post_b = dense_pass_bytes(w)
+    src = "softmax_attention_backward_gb300/csrc/"
+    D = w.head_dim
+    blk = {
+        "workload": w.name,
+        "fwd_bwd_tflops": tflops(f_fwd + f_bwd, t_at["total"]),
+        "pct_of_peak": 100.0 * tflops(f_fwd + f_bwd, t_at["total"]) / peak,
+        "fwd_tflops": tflops(f_fwd, t_at["fwd"]), "bwd_tflops": tflops(f_bwd, t_at["bwd"]),
+        "ms_per_step": t_at["total"],
+        "ms_breakdown": {"fwd": t_at["fwd"], "bwd_preprocess": t_at["pre"],
+                         "bwd_main": t_at["main"], "bwd_postprocess": t_at["post"]},
+        "flops": {"fwd": f_fwd, "bwd": f_bwd},
+        "split": None if t_sp is None else {
+            "fwd_bwd_tflops": tflops(f_fwd + f_bwd, t_sp["total"]),
+            "bwd_tflops": tflops(f_bwd, t_sp["bwd"]), "ms_per_step": t_sp["total"],
+            "ms_breakdown": {"fwd": t_sp["fwd"], "bwd_preprocess": t_sp["pre"],
+                             "bwd_main": t_sp["main"], "bwd_postprocess": t_sp["post"]},
+            "workspace_bytes": ws_split_bytes},
+        "roofline": {"kernel": f"attn_bwd_kernel<{D}>", "bound": "tensor",
+                     "achieved": tflops(f_bwd, t_at["main"]), "peak": peak, "unit": "TFLOP/s",
+                     "frac": tflops(f_bwd, t_at["main"]) / peak,
+                     "peak_kind": f"{pk_kind} bf16 burst",
+                     "traffic": profiled_traffic("attn_bwd_kernel", w.name, src + "attn_bwd.cu"),
+                     "flops_per_launch": f_bwd},
+        "fwd_roofline": {"kernel": f"attn_fwd_kernel<{D}>", "bound": "tensor",
+                         "achieved": tflops(f_fwd, t_at["fwd"]), "peak": peak, "unit": "TFLOP/s",
+                         "frac": tflops(f_fwd, t_at["fwd"]) / peak,
+                         "peak_kind": f"{pk_kind} bf16 burst",
+                         "traffic": profiled_traffic("attn_fwd_kernel", w.name,
+                                                     src + "attn_fwd.cu"),
+                         "flops_per_launch": f_fwd},
+        "hbm_passes": {
+            name: {"kernel": kern, "bound": "hbm", "us": 1e3 * ms, "bytes": b,
+                   "achieved": b / ms / 1e6, "peak": hbm, "unit": "GB/s",
+                   "frac": b / ms / 1e6 / hbm, "peak_kind": f"{pk_kind} copy",
+                   "traffic": profiled_traffic(kern, w.name, src + "attn_bwd_aux.cu")}
+            for name, kern, ms, b in (
+                ("bwd_preprocess", "attn_bwd_preprocess_kernel", t_at["pre"], pre_b),
+                ("bwd_postprocess", "attn_dq_finalize_kernel", t_at["post"], post_b))},
+        "launches_per_step": 5 if w.kind == "thd" else 4,
+    }
+    if not e2e:
+        return blk
+    blk["e2e"] = bench_e2e(args, A, dev, x, (q, k, v, do), (o, lse, delta, dq, dk, dv), kw,
+                           f_fwd + f_bwd, world)
+    return blk
 
-    # end to end through the public API: pinned host inputs -> device -> results
-    # -> host, every step.  Three streams overlap step i's compute with the
-    # host->device copy of step i+1's inputs and the device->host copy of step
-    # i-1's gradients (inputs and gradients double-buffered on the device and
-    # on the host).
+
+def bench_e2e(args, A, dev, x, ins, outs, kw, flops, world):
+    """End to end through the public API: pinned host inputs -> device -> results
+    -> host, every step.  Three streams overlap step i's compute with the
+    host->device copy of step i+1's inputs and the device->host copy of step
+    i-1's gradients (inputs and gradients double-buffered on the device and on
+    the host)."""
+    q, k, v, do = ins
+    o, lse, delta, dq, dk, dv = outs
+    stream = torch.cuda.current_stream()
+    ws = torch.empty(A.attn_bwd_workspace_size(q, k, mode=A.ATTN_DQ_ATOMIC, **kw),
+                     dtype=torch.uint8, device=dev)
     hin = [[x[n].pin_memory() for n in ("q", "k", "v", "do")]]
     hin.append([t.clone().pin_memory() for t in hin[0]])
     dins = [[q, k, v, do], [torch.empty_like(t) for t in (q, k, v, do)]]
@@ -338,11 +425,8 @@ def run_ours(args, w, world, rank, local):
     h2d = sum(t.numel() * t.element_size() for t in hin[0])
     d2h = sum(t.numel() * t.element_size() for t in hout[0])
     s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-    ev = lambda: torch.cuda.Event()
-    in_ready = [ev(), ev()]
-    in_free = [ev(), ev()]
-    out_ready = [ev(), ev()]
-    out_free = [ev(), ev()]
+    ev = torch.cuda.Event
+    in_ready, in_free, out_ready, out_free = ([ev(), ev()] for _ in range(4))
     for e_ in in_free + out_free:
         e_.record(stream)
 
@@ -358,12 +442,12 @@ def run_ours(args, w, world, rank, local):
         stream.wait_event(in_ready[b])
         stream.wait_event(out_free[b])
         A.attn_fwd(qi, ki, vi, out=o, lse=lse, stream=stream, **kw)
-        A.attn_bwd_preprocess(qi, ki, o, doi, mode=A.ATTN_DQ_ATOMIC, workspace=ws[A.ATTN_DQ_ATOMIC],
-                              delta=delta, stream=stream, **kw)
-        A.attn_bwd(qi, ki, vi, doi, lse, delta, mode=A.ATTN_DQ_ATOMIC,
-                   workspace=ws[A.ATTN_DQ_ATOMIC], dk=dki, dv=dvi, stream=stream, **kw)
-        A.attn_bwd_postprocess(qi, ki, dki, dvi, mode=A.ATTN_DQ_ATOMIC,
-                               workspace=ws[A.ATTN_DQ_ATOMIC], dq=dqi, stream=stream, **kw)
+        A.attn_bwd_preprocess(qi, ki, o, doi, mode=A.ATTN_DQ_ATOMIC, workspace=ws, delta=delta,
+                              stream=stream, **kw)
+        A.attn_bwd(qi, ki, vi, doi, lse, delta, mode=A.ATTN_DQ_ATOMIC, workspace=ws, dk=dki,
+                   dv=dvi, stream=stream, **kw)
+        A.attn_bwd_postprocess(qi, ki, dki, dvi, mode=A.ATTN_DQ_ATOMIC, workspace=ws, dq=dqi,
+                               stream=stream, **kw)
         in_free[b].record(stream)
         out_ready[b].record(stream)
         with torch.cuda.stream(s_out):
@@ -389,48 +473,59 @@ def run_ours(args, w, world, rank, local):
     # the last step's gradients must have reached the host intact
     for h_, d_ in zip(hout[(args.steps - 1) & 1], douts[(args.steps - 1) & 1]):
         assert torch.equal(h_, d_.cpu())
+    return {"value": world * tflops(flops, ms_e2e), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e,
+            "overlap": "h2d(i+1) | compute(i) | d2h(i-1) on three streams"}
+
+
+def run_ours(args, w, world, rank, local):
+    import softmax_attention_backward_gb300 as A
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    A.lib()
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    sampler = ClockSampler(f"GPU-{torch.cuda.get_device_properties(dev).uuid}") if rank == 0 else None
+    head = bench_dense(args, w, dev, flush, world, rank, sampler=sampler, e2e=True)
+    clocks = sampler.stop() if sampler else None
+    torch.cuda.empty_cache()
 
     extra = {}
-    if rank == 0 and not args.no_sparse:
-        extra["sparse"] = bench_sparse(args, dev, flush)
+    if not args.no_extras:
+        configs = {}
+        for name in EXTRA_DENSE:
+            if name != w.name:
+                configs[name] = bench_dense(args, W.get_workload(name), dev, flush, world, rank)
+                torch.cuda.empty_cache()
+        extra["configs"] = configs
+        if rank == 0 and not args.no_sparse:
+            extra["sparse"] = bench_sparse(args, dev, flush)
+            torch.cuda.empty_cache()
 
     if rank != 0:
         return
-    pk, pk_kind = peaks()
-    tflops = lambda flops, ms_: flops / (ms_ * 1e-3) / 1e12
-    value = world * tflops(f_fwd + f_bwd, ms)
-    peak = pk["bf16_tflops"]
-    achieved = tflops(f_bwd, ms_main)
-    traffic = profiled_traffic("attn_bwd_kernel", w.name,
-                               "softmax_attention_backward_gb300/csrc/attn_bwd.cu")
-    cpu = cpu_baseline(w, args.cpu_seconds)
     line = {
-        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": config_of(w, "atomic", world),
-        "pct_of_peak": 100.0 * tflops(f_fwd + f_bwd, ms) / peak,
-        "fwd_tflops": tflops(f_fwd, ms_fwd), "bwd_tflops": tflops(f_bwd, ms_bwd),
-        "ms_breakdown": {"fwd": ms_fwd, "bwd_preprocess": reduce_max(t_atomic["pre"], world),
-                         "bwd_main": ms_main, "bwd_postprocess": reduce_max(t_atomic["post"], world)},
-        "split": None if ms_split is None else {
-            "fwd_bwd_tflops": tflops(f_fwd + f_bwd, ms_split),
-            "bwd_tflops": tflops(f_bwd, ms_split_bwd), "ms_per_step": ms_split},
-        "roofline": {"kernel": "attn_bwd_kernel", "bound": "tensor", "achieved": achieved,
-                     "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-                     "peak_kind": f"{pk_kind} bf16 burst",
-                     "traffic": traffic, "flops_per_launch": f_bwd},
-        "cpu_baseline": cpu,
+        "metric": METRIC, "value": world * head["fwd_bwd_tflops"], "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": head["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": config_of(w, world),
+        "pct_of_peak": head["pct_of_peak"],
+        "fwd_tflops": head["fwd_tflops"], "bwd_tflops": head["bwd_tflops"],
+        "ms_breakdown": head["ms_breakdown"], "split": head["split"],
+        "roofline": head["roofline"], "fwd_roofline": head["fwd_roofline"],
+        "hbm_passes": head["hbm_passes"],
+        "cpu_baseline": cpu_baseline(w, args.cpu_seconds) if args.cpu_seconds > 0 else None,
         "clocks": clocks,
-        "e2e": {"value": world * tflops(f_fwd + f_bwd, ms_e2e), "unit": "TFLOP/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e,
-                "overlap": "h2d(i+1) | compute(i) | d2h(i-1) on three streams"},
-        "gpu_launches": (5 if w.kind == "thd" else 4) * args.steps,
+        "e2e": head["e2e"],
+        "gpu_launches": head["launches_per_step"] * args.steps,
         **extra,
     }
     print(json.dumps(line), flush=True)
 
 
+# ----------------------------------------------------------------------------
+# top-k sparse workload
+# ----------------------------------------------------------------------------
 def sparse_logical_bytes(T, H, idx):
     """Logical bytes of the sparse path: gathered KV rows (576 bf16 once per
     token and selected key), Q, O, idx; backward adds dO, dQ and 576 fp32
@@ -470,8 +565,8 @@ def bench_sparse(args, dev, flush):
         torch.cuda.synchronize()
         f_ms.append(e[0].elapsed_time(e[1]))
         b_ms.append(e[1].elapsed_time(e[2]))
-    # ordered (deterministic) dKV: same inputs, its own workspace (fp32 rows per
-    # (token, slot)); bitwise repeat checked on the last two runs
+    # ordered (deterministic) dKV: same inputs, its own workspace; bitwise repeat
+    # checked on the last two runs
     del ws
     wsd = torch.empty(A.sparse_attn_bwd_deterministic_workspace_size(q, idx), dtype=torch.uint8,
                       device=dev)
@@ -490,37 +585,41 @@ def bench_sparse(args, dev, flush):
         if i == 1 + steps - 1:
             dkv_prev.copy_(dkv)
     repeat_equal = bool(torch.equal(dkv_prev, dkv))
+    ws_det = wsd.numel()
     del wsd
     fb, bb, pairs = sparse_logical_bytes(w.seqlen, w.heads_q, x["idx"])
     fm, bm = sum(f_ms) / steps, sum(b_ms) / steps
     dm = sum(d_ms) / len(d_ms)
-    hbm = peaks()[0]["hbm_gbs"]
+    pk, pk_kind = peaks()
+    hbm = pk["hbm_gbs"]
     flops_f = pairs * w.heads_q * 2 * (576 + 512)
     flops_b = pairs * w.heads_q * 2 * (3 * 576 + 2 * 512)
+    src = "softmax_attention_backward_gb300/csrc/"
     return {"workload": w.name, "steps": steps, "fwd_ms": fm, "bwd_ms": bm,
             "fwd_logical_gbs": fb / fm / 1e6, "bwd_logical_gbs": bb / bm / 1e6,
             "fwd_frac_hbm": fb / fm / 1e6 / hbm, "bwd_frac_hbm": bb / bm / 1e6 / hbm,
             "fwd_tflops": flops_f / fm / 1e9, "bwd_tflops": flops_b / bm / 1e9,
+            "roofline": {"kernel": "sparse_bwd_tc_kernel (+ preprocess, cast)", "bound": "hbm",
+                         "achieved": bb / bm / 1e6, "peak": hbm, "unit": "GB/s",
+                         "frac": bb / bm / 1e6 / hbm, "peak_kind": f"{pk_kind} copy",
+                         "bytes": "logical (gathered KV rows once per token, fp32 dKV adds)",
+                         "traffic": profiled_traffic("sparse_bwd_tc_kernel", w.name,
+                                                     src + "sparse_bwd_tc.cu")},
             "bwd_deterministic_ms": dm, "bwd_deterministic_bitwise_repeat": repeat_equal,
+            "bwd_deterministic_workspace_bytes": ws_det,
             "valid_pairs": pairs}
-
-
-def cpu_baseline(w, seconds):
-    torch.set_num_threads(len(os.sched_getaffinity(0)))
-    x = W.make_inputs(w)
-    rate, units, el = oracle_unit_rate(w, x, seconds)
-    return {"value": rate, "unit": "TFLOP/s", "cores": torch.get_num_threads(), "kind": "oracle",
-            "sample": f"{units} independent units of {w.name} (fwd+bwd, fp64) in {el:.1f} s"}
 
 
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
-    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-extras", action="store_true",
+                    help="time only --workload (no other dense workloads, no sparse)")
     ap.add_argument("--no-sparse", action="store_true")
     ap.add_argument("--no-split", action="store_true", help="time only the atomic dQ mode")
     args = ap.parse_args()

@@ -500,6 +500,9 @@ def run_ours(args, w, world, rank, local):
         if rank == 0 and not args.no_sparse:
             extra["sparse"] = bench_sparse(args, dev, flush)
             torch.cuda.empty_cache()
+        if rank == 0:
+            extra["csa_compressor"] = bench_csa(args, dev, flush)
+            torch.cuda.empty_cache()
 
     if rank != 0:
         return
@@ -608,6 +611,97 @@ def bench_sparse(args, dev, flush):
             "bwd_deterministic_ms": dm, "bwd_deterministic_bitwise_repeat": repeat_equal,
             "bwd_deterministic_workspace_bytes": ws_det,
             "valid_pairs": pairs}
+
+
+# ----------------------------------------------------------------------------
+# CSA compressor gated pooling (HBM-bound)
+# ----------------------------------------------------------------------------
+# Kernel times the compressor page reports on one B200 (nsys kernel sums, after
+# its forward vectorization and backward zero-write commits; the backward
+# includes its dAPE zero fill).  Context only: other hardware.
+CSA_PAGE_B200_US = {"csa_1x8192_d128": (4.5, 12.8), "csa_3x8192_d128": (10.0, 22.2),
+                    "csa_1x8192_d512": (12.4, 22.8), "csa_3x8192_d512": (35.0, 66.0)}
+
+
+def csa_bytes(x, ratio, coff):
+    """Algorithmic bytes: the forward reads kv and score at every (token, column)
+    some window reads, ape, and writes out; the backward reads the same plus
+    dout and writes every dkv / dscore position and dape."""
+    D = x["kv"].shape[1] // coff
+    cu, cc = x["cu_seqlens"].tolist(), x["cu_seqlens_comp"].tolist()
+    used = 0
+    for n in range(len(cu) - 1):
+        nb = cc[n + 1] - cc[n]
+        used += nb * ratio * D if coff == 1 else max(0, 2 * nb - 1) * ratio * D
+    ape = x["ape"].numel() * 4
+    out = x["comp_capacity"] * D * 2
+    fwd = used * 4 + ape + out
+    bwd = used * 4 + ape + out + x["kv"].numel() * 2 * 2 + ape
+    return fwd, bwd
+
+
+def bench_csa(args, dev, flush):
+    import softmax_attention_backward_gb300 as A
+    stream = torch.cuda.current_stream()
+    hbm = peaks()[0]["hbm_gbs"]
+    pk_kind = peaks()[1]
+    res = {}
+    iters = max(5, min(args.steps, 20))
+    for name, c in W.CSA_WORKLOADS.items():
+        x = W.csa_inputs(c["lengths"], c["head_dim"], c["ratio"], c["coff"], c["seed"])
+        g = {k: (v.to(dev) if torch.is_tensor(v) else v) for k, v in x.items()}
+        kw = dict(ratio=c["ratio"], coff=c["coff"])
+        out = torch.empty(x["comp_capacity"], c["head_dim"], dtype=torch.bfloat16, device=dev)
+        dkv, dsc, dape = torch.empty_like(g["kv"]), torch.empty_like(g["score"]), \
+            torch.empty_like(g["ape"])
+        ws = torch.empty(A.csa_compressor_bwd_workspace_size(
+            g["kv"], g["cu_seqlens"], g["cu_seqlens_comp"], comp_capacity=x["comp_capacity"],
+            **kw), dtype=torch.uint8, device=dev)
+
+        def fwd():
+            A.csa_compressor_fwd(g["kv"], g["score"], g["ape"], g["cu_seqlens"],
+                                 g["cu_seqlens_comp"], comp_capacity=x["comp_capacity"], out=out,
+                                 **kw)
+
+        def bwd():
+            A.csa_compressor_bwd(g["kv"], g["score"], g["ape"], g["dout"], g["cu_seqlens"],
+                                 g["cu_seqlens_comp"], workspace=ws, dkv=dkv, dscore=dsc,
+                                 dape=dape, **kw)
+
+        times = {}
+        for key, fn in (("fwd", fwd), ("bwd", bwd)):
+            for _ in range(3):
+                fn()
+            ms = []
+            for _ in range(iters):
+                flush.zero_()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                fn()
+                e1.record(stream)
+                torch.cuda.synchronize()
+                ms.append(e0.elapsed_time(e1))
+            times[key] = statistics.median(ms)
+        fb, bb = csa_bytes(x, c["ratio"], c["coff"])
+        page = CSA_PAGE_B200_US[name]
+        res[name] = {
+            "fwd_us": 1e3 * times["fwd"], "bwd_us": 1e3 * times["bwd"],
+            "fwd_gbs": fb / times["fwd"] / 1e6, "bwd_gbs": bb / times["bwd"] / 1e6,
+            "fwd_frac_hbm": fb / times["fwd"] / 1e6 / hbm,
+            "bwd_frac_hbm": bb / times["bwd"] / 1e6 / hbm,
+            "bytes": {"fwd": fb, "bwd": bb},
+            "page_b200_us": {"fwd": page[0], "bwd": page[1]},
+        }
+    return {"ratio": 4, "coff": 2, "iters": iters, "timing": "median, L2 flushed before each launch",
+            "peak": hbm, "peak_kind": f"{pk_kind} copy", "launches_per_bwd": 2,
+            "roofline": {"kernel": "csa_bwd_kernel<4,2> (+ dape reduce) at csa_3x8192_d512",
+                         "bound": "hbm", "achieved": res["csa_3x8192_d512"]["bwd_gbs"],
+                         "peak": hbm, "unit": "GB/s",
+                         "frac": res["csa_3x8192_d512"]["bwd_frac_hbm"],
+                         "traffic": profiled_traffic(
+                             "csa_bwd_kernel", "csa_3x8192_d512",
+                             "softmax_attention_backward_gb300/csrc/csa_compressor.cu")},
+            "shapes": res}
 
 
 def main():

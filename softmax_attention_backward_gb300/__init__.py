@@ -9,7 +9,8 @@ Entry points (same names as the C ABI):
   attn_fwd, attn_bwd_workspace_size, attn_bwd_preprocess, attn_bwd, attn_bwd_postprocess,
   sparse_attn_fwd, sparse_attn_bwd_workspace_size, sparse_attn_bwd,
   sparse_attn_bwd_deterministic_workspace_size, sparse_attn_bwd_deterministic,
-  attn_status_string, attn_version
+  attn_bwd_fixed_scratch, attn_status_string, attn_version   (include/attn.h)
+  csa_compressor_fwd, csa_compressor_bwd_workspace_size, csa_compressor_bwd  (include/dsa.h)
 """
 from __future__ import annotations
 
@@ -26,7 +27,8 @@ __all__ = [
     "sparse_attn_bwd", "sparse_attn_bwd_deterministic_workspace_size", "sparse_attn_bwd_deterministic",
     "attn_status_string", "attn_version", "dense_backward",
     "SPARSE_DIM_QK", "SPARSE_DIM_V", "EXPORTED_SYMBOLS", "attn_bwd_fixed_scratch",
-    "FIXED_SCRATCH_BYTES",
+    "FIXED_SCRATCH_BYTES", "csa_compressor_fwd", "csa_compressor_bwd_workspace_size",
+    "csa_compressor_bwd",
 ]
 
 ATTN_DQ_ATOMIC = 0
@@ -40,6 +42,7 @@ EXPORTED_SYMBOLS = (
     "sparse_attn_fwd", "sparse_attn_bwd_workspace_size", "sparse_attn_bwd",
     "sparse_attn_bwd_deterministic_workspace_size", "sparse_attn_bwd_deterministic",
     "attn_status_string", "attn_version", "attn_bwd_fixed_scratch",
+    "csa_compressor_fwd", "csa_compressor_bwd_workspace_size", "csa_compressor_bwd",
 )
 FIXED_SCRATCH_BYTES = 16 << 20
 
@@ -63,6 +66,15 @@ class _SparseProblem(ctypes.Structure):
     _fields_ = [
         ("tokens", ctypes.c_int), ("heads", ctypes.c_int), ("dim_qk", ctypes.c_int),
         ("dim_v", ctypes.c_int), ("topk", ctypes.c_int), ("scale", ctypes.c_float),
+        ("error_word", ctypes.c_void_p),
+    ]
+
+
+class _CsaProblem(ctypes.Structure):
+    _fields_ = [
+        ("tokens", ctypes.c_int), ("comp_capacity", ctypes.c_int), ("num_seqs", ctypes.c_int),
+        ("head_dim", ctypes.c_int), ("ratio", ctypes.c_int), ("coff", ctypes.c_int),
+        ("cu_seqlens", ctypes.c_void_p), ("cu_seqlens_comp", ctypes.c_void_p),
         ("error_word", ctypes.c_void_p),
     ]
 
@@ -95,11 +107,17 @@ def lib() -> ctypes.CDLL:
         L.sparse_attn_bwd_deterministic_workspace_size.restype = sz
         L.sparse_attn_bwd_deterministic.argtypes = [SP, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
         L.attn_bwd_fixed_scratch.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+        CP = ctypes.POINTER(_CsaProblem)
+        L.csa_compressor_fwd.argtypes = [CP, vp, vp, vp, vp, vp]
+        L.csa_compressor_bwd_workspace_size.argtypes = [CP]
+        L.csa_compressor_bwd_workspace_size.restype = sz
+        L.csa_compressor_bwd.argtypes = [CP, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
         L.attn_status_string.argtypes = [i32]
         L.attn_status_string.restype = ctypes.c_char_p
         L.attn_version.argtypes = []
         for name in ("attn_fwd", "attn_bwd_preprocess", "attn_bwd", "attn_bwd_postprocess",
-                     "sparse_attn_fwd", "sparse_attn_bwd", "attn_bwd_fixed_scratch"):
+                     "sparse_attn_fwd", "sparse_attn_bwd", "attn_bwd_fixed_scratch",
+                     "csa_compressor_fwd", "csa_compressor_bwd"):
             getattr(L, name).restype = i32
         _LIB = L
     return _LIB
@@ -399,3 +417,71 @@ def sparse_attn_bwd_deterministic(q, kv, idx, o, dout, lse, *, scale=None, works
                                                _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dkv),
                                                _ptr(workspace), workspace.numel(), _stream(stream)))
     return dq, dkv
+
+
+# ----------------------------------------------------------------------------
+# CSA compressor gated pooling (include/dsa.h)
+# ----------------------------------------------------------------------------
+def _csa_problem(kv, cu_seqlens, cu_seqlens_comp, ratio, coff, comp_capacity, error_word):
+    p = _CsaProblem()
+    if kv.dim() != 2 or kv.shape[1] % coff:
+        raise ValueError("kv must be [tokens, coff * head_dim]")
+    _need(cu_seqlens, "cu_seqlens", torch.int32, kv.device)
+    _need(cu_seqlens_comp, "cu_seqlens_comp", torch.int32, kv.device)
+    if cu_seqlens.numel() != cu_seqlens_comp.numel():
+        raise ValueError("cu_seqlens and cu_seqlens_comp must have the same length")
+    p.tokens = kv.shape[0]
+    p.comp_capacity = int(comp_capacity)
+    p.num_seqs = cu_seqlens.numel() - 1
+    p.head_dim = kv.shape[1] // coff
+    p.ratio, p.coff = int(ratio), int(coff)
+    p.cu_seqlens = cu_seqlens.data_ptr()
+    p.cu_seqlens_comp = cu_seqlens_comp.data_ptr()
+    p.error_word = None if error_word is None else error_word.data_ptr()
+    return p
+
+
+def csa_compressor_fwd(kv, score, ape, cu_seqlens, cu_seqlens_comp, *, ratio=4, coff=2,
+                       comp_capacity, out=None, error_word=None, stream=None):
+    """kv/score bf16 [T, coff*D], ape fp32 [ratio, coff*D] -> out bf16 [comp_capacity, D]."""
+    dev = kv.device
+    _need(kv, "kv", torch.bfloat16, dev)
+    _need(score, "score", torch.bfloat16, dev)
+    _need(ape, "ape", torch.float32, dev)
+    p = _csa_problem(kv, cu_seqlens, cu_seqlens_comp, ratio, coff, comp_capacity, error_word)
+    out = out if out is not None else torch.empty(p.comp_capacity, p.head_dim,
+                                                  dtype=torch.bfloat16, device=dev)
+    _need(out, "out", torch.bfloat16, dev)
+    _check("csa_compressor_fwd",
+           lib().csa_compressor_fwd(ctypes.byref(p), _ptr(kv), _ptr(score), _ptr(ape), _ptr(out),
+                                    _stream(stream)))
+    return out
+
+
+def csa_compressor_bwd_workspace_size(kv, cu_seqlens, cu_seqlens_comp, *, ratio=4, coff=2,
+                                      comp_capacity) -> int:
+    p = _csa_problem(kv, cu_seqlens, cu_seqlens_comp, ratio, coff, comp_capacity, None)
+    return int(lib().csa_compressor_bwd_workspace_size(ctypes.byref(p)))
+
+
+def csa_compressor_bwd(kv, score, ape, dout, cu_seqlens, cu_seqlens_comp, *, ratio=4, coff=2,
+                       workspace=None, dkv=None, dscore=None, dape=None, error_word=None,
+                       stream=None):
+    """Returns (dkv, dscore) bf16 [T, coff*D] and dape fp32 [ratio, coff*D], all
+    bitwise reproducible."""
+    dev = kv.device
+    for n, t in (("kv", kv), ("score", score), ("dout", dout)):
+        _need(t, n, torch.bfloat16, dev)
+    _need(ape, "ape", torch.float32, dev)
+    p = _csa_problem(kv, cu_seqlens, cu_seqlens_comp, ratio, coff, dout.shape[0], error_word)
+    if workspace is None:
+        n = int(lib().csa_compressor_bwd_workspace_size(ctypes.byref(p)))
+        workspace = torch.empty(max(n, 16), dtype=torch.uint8, device=dev)
+    dkv = dkv if dkv is not None else torch.empty_like(kv)
+    dscore = dscore if dscore is not None else torch.empty_like(score)
+    dape = dape if dape is not None else torch.empty_like(ape)
+    _check("csa_compressor_bwd",
+           lib().csa_compressor_bwd(ctypes.byref(p), _ptr(kv), _ptr(score), _ptr(ape), _ptr(dout),
+                                    _ptr(dkv), _ptr(dscore), _ptr(dape), _ptr(workspace),
+                                    workspace.numel(), _stream(stream)))
+    return dkv, dscore, dape

@@ -100,6 +100,37 @@ def sparse_inputs(tokens: int, heads: int, topk: int, seed: int):
 
 
 # ----------------------------------------------------------------------------
+# CSA compressor gated pooling (THD packs, one head)
+# ----------------------------------------------------------------------------
+def csa_inputs(lengths, head_dim: int, ratio: int, coff: int, seed: int, pad_tokens: int = 0,
+               pad_rows: int = 0):
+    """kv, score bf16 [T, coff*D] and dout bf16 [C_cap, D] N(0,1), ape fp32
+    [ratio, coff*D] N(0,1); cu_seqlens and cu_seqlens_comp int32 (floor(len/ratio)
+    rows per segment).  T = sum(lengths) + pad_tokens, C_cap = total rows +
+    pad_rows; padding rows hold finite random values too."""
+    g = torch.Generator().manual_seed(seed)
+    T = sum(int(n) for n in lengths) + pad_tokens
+    comp = [int(n) // ratio for n in lengths]
+    C = sum(comp) + pad_rows
+    kv = _randn(g, (T, coff * head_dim))
+    score = _randn(g, (T, coff * head_dim))
+    ape = torch.randn(ratio, coff * head_dim, generator=g, dtype=torch.float32)
+    dout = _randn(g, (C, head_dim))
+    return dict(kv=kv, score=score, ape=ape, dout=dout, cu_seqlens=cu_seqlens_from(lengths),
+                cu_seqlens_comp=cu_seqlens_from(comp), comp_capacity=C)
+
+
+# Compressor shapes of the page's benchmark table: THD packs of 8192-token
+# sequences, ratio 4, coff 2, head_dim 128 or 512.
+CSA_WORKLOADS = {
+    "csa_1x8192_d128": dict(lengths=[8192], head_dim=128, ratio=4, coff=2, seed=41),
+    "csa_3x8192_d128": dict(lengths=[8192] * 3, head_dim=128, ratio=4, coff=2, seed=42),
+    "csa_1x8192_d512": dict(lengths=[8192], head_dim=512, ratio=4, coff=2, seed=43),
+    "csa_3x8192_d512": dict(lengths=[8192] * 3, head_dim=512, ratio=4, coff=2, seed=44),
+}
+
+
+# ----------------------------------------------------------------------------
 # The five named workloads
 # ----------------------------------------------------------------------------
 @dataclass

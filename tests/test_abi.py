@@ -1,5 +1,5 @@
 """Host-only checks of the C ABI: the library builds and loads, exports every
-function declared in include/attn.h, and rejects invalid calls before touching
+function declared in include/*.h, and rejects invalid calls before touching
 the GPU (no kernel is launched here)."""
 import ctypes
 import os
@@ -10,8 +10,8 @@ import pytest
 import softmax_attention_backward_gb300 as A
 from softmax_attention_backward_gb300 import build as B
 
-HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include",
-                      "attn.h")
+INCLUDE = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include")
+HEADERS = sorted(os.path.join(INCLUDE, f) for f in os.listdir(INCLUDE) if f.endswith(".h"))
 
 
 @pytest.fixture(scope="module")
@@ -21,7 +21,7 @@ def L():
 
 
 def declared_functions():
-    text = open(HEADER).read()
+    text = "\n".join(open(h).read() for h in HEADERS)
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     return sorted(set(re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\*?\s*([a-z_0-9]+)\(", text,
                                  flags=re.M)))
@@ -153,3 +153,40 @@ def test_python_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(A, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="missing"):
         A.lib()
+
+
+def _csa(**kw):
+    p = A._CsaProblem()
+    p.tokens, p.comp_capacity, p.num_seqs, p.head_dim, p.ratio, p.coff = 64, 16, 2, 128, 4, 2
+    p.cu_seqlens, p.cu_seqlens_comp, p.error_word = FAKE, FAKE + 64, None
+    for k, v in kw.items():
+        setattr(p, k, v)
+    return p
+
+
+def _csa_fwd(L, p, ptrs=(FAKE,) * 4):
+    return L.csa_compressor_fwd(ctypes.byref(p), *[ctypes.c_void_p(x) for x in ptrs], None)
+
+
+def test_csa_compressor_validation(L):
+    assert L.csa_compressor_fwd(None, *[ctypes.c_void_p(FAKE)] * 4, None) == 1
+    assert _csa_fwd(L, _csa(coff=3)) == 2                       # coff outside {1, 2}
+    assert _csa_fwd(L, _csa(ratio=3)) == 2                      # ratio outside {2, 4, 8}
+    assert _csa_fwd(L, _csa(head_dim=100)) == 2                 # not a multiple of 64
+    assert _csa_fwd(L, _csa(head_dim=2048)) == 2                # above 1024
+    assert _csa_fwd(L, _csa(num_seqs=0)) == 1
+    assert _csa_fwd(L, _csa(tokens=-1)) == 1
+    assert _csa_fwd(L, _csa(cu_seqlens=None)) == 1
+    assert _csa_fwd(L, _csa(cu_seqlens=FAKE + 2)) == 3           # int32 array misaligned
+    assert _csa_fwd(L, _csa(tokens=1 << 22, head_dim=512)) == 2  # flat offsets past int32
+    assert _csa_fwd(L, _csa(), (FAKE, 0, FAKE, FAKE)) == 1        # null score
+    assert _csa_fwd(L, _csa(), (FAKE, FAKE + 8, FAKE, FAKE)) == 3
+    assert _csa_fwd(L, _csa(comp_capacity=0)) == 0              # nothing to write
+    # workspace: one fp32 slab of ratio * coff * head_dim per row group
+    n = L.csa_compressor_bwd_workspace_size(ctypes.byref(_csa()))
+    assert n > 0 and n % (4 * 2 * 128 * 4) == 0
+    assert L.csa_compressor_bwd_workspace_size(ctypes.byref(_csa(coff=3))) == 0
+    args = [ctypes.c_void_p(FAKE)] * 7
+    assert L.csa_compressor_bwd(ctypes.byref(_csa()), *args, ctypes.c_void_p(FAKE), n - 4,
+                                None) == 5
+    assert L.csa_compressor_bwd(ctypes.byref(_csa()), *args, None, n, None) == 5

@@ -390,10 +390,10 @@ extern "C" attn_status_t csa_compressor_fwd(const csa_compressor_problem_t* p, c
                                             attn_stream_t stream) {
   const attn_status_t s = check(p);
   if (s != ATTN_OK) return s;
-  if (!kv || !score || !ape || !out) return ATTN_ERR_INVALID_ARG;
+  if (p->comp_capacity == 0) return ATTN_OK;    // no output row: nothing to write
+  if (!ape || !out || (p->tokens > 0 && (!kv || !score))) return ATTN_ERR_INVALID_ARG;
   if (!aligned(kv, 16) || !aligned(score, 16) || !aligned(ape, 16) || !aligned(out, 16))
     return ATTN_ERR_ALIGNMENT;
-  if (p->comp_capacity == 0) return ATTN_OK;
   CsaArgs a = make_args(p);
   a.kv = static_cast<const __nv_bfloat16*>(kv);
   a.score = static_cast<const __nv_bfloat16*>(score);
@@ -421,7 +421,12 @@ extern "C" attn_status_t csa_compressor_bwd(const csa_compressor_problem_t* p, c
                                             size_t workspace_bytes, attn_stream_t stream) {
   const attn_status_t s = check(p);
   if (s != ATTN_OK) return s;
-  if (!kv || !score || !ape || !dout || !dkv || !dscore || !dape) return ATTN_ERR_INVALID_ARG;
+  // token buffers may be null when there is no token, dout when there is no
+  // compressed row (they are never touched then); dape is always written
+  const bool tok = p->tokens > 0;
+  if (!ape || !dape || (tok && (!kv || !score || !dkv || !dscore)) ||
+      (!dout && p->comp_capacity > 0))
+    return ATTN_ERR_INVALID_ARG;
   if (!aligned(kv, 16) || !aligned(score, 16) || !aligned(ape, 16) || !aligned(dout, 16) ||
       !aligned(dkv, 16) || !aligned(dscore, 16) || !aligned(dape, 16))
     return ATTN_ERR_ALIGNMENT;

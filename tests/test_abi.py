@@ -179,7 +179,7 @@ def test_csa_compressor_validation(L):
     assert _csa_fwd(L, _csa(cu_seqlens=None)) == 1
     assert _csa_fwd(L, _csa(cu_seqlens=FAKE + 2)) == 3           # int32 array misaligned
     assert _csa_fwd(L, _csa(tokens=1 << 22, head_dim=512)) == 2  # flat offsets past int32
-    assert _csa_fwd(L, _csa(), (FAKE, 0, FAKE, FAKE)) == 1        # null score
+    assert _csa_fwd(L, _csa(), (FAKE, 0, FAKE, FAKE)) == 1        # null score with tokens
     assert _csa_fwd(L, _csa(), (FAKE, FAKE + 8, FAKE, FAKE)) == 3
     assert _csa_fwd(L, _csa(comp_capacity=0)) == 0              # nothing to write
     # workspace: one fp32 slab of ratio * coff * head_dim per row group

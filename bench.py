@@ -503,6 +503,8 @@ def run_ours(args, w, world, rank, local):
         if rank == 0:
             extra["csa_compressor"] = bench_csa(args, dev, flush)
             torch.cuda.empty_cache()
+            extra["dsa_indexer"] = bench_indexer(args, dev, flush)
+            torch.cuda.empty_cache()
 
     if rank != 0:
         return
@@ -702,6 +704,81 @@ def bench_csa(args, dev, flush):
                              "csa_bwd_kernel", "csa_3x8192_d512",
                              "softmax_attention_backward_gb300/csrc/csa_compressor.cu")},
             "shapes": res}
+
+
+# ----------------------------------------------------------------------------
+# DSA lightning indexer (logits, top-k, backward) and the sparse KL loss
+# ----------------------------------------------------------------------------
+def _time(fn, flush, iters):
+    stream = torch.cuda.current_stream()
+    for _ in range(3):
+        fn()
+    ms = []
+    for _ in range(iters):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms.append(e0.elapsed_time(e1))
+    return statistics.median(ms)
+
+
+def bench_indexer(args, dev, flush):
+    import softmax_attention_backward_gb300 as A
+    c = W.INDEXER_WORKLOAD
+    T, H, K = c["tokens"], c["heads"], c["topk"]
+    x = W.indexer_inputs(T, H, c["seed"], topk=K)
+    q, k, w, g = (x[n].to(dev) for n in ("q", "k", "w", "grad"))
+    logits = torch.empty(T, A.logits_ld(T), dtype=torch.float32, device=dev)
+    idx = torch.empty(T, K, dtype=torch.int32, device=dev)
+    length = torch.empty(T, dtype=torch.int32, device=dev)
+    scores = torch.empty(T, K, dtype=torch.float32, device=dev)
+    dq, dk, dw = torch.empty_like(q), torch.empty_like(k), torch.empty_like(w)
+    iters = max(5, min(args.steps, 20))
+    pk, pk_kind = peaks()
+    peak, hbm = pk["bf16_tflops"], pk["hbm_gbs"]
+    t_fwd = _time(lambda: A.dsa_indexer_fwd(q, k, w, logits=logits), flush, iters)
+    t_topk = _time(lambda: A.dsa_topk(logits, K, heads=H, idx=idx, length=length, scores=scores),
+                   flush, iters)
+    t_bwd = _time(lambda: A.dsa_indexer_bwd(q, k, w, idx, g, dq=dq, dk=dk, dw=dw), flush, iters)
+    pairs_causal = T * (T + 1) // 2                  # (query, key) pairs the logits cover
+    sel = int((idx >= 0).sum().item())               # selected (query, key) pairs
+    f_fwd = 2.0 * pairs_causal * H * W.INDEXER_D
+    f_bwd = 3 * 2.0 * sel * H * W.INDEXER_D
+    b_topk = pairs_causal * 4 + T * K * 8 + T * 4    # visible logits read; idx, scores, length
+    # sparse KL on the sparse attention workload (the indexer's training signal)
+    ws, xs = W.get_workload("sparse_topk2048_t8192_h64"), None
+    xs = W.make_inputs(ws)
+    gq, gkv, gidx = xs["q"].to(dev), xs["kv"].to(dev), xs["idx"].to(dev)
+    _, lse = A.sparse_attn_fwd(gq, gkv, gidx, scale=ws.scale)
+    sc = torch.randn(gidx.shape, generator=torch.Generator().manual_seed(9)).to(dev)
+    loss = torch.empty(ws.seqlen, dtype=torch.float32, device=dev)
+    kgrad = torch.empty_like(sc)
+    t_kl = _time(lambda: A.dsa_sparse_kl(gq, gkv, lse, gidx, sc, scale=ws.scale, loss=loss,
+                                         grad=kgrad), flush, iters)
+    kl_pairs = int((xs["idx"] >= 0).sum().item())
+    f_kl = 2.0 * kl_pairs * ws.heads_q * 576
+    tf = lambda f, ms: f / (ms * 1e-3) / 1e12
+    return {
+        "workload": c["name"], "iters": iters, "timing": "median, L2 flushed before each launch",
+        "fwd": {"kernel": "dsa_indexer_logits_kernel", "us": 1e3 * t_fwd, "tflops": tf(f_fwd, t_fwd),
+                "frac": tf(f_fwd, t_fwd) / peak, "flops": f_fwd},
+        "topk": {"kernel": "dsa_topk_kernel", "us": 1e3 * t_topk, "gbs": b_topk / t_topk / 1e6,
+                 "frac_hbm": b_topk / t_topk / 1e6 / hbm, "bytes": b_topk},
+        "bwd": {"kernel": "dsa_indexer_bwd_kernel (+ zero, cast)", "us": 1e3 * t_bwd,
+                "tflops": tf(f_bwd, t_bwd), "frac": tf(f_bwd, t_bwd) / peak, "flops": f_bwd,
+                "selected_pairs": sel},
+        "sparse_kl": {"kernel": "dsa_sparse_kl_kernel", "workload": ws.name, "us": 1e3 * t_kl,
+                      "tflops": tf(f_kl, t_kl), "frac": tf(f_kl, t_kl) / peak, "flops": f_kl},
+        "peak": {"bf16_tflops": peak, "hbm_gbs": hbm, "kind": f"{pk_kind} (bf16 burst, copy)"},
+        "roofline": {"kernel": "dsa_indexer_logits_kernel", "bound": "tensor",
+                     "achieved": tf(f_fwd, t_fwd), "peak": peak, "unit": "TFLOP/s",
+                     "frac": tf(f_fwd, t_fwd) / peak,
+                     "traffic": profiled_traffic("dsa_indexer_logits_kernel", c["name"],
+                                                 "softmax_attention_backward_gb300/csrc/dsa_indexer.cu")},
+    }
 
 
 def main():

@@ -1,6 +1,8 @@
 /*
  * dsa.h — C ABI of the kernels that surround the sparse attention of the DSA
- * family on GB300 (sm_103a): the CSA compressor's gated-softmax pooling.
+ * family on GB300 (sm_103a): the lightning indexer (logits, top-k selection,
+ * backward), the sparse KL loss that trains it, and the CSA compressor's
+ * gated-softmax pooling.
  * Status codes, the stream handle and the device error-word bits are those of
  * attn.h, and every convention listed there holds here too (caller-owned
  * device pointers, no allocation, no host synchronization, every output element
@@ -14,6 +16,84 @@
 #ifdef __cplusplus
 extern "C" {
 #endif
+
+/*
+ * Lightning indexer ("[2/2] Add TileLang fused DSA kernels support with THD and
+ * CP & Clean up", Megatron-LM #5049: fused indexer forward with logits
+ * cleaning, fused indexer backward returning the gradients of q, k and the
+ * weights, top-k returning (topk_indices, topk_length) with -1 sentinels).
+ *
+ *   logits[t, s] = sum_h w[t, h] * act(<q[t, h], k[s]>)   act = ReLU if use_relu
+ *
+ * for every key s that query t sees (s <= t within t's sequence); every other
+ * entry of the row is written as -inf ("cleaned").
+ * Layouts: q bf16 [tokens, heads, 128], k bf16 [tokens, 128], w fp32
+ * [tokens, heads], logits fp32 [tokens, logits_ld] (row stride logits_ld, a
+ * multiple of 4 and >= tokens; columns past tokens are not written).  THD when
+ * cu_seqlens != NULL (device int32 [num_seqs + 1]): tokens at or past
+ * cu_seqlens[num_seqs] see no key.  Supported: head_dim 128, 1 <= heads <= 64,
+ * 1 <= topk <= 8192 (dsa_topk), tokens * logits_ld < 2^31.
+ */
+typedef struct {
+  int tokens;
+  int heads;
+  int head_dim;
+  int topk;
+  int use_relu;
+  int logits_ld;
+  const int32_t* cu_seqlens; /* optional (THD) */
+  int num_seqs;
+  int32_t* error_word;       /* optional device int32 */
+} dsa_indexer_problem_t;
+
+attn_status_t dsa_indexer_fwd(const dsa_indexer_problem_t* p, const void* q, const void* k,
+                              const float* w, float* logits, attn_stream_t stream);
+
+/* Top-k of each logits row over the keys the row's token sees: the
+ * min(topk, n_t) largest (ties toward the smaller key index), written in
+ * ascending key order to idx int32 [tokens, topk] and padded with -1;
+ * length int32 [tokens] = min(topk, n_t) (the compact-prefix form); scores
+ * fp32 [tokens, topk] = the selected logits (-inf in padded slots).  A NaN
+ * logit ranks below every number. */
+attn_status_t dsa_topk(const dsa_indexer_problem_t* p, const float* logits, int32_t* idx,
+                       int32_t* length, float* scores, attn_stream_t stream);
+
+/* Workspace bytes of dsa_indexer_bwd: the fp32 dk accumulator [tokens, 128]. */
+size_t dsa_indexer_bwd_workspace_size(const dsa_indexer_problem_t* p);
+
+/* Backward of L = sum over valid slots of grad[t, j] * logits[t, idx[t, j]]:
+ *   dz = grad[t, j] * w[t, h] * act'(<q[t, h], k[s]>),   s = idx[t, j]
+ *   dq[t, h] = sum_j dz k[s];  dk[s] += sum_h dz q[t, h];
+ *   dw[t, h] = sum_j grad[t, j] * act(<q[t, h], k[s]>).
+ * idx int32 [tokens, topk] (-1 = empty slot; entries outside [-1, tokens) are
+ * skipped and flagged ATTN_DEVERR_INDEX_RANGE), grad fp32 [tokens, topk];
+ * dq bf16 [tokens, heads, 128], dk bf16 [tokens, 128], dw fp32 [tokens, heads].
+ * dk is summed with fp32 atomic adds (not bitwise reproducible). */
+attn_status_t dsa_indexer_bwd(const dsa_indexer_problem_t* p, const void* q, const void* k,
+                              const float* w, const int32_t* idx, const float* grad, void* dq,
+                              void* dk, float* dw, void* workspace, size_t workspace_bytes,
+                              attn_stream_t stream);
+
+/*
+ * Sparse KL loss of the indexer (the same page's streaming sparse-KL hook; the
+ * KL target and normalisation "including all-invalid/empty rows").  With the
+ * sparse attention of sparse_attn_fwd (problem `p`, q, kv, its lse, the index
+ * lists idx), per token t over its valid slots j:
+ *   P[h, j]    = exp(scale <q[t, h], kv[idx[t, j]]> - lse[t, h])
+ *   target[j]  = (1 / heads) sum_h P[h, j]
+ *   r          = softmax_j(scores[t, j])
+ *   loss[t]    = sum_j target[j] (ln target[j] - ln r[j])     (0 ln 0 = 0)
+ *   grad[t, j] = r[j] - target[j]      (d loss[t] / d scores[t, j]; 0 in -1 slots)
+ * A token without a valid slot gets loss 0.  scores fp32 [tokens, topk] (the
+ * indexer's logits at the slots, e.g. dsa_topk's output), loss fp32 [tokens],
+ * grad fp32 [tokens, topk], target fp32 [tokens, topk] (optional, may be NULL).
+ * The attention probabilities are recomputed chunk by chunk on the tensor cores
+ * and reduced over the heads on chip; nothing of size tokens x heads x topk is
+ * stored.  Supported: the sparse_attn_fwd envelope.
+ */
+attn_status_t dsa_sparse_kl(const sparse_attn_problem_t* p, const void* q, const void* kv,
+                            const float* lse, const int32_t* idx, const float* scores,
+                            float* loss, float* grad, float* target, attn_stream_t stream);
 
 /* Device error-word bit: a segment's compressed-row count in cu_seqlens_comp
  * differs from floor(length / ratio), or cu_seqlens / cu_seqlens_comp are not

@@ -85,6 +85,22 @@ def indexer_logits(q, k, w, cu_seqlens=None, use_relu=True):
     return torch.where(vis, out, torch.full_like(out, NEG_INF))
 
 
+def indexer_logits_rows(q, k, w, rows, cu_seqlens=None, use_relu=True):
+    """Rows `rows` of indexer_logits only ([len(rows), T]): the same sums for
+    the listed query tokens (each row is independent of the others)."""
+    q, k, w = _f64(q), _f64(k), _f64(w)
+    T, H, _ = q.shape
+    rows = [int(r) for r in rows]
+    out = torch.zeros(len(rows), T, dtype=F64)
+    for n, t in enumerate(rows):
+        z = q[t] @ k.T                              # [H, T]
+        if use_relu:
+            z = torch.clamp(z, min=0.0)
+        out[n] = (w[t][:, None] * z).sum(0)
+    vis = visible_keys(T, cu_seqlens)[rows]
+    return torch.where(vis, out, torch.full_like(out, NEG_INF)), vis
+
+
 def topk_select(logits, topk, visible):
     """Per row: the min(topk, n) visible keys of largest logit, ties toward the
     smaller index, in ascending index order.  Returns idx int32 [T, topk] (-1
@@ -106,14 +122,16 @@ def topk_select(logits, topk, visible):
     return idx, length, scores
 
 
-def indexer_backward(q, k, w, idx, grad, use_relu=True):
-    """Gradients of L = sum_{t, j valid} grad[t, j] * I[t, idx[t, j]]."""
+def indexer_backward(q, k, w, idx, grad, use_relu=True, tokens=None):
+    """Gradients of L = sum_{t, j valid} grad[t, j] * I[t, idx[t, j]].  With
+    `tokens`, only those query tokens contribute (dq and dw of other tokens
+    stay zero, dk holds only their share)."""
     q, k, w, grad = _f64(q), _f64(k), _f64(w), _f64(grad)
     T, H, D = q.shape
     dq = torch.zeros_like(q)
     dk = torch.zeros_like(k)
     dw = torch.zeros_like(w)
-    for t in range(T):
+    for t in (range(T) if tokens is None else tokens):
         sel = [(j, int(s)) for j, s in enumerate(idx[t].tolist()) if 0 <= s < k.shape[0]]
         if not sel:
             continue
@@ -131,13 +149,24 @@ def indexer_backward(q, k, w, idx, grad, use_relu=True):
     return dict(dq=dq, dk=dk, dw=dw)
 
 
-def attention_target(q, kv, idx, scale):
+def indexer_dk_rows(q, k, w, idx, grad, rows, use_relu=True):
+    """dk of a few key rows only: the contributions of every token whose list
+    names the row (equal to indexer_backward(...)["dk"][rows])."""
+    rows = [int(r) for r in rows]
+    want = torch.tensor(rows, dtype=idx.dtype)
+    hit = (idx[:, :, None] == want[None, None, :]).any(dim=1).any(dim=1)
+    toks = torch.nonzero(hit).flatten().tolist()
+    return indexer_backward(q, k, w, idx, grad, use_relu, tokens=toks)["dk"][rows]
+
+
+def attention_target(q, kv, idx, scale, tokens=None):
     """p [T, K] fp64: the sparse attention probabilities of each slot averaged
-    over the heads (0 in -1 slots), from the exact fp64 softmax of every head."""
+    over the heads (0 in -1 slots), from the exact fp64 softmax of every head.
+    With `tokens`, only those rows are computed (the others stay zero)."""
     q, kv = _f64(q), _f64(kv)
     T, H, _ = q.shape
     p = torch.zeros(idx.shape, dtype=F64)
-    for t in range(T):
+    for t in (range(T) if tokens is None else tokens):
         js = [j for j, s in enumerate(idx[t].tolist()) if 0 <= s < kv.shape[0]]
         if not js:
             continue

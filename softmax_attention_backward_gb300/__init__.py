@@ -10,6 +10,7 @@ Entry points (same names as the C ABI):
   sparse_attn_fwd, sparse_attn_bwd_workspace_size, sparse_attn_bwd,
   sparse_attn_bwd_deterministic_workspace_size, sparse_attn_bwd_deterministic,
   attn_bwd_fixed_scratch, attn_status_string, attn_version   (include/attn.h)
+  dsa_indexer_fwd, dsa_topk, dsa_indexer_bwd_workspace_size, dsa_indexer_bwd, dsa_sparse_kl,
   csa_compressor_fwd, csa_compressor_bwd_workspace_size, csa_compressor_bwd  (include/dsa.h)
 """
 from __future__ import annotations
@@ -28,7 +29,8 @@ __all__ = [
     "attn_status_string", "attn_version", "dense_backward",
     "SPARSE_DIM_QK", "SPARSE_DIM_V", "EXPORTED_SYMBOLS", "attn_bwd_fixed_scratch",
     "FIXED_SCRATCH_BYTES", "csa_compressor_fwd", "csa_compressor_bwd_workspace_size",
-    "csa_compressor_bwd",
+    "csa_compressor_bwd", "dsa_indexer_fwd", "dsa_topk", "dsa_indexer_bwd_workspace_size",
+    "dsa_indexer_bwd", "dsa_sparse_kl", "INDEXER_HEAD_DIM",
 ]
 
 ATTN_DQ_ATOMIC = 0
@@ -43,7 +45,10 @@ EXPORTED_SYMBOLS = (
     "sparse_attn_bwd_deterministic_workspace_size", "sparse_attn_bwd_deterministic",
     "attn_status_string", "attn_version", "attn_bwd_fixed_scratch",
     "csa_compressor_fwd", "csa_compressor_bwd_workspace_size", "csa_compressor_bwd",
+    "dsa_indexer_fwd", "dsa_topk", "dsa_indexer_bwd_workspace_size", "dsa_indexer_bwd",
+    "dsa_sparse_kl",
 )
+INDEXER_HEAD_DIM = 128
 FIXED_SCRATCH_BYTES = 16 << 20
 
 
@@ -75,6 +80,15 @@ class _CsaProblem(ctypes.Structure):
         ("tokens", ctypes.c_int), ("comp_capacity", ctypes.c_int), ("num_seqs", ctypes.c_int),
         ("head_dim", ctypes.c_int), ("ratio", ctypes.c_int), ("coff", ctypes.c_int),
         ("cu_seqlens", ctypes.c_void_p), ("cu_seqlens_comp", ctypes.c_void_p),
+        ("error_word", ctypes.c_void_p),
+    ]
+
+
+class _IndexerProblem(ctypes.Structure):
+    _fields_ = [
+        ("tokens", ctypes.c_int), ("heads", ctypes.c_int), ("head_dim", ctypes.c_int),
+        ("topk", ctypes.c_int), ("use_relu", ctypes.c_int), ("logits_ld", ctypes.c_int),
+        ("cu_seqlens", ctypes.c_void_p), ("num_seqs", ctypes.c_int),
         ("error_word", ctypes.c_void_p),
     ]
 
@@ -112,12 +126,20 @@ def lib() -> ctypes.CDLL:
         L.csa_compressor_bwd_workspace_size.argtypes = [CP]
         L.csa_compressor_bwd_workspace_size.restype = sz
         L.csa_compressor_bwd.argtypes = [CP, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+        IP = ctypes.POINTER(_IndexerProblem)
+        L.dsa_indexer_fwd.argtypes = [IP, vp, vp, vp, vp, vp]
+        L.dsa_topk.argtypes = [IP, vp, vp, vp, vp, vp]
+        L.dsa_indexer_bwd_workspace_size.argtypes = [IP]
+        L.dsa_indexer_bwd_workspace_size.restype = sz
+        L.dsa_indexer_bwd.argtypes = [IP, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+        L.dsa_sparse_kl.argtypes = [SP, vp, vp, vp, vp, vp, vp, vp, vp, vp]
         L.attn_status_string.argtypes = [i32]
         L.attn_status_string.restype = ctypes.c_char_p
         L.attn_version.argtypes = []
         for name in ("attn_fwd", "attn_bwd_preprocess", "attn_bwd", "attn_bwd_postprocess",
                      "sparse_attn_fwd", "sparse_attn_bwd", "attn_bwd_fixed_scratch",
-                     "csa_compressor_fwd", "csa_compressor_bwd"):
+                     "csa_compressor_fwd", "csa_compressor_bwd", "dsa_indexer_fwd", "dsa_topk",
+                     "dsa_indexer_bwd", "dsa_sparse_kl"):
             getattr(L, name).restype = i32
         _LIB = L
     return _LIB
@@ -485,3 +507,117 @@ def csa_compressor_bwd(kv, score, ape, dout, cu_seqlens, cu_seqlens_comp, *, rat
                                     _ptr(dkv), _ptr(dscore), _ptr(dape), _ptr(workspace),
                                     workspace.numel(), _stream(stream)))
     return dkv, dscore, dape
+
+
+# ----------------------------------------------------------------------------
+# DSA lightning indexer, top-k and sparse KL (include/dsa.h)
+# ----------------------------------------------------------------------------
+def logits_ld(tokens: int) -> int:
+    """Row stride of the logits buffer: tokens rounded up to a multiple of 4."""
+    return (int(tokens) + 3) // 4 * 4
+
+
+def _indexer_problem(q, topk, use_relu, cu_seqlens, error_word, ld=None):
+    p = _IndexerProblem()
+    if q.dim() != 3:
+        raise ValueError("indexer q must be [tokens, heads, head_dim]")
+    p.tokens, p.heads, p.head_dim = q.shape
+    p.topk = int(topk)
+    p.use_relu = 1 if use_relu else 0
+    p.logits_ld = logits_ld(p.tokens) if ld is None else int(ld)
+    if cu_seqlens is not None:
+        _need(cu_seqlens, "cu_seqlens", torch.int32, q.device)
+        p.cu_seqlens = cu_seqlens.data_ptr()
+        p.num_seqs = cu_seqlens.numel() - 1
+    else:
+        p.cu_seqlens, p.num_seqs = None, 0
+    p.error_word = None if error_word is None else error_word.data_ptr()
+    return p
+
+
+def dsa_indexer_fwd(q, k, w, *, use_relu=True, cu_seqlens=None, logits=None, error_word=None,
+                    stream=None):
+    """q bf16 [T,H,128], k bf16 [T,128], w fp32 [T,H] -> logits fp32 [T, logits_ld(T)]
+    (columns past T unwritten; use logits[:, :T])."""
+    dev = q.device
+    _need(q, "q", torch.bfloat16, dev)
+    _need(k, "k", torch.bfloat16, dev)
+    _need(w, "w", torch.float32, dev)
+    p = _indexer_problem(q, 1, use_relu, cu_seqlens, error_word)
+    if logits is None:
+        logits = torch.empty(p.tokens, p.logits_ld, dtype=torch.float32, device=dev)
+    _need(logits, "logits", torch.float32, dev)
+    p.logits_ld = logits.shape[1]
+    _check("dsa_indexer_fwd", lib().dsa_indexer_fwd(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(w),
+                                                    _ptr(logits), _stream(stream)))
+    return logits
+
+
+def dsa_topk(logits, topk, *, heads=1, cu_seqlens=None, idx=None, length=None, scores=None,
+             error_word=None, stream=None):
+    """logits fp32 [T, ld] -> (idx int32 [T,topk], length int32 [T], scores fp32 [T,topk])."""
+    dev = logits.device
+    _need(logits, "logits", torch.float32, dev)
+    T = logits.shape[0]
+    p = _IndexerProblem()
+    p.tokens, p.heads, p.head_dim, p.topk = T, int(heads), INDEXER_HEAD_DIM, int(topk)
+    p.use_relu, p.logits_ld = 1, logits.shape[1]
+    if cu_seqlens is not None:
+        _need(cu_seqlens, "cu_seqlens", torch.int32, dev)
+        p.cu_seqlens, p.num_seqs = cu_seqlens.data_ptr(), cu_seqlens.numel() - 1
+    else:
+        p.cu_seqlens, p.num_seqs = None, 0
+    p.error_word = None if error_word is None else error_word.data_ptr()
+    idx = idx if idx is not None else torch.empty(T, topk, dtype=torch.int32, device=dev)
+    length = length if length is not None else torch.empty(T, dtype=torch.int32, device=dev)
+    scores = scores if scores is not None else torch.empty(T, topk, dtype=torch.float32, device=dev)
+    _check("dsa_topk", lib().dsa_topk(ctypes.byref(p), _ptr(logits), _ptr(idx), _ptr(length),
+                                      _ptr(scores), _stream(stream)))
+    return idx, length, scores
+
+
+def dsa_indexer_bwd(q, k, w, idx, grad, *, use_relu=True, workspace=None, dq=None, dk=None,
+                    dw=None, error_word=None, stream=None):
+    """Gradients (dq bf16 [T,H,128], dk bf16 [T,128], dw fp32 [T,H]) of
+    sum_j grad[t, j] * logits[t, idx[t, j]]."""
+    _nondeterministic("dsa_indexer_bwd (dk)", "a reproducible reduction of dk")
+    dev = q.device
+    _need(q, "q", torch.bfloat16, dev)
+    _need(k, "k", torch.bfloat16, dev)
+    _need(w, "w", torch.float32, dev)
+    _need(idx, "idx", torch.int32, dev)
+    _need(grad, "grad", torch.float32, dev)
+    p = _indexer_problem(q, idx.shape[1], use_relu, None, error_word)
+    if workspace is None:
+        n = int(lib().dsa_indexer_bwd_workspace_size(ctypes.byref(p)))
+        workspace = torch.empty(max(n, 16), dtype=torch.uint8, device=dev)
+    dq = dq if dq is not None else torch.empty_like(q)
+    dk = dk if dk is not None else torch.empty_like(k)
+    dw = dw if dw is not None else torch.empty_like(w)
+    _check("dsa_indexer_bwd",
+           lib().dsa_indexer_bwd(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(w), _ptr(idx), _ptr(grad),
+                                 _ptr(dq), _ptr(dk), _ptr(dw), _ptr(workspace), workspace.numel(),
+                                 _stream(stream)))
+    return dq, dk, dw
+
+
+def dsa_sparse_kl(q, kv, lse, idx, scores, *, scale=None, loss=None, grad=None, target=None,
+                  want_target=False, error_word=None, stream=None):
+    """Sparse KL of the attention target from softmax(scores) per token:
+    returns (loss fp32 [T], grad fp32 [T,K], target fp32 [T,K] or None)."""
+    dev = q.device
+    _need(q, "q", torch.bfloat16, dev)
+    _need(kv, "kv", torch.bfloat16, dev)
+    _need(lse, "lse", torch.float32, dev)
+    _need(idx, "idx", torch.int32, dev)
+    _need(scores, "scores", torch.float32, dev)
+    T = q.shape[0]
+    p = _sparse_problem(q, idx, scale, error_word)
+    loss = loss if loss is not None else torch.empty(T, dtype=torch.float32, device=dev)
+    grad = grad if grad is not None else torch.empty_like(scores)
+    if want_target and target is None:
+        target = torch.empty_like(scores)
+    _check("dsa_sparse_kl",
+           lib().dsa_sparse_kl(ctypes.byref(p), _ptr(q), _ptr(kv), _ptr(lse), _ptr(idx),
+                               _ptr(scores), _ptr(loss), _ptr(grad), _ptr(target), _stream(stream)))
+    return loss, grad, target

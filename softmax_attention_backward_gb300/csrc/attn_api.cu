@@ -134,6 +134,11 @@ attn_status_t validate_dense_problem(const attn_problem_t* p, bool* empty) {
   return check_problem(p, empty);
 }
 
+bool make_bf16_tile_map(CUtensorMap* m, const void* ptr, int batch, int rows, int heads, int dim,
+                        int box_rows) {
+  return make_map(m, ptr, batch, rows, heads, dim, box_rows);
+}
+
 // Streaming multiprocessors of the current device (persistent grid size).
 int sm_count() {
   constexpr int kMaxDevices = 64;

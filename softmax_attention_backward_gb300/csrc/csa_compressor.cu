@@ -119,81 +119,118 @@ __device__ __forceinline__ void unpack4(uint2 u, float* f) {
   f[0] = x.x; f[1] = x.y; f[2] = y.x; f[3] = y.y;
 }
 
-// Loads the window entries of one row for the 4 dims at d: kv as packed bf16
-// (zero for masked entries), score + ape in fp32 (-inf for masked entries, the
-// previous block's entries when b == 0).
+// APE of the thread's 4 dims for every window entry (the same for every row).
+template <int R, int COFF>
+__device__ __forceinline__ void load_ape(const CsaArgs& a, int d, float (&ap)[R * COFF][4]) {
+  using Wn = Win<R, COFF>;
+#pragma unroll
+  for (int e = 0; e < Wn::N; ++e) {
+    const float4 x = __ldg(reinterpret_cast<const float4*>(
+        a.ape + static_cast<size_t>(Wn::r(e)) * a.ld + Wn::off(e, a.D) + d));
+    ap[e][0] = x.x; ap[e][1] = x.y; ap[e][2] = x.z; ap[e][3] = x.w;
+  }
+}
+
+// Loads the window entries of one row for the 4 dims at d as packed bf16 (kv
+// and score); entries of the previous block (e >= R) are loaded from the row's
+// own first token when b == 0 and masked later.
 template <int R, int COFF>
 __device__ __forceinline__ void load_window(const CsaArgs& a, int t0, bool has_prev, int d,
-                                            uint2 (&v)[R * COFF], float (&s)[R * COFF][4]) {
+                                            uint2 (&v)[R * COFF], uint2 (&s)[R * COFF]) {
   using Wn = Win<R, COFF>;
 #pragma unroll
   for (int e = 0; e < Wn::N; ++e) {
     const bool on = e < R || has_prev;
     const int t = on ? Wn::tok(e, t0) : t0;
     const size_t off = static_cast<size_t>(t) * a.ld + Wn::off(e, a.D) + d;
-    const uint2 kv = __ldg(reinterpret_cast<const uint2*>(a.kv + off));
-    ld4(a.score + off, s[e]);
-    const float4 ap = __ldg(reinterpret_cast<const float4*>(
-        a.ape + static_cast<size_t>(Wn::r(e)) * a.ld + Wn::off(e, a.D) + d));
-    v[e] = on ? kv : make_uint2(0u, 0u);
-    s[e][0] = on ? s[e][0] + ap.x : -INFINITY;
-    s[e][1] = on ? s[e][1] + ap.y : -INFINITY;
-    s[e][2] = on ? s[e][2] + ap.z : -INFINITY;
-    s[e][3] = on ? s[e][3] + ap.w : -INFINITY;
+    v[e] = __ldg(reinterpret_cast<const uint2*>(a.kv + off));
+    s[e] = __ldg(reinterpret_cast<const uint2*>(a.score + off));
   }
 }
 
-// Softmax weights over the window (in place in s) and the pooled output.
-template <int N>
-__device__ __forceinline__ void pool(const uint2 (&v)[N], float (&s)[N][4], float* o) {
-  float m[4], z[4] = {0.f, 0.f, 0.f, 0.f}, acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    m[k] = s[0][k];
-#pragma unroll
-    for (int e = 1; e < N; ++e) m[k] = fmaxf(m[k], s[e][k]);
-  }
+// Softmax over the window per dim (masked entries excluded) and the pooled
+// output; the weights go to w when W is true.
+template <int R, int COFF, bool W>
+__device__ __forceinline__ void pool(const uint2 (&v)[R * COFF], const uint2 (&sr)[R * COFF],
+                                     const float (&ap)[R * COFF][4], bool has_prev,
+                                     float (&w)[W ? R * COFF : 1][4], float* o) {
+  constexpr int N = R * COFF;
+  float m[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
   for (int e = 0; e < N; ++e) {
+    if (e >= R && !has_prev) continue;
     float x[4];
-    unpack4(v[e], x);
+    unpack4(sr[e], x);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) m[k] = fmaxf(m[k], x[k] + ap[e][k]);
+  }
+  float z[4] = {0.f, 0.f, 0.f, 0.f}, acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int e = 0; e < N; ++e) {
+    float x[4], y[4];
+    unpack4(sr[e], x);
+    unpack4(v[e], y);
+    const bool on = e < R || has_prev;
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      const float w = exp2f((s[e][k] - m[k]) * kLog2e);   // 0 for masked entries
-      s[e][k] = w;
-      z[k] += w;
-      acc[k] = fmaf(w, x[k], acc[k]);
+      const float ew = on ? exp2f((x[k] + ap[e][k] - m[k]) * kLog2e) : 0.f;
+      if (W) w[W ? e : 0][k] = ew;
+      z[k] += ew;
+      acc[k] = fmaf(ew, y[k], acc[k]);
     }
   }
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
     const float inv = 1.f / z[k];
+    if (W) {
 #pragma unroll
-    for (int e = 0; e < N; ++e) s[e][k] *= inv;
+      for (int e = 0; e < N; ++e) w[W ? e : 0][k] *= inv;
+    }
     o[k] = acc[k] * inv;
   }
 }
 
+// Window of row c into registers; false when c is a padding row or belongs to a
+// rejected segment.
 template <int R, int COFF>
-__global__ void __launch_bounds__(kThreads) csa_fwd_kernel(const CsaArgs a) {
+__device__ __forceinline__ bool fwd_row(const CsaArgs& a, int c, int d, uint2 (&v)[R * COFF],
+                                        uint2 (&sc)[R * COFF], bool& has_prev) {
+  const int n = row_segment(a, c);
+  if (n < 0) return false;
+  const Seg s = load_seg(a, n, R);
+  const int b = c - s.row0;
+  if (!s.ok || b >= s.nb) {
+    if (threadIdx.x % kTPR == 0) flag(a, ATTN_DEVERR_LAYOUT);
+    return false;
+  }
+  has_prev = b > 0;
+  load_window<R, COFF>(a, s.tok0 + b * R, has_prev, d, v, sc);
+  return true;
+}
+
+// Persistent grid: each thread takes two rows per pass (rows c and c + stride),
+// both windows loaded before either is reduced, so twice the loads are in
+// flight and the per-row segment lookups overlap.
+template <int R, int COFF>
+__global__ void __launch_bounds__(kThreads, (R * COFF <= 8) ? 2 : 1) csa_fwd_kernel(const CsaArgs a) {
+  constexpr int N = R * COFF;
   const int tx = threadIdx.x % kTPR, ty = threadIdx.x / kTPR;
   const int d = blockIdx.x * kDC + tx * kVec;
-  for (int c = blockIdx.y * kRPB + ty; c < a.C; c += gridDim.y * kRPB) {
-    float o[4] = {0.f, 0.f, 0.f, 0.f};
-    const int n = row_segment(a, c);
-    if (n >= 0) {
-      const Seg s = load_seg(a, n, R);
-      const int b = c - s.row0;
-      if (s.ok && b < s.nb) {
-        uint2 v[R * COFF];
-        float sc[R * COFF][4];
-        load_window<R, COFF>(a, s.tok0 + b * R, b > 0, d, v, sc);
-        pool<R * COFF>(v, sc, o);
-      } else if (tx == 0) {
-        flag(a, ATTN_DEVERR_LAYOUT);
-      }
-    }
+  const int stride = gridDim.y * kRPB;
+  float ap[N][4];
+  load_ape<R, COFF>(a, d, ap);
+  float unused[1][4];
+  for (int c = blockIdx.y * kRPB + ty; c < a.C; c += 2 * stride) {
+    const int c2 = c + stride;
+    uint2 v[N], v2[N], sc[N], sc2[N];
+    bool hp = false, hp2 = false;
+    const bool on = fwd_row<R, COFF>(a, c, d, v, sc, hp);
+    const bool on2 = c2 < a.C && fwd_row<R, COFF>(a, c2, d, v2, sc2, hp2);
+    float o[4] = {0.f, 0.f, 0.f, 0.f}, o2[4] = {0.f, 0.f, 0.f, 0.f};
+    if (on) pool<R, COFF, false>(v, sc, ap, hp, unused, o);
+    if (on2) pool<R, COFF, false>(v2, sc2, ap, hp2, unused, o2);
     st4(a.out + static_cast<size_t>(c) * a.D + d, o);
+    if (c2 < a.C) st4(a.out + static_cast<size_t>(c2) * a.D + d, o2);
   }
 }
 
@@ -209,6 +246,8 @@ __global__ void __launch_bounds__(kThreads, (R * COFF <= 8) ? 2 : 1) csa_bwd_ker
   const int tx = threadIdx.x % kTPR, ty = threadIdx.x / kTPR;
   const int d = blockIdx.x * kDC + tx * kVec;
   for (int i = 0; i < N * 4; ++i) dacc[i * kThreads + threadIdx.x] = 0.f;
+  float ap[N][4];
+  load_ape<R, COFF>(a, d, ap);
 
   for (int c = blockIdx.y * kRPB + ty; c < a.C; c += gridDim.y * kRPB) {
     const int n = row_segment(a, c);
@@ -220,11 +259,11 @@ __global__ void __launch_bounds__(kThreads, (R * COFF <= 8) ? 2 : 1) csa_bwd_ker
       continue;
     }
     const int t0 = s.tok0 + b * R;
-    uint2 v[N];
+    uint2 v[N], sr[N];
     float w[N][4], o[4], g[4];
-    load_window<R, COFF>(a, t0, b > 0, d, v, w);
+    load_window<R, COFF>(a, t0, b > 0, d, v, sr);
     ld4(a.dout + static_cast<size_t>(c) * a.D + d, g);
-    pool<N>(v, w, o);
+    pool<R, COFF, true>(v, sr, ap, b > 0, w, o);
 #pragma unroll
     for (int e = 0; e < N; ++e) {
       if (e >= R && b == 0) continue;          // no previous block
@@ -399,9 +438,12 @@ extern "C" attn_status_t csa_compressor_fwd(const csa_compressor_problem_t* p, c
   a.score = static_cast<const __nv_bfloat16*>(score);
   a.ape = ape;
   a.out = static_cast<__nv_bfloat16*>(out);
+  // about four CTAs per SM (two rows per thread and pass)
+  const int ndc = p->head_dim / kDC;
   const int sms = sm_count() > 0 ? sm_count() : 1;
-  const int need = (p->comp_capacity + kRPB - 1) / kRPB;
-  const dim3 grid(p->head_dim / kDC, need < 32 * sms ? need : 32 * sms);
+  const int need = (p->comp_capacity + 2 * kRPB - 1) / (2 * kRPB);
+  const int cap = (4 * sms + ndc - 1) / ndc;
+  const dim3 grid(ndc, need < cap ? need : cap);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const cudaError_t e = dispatch(p->ratio, p->coff, [&](auto R, auto CF) {
     csa_fwd_kernel<decltype(R)::value, decltype(CF)::value><<<grid, kThreads, 0, st>>>(a);

@@ -13,6 +13,12 @@ namespace attn {
 // sets *empty when there is nothing to compute.
 attn_status_t validate_dense_problem(const attn_problem_t* p, bool* empty);
 
+// 4-D TMA map over a bf16 tensor [batch, rows, heads, dim] (dim contiguous): box
+// of 64 dims x 1 head x box_rows rows x 1 batch, 128-byte swizzle, zero fill
+// out of bounds.  False when the driver entry point is missing or refuses it.
+bool make_bf16_tile_map(CUtensorMap* m, const void* ptr, int batch, int rows, int heads, int dim,
+                        int box_rows);
+
 // Streaming multiprocessors of the current device (0 if it cannot be read).
 int sm_count();
 

@@ -100,6 +100,32 @@ def sparse_inputs(tokens: int, heads: int, topk: int, seed: int):
 
 
 # ----------------------------------------------------------------------------
+# DSA lightning indexer (H index heads of dim 128, one key per token)
+# ----------------------------------------------------------------------------
+INDEXER_D = 128
+
+
+def indexer_inputs(tokens: int, heads: int, seed: int, topk: int = 0):
+    """q bf16 [T,H,128], k bf16 [T,128] N(0,1); w fp32 [T,H] N(0,1)/sqrt(H); and,
+    with topk > 0, grad fp32 [T,topk] N(0,1) (a gradient for the selected
+    logits)."""
+    g = torch.Generator().manual_seed(seed)
+    q = _randn(g, (tokens, heads, INDEXER_D))
+    k = _randn(g, (tokens, INDEXER_D))
+    w = torch.randn(tokens, heads, generator=g, dtype=torch.float32) / math.sqrt(heads)
+    out = dict(q=q, k=k, w=w)
+    if topk > 0:
+        out["grad"] = torch.randn(tokens, topk, generator=g, dtype=torch.float32)
+    return out
+
+
+# The indexer workload: the sparse attention workload's token count and top-k
+# (one causal sequence of 8192 tokens, 2048 keys per query) with 64 index heads.
+INDEXER_WORKLOAD = dict(name="indexer_t8192_h64_d128_top2048", tokens=8192, heads=64, topk=2048,
+                        seed=5)
+
+
+# ----------------------------------------------------------------------------
 # CSA compressor gated pooling (THD packs, one head)
 # ----------------------------------------------------------------------------
 def csa_inputs(lengths, head_dim: int, ratio: int, coff: int, seed: int, pad_tokens: int = 0,

@@ -166,3 +166,32 @@ def test_attention_target_and_kl():
         return X.sparse_kl(p, s2, idx)[0].sum().item()
     fd = _fd(L, s2)
     assert (fd - grad2).abs().max() < 1e-6
+
+
+def test_row_and_token_restricted_variants_match_the_full_ones():
+    T, H, D, K = 12, 3, 4, 5
+    q, k, w = rnd(T, H, D, seed=20), rnd(T, D, seed=21), rnd(T, H, seed=22)
+    cu = W.cu_seqlens_from([5, 6])
+    full = X.indexer_logits(q, k, w, cu_seqlens=cu)
+    rows = [0, 4, 7, 11]
+    part, vis = X.indexer_logits_rows(q, k, w, rows, cu_seqlens=cu)
+    assert torch.equal(vis, X.visible_keys(T, cu)[rows])
+    fin = torch.isfinite(full[rows])
+    assert torch.equal(fin, torch.isfinite(part))
+    torch.testing.assert_close(part[fin], full[rows][fin], rtol=0, atol=1e-12)
+    idx = W.topk_indices(T, K, seed=23)
+    grad = rnd(T, K, seed=24)
+    r = X.indexer_backward(q, k, w, idx, grad)
+    for kr in ([0], [1, 2, 9], [11]):
+        torch.testing.assert_close(X.indexer_dk_rows(q, k, w, idx, grad, kr), r["dk"][kr],
+                                   rtol=0, atol=1e-12)
+    sub = X.indexer_backward(q, k, w, idx, grad, tokens=[3, 8])
+    for t in (3, 8):
+        torch.testing.assert_close(sub["dq"][t], r["dq"][t], rtol=0, atol=1e-12)
+        torch.testing.assert_close(sub["dw"][t], r["dw"][t], rtol=0, atol=1e-12)
+    assert (sub["dq"][[0, 1, 2]] == 0).all()
+    qa, kv = rnd(T, 2, 6, seed=25), rnd(T, 6, seed=26)
+    pt = X.attention_target(qa, kv, idx, 0.3)
+    ps = X.attention_target(qa, kv, idx, 0.3, tokens=[2, 10])
+    torch.testing.assert_close(ps[[2, 10]], pt[[2, 10]], rtol=0, atol=0)
+    assert (ps[[0, 1, 3]] == 0).all()

@@ -229,6 +229,18 @@ attn_status_t sparse_attn_bwd_deterministic(const sparse_attn_problem_t* p, cons
                                             void* dkv, void* workspace, size_t workspace_bytes,
                                             attn_stream_t stream);
 
+/* Self-test of the bounded waits of the library's kernels (one CTA, two roles
+ * holding a TMEM allocation): one role waits on an mbarrier that never
+ * completes, with a limit of limit_us microseconds (1 .. 1e6), the other on a
+ * second such barrier with the kernels' own limit.  The first wait must run out
+ * and OR ATTN_DEVERR_TIMEOUT into *error_word (device int32); the second must
+ * then stop on the CTA's abort flag; the CTA frees its TMEM and exits.  *result
+ * (device int32) gets bit 0 when the first wait ran out, bit 1 when the second
+ * stopped and bit 2 when it stopped well before its own limit: 7 when the
+ * mechanism works.  Nothing faults or hangs either way. */
+attn_status_t attn_wait_selftest(int32_t* error_word, unsigned limit_us, int32_t* result,
+                                 attn_stream_t stream);
+
 /* Static description of a status code. */
 const char* attn_status_string(attn_status_t s);
 

@@ -30,7 +30,7 @@ __all__ = [
     "SPARSE_DIM_QK", "SPARSE_DIM_V", "EXPORTED_SYMBOLS", "attn_bwd_fixed_scratch",
     "FIXED_SCRATCH_BYTES", "csa_compressor_fwd", "csa_compressor_bwd_workspace_size",
     "csa_compressor_bwd", "dsa_indexer_fwd", "dsa_topk", "dsa_indexer_bwd_workspace_size",
-    "dsa_indexer_bwd", "dsa_sparse_kl", "INDEXER_HEAD_DIM",
+    "dsa_indexer_bwd", "dsa_sparse_kl", "INDEXER_HEAD_DIM", "attn_wait_selftest",
 ]
 
 ATTN_DQ_ATOMIC = 0
@@ -46,7 +46,7 @@ EXPORTED_SYMBOLS = (
     "attn_status_string", "attn_version", "attn_bwd_fixed_scratch",
     "csa_compressor_fwd", "csa_compressor_bwd_workspace_size", "csa_compressor_bwd",
     "dsa_indexer_fwd", "dsa_topk", "dsa_indexer_bwd_workspace_size", "dsa_indexer_bwd",
-    "dsa_sparse_kl",
+    "dsa_sparse_kl", "attn_wait_selftest",
 )
 INDEXER_HEAD_DIM = 128
 FIXED_SCRATCH_BYTES = 16 << 20
@@ -133,6 +133,8 @@ def lib() -> ctypes.CDLL:
         L.dsa_indexer_bwd_workspace_size.restype = sz
         L.dsa_indexer_bwd.argtypes = [IP, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
         L.dsa_sparse_kl.argtypes = [SP, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+        L.attn_wait_selftest.argtypes = [vp, ctypes.c_uint, vp, vp]
+        L.attn_wait_selftest.restype = i32
         L.attn_status_string.argtypes = [i32]
         L.attn_status_string.restype = ctypes.c_char_p
         L.attn_version.argtypes = []
@@ -151,6 +153,18 @@ def attn_status_string(code: int) -> str:
 
 def attn_version() -> int:
     return int(lib().attn_version())
+
+
+def attn_wait_selftest(limit_us=1000, *, device=None, stream=None):
+    """Runs the bounded-wait self-test; returns (result bits, error word)
+    after synchronizing (7 and ATTN_DEVERR_TIMEOUT when the mechanism works)."""
+    dev = device if device is not None else torch.device("cuda", torch.cuda.current_device())
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    res = torch.full((1,), -1, dtype=torch.int32, device=dev)
+    _check("attn_wait_selftest", lib().attn_wait_selftest(_ptr(err), int(limit_us), _ptr(res),
+                                                          _stream(stream)))
+    torch.cuda.synchronize(dev)
+    return int(res.item()), int(err.item())
 
 
 # ----------------------------------------------------------------------------

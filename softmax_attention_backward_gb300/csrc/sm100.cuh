@@ -50,6 +50,7 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 struct AbortCtx {
   int* smem_abort;   // CTA-wide flag in shared memory
   int* err_word;     // device error word (may be null)
+  uint64_t limit_ns = kWaitLimitNs;   // wait limit (the library's kernels keep the default)
 };
 
 __device__ __forceinline__ void raise_error(const AbortCtx& c, int code) {
@@ -124,7 +125,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
     // issue slots and instruction fetch for the warps doing the work
     if (mbar_try_wait_hint(addr, parity, 200000u)) return true;
     if (*reinterpret_cast<volatile int*>(c.smem_abort)) return false;
-    if (globaltimer() - t0 > kWaitLimitNs) {
+    if (globaltimer() - t0 > c.limit_ns) {
       raise_error(c, ATTN_DEVERR_TIMEOUT);
       return false;
     }

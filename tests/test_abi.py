@@ -190,3 +190,10 @@ def test_csa_compressor_validation(L):
     assert L.csa_compressor_bwd(ctypes.byref(_csa()), *args, ctypes.c_void_p(FAKE), n - 4,
                                 None) == 5
     assert L.csa_compressor_bwd(ctypes.byref(_csa()), *args, None, n, None) == 5
+
+
+def test_wait_selftest_validation(L):
+    v = ctypes.c_void_p(FAKE)
+    assert L.attn_wait_selftest(None, 1000, v, None) == 1
+    assert L.attn_wait_selftest(v, 0, v, None) == 1
+    assert L.attn_wait_selftest(v, 2000000, v, None) == 1

@@ -198,3 +198,17 @@ def test_sparse_outputs_fully_written():
     named[idx[idx >= 0].long()] = True
     assert (dkv2[~named] == 0).all()
     assert torch.equal(dq2, dq)
+
+
+def test_bounded_wait_runs_out_sets_timeout_and_returns():
+    """The library's bounded mbarrier wait, made to run out (a barrier nothing
+    completes, 2 ms limit): the error word gets the timeout bit, the other role
+    stops on the abort flag, the CTA frees its TMEM and returns, and the context
+    stays usable for a regular call afterwards."""
+    res, err = A.attn_wait_selftest(2000)
+    assert res == 7, f"self-test result bits {res:#x}"
+    assert err & 0x2
+    q, k, v, do = (t.to(DEV) for t in W.dense_inputs(1, 64, 2, 2, 64, seed=1))
+    o, lse = A.attn_fwd(q, k, v, causal=True)
+    torch.cuda.synchronize()
+    assert torch.isfinite(o.float()).all()

@@ -781,6 +781,18 @@ def bench_indexer(args, dev, flush):
     }
 
 
+def run_leg(args, local):
+    """One extra leg alone (sparse, CSA compressor or indexer), printed as its own
+    JSON object; used by the profiling commands, not a bench line."""
+    import softmax_attention_backward_gb300 as A
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    A.lib()
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    fn = {"sparse": bench_sparse, "csa": bench_csa, "indexer": bench_indexer}[args.leg]
+    print(json.dumps({"leg": args.leg, "result": fn(args, dev, flush)}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -793,6 +805,8 @@ def main():
                     help="time only --workload (no other dense workloads, no sparse)")
     ap.add_argument("--no-sparse", action="store_true")
     ap.add_argument("--no-split", action="store_true", help="time only the atomic dQ mode")
+    ap.add_argument("--leg", choices=["all", "sparse", "csa", "indexer"], default="all",
+                    help="run one extra leg alone and print its block (profiling runs)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -802,6 +816,8 @@ def main():
         raise SystemExit("the sparse workload is timed inside every default run (key 'sparse')")
     if args.impl == "reference":
         run_reference(args, w, world, rank)
+    elif args.leg != "all":
+        run_leg(args, local)
     else:
         run_ours(args, w, world, rank, local)
     if world > 1:

@@ -89,7 +89,8 @@ attn_status_t dsa_indexer_bwd(const dsa_indexer_problem_t* p, const void* q, con
  * grad fp32 [tokens, topk], target fp32 [tokens, topk] (optional, may be NULL).
  * The attention probabilities are recomputed chunk by chunk on the tensor cores
  * and reduced over the heads on chip; nothing of size tokens x heads x topk is
- * stored.  Supported: the sparse_attn_fwd envelope.
+ * stored (the per-slot sums wait in `grad`, which the kernel then overwrites).
+ * Supported: the sparse_attn_fwd envelope.
  */
 attn_status_t dsa_sparse_kl(const sparse_attn_problem_t* p, const void* q, const void* kv,
                             const float* lse, const int32_t* idx, const float* scores,

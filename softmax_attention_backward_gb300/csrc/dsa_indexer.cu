@@ -13,9 +13,11 @@
 //
 // dsa_topk_kernel: one CTA per row; the visible part of the row is loaded
 // into shared memory as order-preserving 32-bit keys and the k-th largest is
-// found by four 8-bit radix passes; the selected positions (ties toward the
-// smaller index) are then compacted in index order with block-wide scans,
-// which yields the ascending key order directly.
+// found by up to four 8-bit radix passes (warp-aggregated histogram atomics, a
+// warp-parallel digit pick, and an early stop once a digit's bin holds exactly
+// the keys still needed); the selected positions (ties toward the smaller
+// index) are then compacted in index order with block-wide scans, which yields
+// the ascending key order directly.
 //
 // dsa_indexer_bwd_kernel (tcgen05): one CTA per token.  Its query heads
 // (64 x 128) load once; its key rows are gathered 64 slots at a time.  Per
@@ -290,7 +292,7 @@ __global__ void __launch_bounds__(TK_THREADS) dsa_topk_kernel(const IxArgs a, in
   __shared__ uint32_t s_key[TK_MAXN];
   __shared__ int s_hist[256];
   __shared__ int s_warp[TK_THREADS / 32];
-  __shared__ uint32_t s_sel[2];                 // digit chosen, remaining count
+  __shared__ uint32_t s_sel[3];                 // digit chosen, keys still needed, its bin count
   const int t = blockIdx.x;
   int lo;
   bool any;
@@ -309,49 +311,87 @@ __global__ void __launch_bounds__(TK_THREADS) dsa_topk_kernel(const IxArgs a, in
   }
   // n > K (n <= T <= TK_MAXN): keys of the visible part of the row
   for (int i = threadIdx.x; i < n; i += TK_THREADS) s_key[i] = order_key(lrow[lo + i]);
+  // Radix select of the K-th largest key, 8 bits per pass from the top.  A pass
+  // stops the search early when the chosen digit's bin holds exactly the keys
+  // still needed: then every key of that prefix class is taken.
   uint32_t prefix = 0, pmask = 0;
-  int remaining = K;                            // elements still to take at or below the prefix
+  int remaining = K;                            // keys still to take inside the prefix class
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   for (int shift = 24; shift >= 0; shift -= 8) {
     for (int i = threadIdx.x; i < 256; i += TK_THREADS) s_hist[i] = 0;
     __syncthreads();
-    for (int i = threadIdx.x; i < n; i += TK_THREADS) {
-      const uint32_t u = s_key[i];
-      if ((u & pmask) == prefix) atomicAdd(&s_hist[(u >> shift) & 0xFF], 1);
+    // histogram of the next digit within the prefix class; lanes holding the
+    // same digit add once (the top digits of a row take few distinct values)
+    for (int i0 = 0; i0 < n; i0 += TK_THREADS) {
+      const int i = i0 + threadIdx.x;
+      int dg = -1;
+      if (i < n) {
+        const uint32_t u = s_key[i];
+        if ((u & pmask) == prefix) dg = static_cast<int>((u >> shift) & 0xFF);
+      }
+      const unsigned peers = __match_any_sync(0xffffffffu, dg);
+      if (dg >= 0 && lane == __ffs(peers) - 1) atomicAdd(&s_hist[dg], __popc(peers));
     }
     __syncthreads();
-    if (threadIdx.x == 0) {
-      int cum = 0, d = 255;
-      for (; d > 0; --d) {
-        if (cum + s_hist[d] >= remaining) break;
-        cum += s_hist[d];
+    if (warp == 0) {
+      // lane l owns bins 255 - 8l .. 248 - 8l; suffix counts by an inclusive scan
+      int cnt[8], tot = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        cnt[j] = s_hist[255 - 8 * lane - j];
+        tot += cnt[j];
       }
-      s_sel[0] = static_cast<uint32_t>(d);
-      s_sel[1] = static_cast<uint32_t>(remaining - cum);
+      int inc = tot;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += y;
+      }
+      const unsigned hit = __ballot_sync(0xffffffffu, inc >= remaining);
+      const int L = __ffs(hit) - 1;              // first lane reaching `remaining` (exists: total >= remaining)
+      if (lane == L) {
+        int before = inc - tot, d = 255 - 8 * lane - 7, c = 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if (before + cnt[j] >= remaining) {
+            d = 255 - 8 * lane - j;
+            c = cnt[j];
+            break;
+          }
+          before += cnt[j];
+        }
+        s_sel[0] = static_cast<uint32_t>(d);
+        s_sel[1] = static_cast<uint32_t>(remaining - before);
+        s_sel[2] = static_cast<uint32_t>(c);
+      }
     }
     __syncthreads();
     prefix |= s_sel[0] << shift;
     pmask |= 0xFFu << shift;
     remaining = static_cast<int>(s_sel[1]);
+    const bool exact = static_cast<int>(s_sel[2]) == remaining;
     __syncthreads();
+    if (exact) break;
   }
-  // threshold key `prefix`: take every key above it and the first `remaining`
-  // keys equal to it (smallest indices first); compact in index order
+  // take every key whose prefix class is above `prefix` and the first
+  // `remaining` keys of the class itself (smallest indices first); compact in
+  // index order
   const int per = (n + TK_THREADS - 1) / TK_THREADS;
   const int b0 = threadIdx.x * per, b1 = min(n, b0 + per);
   int n_eq = 0;
-  for (int i = b0; i < b1; ++i) n_eq += s_key[i] == prefix;
+  for (int i = b0; i < b1; ++i) n_eq += (s_key[i] & pmask) == prefix;
   int tot_eq;
   const int eq_before = block_excl_scan(n_eq, s_warp, tot_eq);
   int n_sel = 0, eq = eq_before;
   for (int i = b0; i < b1; ++i) {
-    const uint32_t u = s_key[i];
+    const uint32_t u = s_key[i] & pmask;
     if (u > prefix || (u == prefix && eq++ < remaining)) ++n_sel;
   }
   int tot_sel;
   int pos = block_excl_scan(n_sel, s_warp, tot_sel);
   eq = eq_before;
   for (int i = b0; i < b1; ++i) {
-    const uint32_t u = s_key[i];
+    const uint32_t u = s_key[i] & pmask;
     if (u > prefix || (u == prefix && eq++ < remaining)) {
       irow[pos] = lo + i;
       srow[pos] = lrow[lo + i];
@@ -374,7 +414,7 @@ constexpr int IB_D = 128;
 constexpr int IB_Q_BYTES = IB_HB * IB_D * 2;    // 16 KB
 constexpr int IB_K_BYTES = IB_NK * IB_D * 2;    // 16 KB
 constexpr int IB_T_BYTES = IB_HB * IB_NK * 2;   // dZ tile, 8 KB
-constexpr int IB_SMEM = IB_Q_BYTES + IB_K_BYTES + IB_T_BYTES + 1024;
+constexpr int IB_SMEM = IB_Q_BYTES + 2 * IB_K_BYTES + IB_T_BYTES + 1024;   // two key chunks
 constexpr int IB_THREADS = 352;                 // 0..3 epilogue, 4..7 dK drain, 8..9 gather, 10 MMA
 constexpr uint32_t IB_TMEM_COLS = 256;
 constexpr uint32_t IB_COL_Z = 0, IB_COL_DQ = 64, IB_COL_PC0 = 128, IB_COL_PC1 = 192;
@@ -407,13 +447,13 @@ __global__ void __launch_bounds__(IB_THREADS, 2) dsa_indexer_bwd_kernel(const Ib
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   uint8_t* sQ = smem;
-  uint8_t* sK = sQ + IB_Q_BYTES;
-  uint8_t* sdZ = sK + IB_K_BYTES;               // [head][slot] bf16, 128-byte rows
-  __shared__ uint64_t bar_in, bar_k_full, bar_k_empty, bar_z_full, bar_z_free, bar_dz_full;
+  uint8_t* sK = sQ + IB_Q_BYTES;                // two chunk buffers
+  uint8_t* sdZ = sK + 2 * IB_K_BYTES;           // [head][slot] bf16, 128-byte rows
+  __shared__ uint64_t bar_in, bar_k_full[2], bar_k_empty[2], bar_z_full, bar_z_free, bar_dz_full;
   __shared__ uint64_t bar_dz_free, bar_pc_full[2], bar_pc_free[2], bar_dq_done;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_flag;
-  __shared__ int s_row[4][IB_NK];               // key row of each slot (-1: none), by chunk mod 4
+  __shared__ int s_row[8][IB_NK];               // key row of each slot (-1: none), by chunk mod 8
   __shared__ float s_g[2][IB_NK];               // slot gradients (0 for empty slots), by chunk mod 2
   __shared__ float s_w[IB_HB];
   __shared__ int s_red[IB_THREADS / 32];
@@ -437,8 +477,10 @@ __global__ void __launch_bounds__(IB_THREADS, 2) dsa_indexer_bwd_kernel(const Ib
     if (threadIdx.x == 0) {
       abort_flag = 0;
       mbar_init(&bar_in, 64);
-      mbar_init(&bar_k_full, 64);
-      mbar_init(&bar_k_empty, 1);
+      for (int b = 0; b < 2; ++b) {
+        mbar_init(&bar_k_full[b], 64);
+        mbar_init(&bar_k_empty[b], 1);
+      }
       mbar_init(&bar_z_full, 1);
       mbar_init(&bar_z_free, 128);
       mbar_init(&bar_dz_full, 128);
@@ -478,15 +520,17 @@ __global__ void __launch_bounds__(IB_THREADS, 2) dsa_indexer_bwd_kernel(const Ib
       cp_async_commit();
     }
     for (int c = 0; c < nchunks; ++c) {
-      if (!mbar_wait_w(&bar_k_empty, (c & 1) ^ 1, ac)) break;
+      const int b = c & 1;
+      // buffer b was last read by the MMAs of chunk c - 2
+      if (!mbar_wait_w(&bar_k_empty[b], ((c >> 1) & 1) ^ 1, ac)) break;
       const int slot = c * IB_NK + pt;
       const int j = slot < a.K ? __ldg(irow + slot) : -1;
       const bool valid = j >= 0 && j < a.T;
       if (!valid && j != -1 && a.err) atomicOr(a.err, ATTN_DEVERR_INDEX_RANGE);
       const int jr = valid ? j : -1;
-      s_row[c & 3][pt] = jr;
+      s_row[c & 7][pt] = jr;
       s_g[c & 1][pt] = valid ? __ldg(grow + slot) : 0.f;
-      const uint32_t base = smem_u32(sK);
+      const uint32_t base = smem_u32(sK + b * IB_K_BYTES);
       const int rw = pt & ~31;
 #pragma unroll
       for (int kk = 0; kk < IB_D / 8; ++kk) {    // 32 rows x 16 chunks / 32 lanes
@@ -502,7 +546,7 @@ __global__ void __launch_bounds__(IB_THREADS, 2) dsa_indexer_bwd_kernel(const Ib
       cp_async_wait<0>();
       fence_proxy_async_smem();
       if (c == 0) mbar_arrive(&bar_in);
-      mbar_arrive(&bar_k_full);
+      mbar_arrive(&bar_k_full[b]);
     }
     cp_async_wait<0>();
   } else if (warp == 10) {
@@ -512,14 +556,15 @@ __global__ void __launch_bounds__(IB_THREADS, 2) dsa_indexer_bwd_kernel(const Ib
       const uint32_t idQ = idesc_bf16(128, IB_HB, true, false);       // dQ^T (dims x heads)
       const uint32_t idK = idesc_bf16(64, 64, true, true);            // dK pieces (slots x dims)
       const uint64_t dQk = desc_kmajor_base(smem_u32(sQ));
-      const uint64_t dKk = desc_kmajor_base(smem_u32(sK));
       const uint64_t ddZk = desc_kmajor_base(smem_u32(sdZ));
       const uint64_t ddZmn = desc_mnmajor_base(smem_u32(sdZ), IB_HB);
-      const uint64_t dKmn = desc_mnmajor_base(smem_u32(sK), IB_NK);
       bool ok = mbar_wait_w(&bar_in, 0, ac);
       int gp = 0;
       for (int c = 0; ok && c < nchunks; ++c) {
-        if (!mbar_wait_w(&bar_k_full, c & 1, ac)) { ok = false; break; }
+        const int b = c & 1;
+        const uint64_t dKk = desc_kmajor_base(smem_u32(sK + b * IB_K_BYTES));
+        const uint64_t dKmn = desc_mnmajor_base(smem_u32(sK + b * IB_K_BYTES), IB_NK);
+        if (!mbar_wait_w(&bar_k_full[b], (c >> 1) & 1, ac)) { ok = false; break; }
         if (c > 0 && !mbar_wait_w(&bar_z_free, (c - 1) & 1, ac)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
@@ -535,7 +580,7 @@ __global__ void __launch_bounds__(IB_THREADS, 2) dsa_indexer_bwd_kernel(const Ib
           umma_ss_w(tmem + IB_COL_DQ, desc_advance(dKmn, mnmajor_step_bytes(kk)),
                     desc_advance(ddZk, kmajor_step_bytes(IB_HB, kk)), idQ,
                     (c > 0 || kk > 0) ? 1u : 0u);
-        umma_commit_w(&bar_k_empty);             // the key rows of this chunk are no longer read
+        umma_commit_w(&bar_k_empty[b]);          // the key rows of this chunk are no longer read
         // dK pieces: D(slots, dims 64p..) = dZ^T(slots, heads) Q_p(heads, dims)
         for (int p = 0; p < IB_D / 64; ++p, ++gp) {
           const int b = gp & 1, use = gp >> 1;
@@ -573,7 +618,7 @@ __global__ void __launch_bounds__(IB_THREADS, 2) dsa_indexer_bwd_kernel(const Ib
         tmem_wait_ld();
         tc_fence_before();
         mbar_arrive(&bar_pc_free[b]);
-        const int j = active ? s_row[c & 3][slot] : -1;
+        const int j = active ? s_row[c & 7][slot] : -1;
         if (j >= 0) {
           float* dst = a.dk_acc + static_cast<size_t>(j) * IB_D + 64 * p;
 #pragma unroll
@@ -594,7 +639,7 @@ __global__ void __launch_bounds__(IB_THREADS, 2) dsa_indexer_bwd_kernel(const Ib
     float dw = 0.f;
     for (int c = 0; ok && c < nchunks; ++c) {
       if (!mbar_wait(&bar_z_full, c & 1, ac)) { ok = false; break; }
-      if (!mbar_wait(&bar_k_full, c & 1, ac)) { ok = false; break; }   // slot gradients of the chunk
+      if (!mbar_wait(&bar_k_full[c & 1], (c >> 1) & 1, ac)) { ok = false; break; }   // slot gradients
       tc_fence_after();
       uint32_t uz[64];
       tmem_ld32_nowait(tmem + lane_base + IB_COL_Z, uz);

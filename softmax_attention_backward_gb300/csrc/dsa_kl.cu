@@ -4,14 +4,16 @@
 //
 // One CTA per token.  The token's query heads load once per 64-head block; its
 // key rows are gathered 64 slots at a time (16-byte cp.async into the SW128
-// K-major layout, as in the sparse attention kernels) and S = Q K^T runs on
-// tcgen05 (M = 64 heads, N = 64 slots, K = 576).  Four warps turn S into the
-// attention probabilities P = exp(scale S - lse) with the forward's lse, stage
-// them in shared memory, and 64 threads add each slot's column over the heads:
-// the target of the chunk, accumulated in shared memory over the head blocks.
-// Nothing of size heads x slots leaves the chip.  After the last chunk the
-// whole CTA forms the softmax of the scores over the valid slots, the loss and
-// its gradient.
+// K-major layout, as in the sparse attention kernels) into two chunk buffers,
+// so the gather of one chunk overlaps the MMA of the other, and S = Q K^T runs
+// on tcgen05 (M = 64 heads, N = 64 slots, K = 576) into two TMEM buffers.  Four
+// warps turn S into the attention probabilities P = exp(scale S - lse) with the
+// forward's lse and sum each slot's column over their heads with a
+// reduce-scatter of warp shuffles; the four warps' sums meet in shared memory
+// and the per-slot total (summed over the head blocks) is kept in the token's
+// row of `grad` until the end.  Nothing of size heads x slots leaves the chip.
+// After the last chunk the whole CTA forms the softmax of the scores over the
+// valid slots, the loss and its gradient (which replaces the kept sums).
 #include <cuda_runtime.h>
 
 #include "dsa.h"
@@ -24,13 +26,10 @@ constexpr int KL_HB = 64;                       // heads per block
 constexpr int KL_NK = 64;                       // slots per chunk
 constexpr int KL_DQK = 576;
 constexpr int KL_Q_BYTES = KL_HB * KL_DQK * 2;  // 72 KB
-constexpr int KL_KV_BYTES = KL_NK * KL_DQK * 2; // 72 KB
-constexpr int KL_MAXK = 8192;                   // slots held in shared memory
-constexpr int KL_P_STRIDE = KL_NK + 1;          // fp32 P staging row stride (conflict-free)
-constexpr int KL_P_BYTES = KL_HB * KL_P_STRIDE * 4;
-constexpr int KL_SMEM = KL_Q_BYTES + KL_KV_BYTES + KL_P_BYTES + KL_MAXK * 4 + 1024;
+constexpr int KL_KV_BYTES = KL_NK * KL_DQK * 2; // 72 KB per chunk buffer
+constexpr int KL_SMEM = KL_Q_BYTES + 2 * KL_KV_BYTES + 1024;
 constexpr int KL_THREADS = 224;                 // 0..3 softmax / target, 4..5 gather, 6 MMA
-constexpr uint32_t KL_TMEM_COLS = 64;
+constexpr uint32_t KL_TMEM_COLS = 128;          // two S buffers of 64 columns
 
 struct KlArgs {
   const __nv_bfloat16* q;
@@ -65,17 +64,37 @@ __device__ __forceinline__ float block_reduce(float v, float* s_red, bool is_max
   return r;
 }
 
+// Sum of v over the 32 lanes of the warp, per column, spread over the lanes:
+// five halving rounds (each lane keeps one half of its columns and adds the
+// partner's copy of that half), after which lane l holds the sums of columns
+// col0(l) and col0(l) + 1.
+__device__ __forceinline__ void column_sums(float (&v)[64], int lane) {
+#pragma unroll
+  for (int o = 16, hs = 32; o >= 1; o >>= 1, hs >>= 1) {
+    const bool up = lane & o;
+#pragma unroll
+    for (int i = 0; i < hs; ++i) {
+      const float send = up ? v[i] : v[i + hs];
+      const float keep = up ? v[i + hs] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+    }
+  }
+}
+__device__ __forceinline__ int col0_of_lane(int lane) {
+  return ((lane >> 4) & 1) * 32 + ((lane >> 3) & 1) * 16 + ((lane >> 2) & 1) * 8 +
+         ((lane >> 1) & 1) * 4 + (lane & 1) * 2;
+}
+
 __global__ void __launch_bounds__(KL_THREADS, 1) dsa_sparse_kl_kernel(const KlArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   uint8_t* sQ = smem;
-  uint8_t* sKV = sQ + KL_Q_BYTES;
-  float* sP = reinterpret_cast<float*>(sKV + KL_KV_BYTES);     // P of one chunk, [head][slot]
-  float* s_tgt = sP + KL_HB * KL_P_STRIDE;                     // per slot: sum of P over heads
-  __shared__ uint64_t bar_kv_full, bar_kv_empty, bar_s_full, bar_s_free;
+  uint8_t* sKV = sQ + KL_Q_BYTES;               // two chunk buffers
+  __shared__ uint64_t bar_kv_full[2], bar_kv_empty[2], bar_s_full[2], bar_s_free[2];
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_flag;
+  __shared__ float s_col[4][KL_NK];             // per softmax warp: column sums of its rows
   __shared__ float s_red[KL_THREADS / 32];
   __shared__ int s_last[KL_THREADS / 32];
 
@@ -83,6 +102,7 @@ __global__ void __launch_bounds__(KL_THREADS, 1) dsa_sparse_kl_kernel(const KlAr
   const int warp = warp_id(), lane = lane_id();
   AbortCtx ac{&abort_flag, a.err};
   const int32_t* irow = a.idx + static_cast<size_t>(t) * a.K;
+  float* grow = a.grad + static_cast<size_t>(t) * a.K;   // holds the head sums until the end
   const int nhb = (a.H + KL_HB - 1) / KL_HB;
 
   int nchunks;
@@ -91,17 +111,18 @@ __global__ void __launch_bounds__(KL_THREADS, 1) dsa_sparse_kl_kernel(const KlAr
     for (int s = threadIdx.x; s < a.K; s += KL_THREADS) {
       const int j = __ldg(irow + s);
       if (j >= 0 && j < a.T) last = s;
-      s_tgt[s] = 0.f;
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) last = max(last, __shfl_xor_sync(0xffffffffu, last, off));
     if (lane == 0) s_last[warp] = last;
     if (threadIdx.x == 0) {
       abort_flag = 0;
-      mbar_init(&bar_kv_full, 64);
-      mbar_init(&bar_kv_empty, 1);
-      mbar_init(&bar_s_full, 1);
-      mbar_init(&bar_s_free, 128);
+      for (int b = 0; b < 2; ++b) {
+        mbar_init(&bar_kv_full[b], 64);
+        mbar_init(&bar_kv_empty[b], 1);
+        mbar_init(&bar_s_full[b], 1);
+        mbar_init(&bar_s_free[b], 128);
+      }
       fence_mbar_init();
     }
     if (warp == 6) tmem_alloc(&tmem_base_sh, KL_TMEM_COLS);
@@ -119,10 +140,12 @@ __global__ void __launch_bounds__(KL_THREADS, 1) dsa_sparse_kl_kernel(const KlAr
     // ---------------- producers: a head block's queries, then the chunks ----------------
     const int pt = threadIdx.x - 128;            // 0..63
     for (int st = 0; st < steps; ++st) {
-      const int hb = st / nchunks, c = st % nchunks;
-      // the single buffers were last read by the S of the previous step
-      if (!mbar_wait_w(&bar_kv_empty, (st & 1) ^ 1, ac)) break;
+      const int hb = st / nchunks, c = st % nchunks, b = st & 1;
+      // buffer b was last read by the S of step st - 2
+      if (!mbar_wait_w(&bar_kv_empty[b], ((st >> 1) & 1) ^ 1, ac)) break;
       if (c == 0) {
+        // a new head block replaces Q: the S of step st - 1 must be done too
+        if (st > 0 && !mbar_wait_w(&bar_kv_empty[(st - 1) & 1], ((st - 1) >> 1) & 1, ac)) break;
         const int h0 = hb * KL_HB, nh = min(KL_HB, a.H - h0);
         const __nv_bfloat16* qb = a.q + (static_cast<size_t>(t) * a.H + h0) * KL_DQK;
         for (int id = pt; id < KL_HB * (KL_DQK / 8); id += 64) {
@@ -138,7 +161,7 @@ __global__ void __launch_bounds__(KL_THREADS, 1) dsa_sparse_kl_kernel(const KlAr
       const bool valid = j >= 0 && j < a.T;
       if (hb == 0 && !valid && j != -1 && a.err) atomicOr(a.err, ATTN_DEVERR_INDEX_RANGE);
       const int jr = valid ? j : -1;
-      const uint32_t base = smem_u32(sKV);
+      const uint32_t base = smem_u32(sKV + b * KL_KV_BYTES);
       const int rw = pt & ~31;
 #pragma unroll
       for (int k = 0; k < KL_DQK / 8; ++k) {   // 32 rows x 72 columns / 32 lanes
@@ -153,25 +176,26 @@ __global__ void __launch_bounds__(KL_THREADS, 1) dsa_sparse_kl_kernel(const KlAr
       cp_async_commit();
       cp_async_wait<0>();
       fence_proxy_async_smem();
-      mbar_arrive(&bar_kv_full);
+      mbar_arrive(&bar_kv_full[b]);
     }
     cp_async_wait<0>();
   } else if (warp == 6) {
-    // ---------------- MMA issuer: S = Q K^T per step ----------------
+    // ---------------- MMA issuer: S = Q K^T per step, two TMEM buffers ----------------
     const uint32_t idS = idesc_bf16(64, KL_NK, false, false);
     const uint64_t dQk = desc_kmajor_base(smem_u32(sQ));
-    const uint64_t dKk = desc_kmajor_base(smem_u32(sKV));
     bool ok = true;
     for (int st = 0; ok && st < steps; ++st) {
-      if (!mbar_wait_w(&bar_kv_full, st & 1, ac)) { ok = false; break; }
-      if (st > 0 && !mbar_wait_w(&bar_s_free, (st - 1) & 1, ac)) { ok = false; break; }
+      const int b = st & 1;
+      if (!mbar_wait_w(&bar_kv_full[b], (st >> 1) & 1, ac)) { ok = false; break; }
+      if (!mbar_wait_w(&bar_s_free[b], ((st >> 1) & 1) ^ 1, ac)) { ok = false; break; }
       tc_fence_after();
+      const uint64_t dKk = desc_kmajor_base(smem_u32(sKV + b * KL_KV_BYTES));
 #pragma unroll 4
       for (int kk = 0; kk < KL_DQK / 16; ++kk)
-        umma_ss_w(tmem, desc_advance(dQk, kmajor_step_bytes(KL_HB, kk)),
+        umma_ss_w(tmem + b * KL_NK, desc_advance(dQk, kmajor_step_bytes(KL_HB, kk)),
                   desc_advance(dKk, kmajor_step_bytes(KL_NK, kk)), idS, kk > 0 ? 1u : 0u);
-      umma_commit_w(&bar_s_full);
-      umma_commit_w(&bar_kv_empty);
+      umma_commit_w(&bar_s_full[b]);
+      umma_commit_w(&bar_kv_empty[b]);
     }
   } else if (warp < 4) {
     // ---------------- P and the per-slot sums over the heads ----------------
@@ -179,9 +203,10 @@ __global__ void __launch_bounds__(KL_THREADS, 1) dsa_sparse_kl_kernel(const KlAr
     const bool active = lane < 16;
     const int row = 16 * qq + (lane & 15);       // head row of the block held by this lane
     const uint32_t lane_base = static_cast<uint32_t>(32 * qq) << 16;
+    const int col0 = col0_of_lane(lane);
     bool ok = true;
     for (int st = 0; ok && st < steps; ++st) {
-      const int hb = st / nchunks, c = st % nchunks;
+      const int hb = st / nchunks, c = st % nchunks, b = st & 1;
       const int h = hb * KL_HB + row;
       const float lse2 = (active && h < a.H) ? __ldg(a.lse + static_cast<size_t>(t) * a.H + h) * kLog2e
                                             : INFINITY;
@@ -192,29 +217,29 @@ __global__ void __launch_bounds__(KL_THREADS, 1) dsa_sparse_kl_kernel(const KlAr
       const unsigned long long vm =
           static_cast<unsigned long long>(__ballot_sync(0xffffffffu, j0 >= 0 && j0 < a.T)) |
           (static_cast<unsigned long long>(__ballot_sync(0xffffffffu, j1 >= 0 && j1 < a.T)) << 32);
-      if (!mbar_wait(&bar_s_full, st & 1, ac)) { ok = false; break; }
+      if (!mbar_wait(&bar_s_full[b], (st >> 1) & 1, ac)) { ok = false; break; }
       tc_fence_after();
       uint32_t us[64];
-      tmem_ld32_nowait(tmem + lane_base, us);
-      tmem_ld32_nowait(tmem + lane_base + 32, us + 32);
+      tmem_ld32_nowait(tmem + lane_base + b * KL_NK, us);
+      tmem_ld32_nowait(tmem + lane_base + b * KL_NK + 32, us + 32);
       tmem_wait_ld();
       tc_fence_before();
-      mbar_arrive(&bar_s_free);
-      if (active) {
+      mbar_arrive(&bar_s_free[b]);
+      float pv[64];
 #pragma unroll
-        for (int cc = 0; cc < 64; ++cc) {
-          float p = ex2(fmaf(__uint_as_float(us[cc]), a.scale_log2, -lse2));
-          if (!((vm >> cc) & 1ull) || !(lse2 < INFINITY)) p = 0.f;
-          sP[row * KL_P_STRIDE + cc] = p;
-        }
+      for (int cc = 0; cc < 64; ++cc) {
+        const float p = ex2(fmaf(__uint_as_float(us[cc]), a.scale_log2, -lse2));
+        pv[cc] = (active && ((vm >> cc) & 1ull) && lse2 < INFINITY) ? p : 0.f;
       }
+      column_sums(pv, lane);
+      s_col[qq][col0] = pv[0];
+      s_col[qq][col0 + 1] = pv[1];
       named_bar_sync(1, 128);
       if (threadIdx.x < KL_NK) {
-        float sum = 0.f;
-#pragma unroll 8
-        for (int r = 0; r < KL_HB; ++r) sum += sP[r * KL_P_STRIDE + threadIdx.x];
+        const float sum = s_col[0][threadIdx.x] + s_col[1][threadIdx.x] + s_col[2][threadIdx.x] +
+                          s_col[3][threadIdx.x];
         const int slot = c * KL_NK + threadIdx.x;
-        if (slot < a.K) s_tgt[slot] += sum;
+        if (slot < a.K) grow[slot] = hb == 0 ? sum : grow[slot] + sum;
       }
       named_bar_sync(1, 128);
     }
@@ -240,13 +265,12 @@ __global__ void __launch_bounds__(KL_THREADS, 1) dsa_sparse_kl_kernel(const KlAr
   z = block_reduce(z, s_red, false);
   const float lnz = mx + logf(z);
   float part = 0.f;
-  float* grow = a.grad + static_cast<size_t>(t) * a.K;
   float* trow = a.target ? a.target + static_cast<size_t>(t) * a.K : nullptr;
   for (int s = threadIdx.x; s < a.K; s += KL_THREADS) {
     const int j = __ldg(irow + s);
     float g = 0.f, p = 0.f;
-    if (ok && j >= 0 && j < a.T) {
-      p = s_tgt[s] * inv_h;
+    if (ok && j >= 0 && j < a.T && s < nchunks * KL_NK) {
+      p = grow[s] * inv_h;
       const float lr = __ldg(srow + s) - lnz;
       g = expf(lr) - p;
       if (p > 0.f) part += p * (logf(p) - lr);
@@ -281,7 +305,6 @@ extern "C" attn_status_t dsa_sparse_kl(const sparse_attn_problem_t* p, const voi
   if (p->dim_qk != KL_DQK || p->dim_v != 512) return ATTN_ERR_UNSUPPORTED;
   if (p->heads != 16 && p->heads != 32 && p->heads != 64 && p->heads != 128)
     return ATTN_ERR_UNSUPPORTED;
-  if (p->topk > KL_MAXK) return ATTN_ERR_UNSUPPORTED;
   if (static_cast<int64_t>(p->tokens) * p->heads * KL_DQK >= (int64_t(1) << 31) ||
       static_cast<int64_t>(p->tokens) * p->topk >= (int64_t(1) << 31))
     return ATTN_ERR_UNSUPPORTED;

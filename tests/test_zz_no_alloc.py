@@ -1,11 +1,13 @@
 """attn_bwd_fixed_scratch: the backward for callers that cannot allocate
 device memory (its Delta and dQ accumulator sit in a static array the library
-owns).  Checked through the C ABI against the regular workspace-based backward,
-on two calls in a row so that leftovers of the first call in the shared array
-cannot leak into the second.  This file is collected last on purpose."""
+owns).  Checked through the C ABI against the regular workspace-based backward
+and against the fp64 oracle, on two calls in a row so that leftovers of the
+first call in the shared array cannot leak into the second.  This file is
+collected last on purpose."""
 import pytest
 import torch
 
+import oracle
 import softmax_attention_backward_gb300 as A
 from softmax_attention_backward_gb300 import workloads as W
 from _util import assert_close
@@ -34,6 +36,10 @@ def test_fixed_scratch_matches_workspace_backward_twice(B, S, hq, hkv, D, causal
         assert int(err.item()) == 0
         for name, g, r in zip(("dq", "dk", "dv"), got, ref):
             assert_close(f"call {call} {name}", g, r.double().cpu())
+        # and directly against the fp64 oracle on the same inputs
+        o64 = oracle.dense_backward(q.cpu(), k.cpu(), v.cpu(), do.cpu(), scale, causal)
+        for name, g in zip(("dq", "dk", "dv"), got):
+            assert_close(f"call {call} {name} vs oracle", g, o64[name])
 
 
 def test_fixed_scratch_thd_and_capacity_limit():

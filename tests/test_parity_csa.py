@@ -120,3 +120,51 @@ def test_csa_inconsistent_layout_is_flagged():
                                 sub["cu_seqlens"], sub["cu_seqlens_comp"], 4, 2, 6)
     assert_close("out[seg 1]", got["out"][9:15], ref["out"])
     assert_close("dkv[seg 1]", got["dkv"][40:64], ref["dkv"])
+
+
+def test_csa_graph_replay_follows_device_side_lengths():
+    """Forward and backward captured in a CUDA graph over a static capacity;
+    replaying after new cu_seqlens / cu_seqlens_comp contents are copied into
+    the captured buffers gives the oracle's result for the new layout (the
+    library never reads the lengths on the host)."""
+    cap_t, cap_c, D = 160, 40, 128
+    first, second = [64, 30, 17], [9, 100, 40]
+    x = W.csa_inputs([cap_t], D, 4, 2, seed=11)
+    g = {n: x[n].to(DEV) for n in ("kv", "score", "ape")}
+    dout = torch.randn(cap_c, D, generator=torch.Generator().manual_seed(2)).to(torch.bfloat16).to(DEV)
+    cu = W.cu_seqlens_from(first).to(DEV)
+    cc = W.cu_seqlens_from([n // 4 for n in first]).to(DEV)
+    out = torch.empty(cap_c, D, dtype=torch.bfloat16, device=DEV)
+    dkv, dsc = torch.empty_like(g["kv"]), torch.empty_like(g["score"])
+    dape = torch.empty_like(g["ape"])
+    n = A.csa_compressor_bwd_workspace_size(g["kv"], cu, cc, comp_capacity=cap_c)
+    ws = torch.empty(n, dtype=torch.uint8, device=DEV)
+
+    def step(stream=None):
+        A.csa_compressor_fwd(g["kv"], g["score"], g["ape"], cu, cc, comp_capacity=cap_c, out=out,
+                             stream=stream)
+        A.csa_compressor_bwd(g["kv"], g["score"], g["ape"], dout, cu, cc, workspace=ws, dkv=dkv,
+                             dscore=dsc, dape=dape, stream=stream)
+
+    step()
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(graph, stream=s):
+            step(stream=s)
+    torch.cuda.synchronize()
+    for lens in (second, first):
+        cu.copy_(W.cu_seqlens_from(lens).to(DEV))
+        cc.copy_(W.cu_seqlens_from([m // 4 for m in lens]).to(DEV))
+        graph.replay()
+        torch.cuda.synchronize()
+        ref = C.compressor_backward(x["kv"], x["score"], x["ape"], dout.cpu(),
+                                    W.cu_seqlens_from(lens),
+                                    W.cu_seqlens_from([m // 4 for m in lens]), 4, 2, cap_c)
+        assert_close("out", out, ref["out"])
+        assert_close("dkv", dkv, ref["dkv"])
+        assert_close("dscore", dsc, ref["dscore"])
+        err = (dape.double().cpu() - ref["dape"]).abs().max().item()
+        assert err <= DAPE_REL * ref["dape"].abs().max().item() + DAPE_ATOL

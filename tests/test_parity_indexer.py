@@ -180,3 +180,105 @@ def test_sparse_kl_topk2048_t8192_h64_sampled():
     close32("target", target[toks], p[toks], rel=1e-3, atol=1e-6)
     close32("grad", grad[toks], rg, rel=1e-3, atol=1e-6)
     close32("loss", loss[toks], rl, rel=1e-3, atol=1e-5)
+
+
+def test_outputs_fully_written_over_nan_canaries():
+    """Every element of every output is written: the buffers start as NaN (or
+    0x7f7f7f7f for the integer ones) and must end up equal to a run on zeroed
+    buffers."""
+    T, H, K = 333, 32, 100
+    x = W.indexer_inputs(T, H, seed=77, topk=K)
+    q, k, w, g = (x[n].to(DEV) for n in ("q", "k", "w", "grad"))
+    ld = A.logits_ld(T)
+
+    def run(fill_f, fill_i):
+        logits = torch.full((T, ld), fill_f, dtype=torch.float32, device=DEV)
+        A.dsa_indexer_fwd(q, k, w, logits=logits)
+        idx = torch.full((T, K), fill_i, dtype=torch.int32, device=DEV)
+        length = torch.full((T,), fill_i, dtype=torch.int32, device=DEV)
+        scores = torch.full((T, K), fill_f, dtype=torch.float32, device=DEV)
+        A.dsa_topk(logits, K, heads=H, idx=idx, length=length, scores=scores)
+        dq = torch.full_like(q, fill_f)
+        dk = torch.full_like(k, fill_f)
+        dw = torch.full_like(w, fill_f)
+        A.dsa_indexer_bwd(q, k, w, idx, g, dq=dq, dk=dk, dw=dw)
+        torch.cuda.synchronize()
+        return logits[:, :T], idx, length, scores, dq, dk, dw
+
+    a = run(float("nan"), 0x7F7F7F7F)
+    b = run(0.0, 0)
+    for n, x1, x2 in zip(("logits", "idx", "length", "scores", "dq", "dk", "dw"), a, b):
+        assert torch.equal(x1, x2), f"{n}: an element was left unwritten"
+
+
+def test_sparse_kl_outputs_fully_written():
+    T, H, K = 100, 64, 80
+    qa, kv, _, idx = W.sparse_inputs(T, H, K, seed=5)
+    gq, gkv, gidx = qa.to(DEV), kv.to(DEV), idx.to(DEV)
+    _, lse = A.sparse_attn_fwd(gq, gkv, gidx)
+    sc = torch.randn(T, K, generator=torch.Generator().manual_seed(1)).to(DEV)
+    outs = []
+    for fill in (float("nan"), 0.0):
+        loss = torch.full((T,), fill, device=DEV)
+        grad = torch.full((T, K), fill, device=DEV)
+        tgt = torch.full((T, K), fill, device=DEV)
+        A.dsa_sparse_kl(gq, gkv, lse, gidx, sc, loss=loss, grad=grad, target=tgt)
+        torch.cuda.synchronize()
+        outs.append((loss, grad, tgt))
+    for x1, x2 in zip(*outs):
+        assert torch.equal(x1, x2)
+
+
+def test_indexer_chain_in_a_cuda_graph():
+    """logits -> top-k -> sparse attention -> KL -> indexer backward captured in
+    one CUDA graph: replays reproduce the eager results, and a replay after new
+    inputs are copied into the captured buffers follows them (no host reads,
+    no allocation inside the calls)."""
+    T, H, K, HA = 256, 64, 64, 16
+    x = W.indexer_inputs(T, H, seed=3, topk=K)
+    qa, kv, _, _ = W.sparse_inputs(T, HA, 1, seed=4)
+    q, k, w = (x[n].to(DEV) for n in ("q", "k", "w"))
+    gqa, gkv = qa.to(DEV), kv.to(DEV)
+    logits = torch.empty(T, A.logits_ld(T), device=DEV)
+    idx = torch.empty(T, K, dtype=torch.int32, device=DEV)
+    length = torch.empty(T, dtype=torch.int32, device=DEV)
+    scores = torch.empty(T, K, device=DEV)
+    o = torch.empty(T, HA, 512, dtype=torch.bfloat16, device=DEV)
+    lse = torch.empty(T, HA, device=DEV)
+    loss = torch.empty(T, device=DEV)
+    grad = torch.empty(T, K, device=DEV)
+    dq, dk, dw = torch.empty_like(q), torch.empty_like(k), torch.empty_like(w)
+    ws = torch.empty(T * 128 * 4, dtype=torch.uint8, device=DEV)
+
+    def chain(stream=None):
+        A.dsa_indexer_fwd(q, k, w, logits=logits, stream=stream)
+        A.dsa_topk(logits, K, heads=H, idx=idx, length=length, scores=scores, stream=stream)
+        A.sparse_attn_fwd(gqa, gkv, idx, out=o, lse=lse, stream=stream)
+        A.dsa_sparse_kl(gqa, gkv, lse, idx, scores, loss=loss, grad=grad, stream=stream)
+        A.dsa_indexer_bwd(q, k, w, idx, grad, workspace=ws, dq=dq, dk=dk, dw=dw, stream=stream)
+
+    chain()
+    torch.cuda.synchronize()
+    eager = [t.clone() for t in (logits, idx, loss, grad, dq, dw)]
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(graph, stream=s):
+            chain(stream=s)
+    torch.cuda.synchronize()
+    graph.replay()
+    torch.cuda.synchronize()
+    for n, e, t in zip(("logits", "idx", "loss", "grad", "dq", "dw"), eager,
+                       (logits, idx, loss, grad, dq, dw)):
+        if n in ("logits", "idx"):
+            assert torch.equal(e, t), n
+        else:
+            torch.testing.assert_close(t, e, rtol=1e-5, atol=1e-6)
+    # new query weights: the replay follows them
+    x2 = W.indexer_inputs(T, H, seed=8, topk=K)
+    w.copy_(x2["w"].to(DEV))
+    graph.replay()
+    torch.cuda.synchronize()
+    ref = X.indexer_logits(x["q"], x["k"], x2["w"])
+    check_logits(logits[:, :T].cpu(), ref)

@@ -208,7 +208,13 @@ def test_outputs_fully_written_over_nan_canaries():
     a = run(float("nan"), 0x7F7F7F7F)
     b = run(0.0, 0)
     for n, x1, x2 in zip(("logits", "idx", "length", "scores", "dq", "dk", "dw"), a, b):
-        assert torch.equal(x1, x2), f"{n}: an element was left unwritten"
+        if n == "dk":
+            # summed with fp32 atomics: every element written (finite), equal up to the
+            # order of the additions
+            assert torch.isfinite(x1.float()).all(), "dk: an element was left unwritten"
+            torch.testing.assert_close(x1.float(), x2.float(), rtol=2e-2, atol=2e-2)
+        else:
+            assert torch.equal(x1, x2), f"{n}: an element was left unwritten"
 
 
 def test_sparse_kl_outputs_fully_written():

@@ -12,8 +12,7 @@
 // wholly after the query tile only write -inf.
 //
 // dsa_topk_kernel: one CTA per row; the visible part of the row is loaded
-// into registers (16 contiguous keys per thread) as order-preserving 32-bit
-// keys and the k-th largest is
+// into shared memory as order-preserving 32-bit keys and the k-th largest is
 // found by up to four 8-bit radix passes (warp-aggregated histogram atomics, a
 // warp-parallel digit pick, and an early stop once a digit's bin holds exactly
 // the keys still needed); the selected positions (ties toward the smaller
@@ -250,19 +249,13 @@ __global__ void __launch_bounds__(IX_THREADS, 1)
 // Top-k selection
 // ---------------------------------------------------------------------------
 constexpr int TK_THREADS = 512;
-constexpr int TK_MAXN = 8192;                   // visible keys of a row (in registers)
+constexpr int TK_MAXN = 8192;                   // visible keys held in shared memory per pass
 
 // Order-preserving key of a float (larger float -> larger key); NaN -> 0.
 __device__ __forceinline__ uint32_t order_key(float v) {
   const uint32_t b = __float_as_uint(v);
   if (v != v) return 0u;
   return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
-}
-
-// The float of an order-preserving key (exact for every non-NaN value; a NaN,
-// whose key is 0, comes back as a NaN).
-__device__ __forceinline__ float key_value(uint32_t k) {
-  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
 }
 
 // Exclusive block-wide prefix sum of one value per thread (TK_THREADS threads);
@@ -293,11 +286,10 @@ __device__ __forceinline__ int block_excl_scan(int v, int* s_warp, int& total) {
   return base + x - v;
 }
 
-constexpr int TK_PER = TK_MAXN / TK_THREADS;     // keys per thread (16, contiguous)
-
-__global__ void __launch_bounds__(TK_THREADS, 2) dsa_topk_kernel(const IxArgs a, int K,
+__global__ void __launch_bounds__(TK_THREADS) dsa_topk_kernel(const IxArgs a, int K,
                                                              int32_t* idx, int32_t* length,
                                                              float* scores) {
+  __shared__ uint32_t s_key[TK_MAXN];
   __shared__ int s_hist[256];
   __shared__ int s_warp[TK_THREADS / 32];
   __shared__ uint32_t s_sel[3];                 // digit chosen, keys still needed, its bin count
@@ -308,51 +300,35 @@ __global__ void __launch_bounds__(TK_THREADS, 2) dsa_topk_kernel(const IxArgs a,
   const int n = any ? t - lo + 1 : 0;
   int32_t* irow = idx + static_cast<size_t>(t) * K;
   float* srow = scores + static_cast<size_t>(t) * K;
-  const float* lrow = a.logits + static_cast<size_t>(t) * a.ld + lo;
+  const float* lrow = a.logits + static_cast<size_t>(t) * a.ld;
   if (n <= K) {
     for (int i = threadIdx.x; i < K; i += TK_THREADS) {
       irow[i] = i < n ? lo + i : -1;
-      srow[i] = i < n ? lrow[i] : -INFINITY;
+      srow[i] = i < n ? lrow[lo + i] : -INFINITY;
     }
     if (threadIdx.x == 0) length[t] = n;
     return;
   }
-  // n > K (n <= T <= TK_MAXN): this thread's keys i0 .. i0 + 15 of the visible
-  // part of the row, held in registers for every pass
-  const int i0 = threadIdx.x * TK_PER;
-  float v[TK_PER];
-  if ((lo & 3) == 0 && i0 + TK_PER <= n) {
-#pragma unroll
-    for (int j = 0; j < TK_PER; j += 4) {
-      const float4 x = __ldg(reinterpret_cast<const float4*>(lrow + i0 + j));
-      v[j] = x.x; v[j + 1] = x.y; v[j + 2] = x.z; v[j + 3] = x.w;
-    }
-  } else {
-#pragma unroll
-    for (int j = 0; j < TK_PER; ++j) v[j] = i0 + j < n ? __ldg(lrow + i0 + j) : 0.f;
-  }
-  uint32_t u[TK_PER];
-  unsigned live = 0;                            // bit j: key j exists
-#pragma unroll
-  for (int j = 0; j < TK_PER; ++j) {
-    u[j] = order_key(v[j]);                     // v is not kept: key_value() inverts the map
-    if (i0 + j < n) live |= 1u << j;
-  }
-  // Radix select of the K-th largest key, 8 bits per pass from the top; a pass
+  // n > K (n <= T <= TK_MAXN): keys of the visible part of the row
+  for (int i = threadIdx.x; i < n; i += TK_THREADS) s_key[i] = order_key(lrow[lo + i]);
+  // Radix select of the K-th largest key, 8 bits per pass from the top.  A pass
   // stops the search early when the chosen digit's bin holds exactly the keys
-  // still needed (then the whole prefix class is taken).
+  // still needed: then every key of that prefix class is taken.
   uint32_t prefix = 0, pmask = 0;
-  int remaining = K;
+  int remaining = K;                            // keys still to take inside the prefix class
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   for (int shift = 24; shift >= 0; shift -= 8) {
     for (int i = threadIdx.x; i < 256; i += TK_THREADS) s_hist[i] = 0;
     __syncthreads();
-    // lanes holding the same digit add once (the top digits of a row take few
-    // distinct values)
-#pragma unroll
-    for (int j = 0; j < TK_PER; ++j) {
-      const bool in = ((live >> j) & 1u) && (u[j] & pmask) == prefix;
-      const int dg = in ? static_cast<int>((u[j] >> shift) & 0xFF) : -1;
+    // histogram of the next digit within the prefix class; lanes holding the
+    // same digit add once (the top digits of a row take few distinct values)
+    for (int i0 = 0; i0 < n; i0 += TK_THREADS) {
+      const int i = i0 + threadIdx.x;
+      int dg = -1;
+      if (i < n) {
+        const uint32_t u = s_key[i];
+        if ((u & pmask) == prefix) dg = static_cast<int>((u >> shift) & 0xFF);
+      }
       const unsigned peers = __match_any_sync(0xffffffffu, dg);
       if (dg >= 0 && lane == __ffs(peers) - 1) atomicAdd(&s_hist[dg], __popc(peers));
     }
@@ -372,7 +348,7 @@ __global__ void __launch_bounds__(TK_THREADS, 2) dsa_topk_kernel(const IxArgs a,
         if (lane >= o) inc += y;
       }
       const unsigned hit = __ballot_sync(0xffffffffu, inc >= remaining);
-      const int L = __ffs(hit) - 1;              // first lane reaching `remaining`
+      const int L = __ffs(hit) - 1;              // first lane reaching `remaining` (exists: total >= remaining)
       if (lane == L) {
         int before = inc - tot, d = 255 - 8 * lane - 7, c = 0;
 #pragma unroll
@@ -399,26 +375,26 @@ __global__ void __launch_bounds__(TK_THREADS, 2) dsa_topk_kernel(const IxArgs a,
   }
   // take every key whose prefix class is above `prefix` and the first
   // `remaining` keys of the class itself (smallest indices first); compact in
-  // index order: each thread's keys are contiguous, so one block scan places them
+  // index order
+  const int per = (n + TK_THREADS - 1) / TK_THREADS;
+  const int b0 = threadIdx.x * per, b1 = min(n, b0 + per);
   int n_eq = 0;
-#pragma unroll
-  for (int j = 0; j < TK_PER; ++j) n_eq += ((live >> j) & 1u) && (u[j] & pmask) == prefix;
+  for (int i = b0; i < b1; ++i) n_eq += (s_key[i] & pmask) == prefix;
   int tot_eq;
   const int eq_before = block_excl_scan(n_eq, s_warp, tot_eq);
-  unsigned take = 0;
-  int eq = eq_before;
-#pragma unroll
-  for (int j = 0; j < TK_PER; ++j) {
-    const uint32_t c = u[j] & pmask;
-    if (((live >> j) & 1u) && (c > prefix || (c == prefix && eq++ < remaining))) take |= 1u << j;
+  int n_sel = 0, eq = eq_before;
+  for (int i = b0; i < b1; ++i) {
+    const uint32_t u = s_key[i] & pmask;
+    if (u > prefix || (u == prefix && eq++ < remaining)) ++n_sel;
   }
   int tot_sel;
-  int pos = block_excl_scan(__popc(take), s_warp, tot_sel);
-#pragma unroll
-  for (int j = 0; j < TK_PER; ++j) {
-    if ((take >> j) & 1u) {
-      irow[pos] = lo + i0 + j;
-      srow[pos] = key_value(u[j]);
+  int pos = block_excl_scan(n_sel, s_warp, tot_sel);
+  eq = eq_before;
+  for (int i = b0; i < b1; ++i) {
+    const uint32_t u = s_key[i] & pmask;
+    if (u > prefix || (u == prefix && eq++ < remaining)) {
+      irow[pos] = lo + i;
+      srow[pos] = lrow[lo + i];
       ++pos;
     }
   }

@@ -188,9 +188,10 @@ attn_status_t attn_fwd(const attn_problem_t* p, const void* q, const void* k, co
   const Problem kp = to_kernel(p);
   const int D = p->head_dim;
   CUtensorMap mq, mk, mv;
+  const int bn = (D == 128) ? 64 : 128;   // key/value tile rows of the forward
   if (!make_map(&mq, q, kp.batch, kp.rows_total, kp.heads_q, D, 128) ||
-      !make_map(&mk, k, kp.batch, kp.rows_total, kp.heads_kv, D, 128) ||
-      !make_map(&mv, v, kp.batch, kp.rows_total, kp.heads_kv, D, 128))
+      !make_map(&mk, k, kp.batch, kp.rows_total, kp.heads_kv, D, bn) ||
+      !make_map(&mv, v, kp.batch, kp.rows_total, kp.heads_kv, D, bn))
     return ATTN_ERR_CUDA;
   FwdArgs a;
   a.p = kp;

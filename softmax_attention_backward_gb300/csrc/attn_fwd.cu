@@ -33,21 +33,26 @@ namespace attn {
 template <int D>
 struct FwdCfg {
   static constexpr int BM = 128;                   // rows per query tile
-  static constexpr int BN = 128;                   // rows per key/value tile
+  // rows per key/value tile: 64 for D = 128, so that S (64 columns), P (32
+  // packed columns) and O (128 columns) of both query tiles fit in TMEM with
+  // P in columns of its own
+  static constexpr int BN = (D == 128) ? 64 : 128;
   static constexpr int Q_BYTES = BM * D * 2;
   static constexpr int KV_BYTES = BN * D * 2;
-  static constexpr int NSLOT = (D == 128) ? 5 : 6; // K/V ring slots
+  static constexpr int NSLOT = (D == 128) ? 8 : 6; // K/V ring slots
   static constexpr int QBUFS = (D == 128) ? 1 : 2; // query-pair buffers (next item prefetch)
   static constexpr int SMEM = QBUFS * 2 * Q_BYTES + NSLOT * KV_BYTES + 1024;
   static constexpr int THREADS = 352;
   static constexpr uint32_t TMEM_COLS = 512;
-  static constexpr uint32_t COL_S0 = 0, COL_S1 = 128, COL_O0 = 256, COL_O1 = 256 + D;
-  // With D = 64 each tile also gets its own P region (64 packed columns), so
-  // S_w(j+1) can be computed while the softmax of tile j runs; with D = 128 P
-  // overwrites the first 64 columns of S_w.
-  static constexpr bool SEP_P = (256 + 2 * D + 2 * 64 <= 512);
-  static constexpr uint32_t COL_P0 = SEP_P ? 256 + 2 * D : COL_S0;
-  static constexpr uint32_t COL_P1 = SEP_P ? 256 + 2 * D + 64 : COL_S1;
+  // S0, S1 in columns [0, 2 BN); O0, O1 in [256, 256 + 2 D); each tile's P (BN/2
+  // packed columns) in a region of its own, so S_w(j+1) can be computed while
+  // the softmax of tile j runs: after S for D = 128, after O for D = 64.
+  static constexpr uint32_t COL_S0 = 0, COL_S1 = BN, COL_O0 = 256, COL_O1 = 256 + D;
+  static constexpr bool SEP_P = true;
+  static constexpr uint32_t COL_P0 = (D == 128) ? 2 * BN : 256 + 2 * D;
+  static constexpr uint32_t COL_P1 = COL_P0 + BN / 2;
+  static_assert(2 * BN + BN <= 256 || D != 128, "S and P of both tiles below O");
+  static_assert(256 + 2 * D <= 512 && (D == 128 || 256 + 2 * D + BN <= 512), "TMEM budget");
 };
 
 // One work item: the two 128-row query tiles m0 .. m0 + 255 of query head h;
@@ -410,9 +415,9 @@ __global__ void __launch_bounds__(352, 1)
             tmem_st32(tO + cc, r);
           }
         }
-        // P (bf16 pairs): 64 packed columns
-        tmem_st32(tP, pk);
-        tmem_st32(tP + 32, pk + 32);
+        // P (bf16 pairs): BN / 2 packed columns
+#pragma unroll
+        for (int cc = 0; cc < C::BN / 2; cc += 32) tmem_st32(tP + cc, pk + cc);
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(&bar_p[t]);

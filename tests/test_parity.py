@@ -354,3 +354,17 @@ def test_sparse_topk2048_t8192_h64_sampled():
     ref = _c5_dkv_reference()
     for c, j in enumerate(C5_ROWS):
         assert_close(f"dkv[{j}]", got["dkv"][j], ref[c])
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_thd_varlen_causal_h16_d64_persistent_sampled(mode):
+    """The c4 lengths at D = 64: 2112 forward items, so the forward and the
+    backward both run their persistent grids over THD sequences."""
+    lens = W.varlen_lengths(3)
+    cap = 32768
+    cu = W.cu_seqlens_from(lens)
+    q, k, v, do = W.thd_inputs(cap, 16, 16, 64, seed=31)
+    got = run_dense(q, k, v, do, True, 0.125, mode, cu=cu, max_seqlen=max(lens))
+    seqs = [1, 3]
+    ref = oracle.thd_backward(q, k, v, do, cu, 0.125, True, seqs=seqs)
+    compare_thd(got, ref, cu, seqs, 16, 16)

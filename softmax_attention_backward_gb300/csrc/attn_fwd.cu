@@ -21,9 +21,12 @@
 // S_w(j), [P_w(j) ready] PV_w(j), S_w(j+1), ...: MMAs from one thread execute
 // in order, so S_w(j+1) never overwrites P_w(j) before PV_w(j) has read it,
 // and a completed S_w(j+1) also means O_w holds every PV_w up to j.
-// With D = 64 the grid is persistent (one CTA per SM walking a static item
-// list, longest first): the next item's query tiles load into a second buffer
-// and its first S MMAs run while the softmax warps write out the previous O.
+// The grid is persistent (one CTA per SM walking a static item list, longest
+// first; not for THD at D = 128): the next item's query tiles load into a
+// second buffer and its first S MMAs run while the softmax warps write out the
+// previous O.  A query tile that does not reach one of the item's K/V tiles
+// still observes that tile's loads and releases their ring slots, so every
+// issuer stays within one phase of every slot.
 #include <cuda_runtime.h>
 
 #include "launch.h"
@@ -39,8 +42,8 @@ struct FwdCfg {
   static constexpr int BN = (D == 128) ? 64 : 128;
   static constexpr int Q_BYTES = BM * D * 2;
   static constexpr int KV_BYTES = BN * D * 2;
-  static constexpr int NSLOT = (D == 128) ? 8 : 6; // K/V ring slots
-  static constexpr int QBUFS = (D == 128) ? 1 : 2; // query-pair buffers (next item prefetch)
+  static constexpr int NSLOT = (D == 128) ? 5 : 6; // K/V ring slots
+  static constexpr int QBUFS = 2;                  // query-pair buffers (next item prefetch)
   static constexpr int SMEM = QBUFS * 2 * Q_BYTES + NSLOT * KV_BYTES + 1024;
   static constexpr int THREADS = 352;
   static constexpr uint32_t TMEM_COLS = 512;
@@ -217,11 +220,6 @@ __global__ void __launch_bounds__(352, 1)
           for (int pn = 0; pn < PANELS; ++pn)
             tma_load_4d(m, &bar_full[slot], dst + pn * C::BN * 128, pn * 64, hk,
                         w.seq.row0 + (i >> 1) * C::BN, w.seq.b);
-          // a query tile that does not reach this K/V tile releases the slot
-          // through the producer (this use's phase is already open), so its
-          // issuer can move on to the next item without waiting for the load
-          for (int t = 0; t < 2; ++t)
-            if ((i >> 1) >= w.n_w[t]) mbar_arrive(&bar_empty[slot]);
         }
         if (ok && q_pending) {
           if (mbar_wait(&bar_qempty[nqb], nq_par, ac)) issue_q(wn, ic + 1);
@@ -306,6 +304,21 @@ __global__ void __launch_bounds__(352, 1)
           // S(j+1) cannot overwrite P(j) (stored over S) before PV(j) read it
           for (int j = 0; ok && j < nt; ++j)
             if (!issue_s(j) || !issue_pv(j)) ok = false;
+        }
+        // K/V tiles of the item this query tile does not reach: its issuer
+        // still waits for each load and releases the slot itself.  A parity
+        // wait is only sound while the waiter is at most one phase behind;
+        // releasing skipped slots on the tile's behalf would let the ring run
+        // on, and this tile's next wait on a slot would then see a completed
+        // phase of matching parity that is not the one it waits for (found
+        // with THD sequences whose last query pair has one tile past the end).
+        for (int j = nt; ok && j < w.n_kv; ++j) {
+#pragma unroll
+          for (int kv = 0; kv < 2; ++kv) {
+            const int gi = gring + 2 * j + kv, sl = gi % C::NSLOT;
+            if (!mbar_wait_w(&bar_full[sl], (gi / C::NSLOT) & 1, ac)) { ok = false; break; }
+            if (lane_id() == 0) mbar_arrive(&bar_empty[sl]);
+          }
         }
         // the query tile is free once this tile's S MMAs have completed
         if (ok) {

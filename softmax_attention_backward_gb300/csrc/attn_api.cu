@@ -274,9 +274,8 @@ attn_status_t attn_bwd(const attn_problem_t* p, attn_dq_mode_t mode, const void*
   const Problem kp = to_kernel(p);
   const int D = p->head_dim;
   CUtensorMap mq, mk, mv, mdo;
-  const int bm = (D == 64) ? 128 : 64;
-  if (!make_map(&mq, q, kp.batch, kp.rows_total, kp.heads_q, D, bm) ||
-      !make_map(&mdo, dout, kp.batch, kp.rows_total, kp.heads_q, D, bm) ||
+  if (!make_map(&mq, q, kp.batch, kp.rows_total, kp.heads_q, D, 128) ||
+      !make_map(&mdo, dout, kp.batch, kp.rows_total, kp.heads_q, D, 128) ||
       !make_map(&mk, k, kp.batch, kp.rows_total, kp.heads_kv, D, 128) ||
       !make_map(&mv, v, kp.batch, kp.rows_total, kp.heads_kv, D, 128))
     return ATTN_ERR_CUDA;
@@ -320,7 +319,7 @@ attn_status_t attn_bwd(const attn_problem_t* p, attn_dq_mode_t mode, const void*
   const int grid = persistent ? sms : static_cast<int>(total);
   a.x_major = persistent ? 1 : 0;
   cudaError_t e = (D == 64) ? launch_attn_bwd<64>(mq, mk, mv, mdo, mdq, mdk, mdv, a, grid, st)
-                            : launch_attn_bwd<128>(mq, mk, mv, mdo, mdq, mdk, mdv, a, grid, st);
+                            : launch_attn_bwd128(mq, mk, mv, mdo, mdk, mdv, a, grid, st);
   return cuda_status(e);
 }
 

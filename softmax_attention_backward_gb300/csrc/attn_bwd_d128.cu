@@ -1,0 +1,544 @@
+// Dense / GQA / THD attention backward at head_dim 128 (the `flash_bwd` stage of
+// "[Example] Introduce split+sum template, and optimize atomic_add performance
+// for bwd examples", tile-ai/tilelang #940: atomic and split variants).
+//
+// Work item = one 128-row K/V tile of one kv head, as in the D = 64 kernel: the
+// CTA owning an item walks the 128-row query tiles of every query head of its
+// GQA group, so dK and dV stay in TMEM for the whole item and are stored once.
+// One step is a 128 x 128 (K/V rows x query rows) tile:
+//   S^T  = K Q^T    ->  P^T  = exp2(S^T c - LSE log2 e)
+//   dP^T = V dO^T   ->  dS^T = P^T o (dP^T - Delta)
+//   dV  += P^T dO,  dK += dS^T Q     (P^T, dS^T: packed bf16, TMEM A operand)
+//   dQ^T = K^T dS^T                  (dS: bf16 tile in shared memory)
+// Every GEMM has N = 128.  An SS MMA of N = 64 reads 6 KB of operands per
+// 16-deep K-step for 2^18 FLOPs, one of N = 128 reads 8 KB for 2^19, so the
+// 128-query step halves the operand traffic per FLOP that bounds the shared
+// memory, and each synchronisation covers twice the work.
+// TMEM (512 columns; lanes = K/V rows, except dQ^T whose lanes are head dims):
+//   0..127    S^T(g).  Each P/dS warpgroup owns 64 of these columns; its P pass
+//             leaves P^T in the first 32 of them and its dS pass dS^T in the
+//             last 32, both over S^T values that thread has already read.
+//   128..255  dP^T(g), then dQ^T(g) once the dS pass has read dP^T(g).
+//   256..383  dV          384..511  dK
+// MMAs issued by one thread run in order, so S^T(g+1) goes out after dK(g)
+// (the last reader of the S^T columns), and dP^T(g+1) after the drain warps
+// have read dQ^T(g) out of TMEM.
+// Shared memory: K, V (32 KB each), two Q slots, one dO slot, the dS tile
+// (32 KB each) and a 16 KB staging tile for the dQ, dK and dV copies out.
+// Warps: 0..7 P/dS (warpgroup w: query columns 64w .. 64w + 63 of every K/V
+// row), 8..15 drain (warpgroup u: dQ^T columns 64u .. 64u + 63, so all of
+// dQ^T leaves TMEM in one load; dV / dK dims 64u .. 64u + 63 at the end of an
+// item), 16 TMA, 17 MMA issuer.
+// dQ leaves through the staging tile 32 query rows at a time, as one bulk
+// reduce-add into the fp32 accumulator (ATOMIC) or one bulk store into this
+// K/V tile's slab (SPLIT).  The scale of dK is applied on the way out, that of
+// dQ in the postprocess pass.
+#include <cuda_runtime.h>
+
+#include "bwd_items.cuh"
+#include "launch.h"
+
+namespace attn {
+namespace {
+
+struct Bwd128 {
+  static constexpr int D = 128, BN = 128, BM = 128, HALF = 64;
+  static constexpr int TILE = 128 * 128 * 2;      // one bf16 128 x 128 tile (two 64-column panels)
+  static constexpr int STG = 16 * 1024;           // 32 dQ rows (fp32) or one dK / dV panel (bf16)
+  static constexpr int OFF_K = 0, OFF_V = TILE, OFF_Q = 2 * TILE, OFF_DO = 4 * TILE,
+                       OFF_DS = 5 * TILE, OFF_STG = 6 * TILE;
+  static constexpr int SMEM = OFF_STG + STG + 1024;
+  static constexpr int THREADS = 576;
+  static constexpr uint32_t COL_S = 0, COL_DP = 128, COL_DV = 256, COL_DK = 384;
+  // packed P^T / dS^T columns of K-step kk (queries 16 kk .. 16 kk + 15) of
+  // the dV / dK MMAs: warpgroup kk / 4 holds them
+  __host__ __device__ static constexpr uint32_t pt_col(int kk) {
+    return COL_S + 64 * (kk >> 2) + 8 * (kk & 3);
+  }
+  __host__ __device__ static constexpr uint32_t dst_col(int kk) { return pt_col(kk) + 32; }
+  static_assert(SMEM <= 227 * 1024 - 4096, "shared memory budget");
+};
+
+__global__ void __launch_bounds__(Bwd128::THREADS, 1)
+    attn_bwd128_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                       const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+                       const __grid_constant__ CUtensorMap tmdK, const __grid_constant__ CUtensorMap tmdV,
+                       const BwdArgs a) {
+  using C = Bwd128;
+  constexpr int BM = C::BM, BN = C::BN, HALF = C::HALF;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint8_t* sK = smem + C::OFF_K;
+  uint8_t* sV = smem + C::OFF_V;
+  uint8_t* sQ = smem + C::OFF_Q;     // two slots
+  uint8_t* sdO = smem + C::OFF_DO;
+  uint8_t* sdS = smem + C::OFF_DS;
+  uint8_t* stg = smem + C::OFF_STG;
+
+  __shared__ uint64_t bar_kv_full, bar_kv_empty, bar_qfull[2], bar_qempty[2], bar_dofull,
+      bar_doempty;
+  __shared__ uint64_t bar_s, bar_dp, bar_p, bar_ds, bar_ds_free, bar_dq_full, bar_dq_empty;
+  __shared__ uint64_t bar_done, bar_dv_empty, bar_dk_empty;
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int abort_flag;
+  __shared__ __align__(16) float s_nlse[2][BM];   // -LSE * log2(e) per query column
+  __shared__ __align__(16) float s_delta[2][BM];
+
+  const Problem& p = a.p;
+  const int warp = warp_id();
+  const int total = a.total_items;
+  const int G = static_cast<int>(p.fd_grp.d);   // query heads per kv head
+  AbortCtx ac{&abort_flag, p.err};
+
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(&bar_kv_full, 1);
+    mbar_init(&bar_kv_empty, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bar_qfull[s], 1);
+      mbar_init(&bar_qempty[s], 1);
+    }
+    mbar_init(&bar_dofull, 1);
+    mbar_init(&bar_doempty, 1);
+    mbar_init(&bar_s, 1);
+    mbar_init(&bar_dp, 1);
+    mbar_init(&bar_p, 256);
+    mbar_init(&bar_ds, 256);
+    mbar_init(&bar_ds_free, 1);
+    mbar_init(&bar_dq_full, 1);
+    mbar_init(&bar_dq_empty, 256);
+    mbar_init(&bar_done, 1);
+    mbar_init(&bar_dv_empty, 256);
+    mbar_init(&bar_dk_empty, 256);
+    fence_mbar_init();
+  }
+  if (warp == 17) tmem_alloc(&tmem_base_sh, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_sh;
+
+  if (warp == 16) {
+    // ---------------- TMA producer ----------------
+    // K/V once per item; Q (two slots) and dO (one slot) once per step.  dO(g)
+    // is last read by dV(g), early in step g, and first needed again by
+    // dP^T(g+1) at the end of it, so one slot keeps up.
+    if (lane_id() == 0) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      tma_prefetch_desc(&tmdO);
+      BwdItem w;
+      int k = 0, ic = 0, gs = 0;
+      bool ok = true;
+      while (ok && next_bwd_item<BN, BM>(p, total, a.n_x, a.x_major, a.fd_nbh, a.fd_nx, k, w)) {
+        if (!mbar_wait(&bar_kv_empty, (ic & 1) ^ 1, ac)) break;
+        mbar_arrive_expect_tx(&bar_kv_full, 2 * C::TILE);
+        for (int pn = 0; pn < 2; ++pn) {
+          tma_load_4d(&tmK, &bar_kv_full, sK + pn * BN * 128, pn * 64, w.hk, w.seq.row0 + w.kv0,
+                      w.seq.b);
+          tma_load_4d(&tmV, &bar_kv_full, sV + pn * BN * 128, pn * 64, w.hk, w.seq.row0 + w.kv0,
+                      w.seq.b);
+        }
+        int ih = 0, ii = -1;   // step it = ih * n_i + ii
+        for (int it = 0; it < w.n_it; ++it) {
+          if (++ii == w.n_i) { ii = 0; ++ih; }
+          const int g = gs + it, qs = g & 1;
+          const int h = w.hk * G + ih;
+          const int row = w.seq.row0 + (w.i_start + ii) * BM;
+          if (!mbar_wait(&bar_qempty[qs], ((g >> 1) & 1) ^ 1, ac)) { ok = false; break; }
+          mbar_arrive_expect_tx(&bar_qfull[qs], C::TILE);
+          for (int pn = 0; pn < 2; ++pn)
+            tma_load_4d(&tmQ, &bar_qfull[qs], sQ + qs * C::TILE + pn * BM * 128, pn * 64, h, row,
+                        w.seq.b);
+          if (!mbar_wait(&bar_doempty, (g & 1) ^ 1, ac)) { ok = false; break; }
+          mbar_arrive_expect_tx(&bar_dofull, C::TILE);
+          for (int pn = 0; pn < 2; ++pn)
+            tma_load_4d(&tmdO, &bar_dofull, sdO + pn * BM * 128, pn * 64, h, row, w.seq.b);
+        }
+        gs += w.n_it;
+        ++ic;
+      }
+    }
+  } else if (warp == 17) {
+    // ---------------- MMA issuer (warp-uniform: one elected lane issues) ----------------
+    // Per step g: dV(g) after P(g); after dS(g): dK(g), S^T(g+1), dQ^T(g), and
+    // dP^T(g+1) once dQ^T(g) has left TMEM.  The first step of an item issues
+    // its own S^T and dP^T.
+    const uint32_t idS = idesc_bf16(128, BM, false, false);   // S^T, dP^T
+    const uint32_t idKV = idesc_bf16(128, 128, false, true);  // dV, dK (A from TMEM)
+    const uint32_t idQ = idesc_bf16(128, BM, true, true);     // dQ^T
+    const uint64_t dK_k = desc_kmajor_base(smem_u32(sK));
+    const uint64_t dV_k = desc_kmajor_base(smem_u32(sV));
+    const uint64_t dK_mn = desc_mnmajor_base(smem_u32(sK), BN);
+    const uint64_t dQ_k0 = desc_kmajor_base(smem_u32(sQ));
+    const uint64_t dQ_mn0 = desc_mnmajor_base(smem_u32(sQ), BM);
+    const uint64_t ddO_k = desc_kmajor_base(smem_u32(sdO));
+    const uint64_t ddO_mn = desc_mnmajor_base(smem_u32(sdO), BM);
+    const uint64_t ddS_mn = desc_mnmajor_base(smem_u32(sdS), BN);
+    auto issue_s = [&](int qs) {   // S^T = K Q^T
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)
+        umma_ss_w(tmem + C::COL_S, desc_advance(dK_k, kmajor_step_bytes(BN, kk)),
+                  desc_advance(dQ_k0, qs * C::TILE + kmajor_step_bytes(BM, kk)), idS, kk > 0);
+      umma_commit_w(&bar_s);
+    };
+    auto issue_dp = [&]() {        // dP^T = V dO^T
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)
+        umma_ss_w(tmem + C::COL_DP, desc_advance(dV_k, kmajor_step_bytes(BN, kk)),
+                  desc_advance(ddO_k, kmajor_step_bytes(BM, kk)), idS, kk > 0);
+      umma_commit_w(&bar_dp);
+    };
+    BwdItem w;
+    int k = 0, ic = 0, gs = 0;
+    bool ok = true;
+    while (ok && next_bwd_item<BN, BM>(p, total, a.n_x, a.x_major, a.fd_nbh, a.fd_nx, k, w)) {
+      if (!mbar_wait_w(&bar_kv_full, ic & 1, ac)) break;
+      for (int it = 0; it < w.n_it; ++it) {
+        const int g = gs + it, qs = g & 1;
+        if (it == 0) {
+          if (!mbar_wait_w(&bar_qfull[qs], (g >> 1) & 1, ac)) { ok = false; break; }
+          tc_fence_after();
+          issue_s(qs);
+          // dQ^T of the previous step still occupies the dP^T columns
+          if (g > 0 && !mbar_wait_w(&bar_dq_empty, (g - 1) & 1, ac)) { ok = false; break; }
+          if (!mbar_wait_w(&bar_dofull, g & 1, ac)) { ok = false; break; }
+          tc_fence_after();
+          issue_dp();
+        }
+        // ---- dV(g) += P^T(g) dO(g) ----
+        if (!mbar_wait_w(&bar_p, g & 1, ac)) { ok = false; break; }
+        // the previous item's epilogue must have read dV out of TMEM
+        if (it == 0 && ic > 0 && !mbar_wait_w(&bar_dv_empty, (ic - 1) & 1, ac)) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          umma_ts_w(tmem + C::COL_DV, tmem + C::pt_col(kk), desc_advance(ddO_mn, mnmajor_step_bytes(kk)),
+                    idKV, (it > 0 || kk > 0) ? 1u : 0u);
+        umma_commit_w(&bar_doempty);   // dP^T(g) and dV(g) have read dO(g)
+        // ---- dK(g) += dS^T(g) Q(g) ----
+        if (!mbar_wait_w(&bar_ds, g & 1, ac)) { ok = false; break; }
+        if (it == 0 && ic > 0 && !mbar_wait_w(&bar_dk_empty, (ic - 1) & 1, ac)) { ok = false; break; }
+        tc_fence_after();
+        const uint64_t qmn = desc_advance(dQ_mn0, qs * C::TILE);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          umma_ts_w(tmem + C::COL_DK, tmem + C::dst_col(kk), desc_advance(qmn, mnmajor_step_bytes(kk)),
+                    idKV, (it > 0 || kk > 0) ? 1u : 0u);
+        umma_commit_w(&bar_qempty[qs]);   // S^T(g) and dK(g) have read Q(g)
+        const bool nx = it + 1 < w.n_it;
+        // ---- S^T(g+1) over the P^T / dS^T columns dV(g) and dK(g) have read ----
+        if (nx) {
+          if (!mbar_wait_w(&bar_qfull[qs ^ 1], ((g + 1) >> 1) & 1, ac)) { ok = false; break; }
+          tc_fence_after();
+          issue_s(qs ^ 1);
+        }
+        // ---- dQ^T(g) = K^T dS^T(g) into the dP^T columns ----
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          umma_ss_w(tmem + C::COL_DP, desc_advance(dK_mn, mnmajor_step_bytes(kk)),
+                    desc_advance(ddS_mn, mnmajor_step_bytes(kk)), idQ, kk > 0);
+        umma_commit_w(&bar_dq_full);
+        umma_commit_w(&bar_ds_free);
+        // ---- dP^T(g+1) once dQ^T(g) has left TMEM ----
+        if (nx) {
+          if (!mbar_wait_w(&bar_dq_empty, g & 1, ac)) { ok = false; break; }
+          if (!mbar_wait_w(&bar_dofull, (g + 1) & 1, ac)) { ok = false; break; }
+          tc_fence_after();
+          issue_dp();
+        }
+      }
+      if (!ok) break;
+      umma_commit_w(&bar_done);       // dV and dK of this item are final
+      umma_commit_w(&bar_kv_empty);
+      gs += w.n_it;
+      ++ic;
+    }
+  } else if (warp < 8) {
+    // ---------------- P / dS warpgroups ----------------
+    const int tid = threadIdx.x;                       // 0..255
+    const int wg = warp >> 2;                          // column half
+    const int r = (warp & 3) * 32 + lane_id();         // K/V row in tile == TMEM lane
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const int c0 = wg * HALF;
+    const float sl2 = a.scale_log2;
+    // LSE or Delta of one query column, loaded one step ahead; the loaded value
+    // is not touched until the next step, so the load latency stays hidden
+    auto fetch = [&](const BwdItem& w, int ih, int ii) -> float {
+      const bool is_lse = tid < BM;
+      const int c = is_lse ? tid : tid - BM;
+      const int h = w.hk * G + ih;
+      const int q = (w.i_start + ii) * BM + c;
+      if (q >= w.seq.len) return is_lse ? INFINITY : 0.f;
+      size_t li;
+      if (p.cu_seqlens)
+        li = static_cast<size_t>(h) * p.rows_total + w.seq.row0 + q;
+      else
+        li = (static_cast<size_t>(w.seq.b) * p.heads_q + h) * p.rows_total + q;
+      return __ldg((is_lse ? a.lse : a.delta) + li);
+    };
+    const uint32_t tS = tmem + lane_base + C::COL_S + c0;    // S^T; P^T at +0, dS^T at +32
+    const uint32_t tDP = tmem + lane_base + C::COL_DP + c0;  // dP^T
+    const uint64_t sl2x2 = f2_pack(sl2, sl2);
+    BwdItem w;
+    int k = 0, gs = 0;
+    bool have = next_bwd_item<BN, BM>(p, total, a.n_x, a.x_major, a.fd_nbh, a.fd_nx, k, w);
+    float pf = have ? fetch(w, 0, 0) : 0.f;
+    bool ok = true;
+    while (ok && have) {
+      const int kv = w.kv0 + r;                        // K/V row inside the sequence
+      const bool kv_ok = kv < w.seq.len;
+      int ih = 0, ii = -1;   // step it = ih * n_i + ii
+      for (int it = 0; it < w.n_it; ++it) {
+        if (++ii == w.n_i) { ii = 0; ++ih; }
+        const int g = gs + it;
+        const int q0 = (w.i_start + ii) * BM;
+        const int buf = g & 1;
+        if (tid < BM) s_nlse[buf][tid] = -pf * kLog2e;   // LSE in the log2 domain, negated
+        else s_delta[buf][tid - BM] = pf;
+        if (it + 1 < w.n_it) {
+          const bool wrap = ii + 1 == w.n_i;
+          pf = fetch(w, wrap ? ih + 1 : ih, wrap ? 0 : ii + 1);
+        } else {
+          // last step of the item: look up the next one for the prefetch
+          BwdItem wn;
+          int kn = k;
+          if (next_bwd_item<BN, BM>(p, total, a.n_x, a.x_major, a.fd_nbh, a.fd_nx, kn, wn))
+            pf = fetch(wn, 0, 0);
+        }
+        named_bar_sync(1, 256);
+        // ---- P^T (K/V row r, query columns c0 .. c0 + 63), two 32-column chunks ----
+        if (!mbar_wait(&bar_s, g & 1, ac)) { ok = false; break; }
+        tc_fence_after();
+        // masking on S: the whole row past the sequence end, the causal
+        // triangle on diagonal tiles (columns c < lim hold earlier queries)
+        const int lim_all = !kv_ok ? HALF : ((p.causal && q0 < w.kv0 + BN) ? kv - q0 - c0 : 0);
+#pragma unroll 1
+        for (int c1 = 0; c1 < HALF; c1 += 32) {
+          uint32_t u[32];
+          tmem_ld32_nowait(tS + c1, u);
+          tmem_wait_ld();
+          const int lim = lim_all - c1;
+          if (lim > 0) {
+#pragma unroll
+            for (int c = 0; c < 32; ++c)
+              if (c < lim) u[c] = 0xff800000u;   // -inf
+          }
+          uint32_t pk[16];
+#pragma unroll
+          for (int c = 0; c < 32; c += 4) {
+            const float4 l4 = *reinterpret_cast<const float4*>(&s_nlse[buf][c0 + c1 + c]);
+            float a0, a1, a2, a3;
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(u[c]), __uint_as_float(u[c + 1])), sl2x2,
+                             f2_pack(l4.x, l4.y)), a0, a1);
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(u[c + 2]), __uint_as_float(u[c + 3])), sl2x2,
+                             f2_pack(l4.z, l4.w)), a2, a3);
+            pk[c / 2] = f2_to_bf16x2(f2_pack(ex2(a0), ex2(a1)));
+            pk[c / 2 + 1] = f2_to_bf16x2(f2_pack(ex2(a2), ex2(a3)));
+          }
+          // over S^T columns c1 / 2 .. c1 / 2 + 15, all read by chunk 0
+          tmem_st16p(tS + c1 / 2, pk);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&bar_p);
+        // ---- dS^T = P^T o (dP^T - Delta) ----
+        if (!mbar_wait(&bar_dp, g & 1, ac)) { ok = false; break; }
+        // dQ^T(g-1) has consumed the dS tile
+        if (g > 0 && !mbar_wait(&bar_ds_free, (g - 1) & 1, ac)) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll 1
+        for (int c1 = 0; c1 < HALF; c1 += 32) {
+          uint32_t u[32], pp[16];
+          tmem_ld32_nowait(tDP + c1, u);
+          tmem_ld16_nowait(tS + c1 / 2, pp);
+          tmem_wait_ld();
+          uint32_t pk[16];
+#pragma unroll
+          for (int c = 0; c < 32; c += 4) {
+            const uint64_t pa = f2_pack(__uint_as_float(pp[c / 2] << 16),
+                                        __uint_as_float(pp[c / 2] & 0xffff0000u));
+            const uint64_t pb = f2_pack(__uint_as_float(pp[c / 2 + 1] << 16),
+                                        __uint_as_float(pp[c / 2 + 1] & 0xffff0000u));
+            const float4 d4 = *reinterpret_cast<const float4*>(&s_delta[buf][c0 + c1 + c]);
+            pk[c / 2] = f2_to_bf16x2(f2_mul(
+                f2_sub(f2_pack(__uint_as_float(u[c]), __uint_as_float(u[c + 1])), f2_pack(d4.x, d4.y)),
+                pa));
+            pk[c / 2 + 1] = f2_to_bf16x2(f2_mul(
+                f2_sub(f2_pack(__uint_as_float(u[c + 2]), __uint_as_float(u[c + 3])),
+                       f2_pack(d4.z, d4.w)),
+                pb));
+          }
+          tmem_st16p(tS + 32 + c1 / 2, pk);   // over S^T columns 32 .. 63 of this half
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int ch = (c0 + c1) / 8 + i;
+            const uint32_t off = (ch >> 3) * BN * 128 + r * 128 + (((ch & 7) ^ (r & 7)) << 4);
+            *reinterpret_cast<uint4*>(sdS + off) =
+                make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+          }
+        }
+        tmem_wait_st();
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(&bar_ds);
+      }
+      gs += w.n_it;
+      have = next_bwd_item<BN, BM>(p, total, a.n_x, a.x_major, a.fd_nbh, a.fd_nx, k, w);
+    }
+  } else if (warp < 16) {
+    // ---------------- drain: dQ every step, dV and dK at the end of an item ----------------
+    const int t = threadIdx.x - 256;                   // 0..255
+    const int grp = t >> 7;                            // column half
+    const int tl = t & 127;                            // TMEM lane: head dim (dQ^T), K/V row (dV, dK)
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    if (t == 0) {
+      tma_prefetch_desc(&tmdK);
+      tma_prefetch_desc(&tmdV);
+    }
+    float* stgf = reinterpret_cast<float*>(stg);
+    BwdItem w;
+    int k = 0, ic = 0, gs = 0;
+    bool ok = true;
+    while (ok && next_bwd_item<BN, BM>(p, total, a.n_x, a.x_major, a.fd_nbh, a.fd_nx, k, w)) {
+      float* base = a.dq_acc;
+      bool slab_ok = true;
+      if (a.split) {
+        if (w.jt >= a.n_split) {
+          slab_ok = false;
+          if (t == 0 && p.err) atomicOr(p.err, ATTN_DEVERR_SEQLEN);
+        } else {
+          base += static_cast<size_t>(w.jt) * a.slab_elems;
+        }
+      }
+      int ih = 0, ii = -1;   // step it = ih * n_i + ii
+      for (int it = 0; it < w.n_it; ++it) {
+        if (++ii == w.n_i) { ii = 0; ++ih; }
+        const int g = gs + it;
+        const int h = w.hk * G + ih;
+        const int q0 = (w.i_start + ii) * BM;
+        if (!mbar_wait(&bar_dq_full, g & 1, ac)) { ok = false; break; }
+        tc_fence_after();
+        // this half's 64 query columns out of TMEM at once, then free it
+        uint32_t u[64];
+        tmem_ld32_nowait(tmem + lane_base + C::COL_DP + 64 * grp, u);
+        tmem_ld32_nowait(tmem + lane_base + C::COL_DP + 64 * grp + 32, u + 32);
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(&bar_dq_empty);
+        float* dst = base + ((static_cast<size_t>(w.seq.b) * p.heads_q + h) * p.rows_total +
+                             w.seq.row0 + q0) * C::D;
+        // four rounds of 32 query rows x 128 dims through the staging tile,
+        // [query][dim] row-major (a warp writes 128 contiguous bytes)
+#pragma unroll
+        for (int rr = 0; rr < 4; ++rr) {
+          if (t == 0) bulk_wait_read<0>();   // the previous copy has read the tile
+          named_bar_sync(2, 256);
+          if (grp == (rr >> 1)) {
+#pragma unroll
+            for (int c = 0; c < 32; ++c) stgf[c * C::D + tl] = __uint_as_float(u[32 * (rr & 1) + c]);
+          }
+          fence_proxy_async_smem();
+          named_bar_sync(2, 256);
+          if (t == 0) {
+            const int nq = min(32, w.seq.len - q0 - 32 * rr);
+            if (slab_ok && nq > 0) {
+              float* d = dst + static_cast<size_t>(32 * rr) * C::D;
+              if (a.split)
+                bulk_store(d, stgf, static_cast<uint32_t>(nq) * C::D * 4);
+              else
+                bulk_reduce_add_f32(d, stgf, static_cast<uint32_t>(nq) * C::D * 4);
+            }
+            bulk_commit();
+          }
+        }
+      }
+      if (!ok) break;
+      // ---- dV and dK (x scale) of this item: dims 64 grp .. 64 grp + 63 ----
+      if (!mbar_wait(&bar_done, ic & 1, ac)) break;
+      tc_fence_after();
+      const int kv = w.kv0 + tl;
+      const bool rows_exact = p.cu_seqlens != nullptr && w.kv0 + BN > w.seq.len;
+      const size_t grow = static_cast<size_t>(w.seq.b) * p.rows_total + w.seq.row0 + kv;
+#pragma unroll
+      for (int which = 0; which < 2; ++which) {
+        const uint32_t col = (which == 0 ? C::COL_DV : C::COL_DK) + 64 * grp;
+        const float mul = which == 0 ? 1.0f : p.scale;
+        uint32_t pkx[32];
+        {
+          uint32_t x[64];
+          tmem_ld32_nowait(tmem + lane_base + col, x);
+          tmem_ld32_nowait(tmem + lane_base + col + 32, x + 32);
+          tmem_wait_ld();
+          tc_fence_before();
+          mbar_arrive(which == 0 ? &bar_dv_empty : &bar_dk_empty);
+#pragma unroll
+          for (int c = 0; c < 32; ++c)
+            pkx[c] = pack_bf16(__uint_as_float(x[2 * c]) * mul, __uint_as_float(x[2 * c + 1]) * mul);
+        }
+        if (rows_exact) {
+          // a THD tile that ends inside the next sequence: row-exact stores
+          if (kv < w.seq.len) {
+            __nv_bfloat16* gdst =
+                (which == 0 ? a.dv : a.dk) + (grow * p.heads_kv + w.hk) * C::D + 64 * grp;
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+              *reinterpret_cast<uint4*>(gdst + 8 * c) =
+                  make_uint4(pkx[4 * c], pkx[4 * c + 1], pkx[4 * c + 2], pkx[4 * c + 3]);
+          }
+        } else {
+          // one 64-dim panel per round in the 128-byte swizzled layout of the
+          // dV / dK tensor maps, then a TMA store
+#pragma unroll
+          for (int pn = 0; pn < 2; ++pn) {
+            if (t == 0) bulk_wait_read<0>();
+            named_bar_sync(2, 256);
+            if (grp == pn) {
+#pragma unroll
+              for (int c = 0; c < 8; ++c) {
+                const uint32_t off = tl * 128 + ((c ^ (tl & 7)) << 4);
+                *reinterpret_cast<uint4*>(stg + off) =
+                    make_uint4(pkx[4 * c], pkx[4 * c + 1], pkx[4 * c + 2], pkx[4 * c + 3]);
+              }
+            }
+            fence_proxy_async_smem();
+            named_bar_sync(2, 256);
+            if (t == 0) {
+              tma_store_4d(which == 0 ? &tmdV : &tmdK, stg, pn * 64, w.hk, w.seq.row0 + w.kv0,
+                           w.seq.b);
+              bulk_commit();
+            }
+          }
+        }
+      }
+      gs += w.n_it;
+      ++ic;
+    }
+    if (t == 0) bulk_wait<0>();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 17) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+    tmem_relinquish();
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_attn_bwd128(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                               const CUtensorMap& dO, const CUtensorMap& dk, const CUtensorMap& dv,
+                               const BwdArgs& a, int grid, cudaStream_t st) {
+  using C = Bwd128;
+  cudaError_t e =
+      cudaFuncSetAttribute(attn_bwd128_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  if (e != cudaSuccess) return e;
+  attn_bwd128_kernel<<<grid, C::THREADS, C::SMEM, st>>>(q, k, v, dO, dk, dv, a);
+  return cudaGetLastError();
+}
+
+}  // namespace attn

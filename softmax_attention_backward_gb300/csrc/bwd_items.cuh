@@ -1,0 +1,61 @@
+// Work items of the dense / GQA / THD backward kernels and their static
+// schedule over a persistent grid (shared by the D = 64 and D = 128 kernels).
+#pragma once
+
+#include "common.cuh"
+
+namespace attn {
+
+// One work item: K/V tile `jt` (rows kv0 .. kv0 + 127 of the sequence) of kv
+// head `hk`, and the n_it = groups * n_i query tiles it meets.
+struct BwdItem {
+  SeqRef seq;
+  int hk, jt, kv0, i_start, n_i, n_it;
+};
+
+// Advances the CTA's round counter `k` to its next valid item.  Round k of
+// the CTA grid takes items k*G .. k*G + G - 1, dealt in snake order (CTA c
+// takes c in even rounds and G - 1 - c in odd ones) to even out the per-CTA
+// work; with one CTA per item (G = total) this is plain blockIdx order.
+// Numbering (`x_major`):
+//  * 1 (persistent grid): tile slot x slowest, so the list runs from the
+//    longest items to the shortest under causal masking (tile 0 of a sequence
+//    meets every query tile, the last tile only the last one);
+//  * 0 (one CTA per item): tile slot fastest within each (batch, kv head),
+//    in reverse, so CTAs resident together work on the same heads.
+template <int BN, int BM>
+__device__ __forceinline__ bool next_bwd_item(const Problem& p, int total, int n_x, int x_major,
+                                              const FastDiv& fd_nbh, const FastDiv& fd_nx,
+                                              int& k, BwdItem& w) {
+  const int G = gridDim.x, c = blockIdx.x;
+  const int groups = static_cast<int>(p.fd_grp.d);
+  const int n_bh = p.heads_kv * p.batch;
+  for (; k * G < total; ++k) {
+    const int idx = k * G + ((k & 1) ? (G - 1 - c) : c);
+    if (idx >= total) continue;
+    int bh, x;
+    if (x_major) {
+      x = static_cast<int>(fdiv(idx, fd_nbh));
+      bh = idx - x * n_bh;
+    } else {
+      bh = static_cast<int>(fdiv(idx, fd_nx));
+      x = idx - bh * n_x;
+    }
+    const int b = static_cast<int>(fdiv(bh, p.fd_hkv));
+    w.hk = bh - b * p.heads_kv;
+    int jt;
+    if (!decode_tile(p, x, b, BN, w.seq, jt)) continue;
+    if (!x_major && p.causal) jt = (w.seq.len + BN - 1) / BN - 1 - jt;
+    w.jt = jt;
+    w.kv0 = jt * BN;
+    w.i_start = p.causal ? w.kv0 / BM : 0;
+    w.n_i = (w.seq.len + BM - 1) / BM - w.i_start;
+    w.n_it = groups * w.n_i;
+    if (w.n_it <= 0) continue;
+    ++k;
+    return true;
+  }
+  return false;
+}
+
+}  // namespace attn

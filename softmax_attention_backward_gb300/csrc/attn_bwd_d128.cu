@@ -29,10 +29,12 @@
 // row), 8..15 drain (warpgroup u: dQ^T columns 64u .. 64u + 63, so all of
 // dQ^T leaves TMEM in one load; dV / dK dims 64u .. 64u + 63 at the end of an
 // item), 16 TMA, 17 MMA issuer.
-// dQ leaves through the staging tile 32 query rows at a time, as one bulk
-// reduce-add into the fp32 accumulator (ATOMIC) or one bulk store into this
-// K/V tile's slab (SPLIT).  The scale of dK is applied on the way out, that of
-// dQ in the postprocess pass.
+// dQ leaves TMEM in one load and goes out per warp, 32 dims x 16 query rows
+// per TMA copy: a reduce-add into the fp32 accumulator (ATOMIC) or a store
+// into this K/V tile's slab (SPLIT).  One 16 KB copy at a time through a
+// shared tile ran at ~11 bytes per clock per SM, which bounded the step; eight
+// independent warps keep eight copies in flight.  The scale of dK is applied
+// on the way out, that of dQ in the postprocess pass.
 #include <cuda_runtime.h>
 
 #include "bwd_items.cuh"
@@ -44,7 +46,8 @@ namespace {
 struct Bwd128 {
   static constexpr int D = 128, BN = 128, BM = 128, HALF = 64;
   static constexpr int TILE = 128 * 128 * 2;      // one bf16 128 x 128 tile (two 64-column panels)
-  static constexpr int STG = 16 * 1024;           // 32 dQ rows (fp32) or one dK / dV panel (bf16)
+  static constexpr int STG = 16 * 1024;           // 8 warps x 2 KB of dQ, or one dK / dV panel
+  static constexpr int DQR = 16;                  // query rows per dQ box (32 dims x 16 rows, fp32)
   static constexpr int OFF_K = 0, OFF_V = TILE, OFF_Q = 2 * TILE, OFF_DO = 4 * TILE,
                        OFF_DS = 5 * TILE, OFF_STG = 6 * TILE;
   static constexpr int SMEM = OFF_STG + STG + 1024;
@@ -62,8 +65,8 @@ struct Bwd128 {
 __global__ void __launch_bounds__(Bwd128::THREADS, 1)
     attn_bwd128_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
-                       const __grid_constant__ CUtensorMap tmdK, const __grid_constant__ CUtensorMap tmdV,
-                       const BwdArgs a) {
+                       const __grid_constant__ CUtensorMap tmDQ, const __grid_constant__ CUtensorMap tmdK,
+                       const __grid_constant__ CUtensorMap tmdV, const BwdArgs a) {
   using C = Bwd128;
   constexpr int BM = C::BM, BN = C::BN, HALF = C::HALF;
   extern __shared__ uint8_t smem_raw[];
@@ -394,11 +397,13 @@ __global__ void __launch_bounds__(Bwd128::THREADS, 1)
     const int grp = t >> 7;                            // column half
     const int tl = t & 127;                            // TMEM lane: head dim (dQ^T), K/V row (dV, dK)
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const int wq = warp & 3;                           // dQ dims 32 wq .. 32 wq + 31
     if (t == 0) {
+      tma_prefetch_desc(&tmDQ);
       tma_prefetch_desc(&tmdK);
       tma_prefetch_desc(&tmdV);
     }
-    float* stgf = reinterpret_cast<float*>(stg);
+    float* sw = reinterpret_cast<float*>(stg) + (warp - 8) * (C::DQR * 32);   // this warp's 2 KB
     BwdItem w;
     int k = 0, ic = 0, gs = 0;
     bool ok = true;
@@ -428,30 +433,41 @@ __global__ void __launch_bounds__(Bwd128::THREADS, 1)
         tmem_wait_ld();
         tc_fence_before();
         mbar_arrive(&bar_dq_empty);
-        float* dst = base + ((static_cast<size_t>(w.seq.b) * p.heads_q + h) * p.rows_total +
-                             w.seq.row0 + q0) * C::D;
-        // four rounds of 32 query rows x 128 dims through the staging tile,
-        // [query][dim] row-major (a warp writes 128 contiguous bytes)
+        // each warp: its 32 dims x 64 queries in boxes of 16 query rows, staged
+        // row-major in its own 2 KB and sent by one TMA reduce-add (ATOMIC) or
+        // store into this K/V tile's slab (SPLIT), with no barrier across
+        // warps, so eight copies are in flight.  A box cut by the end of the
+        // sequence leaves row by row instead (the rows past it belong to the
+        // next sequence).
+        const size_t hrow = (static_cast<size_t>(w.seq.b) * p.heads_q + h) * p.rows_total;
 #pragma unroll
-        for (int rr = 0; rr < 4; ++rr) {
-          if (t == 0) bulk_wait_read<0>();   // the previous copy has read the tile
-          named_bar_sync(2, 256);
-          if (grp == (rr >> 1)) {
+        for (int rr = 0; rr < 64 / C::DQR; ++rr) {
+          const int q = q0 + 64 * grp + C::DQR * rr;     // first query row of the box
+          const int nq = min(C::DQR, w.seq.len - q);
+          if (nq <= 0 || !slab_ok) break;
+          if (nq == C::DQR) {
+            if (lane_id() == 0) bulk_wait_read<0>();   // this warp's previous copy has read sw
+            __syncwarp();
 #pragma unroll
-            for (int c = 0; c < 32; ++c) stgf[c * C::D + tl] = __uint_as_float(u[32 * (rr & 1) + c]);
-          }
-          fence_proxy_async_smem();
-          named_bar_sync(2, 256);
-          if (t == 0) {
-            const int nq = min(32, w.seq.len - q0 - 32 * rr);
-            if (slab_ok && nq > 0) {
-              float* d = dst + static_cast<size_t>(32 * rr) * C::D;
+            for (int c = 0; c < C::DQR; ++c) sw[c * 32 + lane_id()] = __uint_as_float(u[C::DQR * rr + c]);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane_id() == 0) {
               if (a.split)
-                bulk_store(d, stgf, static_cast<uint32_t>(nq) * C::D * 4);
+                tma_store_5d(&tmDQ, sw, 32 * wq, w.seq.row0 + q, h, w.seq.b, w.jt);
               else
-                bulk_reduce_add_f32(d, stgf, static_cast<uint32_t>(nq) * C::D * 4);
+                tma_reduce_add_4d(&tmDQ, sw, 32 * wq, w.seq.row0 + q, h, w.seq.b);
+              bulk_commit();
             }
-            bulk_commit();
+          } else {
+            float* gq = base + (hrow + w.seq.row0 + q) * C::D + 32 * wq + lane_id();
+#pragma unroll
+            for (int c = 0; c < C::DQR; ++c) {
+              if (c < nq) {
+                if (a.split) gq[c * C::D] = __uint_as_float(u[C::DQR * rr + c]);
+                else atomicAdd(gq + c * C::D, __uint_as_float(u[C::DQR * rr + c]));
+              }
+            }
           }
         }
       }
@@ -493,7 +509,7 @@ __global__ void __launch_bounds__(Bwd128::THREADS, 1)
           // dV / dK tensor maps, then a TMA store
 #pragma unroll
           for (int pn = 0; pn < 2; ++pn) {
-            if (t == 0) bulk_wait_read<0>();
+            if (lane_id() == 0) bulk_wait_read<0>();   // every earlier copy has read the tile
             named_bar_sync(2, 256);
             if (grp == pn) {
 #pragma unroll
@@ -513,10 +529,13 @@ __global__ void __launch_bounds__(Bwd128::THREADS, 1)
           }
         }
       }
+      // the next item's dQ boxes reuse the tile the dV / dK stores read
+      if (t == 0) bulk_wait_read<0>();
+      named_bar_sync(2, 256);
       gs += w.n_it;
       ++ic;
     }
-    if (t == 0) bulk_wait<0>();
+    if (lane_id() == 0) bulk_wait<0>();
   }
 
   tc_fence_before();
@@ -531,13 +550,13 @@ __global__ void __launch_bounds__(Bwd128::THREADS, 1)
 }  // namespace
 
 cudaError_t launch_attn_bwd128(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
-                               const CUtensorMap& dO, const CUtensorMap& dk, const CUtensorMap& dv,
-                               const BwdArgs& a, int grid, cudaStream_t st) {
+                               const CUtensorMap& dO, const CUtensorMap& dq, const CUtensorMap& dk,
+                               const CUtensorMap& dv, const BwdArgs& a, int grid, cudaStream_t st) {
   using C = Bwd128;
   cudaError_t e =
       cudaFuncSetAttribute(attn_bwd128_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
-  attn_bwd128_kernel<<<grid, C::THREADS, C::SMEM, st>>>(q, k, v, dO, dk, dv, a);
+  attn_bwd128_kernel<<<grid, C::THREADS, C::SMEM, st>>>(q, k, v, dO, dq, dk, dv, a);
   return cudaGetLastError();
 }
 

@@ -62,7 +62,7 @@ struct BwdArgs {
   size_t slab_elems;    // SPLIT: elements per slab (0 for ATOMIC)
   int n_split;          // SPLIT: number of slabs
   int split;            // 1 = SPLIT
-  int dq_tma;           // 1 = dQ tiles leave through the swizzled TMA map of the accumulator
+  int dq_tma;           // 1 = dQ tiles leave through the TMA map of the accumulator / slabs
   int total_items;      // work items: K/V tile slots x kv heads x batch
   int n_x;              // K/V tile slots per (batch, kv head)
   int x_major;          // item numbering, see next_bwd_item
@@ -79,9 +79,11 @@ template <int D>
 cudaError_t launch_attn_bwd(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                             const CUtensorMap& dO, const CUtensorMap& dq, const CUtensorMap& dk,
                             const CUtensorMap& dv, const BwdArgs& a, int grid, cudaStream_t st);
-// head_dim 128 (attn_bwd_d128.cu): 128 x 128 steps, dQ through bulk copies
+// head_dim 128 (attn_bwd_d128.cu): 128 x 128 steps, dQ through per-warp TMA
+// copies of 32 dims x 16 rows (`dq`: map over the accumulator or the slabs)
 cudaError_t launch_attn_bwd128(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
-                               const CUtensorMap& dO, const CUtensorMap& dk, const CUtensorMap& dv,
+                               const CUtensorMap& dO, const CUtensorMap& dq, const CUtensorMap& dk,
+                               const CUtensorMap& dv,
                                const BwdArgs& a, int grid, cudaStream_t st);
 template <int D>
 cudaError_t launch_bwd_preprocess(const Problem& p, const __nv_bfloat16* o,

@@ -49,11 +49,10 @@ bool make_map(CUtensorMap* m, const void* ptr, int batch, int rows, int heads, i
 
 // Map over the fp32 dQ accumulator [batch, heads, rows, dim] (head-major), or
 // over `n_split` such slabs when n_split > 0 (5-D, slab outermost): box of 32
-// dims x box_rows rows, 128-byte swizzle (the D = 64 staging layout, 128-row
-// boxes) or none (D = 128: one warp's 32 dims x 16 rows, row-major).  Rows
-// past `rows` are clipped by the copy.
+// dims x 128 rows, 128-byte swizzle, matching the staging layout of the D = 64
+// backward kernel.  Rows past `rows` are clipped by the copy.
 bool make_dq_map(CUtensorMap* m, float* acc, int batch, int rows, int heads, int dim, int n_split,
-                 size_t slab_elems, int box_rows, bool swizzle) {
+                 size_t slab_elems) {
   auto fn = encode_fn();
   if (!fn) return false;
   const cuuint32_t rank = n_split > 0 ? 5 : 4;
@@ -64,11 +63,10 @@ bool make_dq_map(CUtensorMap* m, float* acc, int batch, int rows, int heads, int
                            static_cast<cuuint64_t>(rows) * dim * 4,
                            static_cast<cuuint64_t>(heads) * rows * dim * 4,
                            static_cast<cuuint64_t>(slab_elems) * 4};
-  cuuint32_t box[5] = {32, static_cast<cuuint32_t>(box_rows), 1, 1, 1};
+  cuuint32_t box[5] = {32, 128, 1, 1, 1};
   cuuint32_t es[5] = {1, 1, 1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, rank, acc, dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE,
-            swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -296,14 +294,11 @@ attn_status_t attn_bwd(const attn_problem_t* p, attn_dq_mode_t mode, const void*
   // TMA layout keeps free of bank conflicts.  A THD slab store of a tile that
   // crosses a sequence end would overwrite the next sequence's rows of the
   // same slab, so THD + SPLIT keeps the row-exact bulk copy.
-  // D = 128 copies whole 16-row boxes out with TMA and the rows of a box cut
-  // by the end of a sequence with plain per-row accesses, in every mode.
-  a.dq_tma = ((D == 64 && !(kp.cu_seqlens && a.split)) || D == 128) ? 1 : 0;
+  a.dq_tma = (D == 64 && !(kp.cu_seqlens && a.split)) ? 1 : 0;
   CUtensorMap mdq, mdk, mdv;
   memset(&mdq, 0, sizeof(mdq));
   if (a.dq_tma && !make_dq_map(&mdq, a.dq_acc, kp.batch, kp.rows_total, kp.heads_q, D,
-                               a.split ? a.n_split : 0, a.slab_elems, D == 64 ? 128 : 16,
-                               D == 64))
+                               a.split ? a.n_split : 0, a.slab_elems))
     return ATTN_ERR_CUDA;
   if (!make_map(&mdk, dk, kp.batch, kp.rows_total, kp.heads_kv, D, 128) ||
       !make_map(&mdv, dv, kp.batch, kp.rows_total, kp.heads_kv, D, 128))
@@ -324,7 +319,7 @@ attn_status_t attn_bwd(const attn_problem_t* p, attn_dq_mode_t mode, const void*
   const int grid = persistent ? sms : static_cast<int>(total);
   a.x_major = persistent ? 1 : 0;
   cudaError_t e = (D == 64) ? launch_attn_bwd<64>(mq, mk, mv, mdo, mdq, mdk, mdv, a, grid, st)
-                            : launch_attn_bwd128(mq, mk, mv, mdo, mdq, mdk, mdv, a, grid, st);
+                            : launch_attn_bwd128(mq, mk, mv, mdo, a, grid, st);
   return cuda_status(e);
 }
 

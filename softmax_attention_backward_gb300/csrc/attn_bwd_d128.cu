@@ -46,11 +46,9 @@ namespace {
 struct Bwd128 {
   static constexpr int D = 128, BN = 128, BM = 128, HALF = 64;
   static constexpr int TILE = 128 * 128 * 2;      // one bf16 128 x 128 tile (two 64-column panels)
-  static constexpr int STG = 16 * 1024;           // 8 warps x 2 KB of dQ, or one dK / dV panel
-  static constexpr int DQR = 16;                  // query rows per dQ box (32 dims x 16 rows, fp32)
   static constexpr int OFF_K = 0, OFF_V = TILE, OFF_Q = 2 * TILE, OFF_DO = 4 * TILE,
-                       OFF_DS = 5 * TILE, OFF_STG = 6 * TILE;
-  static constexpr int SMEM = OFF_STG + STG + 1024;
+                       OFF_DS = 6 * TILE;
+  static constexpr int SMEM = 7 * TILE + 1024;
   static constexpr int THREADS = 576;
   static constexpr uint32_t COL_S = 0, COL_DP = 128, COL_DV = 256, COL_DK = 384;
   // packed P^T / dS^T columns of K-step kk (queries 16 kk .. 16 kk + 15) of
@@ -59,14 +57,15 @@ struct Bwd128 {
     return COL_S + 64 * (kk >> 2) + 8 * (kk & 3);
   }
   __host__ __device__ static constexpr uint32_t dst_col(int kk) { return pt_col(kk) + 32; }
-  static_assert(SMEM <= 227 * 1024 - 4096, "shared memory budget");
+  // dynamic + the kernel's static shared memory (barriers, one row of LSE and
+  // Delta: about 1.2 KB) within the 227 KB a CTA may use
+  static_assert(SMEM + 1536 <= 227 * 1024, "shared memory budget");
 };
 
 __global__ void __launch_bounds__(Bwd128::THREADS, 1)
     attn_bwd128_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
-                       const __grid_constant__ CUtensorMap tmDQ, const __grid_constant__ CUtensorMap tmdK,
-                       const __grid_constant__ CUtensorMap tmdV, const BwdArgs a) {
+                       const BwdArgs a) {
   using C = Bwd128;
   constexpr int BM = C::BM, BN = C::BN, HALF = C::HALF;
   extern __shared__ uint8_t smem_raw[];
@@ -75,18 +74,19 @@ __global__ void __launch_bounds__(Bwd128::THREADS, 1)
   uint8_t* sK = smem + C::OFF_K;
   uint8_t* sV = smem + C::OFF_V;
   uint8_t* sQ = smem + C::OFF_Q;     // two slots
-  uint8_t* sdO = smem + C::OFF_DO;
+  uint8_t* sdO = smem + C::OFF_DO;   // two slots
   uint8_t* sdS = smem + C::OFF_DS;
-  uint8_t* stg = smem + C::OFF_STG;
 
-  __shared__ uint64_t bar_kv_full, bar_kv_empty, bar_qfull[2], bar_qempty[2], bar_dofull,
-      bar_doempty;
-  __shared__ uint64_t bar_s, bar_dp, bar_p, bar_ds, bar_ds_free, bar_dq_full, bar_dq_empty;
+  __shared__ uint64_t bar_kv_full, bar_kv_empty, bar_qfull[2], bar_qempty[2], bar_dofull[2],
+      bar_doempty[2];
+  __shared__ uint64_t bar_s, bar_dp, bar_p, bar_ds, bar_dq_full, bar_dq_empty;
   __shared__ uint64_t bar_done, bar_dv_empty, bar_dk_empty;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_flag;
-  __shared__ __align__(16) float s_nlse[2][BM];   // -LSE * log2(e) per query column
-  __shared__ __align__(16) float s_delta[2][BM];
+  // -LSE * log2(e) and Delta of the step's query columns; one buffer, so that
+  // the tiles and these fit the 227 KB with the 1 KB alignment margin
+  __shared__ __align__(16) float s_nlse[BM];
+  __shared__ __align__(16) float s_delta[BM];
 
   const Problem& p = a.p;
   const int warp = warp_id();
@@ -101,14 +101,13 @@ __global__ void __launch_bounds__(Bwd128::THREADS, 1)
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bar_qfull[s], 1);
       mbar_init(&bar_qempty[s], 1);
+      mbar_init(&bar_dofull[s], 1);
+      mbar_init(&bar_doempty[s], 1);
     }
-    mbar_init(&bar_dofull, 1);
-    mbar_init(&bar_doempty, 1);
     mbar_init(&bar_s, 1);
     mbar_init(&bar_dp, 1);
     mbar_init(&bar_p, 256);
     mbar_init(&bar_ds, 256);
-    mbar_init(&bar_ds_free, 1);
     mbar_init(&bar_dq_full, 1);
     mbar_init(&bar_dq_empty, 256);
     mbar_init(&bar_done, 1);
@@ -124,9 +123,11 @@ __global__ void __launch_bounds__(Bwd128::THREADS, 1)
 
   if (warp == 16) {
     // ---------------- TMA producer ----------------
-    // K/V once per item; Q (two slots) and dO (one slot) once per step.  dO(g)
-    // is last read by dV(g), early in step g, and first needed again by
-    // dP^T(g+1) at the end of it, so one slot keeps up.
+    // K/V once per item; Q and dO (two slots each) once per step.  dO(g) is
+    // last read by dV(g), in the middle of step g, and dP^T(g+2) needs its
+    // slot again at the end of step g+1: the load has a whole step to arrive
+    // (a dO load under this traffic takes about half a step).  The waits spin:
+    // a suspended producer resumes too late to keep a step ahead.
     if (lane_id() == 0) {
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
@@ -136,7 +137,7 @@ __global__ void __launch_bounds__(Bwd128::THREADS, 1)
       int k = 0, ic = 0, gs = 0;
       bool ok = true;
       while (ok && next_bwd_item<BN, BM>(p, total, a.n_x, a.x_major, a.fd_nbh, a.fd_nx, k, w)) {
-        if (!mbar_wait(&bar_kv_empty, (ic & 1) ^ 1, ac)) break;
+        if (!mbar_wait_spin(&bar_kv_empty, (ic & 1) ^ 1, ac)) break;
         mbar_arrive_expect_tx(&bar_kv_full, 2 * C::TILE);
         for (int pn = 0; pn < 2; ++pn) {
           tma_load_4d(&tmK, &bar_kv_full, sK + pn * BN * 128, pn * 64, w.hk, w.seq.row0 + w.kv0,
@@ -147,18 +148,19 @@ __global__ void __launch_bounds__(Bwd128::THREADS, 1)
         int ih = 0, ii = -1;   // step it = ih * n_i + ii
         for (int it = 0; it < w.n_it; ++it) {
           if (++ii == w.n_i) { ii = 0; ++ih; }
-          const int g = gs + it, qs = g & 1;
+          const int g = gs + it, sl = g & 1, par = ((g >> 1) & 1) ^ 1;
           const int h = w.hk * G + ih;
           const int row = w.seq.row0 + (w.i_start + ii) * BM;
-          if (!mbar_wait(&bar_qempty[qs], ((g >> 1) & 1) ^ 1, ac)) { ok = false; break; }
-          mbar_arrive_expect_tx(&bar_qfull[qs], C::TILE);
+          if (!mbar_wait_spin(&bar_qempty[sl], par, ac)) { ok = false; break; }
+          mbar_arrive_expect_tx(&bar_qfull[sl], C::TILE);
           for (int pn = 0; pn < 2; ++pn)
-            tma_load_4d(&tmQ, &bar_qfull[qs], sQ + qs * C::TILE + pn * BM * 128, pn * 64, h, row,
+            tma_load_4d(&tmQ, &bar_qfull[sl], sQ + sl * C::TILE + pn * BM * 128, pn * 64, h, row,
                         w.seq.b);
-          if (!mbar_wait(&bar_doempty, (g & 1) ^ 1, ac)) { ok = false; break; }
-          mbar_arrive_expect_tx(&bar_dofull, C::TILE);
+          if (!mbar_wait_spin(&bar_doempty[sl], par, ac)) { ok = false; break; }
+          mbar_arrive_expect_tx(&bar_dofull[sl], C::TILE);
           for (int pn = 0; pn < 2; ++pn)
-            tma_load_4d(&tmdO, &bar_dofull, sdO + pn * BM * 128, pn * 64, h, row, w.seq.b);
+            tma_load_4d(&tmdO, &bar_dofull[sl], sdO + sl * C::TILE + pn * BM * 128, pn * 64, h,
+                        row, w.seq.b);
         }
         gs += w.n_it;
         ++ic;
@@ -177,8 +179,8 @@ __global__ void __launch_bounds__(Bwd128::THREADS, 1)
     const uint64_t dK_mn = desc_mnmajor_base(smem_u32(sK), BN);
     const uint64_t dQ_k0 = desc_kmajor_base(smem_u32(sQ));
     const uint64_t dQ_mn0 = desc_mnmajor_base(smem_u32(sQ), BM);
-    const uint64_t ddO_k = desc_kmajor_base(smem_u32(sdO));
-    const uint64_t ddO_mn = desc_mnmajor_base(smem_u32(sdO), BM);
+    const uint64_t ddO_k0 = desc_kmajor_base(smem_u32(sdO));
+    const uint64_t ddO_mn0 = desc_mnmajor_base(smem_u32(sdO), BM);
     const uint64_t ddS_mn = desc_mnmajor_base(smem_u32(sdS), BN);
     auto issue_s = [&](int qs) {   // S^T = K Q^T
 #pragma unroll
@@ -187,11 +189,11 @@ __global__ void __launch_bounds__(Bwd128::THREADS, 1)
                   desc_advance(dQ_k0, qs * C::TILE + kmajor_step_bytes(BM, kk)), idS, kk > 0);
       umma_commit_w(&bar_s);
     };
-    auto issue_dp = [&]() {        // dP^T = V dO^T
+    auto issue_dp = [&](int sl) {  // dP^T = V dO^T
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk)
         umma_ss_w(tmem + C::COL_DP, desc_advance(dV_k, kmajor_step_bytes(BN, kk)),
-                  desc_advance(ddO_k, kmajor_step_bytes(BM, kk)), idS, kk > 0);
+                  desc_advance(ddO_k0, sl * C::TILE + kmajor_step_bytes(BM, kk)), idS, kk > 0);
       umma_commit_w(&bar_dp);
     };
     BwdItem w;
@@ -207,20 +209,25 @@ __global__ void __launch_bounds__(Bwd128::THREADS, 1)
           issue_s(qs);
           // dQ^T of the previous step still occupies the dP^T columns
           if (g > 0 && !mbar_wait_w(&bar_dq_empty, (g - 1) & 1, ac)) { ok = false; break; }
-          if (!mbar_wait_w(&bar_dofull, g & 1, ac)) { ok = false; break; }
+          if (!mbar_wait_w(&bar_dofull[qs], (g >> 1) & 1, ac)) { ok = false; break; }
           tc_fence_after();
-          issue_dp();
+          issue_dp(qs);
         }
         // ---- dV(g) += P^T(g) dO(g) ----
         if (!mbar_wait_w(&bar_p, g & 1, ac)) { ok = false; break; }
         // the previous item's epilogue must have read dV out of TMEM
         if (it == 0 && ic > 0 && !mbar_wait_w(&bar_dv_empty, (ic - 1) & 1, ac)) { ok = false; break; }
         tc_fence_after();
+        const uint64_t omn = desc_advance(ddO_mn0, qs * C::TILE);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          umma_ts_w(tmem + C::COL_DV, tmem + C::pt_col(kk), desc_advance(ddO_mn, mnmajor_step_bytes(kk)),
+          umma_ts_w(tmem + C::COL_DV, tmem + C::pt_col(kk), desc_advance(omn, mnmajor_step_bytes(kk)),
                     idKV, (it > 0 || kk > 0) ? 1u : 0u);
-        umma_commit_w(&bar_doempty);   // dP^T(g) and dV(g) have read dO(g)
+        umma_commit_w(&bar_doempty[qs]);   // dP^T(g) and dV(g) have read dO(g)
+        const bool nx = it + 1 < w.n_it;
+        // Q(g+1) has long arrived; testing it here, while the dS pass runs,
+        // keeps the barrier round trip off the dK -> S^T(g+1) path
+        if (nx && !mbar_wait_w(&bar_qfull[qs ^ 1], ((g + 1) >> 1) & 1, ac)) { ok = false; break; }
         // ---- dK(g) += dS^T(g) Q(g) ----
         if (!mbar_wait_w(&bar_ds, g & 1, ac)) { ok = false; break; }
         if (it == 0 && ic > 0 && !mbar_wait_w(&bar_dk_empty, (ic - 1) & 1, ac)) { ok = false; break; }
@@ -231,26 +238,21 @@ __global__ void __launch_bounds__(Bwd128::THREADS, 1)
           umma_ts_w(tmem + C::COL_DK, tmem + C::dst_col(kk), desc_advance(qmn, mnmajor_step_bytes(kk)),
                     idKV, (it > 0 || kk > 0) ? 1u : 0u);
         umma_commit_w(&bar_qempty[qs]);   // S^T(g) and dK(g) have read Q(g)
-        const bool nx = it + 1 < w.n_it;
         // ---- S^T(g+1) over the P^T / dS^T columns dV(g) and dK(g) have read ----
-        if (nx) {
-          if (!mbar_wait_w(&bar_qfull[qs ^ 1], ((g + 1) >> 1) & 1, ac)) { ok = false; break; }
-          tc_fence_after();
-          issue_s(qs ^ 1);
-        }
+        if (nx) issue_s(qs ^ 1);
         // ---- dQ^T(g) = K^T dS^T(g) into the dP^T columns ----
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
           umma_ss_w(tmem + C::COL_DP, desc_advance(dK_mn, mnmajor_step_bytes(kk)),
                     desc_advance(ddS_mn, mnmajor_step_bytes(kk)), idQ, kk > 0);
         umma_commit_w(&bar_dq_full);
-        umma_commit_w(&bar_ds_free);
         // ---- dP^T(g+1) once dQ^T(g) has left TMEM ----
         if (nx) {
+          // dO(g+1) first: it arrived a step ago, and its test overlaps the drain
+          if (!mbar_wait_w(&bar_dofull[qs ^ 1], ((g + 1) >> 1) & 1, ac)) { ok = false; break; }
           if (!mbar_wait_w(&bar_dq_empty, g & 1, ac)) { ok = false; break; }
-          if (!mbar_wait_w(&bar_dofull, (g + 1) & 1, ac)) { ok = false; break; }
           tc_fence_after();
-          issue_dp();
+          issue_dp(qs ^ 1);
         }
       }
       if (!ok) break;
@@ -298,9 +300,9 @@ __global__ void __launch_bounds__(Bwd128::THREADS, 1)
         if (++ii == w.n_i) { ii = 0; ++ih; }
         const int g = gs + it;
         const int q0 = (w.i_start + ii) * BM;
-        const int buf = g & 1;
-        if (tid < BM) s_nlse[buf][tid] = -pf * kLog2e;   // LSE in the log2 domain, negated
-        else s_delta[buf][tid - BM] = pf;
+        named_bar_sync(1, 256);   // every thread has read the previous step's values
+        if (tid < BM) s_nlse[tid] = -pf * kLog2e;   // LSE in the log2 domain, negated
+        else s_delta[tid - BM] = pf;
         if (it + 1 < w.n_it) {
           const bool wrap = ii + 1 == w.n_i;
           pf = fetch(w, wrap ? ih + 1 : ih, wrap ? 0 : ii + 1);
@@ -332,7 +334,7 @@ __global__ void __launch_bounds__(Bwd128::THREADS, 1)
           uint32_t pk[16];
 #pragma unroll
           for (int c = 0; c < 32; c += 4) {
-            const float4 l4 = *reinterpret_cast<const float4*>(&s_nlse[buf][c0 + c1 + c]);
+            const float4 l4 = *reinterpret_cast<const float4*>(&s_nlse[c0 + c1 + c]);
             float a0, a1, a2, a3;
             f2_unpack(f2_fma(f2_pack(__uint_as_float(u[c]), __uint_as_float(u[c + 1])), sl2x2,
                              f2_pack(l4.x, l4.y)), a0, a1);
@@ -349,8 +351,8 @@ __global__ void __launch_bounds__(Bwd128::THREADS, 1)
         mbar_arrive(&bar_p);
         // ---- dS^T = P^T o (dP^T - Delta) ----
         if (!mbar_wait(&bar_dp, g & 1, ac)) { ok = false; break; }
-        // dQ^T(g-1) has consumed the dS tile
-        if (g > 0 && !mbar_wait(&bar_ds_free, (g - 1) & 1, ac)) { ok = false; break; }
+        // the dS tile is free: dP^T(g) went out after dQ^T(g-1), and its
+        // commit arrives only once every earlier MMA has completed
         tc_fence_after();
 #pragma unroll 1
         for (int c1 = 0; c1 < HALF; c1 += 32) {
@@ -365,7 +367,7 @@ __global__ void __launch_bounds__(Bwd128::THREADS, 1)
                                         __uint_as_float(pp[c / 2] & 0xffff0000u));
             const uint64_t pb = f2_pack(__uint_as_float(pp[c / 2 + 1] << 16),
                                         __uint_as_float(pp[c / 2 + 1] & 0xffff0000u));
-            const float4 d4 = *reinterpret_cast<const float4*>(&s_delta[buf][c0 + c1 + c]);
+            const float4 d4 = *reinterpret_cast<const float4*>(&s_delta[c0 + c1 + c]);
             pk[c / 2] = f2_to_bf16x2(f2_mul(
                 f2_sub(f2_pack(__uint_as_float(u[c]), __uint_as_float(u[c + 1])), f2_pack(d4.x, d4.y)),
                 pa));
@@ -393,17 +395,19 @@ __global__ void __launch_bounds__(Bwd128::THREADS, 1)
     }
   } else if (warp < 16) {
     // ---------------- drain: dQ every step, dV and dK at the end of an item ----------------
+    // dQ^T leaves TMEM in one load (64 query columns per warpgroup) and goes
+    // to global memory straight from registers: the lane of a thread is a
+    // head dim, so one warp instruction covers 32 consecutive dims (128
+    // bytes) of one query row.  ATOMIC adds into the fp32 accumulator with
+    // red.global.add.f32, SPLIT stores into this K/V tile's slab.  Measured
+    // against TMA copies through a shared-memory tile (one 16 KB copy at a
+    // time, then eight per-warp 2 KB copies), this keeps the SM's TMA unit
+    // for the operand loads, and the freed shared memory holds the second dO
+    // slot.
     const int t = threadIdx.x - 256;                   // 0..255
     const int grp = t >> 7;                            // column half
     const int tl = t & 127;                            // TMEM lane: head dim (dQ^T), K/V row (dV, dK)
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const int wq = warp & 3;                           // dQ dims 32 wq .. 32 wq + 31
-    if (t == 0) {
-      tma_prefetch_desc(&tmDQ);
-      tma_prefetch_desc(&tmdK);
-      tma_prefetch_desc(&tmdV);
-    }
-    float* sw = reinterpret_cast<float*>(stg) + (warp - 8) * (C::DQR * 32);   // this warp's 2 KB
     BwdItem w;
     int k = 0, ic = 0, gs = 0;
     bool ok = true;
@@ -423,60 +427,34 @@ __global__ void __launch_bounds__(Bwd128::THREADS, 1)
         if (++ii == w.n_i) { ii = 0; ++ih; }
         const int g = gs + it;
         const int h = w.hk * G + ih;
-        const int q0 = (w.i_start + ii) * BM;
+        const int q = (w.i_start + ii) * BM + 64 * grp;   // first query row of this half
         if (!mbar_wait(&bar_dq_full, g & 1, ac)) { ok = false; break; }
         tc_fence_after();
-        // this half's 64 query columns out of TMEM at once, then free it
         uint32_t u[64];
         tmem_ld32_nowait(tmem + lane_base + C::COL_DP + 64 * grp, u);
         tmem_ld32_nowait(tmem + lane_base + C::COL_DP + 64 * grp + 32, u + 32);
         tmem_wait_ld();
         tc_fence_before();
         mbar_arrive(&bar_dq_empty);
-        // each warp: its 32 dims x 64 queries in boxes of 16 query rows, staged
-        // row-major in its own 2 KB and sent by one TMA reduce-add (ATOMIC) or
-        // store into this K/V tile's slab (SPLIT), with no barrier across
-        // warps, so eight copies are in flight.  A box cut by the end of the
-        // sequence leaves row by row instead (the rows past it belong to the
-        // next sequence).
-        const size_t hrow = (static_cast<size_t>(w.seq.b) * p.heads_q + h) * p.rows_total;
+        const int nq = min(64, w.seq.len - q);
+        if (!slab_ok || nq <= 0) continue;
+        float* gq = base + ((static_cast<size_t>(w.seq.b) * p.heads_q + h) * p.rows_total +
+                            w.seq.row0 + q) * C::D + tl;
+        if (a.split) {
 #pragma unroll
-        for (int rr = 0; rr < 64 / C::DQR; ++rr) {
-          const int q = q0 + 64 * grp + C::DQR * rr;     // first query row of the box
-          const int nq = min(C::DQR, w.seq.len - q);
-          if (nq <= 0 || !slab_ok) break;
-          if (nq == C::DQR) {
-            if (lane_id() == 0) bulk_wait_read<0>();   // this warp's previous copy has read sw
-            __syncwarp();
+          for (int c = 0; c < 64; ++c)
+            if (c < nq) gq[static_cast<size_t>(c) * C::D] = __uint_as_float(u[c]);
+        } else {
 #pragma unroll
-            for (int c = 0; c < C::DQR; ++c) sw[c * 32 + lane_id()] = __uint_as_float(u[C::DQR * rr + c]);
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane_id() == 0) {
-              if (a.split)
-                tma_store_5d(&tmDQ, sw, 32 * wq, w.seq.row0 + q, h, w.seq.b, w.jt);
-              else
-                tma_reduce_add_4d(&tmDQ, sw, 32 * wq, w.seq.row0 + q, h, w.seq.b);
-              bulk_commit();
-            }
-          } else {
-            float* gq = base + (hrow + w.seq.row0 + q) * C::D + 32 * wq + lane_id();
-#pragma unroll
-            for (int c = 0; c < C::DQR; ++c) {
-              if (c < nq) {
-                if (a.split) gq[c * C::D] = __uint_as_float(u[C::DQR * rr + c]);
-                else atomicAdd(gq + c * C::D, __uint_as_float(u[C::DQR * rr + c]));
-              }
-            }
-          }
+          for (int c = 0; c < 64; ++c)
+            if (c < nq) atomicAdd(gq + static_cast<size_t>(c) * C::D, __uint_as_float(u[c]));
         }
       }
       if (!ok) break;
-      // ---- dV and dK (x scale) of this item: dims 64 grp .. 64 grp + 63 ----
+      // ---- dV and dK (x scale) of this item: dims 64 grp .. 64 grp + 63 of row kv ----
       if (!mbar_wait(&bar_done, ic & 1, ac)) break;
       tc_fence_after();
       const int kv = w.kv0 + tl;
-      const bool rows_exact = p.cu_seqlens != nullptr && w.kv0 + BN > w.seq.len;
       const size_t grow = static_cast<size_t>(w.seq.b) * p.rows_total + w.seq.row0 + kv;
 #pragma unroll
       for (int which = 0; which < 2; ++which) {
@@ -494,48 +472,19 @@ __global__ void __launch_bounds__(Bwd128::THREADS, 1)
           for (int c = 0; c < 32; ++c)
             pkx[c] = pack_bf16(__uint_as_float(x[2 * c]) * mul, __uint_as_float(x[2 * c + 1]) * mul);
         }
-        if (rows_exact) {
-          // a THD tile that ends inside the next sequence: row-exact stores
-          if (kv < w.seq.len) {
-            __nv_bfloat16* gdst =
-                (which == 0 ? a.dv : a.dk) + (grow * p.heads_kv + w.hk) * C::D + 64 * grp;
+        // rows past the end of the sequence (or of the tensor) are not written
+        if (kv < w.seq.len) {
+          __nv_bfloat16* gdst =
+              (which == 0 ? a.dv : a.dk) + (grow * p.heads_kv + w.hk) * C::D + 64 * grp;
 #pragma unroll
-            for (int c = 0; c < 8; ++c)
-              *reinterpret_cast<uint4*>(gdst + 8 * c) =
-                  make_uint4(pkx[4 * c], pkx[4 * c + 1], pkx[4 * c + 2], pkx[4 * c + 3]);
-          }
-        } else {
-          // one 64-dim panel per round in the 128-byte swizzled layout of the
-          // dV / dK tensor maps, then a TMA store
-#pragma unroll
-          for (int pn = 0; pn < 2; ++pn) {
-            if (lane_id() == 0) bulk_wait_read<0>();   // every earlier copy has read the tile
-            named_bar_sync(2, 256);
-            if (grp == pn) {
-#pragma unroll
-              for (int c = 0; c < 8; ++c) {
-                const uint32_t off = tl * 128 + ((c ^ (tl & 7)) << 4);
-                *reinterpret_cast<uint4*>(stg + off) =
-                    make_uint4(pkx[4 * c], pkx[4 * c + 1], pkx[4 * c + 2], pkx[4 * c + 3]);
-              }
-            }
-            fence_proxy_async_smem();
-            named_bar_sync(2, 256);
-            if (t == 0) {
-              tma_store_4d(which == 0 ? &tmdV : &tmdK, stg, pn * 64, w.hk, w.seq.row0 + w.kv0,
-                           w.seq.b);
-              bulk_commit();
-            }
-          }
+          for (int c = 0; c < 8; ++c)
+            *reinterpret_cast<uint4*>(gdst + 8 * c) =
+                make_uint4(pkx[4 * c], pkx[4 * c + 1], pkx[4 * c + 2], pkx[4 * c + 3]);
         }
       }
-      // the next item's dQ boxes reuse the tile the dV / dK stores read
-      if (t == 0) bulk_wait_read<0>();
-      named_bar_sync(2, 256);
       gs += w.n_it;
       ++ic;
     }
-    if (lane_id() == 0) bulk_wait<0>();
   }
 
   tc_fence_before();
@@ -550,13 +499,12 @@ __global__ void __launch_bounds__(Bwd128::THREADS, 1)
 }  // namespace
 
 cudaError_t launch_attn_bwd128(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
-                               const CUtensorMap& dO, const CUtensorMap& dq, const CUtensorMap& dk,
-                               const CUtensorMap& dv, const BwdArgs& a, int grid, cudaStream_t st) {
+                               const CUtensorMap& dO, const BwdArgs& a, int grid, cudaStream_t st) {
   using C = Bwd128;
   cudaError_t e =
       cudaFuncSetAttribute(attn_bwd128_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
-  attn_bwd128_kernel<<<grid, C::THREADS, C::SMEM, st>>>(q, k, v, dO, dq, dk, dv, a);
+  attn_bwd128_kernel<<<grid, C::THREADS, C::SMEM, st>>>(q, k, v, dO, a);
   return cudaGetLastError();
 }
 

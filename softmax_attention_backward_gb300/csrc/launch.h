@@ -79,11 +79,10 @@ template <int D>
 cudaError_t launch_attn_bwd(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                             const CUtensorMap& dO, const CUtensorMap& dq, const CUtensorMap& dk,
                             const CUtensorMap& dv, const BwdArgs& a, int grid, cudaStream_t st);
-// head_dim 128 (attn_bwd_d128.cu): 128 x 128 steps, dQ through per-warp TMA
-// copies of 32 dims x 16 rows (`dq`: map over the accumulator or the slabs)
+// head_dim 128 (attn_bwd_d128.cu): 128 x 128 steps; dQ, dK and dV leave from
+// registers with plain global accesses
 cudaError_t launch_attn_bwd128(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
-                               const CUtensorMap& dO, const CUtensorMap& dq, const CUtensorMap& dk,
-                               const CUtensorMap& dv,
+                               const CUtensorMap& dO,
                                const BwdArgs& a, int grid, cudaStream_t st);
 template <int D>
 cudaError_t launch_bwd_preprocess(const Problem& p, const __nv_bfloat16* o,

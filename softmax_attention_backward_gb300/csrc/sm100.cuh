@@ -132,6 +132,26 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
   }
 }
 
+// Bounded wait that polls without suspending: a thread suspended in try_wait
+// resumes some hundreds of cycles after the phase completes, too late for a
+// single-thread role (an MMA issuer, a TMA producer) on a pipeline's critical
+// path.  Not for the many-warp roles, whose polling would take issue slots.
+__device__ __forceinline__ bool mbar_wait_spin(uint64_t* bar, uint32_t parity, const AbortCtx& c) {
+  const uint32_t addr = smem_u32(bar);
+  if (mbar_test_wait(addr, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  for (uint32_t n = 1;; ++n) {
+    if (mbar_test_wait(addr, parity)) return true;
+    if ((n & 255u) == 0) {
+      if (*reinterpret_cast<volatile int*>(c.smem_abort)) return false;
+      if (globaltimer() - t0 > c.limit_ns) {
+        raise_error(c, ATTN_DEVERR_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
 // ---------------------------------------------------------------------------
 // TMA (bulk tensor copies global -> shared, completion on an mbarrier)
 // ---------------------------------------------------------------------------

@@ -360,6 +360,9 @@ def bench_dense(args, w, dev, flush, world, rank, sampler=None, e2e=False):
     pre_b, post_b = dense_pass_bytes(w)
     src = "softmax_attention_backward_gb300/csrc/"
     D = w.head_dim
+    # the dominant kernel: head_dim 64 and 128 have kernels of their own
+    bwd_kernel, bwd_src = (("attn_bwd_kernel<64>", "attn_bwd.cu") if D == 64
+                           else ("attn_bwd128_kernel", "attn_bwd_d128.cu"))
     blk = {
         "workload": w.name,
         "fwd_bwd_tflops": tflops(f_fwd + f_bwd, t_at["total"]),
@@ -375,11 +378,11 @@ def bench_dense(args, w, dev, flush, world, rank, sampler=None, e2e=False):
             "ms_breakdown": {"fwd": t_sp["fwd"], "bwd_preprocess": t_sp["pre"],
                              "bwd_main": t_sp["main"], "bwd_postprocess": t_sp["post"]},
             "workspace_bytes": ws_split_bytes},
-        "roofline": {"kernel": f"attn_bwd_kernel<{D}>", "bound": "tensor",
+        "roofline": {"kernel": bwd_kernel, "bound": "tensor",
                      "achieved": tflops(f_bwd, t_at["main"]), "peak": peak, "unit": "TFLOP/s",
                      "frac": tflops(f_bwd, t_at["main"]) / peak,
                      "peak_kind": f"{pk_kind} bf16 burst",
-                     "traffic": profiled_traffic("attn_bwd_kernel", w.name, src + "attn_bwd.cu"),
+                     "traffic": profiled_traffic(bwd_kernel.split("<")[0], w.name, src + bwd_src),
                      "flops_per_launch": f_bwd},
         "fwd_roofline": {"kernel": f"attn_fwd_kernel<{D}>", "bound": "tensor",
                          "achieved": tflops(f_fwd, t_at["fwd"]), "peak": peak, "unit": "TFLOP/s",

@@ -1,30 +1,29 @@
-// Dense / GQA / THD attention backward (the `flash_bwd` stage of "[Example]
-// Introduce split+sum template, and optimize atomic_add performance for bwd
-// examples", tile-ai/tilelang #940: atomic and split variants).
+// Dense / GQA / THD attention backward at head_dim 64 (the `flash_bwd` stage
+// of "[Example] Introduce split+sum template, and optimize atomic_add
+// performance for bwd examples", tile-ai/tilelang #940: atomic and split
+// variants).  head_dim 128 has a kernel of its own (attn_bwd_d128.cu).
 //
 // Work item = one 128-row K/V tile of one kv head.  The CTA owning an item
 // walks the query tiles of every query head of its GQA group, so dK and dV stay
 // in TMEM for the whole item and are stored once (the group reduction of the
 // #940 GQA backward, where dK is indexed by head // groups, happens on chip,
-// without atomics).  Per query tile i of head h (KV rows j, query rows q):
+// without atomics).  Per 128-row query tile i of head h (KV rows j, query rows q):
 //   S^T  = K Q_i^T   (TMEM)     P^T  = exp2(S^T * c - LSE_q * log2 e)
 //   dP^T = V dO_i^T  (TMEM)     dS^T = P^T o (dP^T - Delta_q)
 //   dV  += P^T dO_i             dK  += dS^T Q_i
 // with P^T and dS^T written back into TMEM as packed bf16 and used as the TMEM
-// A operand of the dV / dK MMAs, and
-//   dQ_i  = dS K  (D = 64, 128-row query tiles)  or
-//   dQ_i^T = K^T dS^T (D = 128, 64-row query tiles) from a bf16 dS tile in
-// shared memory, streamed out of TMEM through a shared-memory tile and either
-// added into one fp32 accumulator (ATOMIC) or stored into the partial slab of
-// this KV tile (SPLIT, summed in order later).  The accumulator and slabs are
+// A operand of the dV / dK MMAs, and dQ_i = dS K from a bf16 dS tile in shared
+// memory, streamed out of TMEM through a shared-memory tile and either added
+// into one fp32 accumulator (ATOMIC) or stored into the partial slab of this
+// KV tile (SPLIT, summed in order later).  The accumulator and slabs are
 // head-major, [batch, head, row, dim], so a query tile of one head is one
 // contiguous block.
 // The kernel is persistent: one CTA per SM walks a static list of items
 // (longest first under causal masking, dealt to the CTAs in snake order), and
 // every role runs ahead into the next item while the previous one finishes:
-// K/V of the next item are loaded while the current one runs (two K/V buffers
-// for D = 64), and dK / dV leave TMEM through the dQ-drain warps, overlapped
-// with the next item's first steps.
+// K/V of the next item are loaded into a second buffer while the current one
+// runs, and dK / dV leave TMEM through the dQ-drain warps, overlapped with the
+// next item's first steps.
 // The scale factor of dK is applied on the way out and that of dQ in the
 // postprocess pass.
 #include <cuda_runtime.h>
@@ -36,43 +35,40 @@ namespace attn {
 
 template <int D>
 struct BwdCfg {
+  static_assert(D == 64, "head_dim 64 only (head_dim 128: attn_bwd_d128.cu)");
   static constexpr int BN = 128;                      // KV rows per item
-  static constexpr int BM = (D == 64) ? 128 : 64;     // query rows per step
+  static constexpr int BM = 128;                      // query rows per step
   static constexpr int HALF = BM / 2;                 // query columns per P/dS thread
   static constexpr int KV_BYTES = BN * D * 2;
   static constexpr int QT_BYTES = BM * D * 2;
   static constexpr int DS_BYTES = BN * BM * 2;        // bf16 dS tile (for dQ)
-  // staging tile for dQ (fp32) and dK/dV (bf16) on their way out: the whole
-  // 64 x 128 dQ tile for D = 128; half of the 128 x 64 tile for D = 64, whose
-  // dQ leaves in two halves, so that three Q/dO stages fit next to two K/V
-  // buffers
-  static constexpr int STG_BYTES = (D == 64) ? BM * D * 2 : BM * D * 4;
-  static constexpr int KV_BUFS = (D == 64) ? 2 : 1;   // K/V buffers (next item prefetch)
+  // staging tile for dQ (fp32) and dK/dV (bf16) on their way out: half of the
+  // 128 x 64 dQ tile, which leaves in two halves, so that three Q/dO stages fit
+  // next to two K/V buffers
+  static constexpr int STG_BYTES = BM * D * 2;
+  static constexpr int KV_BUFS = 2;                   // K/V buffers (next item prefetch)
   static constexpr int NST = 3;                       // Q/dO stages
   static constexpr int SMEM =
       KV_BUFS * 2 * KV_BYTES + 2 * NST * QT_BYTES + DS_BYTES + STG_BYTES + 1024;
-  static constexpr int THREADS = (D == 64) ? 448 : 512;   // one or three issuer warps
+  static constexpr int THREADS = 448;
   static constexpr uint32_t TMEM_COLS = 512;
   // TMEM columns.  S^T and dP^T are BM fp32 columns each; P^T and dS^T are
   // packed bf16 pairs (BM / 2 columns each), P^T in columns of its own so that
   // S^T of the next step can be issued as soon as S^T of this one has been read.
-  // D = 64 (BM = 128) has no room left for dS^T: each thread writes its packed
-  // dS^T over the dP^T columns it has just read (the first half of its own
-  // HALF-column range), and the next dP^T is issued after dK has read them.
-  //   D = 64:  S^T 0..127, dP^T|dS^T 128..255, dV 256, dK 320, dQ 384, P^T 448
-  //   D = 128: S^T 0..63, dP^T 64..127, dV 128, dK 256, dQ 384, P^T 448, dS^T 480
-  static constexpr bool DS_IN_DP = (D == 64);
+  // That leaves no room for dS^T: each thread writes its packed dS^T over the
+  // dP^T columns it has just read (the first half of its own HALF-column
+  // range), and the next dP^T is issued after dK has read them.
+  //   S^T 0..127, dP^T|dS^T 128..255, dV 256, dK 320, dQ 384, P^T 448
   static constexpr uint32_t COL_S = 0;                // S^T (fp32)
   static constexpr uint32_t COL_DP = BM;              // dP^T (fp32)
   static constexpr uint32_t COL_DV = 2 * BM;
   static constexpr uint32_t COL_DK = COL_DV + D;
   static constexpr uint32_t COL_DQ = COL_DK + D;      // one 64-column dQ tile
   static constexpr uint32_t COL_PT = COL_DQ + 64;
-  static constexpr uint32_t COL_DST = COL_PT + BM / 2;
-  static_assert(COL_DST + (DS_IN_DP ? 0 : BM / 2) <= TMEM_COLS, "TMEM budget");
+  static_assert(COL_PT + BM / 2 <= TMEM_COLS, "TMEM budget");
   // TMEM column of the packed dS^T columns of K-step kk (16 queries)
   __host__ __device__ static constexpr uint32_t ds_col(int kk) {
-    return DS_IN_DP ? COL_DP + (16 * kk / HALF) * HALF + (16 * kk % HALF) / 2 : COL_DST + 8 * kk;
+    return COL_DP + (16 * kk / HALF) * HALF + (16 * kk % HALF) / 2;
   }
   // dK and dV leave one after the other through the staging tile
   static_assert(BN * D * 2 <= STG_BYTES, "dK/dV staging");
@@ -80,12 +76,8 @@ struct BwdCfg {
 };
 
 // Warp roles: 0..7 P/dS (two warpgroups, each owns half of the query columns
-// of every KV row), 8..11 dQ drain and dK/dV epilogue, 12 TMA, then the MMA
-// issuers: D = 64 one warp (13) that interleaves independent GEMMs; D = 128
-// three warps (13: S^T and dP^T; 14: dV and dK; 15: dQ) that run
-// independently, synchronized only through the data they exchange, so a
-// step's GEMMs start as soon as their own operands are ready (measured faster
-// for the shorter P/dS passes of 64-row query tiles).
+// of every KV row), 8..11 dQ drain and dK/dV epilogue, 12 TMA, 13 the MMA
+// issuer, which interleaves independent GEMMs.
 template <int D>
 __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -110,8 +102,6 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
   __shared__ uint64_t bar_qfull[C::NST], bar_qempty[C::NST];
   __shared__ uint64_t bar_s, bar_dp, bar_p, bar_ds, bar_pt_done, bar_ds_free;
   __shared__ uint64_t bar_done, bar_dq_full, bar_dq_empty;
-  // D = 128 (three issuers): S^T / dP^T read, dS^T consumed by dK, dS tile by dQ
-  __shared__ uint64_t bar_s_free, bar_dp_free, bar_dst_done, bar_dss_free;
   __shared__ uint64_t bar_dv_empty, bar_dk_empty;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_flag;
@@ -128,11 +118,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     abort_flag = 0;
     for (int b = 0; b < C::KV_BUFS; ++b) {
       mbar_init(&bar_kv_full[b], 1);
-      mbar_init(&bar_kv_empty[b], D == 64 ? 1 : 2);   // D = 128: S/dP and dQ issuers
+      mbar_init(&bar_kv_empty[b], 1);
     }
     for (int s = 0; s < C::NST; ++s) {
       mbar_init(&bar_qfull[s], 1);
-      mbar_init(&bar_qempty[s], D == 64 ? 1 : 2);     // D = 128: S/dP and dV/dK issuers
+      mbar_init(&bar_qempty[s], 1);
     }
     mbar_init(&bar_s, 1);
     mbar_init(&bar_dp, 1);
@@ -140,10 +130,6 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     mbar_init(&bar_ds, 256);
     mbar_init(&bar_pt_done, 1);
     mbar_init(&bar_ds_free, 1);
-    mbar_init(&bar_s_free, 256);
-    mbar_init(&bar_dp_free, 256);
-    mbar_init(&bar_dst_done, 1);
-    mbar_init(&bar_dss_free, 1);
     mbar_init(&bar_done, 1);
     mbar_init(&bar_dq_full, 1);
     mbar_init(&bar_dq_empty, 128);
@@ -198,7 +184,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         ++ic;
       }
     }
-  } else if (D == 64 && warp == 13) {
+  } else if (warp == 13) {
     // ---------------- D = 64: one MMA issuer ----------------
     // The GEMMs go out in two phases per step g, each as soon as the P/dS
     // warps have produced its operand:
@@ -291,15 +277,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
           for (int kk = 0; kk < KV; ++kk)
             umma_ts_w(tmem + C::COL_DK, tmem + C::ds_col(kk), desc_advance(qmn, mnmajor_step_bytes(kk)),
                       idKV, (it > 0 || kk > 0) ? 1u : 0u);
+          // dQ[q, d] = dS[q, kv] K[kv, d]
 #pragma unroll
-          for (int kk = 0; kk < KQ; ++kk) {
-            if (D == 64)   // dQ[q, d] = dS[q, kv] K[kv, d]
-              umma_ss_w(tmem + C::COL_DQ, desc_advance(ddS_mn, mnmajor_step_bytes(kk)),
-                        desc_advance(dK_mn, mnmajor_step_bytes(kk)), idQ, kk > 0);
-            else           // dQ^T[d, q] = K^T[d, kv] dS^T[kv, q]
-              umma_ss_w(tmem + C::COL_DQ, desc_advance(dK_mn, mnmajor_step_bytes(kk)),
-                        desc_advance(ddS_mn, mnmajor_step_bytes(kk)), idQ, kk > 0);
-          }
+          for (int kk = 0; kk < KQ; ++kk)
+            umma_ss_w(tmem + C::COL_DQ, desc_advance(ddS_mn, mnmajor_step_bytes(kk)),
+                      desc_advance(dK_mn, mnmajor_step_bytes(kk)), idQ, kk > 0);
           if (nx) {
 #pragma unroll
             for (int kk = 0; kk < KS; ++kk) issue_dp(kb1, st1, kk);
@@ -317,138 +299,6 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         ++ic;
         w = wn;
         have = have_next;
-      }
-    }
-  } else if (D != 64 && warp == 13) {
-    // ---------------- D = 128 issuer 1: S^T = K Q_i^T, dP^T = V dO_i^T ----------------
-    {   // warp-uniform: one elected lane issues
-      const uint32_t idSD = idesc_bf16(128, BM, false, false);
-      const uint64_t dQ_k0 = desc_kmajor_base(smem_u32(sQ));
-      const uint64_t ddO_k0 = desc_kmajor_base(smem_u32(sdO));
-      BwdItem w;
-      int k = 0, ic = 0, gs = 0;
-      bool ok = true;
-      while (ok && next_bwd_item<BN, BM>(p, total, a.n_x, a.x_major, a.fd_nbh, a.fd_nx, k, w)) {
-        const int kb = ic % C::KV_BUFS, ku = ic / C::KV_BUFS;
-        if (!mbar_wait_w(&bar_kv_full[kb], ku & 1, ac)) break;
-        const uint64_t dK_k = desc_kmajor_base(smem_u32(sK(kb)));
-        const uint64_t dV_k = desc_kmajor_base(smem_u32(sV(kb)));
-        for (int it = 0; it < w.n_it; ++it) {
-          const int g = gs + it;
-          const int st = g % C::NST;
-          if (!mbar_wait_w(&bar_qfull[st], (g / C::NST) & 1, ac)) { ok = false; break; }
-          // S^T region is free once the P pass has read S^T(g-1)
-          if (g > 0 && !mbar_wait_w(&bar_s_free, (g - 1) & 1, ac)) { ok = false; break; }
-          tc_fence_after();
-          const uint64_t qd = desc_advance(dQ_k0, st * C::QT_BYTES);
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk)
-            umma_ss_w(tmem + C::COL_S, desc_advance(dK_k, kmajor_step_bytes(BN, kk)),
-                    desc_advance(qd, kmajor_step_bytes(BM, kk)), idSD, kk > 0);
-          umma_commit_w(&bar_s);
-          // dP^T region is free once the dS pass has read dP^T(g-1)
-          if (g > 0 && !mbar_wait_w(&bar_dp_free, (g - 1) & 1, ac)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint64_t od = desc_advance(ddO_k0, st * C::QT_BYTES);
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk)
-            umma_ss_w(tmem + C::COL_DP, desc_advance(dV_k, kmajor_step_bytes(BN, kk)),
-                    desc_advance(od, kmajor_step_bytes(BM, kk)), idSD, kk > 0);
-          umma_commit_w(&bar_dp);
-          umma_commit_w(&bar_qempty[st]);
-        }
-        if (!ok) break;
-        umma_commit_w(&bar_kv_empty[kb]);
-        gs += w.n_it;
-        ++ic;
-      }
-    }
-  } else if (D != 64 && warp == 14) {
-    // ---------------- issuer 2: dV += P^T dO_i, dK += dS^T Q_i (A from TMEM) ----
-    {   // warp-uniform: one elected lane issues
-      const uint32_t idKV = idesc_bf16(128, D, false, true);
-      const uint64_t dQ_mn0 = desc_mnmajor_base(smem_u32(sQ), BM);
-      const uint64_t ddO_mn0 = desc_mnmajor_base(smem_u32(sdO), BM);
-      BwdItem w;
-      int k = 0, ic = 0, gs = 0;
-      bool ok = true;
-      while (ok && next_bwd_item<BN, BM>(p, total, a.n_x, a.x_major, a.fd_nbh, a.fd_nx, k, w)) {
-        for (int it = 0; it < w.n_it; ++it) {
-          const int g = gs + it;
-          const int st = g % C::NST;
-          if (!mbar_wait_w(&bar_qfull[st], (g / C::NST) & 1, ac)) { ok = false; break; }
-          if (!mbar_wait_w(&bar_p, g & 1, ac)) { ok = false; break; }
-          // the epilogue of the previous item must have read dV out of TMEM
-          if (it == 0 && ic > 0 && !mbar_wait_w(&bar_dv_empty, (ic - 1) & 1, ac)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint64_t omn = desc_advance(ddO_mn0, st * C::QT_BYTES);
-#pragma unroll
-          for (int kk = 0; kk < BM / 16; ++kk)
-            umma_ts_w(tmem + C::COL_DV, tmem + C::COL_PT + 8 * kk,
-                    desc_advance(omn, mnmajor_step_bytes(kk)), idKV, (it > 0 || kk > 0) ? 1u : 0u);
-          umma_commit_w(&bar_pt_done);
-          if (!mbar_wait_w(&bar_ds, g & 1, ac)) { ok = false; break; }
-          if (it == 0 && ic > 0 && !mbar_wait_w(&bar_dk_empty, (ic - 1) & 1, ac)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint64_t qmn = desc_advance(dQ_mn0, st * C::QT_BYTES);
-#pragma unroll
-          for (int kk = 0; kk < BM / 16; ++kk) {
-            const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
-            umma_ts_w(tmem + C::COL_DK, tmem + C::ds_col(kk), desc_advance(qmn, mnmajor_step_bytes(kk)),
-                      idKV, acc);
-          }
-          umma_commit_w(&bar_dst_done);
-          umma_commit_w(&bar_qempty[st]);
-        }
-        if (!ok) break;
-        umma_commit_w(&bar_done);   // dV and dK of this item are final
-        gs += w.n_it;
-        ++ic;
-      }
-    }
-  } else if (D != 64 && warp == 15) {
-    // ---------------- issuer 3: dQ (both operands in shared memory) ----------
-    {   // warp-uniform: one elected lane issues
-      const uint32_t idQ = idesc_bf16(128, 64, true, true);
-      const uint64_t ddS_mn = desc_mnmajor_base(smem_u32(sdS), BN);
-      BwdItem w;
-      int k = 0, ic = 0, gs = 0;
-      bool ok = true;
-      while (ok && next_bwd_item<BN, BM>(p, total, a.n_x, a.x_major, a.fd_nbh, a.fd_nx, k, w)) {
-        const int kb = ic % C::KV_BUFS, ku = ic / C::KV_BUFS;
-        if (!mbar_wait_w(&bar_kv_full[kb], ku & 1, ac)) break;
-        const uint64_t dK_mn = desc_mnmajor_base(smem_u32(sK(kb)), BN);
-        for (int it = 0; it < w.n_it; ++it) {
-          const int g = gs + it;
-          if (!mbar_wait_w(&bar_ds, g & 1, ac)) { ok = false; break; }
-          if (!mbar_wait_w(&bar_dq_empty, (g & 1) ^ 1, ac)) { ok = false; break; }
-          tc_fence_after();
-          const uint32_t tDQ = tmem + C::COL_DQ;
-#pragma unroll
-          for (int kk = 0; kk < BN / 16; ++kk) {
-            if (D == 64)   // dQ[q, d] = dS[q, kv] K[kv, d]
-              umma_ss_w(tDQ, desc_advance(ddS_mn, mnmajor_step_bytes(kk)),
-                      desc_advance(dK_mn, mnmajor_step_bytes(kk)), idQ, kk > 0);
-            else           // dQ^T[d, q] = K^T[d, kv] dS^T[kv, q]
-              umma_ss_w(tDQ, desc_advance(dK_mn, mnmajor_step_bytes(kk)),
-                      desc_advance(ddS_mn, mnmajor_step_bytes(kk)), idQ, kk > 0);
-          }
-          umma_commit_w(&bar_dq_full);
-          umma_commit_w(&bar_dss_free);
-        }
-        if (!ok) break;
-        umma_commit_w(&bar_kv_empty[kb]);
-        gs += w.n_it;
-        ++ic;
       }
     }
   } else if (warp < 8) {
@@ -478,8 +328,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     const uint32_t tSme = tmem + lane_base + C::COL_S + c0;      // this thread's S columns
     const uint32_t tDPme = tmem + lane_base + C::COL_DP + c0;    // this thread's dP columns
     const uint32_t tPTme = tmem + lane_base + C::COL_PT + c0 / 2;
-    const uint32_t tDSTme = tmem + lane_base + C::COL_DST + c0 / 2;
-    const uint32_t tDSme = tmem + lane_base + C::COL_DP + c0;    // D = 64: dS^T over dP^T
+    const uint32_t tDSme = tmem + lane_base + C::COL_DP + c0;    // dS^T over dP^T
     BwdItem w;
     int k = 0, gs = 0;
     bool have = next_bwd_item<BN, BM>(p, total, a.n_x, a.x_major, a.fd_nbh, a.fd_nx, k, w);
@@ -509,8 +358,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         // ---- P^T (KV row r, query columns c0 .. c0 + HALF) ----
         if (!mbar_wait(&bar_s, g & 1, ac)) { ok = false; break; }
         tc_fence_after();
-        if constexpr (D == 64) {
-          // D = 64: both passes run as rolled loops over 32-column chunks.  The
+        {
+          // Both passes run as rolled loops over 32-column chunks.  The
           // smaller loop body keeps the hot code of the eight P/dS warps, the
           // drain warps and the issuer small enough to stay in the
           // instruction cache (measured ~15% faster per step than the fully
@@ -583,102 +432,6 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
                   make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
             }
           }
-        } else {
-        // P^T in fp32 pairs: p2[i] = (P[2i], P[2i+1]) of this thread's
-        // columns; kept for the dS pass unless P^T is read back from TMEM there
-        uint64_t p2[HALF / 2];
-        uint32_t pk[HALF / 2];
-        {
-          uint32_t u[HALF];
-#pragma unroll
-          for (int c = 0; c < HALF; c += 32) tmem_ld32_nowait(tSme + c, u + c);
-          tmem_wait_ld();
-          tc_fence_before();
-          mbar_arrive(&bar_s_free);
-          // masking on S: the whole row past the sequence end, the causal
-          // triangle on diagonal tiles (columns c < lim hold earlier queries)
-          int lim = 0;
-          if (!kv_ok) lim = HALF;
-          else if (p.causal && q0 < w.kv0 + BN) lim = kv - q0 - c0;
-          if (lim > 0) {
-#pragma unroll
-            for (int c = 0; c < HALF; ++c)
-              if (c < lim) u[c] = 0xff800000u;   // -inf
-          }
-          const uint64_t sl2x2 = f2_pack(sl2, sl2);
-#pragma unroll
-          for (int c = 0; c < HALF; c += 4) {
-            const float4 l4 = *reinterpret_cast<const float4*>(&s_nlse[buf][c0 + c]);
-            float a0, a1, a2, a3;
-            f2_unpack(f2_fma(f2_pack(__uint_as_float(u[c]), __uint_as_float(u[c + 1])), sl2x2,
-                             f2_pack(l4.x, l4.y)), a0, a1);
-            f2_unpack(f2_fma(f2_pack(__uint_as_float(u[c + 2]), __uint_as_float(u[c + 3])),
-                             sl2x2, f2_pack(l4.z, l4.w)), a2, a3);
-            const uint64_t q01 = f2_pack(ex2(a0), ex2(a1));
-            const uint64_t q23 = f2_pack(ex2(a2), ex2(a3));
-            pk[c / 2] = f2_to_bf16x2(q01);
-            pk[c / 2 + 1] = f2_to_bf16x2(q23);
-            p2[c / 2] = q01;
-            p2[c / 2 + 1] = q23;
-          }
-        }
-        // P^T(g-1) must have been consumed by dV(g-1)
-        if (g > 0 && !mbar_wait(&bar_pt_done, (g - 1) & 1, ac)) { ok = false; break; }
-        tc_fence_after();
-        if constexpr (HALF / 2 == 32) tmem_st32(tPTme, pk);
-        else tmem_st16p(tPTme, pk);
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(&bar_p);
-        // ---- dS^T = P^T o (dP^T - Delta) ----
-        if (!mbar_wait(&bar_dp, g & 1, ac)) { ok = false; break; }
-        tc_fence_after();
-        {
-          // dP^T in column chunks of 32 (fewer live registers)
-          constexpr int CH = HALF < 32 ? HALF : 32;
-#pragma unroll
-          for (int c1 = 0; c1 < HALF; c1 += CH) {
-            uint32_t u[CH];
-            if constexpr (CH == 32) tmem_ld32_nowait(tDPme + c1, u);
-            else tmem_ld16_nowait(tDPme + c1, u);
-            tmem_wait_ld();
-            if (c1 + CH == HALF) {
-              // every read of the dP^T columns of this step is done
-              tc_fence_before();
-              mbar_arrive(&bar_dp_free);
-            }
-#pragma unroll
-            for (int cc = 0; cc < CH; cc += 4) {
-              const int c = c1 + cc;
-              const uint64_t pa = p2[c / 2], pb = p2[c / 2 + 1];
-              const float4 d4 = *reinterpret_cast<const float4*>(&s_delta[buf][c0 + c]);
-              const uint64_t ds01 = f2_mul(f2_sub(f2_pack(__uint_as_float(u[cc]),
-                                                          __uint_as_float(u[cc + 1])),
-                                                  f2_pack(d4.x, d4.y)),
-                                           pa);
-              const uint64_t ds23 = f2_mul(f2_sub(f2_pack(__uint_as_float(u[cc + 2]),
-                                                          __uint_as_float(u[cc + 3])),
-                                                  f2_pack(d4.z, d4.w)),
-                                           pb);
-              pk[c / 2] = f2_to_bf16x2(ds01);
-              pk[c / 2 + 1] = f2_to_bf16x2(ds23);
-            }
-          }
-        }
-        // dS^T(g-1) must have been consumed by dK(g-1)
-        if (g > 0 && !mbar_wait(&bar_dst_done, (g - 1) & 1, ac)) { ok = false; break; }
-        tc_fence_after();
-        if constexpr (HALF / 2 == 32) tmem_st32(tDSTme, pk);
-        else tmem_st16p(tDSTme, pk);
-        // dS (bf16) also to shared memory for the dQ GEMM
-        if (g > 0 && !mbar_wait(&bar_dss_free, (g - 1) & 1, ac)) { ok = false; break; }
-#pragma unroll
-        for (int i = 0; i < HALF / 8; ++i) {
-          const int ch = c0 / 8 + i;
-          const uint32_t off = (ch >> 3) * BN * 128 + r * 128 + (((ch & 7) ^ (r & 7)) << 4);
-          *reinterpret_cast<uint4*>(sdS + off) =
-              make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
-        }
         }
         tmem_wait_st();
         fence_proxy_async_smem();
@@ -691,15 +444,14 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
   } else {
     // ---------------- dQ drain and dK/dV epilogue (warps 8..11) ----------------
     // dQ: TMEM -> fp32 staging tile in shared memory -> reduce-add into the
-    // accumulator (ATOMIC) or store into this KV tile's slab (SPLIT).  D = 64
-    // leaves in two halves: with dq_tma each 32-column box is staged in the
-    // 128-byte swizzled layout of the accumulator's tensor map (one query row
-    // per thread, conflict-free) and leaves through one TMA tensor copy,
-    // clipped at the end of the rows by the map; otherwise 64 query rows at a
-    // time are staged row-major [query][dim] (the layout of one head's rows in
-    // the head-major accumulator) and leave through one bulk copy of the valid
-    // rows.  D = 128 stages the whole tile ([query][dim], lane = dim) and
-    // leaves through one bulk copy.
+    // accumulator (ATOMIC) or store into this KV tile's slab (SPLIT), in two
+    // halves: with dq_tma each 32-column box is staged in the 128-byte
+    // swizzled layout of the accumulator's tensor map (one query row per
+    // thread, conflict-free) and leaves through one TMA tensor copy, clipped
+    // at the end of the rows by the map; otherwise 64 query rows at a time are
+    // staged row-major [query][dim] (the layout of one head's rows in the
+    // head-major accumulator) and leave through one bulk copy of the valid
+    // rows.
     // dK / dV: at the end of every item, TMEM -> bf16 (dK x scale) -> the same
     // staging tile in the 128-byte swizzled layout of the dK/dV tensor maps ->
     // TMA stores; a THD tile that ends past its sequence is written row by row
@@ -741,7 +493,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         tmem_wait_ld();
         tc_fence_before();
         mbar_arrive(&bar_dq_empty);
-        if constexpr (D == 64) {
+        {
           // two halves through the staging tile: the two 32-dim boxes of the
           // accumulator's map (dq_tma), else query rows 0..63 and 64..127
 #pragma unroll
@@ -786,24 +538,6 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
               }
               bulk_commit();
             }
-          }
-        } else {
-          if (t == 0) bulk_wait_read<0>();   // previous copy finished reading the tile
-          named_bar_sync(2, 128);
-          // lane = head dim, 64 columns = query rows
-#pragma unroll
-          for (int c = 0; c < 64; ++c) sDQ[c * D + t] = __uint_as_float(u[c]);
-          fence_proxy_async_smem();
-          named_bar_sync(2, 128);
-          if (t == 0 && slab_ok) {
-            const int nq = min(BM, w.seq.len - q0);
-            float* dst = base + ((static_cast<size_t>(w.seq.b) * p.heads_q + h) * p.rows_total +
-                                 w.seq.row0 + q0) * D;
-            if (a.split)
-              bulk_store(dst, sDQ, static_cast<uint32_t>(nq) * D * 4);
-            else
-              bulk_reduce_add_f32(dst, sDQ, static_cast<uint32_t>(nq) * D * 4);
-            bulk_commit();
           }
         }
       }

@@ -8,16 +8,22 @@
  *   attn_fwd              O = softmax(scale * Q K^T) V per head, and the row
  *                         log-sum-exp LSE_i = ln sum_j exp(scale * q_i . k_j).
  *   attn_bwd_preprocess   Delta_i = sum_d dO_id * O_id; clears the fp32 dQ
- *                         accumulator when dq_mode is ATTN_DQ_ATOMIC.
+ *                         accumulator when dq_mode is ATTN_DQ_ATOMIC (the
+ *                         order tickets of ATTN_DQ_SPLIT at head_dim 128).
  *   attn_bwd              recomputes P = exp(scale * Q K^T - LSE) tile by tile
  *                         and forms dV = P^T dO, dP = dO V^T,
  *                         dS = P o (dP - Delta), dK = scale dS^T Q,
  *                         dQ = scale dS K.  dQ is accumulated in the workspace
  *                         with fp32 atomics (ATTN_DQ_ATOMIC; #940 description:
- *                         fp32, never bf16, atomics) or as per-KV-tile partials
- *                         (ATTN_DQ_SPLIT; #940 "split+sum template").
- *   attn_bwd_postprocess  dQ = bf16(scale * accumulator) or bf16(scale * sum of
- *                         the partials in ascending KV-tile order).
+ *                         fp32, never bf16, atomics) or in a fixed order
+ *                         (ATTN_DQ_SPLIT; #940 "split+sum template"): at
+ *                         head_dim 64 as per-KV-tile partial slabs, at
+ *                         head_dim 128 added into one accumulator in
+ *                         ascending KV-tile order, each query tile's turn
+ *                         kept by an int32 ticket.
+ *   attn_bwd_postprocess  dQ = bf16(scale * accumulator) or, for the slabs,
+ *                         bf16(scale * sum of the partials in ascending
+ *                         KV-tile order).
  *   sparse_attn_fwd/bwd   the same with a per-token top-k key list over one
  *                         shared KV head of 576 = 512 + 64 dims, values the
  *                         first 512 dims ("[2/2] Add TileLang fused DSA kernels
@@ -66,7 +72,7 @@ typedef enum {
 
 typedef enum {
   ATTN_DQ_ATOMIC = 0, /* fp32 atomic adds into one accumulator (not bitwise reproducible) */
-  ATTN_DQ_SPLIT = 1   /* per-KV-tile partials + ordered sum: bitwise run-to-run identical */
+  ATTN_DQ_SPLIT = 1   /* fixed-order dQ sums: bitwise run-to-run identical */
 } attn_dq_mode_t;
 
 /*
@@ -110,14 +116,17 @@ typedef struct {
 attn_status_t attn_fwd(const attn_problem_t* p, const void* q, const void* k, const void* v,
                        void* o, float* lse, attn_stream_t stream);
 
-/* Bytes of device workspace attn_bwd_preprocess/attn_bwd need for `mode`
- * (fp32 dQ accumulator for ATOMIC, per-KV-tile dQ partials for SPLIT).
- * Returns 0 for an invalid problem. */
+/* Bytes of device workspace attn_bwd_preprocess/attn_bwd need for `mode`:
+ * ATOMIC, the fp32 dQ accumulator (batch x heads_q x rows x head_dim);
+ * SPLIT at head_dim 64, one such slab per 128-row KV tile of the longest
+ * sequence; SPLIT at head_dim 128, the accumulator plus one int32 ticket per
+ * (batch, query head, 128-row tile slot).  Returns 0 for an invalid problem. */
 size_t attn_bwd_workspace_size(const attn_problem_t* p, attn_dq_mode_t mode);
 
 /* Backward preprocess: delta fp32 (same layout as lse) = rowsum(dO * O).
- * In ATOMIC mode it also clears the dQ accumulator inside `workspace`, so it must
- * run before attn_bwd with the same workspace and mode. */
+ * In ATOMIC mode it also clears the dQ accumulator inside `workspace` (SPLIT at
+ * head_dim 128: the tickets), so it must run before attn_bwd with the same
+ * workspace and mode. */
 attn_status_t attn_bwd_preprocess(const attn_problem_t* p, attn_dq_mode_t mode, const void* o,
                                   const void* dout, float* delta, void* workspace,
                                   size_t workspace_bytes, attn_stream_t stream);

@@ -125,6 +125,15 @@ size_t dq_elems(const Problem& k, int D) {
 
 int n_kv_tiles(const Problem& k) { return (k.max_seqlen + 127) / 128; }
 
+// SPLIT at head_dim 128 accumulates in a fixed order into one accumulator,
+// behind one int32 ticket per (batch, query head, 128-row query tile slot);
+// the count is rounded up to whole 16-byte words for the clearing pass.
+size_t dq_tickets(const Problem& k) {
+  const size_t slots = static_cast<size_t>(
+      tile_bound(k.rows_total, k.num_seqs, 128, k.cu_seqlens != nullptr));
+  return (static_cast<size_t>(k.batch) * k.heads_q * slots + 3) / 4 * 4;
+}
+
 attn_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA; }
 
 
@@ -226,7 +235,10 @@ size_t attn_bwd_workspace_size(const attn_problem_t* p, attn_dq_mode_t mode) {
   if (empty) return 0;
   const Problem kp = to_kernel(p);
   const size_t elems = dq_elems(kp, p->head_dim);
-  if (mode == ATTN_DQ_SPLIT) return elems * sizeof(float) * static_cast<size_t>(n_kv_tiles(kp));
+  if (mode == ATTN_DQ_SPLIT) {
+    if (p->head_dim == 128) return (elems + dq_tickets(kp)) * sizeof(float);
+    return elems * sizeof(float) * static_cast<size_t>(n_kv_tiles(kp));
+  }
   return elems * sizeof(float);
 }
 
@@ -241,16 +253,23 @@ attn_status_t attn_bwd_preprocess(const attn_problem_t* p, attn_dq_mode_t mode, 
   if (!aligned16(o) || !aligned16(dout) || !aligned16(delta)) return ATTN_ERR_ALIGNMENT;
   if (empty) return ATTN_OK;
   const size_t need = attn_bwd_workspace_size(p, mode);
-  if (mode == ATTN_DQ_ATOMIC && (!workspace || workspace_bytes < need)) return ATTN_ERR_WORKSPACE;
+  // ATOMIC clears the accumulator; SPLIT at head_dim 128 clears its tickets
+  const bool ordered = mode == ATTN_DQ_SPLIT && p->head_dim == 128;
+  if ((mode == ATTN_DQ_ATOMIC || ordered) && (!workspace || workspace_bytes < need))
+    return ATTN_ERR_WORKSPACE;
   if (workspace && !aligned16(workspace)) return ATTN_ERR_ALIGNMENT;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const Problem kp = to_kernel(p);
+  const size_t elems = dq_elems(kp, p->head_dim);
   float* acc = (mode == ATTN_DQ_ATOMIC) ? static_cast<float*>(workspace) : nullptr;
-  const size_t n = (mode == ATTN_DQ_ATOMIC) ? dq_elems(kp, p->head_dim) : 0;
+  const size_t n = (mode == ATTN_DQ_ATOMIC) ? elems : 0;
+  float* tickets = ordered ? static_cast<float*>(workspace) + elems : nullptr;
+  const size_t nt = ordered ? dq_tickets(kp) : 0;
   const auto* ob = static_cast<const __nv_bfloat16*>(o);
   const auto* db = static_cast<const __nv_bfloat16*>(dout);
-  cudaError_t e = (p->head_dim == 64) ? launch_bwd_preprocess<64>(kp, ob, db, delta, acc, n, st)
-                                      : launch_bwd_preprocess<128>(kp, ob, db, delta, acc, n, st);
+  cudaError_t e = (p->head_dim == 64)
+                      ? launch_bwd_preprocess<64>(kp, ob, db, delta, acc, n, tickets, nt, st)
+                      : launch_bwd_preprocess<128>(kp, ob, db, delta, acc, n, tickets, nt, st);
   return cuda_status(e);
 }
 
@@ -289,6 +308,12 @@ attn_status_t attn_bwd(const attn_problem_t* p, attn_dq_mode_t mode, const void*
   a.split = (mode == ATTN_DQ_SPLIT) ? 1 : 0;
   a.slab_elems = a.split ? dq_elems(kp, D) : 0;
   a.n_split = a.split ? n_kv_tiles(kp) : 0;
+  a.dq_ticket = nullptr;
+  if (a.split && D == 128) {   // one accumulator, ordered by tickets (no slabs)
+    a.slab_elems = 0;
+    a.n_split = 0;
+    a.dq_ticket = reinterpret_cast<int*>(a.dq_acc + dq_elems(kp, D));
+  }
   a.scale_log2 = p->scale * kLog2e;
   // D = 64 stages dQ tiles one query row per thread, which only the swizzled
   // TMA layout keeps free of bank conflicts.  A THD slab store of a tile that
@@ -339,7 +364,9 @@ attn_status_t attn_bwd_postprocess(const attn_problem_t* p, attn_dq_mode_t mode,
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const Problem kp = to_kernel(p);
   const int D = p->head_dim;
-  const int split = (mode == ATTN_DQ_SPLIT) ? 1 : 0;
+  // SPLIT at head_dim 128 leaves one accumulator (filled in a fixed order),
+  // converted like ATOMIC's; head_dim 64 sums its slabs in order
+  const int split = (mode == ATTN_DQ_SPLIT && D == 64) ? 1 : 0;
   const size_t slab = split ? dq_elems(kp, D) : 0;
   const int n_split = split ? n_kv_tiles(kp) : 0;
   const float* acc = static_cast<const float*>(workspace);

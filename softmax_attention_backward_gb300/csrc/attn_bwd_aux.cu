@@ -1,10 +1,12 @@
 // Memory-bound stages around the dense backward:
 //   * preprocess: Delta = rowsum(dO o O) in fp32 (the `flashattn_bwd_preprocess`
 //     stage of tile-ai/tilelang #940) and, for the atomic dQ mode, clearing of
-//     the fp32 dQ accumulator;
-//   * finalize: dQ = bf16(scale * accumulator) for the atomic mode, or
-//     bf16(scale * sum of the per-KV-tile partials in ascending tile order) for
-//     the split mode (the `flashattn_bwd_postprocess` stage of #940 and its
+//     the fp32 dQ accumulator (for the split mode at head_dim 128, of its order
+//     tickets);
+//   * finalize: dQ = bf16(scale * accumulator) for the atomic mode and the
+//     split mode at head_dim 128, or bf16(scale * sum of the per-KV-tile
+//     partials in ascending tile order) for the split mode at head_dim 64
+//     (the `flashattn_bwd_postprocess` stage of #940 and its
 //     split+sum template); THD padding rows of dQ, dK and dV are written as
 //     exact zeros here (the padding contract of cudnn-frontend #427, backward
 //     zero-write commit, tokens beyond cu_seqlens[-1]).
@@ -27,7 +29,9 @@ __global__ void __launch_bounds__(256) attn_bwd_preprocess_kernel(Problem p,
                                                                   const __nv_bfloat16* __restrict__ dout,
                                                                   float* __restrict__ delta,
                                                                   float* __restrict__ dq_acc,
-                                                                  size_t acc_elems) {
+                                                                  size_t acc_elems,
+                                                                  float* __restrict__ clear,
+                                                                  size_t n_clear) {
   constexpr int TPR = D / 8;   // threads per row
   constexpr int RPW = 32 / TPR;   // rows per warp step
   const int end = valid_end(p);
@@ -90,6 +94,10 @@ __global__ void __launch_bounds__(256) attn_bwd_preprocess_kernel(Problem p,
         delta[li] = (static_cast<int>(srow) < end) ? acc[u] : 0.f;
       }
     }
+  }
+  if (clear) {
+    float4* z = reinterpret_cast<float4*>(clear);
+    for (size_t i = gtid; i < n_clear / 4; i += nthreads) z[i] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
   if (dq_acc) {
     // the accumulator is [batch, head, row, dim]: clear the first `end` rows of
@@ -232,10 +240,12 @@ __global__ void __launch_bounds__(256) attn_dq_finalize_kernel(Problem p,
 template <int D>
 cudaError_t launch_bwd_preprocess(const Problem& p, const __nv_bfloat16* o,
                                   const __nv_bfloat16* dout, float* delta, float* dq_acc,
-                                  size_t acc_elems, cudaStream_t st) {
+                                  size_t acc_elems, float* clear, size_t n_clear,
+                                  cudaStream_t st) {
   const size_t rows = static_cast<size_t>(p.batch) * p.rows_total * p.heads_q;
   const int g = resident_grid(attn_bwd_preprocess_kernel<D>, rows * (D / 8), 256);
-  attn_bwd_preprocess_kernel<D><<<g, 256, 0, st>>>(p, o, dout, delta, dq_acc, acc_elems);
+  attn_bwd_preprocess_kernel<D><<<g, 256, 0, st>>>(p, o, dout, delta, dq_acc, acc_elems, clear,
+                                                   n_clear);
   return cudaGetLastError();
 }
 
@@ -254,10 +264,10 @@ cudaError_t launch_dq_finalize(const Problem& p, const float* acc, size_t slab_e
 
 template cudaError_t launch_bwd_preprocess<64>(const Problem&, const __nv_bfloat16*,
                                                const __nv_bfloat16*, float*, float*, size_t,
-                                               cudaStream_t);
+                                               float*, size_t, cudaStream_t);
 template cudaError_t launch_bwd_preprocess<128>(const Problem&, const __nv_bfloat16*,
                                                 const __nv_bfloat16*, float*, float*, size_t,
-                                                cudaStream_t);
+                                                float*, size_t, cudaStream_t);
 template cudaError_t launch_dq_finalize<64>(const Problem&, const float*, size_t, int, int,
                                             __nv_bfloat16*, __nv_bfloat16*, __nv_bfloat16*,
                                             cudaStream_t);

@@ -62,6 +62,24 @@ struct Bwd128 {
   static_assert(SMEM + 1536 <= 227 * 1024, "shared memory budget");
 };
 
+// Step order inside an item: query tiles from the last down to the first, the
+// query heads of the GQA group innermost.  Every K/V tile of a (batch, kv
+// head) then meets query tile i of head h at the same step index,
+// (last - i) * groups + h, whatever its first query tile: the ordered SPLIT
+// accumulation, where K/V tile jt waits for tiles 0 .. jt-1 at each (i, h),
+// keeps all tiles of a head in step instead of throttling each to tile 0.
+__device__ __forceinline__ void next_step(int& ih, int& ii, int groups) {
+  if (++ih == groups) {
+    ih = 0;
+    --ii;
+  }
+}
+
+// kOrdered: the SPLIT mode's fixed-order dQ accumulation (see the drain).
+// Each mode is its own instantiation: the drain loop is sensitive to its code
+// size (the ATOMIC kernel measured 10% slower with the ordered path compiled
+// in).
+template <bool kOrdered>
 __global__ void __launch_bounds__(Bwd128::THREADS, 1)
     attn_bwd128_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
@@ -145,9 +163,9 @@ __global__ void __launch_bounds__(Bwd128::THREADS, 1)
           tma_load_4d(&tmV, &bar_kv_full, sV + pn * BN * 128, pn * 64, w.hk, w.seq.row0 + w.kv0,
                       w.seq.b);
         }
-        int ih = 0, ii = -1;   // step it = ih * n_i + ii
+        int ih = -1, ii = w.n_i - 1;   // step order: see next_step
         for (int it = 0; it < w.n_it; ++it) {
-          if (++ii == w.n_i) { ii = 0; ++ih; }
+          next_step(ih, ii, G);
           const int g = gs + it, sl = g & 1, par = ((g >> 1) & 1) ^ 1;
           const int h = w.hk * G + ih;
           const int row = w.seq.row0 + (w.i_start + ii) * BM;
@@ -290,28 +308,28 @@ __global__ void __launch_bounds__(Bwd128::THREADS, 1)
     BwdItem w;
     int k = 0, gs = 0;
     bool have = next_bwd_item<BN, BM>(p, total, a.n_x, a.x_major, a.fd_nbh, a.fd_nx, k, w);
-    float pf = have ? fetch(w, 0, 0) : 0.f;
+    float pf = have ? fetch(w, 0, w.n_i - 1) : 0.f;
     bool ok = true;
     while (ok && have) {
       const int kv = w.kv0 + r;                        // K/V row inside the sequence
       const bool kv_ok = kv < w.seq.len;
-      int ih = 0, ii = -1;   // step it = ih * n_i + ii
+      int ih = -1, ii = w.n_i - 1;   // step order: see next_step
       for (int it = 0; it < w.n_it; ++it) {
-        if (++ii == w.n_i) { ii = 0; ++ih; }
+        next_step(ih, ii, G);
         const int g = gs + it;
         const int q0 = (w.i_start + ii) * BM;
         named_bar_sync(1, 256);   // every thread has read the previous step's values
         if (tid < BM) s_nlse[tid] = -pf * kLog2e;   // LSE in the log2 domain, negated
         else s_delta[tid - BM] = pf;
         if (it + 1 < w.n_it) {
-          const bool wrap = ii + 1 == w.n_i;
-          pf = fetch(w, wrap ? ih + 1 : ih, wrap ? 0 : ii + 1);
+          const bool wrap = ih + 1 == G;
+          pf = fetch(w, wrap ? 0 : ih + 1, wrap ? ii - 1 : ii);
         } else {
           // last step of the item: look up the next one for the prefetch
           BwdItem wn;
           int kn = k;
           if (next_bwd_item<BN, BM>(p, total, a.n_x, a.x_major, a.fd_nbh, a.fd_nx, kn, wn))
-            pf = fetch(wn, 0, 0);
+            pf = fetch(wn, 0, wn.n_i - 1);
         }
         named_bar_sync(1, 256);
         // ---- P^T (K/V row r, query columns c0 .. c0 + 63), two 32-column chunks ----
@@ -398,8 +416,8 @@ __global__ void __launch_bounds__(Bwd128::THREADS, 1)
     // dQ^T leaves TMEM in one load (64 query columns per warpgroup) and goes
     // to global memory straight from registers: the lane of a thread is a
     // head dim, so one warp instruction covers 32 consecutive dims (128
-    // bytes) of one query row.  ATOMIC adds into the fp32 accumulator with
-    // red.global.add.f32, SPLIT stores into this K/V tile's slab.  Measured
+    // bytes) of one query row, added into the fp32 accumulator with
+    // red.global.add.f32 (ATOMIC; SPLIT in a fixed order, below).  Measured
     // against TMA copies through a shared-memory tile (one 16 KB copy at a
     // time, then eight per-warp 2 KB copies), this keeps the SM's TMA unit
     // for the operand loads, and the freed shared memory holds the second dO
@@ -411,20 +429,23 @@ __global__ void __launch_bounds__(Bwd128::THREADS, 1)
     BwdItem w;
     int k = 0, ic = 0, gs = 0;
     bool ok = true;
-    while (ok && next_bwd_item<BN, BM>(p, total, a.n_x, a.x_major, a.fd_nbh, a.fd_nx, k, w)) {
-      float* base = a.dq_acc;
-      bool slab_ok = true;
-      if (a.split) {
-        if (w.jt >= a.n_split) {
-          slab_ok = false;
-          if (t == 0 && p.err) atomicOr(p.err, ATTN_DEVERR_SEQLEN);
-        } else {
-          base += static_cast<size_t>(w.jt) * a.slab_elems;
-        }
+    // kOrdered: the ticket the last step's adds are behind, released at the
+    // next step once its dQ^T has left TMEM (measured 1.92 ms for the c3
+    // backward against 1.99 with releases batched over four steps, 2.36 with
+    // the query tiles in ascending order)
+    int* pend = nullptr;
+    auto release_pending = [&]() {
+      if (pend) {
+        __threadfence();
+        named_bar_sync(2, 256);
+        if (t == 0) red_release_gpu_add1(pend);
+        pend = nullptr;
       }
-      int ih = 0, ii = -1;   // step it = ih * n_i + ii
+    };
+    while (ok && next_bwd_item<BN, BM>(p, total, a.n_x, a.x_major, a.fd_nbh, a.fd_nx, k, w)) {
+      int ih = -1, ii = w.n_i - 1;   // step order: see next_step
       for (int it = 0; it < w.n_it; ++it) {
-        if (++ii == w.n_i) { ii = 0; ++ih; }
+        next_step(ih, ii, G);
         const int g = gs + it;
         const int h = w.hk * G + ih;
         const int q = (w.i_start + ii) * BM + 64 * grp;   // first query row of this half
@@ -437,19 +458,45 @@ __global__ void __launch_bounds__(Bwd128::THREADS, 1)
         tc_fence_before();
         mbar_arrive(&bar_dq_empty);
         const int nq = min(64, w.seq.len - q);
-        if (!slab_ok || nq <= 0) continue;
-        float* gq = base + ((static_cast<size_t>(w.seq.b) * p.heads_q + h) * p.rows_total +
-                            w.seq.row0 + q) * C::D + tl;
-        if (a.split) {
+        float* gq = a.dq_acc + ((static_cast<size_t>(w.seq.b) * p.heads_q + h) * p.rows_total +
+                                w.seq.row0 + q) * C::D + tl;
+        if constexpr (!kOrdered) {
+          if (nq > 0) {
 #pragma unroll
-          for (int c = 0; c < 64; ++c)
-            if (c < nq) gq[static_cast<size_t>(c) * C::D] = __uint_as_float(u[c]);
+            for (int c = 0; c < 64; ++c)
+              if (c < nq) atomicAdd(gq + static_cast<size_t>(c) * C::D, __uint_as_float(u[c]));
+          }
         } else {
+          // SPLIT (bitwise reproducible): the partials of a query tile go into
+          // the accumulator in ascending K/V tile order.  K/V tile jt waits
+          // until the tile's ticket says jt earlier tiles are in, stores (jt = 0:
+          // the first contribution, the accumulator is not cleared) or adds,
+          // and lets the next tile in.  A ticket only waits for items earlier
+          // in the static item list (smaller jt), which every CTA walks in
+          // order, and all CTAs are resident, so the waits cannot form a cycle;
+          // holding a ticket back by one step does not change that (tile 0
+          // never waits, and the last one is released at the end of the item).
+          int* tk = a.dq_ticket +
+                    (static_cast<size_t>(w.seq.b) * p.heads_q + h) * a.n_x + w.x0 + w.i_start + ii;
+          release_pending();
+          if (t == 0) wait_ticket(tk, w.jt, ac);   // raises the abort flag if it runs out
+          named_bar_sync(2, 256);
+          if (*reinterpret_cast<volatile int*>(&abort_flag)) { ok = false; break; }
+          if (nq > 0) {
+            if (w.jt == 0) {
 #pragma unroll
-          for (int c = 0; c < 64; ++c)
-            if (c < nq) atomicAdd(gq + static_cast<size_t>(c) * C::D, __uint_as_float(u[c]));
+              for (int c = 0; c < 64; ++c)
+                if (c < nq) gq[static_cast<size_t>(c) * C::D] = __uint_as_float(u[c]);
+            } else {
+#pragma unroll
+              for (int c = 0; c < 64; ++c)
+                if (c < nq) atomicAdd(gq + static_cast<size_t>(c) * C::D, __uint_as_float(u[c]));
+            }
+          }
+          pend = tk;
         }
       }
+      if constexpr (kOrdered) release_pending();   // the item's last query tiles
       if (!ok) break;
       // ---- dV and dK (x scale) of this item: dims 64 grp .. 64 grp + 63 of row kv ----
       if (!mbar_wait(&bar_done, ic & 1, ac)) break;
@@ -501,10 +548,10 @@ __global__ void __launch_bounds__(Bwd128::THREADS, 1)
 cudaError_t launch_attn_bwd128(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                                const CUtensorMap& dO, const BwdArgs& a, int grid, cudaStream_t st) {
   using C = Bwd128;
-  cudaError_t e =
-      cudaFuncSetAttribute(attn_bwd128_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  auto kern = a.split ? attn_bwd128_kernel<true> : attn_bwd128_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
-  attn_bwd128_kernel<<<grid, C::THREADS, C::SMEM, st>>>(q, k, v, dO, a);
+  kern<<<grid, C::THREADS, C::SMEM, st>>>(q, k, v, dO, a);
   return cudaGetLastError();
 }
 

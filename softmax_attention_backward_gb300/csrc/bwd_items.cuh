@@ -7,10 +7,12 @@
 namespace attn {
 
 // One work item: K/V tile `jt` (rows kv0 .. kv0 + 127 of the sequence) of kv
-// head `hk`, and the n_it = groups * n_i query tiles it meets.
+// head `hk`, and the n_it = groups * n_i query tiles it meets.  x0 is the tile
+// slot of the sequence's first tile (0 for dense problems), so x0 + i numbers
+// query tile i of the sequence among the n_x slots of a (batch, head).
 struct BwdItem {
   SeqRef seq;
-  int hk, jt, kv0, i_start, n_i, n_it;
+  int hk, jt, kv0, i_start, n_i, n_it, x0;
 };
 
 // Advances the CTA's round counter `k` to its next valid item.  Round k of
@@ -45,6 +47,7 @@ __device__ __forceinline__ bool next_bwd_item(const Problem& p, int total, int n
     w.hk = bh - b * p.heads_kv;
     int jt;
     if (!decode_tile(p, x, b, BN, w.seq, jt)) continue;
+    w.x0 = x - jt;
     if (!x_major && p.causal) jt = (w.seq.len + BN - 1) / BN - 1 - jt;
     w.jt = jt;
     w.kv0 = jt * BN;

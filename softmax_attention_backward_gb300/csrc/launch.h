@@ -59,8 +59,9 @@ struct BwdArgs {
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
   float* dq_acc;        // ATOMIC: accumulator [B, Hq, rows, D]; SPLIT: slab base
-  size_t slab_elems;    // SPLIT: elements per slab (0 for ATOMIC)
-  int n_split;          // SPLIT: number of slabs
+  size_t slab_elems;    // SPLIT, head_dim 64: elements per slab (0 otherwise)
+  int n_split;          // SPLIT, head_dim 64: number of slabs
+  int* dq_ticket;       // SPLIT, head_dim 128: order tickets [batch, head, n_x] (else null)
   int split;            // 1 = SPLIT
   int dq_tma;           // 1 = dQ tiles leave through the TMA map of the accumulator / slabs
   int total_items;      // work items: K/V tile slots x kv heads x batch
@@ -84,10 +85,13 @@ cudaError_t launch_attn_bwd(const CUtensorMap& q, const CUtensorMap& k, const CU
 cudaError_t launch_attn_bwd128(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                                const CUtensorMap& dO,
                                const BwdArgs& a, int grid, cudaStream_t st);
+// `clear` (n_clear 4-byte words, a multiple of 4) is zeroed as well when not
+// null (the order tickets of SPLIT at head_dim 128).
 template <int D>
 cudaError_t launch_bwd_preprocess(const Problem& p, const __nv_bfloat16* o,
                                   const __nv_bfloat16* dout, float* delta, float* dq_acc,
-                                  size_t acc_elems, cudaStream_t st);
+                                  size_t acc_elems, float* clear, size_t n_clear,
+                                  cudaStream_t st);
 template <int D>
 cudaError_t launch_dq_finalize(const Problem& p, const float* acc, size_t slab_elems, int split,
                                int n_split, __nv_bfloat16* dq, __nv_bfloat16* dk,

@@ -152,6 +152,31 @@ __device__ __forceinline__ bool mbar_wait_spin(uint64_t* bar, uint32_t parity, c
   }
 }
 
+// Bounded wait until the int at `tk` (global memory, written by other CTAs)
+// equals `want`, with acquire semantics at GPU scope.
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ bool wait_ticket(const int* tk, int want, const AbortCtx& c) {
+  if (ld_acquire_gpu(tk) == want) return true;
+  const uint64_t t0 = globaltimer();
+  while (true) {
+    __nanosleep(64);
+    if (ld_acquire_gpu(tk) == want) return true;
+    if (*reinterpret_cast<volatile int*>(c.smem_abort)) return false;
+    if (globaltimer() - t0 > c.limit_ns) {
+      raise_error(c, ATTN_DEVERR_TIMEOUT);
+      return false;
+    }
+  }
+}
+// Adds one to the int at `tk` with release semantics at GPU scope.
+__device__ __forceinline__ void red_release_gpu_add1(int* tk) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(tk) : "memory");
+}
+
 // ---------------------------------------------------------------------------
 // TMA (bulk tensor copies global -> shared, completion on an mbarrier)
 // ---------------------------------------------------------------------------

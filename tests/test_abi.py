@@ -79,7 +79,12 @@ def test_thd_validation_and_workspace(L):
     p = _problem(**thd)
     per = 32768 * 16 * 128 * 4
     assert L.attn_bwd_workspace_size(ctypes.byref(p), 0) == per
-    assert L.attn_bwd_workspace_size(ctypes.byref(p), 1) == per * ((3670 + 127) // 128)
+    # SPLIT, head_dim 128: one accumulator + an int32 order ticket per (head,
+    # query tile slot); THD slots: 32768 / 128 + one per sequence
+    assert L.attn_bwd_workspace_size(ctypes.byref(p), 1) == per + 16 * (256 + 4) * 4
+    # SPLIT, head_dim 64: one slab per K/V tile of the longest sequence
+    p64 = _problem(**dict(thd, head_dim=64))
+    assert L.attn_bwd_workspace_size(ctypes.byref(p64), 1) == per // 2 * ((3670 + 127) // 128)
     # workspace missing / too small is rejected before any launch
     args = [ctypes.c_void_p(FAKE)] * 8           # q k v dout lse delta dk dv
     assert L.attn_bwd(ctypes.byref(p), 0, *args, None, 0, None) == 5
@@ -95,7 +100,9 @@ def test_dense_workspace_sizes(L):
     p = _problem(batch=4, seqlen=4096, heads_q=32, heads_kv=8, head_dim=128, causal=1)
     per = 4 * 4096 * 32 * 128 * 4
     assert L.attn_bwd_workspace_size(ctypes.byref(p), 0) == per
-    assert L.attn_bwd_workspace_size(ctypes.byref(p), 1) == per * 32
+    assert L.attn_bwd_workspace_size(ctypes.byref(p), 1) == per + 4 * 32 * 32 * 4
+    p64 = _problem(batch=4, seqlen=4096, heads_q=32, heads_kv=8, head_dim=64, causal=1)
+    assert L.attn_bwd_workspace_size(ctypes.byref(p64), 1) == per // 2 * 32
     assert L.attn_bwd_workspace_size(ctypes.byref(_problem(head_dim=80)), 0) == 0
 
 

@@ -1,7 +1,9 @@
 """GPU tests of the buffer, determinism, graph and error contracts of the C ABI.
 
-- ATTN_DQ_SPLIT gradients are bitwise identical run to run (disjoint partial
-  stores + fixed-order sum), and independent of the workspace contents.
+- ATTN_DQ_SPLIT gradients are bitwise identical run to run (head_dim 64:
+  disjoint partial stores + fixed-order sum; head_dim 128: partials added in
+  K/V tile order behind per-query-tile tickets), and independent of the
+  workspace contents.
 - Every output element is written: buffers pre-filled with NaN come out
   finite, and THD padding rows come out as exact zeros (the exact-zero
   contract of cudnn-frontend #427 for tokens past cu_seqlens[-1]).
@@ -38,6 +40,51 @@ def test_split_mode_is_bitwise_deterministic(D):
     for r in runs[1:]:
         for a, b in zip(runs[0], r):
             assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_split_mode_d128_ordered_accumulation_is_bitwise_deterministic(causal):
+    # head_dim 128 adds the dQ partials of a query tile in K/V tile order behind
+    # a ticket; at this size the K/V tiles of one (batch, kv head) run on many
+    # CTAs at once, so the tickets are contended
+    q, k, v, do = _dense(B=2, S=2048, hq=8, hkv=2, D=128, seed=11)
+    o, lse = A.attn_fwd(q, k, v, causal=causal)
+    n = A.attn_bwd_workspace_size(q, k, mode=A.ATTN_DQ_SPLIT, causal=causal)
+    runs = []
+    for i in range(3):
+        ws = torch.full((n,), 0xFF if i % 2 else 0x7F, dtype=torch.uint8, device=DEV)
+        runs.append(A.dense_backward(q, k, v, o, lse, do, mode=A.ATTN_DQ_SPLIT, causal=causal,
+                                     workspace=ws))
+    for r in runs[1:]:
+        for x, y in zip(runs[0], r):
+            assert torch.equal(x, y)
+    # and the same gradients as the unordered accumulation, up to addition order
+    ref = A.dense_backward(q, k, v, o, lse, do, mode=A.ATTN_DQ_ATOMIC, causal=causal)
+    for name, x, y in zip(("dq", "dk", "dv"), runs[0], ref):
+        assert_close(name, x, y.double().cpu())
+
+
+def test_split_mode_d128_thd_is_bitwise_deterministic():
+    lens = [1500, 1, 700, 2100, 0, 300]
+    cap = sum(lens) + 64
+    q, k, v, do = (t.to(DEV) for t in W.thd_inputs(cap, 8, 2, 128, seed=12))
+    cu = W.cu_seqlens_from(lens).to(DEV)
+    kw = dict(causal=True, cu_seqlens=cu, max_seqlen=max(lens))
+    o, lse = A.attn_fwd(q, k, v, **kw)
+    n = A.attn_bwd_workspace_size(q, k, mode=A.ATTN_DQ_SPLIT, **kw)
+    runs = []
+    for i in range(3):
+        ws = torch.full((n,), 0xFF if i % 2 else 0x7F, dtype=torch.uint8, device=DEV)
+        runs.append(A.dense_backward(q, k, v, o, lse, do, mode=A.ATTN_DQ_SPLIT, workspace=ws,
+                                     **kw))
+    for r in runs[1:]:
+        for x, y in zip(runs[0], r):
+            assert torch.equal(x, y)
+    ref = oracle.thd_backward(*(t.cpu() for t in (q, k, v, do)), cu.cpu(), 128 ** -0.5, True,
+                              seqs=[0, 2])
+    for key, t in zip(("dq", "dk", "dv"), runs[0]):
+        for s0, s1 in ((0, 1500), (1501, 2201)):
+            assert_close(f"{key} rows {s0}..{s1}", t[s0:s1], ref[key][s0:s1])
 
 
 def test_outputs_fully_written_dense():

@@ -83,19 +83,23 @@ def test_dense_small_full(mode, B, S, hq, hkv, D, causal):
 
 
 @pytest.mark.parametrize("mode", MODES)
-@pytest.mark.parametrize("B,S,hq,hkv,D", [
-    (5, 1000, 10, 5, 64),    # persistent grids over 5*5 kv heads, ragged last tile
-    (4, 3000, 6, 2, 128),    # persistent backward, 3:1 groups, ragged last tile
+@pytest.mark.parametrize("B,S,hq,hkv,D,causal", [
+    (5, 1000, 10, 5, 64, True),     # persistent grids over 5*5 kv heads, ragged last tile
+    (4, 3000, 6, 2, 128, True),     # persistent backward, 3:1 groups, ragged last tile
+    (3, 1500, 16, 2, 128, False),   # 8:1 groups, no mask: every K/V tile meets every query tile
+    (2, 2100, 16, 2, 128, True),    # 8:1 groups under the causal mask
 ])
-def test_dense_persistent_odd_shapes_sampled(mode, B, S, hq, hkv, D):
+def test_dense_persistent_odd_shapes_sampled(mode, B, S, hq, hkv, D, causal):
     """More items than SMs with batch * heads and tile counts that are not
     powers of two: the item decoding of the persistent grids (division by
-    invariant integers) on the paths the small cases do not take."""
+    invariant integers) on the paths the small cases do not take, and large
+    GQA groups (the head_dim 128 backward walks a group's query heads
+    innermost)."""
     q, k, v, do = W.dense_inputs(B, S, hq, hkv, D, seed=200 + S)
     scale = D ** -0.5
-    got = run_dense(q, k, v, do, True, scale, mode)
+    got = run_dense(q, k, v, do, causal, scale, mode)
     units = [(0, 0), (B - 1, hkv - 1), (B // 2, hkv // 2)]
-    ref = oracle.dense_backward(q, k, v, do, scale, True, kv_heads=units)
+    ref = oracle.dense_backward(q, k, v, do, scale, causal, kv_heads=units)
     compare_dense(got, ref, units, hq, hkv)
 
 

@@ -461,10 +461,19 @@ __global__ void __launch_bounds__(Bwd128::THREADS, 1)
         float* gq = a.dq_acc + ((static_cast<size_t>(w.seq.b) * p.heads_q + h) * p.rows_total +
                                 w.seq.row0 + q) * C::D + tl;
         if constexpr (!kOrdered) {
+          // The 64 adds per thread are paced over the step: a burst of them
+          // fills the load/store queues the P/dS warps' shared-memory accesses
+          // go through on the step's critical path.  After every 16 adds the
+          // thread sleeps 400 ns unless the next step's dQ^T is already
+          // waiting (c3 backward 1.447 -> 1.332 ms; a fixed 650 ns pause made
+          // the drain the bottleneck, 1.62 ms, hence the test).
           if (nq > 0) {
+            const uint32_t next_full = smem_u32(&bar_dq_full);
 #pragma unroll
-            for (int c = 0; c < 64; ++c)
+            for (int c = 0; c < 64; ++c) {
               if (c < nq) atomicAdd(gq + static_cast<size_t>(c) * C::D, __uint_as_float(u[c]));
+              if ((c & 15) == 15 && c < 63 && !mbar_test_wait(next_full, (g + 1) & 1)) __nanosleep(400);
+            }
           }
         } else {
           // SPLIT (bitwise reproducible): the partials of a query tile go into

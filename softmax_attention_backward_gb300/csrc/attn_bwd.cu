@@ -100,7 +100,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
 
   __shared__ uint64_t bar_kv_full[C::KV_BUFS], bar_kv_empty[C::KV_BUFS];
   __shared__ uint64_t bar_qfull[C::NST], bar_qempty[C::NST];
-  __shared__ uint64_t bar_s, bar_dp, bar_p, bar_ds, bar_pt_done, bar_ds_free;
+  __shared__ uint64_t bar_s, bar_dp, bar_p, bar_ds;
   __shared__ uint64_t bar_done, bar_dq_full, bar_dq_empty;
   __shared__ uint64_t bar_dv_empty, bar_dk_empty;
   __shared__ uint32_t tmem_base_sh;
@@ -128,8 +128,6 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     mbar_init(&bar_dp, 1);
     mbar_init(&bar_p, 256);
     mbar_init(&bar_ds, 256);
-    mbar_init(&bar_pt_done, 1);
-    mbar_init(&bar_ds_free, 1);
     mbar_init(&bar_done, 1);
     mbar_init(&bar_dq_full, 1);
     mbar_init(&bar_dq_empty, 128);
@@ -264,7 +262,6 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
           for (int kk = 0; kk < KV; ++kk)
             umma_ts_w(tmem + C::COL_DV, tmem + C::COL_PT + 8 * kk,
                       desc_advance(omn, mnmajor_step_bytes(kk)), idKV, (it > 0 || kk > 0) ? 1u : 0u);
-          umma_commit_w(&bar_pt_done);
           // ---- phase B: dK(g), dQ(g) [, dP^T(g+1)] ----
           if (!mbar_wait_w(&bar_ds, g & 1, ac)) { ok = false; break; }
           if (!mbar_wait_w(&bar_dq_empty, (g & 1) ^ 1, ac)) { ok = false; break; }
@@ -288,7 +285,6 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
             umma_commit_w(&bar_dp);
           }
           umma_commit_w(&bar_dq_full);
-          umma_commit_w(&bar_ds_free);
           umma_commit_w(&bar_qempty[st]);
           sdp_done = nx;
         }
@@ -367,9 +363,12 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
           // the P^T columns in the dS pass.
           const int lim_all = !kv_ok ? HALF : ((p.causal && q0 < w.kv0 + BN) ? kv - q0 - c0 : 0);
           const uint64_t sl2x2 = f2_pack(sl2, sl2);
-          // P^T(g-1) must have been consumed by dV(g-1)
-          if (g > 0 && !mbar_wait(&bar_pt_done, (g - 1) & 1, ac)) { ok = false; break; }
-          tc_fence_after();
+          // dV(g-1) has read P^T(g-1), and dK(g-1) / dQ(g-1) the dS tile,
+          // once dP^T(g) has completed: the issuer sends dP^T(g) after them,
+          // and its commit arrives only when every earlier MMA has completed.
+          // So one wait on dP^T(g), before the first P^T store, covers both
+          // (separate waits on those phases, long complete, still cost ~300
+          // and ~500 cycles per step on the critical path).
 #pragma unroll 1
           for (int c1 = 0; c1 < HALF; c1 += 32) {
             uint32_t u[32];
@@ -393,15 +392,16 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
               pk[c / 2] = f2_to_bf16x2(f2_pack(ex2(a0), ex2(a1)));
               pk[c / 2 + 1] = f2_to_bf16x2(f2_pack(ex2(a2), ex2(a3)));
             }
+            if (c1 == 0) {
+              if (!mbar_wait(&bar_dp, g & 1, ac)) { ok = false; break; }
+              tc_fence_after();
+            }
             tmem_st16p(tPTme + c1 / 2, pk);
           }
+          if (!ok) break;
           tmem_wait_st();
           tc_fence_before();
           mbar_arrive(&bar_p);
-          if (!mbar_wait(&bar_dp, g & 1, ac)) { ok = false; break; }
-          // dK(g-1) and dQ(g-1) have consumed the dS tile
-          if (g > 0 && !mbar_wait(&bar_ds_free, (g - 1) & 1, ac)) { ok = false; break; }
-          tc_fence_after();
 #pragma unroll 1
           for (int c1 = 0; c1 < HALF; c1 += 32) {
             uint32_t u[32], pp[16];

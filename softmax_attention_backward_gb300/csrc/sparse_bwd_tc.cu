@@ -11,16 +11,20 @@
 //   P    = exp(S c - LSE),  dS = P o (dP - Delta) c        (softmax warps)
 //   dQ^T += K^T dS^T  (value dims on TMEM lanes: four M = 128 tiles for dims
 //                      0..511 and one M = 64 tile for dims 512..575, 64 heads)
-//   dKV[s] += dS^T Q + P^T [dO | 0]   in nine 64-dim pieces (M = 64 slots,
-//                      N = 64 dims), each drained from TMEM into the fp32 dKV
-//                      accumulator with vector reductions while the next
-//                      piece is computed (two piece buffers); in the ordered
+//   dKV[s]^T += Q^T dS + [dO | 0]^T P   in five pieces of value dims (four
+//                      M = 128 pieces for dims 0..511, one M = 64 piece for
+//                      512..575; N = 64 slots), each drained from TMEM into
+//                      the fp32 dKV accumulator while the next piece is
+//                      computed (two piece buffers): a lane holds one dim of
+//                      every slot; groups of four lanes transpose 4 x 4
+//                      blocks by shuffles and add 16-byte vectors, eight
+//                      lanes to 128 bytes of one key row; in the ordered
 //                      (deterministic) path the drain instead stores the
 //                      piece into this (token, slot, head block)'s own
 //                      contribution row, summed later in token order
 //                      (sparse_dkv_ordered.cu)
 // P and dS go through shared memory as bf16 [head][slot] tiles, which serve
-// as the K-major B operand of dQ^T and the MN-major A operand of the dKV
+// as the K-major B operand of dQ^T and the MN-major B operand of the dKV
 // pieces.  The scale c is folded into dS, so dQ and dKV need none later.
 // An M = 64 accumulator keeps row r in TMEM lane 32 (r / 16) + r % 16.
 //
@@ -46,7 +50,7 @@ constexpr int SB_SMEM = SB_Q_BYTES + SB_DO_BYTES + SB_KV_BYTES + 2 * SB_T_BYTES 
 constexpr int SB_THREADS = 352;
 constexpr int SB_PRODUCERS = 64;               // warps 8..9
 static_assert(SB_PRODUCERS == SB_NK, "one producer lane holds each slot's index");
-constexpr int SB_PIECES = SB_DQK / 64;         // 64-dim pieces of a dKV row
+constexpr int SB_PIECES = 5;                   // dKV^T pieces: dims 128 p.. (p < 4), 512..575
 constexpr uint32_t SB_TMEM_COLS = 512;
 constexpr uint32_t SB_COL_S = 0, SB_COL_DP = 64;
 constexpr uint32_t SB_COL_DQ = 128;            // five dQ^T tiles of 64 columns
@@ -64,6 +68,9 @@ __device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float 
 
 }  // namespace
 
+// kContrib: the ordered path (contribution rows) instead of the fp32 reductions;
+// one instantiation per mode keeps the drain loop free of the other's code.
+template <bool kContrib>
 __global__ void __launch_bounds__(SB_THREADS, 1) sparse_bwd_tc_kernel(const SparseArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -199,7 +206,8 @@ __global__ void __launch_bounds__(SB_THREADS, 1) sparse_bwd_tc_kernel(const Spar
       const uint32_t idS = idesc_bf16(64, SB_NK, false, false);        // S, dP
       const uint32_t idQ128 = idesc_bf16(128, SB_HB, true, false);     // dQ^T tiles
       const uint32_t idQ64 = idesc_bf16(64, SB_HB, true, false);       // dQ^T dims 512..575
-      const uint32_t idKV = idesc_bf16(64, 64, true, true);            // dKV pieces
+      const uint32_t idKV128 = idesc_bf16(128, SB_NK, true, true);     // dKV^T pieces 0..3
+      const uint32_t idKV64 = idesc_bf16(64, SB_NK, true, true);       // dKV^T piece 4
       const uint64_t dQk = desc_kmajor_base(smem_u32(sQ));
       const uint64_t ddOk = desc_kmajor_base(smem_u32(sdO));
       const uint64_t dKk = desc_kmajor_base(smem_u32(sKV));
@@ -238,23 +246,23 @@ __global__ void __launch_bounds__(SB_THREADS, 1) sparse_bwd_tc_kernel(const Spar
                     (c > 0 || kk > 0) ? 1u : 0u);
         }
         umma_commit_w(&bar_kv_empty);                // K and V of this chunk are no longer read
-        // dKV pieces: D(slots, dims 64p..) = dS^T Q_p + P^T dO_p
+        // dKV^T pieces: D(dims 128p.., slots) = Q_p^T dS + dO_p^T P
         for (int p = 0; p < SB_PIECES; ++p, ++gp) {
           const int b = gp & 1, use = gp >> 1;
           if (!mbar_wait_w(&bar_pc_free[b], (use & 1) ^ 1, ac)) { ok = false; break; }
           tc_fence_after();
           const uint32_t dst = tmem + (b ? SB_COL_DP : SB_COL_PC);
-          const uint64_t dQmn = desc_mnmajor_base(smem_u32(sQ + p * SB_HB * 128), SB_HB);
+          const uint64_t dQmn = desc_mnmajor_base(smem_u32(sQ + 2 * p * SB_HB * 128), SB_HB);
 #pragma unroll
           for (int kk = 0; kk < SB_HB / 16; ++kk)
-            umma_ss_w(dst, desc_advance(ddSmn, mnmajor_step_bytes(kk)),
-                    desc_advance(dQmn, mnmajor_step_bytes(kk)), idKV, kk > 0);
-          if (p < SB_DV / 64) {
-            const uint64_t ddOmn = desc_mnmajor_base(smem_u32(sdO + p * SB_HB * 128), SB_HB);
+            umma_ss_w(dst, desc_advance(dQmn, mnmajor_step_bytes(kk)),
+                    desc_advance(ddSmn, mnmajor_step_bytes(kk)), p < 4 ? idKV128 : idKV64, kk > 0);
+          if (p < 4) {
+            const uint64_t ddOmn = desc_mnmajor_base(smem_u32(sdO + 2 * p * SB_HB * 128), SB_HB);
 #pragma unroll
             for (int kk = 0; kk < SB_HB / 16; ++kk)
-              umma_ss_w(dst, desc_advance(dPmn, mnmajor_step_bytes(kk)),
-                      desc_advance(ddOmn, mnmajor_step_bytes(kk)), idKV, 1u);
+              umma_ss_w(dst, desc_advance(ddOmn, mnmajor_step_bytes(kk)),
+                      desc_advance(dPmn, mnmajor_step_bytes(kk)), idKV128, 1u);
           }
           umma_commit_w(&bar_pc_full[b]);
           if (b == 1) ++n1;
@@ -266,13 +274,15 @@ __global__ void __launch_bounds__(SB_THREADS, 1) sparse_bwd_tc_kernel(const Spar
     }
   } else if (warp >= 4) {
     // ---------------- dKV drain (warps 4..7) ----------------
+    // warp q reads TMEM lanes 32 q..32 q + 31: dims 128 p + 32 q + lane of
+    // pieces 0..3; of the M = 64 piece 4, lanes 0..15 hold dims 512 + 16 q + lane
     const int q = warp - 4;
-    const bool active = lane < 16;
-    const int slot = 16 * q + (lane & 15);         // slot row of the M = 64 piece
     const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
     int gp = 0;
     bool ok = true;
     for (int c = 0; ok && c < nchunks; ++c) {
+      int j0 = -1, j1 = -1;   // slot rows of the chunk, shuffled to the warp slot by slot
+      const size_t crow0 = (static_cast<size_t>(t) * a.K + c * SB_NK) * gridDim.y + blockIdx.y;
       for (int p = 0; p < SB_PIECES; ++p, ++gp) {
         const int b = gp & 1, use = gp >> 1;
         if (!mbar_wait(&bar_pc_full[b], use & 1, ac)) { ok = false; break; }
@@ -284,24 +294,38 @@ __global__ void __launch_bounds__(SB_THREADS, 1) sparse_bwd_tc_kernel(const Spar
         tmem_wait_ld();
         tc_fence_before();
         mbar_arrive(&bar_pc_free[b]);
-        const int j = active ? s_row[c & 3][slot] : -1;
-        if (j >= 0 && a.contrib) {
-          // ordered path: this (token, slot, head block) row, stored once
-          float* dst = a.contrib +
-                       ((static_cast<size_t>(t) * a.K + c * SB_NK + slot) * gridDim.y + blockIdx.y) *
-                           SB_DQK +
-                       64 * p;
+        if (p == 0) {   // written before the chunk's first piece was issued
+          j0 = s_row[c & 3][lane];
+          j1 = s_row[c & 3][32 + lane];
+        }
+        const bool lane_ok = p < 4 || lane < 16;
+        const int d = p < 4 ? 128 * p + 32 * q + lane : 512 + 16 * q + (lane & 15);
+        // four lanes (dims d0..d0 + 3) transpose their 4 x 4 block of four
+        // slots by two butterfly exchanges, so that lane r then holds dims
+        // d0..d0 + 3 of slot s0 + r: one 16-byte access per lane, eight lanes
+        // covering 128 bytes of the same destination row
+        const int r = lane & 3;
+        const bool hi = (r & 2) != 0, od = (r & 1) != 0;
+        const int d0 = d - r;
 #pragma unroll
-          for (int i = 0; i < 16; ++i)
-            *reinterpret_cast<float4*>(dst + 4 * i) =
-                make_float4(__uint_as_float(u[4 * i]), __uint_as_float(u[4 * i + 1]),
-                            __uint_as_float(u[4 * i + 2]), __uint_as_float(u[4 * i + 3]));
-        } else if (j >= 0) {
-          float* dst = a.dkv_acc + static_cast<size_t>(j) * SB_DQK + 64 * p;
-#pragma unroll
-          for (int i = 0; i < 16; ++i)
-            red_add_v4(dst + 4 * i, __uint_as_float(u[4 * i]), __uint_as_float(u[4 * i + 1]),
-                       __uint_as_float(u[4 * i + 2]), __uint_as_float(u[4 * i + 3]));
+        for (int s0 = 0; s0 < SB_NK; s0 += 4) {
+          float v0 = __uint_as_float(u[s0]), v1 = __uint_as_float(u[s0 + 1]);
+          float v2 = __uint_as_float(u[s0 + 2]), v3 = __uint_as_float(u[s0 + 3]);
+          float x0 = __shfl_xor_sync(0xffffffffu, hi ? v0 : v2, 2);
+          float x1 = __shfl_xor_sync(0xffffffffu, hi ? v1 : v3, 2);
+          if (hi) { v0 = x0; v1 = x1; } else { v2 = x0; v3 = x1; }
+          x0 = __shfl_xor_sync(0xffffffffu, od ? v0 : v1, 1);
+          x1 = __shfl_xor_sync(0xffffffffu, od ? v2 : v3, 1);
+          if (od) { v0 = x0; v2 = x1; } else { v1 = x0; v3 = x1; }
+          const int j = __shfl_sync(0xffffffffu, s0 < 32 ? j0 : j1, (s0 & 31) + r);
+          if (j >= 0 && lane_ok) {
+            if constexpr (kContrib)   // this (token, slot, head block) row, stored once
+              __stcs(reinterpret_cast<float4*>(
+                         a.contrib + (crow0 + static_cast<size_t>(s0 + r) * gridDim.y) * SB_DQK + d0),
+                     make_float4(v0, v1, v2, v3));
+            else
+              red_add_v4(a.dkv_acc + static_cast<size_t>(j) * SB_DQK + d0, v0, v1, v2, v3);
+          }
         }
       }
     }
@@ -397,11 +421,11 @@ __global__ void __launch_bounds__(SB_THREADS, 1) sparse_bwd_tc_kernel(const Spar
 }
 
 cudaError_t launch_sparse_bwd_main(const SparseArgs& a, cudaStream_t st) {
-  cudaError_t e = cudaFuncSetAttribute(sparse_bwd_tc_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, SB_SMEM);
+  auto kern = a.contrib ? sparse_bwd_tc_kernel<true> : sparse_bwd_tc_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SB_SMEM);
   if (e != cudaSuccess) return e;
   dim3 grid(a.T, (a.H + SB_HB - 1) / SB_HB);
-  sparse_bwd_tc_kernel<<<grid, SB_THREADS, SB_SMEM, st>>>(a);
+  kern<<<grid, SB_THREADS, SB_SMEM, st>>>(a);
   return cudaGetLastError();
 }
 

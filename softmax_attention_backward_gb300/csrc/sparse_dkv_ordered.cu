@@ -105,28 +105,36 @@ __global__ void __launch_bounds__(kCsrThreads) csr_fill_kernel(const int32_t* __
   }
 }
 
-// One warp per key row: lane l owns dims 2l + 64k, k = 0..8 (float2 each).
-__global__ void __launch_bounds__(256) dkv_reduce_kernel(const float* __restrict__ contrib,
-                                                         const int32_t* __restrict__ entries,
-                                                         const int32_t* __restrict__ off, int T,
-                                                         int nhb, __nv_bfloat16* __restrict__ dkv) {
-  const int j = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  if (j >= T) return;
+// One CTA of kRedWarps warps per key row.  The row's contribution rows (in
+// entry order) are cut into kRedWarps contiguous segments of equal count;
+// warp w sums segment w in order, lane l owning dims 2l + 64k, k = 0..8
+// (float2 each), and the partial sums are added in warp order.  The tree
+// depends only on the entry list, so the result is bitwise repeatable, and
+// the rows named by many tokens (the first rows under a causal selection)
+// are spread over eight warps instead of setting the kernel's length.
+constexpr int kRedWarps = 8;
+
+__global__ void __launch_bounds__(32 * kRedWarps) dkv_reduce_kernel(
+    const float* __restrict__ contrib, const int32_t* __restrict__ entries,
+    const int32_t* __restrict__ off, int T, int nhb, __nv_bfloat16* __restrict__ dkv) {
+  __shared__ float2 part[kRedWarps][kDqk / 2];
+  const int j = blockIdx.x;
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
   float acc[18];
 #pragma unroll
   for (int i = 0; i < 18; ++i) acc[i] = 0.f;
   const int e0 = off[j], e1 = off[j + 1];
-  const int nrow = (e1 - e0) * nhb;   // contribution rows of key row j, in order
+  const long long nrow = static_cast<long long>(e1 - e0) * nhb;   // contribution rows of key row j
+  const int i_end = static_cast<int>(nrow * (w + 1) / kRedWarps);
   auto row_of = [&](int i) -> const float2* {
     const int e = e0 + i / nhb, h = i - (i / nhb) * nhb;
     const size_t base = (static_cast<size_t>(__ldg(entries + e)) * nhb + h) * kDqk;
     return reinterpret_cast<const float2*>(contrib + base) + lane;
   };
-  int i = 0;
+  int i = static_cast<int>(nrow * w / kRedWarps);
   // four rows in flight per warp (the loads of a row are independent of the
   // sums, so they overlap; the additions stay in row order)
-  for (; i + 4 <= nrow; i += 4) {
+  for (; i + 4 <= i_end; i += 4) {
     float2 v[4][9];
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
@@ -142,7 +150,7 @@ __global__ void __launch_bounds__(256) dkv_reduce_kernel(const float* __restrict
         acc[2 * k + 1] += v[u][k].y;
       }
   }
-  for (; i < nrow; ++i) {
+  for (; i < i_end; ++i) {
     const float2* r = row_of(i);
     float2 v[9];
 #pragma unroll
@@ -153,9 +161,19 @@ __global__ void __launch_bounds__(256) dkv_reduce_kernel(const float* __restrict
       acc[2 * k + 1] += v[k].y;
     }
   }
-  uint32_t* out = reinterpret_cast<uint32_t*>(dkv + static_cast<size_t>(j) * kDqk);
 #pragma unroll
-  for (int k = 0; k < 9; ++k) out[lane + 32 * k] = pack_bf16(acc[2 * k], acc[2 * k + 1]);
+  for (int k = 0; k < 9; ++k) part[w][lane + 32 * k] = make_float2(acc[2 * k], acc[2 * k + 1]);
+  __syncthreads();
+  uint32_t* out = reinterpret_cast<uint32_t*>(dkv + static_cast<size_t>(j) * kDqk);
+  for (int d = threadIdx.x; d < kDqk / 2; d += 32 * kRedWarps) {
+    float2 sum = part[0][d];
+#pragma unroll
+    for (int u = 1; u < kRedWarps; ++u) {
+      sum.x += part[u][d].x;
+      sum.y += part[u][d].y;
+    }
+    out[d] = pack_bf16(sum.x, sum.y);
+  }
 }
 
 }  // namespace
@@ -192,9 +210,8 @@ cudaError_t launch_sparse_csr(const int32_t* idx, int T, int K, const SparseCsrL
 cudaError_t launch_sparse_dkv_reduce(const float* contrib, const int32_t* entries,
                                      const int32_t* off, int T, int nhb, __nv_bfloat16* dkv,
                                      cudaStream_t st) {
-  const int warps_per_block = 8;
-  dkv_reduce_kernel<<<(T + warps_per_block - 1) / warps_per_block, 32 * warps_per_block, 0, st>>>(
-      contrib, entries, off, T, nhb, dkv);
+  if (T <= 0) return cudaSuccess;
+  dkv_reduce_kernel<<<T, 32 * kRedWarps, 0, st>>>(contrib, entries, off, T, nhb, dkv);
   return cudaGetLastError();
 }
 

@@ -227,7 +227,9 @@ attn_status_t sparse_attn_bwd(const sparse_attn_problem_t* p, const void* q, con
  * shared accumulator, the main kernel stores each (token, slot, 64-head block)
  * contribution to dkv once in the workspace; the index lists are inverted
  * into a per-key-row list of (token, slot) in ascending token order, and each
- * key row sums its contributions in that order (fp32) before the bf16 cast.
+ * key row sums its contributions in a fixed order set by that list alone (fp32:
+ * eight contiguous segments of the list, each summed in list order, then the
+ * segment sums in segment order) before the bf16 cast.
  * Workspace: tokens * topk * ceil(heads / 64) * dim_qk fp32 contribution rows
  * plus Delta and the inverted lists (tokens * topk int32 and small tables);
  * at tokens 8192, topk 2048, 64 heads about 38.7 GB. */

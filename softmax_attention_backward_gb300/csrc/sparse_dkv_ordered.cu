@@ -14,9 +14,11 @@
 //          across key rows (row offsets)
 //   fill   each token block walks its tokens in order and appends (t, slot)
 //          at its row's running position
-// and one warp per key row sums its contribution rows in that order and
-// writes the bf16 dKV row.  The result is bitwise reproducible; it differs
-// from the atomic path only in the order of the fp32 additions.
+// and one CTA per key row sums its contribution rows in a fixed tree (eight
+// contiguous segments of the ordered list, each summed in order by a warp,
+// then the segment sums in segment order) and writes the bf16 dKV row.  The
+// result is bitwise reproducible; it differs from the atomic path only in the
+// order of the fp32 additions.
 #include <cuda_runtime.h>
 
 #include "launch.h"

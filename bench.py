@@ -647,7 +647,6 @@ def csa_bytes(x, ratio, coff):
 
 def bench_csa(args, dev, flush):
     import softmax_attention_backward_gb300 as A
-    stream = torch.cuda.current_stream()
     hbm = peaks()[0]["hbm_gbs"]
     pk_kind = peaks()[1]
     res = {}
@@ -673,20 +672,7 @@ def bench_csa(args, dev, flush):
                                  g["cu_seqlens_comp"], workspace=ws, dkv=dkv, dscore=dsc,
                                  dape=dape, **kw)
 
-        times = {}
-        for key, fn in (("fwd", fwd), ("bwd", bwd)):
-            for _ in range(3):
-                fn()
-            ms = []
-            for _ in range(iters):
-                flush.zero_()
-                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                e0.record(stream)
-                fn()
-                e1.record(stream)
-                torch.cuda.synchronize()
-                ms.append(e0.elapsed_time(e1))
-            times[key] = statistics.median(ms)
+        times = {key: _time(fn, flush, iters) for key, fn in (("fwd", fwd), ("bwd", bwd))}
         fb, bb = csa_bytes(x, c["ratio"], c["coff"])
         page = CSA_PAGE_B200_US[name]
         res[name] = {
@@ -697,7 +683,7 @@ def bench_csa(args, dev, flush):
             "bytes": {"fwd": fb, "bwd": bb},
             "page_b200_us": {"fwd": page[0], "bwd": page[1]},
         }
-    return {"ratio": 4, "coff": 2, "iters": iters, "timing": "median, L2 flushed before each launch",
+    return {"ratio": 4, "coff": 2, "iters": iters, "timing": "median of CUDA-graph replays, L2 flushed before each",
             "peak": hbm, "peak_kind": f"{pk_kind} copy", "launches_per_bwd": 2,
             "roofline": {"kernel": "csa_bwd_kernel<4,2> (+ dape reduce) at csa_3x8192_d512",
                          "bound": "hbm", "achieved": res["csa_3x8192_d512"]["bwd_gbs"],
@@ -713,15 +699,29 @@ def bench_csa(args, dev, flush):
 # DSA lightning indexer (logits, top-k, backward) and the sparse KL loss
 # ----------------------------------------------------------------------------
 def _time(fn, flush, iters):
+    """Median device time of fn's launches after an L2 flush, replayed from a
+    CUDA graph captured once: the host work of the Python binding stays out of
+    the timed region (for a few-microsecond kernel it takes longer than the
+    flush, and the GPU would sit idle inside the events waiting for the launch)."""
     stream = torch.cuda.current_stream()
     for _ in range(3):
         fn()
+    side = torch.cuda.Stream()
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        fn()
+    stream.wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        fn()
+    torch.cuda.synchronize()
     ms = []
     for _ in range(iters):
         flush.zero_()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        fn()
+        graph.replay()
         e1.record(stream)
         torch.cuda.synchronize()
         ms.append(e0.elapsed_time(e1))
@@ -765,7 +765,7 @@ def bench_indexer(args, dev, flush):
     f_kl = 2.0 * kl_pairs * ws.heads_q * 576
     tf = lambda f, ms: f / (ms * 1e-3) / 1e12
     return {
-        "workload": c["name"], "iters": iters, "timing": "median, L2 flushed before each launch",
+        "workload": c["name"], "iters": iters, "timing": "median of CUDA-graph replays, L2 flushed before each",
         "fwd": {"kernel": "dsa_indexer_logits_kernel", "us": 1e3 * t_fwd, "tflops": tf(f_fwd, t_fwd),
                 "frac": tf(f_fwd, t_fwd) / peak, "flops": f_fwd},
         "topk": {"kernel": "dsa_topk_kernel", "us": 1e3 * t_topk, "gbs": b_topk / t_topk / 1e6,

@@ -46,16 +46,36 @@ struct CsaArgs {
   int32_t* err;
 };
 
+// Segment boundaries (cu_seqlens, cu_seqlens_comp) as the kernels read them:
+// staged once per CTA in shared memory when there are at most kSegCache
+// segments (one global round trip instead of two dependent ones per row),
+// else straight from global memory.
+constexpr int kSegCache = 511;
+struct SegTab {
+  const int32_t* cu;
+  const int32_t* cuc;
+};
+
+__device__ __forceinline__ SegTab stage_segments(const CsaArgs& a, int32_t* s_cu, int32_t* s_cuc) {
+  if (a.nseq > kSegCache) return SegTab{a.cu, a.cuc};   // CTA-uniform
+  for (int i = threadIdx.x; i <= a.nseq; i += blockDim.x) {
+    s_cu[i] = __ldg(a.cu + i);
+    s_cuc[i] = __ldg(a.cuc + i);
+  }
+  __syncthreads();
+  return SegTab{s_cu, s_cuc};
+}
+
 // Token range and compressed rows of segment n, validated on the device.
 struct Seg {
   int tok0, len, row0, nb;
   bool ok;
 };
 
-__device__ __forceinline__ Seg load_seg(const CsaArgs& a, int n, int ratio) {
+__device__ __forceinline__ Seg load_seg(const CsaArgs& a, const SegTab& tb, int n, int ratio) {
   Seg s;
-  const int t0 = __ldg(a.cu + n), t1 = __ldg(a.cu + n + 1);
-  const int c0 = __ldg(a.cuc + n), c1 = __ldg(a.cuc + n + 1);
+  const int t0 = tb.cu[n], t1 = tb.cu[n + 1];
+  const int c0 = tb.cuc[n], c1 = tb.cuc[n + 1];
   s.ok = 0 <= t0 && t0 <= t1 && t1 <= a.T && 0 <= c0 && c0 <= c1 && c1 <= a.C;
   s.tok0 = min(max(t0, 0), a.T);
   s.len = s.ok ? t1 - t0 : 0;
@@ -70,12 +90,12 @@ __device__ __forceinline__ Seg load_seg(const CsaArgs& a, int n, int ratio) {
 }
 
 // Segment of compressed row c (the last n with cuc[n] <= c), or -1.
-__device__ __forceinline__ int row_segment(const CsaArgs& a, int c) {
-  if (c < __ldg(a.cuc) || c >= __ldg(a.cuc + a.nseq)) return -1;
+__device__ __forceinline__ int row_segment(const CsaArgs& a, const SegTab& tb, int c) {
+  if (c < tb.cuc[0] || c >= tb.cuc[a.nseq]) return -1;
   int lo = 0, hi = a.nseq;
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
-    if (__ldg(a.cuc + mid) <= c) lo = mid; else hi = mid;
+    if (tb.cuc[mid] <= c) lo = mid; else hi = mid;
   }
   return lo;
 }
@@ -119,7 +139,8 @@ __device__ __forceinline__ void unpack4(uint2 u, float* f) {
   f[0] = x.x; f[1] = x.y; f[2] = y.x; f[3] = y.y;
 }
 
-// APE of the thread's 4 dims for every window entry (the same for every row).
+// APE of the thread's 4 dims for every window entry (the same for every row),
+// times log2 e: the softmax runs in base 2.
 template <int R, int COFF>
 __device__ __forceinline__ void load_ape(const CsaArgs& a, int d, float (&ap)[R * COFF][4]) {
   using Wn = Win<R, COFF>;
@@ -127,7 +148,7 @@ __device__ __forceinline__ void load_ape(const CsaArgs& a, int d, float (&ap)[R 
   for (int e = 0; e < Wn::N; ++e) {
     const float4 x = __ldg(reinterpret_cast<const float4*>(
         a.ape + static_cast<size_t>(Wn::r(e)) * a.ld + Wn::off(e, a.D) + d));
-    ap[e][0] = x.x; ap[e][1] = x.y; ap[e][2] = x.z; ap[e][3] = x.w;
+    ap[e][0] = x.x * kLog2e; ap[e][1] = x.y * kLog2e; ap[e][2] = x.z * kLog2e; ap[e][3] = x.w * kLog2e;
   }
 }
 
@@ -149,12 +170,16 @@ __device__ __forceinline__ void load_window(const CsaArgs& a, int t0, bool has_p
 }
 
 // Softmax over the window per dim (masked entries excluded) and the pooled
-// output; the weights go to w when W is true.
+// output; the weights go to w when W is true.  Base 2: with ap holding
+// log2 e * ape, (score + ape) log2 e is one FMA per entry and dim, and the
+// exponent is ex2.approx.
 template <int R, int COFF, bool W>
 __device__ __forceinline__ void pool(const uint2 (&v)[R * COFF], const uint2 (&sr)[R * COFF],
                                      const float (&ap)[R * COFF][4], bool has_prev,
                                      float (&w)[W ? R * COFF : 1][4], float* o) {
   constexpr int N = R * COFF;
+  // the exponent argument is recomputed in the second pass rather than kept:
+  // one FMA against 4 N live registers
   float m[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
   for (int e = 0; e < N; ++e) {
@@ -162,7 +187,7 @@ __device__ __forceinline__ void pool(const uint2 (&v)[R * COFF], const uint2 (&s
     float x[4];
     unpack4(sr[e], x);
 #pragma unroll
-    for (int k = 0; k < 4; ++k) m[k] = fmaxf(m[k], x[k] + ap[e][k]);
+    for (int k = 0; k < 4; ++k) m[k] = fmaxf(m[k], fmaf(x[k], kLog2e, ap[e][k]));
   }
   float z[4] = {0.f, 0.f, 0.f, 0.f}, acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -173,7 +198,7 @@ __device__ __forceinline__ void pool(const uint2 (&v)[R * COFF], const uint2 (&s
     const bool on = e < R || has_prev;
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      const float ew = on ? exp2f((x[k] + ap[e][k] - m[k]) * kLog2e) : 0.f;
+      const float ew = on ? ex2(fmaf(x[k], kLog2e, ap[e][k]) - m[k]) : 0.f;
       if (W) w[W ? e : 0][k] = ew;
       z[k] += ew;
       acc[k] = fmaf(ew, y[k], acc[k]);
@@ -181,7 +206,7 @@ __device__ __forceinline__ void pool(const uint2 (&v)[R * COFF], const uint2 (&s
   }
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
-    const float inv = 1.f / z[k];
+    const float inv = __fdividef(1.f, z[k]);
     if (W) {
 #pragma unroll
       for (int e = 0; e < N; ++e) w[W ? e : 0][k] *= inv;
@@ -193,11 +218,12 @@ __device__ __forceinline__ void pool(const uint2 (&v)[R * COFF], const uint2 (&s
 // Window of row c into registers; false when c is a padding row or belongs to a
 // rejected segment.
 template <int R, int COFF>
-__device__ __forceinline__ bool fwd_row(const CsaArgs& a, int c, int d, uint2 (&v)[R * COFF],
-                                        uint2 (&sc)[R * COFF], bool& has_prev) {
-  const int n = row_segment(a, c);
+__device__ __forceinline__ bool fwd_row(const CsaArgs& a, const SegTab& tb, int c, int d,
+                                        uint2 (&v)[R * COFF], uint2 (&sc)[R * COFF],
+                                        bool& has_prev) {
+  const int n = row_segment(a, tb, c);
   if (n < 0) return false;
-  const Seg s = load_seg(a, n, R);
+  const Seg s = load_seg(a, tb, n, R);
   const int b = c - s.row0;
   if (!s.ok || b >= s.nb) {
     if (threadIdx.x % kTPR == 0) flag(a, ATTN_DEVERR_LAYOUT);
@@ -208,29 +234,36 @@ __device__ __forceinline__ bool fwd_row(const CsaArgs& a, int c, int d, uint2 (&
   return true;
 }
 
-// Persistent grid: each thread takes two rows per pass (rows c and c + stride),
-// both windows loaded before either is reduced, so twice the loads are in
-// flight and the per-row segment lookups overlap.
-template <int R, int COFF>
+// Persistent grid: each thread takes RPT rows per pass (c, c + stride, ...),
+// all windows loaded before any is reduced, so that RPT times the loads are in
+// flight and the per-row segment lookups overlap.  RPT = 1 when the rows fit in
+// about four CTAs per SM that way (more threads for the short problems), else 2.
+template <int R, int COFF, int RPT>
 __global__ void __launch_bounds__(kThreads, (R * COFF <= 8) ? 2 : 1) csa_fwd_kernel(const CsaArgs a) {
   constexpr int N = R * COFF;
+  __shared__ int32_t s_cu[kSegCache + 1], s_cuc[kSegCache + 1];
   const int tx = threadIdx.x % kTPR, ty = threadIdx.x / kTPR;
   const int d = blockIdx.x * kDC + tx * kVec;
   const int stride = gridDim.y * kRPB;
   float ap[N][4];
-  load_ape<R, COFF>(a, d, ap);
+  load_ape<R, COFF>(a, d, ap);   // in flight while the segment table is staged
+  const SegTab tb = stage_segments(a, s_cu, s_cuc);
   float unused[1][4];
-  for (int c = blockIdx.y * kRPB + ty; c < a.C; c += 2 * stride) {
-    const int c2 = c + stride;
-    uint2 v[N], v2[N], sc[N], sc2[N];
-    bool hp = false, hp2 = false;
-    const bool on = fwd_row<R, COFF>(a, c, d, v, sc, hp);
-    const bool on2 = c2 < a.C && fwd_row<R, COFF>(a, c2, d, v2, sc2, hp2);
-    float o[4] = {0.f, 0.f, 0.f, 0.f}, o2[4] = {0.f, 0.f, 0.f, 0.f};
-    if (on) pool<R, COFF, false>(v, sc, ap, hp, unused, o);
-    if (on2) pool<R, COFF, false>(v2, sc2, ap, hp2, unused, o2);
-    st4(a.out + static_cast<size_t>(c) * a.D + d, o);
-    if (c2 < a.C) st4(a.out + static_cast<size_t>(c2) * a.D + d, o2);
+  for (int c = blockIdx.y * kRPB + ty; c < a.C; c += RPT * stride) {
+    uint2 v[RPT][N], sc[RPT][N];
+    bool hp[RPT], on[RPT];
+#pragma unroll
+    for (int u = 0; u < RPT; ++u) {
+      hp[u] = false;
+      on[u] = c + u * stride < a.C && fwd_row<R, COFF>(a, tb, c + u * stride, d, v[u], sc[u], hp[u]);
+    }
+#pragma unroll
+    for (int u = 0; u < RPT; ++u) {
+      if (c + u * stride >= a.C) continue;
+      float o[4] = {0.f, 0.f, 0.f, 0.f};
+      if (on[u]) pool<R, COFF, false>(v[u], sc[u], ap, hp[u], unused, o);
+      st4(a.out + static_cast<size_t>(c + u * stride) * a.D + d, o);
+    }
   }
 }
 
@@ -243,16 +276,18 @@ template <int R, int COFF>
 __global__ void __launch_bounds__(kThreads, (R * COFF <= 8) ? 2 : 1) csa_bwd_kernel(const CsaArgs a) {
   constexpr int N = R * COFF;
   extern __shared__ float dacc[];              // [N * 4][kThreads]
+  __shared__ int32_t s_cu[kSegCache + 1], s_cuc[kSegCache + 1];
   const int tx = threadIdx.x % kTPR, ty = threadIdx.x / kTPR;
   const int d = blockIdx.x * kDC + tx * kVec;
-  for (int i = 0; i < N * 4; ++i) dacc[i * kThreads + threadIdx.x] = 0.f;
   float ap[N][4];
-  load_ape<R, COFF>(a, d, ap);
+  load_ape<R, COFF>(a, d, ap);   // in flight while the segment table is staged
+  for (int i = 0; i < N * 4; ++i) dacc[i * kThreads + threadIdx.x] = 0.f;
+  const SegTab tb = stage_segments(a, s_cu, s_cuc);
 
   for (int c = blockIdx.y * kRPB + ty; c < a.C; c += gridDim.y * kRPB) {
-    const int n = row_segment(a, c);
+    const int n = row_segment(a, tb, c);
     if (n < 0) continue;                       // padding row: its dout is ignored
-    const Seg s = load_seg(a, n, R);
+    const Seg s = load_seg(a, tb, n, R);
     const int b = c - s.row0;
     if (!s.ok || b >= s.nb) {
       if (tx == 0) flag(a, ATTN_DEVERR_LAYOUT);
@@ -304,12 +339,12 @@ __global__ void __launch_bounds__(kThreads, (R * COFF <= 8) ? 2 : 1) csa_bwd_ker
   // Segments without a compressed row (shorter than ratio, or rejected
   // layouts): every token is zero.  Then the padding tokens.
   for (int n = blockIdx.y * kRPB + ty; n < a.nseq; n += gridDim.y * kRPB) {
-    const Seg s = load_seg(a, n, R);
+    const Seg s = load_seg(a, tb, n, R);
     if (s.nb > 0) continue;
     int t_lo = s.tok0, t_hi = s.tok0 + s.len;
     if (!s.ok) {                                // zero what the segment claims, in bounds
-      t_lo = min(max(__ldg(a.cu + n), 0), a.T);
-      t_hi = min(max(__ldg(a.cu + n + 1), t_lo), a.T);
+      t_lo = min(max(tb.cu[n], 0), a.T);
+      t_hi = min(max(tb.cu[n + 1], t_lo), a.T);
       if (tx == 0) flag(a, ATTN_DEVERR_LAYOUT);
     }
     for (int t = t_lo; t < t_hi; ++t) {
@@ -321,7 +356,7 @@ __global__ void __launch_bounds__(kThreads, (R * COFF <= 8) ? 2 : 1) csa_bwd_ker
       }
     }
   }
-  const int end = min(max(__ldg(a.cu + a.nseq), 0), a.T);
+  const int end = min(max(tb.cu[a.nseq], 0), a.T);
   for (int t = end + blockIdx.y * kRPB + ty; t < a.T; t += gridDim.y * kRPB) {
 #pragma unroll
     for (int h = 0; h < COFF; ++h) {
@@ -438,15 +473,20 @@ extern "C" attn_status_t csa_compressor_fwd(const csa_compressor_problem_t* p, c
   a.score = static_cast<const __nv_bfloat16*>(score);
   a.ape = ape;
   a.out = static_cast<__nv_bfloat16*>(out);
-  // about four CTAs per SM (two rows per thread and pass)
+  // about four CTAs per SM: one row per thread and pass when the rows fit
+  // that way, else two
   const int ndc = p->head_dim / kDC;
   const int sms = sm_count() > 0 ? sm_count() : 1;
-  const int need = (p->comp_capacity + 2 * kRPB - 1) / (2 * kRPB);
   const int cap = (4 * sms + ndc - 1) / ndc;
-  const dim3 grid(ndc, need < cap ? need : cap);
+  const int need1 = (p->comp_capacity + kRPB - 1) / kRPB;
+  const int need2 = (p->comp_capacity + 2 * kRPB - 1) / (2 * kRPB);
+  const bool one = need1 <= cap;
+  const dim3 grid(ndc, one ? need1 : (need2 < cap ? need2 : cap));
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const cudaError_t e = dispatch(p->ratio, p->coff, [&](auto R, auto CF) {
-    csa_fwd_kernel<decltype(R)::value, decltype(CF)::value><<<grid, kThreads, 0, st>>>(a);
+    constexpr int r = decltype(R)::value, cf = decltype(CF)::value;
+    if (one) csa_fwd_kernel<r, cf, 1><<<grid, kThreads, 0, st>>>(a);
+    else csa_fwd_kernel<r, cf, 2><<<grid, kThreads, 0, st>>>(a);
     return cudaGetLastError();
   });
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;

@@ -16,8 +16,9 @@
 // found by up to four 8-bit radix passes (warp-aggregated histogram atomics, a
 // warp-parallel digit pick, and an early stop once a digit's bin holds exactly
 // the keys still needed); the selected positions (ties toward the smaller
-// index) are then compacted in index order with block-wide scans, which yields
-// the ascending key order directly.
+// index) are then compacted in index order, each warp walking a contiguous
+// segment with ballot counts and one scan of the warp totals, which yields the
+// ascending key order directly.
 //
 // dsa_indexer_bwd_kernel (tcgen05): one CTA per token.  Its query heads
 // (64 x 128) load once; its key rows are gathered 64 slots at a time.  Per
@@ -258,40 +259,12 @@ __device__ __forceinline__ uint32_t order_key(float v) {
   return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
 }
 
-// Exclusive block-wide prefix sum of one value per thread (TK_THREADS threads);
-// returns the exclusive prefix and writes the total.
-__device__ __forceinline__ int block_excl_scan(int v, int* s_warp, int& total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int x = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, x, o);
-    if (lane >= o) x += y;
-  }
-  if (lane == 31) s_warp[warp] = x;
-  __syncthreads();
-  if (warp == 0) {
-    int w = lane < TK_THREADS / 32 ? s_warp[lane] : 0;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, w, o);
-      if (lane >= o) w += y;
-    }
-    if (lane < TK_THREADS / 32) s_warp[lane] = w;   // inclusive warp totals
-  }
-  __syncthreads();
-  total = s_warp[TK_THREADS / 32 - 1];
-  const int base = warp > 0 ? s_warp[warp - 1] : 0;
-  __syncthreads();
-  return base + x - v;
-}
-
 __global__ void __launch_bounds__(TK_THREADS) dsa_topk_kernel(const IxArgs a, int K,
                                                              int32_t* idx, int32_t* length,
                                                              float* scores) {
   __shared__ uint32_t s_key[TK_MAXN];
   __shared__ int s_hist[256];
-  __shared__ int s_warp[TK_THREADS / 32];
+  __shared__ int s_warp[2 * (TK_THREADS / 32)];
   __shared__ uint32_t s_sel[3];                 // digit chosen, keys still needed, its bin count
   const int t = blockIdx.x;
   int lo;
@@ -375,29 +348,58 @@ __global__ void __launch_bounds__(TK_THREADS) dsa_topk_kernel(const IxArgs a, in
   }
   // take every key whose prefix class is above `prefix` and the first
   // `remaining` keys of the class itself (smallest indices first); compact in
-  // index order
-  const int per = (n + TK_THREADS - 1) / TK_THREADS;
-  const int b0 = threadIdx.x * per, b1 = min(n, b0 + per);
-  int n_eq = 0;
-  for (int i = b0; i < b1; ++i) n_eq += (s_key[i] & pmask) == prefix;
-  int tot_eq;
-  const int eq_before = block_excl_scan(n_eq, s_warp, tot_eq);
-  int n_sel = 0, eq = eq_before;
-  for (int i = b0; i < b1; ++i) {
-    const uint32_t u = s_key[i] & pmask;
-    if (u > prefix || (u == prefix && eq++ < remaining)) ++n_sel;
+  // index order.  A taken key's slot is the number of taken keys before it:
+  // (keys above the class before it) + min(keys of the class before it,
+  // remaining).  Each warp walks a contiguous segment of the row 32 keys at a
+  // time, its lanes on consecutive keys (conflict-free shared-memory reads),
+  // and counts with ballots; two walks (counts, then slots) around one scan of
+  // the warp totals.  (A thread walking its own contiguous run of n / 512 keys
+  // read shared memory with an n / 512-word stride between lanes: up to a
+  // 16-way bank conflict on every access.)
+  constexpr int NW = TK_THREADS / 32;
+  const int seg = (n + NW - 1) / NW;
+  const int w0 = min(n, warp * seg), w1 = min(n, w0 + seg);
+  const unsigned lt = (1u << lane) - 1u;
+  int c_above = 0, c_eq = 0;
+  for (int i0 = w0; i0 < w1; i0 += 32) {
+    const int i = i0 + lane;
+    const bool v = i < w1;
+    const uint32_t u = v ? (s_key[i] & pmask) : 0u;
+    c_above += __popc(__ballot_sync(0xffffffffu, v && u > prefix));
+    c_eq += __popc(__ballot_sync(0xffffffffu, v && u == prefix));
   }
-  int tot_sel;
-  int pos = block_excl_scan(n_sel, s_warp, tot_sel);
-  eq = eq_before;
-  for (int i = b0; i < b1; ++i) {
-    const uint32_t u = s_key[i] & pmask;
-    if (u > prefix || (u == prefix && eq++ < remaining)) {
+  if (lane == 0) {
+    s_warp[warp] = c_above;
+    s_warp[NW + warp] = c_eq;
+  }
+  __syncthreads();
+  int ab = 0, eb = 0, tot_above = 0, tot_eq = 0;
+#pragma unroll
+  for (int w = 0; w < NW; ++w) {
+    const int x = s_warp[w], y = s_warp[NW + w];
+    if (w < warp) {
+      ab += x;
+      eb += y;
+    }
+    tot_above += x;
+    tot_eq += y;
+  }
+  for (int i0 = w0; i0 < w1; i0 += 32) {
+    const int i = i0 + lane;
+    const bool v = i < w1;
+    const uint32_t u = v ? (s_key[i] & pmask) : 0u;
+    const bool above = v && u > prefix, in_class = v && u == prefix;
+    const unsigned ma = __ballot_sync(0xffffffffu, above), me = __ballot_sync(0xffffffffu, in_class);
+    const int ra = ab + __popc(ma & lt), re = eb + __popc(me & lt);
+    if (above || (in_class && re < remaining)) {
+      const int pos = ra + min(re, remaining);
       irow[pos] = lo + i;
       srow[pos] = lrow[lo + i];
-      ++pos;
     }
+    ab += __popc(ma);
+    eb += __popc(me);
   }
+  const int tot_sel = tot_above + min(tot_eq, remaining);
   for (int i = tot_sel + threadIdx.x; i < K; i += TK_THREADS) {
     irow[i] = -1;
     srow[i] = -INFINITY;

@@ -254,8 +254,9 @@ constexpr int TK_MAXN = 8192;                   // visible keys held in shared m
 
 // Order-preserving key of a float (larger float -> larger key); NaN -> 0.
 __device__ __forceinline__ uint32_t order_key(float v) {
-  const uint32_t b = __float_as_uint(v);
   if (v != v) return 0u;
+  // -0.0 takes the key of +0.0: equal values, so the index decides between them
+  const uint32_t b = __float_as_uint(v == 0.f ? 0.f : v);
   return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
 }
 

@@ -71,6 +71,23 @@ def test_indexer_logits_topk_small_full(T, H, lens, relu, K):
     assert int(err.item()) == 0
 
 
+@pytest.mark.parametrize("seed", [0, 1])
+def test_topk_heavy_ties_and_signed_zeros(seed):
+    """Logits of five integer levels, zeros of both signs: the threshold class
+    holds many keys, of which only the first (smallest indices) are taken, and
+    -0.0 ties with +0.0 as equal values do."""
+    T, K = 700, 128
+    g = torch.Generator().manual_seed(seed)
+    lg = torch.randint(-2, 3, (T, T), generator=g).float()
+    neg = (lg == 0) & (torch.rand(T, T, generator=g) < 0.5)
+    lg[neg] = -0.0
+    logits = torch.full((T, A.logits_ld(T)), float("-inf"))
+    logits[:, :T] = lg
+    idx, length, scores = A.dsa_topk(logits.to(DEV), K)
+    torch.cuda.synchronize()
+    check_topk(lg, X.visible_keys(T), K, idx, length, scores)
+
+
 @pytest.mark.parametrize("T,H,K,relu", [(300, 64, 64, True), (200, 16, 250, False),
                                         (150, 32, 33, True)])
 def test_indexer_backward_small_full(T, H, K, relu):

@@ -116,6 +116,7 @@ Problem to_kernel(const attn_problem_t* p) {
   k.fd_hq = make_fastdiv(static_cast<uint32_t>(k.heads_q));
   k.fd_hkv = make_fastdiv(static_cast<uint32_t>(k.heads_kv));
   k.fd_grp = make_fastdiv(static_cast<uint32_t>(k.heads_kv > 0 ? k.heads_q / k.heads_kv : 1));
+  k.fd_ns = make_fastdiv(static_cast<uint32_t>(k.num_seqs > 0 ? k.num_seqs : 1));
   return k;
 }
 
@@ -343,6 +344,12 @@ attn_status_t attn_bwd(const attn_problem_t* p, attn_dq_mode_t mode, const void*
   const bool persistent = total > sms;
   const int grid = persistent ? sms : static_cast<int>(total);
   a.x_major = persistent ? 1 : 0;
+  // THD on the persistent grid: list positions tile-major over the sequences
+  // (every sequence's first, longest tiles first) when that numbering fits the
+  // slot bound, i.e. leaves few empty positions
+  if (persistent && kp.cu_seqlens &&
+      static_cast<int64_t>(n_kv_tiles(kp)) * kp.num_seqs <= static_cast<int64_t>(gx))
+    a.x_major = 2;
   cudaError_t e = (D == 64) ? launch_attn_bwd<64>(mq, mk, mv, mdo, mdq, mdk, mdv, a, grid, st)
                             : launch_attn_bwd128(mq, mk, mv, mdo, a, grid, st);
   return cuda_status(e);

@@ -485,8 +485,8 @@ __global__ void __launch_bounds__(Bwd128::THREADS, 1)
           // order, and all CTAs are resident, so the waits cannot form a cycle;
           // holding a ticket back by one step does not change that (tile 0
           // never waits, and the last one is released at the end of the item).
-          int* tk = a.dq_ticket +
-                    (static_cast<size_t>(w.seq.b) * p.heads_q + h) * a.n_x + w.x0 + w.i_start + ii;
+          int* tk = a.dq_ticket + (static_cast<size_t>(w.seq.b) * p.heads_q + h) * a.n_x + w.x0 +
+                    (w.i_start + ii) * w.xs;
           release_pending();
           if (t == 0) wait_ticket(tk, w.jt, ac);   // raises the abort flag if it runs out
           named_bar_sync(2, 256);

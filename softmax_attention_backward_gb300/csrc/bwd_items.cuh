@@ -2,17 +2,20 @@
 // schedule over a persistent grid (shared by the D = 64 and D = 128 kernels).
 #pragma once
 
+#include "attn.h"
 #include "common.cuh"
 
 namespace attn {
 
 // One work item: K/V tile `jt` (rows kv0 .. kv0 + 127 of the sequence) of kv
-// head `hk`, and the n_it = groups * n_i query tiles it meets.  x0 is the tile
-// slot of the sequence's first tile (0 for dense problems), so x0 + i numbers
-// query tile i of the sequence among the n_x slots of a (batch, head).
+// head `hk`, and the n_it = groups * n_i query tiles it meets.  x0 + xs * i
+// numbers query tile i of the sequence among the n_x slots of a (batch, head):
+// x0 is the slot of the sequence's first tile and xs = 1 (slots sequence by
+// sequence; 0 and 1 for dense problems), or x0 is the sequence and xs the
+// number of sequences (slots tile-major, see next_bwd_item).
 struct BwdItem {
   SeqRef seq;
-  int hk, jt, kv0, i_start, n_i, n_it, x0;
+  int hk, jt, kv0, i_start, n_i, n_it, x0, xs;
 };
 
 // Advances the CTA's round counter `k` to its next valid item.  Round k of
@@ -23,6 +26,11 @@ struct BwdItem {
 //  * 1 (persistent grid): tile slot x slowest, so the list runs from the
 //    longest items to the shortest under causal masking (tile 0 of a sequence
 //    meets every query tile, the last tile only the last one);
+//  * 2 (persistent grid, THD): as 1, but slot x is tile x / num_seqs of
+//    sequence x % num_seqs, so the first tiles of every sequence come before
+//    the later tiles of any (numbered sequence by sequence, a long sequence's
+//    first tiles would come after a shorter one's last ones); slots past a
+//    sequence's end are empty;
 //  * 0 (one CTA per item): tile slot fastest within each (batch, kv head),
 //    in reverse, so CTAs resident together work on the same heads.
 template <int BN, int BM>
@@ -46,9 +54,28 @@ __device__ __forceinline__ bool next_bwd_item(const Problem& p, int total, int n
     const int b = static_cast<int>(fdiv(bh, p.fd_hkv));
     w.hk = bh - b * p.heads_kv;
     int jt;
-    if (!decode_tile(p, x, b, BN, w.seq, jt)) continue;
-    w.x0 = x - jt;
-    if (!x_major && p.causal) jt = (w.seq.len + BN - 1) / BN - 1 - jt;
+    if (x_major == 2) {
+      const int q = static_cast<int>(fdiv(static_cast<uint32_t>(x), p.fd_ns));
+      const int sq = x - q * p.num_seqs;
+      const int t0 = __ldg(p.cu_seqlens + sq), t1 = __ldg(p.cu_seqlens + sq + 1);
+      const int len = t1 > t0 ? t1 - t0 : 0;
+      const int nt = (len + BN - 1) / BN;
+      // a sequence longer than max_seqlen may have tiles past the last slot
+      if (q == 0 && nt > 0 && (nt - 1) * p.num_seqs + sq >= n_x && p.err)
+        atomicOr(p.err, ATTN_DEVERR_SEQLEN);
+      if (q >= nt) continue;
+      jt = q;
+      w.seq.b = 0;
+      w.seq.row0 = t0;
+      w.seq.len = len;
+      w.x0 = sq;
+      w.xs = p.num_seqs;
+    } else {
+      if (!decode_tile(p, x, b, BN, w.seq, jt)) continue;
+      w.x0 = x - jt;
+      w.xs = 1;
+      if (!x_major && p.causal) jt = (w.seq.len + BN - 1) / BN - 1 - jt;
+    }
     w.jt = jt;
     w.kv0 = jt * BN;
     w.i_start = p.causal ? w.kv0 / BM : 0;

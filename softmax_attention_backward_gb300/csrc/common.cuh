@@ -35,6 +35,7 @@ struct Problem {
   int max_seqlen;   // THD: bound on any sequence length
   int32_t* err;
   FastDiv fd_hq, fd_hkv, fd_grp;   // heads_q, heads_kv, heads_q / heads_kv
+  FastDiv fd_ns;                   // num_seqs (1 for dense)
 };
 
 // One sequence of a problem: rows [row0, row0 + len) of batch entry `b`.

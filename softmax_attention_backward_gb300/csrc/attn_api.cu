@@ -217,12 +217,18 @@ attn_status_t attn_fwd(const attn_problem_t* p, const void* q, const void* k, co
   a.fd_nbh = make_fastdiv(static_cast<uint32_t>(kp.heads_q * kp.batch));
   const int sms = sm_count();
   if (sms <= 0) return ATTN_ERR_CUDA;
-  // Persistent grid (one CTA per SM, the next item's query pair prefetched)
-  // except for THD at D = 128, whose items vary most in length: there the
-  // hardware's placement of one CTA per item balanced better (c4 forward 766
-  // against 711 TFLOP/s persistent).
-  const bool persistent = total > sms && (D == 64 || kp.cu_seqlens == nullptr);
+  // Persistent grid (one CTA per SM, the next item's query pair prefetched).
+  // For THD the slots run pair-rank-major over the sequences (every
+  // sequence's longest pairs first) when that numbering fits the slot bound:
+  // numbered sequence by sequence, the static list put a long sequence's
+  // longest pairs after a shorter one's shortest, and at D = 128 one CTA per
+  // item balanced better (c4 forward 766 against 711 TFLOP/s); pair-rank-major
+  // it runs at 854.
+  const bool persistent = total > sms;
   a.x_major = persistent ? 1 : 0;
+  if (persistent && kp.cu_seqlens &&
+      static_cast<int64_t>((kp.max_seqlen + 255) / 256) * kp.num_seqs <= static_cast<int64_t>(gx))
+    a.x_major = 2;
   const int grid = persistent ? sms : static_cast<int>(total);
   cudaError_t e = (D == 64) ? launch_attn_fwd<64>(mq, mk, mv, a, grid, st)
                             : launch_attn_fwd<128>(mq, mk, mv, a, grid, st);

@@ -91,7 +91,26 @@ __device__ __forceinline__ bool next_fwd_item(const Problem& p, int total, int n
     const int b = static_cast<int>(fdiv(bh, p.fd_hq));
     w.h = bh - b * p.heads_q;
     int pair;
-    if (!decode_tile(p, x, b, 2 * BM, w.seq, pair)) continue;
+    if (x_major == 2) {
+      // THD: slot x is pair rank x / num_seqs of sequence x % num_seqs, so the
+      // longest pairs of every sequence come first; ranks past a sequence's
+      // end are empty
+      const int q = static_cast<int>(fdiv(static_cast<uint32_t>(x), p.fd_ns));
+      const int sq = x - q * p.num_seqs;
+      const int t0 = __ldg(p.cu_seqlens + sq), t1 = __ldg(p.cu_seqlens + sq + 1);
+      const int len = t1 > t0 ? t1 - t0 : 0;
+      const int np = (len + 2 * BM - 1) / (2 * BM);
+      // a sequence longer than max_seqlen may have pairs past the last slot
+      if (q == 0 && np > 0 && (np - 1) * p.num_seqs + sq >= n_x && p.err)
+        atomicOr(p.err, ATTN_DEVERR_SEQLEN);
+      if (q >= np) continue;
+      w.seq.b = 0;
+      w.seq.row0 = t0;
+      w.seq.len = len;
+      pair = q;
+    } else if (!decode_tile(p, x, b, 2 * BM, w.seq, pair)) {
+      continue;
+    }
     if (p.causal) pair = (w.seq.len + 2 * BM - 1) / (2 * BM) - 1 - pair;
     w.m0 = pair * 2 * BM;
 #pragma unroll

@@ -573,7 +573,8 @@ def bench_sparse(args, dev, flush):
         torch.cuda.synchronize()
         f_ms.append(e[0].elapsed_time(e[1]))
         b_ms.append(e[1].elapsed_time(e[2]))
-    # ordered (deterministic) dKV: same inputs, its own workspace; bitwise repeat
+    # deterministic dKV (private slabs summed in slab order): same inputs, its own
+    # workspace; bitwise repeat
     # checked on the last two runs
     del ws
     wsd = torch.empty(A.sparse_attn_bwd_deterministic_workspace_size(q, idx), dtype=torch.uint8,

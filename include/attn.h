@@ -210,11 +210,14 @@ typedef struct {
 attn_status_t sparse_attn_fwd(const sparse_attn_problem_t* p, const void* q, const void* kv,
                               const int32_t* idx, void* o, float* lse, attn_stream_t stream);
 
-/* Workspace bytes for sparse_attn_bwd (fp32 dKV accumulator + fp32 Delta). */
+/* Workspace bytes for sparse_attn_bwd: fp32 dKV accumulator [tokens, dim_qk],
+ * fp32 Delta [tokens, heads] and int32 chunk counts [tokens], each 256-byte
+ * aligned. */
 size_t sparse_attn_bwd_workspace_size(const sparse_attn_problem_t* p);
 
 /* Backward: dq [tokens, heads, dim_qk] bf16, dkv [tokens, dim_qk] bf16.  Runs the
- * preprocess (Delta, clearing the accumulator), the main kernel (dQ by disjoint
+ * preprocess (Delta, the number of 64-slot chunks up to each token's last
+ * valid slot, clearing the accumulator), the main kernel (dQ by disjoint
  * stores, dKV by fp32 atomic adds, so dKV is not bitwise reproducible) and the
  * fp32 -> bf16 cast of dKV. */
 attn_status_t sparse_attn_bwd(const sparse_attn_problem_t* p, const void* q, const void* kv,
@@ -223,16 +226,19 @@ attn_status_t sparse_attn_bwd(const sparse_attn_problem_t* p, const void* q, con
                               size_t workspace_bytes, attn_stream_t stream);
 
 /* Deterministic variant of sparse_attn_bwd: the same dq (bitwise) and dkv
- * within rounding, with dkv bitwise reproducible.  Instead of adding into a
- * shared accumulator, the main kernel stores each (token, slot, 64-head block)
- * contribution to dkv once in the workspace; the index lists are inverted
- * into a per-key-row list of (token, slot) in ascending token order, and each
- * key row sums its contributions in a fixed order set by that list alone (fp32:
- * eight contiguous segments of the list, each summed in list order, then the
- * segment sums in segment order) before the bf16 cast.
- * Workspace: tokens * topk * ceil(heads / 64) * dim_qk fp32 contribution rows
- * plus Delta and the inverted lists (tokens * topk int32 and small tables);
- * at tokens 8192, topk 2048, 64 heads about 38.7 GB. */
+ * within rounding, with dkv bitwise reproducible.  The main kernel runs
+ * min(152, tokens * ceil(heads / 64)) CTAs; CTA b takes the (token, 64-head
+ * block) items b, b + grid, ... in that order and adds its dKV contributions
+ * into its own fp32 [tokens, dim_qk] slab of the workspace.  A token names a
+ * key row at most once, so an item adds at most once into each slab address,
+ * and the CTA orders its items' adds (a fence and a barrier between items):
+ * every slab address receives its adds in a fixed order.  The slabs are then
+ * summed in slab order and cast to bf16.  The slab count does not depend on the
+ * device, so neither does the result.  Index lists that name a key row twice
+ * break the contract (the two adds of that item then meet in either order).
+ * Workspace: slabs * tokens * dim_qk fp32 plus Delta and the chunk counts (the
+ * slabs are cleared by the call); at tokens 8192, 64 heads 2.87 GB for any
+ * topk. */
 size_t sparse_attn_bwd_deterministic_workspace_size(const sparse_attn_problem_t* p);
 attn_status_t sparse_attn_bwd_deterministic(const sparse_attn_problem_t* p, const void* q,
                                             const void* kv, const int32_t* idx, const void* o,

@@ -444,78 +444,44 @@ attn_status_t sparse_attn_fwd(const sparse_attn_problem_t* p, const void* q, con
   return cuda_status(launch_sparse_fwd(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+// Sparse backward workspace: fp32 dKV accumulator (shared: [T, 576]; slabs:
+// slabs x [T, 576]) | Delta [T, H] fp32 | chunk counts [T] int32, each
+// 256-byte aligned.
+struct SparseBwdWs {
+  size_t acc, delta, nch, bytes;
+};
+static int sparse_slabs(const sparse_attn_problem_t* p) {
+  const int64_t items = static_cast<int64_t>(p->tokens) * ((p->heads + 63) / 64);
+  return static_cast<int>(items < kSparseSlabs ? items : kSparseSlabs);
+}
+static SparseBwdWs sparse_bwd_ws(const sparse_attn_problem_t* p, int slabs) {
+  SparseBwdWs w{};
+  const size_t T = static_cast<size_t>(p->tokens);
+  size_t at = 0;
+  w.acc = at;   at += align256(static_cast<size_t>(slabs > 0 ? slabs : 1) * T * p->dim_qk * sizeof(float));
+  w.delta = at; at += align256(T * p->heads * sizeof(float));
+  w.nch = at;   at += align256(T * sizeof(int32_t));
+  w.bytes = at;
+  return w;
+}
+
 size_t sparse_attn_bwd_workspace_size(const sparse_attn_problem_t* p) {
   bool empty;
   if (check_sparse(p, &empty) != ATTN_OK || empty) return 0;
-  return align256(static_cast<size_t>(p->tokens) * p->dim_qk * sizeof(float)) +
-         align256(static_cast<size_t>(p->tokens) * p->heads * sizeof(float));
-}
-
-attn_status_t sparse_attn_bwd(const sparse_attn_problem_t* p, const void* q, const void* kv,
-                              const int32_t* idx, const void* o, const void* dout,
-                              const float* lse, void* dq, void* dkv, void* workspace,
-                              size_t workspace_bytes, attn_stream_t stream) {
-  bool empty;
-  attn_status_t s = check_sparse(p, &empty);
-  if (s != ATTN_OK) return s;
-  if (!q || !kv || !o || !dout || !lse || !dq || !dkv || (!idx && p->topk > 0))
-    return ATTN_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(kv) || !aligned16(o) || !aligned16(dout) || !aligned16(lse) ||
-      !aligned16(dq) || !aligned16(dkv) || (reinterpret_cast<uintptr_t>(idx) & 3u))
-    return ATTN_ERR_ALIGNMENT;
-  if (empty) return ATTN_OK;
-  const size_t need = sparse_attn_bwd_workspace_size(p);
-  if (!workspace || workspace_bytes < need) return ATTN_ERR_WORKSPACE;
-  if (!aligned16(workspace)) return ATTN_ERR_ALIGNMENT;
-  SparseArgs a = sparse_args(p);
-  a.q = static_cast<const __nv_bfloat16*>(q);
-  a.kv = static_cast<const __nv_bfloat16*>(kv);
-  a.idx = idx;
-  a.o = static_cast<__nv_bfloat16*>(const_cast<void*>(o));
-  a.dout = static_cast<const __nv_bfloat16*>(dout);
-  a.lse_in = lse;
-  a.dq = static_cast<__nv_bfloat16*>(dq);
-  a.dkv_acc = static_cast<float*>(workspace);
-  float* delta = reinterpret_cast<float*>(
-      static_cast<uint8_t*>(workspace) +
-      align256(static_cast<size_t>(p->tokens) * p->dim_qk * sizeof(float)));
-  return cuda_status(launch_sparse_bwd(a, delta, static_cast<__nv_bfloat16*>(dkv),
-                                       reinterpret_cast<cudaStream_t>(stream)));
-}
-
-// Ordered (deterministic) sparse backward: workspace = contribution rows
-// [T, K, head blocks, 576] fp32 | Delta [T, H] | CSR table [nblk, T] | totals
-// [T] | row offsets [T + 1] | entries [T * K], each 256-byte aligned.
-struct SparseOrderedWs {
-  size_t contrib, delta, table, total, off, entries, bytes;
-};
-static SparseOrderedWs sparse_ordered_ws(const sparse_attn_problem_t* p) {
-  SparseOrderedWs w{};
-  const size_t T = static_cast<size_t>(p->tokens), K = static_cast<size_t>(p->topk);
-  const size_t nhb = static_cast<size_t>((p->heads + 63) / 64);
-  const SparseCsrLayout l = sparse_csr_layout(p->tokens, p->topk);
-  size_t at = 0;
-  w.contrib = at; at += align256(T * K * nhb * p->dim_qk * sizeof(float));
-  w.delta = at;   at += align256(T * p->heads * sizeof(float));
-  w.table = at;   at += align256(l.table_elems * sizeof(int32_t));
-  w.total = at;   at += align256(l.total_elems * sizeof(int32_t));
-  w.off = at;     at += align256(l.off_elems * sizeof(int32_t));
-  w.entries = at; at += align256(l.entry_elems * sizeof(int32_t));
-  w.bytes = at;
-  return w;
+  return sparse_bwd_ws(p, 0).bytes;
 }
 
 size_t sparse_attn_bwd_deterministic_workspace_size(const sparse_attn_problem_t* p) {
   bool empty;
   if (check_sparse(p, &empty) != ATTN_OK || empty) return 0;
-  return sparse_ordered_ws(p).bytes;
+  return sparse_bwd_ws(p, sparse_slabs(p)).bytes;
 }
 
-attn_status_t sparse_attn_bwd_deterministic(const sparse_attn_problem_t* p, const void* q,
-                                            const void* kv, const int32_t* idx, const void* o,
-                                            const void* dout, const float* lse, void* dq,
-                                            void* dkv, void* workspace, size_t workspace_bytes,
-                                            attn_stream_t stream) {
+static attn_status_t sparse_bwd_call(const sparse_attn_problem_t* p, bool deterministic,
+                                     const void* q, const void* kv, const int32_t* idx,
+                                     const void* o, const void* dout, const float* lse, void* dq,
+                                     void* dkv, void* workspace, size_t workspace_bytes,
+                                     attn_stream_t stream) {
   bool empty;
   attn_status_t s = check_sparse(p, &empty);
   if (s != ATTN_OK) return s;
@@ -525,7 +491,8 @@ attn_status_t sparse_attn_bwd_deterministic(const sparse_attn_problem_t* p, cons
       !aligned16(dq) || !aligned16(dkv) || (reinterpret_cast<uintptr_t>(idx) & 3u))
     return ATTN_ERR_ALIGNMENT;
   if (empty) return ATTN_OK;
-  const SparseOrderedWs w = sparse_ordered_ws(p);
+  const int slabs = deterministic ? sparse_slabs(p) : 0;
+  const SparseBwdWs w = sparse_bwd_ws(p, slabs);
   if (!workspace || workspace_bytes < w.bytes) return ATTN_ERR_WORKSPACE;
   if (!aligned16(workspace)) return ATTN_ERR_ALIGNMENT;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -537,13 +504,29 @@ attn_status_t sparse_attn_bwd_deterministic(const sparse_attn_problem_t* p, cons
   a.dout = static_cast<const __nv_bfloat16*>(dout);
   a.lse_in = lse;
   a.dq = static_cast<__nv_bfloat16*>(dq);
-  a.dkv_acc = nullptr;
-  a.contrib = reinterpret_cast<float*>(ws + w.contrib);
-  return cuda_status(launch_sparse_bwd_ordered(
-      a, reinterpret_cast<float*>(ws + w.delta), reinterpret_cast<int32_t*>(ws + w.table),
-      reinterpret_cast<int32_t*>(ws + w.total), reinterpret_cast<int32_t*>(ws + w.off),
-      reinterpret_cast<int32_t*>(ws + w.entries), static_cast<__nv_bfloat16*>(dkv),
-      reinterpret_cast<cudaStream_t>(stream)));
+  a.dkv_acc = reinterpret_cast<float*>(ws + w.acc);
+  a.nch = reinterpret_cast<int32_t*>(ws + w.nch);
+  a.slabs = slabs;
+  return cuda_status(launch_sparse_bwd(a, reinterpret_cast<float*>(ws + w.delta),
+                                       static_cast<__nv_bfloat16*>(dkv),
+                                       reinterpret_cast<cudaStream_t>(stream)));
+}
+
+attn_status_t sparse_attn_bwd(const sparse_attn_problem_t* p, const void* q, const void* kv,
+                              const int32_t* idx, const void* o, const void* dout,
+                              const float* lse, void* dq, void* dkv, void* workspace,
+                              size_t workspace_bytes, attn_stream_t stream) {
+  return sparse_bwd_call(p, false, q, kv, idx, o, dout, lse, dq, dkv, workspace, workspace_bytes,
+                         stream);
+}
+
+attn_status_t sparse_attn_bwd_deterministic(const sparse_attn_problem_t* p, const void* q,
+                                            const void* kv, const int32_t* idx, const void* o,
+                                            const void* dout, const float* lse, void* dq,
+                                            void* dkv, void* workspace, size_t workspace_bytes,
+                                            attn_stream_t stream) {
+  return sparse_bwd_call(p, true, q, kv, idx, o, dout, lse, dq, dkv, workspace, workspace_bytes,
+                         stream);
 }
 
 }  // extern "C"

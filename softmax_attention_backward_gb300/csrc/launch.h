@@ -101,6 +101,14 @@ cudaError_t launch_dq_finalize(const Problem& p, const float* acc, size_t slab_e
 
 namespace attn {
 
+// Key slots per chunk of the sparse backward main kernel.
+constexpr int kSparseChunk = 64;
+// Private fp32 dKV accumulators of the deterministic sparse backward: its
+// main kernel runs this many CTAs (fewer when there are fewer items), one slab
+// each.  A fixed count, not the device's SM count, so that the result does not
+// depend on the device.
+constexpr int kSparseSlabs = 152;
+
 struct SparseArgs {
   const __nv_bfloat16* q;
   const __nv_bfloat16* kv;
@@ -111,37 +119,20 @@ struct SparseArgs {
   const float* lse_in;
   const float* delta;
   __nv_bfloat16* dq;
-  float* dkv_acc;        // atomic path: fp32 dKV accumulator [T, 576]
-  float* contrib;        // ordered path: per (token, slot, head block) dKV rows, else null
+  float* dkv_acc;        // fp32 dKV accumulator [T, 576], or slabs x [T, 576]
+  int32_t* nch;          // backward: chunks of 64 slots per token (preprocess output)
+  int slabs;             // 0: one shared accumulator; else the number of private slabs
   int T, H, K;
   float scale, scale_log2;
   int32_t* err;
 };
 
 cudaError_t launch_sparse_fwd(const SparseArgs& a, cudaStream_t st);
+// Backward: preprocess (Delta, chunk counts, clearing the accumulator or
+// slabs), main kernel, then the bf16 cast (shared accumulator) or the
+// slab-order sum and cast (slabs).
 cudaError_t launch_sparse_bwd(const SparseArgs& a, float* delta, __nv_bfloat16* dkv,
                               cudaStream_t st);
 cudaError_t launch_sparse_bwd_main(const SparseArgs& a, cudaStream_t st);
-
-// Deterministic dKV (sparse_dkv_ordered.cu): CSR of the index lists by key
-// row, entries in ascending token order, and the ordered row reduction.
-struct SparseCsrLayout {
-  int nblk, tb;                // token blocks of tb tokens
-  size_t table_elems;          // int32 [nblk, T]
-  size_t total_elems;          // int32 [T]
-  size_t off_elems;            // int32 [T + 1]
-  size_t entry_elems;          // int32 [T * K]
-};
-SparseCsrLayout sparse_csr_layout(int T, int K);
-cudaError_t launch_sparse_csr(const int32_t* idx, int T, int K, const SparseCsrLayout& l,
-                              int32_t* table, int32_t* total, int32_t* off, int32_t* entries,
-                              cudaStream_t st);
-cudaError_t launch_sparse_dkv_reduce(const float* contrib, const int32_t* entries,
-                                     const int32_t* off, int T, int nhb, __nv_bfloat16* dkv,
-                                     cudaStream_t st);
-// Ordered backward: Delta, CSR, main kernel storing contribution rows, reduce.
-cudaError_t launch_sparse_bwd_ordered(const SparseArgs& a, float* delta, int32_t* table,
-                                      int32_t* total, int32_t* off, int32_t* entries,
-                                      __nv_bfloat16* dkv, cudaStream_t st);
 
 }  // namespace attn

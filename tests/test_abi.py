@@ -126,27 +126,28 @@ def test_sparse_validation(L):
     assert f(_sparse(tokens=0)) == 0
     p = _sparse()
     ws = L.sparse_attn_bwd_workspace_size(ctypes.byref(p))
-    assert ws == 8192 * 576 * 4 + 8192 * 64 * 4
+    assert ws == 8192 * 576 * 4 + 8192 * 64 * 4 + 8192 * 4    # accumulator, Delta, chunk counts
     args = [ctypes.c_void_p(FAKE)] * 8          # q kv idx o dout lse dq dkv
     assert L.sparse_attn_bwd(ctypes.byref(p), *args, ctypes.c_void_p(FAKE), ws - 1, None) == 5
 
 
 def test_sparse_deterministic_workspace_and_validation(L):
-    """Workspace of the ordered sparse backward: fp32 contribution rows per
-    (token, slot, 64-head block), Delta, the per-token-block counts, the row
-    totals and offsets, and one int32 entry per (token, slot); each piece is
+    """Workspace of the deterministic sparse backward: one fp32 [tokens, 576]
+    dKV slab per CTA of its main kernel (152, or one per (token, 64-head
+    block) item when there are fewer), Delta and the chunk counts; each piece
     256-byte aligned.  Calls with a short workspace or bad shapes are refused
     before any launch."""
     a256 = lambda x: (x + 255) // 256 * 256
     p = _sparse()
     ws = L.sparse_attn_bwd_deterministic_workspace_size(ctypes.byref(p))
-    assert ws == (8192 * 2048 * 1 * 576 * 4 + 8192 * 64 * 4 + 128 * 8192 * 4 + a256(8192 * 4)
-                  + a256(8193 * 4) + 8192 * 2048 * 4)
-    # 128 heads: two head blocks per token; few tokens: one token per block
-    p2 = _sparse(tokens=100, heads=128, topk=64)
+    assert ws == 152 * 8192 * 576 * 4 + 8192 * 64 * 4 + 8192 * 4
+    # 128 heads: two head blocks per token; few items: one slab per item
+    p2 = _sparse(tokens=50, heads=128, topk=64)
     assert L.sparse_attn_bwd_deterministic_workspace_size(ctypes.byref(p2)) == (
-        a256(100 * 64 * 2 * 576 * 4) + a256(100 * 128 * 4) + a256(100 * 100 * 4) + a256(100 * 4)
-        + a256(101 * 4) + a256(100 * 64 * 4))
+        a256(100 * 50 * 576 * 4) + a256(50 * 128 * 4) + a256(50 * 4))
+    p3 = _sparse(tokens=100, heads=128, topk=64)
+    assert L.sparse_attn_bwd_deterministic_workspace_size(ctypes.byref(p3)) == (
+        a256(152 * 100 * 576 * 4) + a256(100 * 128 * 4) + a256(100 * 4))
     assert L.sparse_attn_bwd_deterministic_workspace_size(ctypes.byref(_sparse(heads=48))) == 0
     args = [ctypes.c_void_p(FAKE)] * 8          # q kv idx o dout lse dq dkv
     f = lambda q, *rest: L.sparse_attn_bwd_deterministic(ctypes.byref(q), *rest)

@@ -189,8 +189,8 @@ def test_sparse_out_of_range_index_is_flagged_and_skipped():
     ref_o, ref_lse = oracle.sparse_forward(q, kv, cleaned, 576 ** -0.5)
     assert_close("o", o, ref_o)
     assert_lse("lse", lse, ref_lse)
-    # both backward paths skip the bad slots (the ordered one also when it
-    # inverts the index lists) and flag them
+    # both backward paths skip the bad slots (the deterministic one in its
+    # chunk counts and its slab adds alike) and flag them
     ref = oracle.sparse_backward(q, kv, cleaned, do, 576 ** -0.5)
     for bwd in (A.sparse_attn_bwd, A.sparse_attn_bwd_deterministic):
         err.zero_()
@@ -234,7 +234,8 @@ def test_sparse_outputs_fully_written():
     A.sparse_attn_bwd(q, kv, idx, o, do, lse, workspace=ws, dq=dq, dkv=dkv)
     for t in (o, lse, dq, dkv):
         assert torch.isfinite(t).all()
-    # ordered path: 0xFF-filled workspace and NaN outputs, every slot still written,
+    # deterministic path: 0xFF-filled workspace (its slabs are cleared by the call)
+    # and NaN outputs, every slot still written,
     # key rows that no token names get exact zeros
     dq2, dkv2 = torch.full_like(q, float("nan")), torch.full_like(kv, float("nan"))
     ws2 = torch.full((A.sparse_attn_bwd_deterministic_workspace_size(q, idx),), 0xFF,

@@ -35,7 +35,10 @@ __global__ void __launch_bounds__(256) attn_bwd_preprocess_kernel(Problem p,
   constexpr int TPR = D / 8;   // threads per row
   constexpr int RPW = 32 / TPR;   // rows per warp step
   const int end = valid_end(p);
-  const uint32_t nrows = static_cast<uint32_t>(p.batch) * p.rows_total * p.heads_q;
+  // THD (batch 1): the rows before the end of the last sequence here, the
+  // padding rows' exact zeros by the contiguous fill below
+  const uint32_t nrows = p.cu_seqlens ? static_cast<uint32_t>(end) * p.heads_q
+                                      : static_cast<uint32_t>(p.batch) * p.rows_total * p.heads_q;
   const uint32_t nthreads = gridDim.x * blockDim.x;
   const uint32_t gtid = blockIdx.x * blockDim.x + threadIdx.x;
   const int sub = threadIdx.x % TPR;
@@ -50,12 +53,8 @@ __global__ void __launch_bounds__(256) attn_bwd_preprocess_kernel(Problem p,
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
       rr[u] = base + u * RPW + (threadIdx.x % 32) / TPR;
-      // THD rows past the last sequence (srow >= end) get Delta = 0 without
-      // reading O and dO
       ov[u] = dv[u] = make_uint4(0u, 0u, 0u, 0u);
-      // (THD has batch 1, so the row of pair rr is rr / heads_q)
-      if (rr[u] < nrows &&
-          (p.cu_seqlens == nullptr || static_cast<int>(fdiv(rr[u], p.fd_hq)) < end)) {
+      if (rr[u] < nrows) {
         ov[u] = *reinterpret_cast<const uint4*>(o + static_cast<size_t>(rr[u]) * D + sub * 8);
         dv[u] = *reinterpret_cast<const uint4*>(dout + static_cast<size_t>(rr[u]) * D + sub * 8);
       }
@@ -91,8 +90,16 @@ __global__ void __launch_bounds__(256) attn_bwd_preprocess_kernel(Problem p,
           li = static_cast<size_t>(h) * rt + srow;
         else
           li = (static_cast<size_t>(b) * hq + h) * rt + srow;
-        delta[li] = (static_cast<int>(srow) < end) ? acc[u] : 0.f;
+        delta[li] = acc[u];
       }
+    }
+  }
+  if (p.cu_seqlens) {
+    // Delta of the THD padding rows (end .. rows_total of every head): exact zeros
+    const uint32_t pad = rt - static_cast<uint32_t>(end);
+    for (uint32_t i = gtid; i < pad * hq; i += nthreads) {
+      const uint32_t h = i / pad;
+      delta[static_cast<size_t>(h) * rt + end + (i - h * pad)] = 0.f;
     }
   }
   if (clear) {

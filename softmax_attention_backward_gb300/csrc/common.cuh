@@ -84,9 +84,11 @@ inline int tile_bound(int rows_total, int num_seqs, int tile_rows, bool packed) 
   return packed ? base + num_seqs : base;
 }
 
-// End of the valid rows of a THD problem (cu_seqlens[num_seqs]); rows_total for dense.
+// End of the valid rows of a THD problem (cu_seqlens[num_seqs], kept within
+// [0, rows_total] so that a list breaking its contract cannot move the passes
+// that use it out of their buffers); rows_total for dense.
 __device__ __forceinline__ int valid_end(const Problem& p) {
-  return p.cu_seqlens ? __ldg(p.cu_seqlens + p.num_seqs) : p.rows_total;
+  return p.cu_seqlens ? min(max(__ldg(p.cu_seqlens + p.num_seqs), 0), p.rows_total) : p.rows_total;
 }
 
 }  // namespace attn

@@ -282,6 +282,36 @@ def test_sparse_empty_lists_and_scattered_sentinels(deterministic):
         assert (got["o"][t] == 0).all() and (got["dq"][t] == 0).all()
 
 
+def test_sparse_deterministic_item_walk_with_empty_and_short_lists():
+    """The deterministic main kernel runs 152 CTAs, each walking its items (a
+    token and a 64-head block) in order: 500 tokens x 2 head blocks gives each
+    CTA six or seven items, among them tokens with no valid slot (every 7th:
+    dq = 0, skipped by every role) and tokens whose valid slots end in the
+    first, second or third of the four chunks (top-k 200, the last chunk
+    ragged).  Parity with the oracle, dKV bitwise equal over repeats, dQ
+    bitwise equal to the atomic path."""
+    T, H, K = 500, 128, 200
+    q, kv, do, _ = W.sparse_inputs(T, H, 1, seed=71)
+    idx = _random_index_lists(T, K, seed=72)
+    idx[::7] = -1
+    for t, last in ((3, 10), (4, 70), (9, 130), (10, 64), (11, 63)):
+        idx[t, last + 1:] = -1
+    scale = 576 ** -0.5
+    got = run_sparse(q, kv, idx, do, scale, deterministic=True)
+    ref = oracle.sparse_backward(q, kv, idx, do, scale)
+    assert_close("dq", got["dq"], ref["dq"])
+    assert_close("dkv", got["dkv"], ref["dkv"])
+    assert (got["dq"][::7] == 0).all()
+    gq, gkv, gidx, gdo = got["gpu"]
+    for _ in range(2):
+        dq2, dkv2 = A.sparse_attn_bwd_deterministic(gq, gkv, gidx, got["o"], gdo, got["lse"],
+                                                    scale=scale)
+        assert torch.equal(dkv2, got["dkv"]) and torch.equal(dq2, got["dq"])
+    dq_at, dkv_at = A.sparse_attn_bwd(gq, gkv, gidx, got["o"], gdo, got["lse"], scale=scale)
+    assert torch.equal(dq_at, got["dq"])
+    assert_close("dkv (atomic)", dkv_at, ref["dkv"])
+
+
 def _random_sparse_cases(n=4, seed=2030):
     """Seeded top-k problems: 1-300 tokens, heads in {16, 32, 64, 128}, top-k 1-300."""
     g = torch.Generator().manual_seed(seed)

@@ -10,6 +10,7 @@
 
 #include "attn.h"
 #include "launch.h"
+#include "thd_order.cuh"
 
 namespace attn {
 
@@ -223,12 +224,14 @@ attn_status_t attn_fwd(const attn_problem_t* p, const void* q, const void* k, co
   // numbered sequence by sequence, the static list put a long sequence's
   // longest pairs after a shorter one's shortest, and at D = 128 one CTA per
   // item balanced better (c4 forward 766 against 711 TFLOP/s); pair-rank-major
-  // it runs at 854.
+  // it runs at 854.  Causal packs of at most 32 sequences take the list of
+  // thd_order.cuh instead (descending work, no empty positions): c4 forward
+  // 193 -> 186 us.
   const bool persistent = total > sms;
   a.x_major = persistent ? 1 : 0;
   if (persistent && kp.cu_seqlens &&
       static_cast<int64_t>((kp.max_seqlen + 255) / 256) * kp.num_seqs <= static_cast<int64_t>(gx))
-    a.x_major = 2;
+    a.x_major = (kp.causal && kp.num_seqs <= kThdOrderSeqs) ? 3 : 2;
   const int grid = persistent ? sms : static_cast<int>(total);
   cudaError_t e = (D == 64) ? launch_attn_fwd<64>(mq, mk, mv, a, grid, st)
                             : launch_attn_fwd<128>(mq, mk, mv, a, grid, st);
@@ -352,10 +355,13 @@ attn_status_t attn_bwd(const attn_problem_t* p, attn_dq_mode_t mode, const void*
   a.x_major = persistent ? 1 : 0;
   // THD on the persistent grid: list positions tile-major over the sequences
   // (every sequence's first, longest tiles first) when that numbering fits the
-  // slot bound, i.e. leaves few empty positions
+  // slot bound, i.e. leaves few empty positions; with atomic dQ, causal packs
+  // of at most 32 sequences in the descending-work list of thd_order.cuh
+  // (c4 backward 416.6 -> 402.7 us; the split mode measured 3% slower with
+  // it and keeps the tile-major list)
   if (persistent && kp.cu_seqlens &&
       static_cast<int64_t>(n_kv_tiles(kp)) * kp.num_seqs <= static_cast<int64_t>(gx))
-    a.x_major = 2;
+    a.x_major = (kp.causal && kp.num_seqs <= kThdOrderSeqs && !a.split) ? 3 : 2;
   cudaError_t e = (D == 64) ? launch_attn_bwd<64>(mq, mk, mv, mdo, mdq, mdk, mdv, a, grid, st)
                             : launch_attn_bwd128(mq, mk, mv, mdo, a, grid, st);
   return cuda_status(e);

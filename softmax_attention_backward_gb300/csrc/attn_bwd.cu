@@ -78,7 +78,8 @@ struct BwdCfg {
 // Warp roles: 0..7 P/dS (two warpgroups, each owns half of the query columns
 // of every KV row), 8..11 dQ drain and dK/dV epilogue, 12 TMA, 13 the MMA
 // issuer, which interleaves independent GEMMs.
-template <int D>
+// kThd: the instantiation for numbering 3; the others carry none of its code
+template <int D, bool kThd>
 __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
@@ -105,6 +106,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
   __shared__ uint64_t bar_dv_empty, bar_dk_empty;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_flag;
+  __shared__ ThdOrder s_thd;   // the item list of numbering 3
   __shared__ __align__(16) float s_nlse[2][BM];   // -LSE * log2(e) per query column
   __shared__ __align__(16) float s_delta[2][BM];
 
@@ -135,6 +137,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     mbar_init(&bar_dk_empty, 128);
     fence_mbar_init();
   }
+  if constexpr (kThd)
+    if (warp == 1) thd_order_build(p, BN, p.heads_kv * p.batch, s_thd);
   if (warp == 13) tmem_alloc(&tmem_base_sh, C::TMEM_COLS);
   tc_fence_before();
   __syncthreads();
@@ -150,8 +154,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       tma_prefetch_desc(&tmdO);
       BwdItem w;
       int k = 0, ic = 0, gs = 0;
+      ThdCursor cur;
       bool ok = true;
-      while (ok && next_bwd_item<BN, BM>(p, total, a.n_x, a.x_major, a.fd_nbh, a.fd_nx, k, w)) {
+      while (ok && next_bwd_item<BN, BM, kThd>(p, total, a.n_x, a.x_major, a.fd_nbh, a.fd_nx, s_thd, cur, k, w)) {
         const int kb = ic % C::KV_BUFS, ku = ic / C::KV_BUFS;
         if (!mbar_wait(&bar_kv_empty[kb], (ku & 1) ^ 1, ac)) break;
         mbar_arrive_expect_tx(&bar_kv_full[kb], 2 * C::KV_BYTES);
@@ -224,12 +229,13 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       };
       BwdItem w, wn;
       int k = 0, ic = 0, gs = 0;
+      ThdCursor cur;
       bool ok = true;
-      bool have = next_bwd_item<BN, BM>(p, total, a.n_x, a.x_major, a.fd_nbh, a.fd_nx, k, w);
+      bool have = next_bwd_item<BN, BM, kThd>(p, total, a.n_x, a.x_major, a.fd_nbh, a.fd_nx, s_thd, cur, k, w);
       bool sdp_done = false;   // S^T/dP^T of the next step already issued
       while (ok && have) {
         const int kb = ic % C::KV_BUFS, ku = ic / C::KV_BUFS;
-        const bool have_next = next_bwd_item<BN, BM>(p, total, a.n_x, a.x_major, a.fd_nbh, a.fd_nx, k, wn);
+        const bool have_next = next_bwd_item<BN, BM, kThd>(p, total, a.n_x, a.x_major, a.fd_nbh, a.fd_nx, s_thd, cur, k, wn);
         const int kbn = (ic + 1) % C::KV_BUFS, kun = (ic + 1) / C::KV_BUFS;
         if (!mbar_wait_w(&bar_kv_full[kb], ku & 1, ac)) break;
         const uint64_t dK_mn = desc_mnmajor_base(smem_u32(sK(kb)), BN);
@@ -327,7 +333,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     const uint32_t tDSme = tmem + lane_base + C::COL_DP + c0;    // dS^T over dP^T
     BwdItem w;
     int k = 0, gs = 0;
-    bool have = next_bwd_item<BN, BM>(p, total, a.n_x, a.x_major, a.fd_nbh, a.fd_nx, k, w);
+    ThdCursor cur;
+    bool have = next_bwd_item<BN, BM, kThd>(p, total, a.n_x, a.x_major, a.fd_nbh, a.fd_nx, s_thd, cur, k, w);
     float pf = have ? fetch(w, 0, 0) : 0.f;
     bool ok = true;
     while (ok && have) {
@@ -348,7 +355,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
           // last step of the item: look up the next one for the prefetch
           BwdItem wn;
           int kn = k;
-          if (next_bwd_item<BN, BM>(p, total, a.n_x, a.x_major, a.fd_nbh, a.fd_nx, kn, wn)) pf = fetch(wn, 0, 0);
+          ThdCursor cn = cur;
+          if (next_bwd_item<BN, BM, kThd>(p, total, a.n_x, a.x_major, a.fd_nbh, a.fd_nx, s_thd, cn, kn, wn)) pf = fetch(wn, 0, 0);
         }
         named_bar_sync(1, 256);
         // ---- P^T (KV row r, query columns c0 .. c0 + HALF) ----
@@ -439,7 +447,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         mbar_arrive(&bar_ds);
       }
       gs += w.n_it;
-      have = next_bwd_item<BN, BM>(p, total, a.n_x, a.x_major, a.fd_nbh, a.fd_nx, k, w);
+      have = next_bwd_item<BN, BM, kThd>(p, total, a.n_x, a.x_major, a.fd_nbh, a.fd_nx, s_thd, cur, k, w);
     }
   } else {
     // ---------------- dQ drain and dK/dV epilogue (warps 8..11) ----------------
@@ -466,8 +474,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     uint8_t* stg = reinterpret_cast<uint8_t*>(sDQ);
     BwdItem w;
     int k = 0, ic = 0, gs = 0;
+    ThdCursor cur;
     bool ok = true;
-    while (ok && next_bwd_item<BN, BM>(p, total, a.n_x, a.x_major, a.fd_nbh, a.fd_nx, k, w)) {
+    while (ok && next_bwd_item<BN, BM, kThd>(p, total, a.n_x, a.x_major, a.fd_nbh, a.fd_nx, s_thd, cur, k, w)) {
       float* base = a.dq_acc;
       bool slab_ok = true;
       if (a.split) {
@@ -619,7 +628,7 @@ cudaError_t launch_attn_bwd(const CUtensorMap& q, const CUtensorMap& k, const CU
                             const CUtensorMap& dO, const CUtensorMap& dq, const CUtensorMap& dk,
                             const CUtensorMap& dv, const BwdArgs& a, int grid, cudaStream_t st) {
   using C = BwdCfg<D>;
-  auto kern = attn_bwd_kernel<D>;
+  auto kern = a.x_major == 3 ? attn_bwd_kernel<D, true> : attn_bwd_kernel<D, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   kern<<<grid, C::THREADS, C::SMEM, st>>>(q, k, v, dO, dq, dk, dv, a);

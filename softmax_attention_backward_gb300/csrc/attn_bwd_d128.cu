@@ -79,7 +79,9 @@ __device__ __forceinline__ void next_step(int& ih, int& ii, int groups) {
 // Each mode is its own instantiation: the drain loop is sensitive to its code
 // size (the ATOMIC kernel measured 10% slower with the ordered path compiled
 // in).
-template <bool kOrdered>
+// kThd: the instantiation for numbering 3 (atomic dQ only); the others carry
+// none of its code (the ordered drain loop slowed by 7% with it inlined)
+template <bool kOrdered, bool kThd>
 __global__ void __launch_bounds__(Bwd128::THREADS, 1)
     attn_bwd128_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
@@ -101,6 +103,7 @@ __global__ void __launch_bounds__(Bwd128::THREADS, 1)
   __shared__ uint64_t bar_done, bar_dv_empty, bar_dk_empty;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_flag;
+  __shared__ ThdOrder s_thd;   // the item list of numbering 3
   // -LSE * log2(e) and Delta of the step's query columns; one buffer, so that
   // the tiles and these fit the 227 KB with the 1 KB alignment margin
   __shared__ __align__(16) float s_nlse[BM];
@@ -133,6 +136,8 @@ __global__ void __launch_bounds__(Bwd128::THREADS, 1)
     mbar_init(&bar_dk_empty, 256);
     fence_mbar_init();
   }
+  if constexpr (kThd)
+    if (warp == 1) thd_order_build(p, BN, p.heads_kv * p.batch, s_thd);
   if (warp == 17) tmem_alloc(&tmem_base_sh, 512);
   tc_fence_before();
   __syncthreads();
@@ -153,8 +158,9 @@ __global__ void __launch_bounds__(Bwd128::THREADS, 1)
       tma_prefetch_desc(&tmdO);
       BwdItem w;
       int k = 0, ic = 0, gs = 0;
+      ThdCursor cur;
       bool ok = true;
-      while (ok && next_bwd_item<BN, BM>(p, total, a.n_x, a.x_major, a.fd_nbh, a.fd_nx, k, w)) {
+      while (ok && next_bwd_item<BN, BM, kThd>(p, total, a.n_x, a.x_major, a.fd_nbh, a.fd_nx, s_thd, cur, k, w)) {
         if (!mbar_wait_spin(&bar_kv_empty, (ic & 1) ^ 1, ac)) break;
         mbar_arrive_expect_tx(&bar_kv_full, 2 * C::TILE);
         for (int pn = 0; pn < 2; ++pn) {
@@ -216,8 +222,9 @@ __global__ void __launch_bounds__(Bwd128::THREADS, 1)
     };
     BwdItem w;
     int k = 0, ic = 0, gs = 0;
+    ThdCursor cur;
     bool ok = true;
-    while (ok && next_bwd_item<BN, BM>(p, total, a.n_x, a.x_major, a.fd_nbh, a.fd_nx, k, w)) {
+    while (ok && next_bwd_item<BN, BM, kThd>(p, total, a.n_x, a.x_major, a.fd_nbh, a.fd_nx, s_thd, cur, k, w)) {
       if (!mbar_wait_w(&bar_kv_full, ic & 1, ac)) break;
       for (int it = 0; it < w.n_it; ++it) {
         const int g = gs + it, qs = g & 1;
@@ -307,7 +314,8 @@ __global__ void __launch_bounds__(Bwd128::THREADS, 1)
     const uint64_t sl2x2 = f2_pack(sl2, sl2);
     BwdItem w;
     int k = 0, gs = 0;
-    bool have = next_bwd_item<BN, BM>(p, total, a.n_x, a.x_major, a.fd_nbh, a.fd_nx, k, w);
+    ThdCursor cur;
+    bool have = next_bwd_item<BN, BM, kThd>(p, total, a.n_x, a.x_major, a.fd_nbh, a.fd_nx, s_thd, cur, k, w);
     float pf = have ? fetch(w, 0, w.n_i - 1) : 0.f;
     bool ok = true;
     while (ok && have) {
@@ -328,7 +336,8 @@ __global__ void __launch_bounds__(Bwd128::THREADS, 1)
           // last step of the item: look up the next one for the prefetch
           BwdItem wn;
           int kn = k;
-          if (next_bwd_item<BN, BM>(p, total, a.n_x, a.x_major, a.fd_nbh, a.fd_nx, kn, wn))
+          ThdCursor cn = cur;
+          if (next_bwd_item<BN, BM, kThd>(p, total, a.n_x, a.x_major, a.fd_nbh, a.fd_nx, s_thd, cn, kn, wn))
             pf = fetch(wn, 0, wn.n_i - 1);
         }
         named_bar_sync(1, 256);
@@ -409,7 +418,7 @@ __global__ void __launch_bounds__(Bwd128::THREADS, 1)
         mbar_arrive(&bar_ds);
       }
       gs += w.n_it;
-      have = next_bwd_item<BN, BM>(p, total, a.n_x, a.x_major, a.fd_nbh, a.fd_nx, k, w);
+      have = next_bwd_item<BN, BM, kThd>(p, total, a.n_x, a.x_major, a.fd_nbh, a.fd_nx, s_thd, cur, k, w);
     }
   } else if (warp < 16) {
     // ---------------- drain: dQ every step, dV and dK at the end of an item ----------------
@@ -428,6 +437,7 @@ __global__ void __launch_bounds__(Bwd128::THREADS, 1)
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     BwdItem w;
     int k = 0, ic = 0, gs = 0;
+    ThdCursor cur;
     bool ok = true;
     // kOrdered: the ticket the last step's adds are behind, released at the
     // next step once its dQ^T has left TMEM (measured 1.92 ms for the c3
@@ -442,7 +452,7 @@ __global__ void __launch_bounds__(Bwd128::THREADS, 1)
         pend = nullptr;
       }
     };
-    while (ok && next_bwd_item<BN, BM>(p, total, a.n_x, a.x_major, a.fd_nbh, a.fd_nx, k, w)) {
+    while (ok && next_bwd_item<BN, BM, kThd>(p, total, a.n_x, a.x_major, a.fd_nbh, a.fd_nx, s_thd, cur, k, w)) {
       int ih = -1, ii = w.n_i - 1;   // step order: see next_step
       for (int it = 0; it < w.n_it; ++it) {
         next_step(ih, ii, G);
@@ -485,9 +495,15 @@ __global__ void __launch_bounds__(Bwd128::THREADS, 1)
           // order, and all CTAs are resident, so the waits cannot form a cycle;
           // holding a ticket back by one step does not change that (tile 0
           // never waits, and the last one is released at the end of the item).
-          int* tk = a.dq_ticket + (static_cast<size_t>(w.seq.b) * p.heads_q + h) * a.n_x + w.x0 +
-                    (w.i_start + ii) * w.xs;
+          const int slot = w.x0 + (w.i_start + ii) * w.xs;
           release_pending();
+          // a sequence longer than max_seqlen (flagged) can reach past the
+          // ticket slots: its query tiles there are left out
+          if (slot >= a.n_x) {
+            if (t == 0 && p.err) atomicOr(p.err, ATTN_DEVERR_SEQLEN);
+            continue;
+          }
+          int* tk = a.dq_ticket + (static_cast<size_t>(w.seq.b) * p.heads_q + h) * a.n_x + slot;
           if (t == 0) wait_ticket(tk, w.jt, ac);   // raises the abort flag if it runs out
           named_bar_sync(2, 256);
           if (*reinterpret_cast<volatile int*>(&abort_flag)) { ok = false; break; }
@@ -557,7 +573,8 @@ __global__ void __launch_bounds__(Bwd128::THREADS, 1)
 cudaError_t launch_attn_bwd128(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                                const CUtensorMap& dO, const BwdArgs& a, int grid, cudaStream_t st) {
   using C = Bwd128;
-  auto kern = a.split ? attn_bwd128_kernel<true> : attn_bwd128_kernel<false>;
+  auto kern = a.split ? attn_bwd128_kernel<true, false>
+                      : (a.x_major == 3 ? attn_bwd128_kernel<false, true> : attn_bwd128_kernel<false, false>);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   kern<<<grid, C::THREADS, C::SMEM, st>>>(q, k, v, dO, a);

@@ -30,6 +30,7 @@
 #include <cuda_runtime.h>
 
 #include "launch.h"
+#include "thd_order.cuh"
 
 namespace attn {
 
@@ -71,12 +72,37 @@ struct FwdItem {
 // longest items to the shortest; 0 = pair slot fastest within each (batch,
 // head), i.e. blockIdx order of the one-CTA-per-item grid.  Under causal
 // masking the last pair of a sequence is the longest, so slots are reversed.
-template <int BM, int BN>
+template <int BM, int BN, bool kThd>
 __device__ __forceinline__ bool next_fwd_item(const Problem& p, int total, int n_x, int x_major,
                                               const FastDiv& fd_nbh, const FastDiv& fd_nx,
-                                              int& k, FwdItem& w) {
+                                              const ThdOrder& thd, ThdCursor& cur, int& k,
+                                              FwdItem& w) {
   const int G = gridDim.x, c = blockIdx.x;
   const int n_bh = p.heads_q * p.batch;
+  if constexpr (kThd) {   // causal THD, the list of thd_order.cuh (numbering 3)
+    for (; k * G < thd.n_items; ++k) {
+      const int idx = k * G + ((k & 1) ? (G - 1 - c) : c);
+      if (idx >= thd.n_items) continue;
+      int pos, h;
+      if (!thd_locate(thd, n_bh, fd_nbh, idx, cur, pos, h)) return false;
+      const int sq = thd.seq[pos];
+      const int t0 = __ldg(p.cu_seqlens + sq), t1 = __ldg(p.cu_seqlens + sq + 1);
+      w.h = h;
+      w.seq.b = 0;
+      w.seq.row0 = t0;
+      w.seq.len = t1 > t0 ? t1 - t0 : 0;
+      w.m0 = (cur.v - 1) * 2 * BM;   // the pair of level v
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        const int r0 = w.m0 + t * BM;
+        w.n_w[t] = r0 >= w.seq.len ? 0 : (min(w.seq.len, r0 + BM) + BN - 1) / BN;
+      }
+      w.n_kv = max(w.n_w[0], w.n_w[1]);
+      ++k;
+      return true;
+    }
+    return false;
+  }
   for (; k * G < total; ++k) {
     const int idx = k * G + ((k & 1) ? (G - 1 - c) : c);
     if (idx >= total) continue;
@@ -131,7 +157,9 @@ __device__ __forceinline__ bool next_fwd_item(const Problem& p, int total, int n
   return false;
 }
 
-template <int D>
+// kThd: the instantiation for numbering 3 (the other numberings carry none of
+// its code: the dense forward measured 2% slower with both in one kernel)
+template <int D, bool kThd>
 __global__ void __launch_bounds__(352, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const FwdArgs a) {
@@ -148,6 +176,7 @@ __global__ void __launch_bounds__(352, 1)
   __shared__ uint64_t bar_s[2], bar_p[2], bar_o[2], bar_sfree[2], bar_stagger;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_flag;
+  __shared__ ThdOrder s_thd;   // the item list of numbering 3
 
   const Problem& p = a.p;
   const int warp = warp_id();
@@ -174,6 +203,8 @@ __global__ void __launch_bounds__(352, 1)
     mbar_init(&bar_stagger, 1);
     fence_mbar_init();
   }
+  if constexpr (kThd)
+    if (warp == 1) thd_order_build(p, 2 * C::BM, p.heads_q * p.batch, s_thd);
   if (warp == 9) tmem_alloc(&tmem_base_sh, C::TMEM_COLS);
   tc_fence_before();
   __syncthreads();
@@ -196,7 +227,8 @@ __global__ void __launch_bounds__(352, 1)
       };
       FwdItem w, wn;
       int k = 0, ic = 0, gring = 0;
-      bool have = next_fwd_item<C::BM, C::BN>(p, total, a.n_x, a.x_major, a.fd_nbh, a.fd_nx, k, w);
+      ThdCursor cur;
+      bool have = next_fwd_item<C::BM, C::BN, kThd>(p, total, a.n_x, a.x_major, a.fd_nbh, a.fd_nx, s_thd, cur, k, w);
       bool ok = true;
       if (have) {
         if (mbar_wait(&bar_qempty[0], 1, ac)) issue_q(w, 0);
@@ -207,7 +239,7 @@ __global__ void __launch_bounds__(352, 1)
         // the next item's query pair is loaded as soon as its buffer frees
         // (with two buffers: when the previous item's S MMAs are done), while
         // this item's K/V tiles stream through the ring
-        const bool have_next = next_fwd_item<C::BM, C::BN>(p, total, a.n_x, a.x_major, a.fd_nbh, a.fd_nx, k, wn);
+        const bool have_next = next_fwd_item<C::BM, C::BN, kThd>(p, total, a.n_x, a.x_major, a.fd_nbh, a.fd_nx, s_thd, cur, k, wn);
         bool q_pending = have_next;
         const int nqb = (ic + 1) % C::QBUFS;
         const uint32_t nq_par = (((ic + 1) / C::QBUFS) & 1) ^ 1;
@@ -263,8 +295,9 @@ __global__ void __launch_bounds__(352, 1)
       const uint32_t tP = tmem + (t ? C::COL_P1 : C::COL_P0);
       FwdItem w;
       int k = 0, ic = 0, gring = 0, cs = 0;   // cs: S tiles of this query tile so far
+      ThdCursor cur;
       bool ok = true;
-      while (ok && next_fwd_item<C::BM, C::BN>(p, total, a.n_x, a.x_major, a.fd_nbh, a.fd_nx, k, w)) {
+      while (ok && next_fwd_item<C::BM, C::BN, kThd>(p, total, a.n_x, a.x_major, a.fd_nbh, a.fd_nx, s_thd, cur, k, w)) {
         const int qb = ic % C::QBUFS, qu = ic / C::QBUFS;
         const int nt = w.n_w[t];
         if (!mbar_wait_w(&bar_q[qb], qu & 1, ac)) break;
@@ -360,8 +393,9 @@ __global__ void __launch_bounds__(352, 1)
     const float sl2 = a.scale_log2;
     FwdItem w;
     int k = 0, cs = 0;
+    ThdCursor cur;
     bool ok = true;
-    while (ok && next_fwd_item<C::BM, C::BN>(p, total, a.n_x, a.x_major, a.fd_nbh, a.fd_nx, k, w)) {
+    while (ok && next_fwd_item<C::BM, C::BN, kThd>(p, total, a.n_x, a.x_major, a.fd_nbh, a.fd_nx, s_thd, cur, k, w)) {
       const int row = w.m0 + t * C::BM + tr;   // row inside the sequence
       const int nt = w.n_w[t];
       float m_run = -INFINITY, l_run = 0.f;
@@ -520,7 +554,7 @@ template <int D>
 cudaError_t launch_attn_fwd(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                             const FwdArgs& a, int grid_x, cudaStream_t st) {
   using C = FwdCfg<D>;
-  auto kern = attn_fwd_kernel<D>;
+  auto kern = a.x_major == 3 ? attn_fwd_kernel<D, true> : attn_fwd_kernel<D, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   kern<<<grid_x, C::THREADS, C::SMEM, st>>>(q, k, v, a);

@@ -4,6 +4,7 @@
 
 #include "attn.h"
 #include "common.cuh"
+#include "thd_order.cuh"
 
 namespace attn {
 
@@ -31,15 +32,42 @@ struct BwdItem {
 //    the later tiles of any (numbered sequence by sequence, a long sequence's
 //    first tiles would come after a shorter one's last ones); slots past a
 //    sequence's end are empty;
+//  * 3 (persistent grid, causal THD of at most 32 sequences): the list of
+//    thd_order.cuh, in descending order of work without empty positions;
 //  * 0 (one CTA per item): tile slot fastest within each (batch, kv head),
 //    in reverse, so CTAs resident together work on the same heads.
-template <int BN, int BM>
+template <int BN, int BM, bool kThd>
 __device__ __forceinline__ bool next_bwd_item(const Problem& p, int total, int n_x, int x_major,
                                               const FastDiv& fd_nbh, const FastDiv& fd_nx,
-                                              int& k, BwdItem& w) {
+                                              const ThdOrder& thd, ThdCursor& cur, int& k,
+                                              BwdItem& w) {
   const int G = gridDim.x, c = blockIdx.x;
   const int groups = static_cast<int>(p.fd_grp.d);
   const int n_bh = p.heads_kv * p.batch;
+  if constexpr (kThd) {   // numbering 3 (the other numberings carry none of its code)
+    for (; k * G < thd.n_items; ++k) {
+      const int idx = k * G + ((k & 1) ? (G - 1 - c) : c);
+      if (idx >= thd.n_items) continue;
+      int pos, h;
+      if (!thd_locate(thd, n_bh, fd_nbh, idx, cur, pos, h)) return false;
+      const int sq = thd.seq[pos];
+      const int t0 = __ldg(p.cu_seqlens + sq), t1 = __ldg(p.cu_seqlens + sq + 1);
+      w.hk = h;
+      w.seq.b = 0;
+      w.seq.row0 = t0;
+      w.seq.len = t1 > t0 ? t1 - t0 : 0;
+      w.x0 = sq;
+      w.xs = p.num_seqs;
+      w.jt = thd.n_sorted[pos] - cur.v;   // K/V tile meeting v query tiles
+      w.kv0 = w.jt * BN;
+      w.i_start = w.kv0 / BM;
+      w.n_i = (w.seq.len + BM - 1) / BM - w.i_start;
+      w.n_it = groups * w.n_i;
+      ++k;
+      return true;
+    }
+    return false;
+  }
   for (; k * G < total; ++k) {
     const int idx = k * G + ((k & 1) ? (G - 1 - c) : c);
     if (idx >= total) continue;

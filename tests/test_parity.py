@@ -206,6 +206,27 @@ def test_thd_random_lengths(mode, lens, pad, hq, hkv, D, causal):
 
 
 @pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("D", [64, 128])
+def test_thd_many_sequences_descending_work_list(mode, D):
+    """A causal pack of 24 sequences of 0-256 rows (two empty), 8 query heads
+    over 4 kv heads: both grids are persistent (288 forward and 192 backward
+    slots over 152 CTAs) and walk the descending-work item list of at most 32
+    sequences, whose levels mix sequences of different lengths.  Full parity,
+    padding rows exact zeros."""
+    g = torch.Generator().manual_seed(90 + D)
+    lens = [int(x) for x in torch.randint(1, 257, (24,), generator=g)]
+    lens[5] = lens[17] = 0
+    lens[9] = 256
+    cap = sum(lens) + 40
+    cu = W.cu_seqlens_from(lens)
+    q, k, v, do = W.thd_inputs(cap, 8, 4, D, seed=91 + D)
+    scale = D ** -0.5
+    got = run_dense(q, k, v, do, True, scale, mode, cu=cu, max_seqlen=256)
+    ref = oracle.thd_backward(q, k, v, do, cu, scale, True)
+    compare_thd(got, ref, cu, [n for n in range(len(lens)) if lens[n] > 0], 8, 4)
+
+
+@pytest.mark.parametrize("mode", MODES)
 def test_thd_varlen_causal_h16_d128_sampled(mode):
     w, x = workload_inputs("thd_varlen_causal_h16_d128")
     got = run_dense(x["q"], x["k"], x["v"], x["do"], w.causal, w.scale, mode, cu=x["cu_seqlens"],

@@ -29,6 +29,8 @@
 // row), 8..15 drain (warpgroup u: dQ^T columns 64u .. 64u + 63, so all of
 // dQ^T leaves TMEM in one load; dV / dK dims 64u .. 64u + 63 at the end of an
 // item), 16 TMA, 17 MMA issuer.
+// For THD, warp 18 writes the exact zeros of the padding rows of dK and dV
+// (this CTA's slice) while the others compute.
 // dQ leaves TMEM in one load and goes out per warp, 32 dims x 16 query rows
 // per TMA copy: a reduce-add into the fp32 accumulator (ATOMIC) or a store
 // into this K/V tile's slab (SPLIT).  One 16 KB copy at a time through a
@@ -50,6 +52,7 @@ struct Bwd128 {
                        OFF_DS = 6 * TILE;
   static constexpr int SMEM = 7 * TILE + 1024;
   static constexpr int THREADS = 576;
+  static constexpr int THREADS_PAD = 608;   // with the padding warp (THD)
   static constexpr uint32_t COL_S = 0, COL_DP = 128, COL_DV = 256, COL_DK = 384;
   // packed P^T / dS^T columns of K-step kk (queries 16 kk .. 16 kk + 15) of
   // the dV / dK MMAs: warpgroup kk / 4 holds them
@@ -79,10 +82,12 @@ __device__ __forceinline__ void next_step(int& ih, int& ii, int groups) {
 // Each mode is its own instantiation: the drain loop is sensitive to its code
 // size (the ATOMIC kernel measured 10% slower with the ordered path compiled
 // in).
-// kThd: the instantiation for numbering 3 (atomic dQ only); the others carry
-// none of its code (the ordered drain loop slowed by 7% with it inlined)
-template <bool kOrdered, bool kThd>
-__global__ void __launch_bounds__(Bwd128::THREADS, 1)
+// kThd: the instantiation for numbering 3 (atomic dQ only); kPad: THD, with
+// the padding warp.  The other instantiations carry none of their code: the
+// ordered drain loop slowed by 7% with numbering 3 inlined, the dense backward
+// by 4% with the padding warp in the kernel.
+template <bool kOrdered, bool kThd, bool kPad>
+__global__ void __launch_bounds__(kPad ? Bwd128::THREADS_PAD : Bwd128::THREADS, 1)
     attn_bwd128_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                        const BwdArgs a) {
@@ -103,6 +108,7 @@ __global__ void __launch_bounds__(Bwd128::THREADS, 1)
   __shared__ uint64_t bar_done, bar_dv_empty, bar_dk_empty;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_flag;
+  __shared__ int s_mma_done;   // the MMA issuer has left its item loop
   __shared__ ThdOrder s_thd;   // the item list of numbering 3
   // -LSE * log2(e) and Delta of the step's query columns; one buffer, so that
   // the tiles and these fit the 227 KB with the 1 KB alignment margin
@@ -117,6 +123,7 @@ __global__ void __launch_bounds__(Bwd128::THREADS, 1)
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
+    s_mma_done = 0;
     mbar_init(&bar_kv_full, 1);
     mbar_init(&bar_kv_empty, 1);
     for (int s = 0; s < 2; ++s) {
@@ -286,6 +293,7 @@ __global__ void __launch_bounds__(Bwd128::THREADS, 1)
       gs += w.n_it;
       ++ic;
     }
+    if constexpr (kPad) *reinterpret_cast<volatile int*>(&s_mma_done) = 1;
   } else if (warp < 8) {
     // ---------------- P / dS warpgroups ----------------
     const int tid = threadIdx.x;                       // 0..255
@@ -557,6 +565,28 @@ __global__ void __launch_bounds__(Bwd128::THREADS, 1)
       gs += w.n_it;
       ++ic;
     }
+  } else if constexpr (kPad) {
+    // ---------------- warp 18: THD padding rows of dK and dV ----------------
+    // Rows at or past cu_seqlens[num_seqs] are outputs of exact zeros; the CTA
+    // writes its share of both tensors during the kernel, 4 KB at a time with
+    // a 1 us pause while the MMA issuer still has items, so that the stores
+    // neither crowd the load/store path of the other roles nor, once the
+    // items are done, hold the CTA back.
+    {
+      const int lane = lane_id();
+      const int end = valid_end(p);
+      const size_t per_row = static_cast<size_t>(p.heads_kv) * C::D / 8;   // 16-byte words
+      const size_t n = static_cast<size_t>(p.rows_total - end) * per_row;
+      const size_t lo = n * blockIdx.x / gridDim.x, hi = n * (blockIdx.x + 1) / gridDim.x;
+      uint4* k4 = reinterpret_cast<uint4*>(a.dk) + static_cast<size_t>(end) * per_row;
+      uint4* v4 = reinterpret_cast<uint4*>(a.dv) + static_cast<size_t>(end) * per_row;
+      int it = 0;
+      for (size_t i = lo + lane; i < hi; i += 32) {
+        k4[i] = make_uint4(0u, 0u, 0u, 0u);
+        v4[i] = make_uint4(0u, 0u, 0u, 0u);
+        if ((++it & 3) == 0 && !*reinterpret_cast<volatile int*>(&s_mma_done)) __nanosleep(1000);
+      }
+    }
   }
 
   tc_fence_before();
@@ -573,11 +603,14 @@ __global__ void __launch_bounds__(Bwd128::THREADS, 1)
 cudaError_t launch_attn_bwd128(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                                const CUtensorMap& dO, const BwdArgs& a, int grid, cudaStream_t st) {
   using C = Bwd128;
-  auto kern = a.split ? attn_bwd128_kernel<true, false>
-                      : (a.x_major == 3 ? attn_bwd128_kernel<false, true> : attn_bwd128_kernel<false, false>);
+  const bool pad = a.pad_zero != 0;
+  auto kern = a.split ? (pad ? attn_bwd128_kernel<true, false, true> : attn_bwd128_kernel<true, false, false>)
+              : a.x_major == 3 ? attn_bwd128_kernel<false, true, true>
+              : (pad ? attn_bwd128_kernel<false, false, true> : attn_bwd128_kernel<false, false, false>);
+  const int threads = pad ? C::THREADS_PAD : C::THREADS;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
-  kern<<<grid, C::THREADS, C::SMEM, st>>>(q, k, v, dO, a);
+  kern<<<grid, threads, C::SMEM, st>>>(q, k, v, dO, a);
   return cudaGetLastError();
 }
 

@@ -67,6 +67,7 @@ struct BwdArgs {
   int total_items;      // work items: K/V tile slots x kv heads x batch
   int n_x;              // K/V tile slots per (batch, kv head)
   int x_major;          // item numbering, see next_bwd_item
+  int pad_zero;         // THD, head_dim 128: the kernel writes the padding rows of dK and dV
   float scale_log2;
   FastDiv fd_nx, fd_nbh; // n_x and heads_kv * batch
 };

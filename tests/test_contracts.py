@@ -105,11 +105,16 @@ def test_outputs_fully_written_dense():
 
 
 @pytest.mark.parametrize("mode", [0, 1])
-def test_thd_padding_rows_exact_zero_in_nan_buffers(mode):
+@pytest.mark.parametrize("D", [64, 128])
+def test_thd_padding_rows_exact_zero_in_nan_buffers(mode, D):
+    """Padding rows of every output exact zeros in NaN-filled buffers: at head_dim
+    64 the postprocess writes those of dq, dk and dv, at head_dim 128 attn_bwd
+    writes those of dk and dv (a warp of the main kernel) and the postprocess
+    those of dq."""
     lens = [5, 130, 64]
     cap = 256
     cu = W.cu_seqlens_from(lens).to(DEV)
-    q, k, v, do = (t.to(DEV) for t in W.thd_inputs(cap, 4, 2, 64, seed=12))
+    q, k, v, do = (t.to(DEV) for t in W.thd_inputs(cap, 4, 2, D, seed=12))
     o = torch.full_like(q, float("nan"))
     lse = torch.full((4, cap), float("nan"), dtype=torch.float32, device=DEV)
     A.attn_fwd(q, k, v, causal=True, cu_seqlens=cu, max_seqlen=130, out=o, lse=lse)
@@ -130,7 +135,7 @@ def test_thd_padding_rows_exact_zero_in_nan_buffers(mode):
         assert torch.isfinite(t).all()
         assert (t[end:] == 0).all()
     assert torch.isneginf(lse[:, end:]).all() and torch.isfinite(lse[:, :end]).all()
-    ref = oracle.thd_backward(*(t.cpu() for t in (q, k, v, do)), cu.cpu(), 0.125, True)
+    ref = oracle.thd_backward(*(t.cpu() for t in (q, k, v, do)), cu.cpu(), D ** -0.5, True)
     assert_close("dq", dq, ref["dq"])
     assert_close("dk", dk, ref["dk"])
 

@@ -235,7 +235,6 @@ attn_status_t attn_fwd(const attn_problem_t* p, const void* q, const void* k, co
   const int grid = persistent ? sms : static_cast<int>(total);
   cudaError_t e = (D == 64) ? launch_attn_fwd<64>(mq, mk, mv, a, grid, st)
                             : launch_attn_fwd<128>(mq, mk, mv, a, grid, st);
-  if (e == cudaSuccess && kp.cu_seqlens) e = launch_thd_fwd_pad(kp, a.o, lse, D, st);
   return cuda_status(e);
 }
 

@@ -47,6 +47,7 @@ struct FwdCfg {
   static constexpr int QBUFS = 2;                  // query-pair buffers (next item prefetch)
   static constexpr int SMEM = QBUFS * 2 * Q_BYTES + NSLOT * KV_BYTES + 1024;
   static constexpr int THREADS = 352;
+  static constexpr int THREADS_PAD = 384;   // with the padding warp (THD)
   static constexpr uint32_t TMEM_COLS = 512;
   // S0, S1 in columns [0, 2 BN); O0, O1 in [256, 256 + 2 D); each tile's P (BN/2
   // packed columns) in a region of its own, so S_w(j+1) can be computed while
@@ -157,10 +158,12 @@ __device__ __forceinline__ bool next_fwd_item(const Problem& p, int total, int n
   return false;
 }
 
-// kThd: the instantiation for numbering 3 (the other numberings carry none of
-// its code: the dense forward measured 2% slower with both in one kernel)
-template <int D, bool kThd>
-__global__ void __launch_bounds__(352, 1)
+// kThd: the instantiation for numbering 3; kPad: THD, with warp 11 writing
+// the padding rows of O and LSE during the computation.  The others carry
+// none of their code (the dense forward measured 2% slower with numbering 3
+// in the same kernel).
+template <int D, bool kThd, bool kPad>
+__global__ void __launch_bounds__(kPad ? FwdCfg<D>::THREADS_PAD : FwdCfg<D>::THREADS, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const FwdArgs a) {
   using C = FwdCfg<D>;
@@ -176,6 +179,7 @@ __global__ void __launch_bounds__(352, 1)
   __shared__ uint64_t bar_s[2], bar_p[2], bar_o[2], bar_sfree[2], bar_stagger;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_flag;
+  __shared__ int s_mma_done;   // an MMA issuer has left its item loop
   __shared__ ThdOrder s_thd;   // the item list of numbering 3
 
   const Problem& p = a.p;
@@ -186,6 +190,7 @@ __global__ void __launch_bounds__(352, 1)
   // ---- setup ---------------------------------------------------------------
   if (threadIdx.x == 0) {
     abort_flag = 0;
+    s_mma_done = 0;
     for (int b = 0; b < C::QBUFS; ++b) {
       mbar_init(&bar_q[b], 1);
       mbar_init(&bar_qempty[b], 2);      // released by both issuers
@@ -382,7 +387,8 @@ __global__ void __launch_bounds__(352, 1)
         ++ic;
       }
     }
-  } else {
+    if constexpr (kPad) *reinterpret_cast<volatile int*>(&s_mma_done) = 1;
+  } else if (kPad ? warp < 8 : true) {
     // ---------------- softmax warpgroups ----------------
     const int t = warp >> 2;                 // query tile of this warpgroup
     const int tr = threadIdx.x & 127;        // row within the tile == TMEM lane
@@ -523,6 +529,30 @@ __global__ void __launch_bounds__(352, 1)
       }
       cs += nt;
     }
+  } else if constexpr (kPad) {
+    // ---------------- warp 11: THD padding rows of O and LSE ----------------
+    // Rows at or past cu_seqlens[num_seqs]: O exact zeros, LSE -inf.  The CTA
+    // writes its slice during the computation, 4 KB of O at a time with a 1 us
+    // pause while the MMA issuers still have items.
+    const int lane = lane_id();
+    const int end = valid_end(p);
+    const uint32_t rows = static_cast<uint32_t>(p.rows_total - end);
+    const size_t per_row = static_cast<size_t>(p.heads_q) * D / 8;   // 16-byte words of O
+    const size_t n = rows * per_row;
+    const size_t lo = n * blockIdx.x / gridDim.x, hi = n * (blockIdx.x + 1) / gridDim.x;
+    uint4* o4 = reinterpret_cast<uint4*>(a.o) + static_cast<size_t>(end) * per_row;
+    int it = 0;
+    for (size_t i = lo + lane; i < hi; i += 32) {
+      o4[i] = make_uint4(0u, 0u, 0u, 0u);
+      if ((++it & 7) == 0 && !*reinterpret_cast<volatile int*>(&s_mma_done)) __nanosleep(1000);
+    }
+    const uint64_t nl = static_cast<uint64_t>(rows) * static_cast<uint32_t>(p.heads_q);
+    const uint32_t llo = static_cast<uint32_t>(nl * blockIdx.x / gridDim.x);
+    const uint32_t lhi = static_cast<uint32_t>(nl * (blockIdx.x + 1) / gridDim.x);
+    for (uint32_t i = llo + lane; i < lhi; i += 32) {
+      const uint32_t hh = i / rows, r = i - hh * rows;
+      a.lse[static_cast<size_t>(hh) * p.rows_total + end + r] = -INFINITY;
+    }
   }
 
   tc_fence_before();
@@ -535,29 +565,16 @@ __global__ void __launch_bounds__(352, 1)
 }
 
 // THD padding rows [cu_seqlens[num_seqs], capacity): O = 0, LSE = -inf.
-__global__ void thd_fwd_pad_kernel(Problem p, __nv_bfloat16* o, float* lse, int head_dim) {
-  const int end = valid_end(p);
-  const int rows = p.rows_total - end;
-  if (rows <= 0) return;
-  const size_t n_o = static_cast<size_t>(rows) * p.heads_q * head_dim / 8;  // uint4 chunks
-  uint4* o4 = reinterpret_cast<uint4*>(o + static_cast<size_t>(end) * p.heads_q * head_dim);
-  for (size_t i = blockIdx.x * blockDim.x + threadIdx.x; i < n_o; i += gridDim.x * blockDim.x)
-    o4[i] = make_uint4(0, 0, 0, 0);
-  const size_t n_l = static_cast<size_t>(rows) * p.heads_q;
-  for (size_t i = blockIdx.x * blockDim.x + threadIdx.x; i < n_l; i += gridDim.x * blockDim.x) {
-    const size_t hh = i / rows, r = i % rows;
-    lse[hh * p.rows_total + end + r] = -INFINITY;
-  }
-}
-
 template <int D>
 cudaError_t launch_attn_fwd(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                             const FwdArgs& a, int grid_x, cudaStream_t st) {
   using C = FwdCfg<D>;
-  auto kern = a.x_major == 3 ? attn_fwd_kernel<D, true> : attn_fwd_kernel<D, false>;
+  const bool pad = a.p.cu_seqlens != nullptr;
+  auto kern = !pad ? attn_fwd_kernel<D, false, false>
+              : a.x_major == 3 ? attn_fwd_kernel<D, true, true> : attn_fwd_kernel<D, false, true>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
-  kern<<<grid_x, C::THREADS, C::SMEM, st>>>(q, k, v, a);
+  kern<<<grid_x, pad ? C::THREADS_PAD : C::THREADS, C::SMEM, st>>>(q, k, v, a);
   return cudaGetLastError();
 }
 
@@ -565,11 +582,5 @@ template cudaError_t launch_attn_fwd<64>(const CUtensorMap&, const CUtensorMap&,
                                          const CUtensorMap&, const FwdArgs&, int, cudaStream_t);
 template cudaError_t launch_attn_fwd<128>(const CUtensorMap&, const CUtensorMap&,
                                           const CUtensorMap&, const FwdArgs&, int, cudaStream_t);
-
-cudaError_t launch_thd_fwd_pad(const Problem& p, __nv_bfloat16* o, float* lse, int head_dim,
-                               cudaStream_t st) {
-  thd_fwd_pad_kernel<<<304, 256, 0, st>>>(p, o, lse, head_dim);
-  return cudaGetLastError();
-}
 
 }  // namespace attn

@@ -75,8 +75,6 @@ struct BwdArgs {
 template <int D>
 cudaError_t launch_attn_fwd(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                             const FwdArgs& a, int grid_x, cudaStream_t st);
-cudaError_t launch_thd_fwd_pad(const Problem& p, __nv_bfloat16* o, float* lse, int head_dim,
-                               cudaStream_t st);
 template <int D>
 cudaError_t launch_attn_bwd(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                             const CUtensorMap& dO, const CUtensorMap& dq, const CUtensorMap& dk,

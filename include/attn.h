@@ -132,8 +132,8 @@ attn_status_t attn_bwd_preprocess(const attn_problem_t* p, attn_dq_mode_t mode, 
                                   size_t workspace_bytes, attn_stream_t stream);
 
 /* Backward main pass: q, k, v, dout bf16; lse, delta fp32 (from attn_fwd and
- * attn_bwd_preprocess) -> dk, dv bf16 (every non-padding row; for THD at
- * head_dim 128 the padding rows too, as exact zeros) and the fp32 dQ
+ * attn_bwd_preprocess) -> dk, dv bf16 (every non-padding row; for THD the
+ * padding rows too, as exact zeros) and the fp32 dQ
  * accumulator or partials inside `workspace`.  GQA dK/dV are summed over each
  * KV head's query heads inside the kernel (no atomics on dK/dV).  Must be
  * followed by attn_bwd_postprocess with the same workspace and mode. */
@@ -144,8 +144,8 @@ attn_status_t attn_bwd(const attn_problem_t* p, attn_dq_mode_t mode, const void*
 
 /* Backward postprocess: dq bf16 from the workspace of attn_bwd; for THD it also
  * writes the padding rows (at or past cu_seqlens[num_seqs]) of dq as exact
- * zeros, and those of dk and dv at head_dim 64 (at head_dim 128 attn_bwd wrote
- * them).  After it, every element of dq, dk and dv has been written. */
+ * zeros (attn_bwd wrote those of dk and dv).  After it, every element of dq,
+ * dk and dv has been written. */
 attn_status_t attn_bwd_postprocess(const attn_problem_t* p, attn_dq_mode_t mode,
                                    const void* workspace, size_t workspace_bytes, void* dq,
                                    void* dk, void* dv, attn_stream_t stream);

@@ -361,9 +361,9 @@ attn_status_t attn_bwd(const attn_problem_t* p, attn_dq_mode_t mode, const void*
   if (persistent && kp.cu_seqlens &&
       static_cast<int64_t>(n_kv_tiles(kp)) * kp.num_seqs <= static_cast<int64_t>(gx))
     a.x_major = (kp.causal && kp.num_seqs <= kThdOrderSeqs && !a.split) ? 3 : 2;
-  // THD at head_dim 128: the padding rows of dK and dV are written by the main
-  // kernel (a warp of its own, during the computation) instead of the postprocess
-  a.pad_zero = (D == 128 && kp.cu_seqlens) ? 1 : 0;
+  // THD: the padding rows of dK and dV are written by the main kernel (a warp
+  // of its own, during the computation) instead of the postprocess
+  a.pad_zero = kp.cu_seqlens ? 1 : 0;
   cudaError_t e = (D == 64) ? launch_attn_bwd<64>(mq, mk, mv, mdo, mdq, mdk, mdv, a, grid, st)
                             : launch_attn_bwd128(mq, mk, mv, mdo, a, grid, st);
   return cuda_status(e);
@@ -392,8 +392,8 @@ attn_status_t attn_bwd_postprocess(const attn_problem_t* p, attn_dq_mode_t mode,
   const int n_split = split ? n_kv_tiles(kp) : 0;
   const float* acc = static_cast<const float*>(workspace);
   auto* dqb = static_cast<__nv_bfloat16*>(dq);
-  // THD at head_dim 128: attn_bwd wrote the padding rows of dk and dv
-  const bool kv_pad_done = D == 128 && kp.cu_seqlens;
+  // THD: attn_bwd wrote the padding rows of dk and dv
+  const bool kv_pad_done = kp.cu_seqlens != nullptr;
   auto* dkb = kv_pad_done ? nullptr : static_cast<__nv_bfloat16*>(dk);
   auto* dvb = kv_pad_done ? nullptr : static_cast<__nv_bfloat16*>(dv);
   cudaError_t e = (D == 64) ? launch_dq_finalize<64>(kp, acc, slab, split, n_split, dqb, dkb, dvb, st)

@@ -51,6 +51,7 @@ struct BwdCfg {
   static constexpr int SMEM =
       KV_BUFS * 2 * KV_BYTES + 2 * NST * QT_BYTES + DS_BYTES + STG_BYTES + 1024;
   static constexpr int THREADS = 448;
+  static constexpr int THREADS_PAD = 480;   // with the padding warp (THD)
   static constexpr uint32_t TMEM_COLS = 512;
   // TMEM columns.  S^T and dP^T are BM fp32 columns each; P^T and dS^T are
   // packed bf16 pairs (BM / 2 columns each), P^T in columns of its own so that
@@ -78,9 +79,11 @@ struct BwdCfg {
 // Warp roles: 0..7 P/dS (two warpgroups, each owns half of the query columns
 // of every KV row), 8..11 dQ drain and dK/dV epilogue, 12 TMA, 13 the MMA
 // issuer, which interleaves independent GEMMs.
-// kThd: the instantiation for numbering 3; the others carry none of its code
-template <int D, bool kThd>
-__global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
+// kThd: the instantiation for numbering 3; kPad: THD, with warp 14 writing the
+// padding rows of dK and dV during the computation.  The others carry none of
+// their code.
+template <int D, bool kThd, bool kPad>
+__global__ void __launch_bounds__(kPad ? BwdCfg<D>::THREADS_PAD : BwdCfg<D>::THREADS, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                     const __grid_constant__ CUtensorMap tmDQ, const __grid_constant__ CUtensorMap tmdK,
@@ -106,6 +109,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
   __shared__ uint64_t bar_dv_empty, bar_dk_empty;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_flag;
+  __shared__ int s_mma_done;   // the MMA issuer has left its item loop
   __shared__ ThdOrder s_thd;   // the item list of numbering 3
   __shared__ __align__(16) float s_nlse[2][BM];   // -LSE * log2(e) per query column
   __shared__ __align__(16) float s_delta[2][BM];
@@ -118,6 +122,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
+    s_mma_done = 0;
     for (int b = 0; b < C::KV_BUFS; ++b) {
       mbar_init(&bar_kv_full[b], 1);
       mbar_init(&bar_kv_empty[b], 1);
@@ -303,6 +308,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         have = have_next;
       }
     }
+    if constexpr (kPad) *reinterpret_cast<volatile int*>(&s_mma_done) = 1;
   } else if (warp < 8) {
     // ---------------- P / dS warpgroups ----------------
     const int tid = threadIdx.x;                       // 0..255
@@ -449,7 +455,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       gs += w.n_it;
       have = next_bwd_item<BN, BM, kThd>(p, total, a.n_x, a.x_major, a.fd_nbh, a.fd_nx, s_thd, cur, k, w);
     }
-  } else {
+  } else if (kPad ? warp < 12 : true) {
     // ---------------- dQ drain and dK/dV epilogue (warps 8..11) ----------------
     // dQ: TMEM -> fp32 staging tile in shared memory -> reduce-add into the
     // accumulator (ATOMIC) or store into this KV tile's slab (SPLIT), in two
@@ -612,6 +618,24 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       ++ic;
     }
     if (t == 0) bulk_wait<0>();
+  } else if constexpr (kPad) {
+    // ---------------- warp 14: THD padding rows of dK and dV ----------------
+    // Exact zeros for the rows at or past cu_seqlens[num_seqs] (this CTA's
+    // slice of both tensors), 4 KB at a time with a 1 us pause while the MMA
+    // issuer still has items.
+    const int lane = lane_id();
+    const int end = valid_end(p);
+    const size_t per_row = static_cast<size_t>(p.heads_kv) * D / 8;   // 16-byte words
+    const size_t n = static_cast<size_t>(p.rows_total - end) * per_row;
+    const size_t lo = n * blockIdx.x / gridDim.x, hi = n * (blockIdx.x + 1) / gridDim.x;
+    uint4* k4 = reinterpret_cast<uint4*>(a.dk) + static_cast<size_t>(end) * per_row;
+    uint4* v4 = reinterpret_cast<uint4*>(a.dv) + static_cast<size_t>(end) * per_row;
+    int it = 0;
+    for (size_t i = lo + lane; i < hi; i += 32) {
+      k4[i] = make_uint4(0u, 0u, 0u, 0u);
+      v4[i] = make_uint4(0u, 0u, 0u, 0u);
+      if ((++it & 3) == 0 && !*reinterpret_cast<volatile int*>(&s_mma_done)) __nanosleep(1000);
+    }
   }
 
   tc_fence_before();
@@ -628,10 +652,12 @@ cudaError_t launch_attn_bwd(const CUtensorMap& q, const CUtensorMap& k, const CU
                             const CUtensorMap& dO, const CUtensorMap& dq, const CUtensorMap& dk,
                             const CUtensorMap& dv, const BwdArgs& a, int grid, cudaStream_t st) {
   using C = BwdCfg<D>;
-  auto kern = a.x_major == 3 ? attn_bwd_kernel<D, true> : attn_bwd_kernel<D, false>;
+  const bool pad = a.pad_zero != 0;
+  auto kern = a.x_major == 3 ? attn_bwd_kernel<D, true, true>
+              : (pad ? attn_bwd_kernel<D, false, true> : attn_bwd_kernel<D, false, false>);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
-  kern<<<grid, C::THREADS, C::SMEM, st>>>(q, k, v, dO, dq, dk, dv, a);
+  kern<<<grid, pad ? C::THREADS_PAD : C::THREADS, C::SMEM, st>>>(q, k, v, dO, dq, dk, dv, a);
   return cudaGetLastError();
 }
 

@@ -230,8 +230,8 @@ __global__ void __launch_bounds__(256) attn_dq_finalize_kernel(Problem p,
       store(di, v);
     }
   }
-  // THD: zero dK / dV rows past the last sequence (head_dim 128: written by the
-  // backward main kernel, and dk = dv = null here)
+  // THD: zero dK / dV rows past the last sequence (when dk is not null; the
+  // backward main kernels write them and pass null here)
   if (p.cu_seqlens && dk) {
     const size_t n = static_cast<size_t>(p.rows_total - end) * p.heads_kv * D / 8;
     const size_t off = static_cast<size_t>(end) * p.heads_kv * D / 8;
